@@ -1,0 +1,230 @@
+"""CPU oracle for the block-scaled quantize + GEMM path (ctypes over bsq_oracle.c).
+
+TEST INFRASTRUCTURE. Only the test suite, the smoke check and the benchmark's CPU-baseline
+leg import this package. The product library never does, and nothing here is shared with
+the CUDA path: the two meet only through the seeded inputs of ``workloads``.
+
+The C source states the readings it takes where the pages are silent (rounding, the
+UE8M0 exponent rule, NVFP4 arithmetic order, nibble order, scale layout).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from typing import Optional, Tuple
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "bsq_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+
+MXFP8, NVFP4, MXFP4 = 1, 2, 3
+FMT_IDS = {"mxfp8": MXFP8, "nvfp4": NVFP4, "mxfp4": MXFP4}
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+def build(force: bool = False) -> str:
+    """Compile bsq_oracle.c into liboracle.so next to it (gcc, OpenMP, no FMA contraction)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + ".tmp%d" % os.getpid()
+        cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fopenmp",
+               "-fPIC", "-shared", _SRC, "-o", tmp, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    if _lib is None:
+        build()
+        L = ctypes.CDLL(_LIB)
+        i64, u8p, f64p, vp = ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p
+        L.orc_decode_e4m3.restype = ctypes.c_double
+        L.orc_decode_e4m3.argtypes = [ctypes.c_uint]
+        L.orc_decode_e2m1.restype = ctypes.c_double
+        L.orc_decode_e2m1.argtypes = [ctypes.c_uint]
+        L.orc_decode_ue8m0.restype = ctypes.c_double
+        L.orc_decode_ue8m0.argtypes = [ctypes.c_uint]
+        L.orc_encode_e4m3.restype = ctypes.c_uint
+        L.orc_encode_e4m3.argtypes = [ctypes.c_double]
+        L.orc_encode_e2m1.restype = ctypes.c_uint
+        L.orc_encode_e2m1.argtypes = [ctypes.c_double]
+        L.orc_scale_tiled_offset.restype = i64
+        L.orc_scale_tiled_offset.argtypes = [i64, i64, i64]
+        L.orc_scales_tiled_bytes.restype = i64
+        L.orc_scales_tiled_bytes.argtypes = [ctypes.c_int, i64, i64]
+        L.orc_codes_bytes.restype = i64
+        L.orc_codes_bytes.argtypes = [ctypes.c_int, i64, i64]
+        L.orc_tile_scales.restype = ctypes.c_int
+        L.orc_tile_scales.argtypes = [ctypes.c_int, u8p, i64, i64, ctypes.c_float, ctypes.c_float, u8p]
+        L.orc_quantize_mx.restype = ctypes.c_int
+        L.orc_quantize_mx.argtypes = [ctypes.c_int, vp, ctypes.c_int, i64, i64, u8p, u8p]
+        L.orc_quantize_nvfp4.restype = ctypes.c_int
+        L.orc_quantize_nvfp4.argtypes = [vp, ctypes.c_int, i64, i64, ctypes.c_int, ctypes.c_float,
+                                         u8p, u8p, vp, vp]
+        L.orc_tensor_amax.restype = ctypes.c_float
+        L.orc_tensor_amax.argtypes = [vp, ctypes.c_int, i64]
+        L.orc_decode.restype = ctypes.c_int
+        L.orc_decode.argtypes = [ctypes.c_int, u8p, u8p, i64, i64, f64p]
+        L.orc_gemm.restype = ctypes.c_int
+        L.orc_gemm.argtypes = [f64p, f64p, vp, i64, i64, i64, ctypes.c_double, i64, i64, f64p, vp]
+        L.orc_num_threads.restype = ctypes.c_int
+        L.orc_set_num_threads.argtypes = [ctypes.c_int]
+        _lib = L
+    return _lib
+
+
+def _ptr(a: Optional[np.ndarray]):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _fmt(fmt) -> int:
+    return FMT_IDS[fmt] if isinstance(fmt, str) else int(fmt)
+
+
+def num_threads() -> int:
+    return lib().orc_num_threads()
+
+
+def set_num_threads(n: int) -> None:
+    lib().orc_set_num_threads(int(n))
+
+
+# --- scalar codecs -------------------------------------------------------------------------
+def decode_e4m3(c: int) -> float:
+    return lib().orc_decode_e4m3(int(c))
+
+
+def decode_e2m1(c: int) -> float:
+    return lib().orc_decode_e2m1(int(c))
+
+
+def decode_ue8m0(c: int) -> float:
+    return lib().orc_decode_ue8m0(int(c))
+
+
+def encode_e4m3(v: float) -> int:
+    return lib().orc_encode_e4m3(float(v))
+
+
+def encode_e2m1(v: float) -> int:
+    return lib().orc_encode_e2m1(float(v))
+
+
+# --- layout --------------------------------------------------------------------------------
+def codes_bytes(fmt, rows: int, cols: int) -> int:
+    return int(lib().orc_codes_bytes(_fmt(fmt), rows, cols))
+
+
+def scales_tiled_bytes(fmt, rows: int, cols: int) -> int:
+    return int(lib().orc_scales_tiled_bytes(_fmt(fmt), rows, cols))
+
+
+def scale_tiled_offset(r: int, c: int, n_scale_cols: int) -> int:
+    return int(lib().orc_scale_tiled_offset(r, c, n_scale_cols))
+
+
+def block_size(fmt) -> int:
+    return 16 if _fmt(fmt) == NVFP4 else 32
+
+
+def tile_scales(fmt, plain: np.ndarray, rows: int, cols: int, g: float = 0.0, amax: float = 0.0) -> np.ndarray:
+    plain = np.ascontiguousarray(plain, dtype=np.uint8)
+    out = np.empty(scales_tiled_bytes(fmt, rows, cols), dtype=np.uint8)
+    st = lib().orc_tile_scales(_fmt(fmt), _ptr(plain), rows, cols, g, amax, _ptr(out))
+    assert st == 0, st
+    return out
+
+
+# --- quantizers ----------------------------------------------------------------------------
+class Quantized:
+    """codes (uint8, packed), plain scales (rows x cols/bs), per-tensor g and amax (NVFP4)."""
+
+    def __init__(self, fmt: int, rows: int, cols: int, codes: np.ndarray, scales: np.ndarray,
+                 g: float = 1.0, amax: float = 0.0):
+        self.fmt, self.rows, self.cols = fmt, rows, cols
+        self.codes, self.scales, self.g, self.amax = codes, scales, g, amax
+
+    def tiled_scales(self) -> np.ndarray:
+        return tile_scales(self.fmt, self.scales, self.rows, self.cols, self.g if self.fmt == NVFP4 else 0.0,
+                           self.amax if self.fmt == NVFP4 else 0.0)
+
+    def decode(self) -> np.ndarray:
+        return decode(self.fmt, self.codes, self.scales, self.rows, self.cols)
+
+
+def _src(x: np.ndarray) -> Tuple[np.ndarray, int]:
+    x = np.ascontiguousarray(x)
+    if x.dtype == np.float32:
+        return x, 1
+    assert x.dtype == np.uint16, "sources are fp32 values or bf16 bit patterns (uint16)"
+    return x, 0
+
+
+def quantize(fmt, x: np.ndarray, global_scale: Optional[float] = None) -> Quantized:
+    f = _fmt(fmt)
+    x, is_f32 = _src(x)
+    rows, cols = x.shape
+    codes = np.zeros(codes_bytes(f, rows, cols), dtype=np.uint8)
+    bs = block_size(f)
+    scales = np.zeros((rows, cols // bs), dtype=np.uint8)
+    L = lib()
+    if f == NVFP4:
+        g = np.zeros(1, np.float32)
+        amax = np.zeros(1, np.float32)
+        st = L.orc_quantize_nvfp4(_ptr(x), is_f32, rows, cols, 0 if global_scale is None else 1,
+                                  0.0 if global_scale is None else float(global_scale),
+                                  _ptr(codes), _ptr(scales), _ptr(g), _ptr(amax))
+        if st:
+            raise ValueError("oracle quantize failed: %d" % st)
+        return Quantized(f, rows, cols, codes, scales, float(g[0]), float(amax[0]))
+    st = L.orc_quantize_mx(f, _ptr(x), is_f32, rows, cols, _ptr(codes), _ptr(scales))
+    if st:
+        raise ValueError("oracle quantize failed: %d" % st)
+    return Quantized(f, rows, cols, codes, scales)
+
+
+def tensor_amax(x: np.ndarray) -> float:
+    x, is_f32 = _src(x)
+    return float(lib().orc_tensor_amax(_ptr(x), is_f32, x.size))
+
+
+def decode(fmt, codes: np.ndarray, scales: np.ndarray, rows: int, cols: int) -> np.ndarray:
+    f = _fmt(fmt)
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    scales = np.ascontiguousarray(scales, dtype=np.uint8)
+    out = np.empty((rows, cols), dtype=np.float64)
+    st = lib().orc_decode(f, _ptr(codes), _ptr(scales), rows, cols, _ptr(out))
+    assert st == 0, st
+    return out
+
+
+def gemm(A: np.ndarray, B: np.ndarray, bias: Optional[np.ndarray] = None, alpha: float = 1.0,
+         rows: Optional[Tuple[int, int]] = None, want_abs: bool = True):
+    """fp64 out = alpha * A . B^T + bias for output rows [r0, r1); returns (out, abs_sum)."""
+    A = np.ascontiguousarray(A, dtype=np.float64)
+    B = np.ascontiguousarray(B, dtype=np.float64)
+    M, K = A.shape
+    N, K2 = B.shape
+    assert K == K2
+    r0, r1 = (0, M) if rows is None else rows
+    out = np.empty((r1 - r0, N), dtype=np.float64)
+    ab = np.empty((r1 - r0, N), dtype=np.float64) if want_abs else None
+    bias_arr = None if bias is None else np.ascontiguousarray(bias, dtype=np.uint16)
+    st = lib().orc_gemm(_ptr(A), _ptr(B), _ptr(bias_arr), M, N, K, float(alpha), r0, r1, _ptr(out), _ptr(ab))
+    assert st == 0, st
+    return out, ab
+
+
+def reference_linear(fmt, a_src: np.ndarray, b_src: np.ndarray, bias: Optional[np.ndarray] = None,
+                     rows: Optional[Tuple[int, int]] = None):
+    """The whole path on the CPU: quantize A and B, decode, fp64 GEMM (+ alpha for NVFP4)."""
+    qa = quantize(fmt, a_src)
+    qb = quantize(fmt, b_src)
+    alpha = qa.g * qb.g if qa.fmt == NVFP4 else 1.0
+    out, ab = gemm(qa.decode(), qb.decode(), bias, alpha, rows)
+    return qa, qb, out, ab

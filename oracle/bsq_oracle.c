@@ -1,0 +1,401 @@
+/*
+ * bsq_oracle.c -- plain, slow CPU oracle for block-scaled quantization (MXFP8, NVFP4,
+ * MXFP4) and the block-scaled GEMM with a bias epilogue.
+ *
+ * TEST INFRASTRUCTURE. Only the test suite, the smoke check and the CPU-baseline leg of
+ * the benchmark load this library. The product (libbsq.so and its Python binding) never
+ * calls it, and it shares no source, header, table or helper with the CUDA path.
+ *
+ * Sources (page title, section):
+ *   [LT]  "lightly-train - DINOv3 + EoMT inference and training optimisation on RTX 5090"
+ *         README, section 2 (number-format table): MXFP8 = E4M3 elements + a UE8M0 scale per
+ *         1x32 block (8.25 bits/value); NVFP4 = e2m1 elements + an E4M3 scale per 1x16
+ *         block + an fp32 per-tensor scale (4.5 bits/value); MXFP4 = e2m1 + UE8M0 per 1x32
+ *         (4.25 bits/value). Section 4.7: the fake-quant study rounds to nearest ("RN").
+ *         Section 5.5: 4-bit operands are K-major, every GEMM is written "TN".
+ *   [BF]  "2x, not 16x: the real ledger of BF16 mixed precision" blog, section 2 table
+ *         (bf16 = 8 exponent / 7 mantissa bits) and section 5.4 (largest finite E4M3 = 448).
+ *
+ * The pages leave these steps open; the oracle takes the following readings:
+ *   R1  Rounding of elements and E4M3 scales: round to nearest, ties to even, from the
+ *       exact value; magnitudes at or above the largest finite value saturate to it
+ *       (448 for E4M3, 6 for e2m1). A zero result keeps the sign of its input.
+ *   R2  UE8M0 exponent of a 1x32 block: e = floor(log2(amax)) - emax_elem, emax_elem = 8
+ *       (E4M3) or 2 (e2m1), clamped to [-127, 127]; amax = 0 gives e = -127. The scale byte
+ *       is e + 127 and the element is RNE_sat(x * 2^-e). (The shared-exponent rule of the
+ *       OCP microscaling formats.)
+ *   R3  NVFP4 per-tensor scale g = fp32(amax_tensor / 2688), 2688 = 6 * 448. Per 1x16 block:
+ *       s_code = E4M3 RNE_sat(fp32(bamax / fp32(6 * g))), s = decode(s_code); elements
+ *       y = fp32(x / fp32(s * g)), code = e2m1 RNE_sat(y). Every step is one IEEE fp32
+ *       operation rounded to nearest (no fused multiply-add). s = 0 (which includes g = 0)
+ *       makes every code of the block a zero carrying the sign of its input. With a given
+ *       per-tensor scale the same steps run from that g.
+ *   R4  Packing: codes are row-major with K contiguous; e2m1 element 2j is the low nibble
+ *       of byte j and element 2j+1 the high nibble.
+ *   R5  Scale layout: tiles of 128 rows x 4 scale columns (512 bytes); tile index =
+ *       (row / 128) * n_col_tiles + col / 4; inside a tile byte (row % 32) * 16 +
+ *       ((row / 32) % 4) * 4 + col % 4. Padding rows/columns hold 0. For NVFP4 a 16-byte
+ *       tail after the tiles holds {g, amax_tensor, 0, 0} as fp32.
+ *   R6  GEMM: y[m,n] = alpha * sum_k Ahat[m,k] * Bhat[n,k] + bias[n] in fp64, kept unrounded;
+ *       alpha = g_A * g_B for NVFP4 (the block-scaled sum is formed first), 1 otherwise.
+ *   R7  Non-finite inputs are outside the contract; the quantizers reject them.
+ *
+ * Pins (tests that tie this code to something other than itself) are in the test suite:
+ * exhaustive decode tables against two independent float8/float4 libraries, encoders
+ * against brute-force nearest search over every bf16 value, power-of-two / top-binade /
+ * shift invariants of the UE8M0 rule, NVFP4 sign symmetry and a hand-derived block, the
+ * GEMM against a library matmul on tiny cases and closed forms. The scale layout R5 is a
+ * convention (not a value the method fixes); on the CPU it is held to bijectivity and
+ * zero padding, and on the GPU the tensor cores' own reading of it pins it end to end.
+ *
+ * Build: gcc -O2 -std=c11 -ffp-contract=off -fopenmp -fPIC -shared (no fast-math).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORC_MXFP8 1
+#define ORC_NVFP4 2
+#define ORC_MXFP4 3
+
+#define ORC_OK 0
+#define ORC_ERR_ARG -1
+#define ORC_ERR_SHAPE -2
+#define ORC_ERR_NONFINITE -3
+
+int orc_version(void) { return 1; }
+
+int orc_num_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+void orc_set_num_threads(int n) {
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
+/* ------------------------------------------------------------------------------------
+ * Decoders (format definitions).
+ * ---------------------------------------------------------------------------------- */
+
+/* E4M3 ("FN": no infinities, only S.1111.111 is NaN): sign s, exponent field E (bias 7),
+ * mantissa m. E = 0 is subnormal: m * 2^-9. Largest finite 0x7E = 1.75 * 2^8 = 448 [BF 5.4]. */
+double orc_decode_e4m3(unsigned c) {
+    unsigned s = (c >> 7) & 1u, E = (c >> 3) & 15u, m = c & 7u;
+    double mag;
+    if (E == 15u && m == 7u) return NAN;
+    if (E == 0u) mag = ldexp((double)m, -9);
+    else mag = ldexp(1.0 + (double)m / 8.0, (int)E - 7);
+    return s ? -mag : mag;
+}
+
+/* e2m1: sign, 2-bit exponent (bias 1), 1-bit mantissa; E = 0 is subnormal m * 0.5.
+ * Magnitudes {0, .5, 1, 1.5, 2, 3, 4, 6}. Only the low nibble of c is read. */
+double orc_decode_e2m1(unsigned c) {
+    unsigned s = (c >> 3) & 1u, E = (c >> 1) & 3u, m = c & 1u;
+    double mag;
+    if (E == 0u) mag = 0.5 * (double)m;
+    else mag = ldexp(1.0 + (double)m / 2.0, (int)E - 1);
+    return s ? -mag : mag;
+}
+
+/* UE8M0: a bare biased exponent, 2^(b - 127); 0xFF is NaN. */
+double orc_decode_ue8m0(unsigned c) {
+    c &= 0xFFu;
+    if (c == 0xFFu) return NAN;
+    return ldexp(1.0, (int)c - 127);
+}
+
+float orc_bf16_to_f32(uint16_t b) {
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return f;
+}
+
+/* ------------------------------------------------------------------------------------
+ * Encoders: round to nearest, ties to even, saturating (reading R1).
+ *
+ * A format with `mbits` mantissa bits and smallest normal exponent `emin` spaces its
+ * values 2^(E - mbits) apart inside the binade [2^E, 2^(E+1)) and 2^(emin - mbits) apart
+ * below 2^emin (subnormals). With E = max(floor(log2 |v|), emin), q = |v| / 2^(E - mbits)
+ * is exact in fp64 and the magnitude code is ((E - emin) << mbits) + RNE(q): the integer
+ * q' = RNE(q) carries the code's last bit, so "ties to even" on q' is "ties to the even
+ * code", and q' = 2^(mbits+1) rolls over into the next binade's first code.
+ * ---------------------------------------------------------------------------------- */
+static unsigned encode_rne_sat(double v, int mbits, int emin, double maxval, unsigned maxcode,
+                               unsigned signbit_pos) {
+    unsigned sign = signbit(v) ? 1u : 0u;
+    double a = fabs(v);
+    unsigned mag;
+    if (a >= maxval) {
+        mag = maxcode;
+    } else {
+        int ex = 0;
+        int E;
+        double q, r;
+        if (a == 0.0) {
+            E = emin;
+        } else {
+            (void)frexp(a, &ex); /* a = f * 2^ex, f in [0.5, 1): floor(log2 a) = ex - 1 */
+            E = ex - 1;
+            if (E < emin) E = emin;
+        }
+        q = ldexp(a, mbits - E);    /* exact: scaling by a power of two */
+        r = nearbyint(q);           /* default rounding mode: to nearest, ties to even */
+        mag = ((unsigned)(E - emin) << mbits) + (unsigned)r;
+        if (mag > maxcode) mag = maxcode; /* cannot trigger for a < maxval; kept as a guard */
+    }
+    return (sign << signbit_pos) | mag;
+}
+
+unsigned orc_encode_e4m3(double v) { return encode_rne_sat(v, 3, -6, 448.0, 0x7Eu, 7); }
+unsigned orc_encode_e2m1(double v) { return encode_rne_sat(v, 1, 0, 6.0, 0x7u, 3); }
+
+/* ------------------------------------------------------------------------------------
+ * Scale layout (reading R5).
+ * ---------------------------------------------------------------------------------- */
+static int64_t block_size(int fmt) { return fmt == ORC_NVFP4 ? 16 : 32; }
+
+static int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+int64_t orc_scale_tiled_offset(int64_t r, int64_t c, int64_t n_scale_cols) {
+    int64_t n_col_tiles = ceil_div(n_scale_cols, 4);
+    int64_t tile = (r / 128) * n_col_tiles + c / 4;
+    return tile * 512 + (r % 32) * 16 + ((r / 32) % 4) * 4 + (c % 4);
+}
+
+int64_t orc_scales_tiled_bytes(int fmt, int64_t rows, int64_t cols) {
+    int64_t nsc = cols / block_size(fmt);
+    int64_t bytes = ceil_div(rows, 128) * ceil_div(nsc, 4) * 512;
+    return fmt == ORC_NVFP4 ? bytes + 16 : bytes;
+}
+
+int64_t orc_codes_bytes(int fmt, int64_t rows, int64_t cols) {
+    return fmt == ORC_MXFP8 ? rows * cols : rows * cols / 2;
+}
+
+/* Plain row-major scales (rows x n_scale_cols) -> tiled layout; pads are 0, NVFP4 tail set. */
+int orc_tile_scales(int fmt, const uint8_t* plain, int64_t rows, int64_t cols, float g, float amax,
+                    uint8_t* tiled) {
+    int64_t nsc, bytes, r, c;
+    if (!plain || !tiled || rows <= 0 || cols <= 0) return ORC_ERR_ARG;
+    nsc = cols / block_size(fmt);
+    bytes = orc_scales_tiled_bytes(fmt, rows, cols);
+    memset(tiled, 0, (size_t)bytes);
+    for (r = 0; r < rows; ++r)
+        for (c = 0; c < nsc; ++c) tiled[orc_scale_tiled_offset(r, c, nsc)] = plain[r * nsc + c];
+    if (fmt == ORC_NVFP4) {
+        float tail[4] = {g, amax, 0.0f, 0.0f};
+        memcpy(tiled + bytes - 16, tail, 16);
+    }
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------------------
+ * Quantizers.
+ * ---------------------------------------------------------------------------------- */
+static float load_src(const void* src, int src_f32, int64_t i) {
+    if (src_f32) return ((const float*)src)[i];
+    return orc_bf16_to_f32(((const uint16_t*)src)[i]);
+}
+
+static int check_finite(const void* src, int src_f32, int64_t n) {
+    int64_t i;
+    int bad = 0;
+#pragma omp parallel for reduction(| : bad)
+    for (i = 0; i < n; ++i) {
+        float x = load_src(src, src_f32, i);
+        if (!isfinite(x)) bad |= 1;
+    }
+    return bad ? ORC_ERR_NONFINITE : ORC_OK;
+}
+
+static void put_code(int fmt, uint8_t* codes, int64_t idx, unsigned code) {
+    if (fmt == ORC_MXFP8) {
+        codes[idx] = (uint8_t)code;
+    } else { /* reading R4: even element in the low nibble */
+        uint8_t* b = &codes[idx >> 1];
+        if ((idx & 1) == 0) *b = (uint8_t)((*b & 0xF0u) | (code & 0xFu));
+        else *b = (uint8_t)((*b & 0x0Fu) | ((code & 0xFu) << 4));
+    }
+}
+
+/* MXFP8 / MXFP4 [LT section 2] with the shared-exponent rule R2.
+ * src: rows x cols, bf16 bits (src_f32 = 0) or fp32. codes: MXFP8 rows*cols bytes, MXFP4
+ * rows*cols/2 bytes. scales: plain row-major rows x (cols/32) UE8M0 bytes. */
+int orc_quantize_mx(int fmt, const void* src, int src_f32, int64_t rows, int64_t cols,
+                    uint8_t* codes, uint8_t* scales) {
+    int64_t nsc, r;
+    int emax_elem, st;
+    if (!src || !codes || !scales || rows <= 0 || cols <= 0) return ORC_ERR_ARG;
+    if (fmt != ORC_MXFP8 && fmt != ORC_MXFP4) return ORC_ERR_ARG;
+    if (cols % 32) return ORC_ERR_SHAPE;
+    st = check_finite(src, src_f32, rows * cols);
+    if (st) return st;
+    nsc = cols / 32;
+    emax_elem = fmt == ORC_MXFP8 ? 8 : 2; /* exponent of the largest binade: 448 = 1.75*2^8, 6 = 1.5*2^2 */
+#pragma omp parallel for schedule(static)
+    for (r = 0; r < rows; ++r) {
+        int64_t b;
+        for (b = 0; b < nsc; ++b) {
+            int64_t k, base = r * cols + b * 32;
+            double amax = 0.0;
+            int e, ex;
+            for (k = 0; k < 32; ++k) {
+                double a = fabs((double)load_src(src, src_f32, base + k));
+                if (a > amax) amax = a;
+            }
+            if (amax == 0.0) {
+                e = -127;
+            } else {
+                (void)frexp(amax, &ex);
+                e = (ex - 1) - emax_elem;
+                if (e < -127) e = -127;
+                if (e > 127) e = 127;
+            }
+            scales[r * nsc + b] = (uint8_t)(e + 127);
+            for (k = 0; k < 32; ++k) {
+                double v = ldexp((double)load_src(src, src_f32, base + k), -e); /* exact */
+                unsigned code = fmt == ORC_MXFP8 ? orc_encode_e4m3(v) : orc_encode_e2m1(v);
+                put_code(fmt, codes, base + k, code);
+            }
+        }
+    }
+    return ORC_OK;
+}
+
+float orc_tensor_amax(const void* src, int src_f32, int64_t n) {
+    int64_t i;
+    float amax = 0.0f;
+#pragma omp parallel for reduction(max : amax)
+    for (i = 0; i < n; ++i) {
+        float a = fabsf(load_src(src, src_f32, i));
+        if (a > amax) amax = a;
+    }
+    return amax;
+}
+
+/* NVFP4 [LT section 2] with the two-level scaling R3.
+ * scales: plain row-major rows x (cols/16) E4M3 bytes. g_out / amax_out receive the
+ * per-tensor scale used and the tensor's own amax. */
+int orc_quantize_nvfp4(const void* src, int src_f32, int64_t rows, int64_t cols, int global_given,
+                       float g_in, uint8_t* codes, uint8_t* scales, float* g_out, float* amax_out) {
+    int64_t nsc, r;
+    float amax, g, six_g;
+    int st;
+    if (!src || !codes || !scales || rows <= 0 || cols <= 0) return ORC_ERR_ARG;
+    if (cols % 16) return ORC_ERR_SHAPE;
+    st = check_finite(src, src_f32, rows * cols);
+    if (st) return st;
+    if (global_given && !(isfinite(g_in) && g_in >= 0.0f)) return ORC_ERR_ARG;
+    nsc = cols / 16;
+    amax = orc_tensor_amax(src, src_f32, rows * cols);
+    g = global_given ? g_in : amax / 2688.0f; /* one fp32 division, 2688 = 6 * 448 */
+    six_g = 6.0f * g;                          /* one fp32 multiplication */
+#pragma omp parallel for schedule(static)
+    for (r = 0; r < rows; ++r) {
+        int64_t b;
+        for (b = 0; b < nsc; ++b) {
+            int64_t k, base = r * cols + b * 16;
+            float bamax = 0.0f, q, s, sg;
+            unsigned s_code;
+            for (k = 0; k < 16; ++k) {
+                float a = fabsf(load_src(src, src_f32, base + k));
+                if (a > bamax) bamax = a;
+            }
+            if (g == 0.0f) {
+                s_code = 0;
+            } else {
+                q = bamax / six_g;                       /* fp32 division */
+                s_code = orc_encode_e4m3((double)q) & 0x7Fu; /* q >= 0; a +0 code for q = 0 */
+            }
+            scales[r * nsc + b] = (uint8_t)s_code;
+            s = (float)orc_decode_e4m3(s_code);          /* exact in fp32 */
+            sg = s * g;                                  /* fp32 multiplication */
+            for (k = 0; k < 16; ++k) {
+                float x = load_src(src, src_f32, base + k);
+                unsigned code;
+                if (s == 0.0f) {
+                    code = signbit(x) ? 0x8u : 0x0u;
+                } else {
+                    float y = x / sg;                    /* fp32 division */
+                    code = orc_encode_e2m1((double)y);
+                }
+                put_code(ORC_NVFP4, codes, base + k, code);
+            }
+        }
+    }
+    if (g_out) *g_out = g;
+    if (amax_out) *amax_out = amax;
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------------------
+ * Decode to fp64 (exact): MX x = code * 2^(byte - 127); NVFP4 x = code * s (the per-tensor
+ * g is applied by the GEMM's alpha, reading R6). scales are plain row-major.
+ * ---------------------------------------------------------------------------------- */
+int orc_decode(int fmt, const uint8_t* codes, const uint8_t* scales, int64_t rows, int64_t cols,
+               double* out) {
+    int64_t bs, nsc, r;
+    if (!codes || !scales || !out || rows <= 0 || cols <= 0) return ORC_ERR_ARG;
+    bs = block_size(fmt);
+    if (cols % bs) return ORC_ERR_SHAPE;
+    nsc = cols / bs;
+#pragma omp parallel for schedule(static)
+    for (r = 0; r < rows; ++r) {
+        int64_t k;
+        for (k = 0; k < cols; ++k) {
+            int64_t idx = r * cols + k;
+            uint8_t sb = scales[r * nsc + k / bs];
+            double v, s;
+            if (fmt == ORC_MXFP8) v = orc_decode_e4m3(codes[idx]);
+            else v = orc_decode_e2m1((idx & 1) ? (codes[idx >> 1] >> 4) : (codes[idx >> 1] & 0xFu));
+            s = fmt == ORC_NVFP4 ? orc_decode_e4m3(sb) : orc_decode_ue8m0(sb);
+            out[idx] = v * s;
+        }
+    }
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------------------
+ * GEMM (reading R6), rows [row0, row1) of the output:
+ *   out[m - row0, n] = alpha * sum_k A[m,k] * B[n,k] + bias[n]
+ *   abs_out[m - row0, n] = |alpha| * sum_k |A[m,k] * B[n,k]|   (for the tolerance)
+ * A: M x K, B: N x K (both K contiguous), fp64. bias: N bf16 bits or NULL.
+ * ---------------------------------------------------------------------------------- */
+int orc_gemm(const double* A, const double* B, const uint16_t* bias, int64_t M, int64_t N, int64_t K,
+             double alpha, int64_t row0, int64_t row1, double* out, double* abs_out) {
+    int64_t m;
+    if (!A || !B || !out || M <= 0 || N <= 0 || K <= 0) return ORC_ERR_ARG;
+    if (row0 < 0 || row1 > M || row0 >= row1) return ORC_ERR_ARG;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (m = row0; m < row1; ++m) {
+        const double* a = A + m * K;
+        int64_t n;
+        for (n = 0; n < N; ++n) {
+            const double* b = B + n * K;
+            double acc = 0.0, acc_abs = 0.0;
+            int64_t k;
+            for (k = 0; k < K; ++k) {
+                double p = a[k] * b[k];
+                acc += p;
+                acc_abs += fabs(p);
+            }
+            out[(m - row0) * N + n] = alpha * acc + (bias ? (double)orc_bf16_to_f32(bias[n]) : 0.0);
+            if (abs_out) abs_out[(m - row0) * N + n] = fabs(alpha) * acc_abs;
+        }
+    }
+    return ORC_OK;
+}
