@@ -1,0 +1,188 @@
+"""Python binding of libbsq.so: block-scaled quantization (MXFP8, NVFP4, MXFP4) and the
+block-scaled GEMM with a fused bias + bf16 epilogue on GB300 (sm_103a).
+
+The functions named like the C ABI (``bsq_quantize``, ``bsq_gemm``, ...) only marshal
+arguments: torch tensors are passed as device pointers, the current torch stream as the
+CUDA stream. ``quantize`` / ``gemm`` / ``linear`` add output allocation with torch (device
+memory is the only thing torch provides here). Every step of the computation runs in the
+library's CUDA kernels; there is no other implementation, and importing this package
+raises if libbsq.so is missing.
+"""
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+import os
+from typing import Optional, Union
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libbsq.so")
+
+MXFP8, NVFP4, MXFP4 = 1, 2, 3
+FLAG_SRC_F32 = 0x100
+FLAG_GLOBAL_GIVEN = 0x200
+FORMATS = {"mxfp8": MXFP8, "nvfp4": NVFP4, "mxfp4": MXFP4}
+
+OK, ERR_ARG, ERR_SHAPE, ERR_ALIGN, ERR_ARCH, ERR_LAUNCH, ERR_TIMEOUT = 0, -1, -2, -3, -4, -5, -6
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError("libbsq.so is not built (run block_scaled_precision_bsq_gb300.build.build() "
+                      "or __graft_entry__.build()); there is no fallback implementation")
+
+_lib = ctypes.CDLL(LIB_PATH)
+_i64, _vp, _int = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
+_lib.bsq_codes_bytes.restype = ctypes.c_size_t
+_lib.bsq_codes_bytes.argtypes = [_int, _i64, _i64]
+_lib.bsq_scales_bytes.restype = ctypes.c_size_t
+_lib.bsq_scales_bytes.argtypes = [_int, _i64, _i64]
+_lib.bsq_quantize.restype = _int
+_lib.bsq_quantize.argtypes = [_int, _vp, _i64, _i64, _vp, _vp, _vp, _vp]
+_lib.bsq_gemm.restype = _int
+_lib.bsq_gemm.argtypes = [_int, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp]
+_lib.bsq_get_device_status.restype = _int
+_lib.bsq_get_device_status.argtypes = [_vp]
+_lib.bsq_selftest_timeout.restype = _int
+_lib.bsq_selftest_timeout.argtypes = [_i64, _vp]
+_lib.bsq_last_error.restype = _int
+_lib.bsq_strerror.restype = ctypes.c_char_p
+_lib.bsq_strerror.argtypes = [_int]
+
+EXPORTS = ("bsq_codes_bytes", "bsq_scales_bytes", "bsq_quantize", "bsq_gemm", "bsq_get_device_status",
+           "bsq_selftest_timeout", "bsq_last_error", "bsq_strerror")
+
+Ptr = Union[int, None, torch.Tensor]
+
+
+class BsqError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__("%s failed: %d (%s)" % (what, code, bsq_strerror(code)))
+        self.code = code
+
+
+def _p(x: Ptr) -> Optional[int]:
+    if x is None:
+        return None
+    if isinstance(x, torch.Tensor):
+        return x.data_ptr() if x.numel() > 0 else None
+    return int(x)
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream if torch.cuda.is_available() else None
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _fmt(fmt) -> int:
+    return FORMATS[fmt] if isinstance(fmt, str) else int(fmt)
+
+
+# ---------------------------------------------------------------- C ABI, one to one
+def bsq_codes_bytes(fmt, rows: int, cols: int) -> int:
+    return int(_lib.bsq_codes_bytes(_fmt(fmt), rows, cols))
+
+
+def bsq_scales_bytes(fmt, rows: int, cols: int) -> int:
+    return int(_lib.bsq_scales_bytes(_fmt(fmt), rows, cols))
+
+
+def bsq_quantize(fmt_flags: int, src: Ptr, rows: int, cols: int, codes: Ptr, scales: Ptr,
+                 global_scale: Ptr = None, stream=None) -> int:
+    return int(_lib.bsq_quantize(int(fmt_flags), _p(src), rows, cols, _p(codes), _p(scales), _p(global_scale),
+                                 _stream(stream)))
+
+
+def bsq_gemm(fmt, A: Ptr, A_scales: Ptr, B: Ptr, B_scales: Ptr, bias: Ptr, out: Ptr, M: int, N: int, K: int,
+             stream=None) -> int:
+    return int(_lib.bsq_gemm(_fmt(fmt), _p(A), _p(A_scales), _p(B), _p(B_scales), _p(bias), _p(out), M, N, K,
+                             _stream(stream)))
+
+
+def bsq_get_device_status(stream=None) -> int:
+    return int(_lib.bsq_get_device_status(_stream(stream)))
+
+
+def bsq_selftest_timeout(limit_ns: int, stream=None) -> int:
+    return int(_lib.bsq_selftest_timeout(int(limit_ns), _stream(stream)))
+
+
+def bsq_last_error() -> int:
+    return int(_lib.bsq_last_error())
+
+
+def bsq_strerror(code: int) -> str:
+    return _lib.bsq_strerror(int(code)).decode()
+
+
+# ---------------------------------------------------------------- tensor-level helpers
+@dataclasses.dataclass
+class QTensor:
+    """A quantized rows x cols matrix: packed codes, tiled scales (with the NVFP4 tail) and,
+    for NVFP4, a one-element fp32 tensor holding the per-tensor scale g."""
+
+    fmt: int
+    rows: int
+    cols: int
+    codes: torch.Tensor
+    scales: torch.Tensor
+    global_scale: Optional[torch.Tensor] = None
+
+
+def empty_qtensor(fmt, rows: int, cols: int, device="cuda") -> QTensor:
+    f = _fmt(fmt)
+    codes = torch.empty(bsq_codes_bytes(f, rows, cols), dtype=torch.uint8, device=device)
+    scales = torch.empty(bsq_scales_bytes(f, rows, cols), dtype=torch.uint8, device=device)
+    g = torch.empty(1, dtype=torch.float32, device=device) if f == NVFP4 else None
+    return QTensor(f, rows, cols, codes, scales, g)
+
+
+def quantize(fmt, x: torch.Tensor, global_scale: Optional[torch.Tensor] = None, out: Optional[QTensor] = None,
+             stream=None) -> QTensor:
+    """Quantize a contiguous bf16 or fp32 CUDA matrix along its last dimension."""
+    f = _fmt(fmt)
+    assert x.is_cuda and x.is_contiguous() and x.dim() == 2, "x must be a contiguous 2-D CUDA tensor"
+    rows, cols = x.shape
+    flags = f
+    if x.dtype == torch.float32:
+        flags |= FLAG_SRC_F32
+    elif x.dtype != torch.bfloat16:
+        raise TypeError("x must be bfloat16 or float32")
+    q = out if out is not None else empty_qtensor(f, rows, cols, x.device)
+    g = q.global_scale
+    if global_scale is not None:
+        flags |= FLAG_GLOBAL_GIVEN
+        g = global_scale
+    rc = bsq_quantize(flags, x, rows, cols, q.codes, q.scales, g, stream)
+    if rc != OK:
+        raise BsqError(rc, "bsq_quantize")
+    if global_scale is not None:
+        q.global_scale = global_scale
+    return q
+
+
+def gemm(qa: QTensor, qb: QTensor, bias: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
+         stream=None) -> torch.Tensor:
+    """out[M, N] = bf16(alpha * A_hat . B_hat^T + bias), A: M x K, B: N x K (weight layout)."""
+    assert qa.fmt == qb.fmt and qa.cols == qb.cols
+    M, K, N = qa.rows, qa.cols, qb.rows
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=qa.codes.device)
+    if bias is not None:
+        assert bias.dtype == torch.bfloat16 and bias.numel() == N and bias.is_contiguous()
+    rc = bsq_gemm(qa.fmt, qa.codes, qa.scales, qb.codes, qb.scales, bias, out, M, N, K, stream)
+    if rc != OK:
+        raise BsqError(rc, "bsq_gemm")
+    return out
+
+
+def linear(fmt, x: torch.Tensor, w: torch.Tensor, bias: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """The whole block-scaled linear layer: quantize x and w along K, then the GEMM."""
+    return gemm(quantize(fmt, x, stream=stream), quantize(fmt, w, stream=stream), bias, stream=stream)
+
+
+def device_status(stream=None) -> int:
+    return bsq_get_device_status(stream)

@@ -1,0 +1,169 @@
+// bsq_api.cu -- the extern "C" entry points of libbsq.so: argument validation, per-device
+// properties, the device status word, and dispatch to the kernel launchers.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/bsq.h"
+#include "bsq_device.cuh"
+#include "bsq_internal.h"
+
+namespace bsq {
+
+// One status word per device (each device holds its own copy of this module's globals).
+// Kernels record the first failure with atomicCAS; bsq_get_device_status reads and clears.
+__device__ int g_status_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+DeviceInfo g_dev[kMaxDevices];
+std::once_flag g_dev_once[kMaxDevices];
+thread_local int t_last_error = 0;
+
+int fail(int code) {
+  t_last_error = code;
+  return code;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+__global__ void selftest_timeout_kernel(int64_t limit_ns, int* status) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    // nothing ever arrives on `bar`: the bounded wait must give up and record the timeout
+    mbar_wait_bounded(&bar, 0, &abort_flag, status, static_cast<uint64_t>(limit_ns));
+  }
+}
+
+}  // namespace
+
+const DeviceInfo* current_device() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::call_once(g_dev_once[dev], [dev] {
+    DeviceInfo d;
+    d.device = dev;
+    if (cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return;
+    if (cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return;
+    if (cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) return;
+    if (d.cc_major != 10 || d.cc_minor != 3) {
+      g_dev[dev] = d;  // recorded, status stays nullptr -> BSQ_ERR_ARCH
+      return;
+    }
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return;
+    d.status = static_cast<int*>(p);
+    g_dev[dev] = d;
+  });
+  const DeviceInfo& d = g_dev[dev];
+  return d.status != nullptr ? &d : nullptr;
+}
+
+int launch_selftest_timeout(int64_t limit_ns, cudaStream_t stream, const DeviceInfo& dev) {
+  selftest_timeout_kernel<<<1, 32, 0, stream>>>(limit_ns, dev.status);
+  return cudaGetLastError() == cudaSuccess ? BSQ_OK : BSQ_ERR_LAUNCH;
+}
+
+}  // namespace bsq
+
+using bsq::aligned16;
+using bsq::fail;
+
+extern "C" {
+
+size_t bsq_codes_bytes(int fmt, int64_t rows, int64_t cols) {
+  if (rows <= 0 || cols <= 0) return 0;
+  if (fmt == BSQ_MXFP8) return static_cast<size_t>(rows * cols);
+  if (fmt == BSQ_NVFP4 || fmt == BSQ_MXFP4) return static_cast<size_t>(rows * cols / 2);
+  return 0;
+}
+
+size_t bsq_scales_bytes(int fmt, int64_t rows, int64_t cols) {
+  if (rows <= 0 || cols <= 0 || (fmt != BSQ_MXFP8 && fmt != BSQ_NVFP4 && fmt != BSQ_MXFP4)) return 0;
+  const int64_t body = bsq::scales_body_bytes(fmt, rows, cols);
+  return static_cast<size_t>(fmt == BSQ_NVFP4 ? body + 16 : body);
+}
+
+int bsq_quantize(int fmt_flags, const void* src, int64_t rows, int64_t cols, void* codes, void* scales,
+                 float* global_scale, bsq_stream_t stream) {
+  const int fmt = fmt_flags & BSQ_FMT_MASK;
+  const int flags = fmt_flags & ~BSQ_FMT_MASK;
+  if (fmt != BSQ_MXFP8 && fmt != BSQ_NVFP4 && fmt != BSQ_MXFP4) return fail(BSQ_ERR_ARG);
+  if (flags & ~(BSQ_FLAG_SRC_F32 | BSQ_FLAG_GLOBAL_GIVEN)) return fail(BSQ_ERR_ARG);
+  if (src == nullptr || codes == nullptr || scales == nullptr || rows <= 0 || cols <= 0) return fail(BSQ_ERR_ARG);
+  const bool given = (flags & BSQ_FLAG_GLOBAL_GIVEN) != 0;
+  if (fmt == BSQ_NVFP4 && given && global_scale == nullptr) return fail(BSQ_ERR_ARG);
+  if (fmt != BSQ_NVFP4 && given) return fail(BSQ_ERR_ARG);
+  if (cols % bsq::block_size(fmt) != 0) return fail(BSQ_ERR_SHAPE);
+  if (!aligned16(src) || !aligned16(codes) || !aligned16(scales)) return fail(BSQ_ERR_ALIGN);
+  if (global_scale != nullptr && (reinterpret_cast<uintptr_t>(global_scale) & 3u)) return fail(BSQ_ERR_ALIGN);
+  const bsq::DeviceInfo* dev = bsq::current_device();
+  if (dev == nullptr) return fail(BSQ_ERR_ARCH);
+  const int st = bsq::launch_quantize(fmt, (flags & BSQ_FLAG_SRC_F32) != 0, given, src, rows, cols, codes, scales,
+                                      fmt == BSQ_NVFP4 ? global_scale : nullptr, reinterpret_cast<cudaStream_t>(stream),
+                                      *dev);
+  return st == BSQ_OK ? BSQ_OK : fail(st);
+}
+
+int bsq_gemm(int fmt, const void* A, const void* A_scales, const void* B, const void* B_scales,
+             const void* bias_bf16, void* out_bf16, int64_t M, int64_t N, int64_t K, bsq_stream_t stream) {
+  if (fmt != BSQ_MXFP8 && fmt != BSQ_NVFP4 && fmt != BSQ_MXFP4) return fail(BSQ_ERR_ARG);
+  if (A == nullptr || A_scales == nullptr || B == nullptr || B_scales == nullptr || out_bf16 == nullptr)
+    return fail(BSQ_ERR_ARG);
+  if (M <= 0 || N <= 0 || K <= 0) return fail(BSQ_ERR_ARG);
+  if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return fail(BSQ_ERR_SHAPE);
+  if (K % (fmt == BSQ_MXFP8 ? 128 : 256) != 0 || N % 8 != 0) return fail(BSQ_ERR_SHAPE);
+  if (!aligned16(A) || !aligned16(A_scales) || !aligned16(B) || !aligned16(B_scales) || !aligned16(out_bf16))
+    return fail(BSQ_ERR_ALIGN);
+  if (bias_bf16 != nullptr && (reinterpret_cast<uintptr_t>(bias_bf16) & 1u)) return fail(BSQ_ERR_ALIGN);
+  const bsq::DeviceInfo* dev = bsq::current_device();
+  if (dev == nullptr) return fail(BSQ_ERR_ARCH);
+  const int st = bsq::launch_gemm(fmt, A, A_scales, B, B_scales, bias_bf16, out_bf16, M, N, K,
+                                  reinterpret_cast<cudaStream_t>(stream), *dev);
+  return st == BSQ_OK ? BSQ_OK : fail(st);
+}
+
+int bsq_get_device_status(bsq_stream_t stream) {
+  const bsq::DeviceInfo* dev = bsq::current_device();
+  if (dev == nullptr) return fail(BSQ_ERR_ARCH);
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return fail(BSQ_ERR_LAUNCH);
+  int v = 0;
+  const int zero = 0;
+  if (cudaMemcpy(&v, dev->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return fail(BSQ_ERR_LAUNCH);
+  if (cudaMemcpy(dev->status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return fail(BSQ_ERR_LAUNCH);
+  return v;
+}
+
+int bsq_selftest_timeout(int64_t limit_ns, bsq_stream_t stream) {
+  if (limit_ns < 1000 || limit_ns > 10000000000ll) return fail(BSQ_ERR_ARG);
+  const bsq::DeviceInfo* dev = bsq::current_device();
+  if (dev == nullptr) return fail(BSQ_ERR_ARCH);
+  const int st = bsq::launch_selftest_timeout(limit_ns, reinterpret_cast<cudaStream_t>(stream), *dev);
+  return st == BSQ_OK ? BSQ_OK : fail(st);
+}
+
+int bsq_last_error(void) { return bsq::t_last_error; }
+
+const char* bsq_strerror(int status) {
+  switch (status) {
+    case BSQ_OK: return "ok";
+    case BSQ_ERR_ARG: return "invalid argument (null pointer, non-positive size, unknown format or flag)";
+    case BSQ_ERR_SHAPE: return "unsupported shape (block size, K or N multiple)";
+    case BSQ_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case BSQ_ERR_ARCH: return "no compute capability 10.3 (GB300) device";
+    case BSQ_ERR_LAUNCH: return "CUDA launch or runtime error";
+    case BSQ_ERR_TIMEOUT: return "a kernel's bounded wait timed out";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

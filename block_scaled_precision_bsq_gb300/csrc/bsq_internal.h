@@ -1,0 +1,38 @@
+// bsq_internal.h -- host-side declarations shared by the translation units of libbsq.so.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace bsq {
+
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+inline int64_t block_size(int fmt) { return fmt == 2 /*BSQ_NVFP4*/ ? 16 : 32; }
+
+// Bytes of the tiled scale body (128-row x 4-column tiles of 512 bytes), without the NVFP4 tail.
+inline int64_t scales_body_bytes(int fmt, int64_t rows, int64_t cols) {
+  const int64_t nsc = cols / block_size(fmt);
+  return ceil_div(rows, 128) * ceil_div(nsc, 4) * 512;
+}
+
+struct DeviceInfo {
+  int device = -1;
+  int num_sms = 0;
+  int cc_major = 0, cc_minor = 0;
+  int* status = nullptr;  // device address of the status word
+};
+
+// Current device's cached properties (and the status word's address); nullptr when no
+// usable device. Thread-safe.
+const DeviceInfo* current_device();
+
+int launch_quantize(int fmt, bool src_f32, bool global_given, const void* src, int64_t rows, int64_t cols,
+                    void* codes, void* scales, float* global_scale, cudaStream_t stream, const DeviceInfo& dev);
+
+int launch_gemm(int fmt, const void* A, const void* A_scales, const void* B, const void* B_scales, const void* bias,
+                void* out, int64_t M, int64_t N, int64_t K, cudaStream_t stream, const DeviceInfo& dev);
+
+int launch_selftest_timeout(int64_t limit_ns, cudaStream_t stream, const DeviceInfo& dev);
+
+}  // namespace bsq

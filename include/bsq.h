@@ -1,0 +1,143 @@
+/*
+ * bsq.h -- C ABI of libbsq.so: block-scaled low-precision quantization (MXFP8, NVFP4,
+ * MXFP4) and the block-scaled GEMM with a fused bias + bf16 epilogue, for GB300 (sm_103a).
+ *
+ * The method: the linear layers of a ViT block (qkv, proj, fc1, fc2) run as block-scaled
+ * low-precision GEMMs ("lightly-train - DINOv3 + EoMT on RTX 5090" README, section 2 number
+ * formats table; sections 4.3 and 5.3 name the quantized GEMMs). A layer is two steps:
+ *   1. per-block quantization of a bf16 (or fp32) matrix along its K dimension;
+ *   2. out = bf16(alpha * sum_k Ahat[m,k] * Bhat[n,k] + bias[n]), fp32 accumulation.
+ *
+ * Conventions shared by every entry point
+ *   - All buffer pointers are DEVICE pointers, 16-byte aligned, allocated by the caller;
+ *     the library allocates no memory and keeps no per-call state. Its only state is one
+ *     status word per device (see bsq_get_device_status) and a thread-local last error.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default stream) and
+ *     returns without synchronising, except bsq_get_device_status.
+ *   - Matrices are row-major. Quantized operands are "K-major": element (r, k) of a
+ *     rows x cols matrix is at r * cols + k (the "TN" GEMM of section 5.5 of the README).
+ *   - Return value 0 = enqueued; a negative BSQ_ERR_* = nothing was enqueued (argument
+ *     errors) or the launch failed (BSQ_ERR_LAUNCH). Device-side failures (a bounded wait
+ *     that gave up) are reported later through bsq_get_device_status.
+ *   - Requires a compute capability 10.3 device (GB300); otherwise BSQ_ERR_ARCH.
+ */
+#ifndef BSQ_H
+#define BSQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* bsq_stream_t; /* identical to cudaStream_t */
+
+/* Formats (README section 2, number-format table):
+ *   BSQ_MXFP8  E4M3 elements, one UE8M0 (power-of-two) scale per 1x32 block, 8.25 bits/value.
+ *   BSQ_NVFP4  e2m1 elements (2 per byte), one E4M3 scale per 1x16 block and one fp32
+ *              per-tensor scale g, 4.5 bits/value.
+ *   BSQ_MXFP4  e2m1 elements, one UE8M0 scale per 1x32 block, 4.25 bits/value. */
+typedef enum { BSQ_MXFP8 = 1, BSQ_NVFP4 = 2, BSQ_MXFP4 = 3 } bsq_format;
+
+/* Flags OR-ed into bsq_quantize's first argument. */
+#define BSQ_FMT_MASK 0xFF
+#define BSQ_FLAG_SRC_F32 0x100      /* src holds fp32 values; default: bf16 */
+#define BSQ_FLAG_GLOBAL_GIVEN 0x200 /* NVFP4: read g from *global_scale instead of computing it
+                                       (a static or delayed per-tensor scale, README sections
+                                       4.3 and 5.5) */
+
+/* Status codes. */
+#define BSQ_OK 0
+#define BSQ_ERR_ARG -1     /* null pointer, non-positive size, unknown format or flag */
+#define BSQ_ERR_SHAPE -2   /* a size the format or the GEMM cannot tile (see each call) */
+#define BSQ_ERR_ALIGN -3   /* a pointer is not 16-byte aligned */
+#define BSQ_ERR_ARCH -4    /* no CUDA device, or not compute capability 10.3 */
+#define BSQ_ERR_LAUNCH -5  /* the CUDA runtime reported an error at launch */
+#define BSQ_ERR_TIMEOUT -6 /* a kernel's bounded wait gave up (device status only) */
+
+/*
+ * bsq_codes_bytes: size of the element-code buffer of a rows x cols matrix.
+ *   MXFP8: rows * cols bytes (one E4M3 code per byte).
+ *   NVFP4, MXFP4: rows * cols / 2 bytes; element 2j in the low nibble of byte j, 2j+1 in
+ *   the high nibble. Returns 0 for invalid arguments.
+ */
+size_t bsq_codes_bytes(int fmt, int64_t rows, int64_t cols);
+
+/*
+ * bsq_scales_bytes: size of the scale buffer of a rows x cols matrix.
+ * Block scales are stored in tiles of 128 rows x 4 scale columns (512 bytes): the scale of
+ * row r and block column c lives in tile (r / 128) * ceil(nsc / 4) + c / 4 at byte
+ * (r % 32) * 16 + ((r / 32) % 4) * 4 + c % 4, nsc = cols / block size. Rows are padded to
+ * 128 and scale columns to 4; padding bytes are written as 0. This is the layout the
+ * tensor cores' scale-factor copy consumes, so the GEMM reads it without reshuffling.
+ * NVFP4 appends a 16-byte tail {g, amax, 0, 0} (fp32): the per-tensor scale used and the
+ * amax of the quantized tensor (the source of a delayed scale for the next call).
+ * Returns 0 for invalid arguments.
+ */
+size_t bsq_scales_bytes(int fmt, int64_t rows, int64_t cols);
+
+/*
+ * bsq_quantize: quantize a rows x cols matrix along cols (K) in 1x32 (MX) or 1x16 (NVFP4)
+ * blocks.
+ *   fmt_flags    bsq_format | BSQ_FLAG_* bits.
+ *   src          rows x cols bf16 (default) or fp32 (BSQ_FLAG_SRC_F32) values, finite.
+ *   codes        bsq_codes_bytes(fmt, rows, cols) bytes, written.
+ *   scales       bsq_scales_bytes(fmt, rows, cols) bytes, written (including padding).
+ *   global_scale NVFP4 only, one fp32 in device memory. Without BSQ_FLAG_GLOBAL_GIVEN it
+ *                receives g = amax(|src|) / 2688 (may be NULL: g is also in the scale tail);
+ *                with the flag it is read as g (must not be NULL). Ignored for MX formats.
+ * Rules (README section 2; rounding to nearest even with saturation at the largest finite
+ * value, 448 for E4M3 and 6 for e2m1):
+ *   MX     per block e = floor(log2(amax)) - emax (emax 8 for E4M3, 2 for e2m1), clamped to
+ *          [-127, 127], amax = 0 -> -127; scale byte e + 127; code = RNE_sat(x * 2^-e).
+ *   NVFP4  s = E4M3 RNE_sat(bamax / (6 g)); code = e2m1 RNE_sat(x / (s g)), each step one
+ *          IEEE fp32 operation; s = 0 gives zero codes carrying the sign of x.
+ * Shapes: cols % 32 == 0 (MX) or cols % 16 == 0 (NVFP4), else BSQ_ERR_SHAPE; any rows >= 1.
+ * Codes and scales are bit-exact functions of the input (no dependence on launch shape).
+ */
+int bsq_quantize(int fmt_flags, const void* src, int64_t rows, int64_t cols, void* codes, void* scales,
+                 float* global_scale, bsq_stream_t stream);
+
+/*
+ * bsq_gemm: out[m, n] = bf16_rn(alpha * sum_k Ahat[m,k] * Bhat[n,k] + bias[n]).
+ *   A, A_scales  M x K operand as written by bsq_quantize(fmt, ..., M, K, ...).
+ *   B, B_scales  N x K operand (the nn.Linear weight layout) from bsq_quantize(fmt, ..., N, K, ...).
+ *   bias_bf16    N bf16 values, or NULL for no bias.
+ *   out_bf16     M x N bf16, row-major, written.
+ *   alpha        1 for MX formats; g_A * g_B for NVFP4, read on the device from the two
+ *                scale tails (no host synchronisation).
+ * Products are accumulated in fp32 in the tensor cores (tcgen05 block-scaled MMA).
+ * Shapes: K % 128 == 0 (MXFP8) or K % 256 == 0 (NVFP4, MXFP4); N % 8 == 0; M >= 1 (rows
+ * past M are never written). Otherwise BSQ_ERR_SHAPE.
+ */
+int bsq_gemm(int fmt, const void* A, const void* A_scales, const void* B, const void* B_scales,
+             const void* bias_bf16, void* out_bf16, int64_t M, int64_t N, int64_t K, bsq_stream_t stream);
+
+/*
+ * bsq_get_device_status: synchronise `stream`, then read and clear the current device's
+ * status word. Returns BSQ_OK, BSQ_ERR_TIMEOUT (a kernel's bounded wait on an mbarrier
+ * gave up; that kernel returned early and its outputs are incomplete) or BSQ_ERR_LAUNCH
+ * (a CUDA error while synchronising).
+ */
+int bsq_get_device_status(bsq_stream_t stream);
+
+/*
+ * bsq_selftest_timeout: enqueue a one-thread kernel that waits on an mbarrier nothing
+ * arrives on, bounded by limit_ns nanoseconds of %globaltimer; it then records
+ * BSQ_ERR_TIMEOUT in the device status word and returns. Exercises the failure path of
+ * every bounded wait without faulting or hanging the GPU. limit_ns in [1e3, 1e10].
+ */
+int bsq_selftest_timeout(int64_t limit_ns, bsq_stream_t stream);
+
+/* bsq_last_error: the calling thread's last non-zero return code (0 if none). */
+int bsq_last_error(void);
+
+/* bsq_strerror: a static string describing a status code. */
+const char* bsq_strerror(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BSQ_H */

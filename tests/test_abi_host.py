@@ -1,0 +1,78 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads and exports every
+function include/bsq.h declares, the size helpers, and argument validation that returns
+before any CUDA call."""
+import ctypes
+import importlib.util
+import os
+import re
+
+import pytest
+
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "bsq.h")
+
+
+@pytest.fixture(scope="module")
+def bsq():
+    spec = importlib.util.spec_from_file_location("_bsq_build", os.path.join(ROOT, "block_scaled_precision_bsq_gb300",
+                                                                            "build.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    mod.build()
+    import block_scaled_precision_bsq_gb300 as b
+
+    return b
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(bsq_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(bsq):
+    names = declared_functions()
+    assert len(names) >= 8
+    lib = ctypes.CDLL(bsq.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(bsq.EXPORTS)
+
+
+@pytest.mark.parametrize("fmt", ["mxfp8", "nvfp4", "mxfp4"])
+@pytest.mark.parametrize("rows,cols", [(1, 32), (128, 256), (200, 96), (7203, 1024), (51200, 4096)])
+def test_size_helpers_match_the_oracle_layout(bsq, fmt, rows, cols):
+    if fmt == "nvfp4" or cols % 32 == 0:
+        assert bsq.bsq_codes_bytes(fmt, rows, cols) == oracle.codes_bytes(fmt, rows, cols)
+        assert bsq.bsq_scales_bytes(fmt, rows, cols) == oracle.scales_tiled_bytes(fmt, rows, cols)
+
+
+def test_size_helpers_reject_bad_args(bsq):
+    assert bsq.bsq_codes_bytes(9, 4, 32) == 0
+    assert bsq.bsq_scales_bytes("mxfp8", 0, 32) == 0
+    assert bsq.bsq_codes_bytes("nvfp4", -1, 32) == 0
+
+
+def test_argument_errors_before_any_cuda_call(bsq):
+    p = 1 << 20  # a 16-byte aligned dummy address: never dereferenced on these paths
+    assert bsq.bsq_quantize(7, p, 4, 32, p, p) == bsq.ERR_ARG                          # unknown format
+    assert bsq.bsq_quantize(bsq.MXFP8 | 0x4000, p, 4, 32, p, p) == bsq.ERR_ARG         # unknown flag
+    assert bsq.bsq_quantize(bsq.MXFP8, None, 4, 32, p, p) == bsq.ERR_ARG
+    assert bsq.bsq_quantize(bsq.MXFP8, p, 0, 32, p, p) == bsq.ERR_ARG
+    assert bsq.bsq_quantize(bsq.MXFP8, p, 4, 48, p, p) == bsq.ERR_SHAPE                # 48 % 32
+    assert bsq.bsq_quantize(bsq.NVFP4, p, 4, 40, p, p) == bsq.ERR_SHAPE                # 40 % 16
+    assert bsq.bsq_quantize(bsq.NVFP4 | bsq.FLAG_GLOBAL_GIVEN, p, 4, 32, p, p, None) == bsq.ERR_ARG
+    assert bsq.bsq_quantize(bsq.MXFP8 | bsq.FLAG_GLOBAL_GIVEN, p, 4, 32, p, p, p) == bsq.ERR_ARG
+    assert bsq.bsq_quantize(bsq.MXFP8, p + 8, 4, 32, p, p) == bsq.ERR_ALIGN
+    assert bsq.bsq_last_error() == bsq.ERR_ALIGN
+    assert bsq.bsq_gemm(bsq.MXFP8, p, p, p, p, None, p, 128, 256, 96) == bsq.ERR_SHAPE    # K % 128
+    assert bsq.bsq_gemm(bsq.NVFP4, p, p, p, p, None, p, 128, 256, 128) == bsq.ERR_SHAPE   # K % 256
+    assert bsq.bsq_gemm(bsq.MXFP4, p, p, p, p, None, p, 128, 260, 256) == bsq.ERR_SHAPE   # N % 8
+    assert bsq.bsq_gemm(bsq.MXFP8, p, p, p, p, None, None, 128, 256, 256) == bsq.ERR_ARG
+    assert bsq.bsq_gemm(bsq.MXFP8, p, p + 4, p, p, None, p, 128, 256, 256) == bsq.ERR_ALIGN
+    assert bsq.bsq_gemm(bsq.MXFP8, p, p, p, p, p + 1, p, 128, 256, 256) == bsq.ERR_ALIGN
+    assert bsq.bsq_selftest_timeout(10, None) == bsq.ERR_ARG
+    assert bsq.bsq_strerror(bsq.ERR_TIMEOUT).startswith("a kernel")
+    assert bsq.bsq_strerror(12345) == "unknown status"

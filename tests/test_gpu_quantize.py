@@ -1,0 +1,103 @@
+"""GPU parity of the quantizer kernels against the CPU oracle: codes, tiled scales (with
+padding) and the NVFP4 tail must be bit-identical."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests.gpu_util import to_dev
+from workloads import WORKLOADS, f32_to_bf16_bits, make_activations, make_weights, random_matrix
+
+pytestmark = pytest.mark.gpu
+
+SHAPES = [(1, 32), (7, 96), (128, 256), (130, 512), (200, 768), (257, 1056), (64, 4096)]
+DISTS = ["normal", "student_t4", "uniform_exp"]
+
+
+def _bsq():
+    import block_scaled_precision_bsq_gb300 as bsq
+
+    return bsq
+
+
+def _compare(fmt, x_np, global_scale=None, label=""):
+    bsq = _bsq()
+    q = oracle.quantize(fmt, x_np, global_scale=global_scale)
+    x = to_dev(x_np)
+    gs = None if global_scale is None else torch.tensor([global_scale], dtype=torch.float32, device="cuda")
+    gq = bsq.quantize(fmt, x, global_scale=gs)
+    assert bsq.device_status() == 0
+    codes = gq.codes.cpu().numpy()
+    assert np.array_equal(codes, q.codes), "%s codes: %d bytes differ (first at %d)" % (
+        label, int((codes != q.codes).sum()), int(np.argmax(codes != q.codes)))
+    scales = gq.scales.cpu().numpy()
+    want = q.tiled_scales()
+    assert np.array_equal(scales, want), "%s scales: %d bytes differ (first at %d)" % (
+        label, int((scales != want).sum()), int(np.argmax(scales != want)))
+    if q.fmt == oracle.NVFP4 and global_scale is None:
+        assert gq.global_scale.item() == q.g
+    return gq, q
+
+
+@pytest.mark.parametrize("fmt", ["mxfp8", "nvfp4", "mxfp4"])
+@pytest.mark.parametrize("rows,cols", SHAPES)
+@pytest.mark.parametrize("dist", DISTS)
+def test_quantize_bf16_matches_oracle(fmt, rows, cols, dist):
+    x = random_matrix(rows, cols, seed=rows * 7 + cols, dist=dist)
+    _compare(fmt, x, label="%s %dx%d %s" % (fmt, rows, cols, dist))
+
+
+@pytest.mark.parametrize("fmt", ["mxfp8", "nvfp4", "mxfp4"])
+@pytest.mark.parametrize("rows,cols", [(3, 32), (128, 256), (131, 1024)])
+def test_quantize_fp32_matches_oracle(fmt, rows, cols):
+    x = random_matrix(rows, cols, seed=5, dist="uniform_exp", src_f32=True)
+    _compare(fmt, x, label="%s f32" % fmt)
+
+
+@pytest.mark.parametrize("rows,cols", [(3, 48), (130, 272), (64, 1024)])
+@pytest.mark.parametrize("g", [1.0, 0.0123, 1e-6])
+def test_nvfp4_given_scale(rows, cols, g):
+    x = random_matrix(rows, cols, seed=9, dist="student_t4")
+    gq, q = _compare("nvfp4", x, global_scale=g, label="nvfp4 given g=%g" % g)
+    assert gq.global_scale.item() == np.float32(g)
+
+
+def test_nvfp4_cols_multiple_of_16_only():
+    # 48 and 272 columns: scale columns not a multiple of 4 -> zero padding inside the tile
+    for cols in (16, 48, 272):
+        _compare("nvfp4", random_matrix(5, cols, seed=cols), label="nvfp4 cols=%d" % cols)
+
+
+@pytest.mark.parametrize("fmt", ["mxfp8", "nvfp4", "mxfp4"])
+def test_special_values(fmt):
+    # zeros, negative zeros, exact ties, saturating blocks, subnormal bf16, a zero block
+    vals = np.array([0.0, -0.0, 448.0, -500.0, 304.0, 2.5, -3.5, 0.25, 6.0, 7.0, 1e-38, -1e-39, 1.0625,
+                     3e38, -3e38, 5.0], dtype=np.float32)
+    x = np.zeros((4, 64), np.float32)
+    x[0, :16] = vals
+    x[1, :16] = vals[::-1]
+    x[2, 32:48] = vals * np.float32(1e-30)
+    x[3, :] = -0.0
+    _compare(fmt, f32_to_bf16_bits(x), label="%s specials" % fmt)
+    _compare(fmt, x, label="%s specials f32" % fmt)
+
+
+def test_nvfp4_all_zero_tensor():
+    x = np.zeros((2, 32), np.float32)
+    x[1, 5] = -0.0
+    gq, q = _compare("nvfp4", f32_to_bf16_bits(x), label="nvfp4 zero tensor")
+    assert gq.global_scale.item() == 0.0
+
+
+@pytest.mark.parametrize("name", ["vitb_fc1_mxfp8", "vitl_mxfp8", "vitl_nvfp4", "vitl_mlp_large"])
+def test_full_size_workload_quantize(name):
+    """Every activation and weight tensor of the workload, at full size, bit-exact."""
+    seen = set()
+    for g in WORKLOADS[name].gemms:
+        for kind, make in (("A", make_activations), ("B", make_weights)):
+            key = (kind, g.fmt, g.M if kind == "A" else g.N, g.K, g.a_dist if kind == "A" else "w")
+            if key in seen:
+                continue
+            seen.add(key)
+            _compare(g.fmt, make(g), label="%s %s %s" % (name, g.name, kind))
+            torch.cuda.empty_cache()
