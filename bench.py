@@ -1,0 +1,414 @@
+#!/usr/bin/env python3
+"""Benchmark of the block-scaled linear layer on GB300.
+
+One step = the whole hot path over one batch: quantize the activations A (M x K) and the
+weights B (N x K) along K, then the block-scaled GEMM with the fused bias + bf16 epilogue.
+Default workload: ViT-B/16 MLP fc1 at training shape in MXFP8 (M = 14336, K = 768,
+N = 3072). Inputs are seeded synthetic data resident in HBM; the L2 cache is flushed (a
+256 MB write) between timed steps and every step is timed with CUDA events on the stream
+the kernels run on.
+
+Printed JSON line: value = TFLOP/s of the whole step (2 M N K per GEMM); `roofline` for
+the dominant kernel (the GEMM) against the measured bf16 tensor peak times the nominal
+FP8 (x2) or FP4 (x6) ratio; `quantize` = the quantizer kernels' algorithmic GB/s against
+the measured HBM copy bandwidth; `e2e` = the same metric through the C ABI with pinned
+host buffers and the host<->device copies inside the timed region; `cpu_baseline` = the
+CPU oracle timed on a bounded sample of the same workload.
+
+--impl reference times the CPU oracle (the reference implementation of this path) alone.
+With --gpus N (N > 1, launched by torchrun) every rank runs an independent replica of the
+workload on its own GPU: the path shards by rows with no exchange (weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from workloads import MXFP8, NVFP4, MXFP4, WORKLOADS, make_activations, make_bias, make_weights  # noqa: E402
+
+METRIC = "block-scaled GEMM TFLOPS (% dense FP8/FP4 peak); quantize GB/s (% HBM)"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+NOMINAL_RATIO = {MXFP8: 4.5 / 2.25, NVFP4: 13.5 / 2.25, MXFP4: 13.5 / 2.25}
+L2_FLUSH_BYTES = 256 << 20
+FMT_NAME = {MXFP8: "mxfp8", NVFP4: "nvfp4", MXFP4: "mxfp4"}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return json.load(f), "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def quant_bytes(fmt: str, rows: int, cols: int, src_bytes: int, computed_global: bool) -> int:
+    """Algorithmic HBM bytes of one quantizer call: read the source once (twice for NVFP4
+    with a computed per-tensor scale: the amax pass), write codes and scales."""
+    n = rows * cols
+    codes = n if fmt == MXFP8 else n // 2
+    scales = n // (16 if fmt == NVFP4 else 32)
+    reads = n * src_bytes * (2 if (fmt == NVFP4 and computed_global) else 1)
+    return reads + codes + scales
+
+
+def gemm_bytes(fmt: str, M: int, N: int, K: int, bias: bool) -> int:
+    """Algorithmic HBM bytes of one GEMM: codes and scales of A and B once, bf16 out, bias."""
+    cb = 1 if fmt == MXFP8 else 0.5
+    sb = 1 / (16 if fmt == NVFP4 else 32)
+    return int((M + N) * K * (cb + sb) + 2 * M * N + (2 * N if bias else 0))
+
+
+# ----------------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples every 100 ms while the timed loop runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: str, out_path: str):
+        self.out_path = out_path
+        self.proc = None
+        try:
+            self.f = open(out_path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                                          "-lms", "100", "-i", gpu_index], stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.out_path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                    power.append(float(parts[3]))
+                except ValueError:
+                    continue
+                for nm, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_max": max(power) if power else None}
+
+
+# ----------------------------------------------------------------------------------- oracle timing
+def _oracle_linear_rows(g, rows: int) -> float:
+    import oracle
+
+    a = make_activations(g, rows=rows) if g.a_dist != "normal_outlier50" else make_activations(g)
+    b = make_weights(g)
+    bias = make_bias(g)
+    t0 = time.perf_counter()
+    qa = oracle.quantize(g.fmt, a)
+    qb = oracle.quantize(g.fmt, b)
+    alpha = qa.g * qb.g if qa.fmt == oracle.NVFP4 else 1.0
+    oracle.gemm(qa.decode(), qb.decode(), bias, alpha, want_abs=False)
+    return time.perf_counter() - t0
+
+
+def cpu_oracle_sample(gemms, target_s: float = 10.0):
+    """Time the CPU oracle (as it stands, all host cores) on a bounded sample of the workload:
+    for each GEMM, quantize R rows of A and all of B, decode, fp64 GEMM of those R rows, with R
+    chosen from two calibration runs so that the sample takes about `target_s` seconds (at
+    most the whole of A). Returns (TFLOP/s, seconds, cores, description)."""
+    import oracle
+
+    flops, secs, parts = 0, 0.0, []
+    for g in gemms:
+        rows = g.M
+        if g.a_dist != "normal_outlier50":
+            # t(R) = fixed (all of B) + R * per_row
+            t32, t160 = _oracle_linear_rows(g, 32), _oracle_linear_rows(g, 160)
+            per_row = max((t160 - t32) / 128.0, 1e-9)
+            fixed = max(t32 - 32 * per_row, 0.0)
+            rows = int(min(g.M, max(32, (target_s / len(gemms) - fixed) / per_row)))
+        secs += _oracle_linear_rows(g, rows)
+        flops += 2 * rows * g.N * g.K
+        parts.append("%s: %d of %d rows" % (g.name, rows, g.M))
+    desc = "oracle quantize (R rows of A, all of B) + decode + fp64 GEMM of R rows; " + ", ".join(parts)
+    return flops / secs / 1e12, secs, oracle.num_threads(), desc
+
+
+def config_of(wl):
+    return {"workload": wl.name, "description": wl.description,
+            "gemms": [{"name": g.name, "format": g.fmt, "M": g.M, "N": g.N, "K": g.K} for g in wl.gemms],
+            "l2": "flushed between timed steps (256 MB write)"}
+
+
+# ----------------------------------------------------------------------------------- reference arm
+def run_reference(args, rank: int, world: int):
+    """The CPU oracle, as it stands, on the host cores (rank 0 only)."""
+    if rank != 0:
+        return 0
+    wl = WORKLOADS[args.workload]
+    import oracle
+
+    oracle.build()
+    cpu_oracle_sample(wl.gemms, target_s=0.5)  # warm-up: page in the inputs and the library
+    vals, secs_total = [], 0.0
+    steps = max(1, min(args.steps, 3))
+    cores, desc = None, ""
+    for _ in range(steps):
+        v, secs, cores, desc = cpu_oracle_sample(wl.gemms, target_s=args.cpu_seconds)
+        vals.append(v)
+        secs_total += secs
+    value = statistics.median(vals)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": steps, "warmup": args.warmup, "ms_per_step": secs_total / steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic", "config": config_of(wl),
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------------- GPU arm
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "block_scaled_precision_bsq_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel_hash: str, workload: str):
+    """DRAM bytes per GEMM launch from the committed ncu summary, if it was taken on the
+    current kernel sources; otherwise None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(workload)
+    if not e or e.get("kernel_source_hash") != kernel_hash:
+        return None
+    return e.get("gemm_dram_bytes_per_launch")
+
+
+def run_gpu(args, rank: int, world: int):
+    import torch
+
+    import __graft_entry__ as ge
+
+    ge.build()
+    import block_scaled_precision_bsq_gb300 as bsq
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    wl = WORKLOADS[args.workload]
+    peaks, peak_src = load_peaks()
+
+    # ------------------------------------------------------------ inputs, resident in HBM
+    def host(x):
+        t = torch.from_numpy(x.view(np.int16) if x.dtype == np.uint16 else x)
+        return (t.view(torch.bfloat16) if x.dtype == np.uint16 else t).pin_memory()
+
+    layers = []
+    for g in wl.gemms:
+        a, b, bias = make_activations(g), make_weights(g), make_bias(g)
+        ha, hb = host(a), host(b)
+        hbias = host(bias) if bias is not None else None
+        L = {"g": g, "ha": ha, "hb": hb, "hbias": hbias,
+             "a": ha.to(dev), "b": hb.to(dev), "bias": hbias.to(dev) if hbias is not None else None,
+             "qa": bsq.empty_qtensor(g.fmt, g.M, g.K, dev), "qb": bsq.empty_qtensor(g.fmt, g.N, g.K, dev),
+             "out": torch.empty((g.M, g.N), dtype=torch.bfloat16, device=dev),
+             "hout": torch.empty((g.M, g.N), dtype=torch.bfloat16).pin_memory()}
+        layers.append(L)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def step(ev=None):
+        # ev: per layer (quantize start, quantize end, gemm start, gemm end) events, or None
+        for i, L in enumerate(layers):
+            e = ev[i] if ev is not None else None
+            if e:
+                e[0].record(stream)
+            bsq.quantize(L["g"].fmt, L["a"], out=L["qa"], stream=stream)
+            bsq.quantize(L["g"].fmt, L["b"], out=L["qb"], stream=stream)
+            if e:
+                e[1].record(stream)
+                e[2].record(stream)
+            bsq.gemm(L["qa"], L["qb"], L["bias"], out=L["out"], stream=stream)
+            if e:
+                e[3].record(stream)
+
+    # our kernels per step: 2 quantize (+1 amax pass each for NVFP4) + 1 GEMM per layer
+    launches_per_step = sum(3 + (2 if L["g"].fmt == NVFP4 else 0) for L in layers)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert bsq.device_status() == 0
+
+    # ------------------------------------------------------------ timed region
+    evs = [[tuple(torch.cuda.Event(enable_timing=True) for _ in range(4)) for _ in layers]
+           for _ in range(args.steps)]
+    if "CUDA_VISIBLE_DEVICES" in os.environ:
+        gpu_index = os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local]
+    else:
+        gpu_index = str(local)
+    out_dir = os.path.join(ROOT, "gpurun_out") if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else \
+        os.path.join(ROOT, "_build")
+    os.makedirs(out_dir, exist_ok=True)
+    sampler = ClockSampler(gpu_index, os.path.join(out_dir, "clocks_rank%d.csv" % rank))
+    time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
+    for s in range(args.steps):
+        flush.zero_()
+        step(evs[s])
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    st = bsq.device_status()
+    assert st == 0, "device status %d" % st
+
+    step_ms = [sum(e[0].elapsed_time(e[3]) for e in evs[s]) for s in range(args.steps)]
+    q_ms = [sum(e[0].elapsed_time(e[1]) for e in evs[s]) for s in range(args.steps)]
+    g_ms = [sum(e[2].elapsed_time(e[3]) for e in evs[s]) for s in range(args.steps)]
+    ms_per_step = float(np.mean(step_ms))
+    if world > 1:
+        t = torch.tensor([ms_per_step], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_per_step = float(t.item())
+    flops = sum(L["g"].flops for L in layers)
+    value = world * flops / (ms_per_step * 1e-3) / 1e12
+
+    # dominant kernel: the GEMM
+    fmt0 = layers[0]["g"].fmt
+    gemm_ms = float(np.mean(g_ms))
+    gemm_tflops = flops / (gemm_ms * 1e-3) / 1e12
+    peak_bf16 = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    peak_tc = peak_bf16 * NOMINAL_RATIO[fmt0]
+    khash = kernel_source_hash()
+    traffic = recorded_traffic(khash, wl.name)
+    q_bytes = sum(quant_bytes(L["g"].fmt, L["g"].M, L["g"].K, 4 if L["g"].src_f32 else 2, True) +
+                  quant_bytes(L["g"].fmt, L["g"].N, L["g"].K, 4 if L["g"].src_f32 else 2, True) for L in layers)
+    q_ms_mean = float(np.mean(q_ms))
+    q_gbs = q_bytes / (q_ms_mean * 1e-3) / 1e9
+    hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    g_bytes = sum(gemm_bytes(L["g"].fmt, L["g"].M, L["g"].N, L["g"].K, L["bias"] is not None) for L in layers)
+    t_ideal = max(flops / (peak_tc * 1e12), g_bytes / (hbm * 1e9))
+
+    # ------------------------------------------------------------ end to end through host buffers
+    e2e_steps = max(3, min(args.steps, args.e2e_steps))
+    h2d = sum(L["ha"].numel() * L["ha"].element_size() + L["hb"].numel() * L["hb"].element_size() +
+              (L["hbias"].numel() * 2 if L["hbias"] is not None else 0) for L in layers)
+    d2h = sum(L["hout"].numel() * 2 for L in layers)
+
+    def e2e_step():
+        for L in layers:
+            L["a"].copy_(L["ha"], non_blocking=True)
+            L["b"].copy_(L["hb"], non_blocking=True)
+            if L["hbias"] is not None:
+                L["bias"].copy_(L["hbias"], non_blocking=True)
+            bsq.quantize(L["g"].fmt, L["a"], out=L["qa"], stream=stream)
+            bsq.quantize(L["g"].fmt, L["b"], out=L["qb"], stream=stream)
+            bsq.gemm(L["qa"], L["qb"], L["bias"], out=L["out"], stream=stream)
+            L["hout"].copy_(L["out"], non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    e2e_value = world * flops / (e2e_ms * 1e-3) / 1e12
+    assert bsq.device_status() == 0
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": FMT_NAME[fmt0], "data": "synthetic", "config": config_of(wl),
+        "gpu_launches": launches_per_step * args.steps,
+        "roofline": {"bound": "tensor", "achieved": gemm_tflops, "peak": peak_tc, "unit": "TFLOP/s",
+                     "frac": gemm_tflops / peak_tc, "traffic": traffic,
+                     "peak_source": "%s bf16 %.1f TFLOP/s x nominal %s ratio %.0f" % (
+                         peak_src, peak_bf16, FMT_NAME[fmt0], NOMINAL_RATIO[fmt0]),
+                     "attainable_frac": t_ideal / (gemm_ms * 1e-3), "kernel": "gemm_kernel",
+                     "gemm_ms": gemm_ms, "algorithmic_bytes": g_bytes},
+        "quantize": {"achieved": q_gbs, "unit": "GB/s", "peak": hbm, "frac": q_gbs / hbm, "ms_per_step": q_ms_mean,
+                     "bytes_per_step": q_bytes, "peak_source": "%s HBM copy" % peak_src},
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_ms, "steps": e2e_steps},
+        "clocks": clocks,
+        "wall_s_timed_region": t_wall,
+        "kernel_source_hash": khash,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, secs, cores, desc = cpu_oracle_sample(wl.gemms, target_s=args.cpu_seconds)
+        line["cpu_baseline"] = {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc,
+                                "seconds": secs}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="vitb_fc1_mxfp8")
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="size of the CPU oracle sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl")
+        try:
+            return run_gpu(args, rank, world)
+        finally:
+            dist.destroy_process_group()
+    return run_gpu(args, rank, world)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

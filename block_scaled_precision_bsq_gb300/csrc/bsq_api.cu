@@ -5,7 +5,7 @@
 #include <cstdint>
 #include <mutex>
 
-#include "../../include/bsq.h"
+#include "bsq.h"
 #include "bsq_device.cuh"
 #include "bsq_internal.h"
 

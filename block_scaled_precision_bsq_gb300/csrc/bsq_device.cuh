@@ -6,7 +6,7 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
-#include "../../include/bsq.h"
+#include "bsq.h"
 
 namespace bsq {
 
