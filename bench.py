@@ -190,6 +190,21 @@ def run_reference(args, rank: int, world: int):
     return 0
 
 
+# ----------------------------------------------------------------------------------- replicas
+def replica_throughput(ms_local: float, flops_per_rank: int, world: int, device=None):
+    """Whole-job throughput of N independent replicas: every rank processed the same work,
+    the job took the slowest rank's time. Returns (max ms over ranks, TFLOP/s of all ranks)."""
+    ms = ms_local
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        t = torch.tensor([ms_local], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return ms, world * flops_per_rank / (ms * 1e-3) / 1e12
+
+
 # ----------------------------------------------------------------------------------- GPU arm
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
@@ -300,13 +315,8 @@ def run_gpu(args, rank: int, world: int):
     step_ms = [sum(e[0].elapsed_time(e[3]) for e in evs[s]) for s in range(args.steps)]
     q_ms = [sum(e[0].elapsed_time(e[1]) for e in evs[s]) for s in range(args.steps)]
     g_ms = [sum(e[2].elapsed_time(e[3]) for e in evs[s]) for s in range(args.steps)]
-    ms_per_step = float(np.mean(step_ms))
-    if world > 1:
-        t = torch.tensor([ms_per_step], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_per_step = float(t.item())
     flops = sum(L["g"].flops for L in layers)
-    value = world * flops / (ms_per_step * 1e-3) / 1e12
+    ms_per_step, value = replica_throughput(float(np.mean(step_ms)), flops, world, dev)
 
     # dominant kernel: the GEMM
     fmt0 = layers[0]["g"].fmt
