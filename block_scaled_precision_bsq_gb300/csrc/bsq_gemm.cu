@@ -39,7 +39,6 @@ constexpr int BM = 128;
 constexpr int BN = 256;
 constexpr int kRowBytes = 128;  // K bytes per stage and row: one 128-byte swizzle span
 constexpr int kNumEpiWarps = 8;
-constexpr int kThreads = (2 + kNumEpiWarps) * 32;
 constexpr int kAccCols = BN;     // fp32 accumulator columns in TMEM
 constexpr uint32_t kTmemCols = 512;
 constexpr int kABytes = BM * kRowBytes;  // 16 KB
@@ -50,16 +49,27 @@ template <int FMT>
 struct Cfg;
 template <>
 struct Cfg<BSQ_MXFP8> {  // 128 K per stage = 4 MMAs of K 32; 4 UE8M0 scales per row per stage
-  static constexpr int kStages = 4, kKElems = 128, kAtoms = 1, kSfCols = 16;
+  static constexpr int kStages = 4, kKElems = 128, kAtoms = 1, kSfCols = 16, kSfWarps = 1;
 };
 template <>
 struct Cfg<BSQ_NVFP4> {  // 256 K per stage = 4 MMAs of K 64; 16 E4M3 scales per row per stage
-  static constexpr int kStages = 3, kKElems = 256, kAtoms = 4, kSfCols = 64;
+  static constexpr int kStages = 3, kKElems = 256, kAtoms = 4, kSfCols = 64, kSfWarps = 2;
 };
 template <>
 struct Cfg<BSQ_MXFP4> {  // 256 K per stage = 4 MMAs of K 64; 8 UE8M0 scales per row per stage
-  static constexpr int kStages = 4, kKElems = 256, kAtoms = 2, kSfCols = 32;
+  static constexpr int kStages = 4, kKElems = 256, kAtoms = 2, kSfCols = 32, kSfWarps = 1;
 };
+
+// Warp roles: 0 TMA producer, 1 MMA issuer, 2 .. 1 + kSfWarps scale-factor copiers, then
+// kNumEpiWarps epilogue warps.
+template <int FMT>
+__host__ __device__ constexpr int first_epi_warp() {
+  return 2 + Cfg<FMT>::kSfWarps;
+}
+template <int FMT>
+__host__ __device__ constexpr int threads_of() {
+  return (first_epi_warp<FMT>() + kNumEpiWarps) * 32;
+}
 
 template <int FMT>
 struct Smem {
@@ -73,7 +83,7 @@ struct Smem {
   static constexpr int epi_off = ((sfb_off + S * kSfbBytes) + 1023) / 1024 * 1024;
   static constexpr int bias_off = epi_off + kNumEpiWarps * kEpiChunkBytes;
   static constexpr int bar_off = bias_off + kNumEpiWarps * 128 * 4;
-  static constexpr int kNumBars = 2 * S + 3;
+  static constexpr int kNumBars = 3 * S + 4;
   static constexpr int misc_off = bar_off + kNumBars * 8;
   static constexpr int total = misc_off + 16;
   static constexpr int alloc = total + 1024;  // slack for aligning the base to 1024
@@ -111,7 +121,7 @@ struct GemmArgs {
 };
 
 template <int FMT>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(threads_of<FMT>(), 1)
     gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
                 const __grid_constant__ CUtensorMap mapOut, const GemmArgs args) {
   using C = Cfg<FMT>;
@@ -122,9 +132,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::bar_off);
   uint64_t* full_bar = bars;
   uint64_t* empty_bar = bars + S;
-  uint64_t* tmem_full = bars + 2 * S;
-  uint64_t* tmem_empty = bars + 2 * S + 1;
-  uint64_t* drain_bar = bars + 2 * S + 2;
+  uint64_t* sf_ready = bars + 2 * S;
+  uint64_t* tmem_full = bars + 3 * S;
+  uint64_t* tmem_empty = bars + 3 * S + 1;
+  uint64_t* drain_bar = bars + 3 * S + 2;     // MMA issuer's outstanding work
+  uint64_t* sf_drain_bar = bars + 3 * S + 3;  // scale-factor copiers' outstanding work
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L::misc_off);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::misc_off + 4);
 
@@ -135,10 +147,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < S; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
+      mbar_init(&sf_ready[s], C::kSfWarps);
     }
     mbar_init(tmem_full, 1);
     mbar_init(tmem_empty, kNumEpiWarps);
     mbar_init(drain_bar, 1);
+    mbar_init(sf_drain_bar, C::kSfWarps);
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&mapA);
@@ -187,39 +201,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1 && lane == 0) {
     // ------------------------------------------------------------------ MMA issuer
+    // Every tcgen05 instruction and every mbarrier wait costs the issuing thread a few dozen
+    // cycles; one MMA of 128 x 256 takes 128 tensor cycles. The issuer therefore does only the
+    // waits, the four MMAs and the commit of each stage (the scale-factor copies run on their
+    // own warps), with descriptors precomputed so that each MMA is a couple of adds.
     int stage = 0;
     uint32_t phase = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
+    const uint64_t adesc0 = smem_desc(smem_u32(smem + L::a_off), 16, 1024, kSwizzle128B);
+    const uint64_t bdesc0 = smem_desc(smem_u32(smem + L::b_off), 16, 1024, kSwizzle128B);
     for (int tile = blockIdx.x; tile < args.num_tiles && ok; tile += gridDim.x) {
       // wait until the epilogue has drained the accumulator of the previous tile
       if (!mbar_wait_bounded(tmem_empty, acc_phase ^ 1u, abort_flag, args.status)) break;
       acc_phase ^= 1u;
       tc_fence_after();
       for (int kb = 0; kb < args.nk; ++kb) {
-        if (!mbar_wait_bounded(&full_bar[stage], phase, abort_flag, args.status)) {
+        // operands landed (full) and this stage's scale factors are in TMEM (sf_ready)
+        if (!mbar_wait_bounded(&full_bar[stage], phase, abort_flag, args.status) ||
+            !mbar_wait_bounded(&sf_ready[stage], phase, abort_flag, args.status)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t sfa_t = tmem_base + kAccCols + stage * C::kSfCols;
         const uint32_t sfb_t = sfa_t + 4 * C::kAtoms;
-        const uint32_t sfa_s = smem_u32(smem + L::sfa_off + stage * L::kSfaBytes);
-        const uint32_t sfb_s = smem_u32(smem + L::sfb_off + stage * L::kSfbBytes);
-#pragma unroll
-        for (int at = 0; at < C::kAtoms; ++at) {
-          tc_cp_32x128b_warpx4(sfa_t + 4 * at, smem_desc(sfa_s + 512 * at, 128, 128, kSwizzleNone));
-#pragma unroll
-          for (int h = 0; h < 2; ++h)
-            tc_cp_32x128b_warpx4(sfb_t + 8 * at + 4 * h,
-                                 smem_desc(sfb_s + h * L::kSfaBytes + 512 * at, 128, 128, kSwizzleNone));
-        }
-        const uint32_t a_s = smem_u32(smem + L::a_off + stage * kABytes);
-        const uint32_t b_s = smem_u32(smem + L::b_off + stage * kBBytes);
+        // start-address field of the descriptors is in 16-byte units (stays below 2^14)
+        const uint64_t adesc = adesc0 + static_cast<uint64_t>((stage * kABytes) >> 4);
+        const uint64_t bdesc = bdesc0 + static_cast<uint64_t>((stage * kBBytes) >> 4);
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          const uint64_t adesc = smem_desc(a_s + 32 * k, 16, 1024, kSwizzle128B);
-          const uint64_t bdesc = smem_desc(b_s + 32 * k, 16, 1024, kSwizzle128B);
           uint32_t sfa = sfa_t, sfb = sfb_t, id = 0;
           if constexpr (FMT == BSQ_MXFP8) {
             id = k;  // byte k of each 32-bit scale cell: K block k of this stage
@@ -231,7 +242,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             sfb += 8 * (k >> 1);
             id = 2 * (k & 1);
           }
-          tc_mma_block_scaled<FMT>(tmem_base, adesc, bdesc, make_idesc<FMT>(id), sfa, sfb, (kb | k) != 0 ? 1u : 0u);
+          tc_mma_block_scaled<FMT>(tmem_base, adesc + 2 * k, bdesc + 2 * k, make_idesc<FMT>(id), sfa, sfb,
+                                   (kb | k) != 0 ? 1u : 0u);
         }
         tc_commit(&empty_bar[stage]);  // the stage is free once these MMAs have read it
         if (++stage == S) {
@@ -244,12 +256,59 @@ __global__ void __launch_bounds__(kThreads, 1)
     // every tensor-core operation of this thread must finish before TMEM is released
     tc_commit(drain_bar);
     mbar_wait_bounded(drain_bar, 0, nullptr, args.status);
-  } else if (warp >= 2) {
+  } else if (warp >= 2 && warp < first_epi_warp<FMT>()) {
+    // ------------------------------------------------------------------ scale-factor copiers
+    // Each of the kSfWarps warps copies its share of the stage's 512-byte scale atoms from
+    // shared memory into the stage's TMEM slot, then commits onto sf_ready[stage] (count
+    // kSfWarps): the commit arrives once the copies are done.
+    if (lane == 0) {
+      constexpr int kCps = 3 * C::kAtoms;  // A atoms, then B atoms (two 128-row halves each)
+      constexpr int kPer = kCps / C::kSfWarps;
+      static_assert(kCps % C::kSfWarps == 0, "scale copies split evenly");
+      const int first = (warp - 2) * kPer;
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < args.num_tiles && ok; tile += gridDim.x) {
+        for (int kb = 0; kb < args.nk; ++kb) {
+          if (!mbar_wait_bounded(&full_bar[stage], phase, abort_flag, args.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sfa_t = tmem_base + kAccCols + stage * C::kSfCols;
+          const uint32_t sfb_t = sfa_t + 4 * C::kAtoms;
+          const uint32_t sfa_s = smem_u32(smem + L::sfa_off + stage * L::kSfaBytes);
+          const uint32_t sfb_s = smem_u32(smem + L::sfb_off + stage * L::kSfbBytes);
+#pragma unroll
+          for (int c = 0; c < kPer; ++c) {
+            const int i = first + c;
+            if (i < C::kAtoms) {
+              tc_cp_32x128b_warpx4(sfa_t + 4 * i, smem_desc(sfa_s + 512 * i, 128, 128, kSwizzleNone));
+            } else {
+              const int j = i - C::kAtoms, at = j >> 1, h = j & 1;
+              tc_cp_32x128b_warpx4(sfb_t + 8 * at + 4 * h,
+                                   smem_desc(sfb_s + h * L::kSfaBytes + 512 * at, 128, 128, kSwizzleNone));
+            }
+          }
+          tc_commit(&sf_ready[stage]);
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // the copies must be finished before TMEM is released
+      tc_commit(sf_drain_bar);
+      mbar_wait_bounded(sf_drain_bar, 0, nullptr, args.status);
+    }
+  } else if (warp >= first_epi_warp<FMT>()) {
     // ------------------------------------------------------------------ epilogue
-    const uint32_t quad = warp & 3u;
-    const uint32_t half = (warp - 2) >> 2;
-    uint8_t* stage_buf = smem + L::epi_off + (warp - 2) * kEpiChunkBytes;
-    float* bias_s = reinterpret_cast<float*>(smem + L::bias_off) + (warp - 2) * 128;
+    const uint32_t e = warp - first_epi_warp<FMT>();  // 0..7
+    const uint32_t quad = warp & 3u;                  // TMEM lane quadrant this warp may access
+    const uint32_t half = e >> 2;
+    uint8_t* stage_buf = smem + L::epi_off + e * kEpiChunkBytes;
+    float* bias_s = reinterpret_cast<float*>(smem + L::bias_off) + e * 128;
     float alpha = 1.0f;
     if constexpr (FMT == BSQ_NVFP4) alpha = __fmul_rn(*args.ga, *args.gb);
     uint32_t acc_phase = 0;
@@ -392,7 +451,7 @@ int run_gemm(const void* A, const void* A_scales, const void* B, const void* B_s
   a.sfb_row_tiles = static_cast<int>(ceil_div(N, 128));
   a.status = dev.status;
   const int grid = std::min(a.num_tiles, dev.num_sms);
-  gemm_kernel<FMT><<<grid, kThreads, Smem<FMT>::alloc, stream>>>(mA, mB, mOut, a);
+  gemm_kernel<FMT><<<grid, threads_of<FMT>(), Smem<FMT>::alloc, stream>>>(mA, mB, mOut, a);
   return cudaGetLastError() == cudaSuccess ? BSQ_OK : BSQ_ERR_LAUNCH;
 }
 
