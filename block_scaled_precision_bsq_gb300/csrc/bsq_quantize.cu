@@ -28,6 +28,12 @@ namespace bsq {
 namespace {
 
 constexpr int kThreads = 256;
+// Resident CTAs per SM (and so the register budget: 65536 / (256 * n)). fp32 sources and
+// NVFP4 hold more live values per lane.
+template <int FMT, bool F32>
+__host__ __device__ constexpr int ctas_per_sm() {
+  return F32 ? 2 : (FMT == BSQ_NVFP4 ? 3 : 4);
+}
 constexpr int kUnroll = 4;
 constexpr int kSeg = 256;  // elements per warp step
 
@@ -98,7 +104,7 @@ __device__ __forceinline__ int64_t scale_word_offset(int64_t r, int64_t c4, int6
 }
 
 template <int FMT, bool F32, int NV>
-__global__ void __launch_bounds__(kThreads) quantize_kernel(QuantArgs a) {
+__global__ void __launch_bounds__(kThreads, (ctas_per_sm<FMT, F32>())) quantize_kernel(QuantArgs a) {
   constexpr bool kFp4 = (FMT != BSQ_MXFP8);
   constexpr int kLanesPerBlock = (FMT == BSQ_NVFP4) ? 2 : 4;
   constexpr uint32_t kEmax = (FMT == BSQ_MXFP8) ? 8u : 2u;
@@ -123,36 +129,49 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(QuantArgs a) {
   }
   uint32_t run_max = 0;  // NVFP4 given-scale mode: running magnitude max for the tail
 
-  for (int64_t base = warp * kUnroll; base < a.total_segs; base += nwarps * kUnroll) {
-    Loaded<F32> L[kUnroll];
-    int64_t row[kUnroll], k0[kUnroll];
-    bool live[kUnroll];
+  // Work unit: one batch = up to kUnroll consecutive 256-element segments of one row. Warps
+  // walk the batches with a grid stride and prefetch the next batch's loads before working
+  // on the current one, so every warp keeps two batches of 16-byte loads in flight.
+  const uint32_t bpr = static_cast<uint32_t>((a.segs_per_row + kUnroll - 1) / kUnroll);
+  const uint32_t total = static_cast<uint32_t>(a.rows) * bpr;
+  auto load_batch = [&](uint32_t b, Loaded<F32> (&dst)[kUnroll]) {
+    const uint32_t row = b / bpr;
+    const int64_t seg0 = static_cast<int64_t>(b - row * bpr) * kUnroll;
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
-      const int64_t seg = base + u;
-      row[u] = seg / a.segs_per_row;
-      k0[u] = (seg - row[u] * a.segs_per_row) * kSeg + lane * 8;
-      live[u] = (seg < a.total_segs) && (k0[u] < a.cols);
-      if (live[u]) {
-        const int64_t e = row[u] * a.cols + k0[u];
+      const int64_t k0 = (seg0 + u) * kSeg + lane * 8;
+      if (k0 < a.cols) {
+        const int64_t e = static_cast<int64_t>(row) * a.cols + k0;
         if constexpr (F32) {
           const uint4* p = reinterpret_cast<const uint4*>(static_cast<const float*>(a.src) + e);
-          L[u].v[0] = __ldcs(p);
-          L[u].v[1] = __ldcs(p + 1);
+          dst[u].v[0] = __ldcs(p);
+          dst[u].v[1] = __ldcs(p + 1);
         } else {
-          L[u].v[0] = __ldcs(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.src) + e));
+          dst[u].v[0] = __ldcs(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.src) + e));
         }
       } else {
 #pragma unroll
-        for (int i = 0; i < (F32 ? 2 : 1); ++i) L[u].v[i] = make_uint4(0, 0, 0, 0);
+        for (int i = 0; i < (F32 ? 2 : 1); ++i) dst[u].v[i] = make_uint4(0, 0, 0, 0);
       }
     }
+  };
+  Loaded<F32> cur[kUnroll], nxt[kUnroll];
+  uint32_t b = static_cast<uint32_t>(warp);
+  if (b < total) load_batch(b, cur);
+  for (; b < total; b += static_cast<uint32_t>(nwarps)) {
+    const uint32_t bn = b + static_cast<uint32_t>(nwarps);
+    if (bn < total) load_batch(bn, nxt);
+    const uint32_t row = b / bpr;
+    const int64_t seg0 = static_cast<int64_t>(b - row * bpr) * kUnroll;
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
-      if (base + u >= a.total_segs) break;  // warp-uniform
+      if (seg0 + u >= a.segs_per_row) break;  // warp-uniform
+      const int64_t brow = row;
+      const int64_t bk0 = (seg0 + u) * kSeg + lane * 8;
+      const bool blive = bk0 < a.cols;
       float x[8];
       uint32_t mag;
-      unpack8<F32>(L[u], x, mag);
+      unpack8<F32>(cur[u], x, mag);
       // block maximum across the lanes of one block
       mag = max(mag, __shfl_xor_sync(0xFFFFFFFFu, mag, 1));
       if (kLanesPerBlock == 4) mag = max(mag, __shfl_xor_sync(0xFFFFFFFFu, mag, 2));
@@ -189,8 +208,8 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(QuantArgs a) {
         }
       }
 
-      if (live[u]) {
-        const int64_t e = row[u] * a.cols + k0[u];
+      if (blive) {
+        const int64_t e = brow * a.cols + bk0;
         if constexpr (kFp4) {
           *reinterpret_cast<uint32_t*>(a.codes + (e >> 1)) = code_lo;
         } else {
@@ -204,14 +223,16 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(QuantArgs a) {
       const uint32_t s2 = __shfl_down_sync(0xFFFFFFFFu, sbyte, 2 * kLanesPerBlock);
       const uint32_t s3 = __shfl_down_sync(0xFFFFFFFFu, sbyte, 3 * kLanesPerBlock);
       if ((lane % (4 * kLanesPerBlock)) == 0) {
-        const int64_t seg_k0 = k0[u] - lane * 8;
+        const int64_t seg_k0 = bk0 - lane * 8;
         const int64_t c4 = seg_k0 / (FMT == BSQ_NVFP4 ? 16 : 32) + lane / kLanesPerBlock;
         if (c4 < a.nsc) {
           const uint32_t word = sbyte | (s1 << 8) | (s2 << 16) | (s3 << 24);
-          *reinterpret_cast<uint32_t*>(a.scales + scale_word_offset(row[u], c4, a.nct)) = word;
+          *reinterpret_cast<uint32_t*>(a.scales + scale_word_offset(brow, c4, a.nct)) = word;
         }
       }
     }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) cur[u] = nxt[u];
   }
 
   if constexpr (NV == kNvGiven) {
@@ -302,9 +323,13 @@ int launch_quantize(int fmt, bool src_f32, bool global_given, const void* src, i
   }
   if (err != cudaSuccess) return BSQ_ERR_LAUNCH;
 
-  const int64_t warps = ceil_div(a.total_segs, kUnroll);
-  const int64_t max_grid = static_cast<int64_t>(dev.num_sms) * 8;
-  const int grid = static_cast<int>(std::min<int64_t>(ceil_div(warps, kThreads / 32), max_grid));
+  // Persistent grid: as many CTAs as stay resident (a second wave would serialise a kernel
+  // that lasts only a few microseconds), never more than there are batches of work.
+  const int64_t batches = rows * ceil_div(a.segs_per_row, kUnroll);
+  const int per_sm = fmt == BSQ_NVFP4 ? (src_f32 ? ctas_per_sm<BSQ_NVFP4, true>() : ctas_per_sm<BSQ_NVFP4, false>())
+                                      : (src_f32 ? ctas_per_sm<BSQ_MXFP8, true>() : ctas_per_sm<BSQ_MXFP8, false>());
+  const int64_t max_grid = static_cast<int64_t>(dev.num_sms) * per_sm;
+  const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(ceil_div(batches, kThreads / 32), max_grid)));
 
   if (fmt == BSQ_NVFP4) {
     a.tail = reinterpret_cast<uint32_t*>(a.scales + body);
