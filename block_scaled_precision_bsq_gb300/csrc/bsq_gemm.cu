@@ -5,22 +5,31 @@
 // ones of the "lightly-train - DINOv3 + EoMT on RTX 5090" README, section 2; the README's
 // kernels are sm_120 mma.sync designs, this one is written for tcgen05 + TMEM + TMA.
 //
-// Design (one CTA per SM, persistent over 128 x 256 output tiles):
-//   warp 0      TMA producer: A tile 128 rows x 128 bytes, B tile 256 rows x 128 bytes
-//               (128-byte swizzle, K-major), plus the tile's scale-factor atoms (512-byte
-//               blocks already in the tcgen05 layout) by bulk copy, into a kStages ring.
-//   warp 1      TMEM owner and MMA issuer: per stage it copies the scale atoms smem -> TMEM
-//               (tcgen05.cp 32x128b.warpx4, one TMEM slot per ring stage) and issues four
-//               block-scaled MMAs of M=128, N=256 into one fp32 accumulator (256 columns);
-//               tcgen05.commit frees the stage and, after the last K step, signals the tile.
-//   warps 2..9  epilogue: warp w reads TMEM lanes 32*(w%4).. (its quadrant), columns
-//               128*((w-2)/4).. (its half); it drains its 32 x 128 accumulator block to
-//               registers, releases the accumulator to the MMA warp at once, then applies
-//               alpha and bias, rounds to bf16 and writes 32 x 32 chunks through a
-//               64-byte-swizzled staging buffer with TMA stores.
+// Why 2-SM tiles. A stage of a 128 x 256 single-CTA tile brings 48 KB into one SM's shared
+// memory for 512 tensor cycles of work, and TMA fills one SM's shared memory at ~84 bytes per
+// cycle (measured on GB300), so a single CTA cannot feed its tensor core. The 2-SM MMA
+// (.cta_group::2) computes a 256 x 256 tile on a pair of SMs with each SM holding only its 128
+// rows of A and its 128-row half of B: 32 KB per stage per SM for the same 512 cycles.
+//
+// Design (a (2,1,1) cluster per SM pair, persistent over 256 x 256 tiles; rank 0 = leader):
+//   warp 0      (both CTAs) TMA producer: own A rows, own half of the B rows (K chunks of
+//               128 bytes, 128-byte swizzle, K-major), own A scale atoms and all B scale atoms
+//               of the tile, into a kStages ring. Every copy is a 3-D tensor copy in its
+//               .cta_group::2 form, completing on the LEADER's full[] barrier, which expects
+//               the bytes of both CTAs: the leader learns that the whole stage landed without
+//               any relay between the CTAs.
+//   warp 1      leader: TMEM owner and MMA issuer (tcgen05.mma.cta_group::2, M=256 N=256), one
+//               commit per stage multicast to both CTAs' empty[] barriers, one per tile to
+//               both CTAs' tmem_full.
+//   warps 2..   leader (formats with many scale atoms): scale-factor copiers
+//               (tcgen05.cp.cta_group::2: each CTA's TMEM gets its own shared-memory atoms),
+//               committing onto sf_ready[].
+//   last 8      (both CTAs) epilogue: drain the CTA's 128 x 256 fp32 accumulator, alpha + bias,
+//               bf16, 64B-swizzled staging, TMA store; tell the leader (tmem_empty, 16
+//               arrivals) as soon as the accumulator has been read.
 // Every mbarrier wait is bounded (%globaltimer); on a timeout the kernel records
-// BSQ_ERR_TIMEOUT in the device status word, all roles leave their loops, the MMA warp
-// waits for its own outstanding tensor-core work and TMEM is released before exit.
+// BSQ_ERR_TIMEOUT in the device status word, the roles leave their loops, outstanding
+// tensor-core work is waited for and TMEM is released after a final cluster barrier.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -35,33 +44,43 @@
 namespace bsq {
 namespace {
 
-constexpr int BM = 128;
-constexpr int BN = 256;
-constexpr int kRowBytes = 128;  // K bytes per stage and row: one 128-byte swizzle span
+constexpr int BM = 128;         // rows of A per CTA (256 per pair)
+constexpr int BN = 256;         // columns of the output tile (both CTAs)
+constexpr int BNH = BN / 2;       // rows of B held per CTA
+constexpr int kChunkBytes = 128;  // one 128-byte swizzle span of K per row
 constexpr int kNumEpiWarps = 8;
-constexpr int kAccCols = BN;     // fp32 accumulator columns in TMEM
+constexpr int kAccCols = BN;  // fp32 accumulator columns in TMEM
 constexpr uint32_t kTmemCols = 512;
-constexpr int kABytes = BM * kRowBytes;  // 16 KB
-constexpr int kBBytes = BN * kRowBytes;  // 32 KB
-constexpr int kEpiChunkBytes = 32 * 32 * 2;
 
+// Per format: kChunks 128-byte K chunks per stage (loaded as one 3-D TMA box per operand:
+// measured TMA cost falls with fewer, larger operations), kKElems K elements per stage,
+// kAtoms 512-byte scale atoms per 128 rows per stage, kSfCols TMEM columns of one stage's
+// scale slot (4 per A atom, 8 per B atom), kEpiCols output columns per epilogue store chunk.
 template <int FMT>
 struct Cfg;
 template <>
-struct Cfg<BSQ_MXFP8> {  // 128 K per stage = 4 MMAs of K 32; 4 UE8M0 scales per row per stage
-  static constexpr int kStages = 4, kKElems = 128, kAtoms = 1, kSfCols = 16, kSfWarps = 1;
+struct Cfg<BSQ_MXFP8> {  // 256 K per stage = 8 MMAs of K 32; 8 UE8M0 scales per row per stage
+  static constexpr int kChunks = 2, kStages = 3, kKElems = 256, kAtoms = 2, kSfWarps = 0, kEpiCols = 32;
 };
 template <>
 struct Cfg<BSQ_NVFP4> {  // 256 K per stage = 4 MMAs of K 64; 16 E4M3 scales per row per stage
-  static constexpr int kStages = 3, kKElems = 256, kAtoms = 4, kSfCols = 64, kSfWarps = 2;
+  static constexpr int kChunks = 1, kStages = 5, kKElems = 256, kAtoms = 4, kSfWarps = 2, kEpiCols = 32;
 };
 template <>
-struct Cfg<BSQ_MXFP4> {  // 256 K per stage = 4 MMAs of K 64; 8 UE8M0 scales per row per stage
-  static constexpr int kStages = 4, kKElems = 256, kAtoms = 2, kSfCols = 32, kSfWarps = 1;
+struct Cfg<BSQ_MXFP4> {  // 512 K per stage = 8 MMAs of K 64; 16 UE8M0 scales per row per stage
+  static constexpr int kChunks = 2, kStages = 3, kKElems = 512, kAtoms = 4, kSfWarps = 1, kEpiCols = 16;
 };
+template <int FMT>
+__host__ __device__ constexpr int sf_cols() {
+  return 12 * Cfg<FMT>::kAtoms;
+}
 
-// Warp roles: 0 TMA producer, 1 MMA issuer, 2 .. 1 + kSfWarps scale-factor copiers, then
-// kNumEpiWarps epilogue warps.
+// Warp roles: 0 TMA producer, 1 MMA issuer (leader), 2 .. 1 + kSfWarps
+// scale-factor copiers (leader), then kNumEpiWarps epilogue warps. With kSfWarps = 0 the MMA
+// issuer copies the scale factors itself, right before the stage's MMAs: in one thread the
+// tensor pipe keeps them in order, with no extra barrier hop (a copier warp's copies queue
+// behind the MMAs already issued and delay the next stage). Formats whose copies would not
+// fit in the issuer's time budget (12 copies per stage) use copier warps.
 template <int FMT>
 __host__ __device__ constexpr int first_epi_warp() {
   return 2 + Cfg<FMT>::kSfWarps;
@@ -74,8 +93,11 @@ __host__ __device__ constexpr int threads_of() {
 template <int FMT>
 struct Smem {
   static constexpr int S = Cfg<FMT>::kStages;
-  static constexpr int kSfaBytes = Cfg<FMT>::kAtoms * 512;
-  static constexpr int kSfbBytes = 2 * Cfg<FMT>::kAtoms * 512;
+  static constexpr int kABytes = Cfg<FMT>::kChunks * BM * kChunkBytes;   // own 128 rows of A
+  static constexpr int kBBytes = Cfg<FMT>::kChunks * BNH * kChunkBytes;  // own 128-row half of B
+  static constexpr int kSfaBytes = Cfg<FMT>::kAtoms * 512;      // this CTA's 128 A rows
+  static constexpr int kSfbBytes = 2 * Cfg<FMT>::kAtoms * 512;  // all 256 B rows of the tile
+  static constexpr int kEpiChunkBytes = 32 * Cfg<FMT>::kEpiCols * 2;
   static constexpr int a_off = 0;
   static constexpr int b_off = a_off + S * kABytes;
   static constexpr int sfa_off = b_off + S * kBBytes;
@@ -91,38 +113,36 @@ struct Smem {
 static_assert(Smem<BSQ_MXFP8>::alloc <= 232448, "MXFP8 shared memory budget");
 static_assert(Smem<BSQ_NVFP4>::alloc <= 232448, "NVFP4 shared memory budget");
 static_assert(Smem<BSQ_MXFP4>::alloc <= 232448, "MXFP4 shared memory budget");
-static_assert(kAccCols + Cfg<BSQ_MXFP8>::kStages * Cfg<BSQ_MXFP8>::kSfCols <= 512, "TMEM budget");
-static_assert(kAccCols + Cfg<BSQ_NVFP4>::kStages * Cfg<BSQ_NVFP4>::kSfCols <= 512, "TMEM budget");
-static_assert(kAccCols + Cfg<BSQ_MXFP4>::kStages * Cfg<BSQ_MXFP4>::kSfCols <= 512, "TMEM budget");
+static_assert(kAccCols + Cfg<BSQ_MXFP8>::kStages * sf_cols<BSQ_MXFP8>() <= 512, "TMEM budget");
+static_assert(kAccCols + Cfg<BSQ_NVFP4>::kStages * sf_cols<BSQ_NVFP4>() <= 512, "TMEM budget");
+static_assert(kAccCols + Cfg<BSQ_MXFP4>::kStages * sf_cols<BSQ_MXFP4>() <= 512, "TMEM budget");
 
 // Instruction descriptor of a block-scaled MMA (kinds mxf8f6f4 / mxf4 / mxf4nvf4):
 // bits 4-5 scale-factor B id, 7-9 A type, 10-12 B type, 15/16 A/B major (0 = K-major),
 // 17-22 N >> 3, 23 scale type (1 = UE8M0, 0 = UE4M3), 27-28 M >> 7, 29-30 scale-factor A id.
-// Element types: E4M3 = 0 under mxf8f6f4, E2M1 = 1 under mxf4 / mxf4nvf4.
+// Element types: E4M3 = 0 under mxf8f6f4, E2M1 = 1 under mxf4 / mxf4nvf4. M = 256 (the pair).
 template <int FMT>
 __host__ __device__ constexpr uint32_t make_idesc(uint32_t sf_id) {
   const uint32_t t = (FMT == BSQ_MXFP8) ? 0u : 1u;
   const uint32_t ue8m0 = (FMT == BSQ_NVFP4) ? 0u : 1u;
   return (sf_id << 4) | (t << 7) | (t << 10) | (static_cast<uint32_t>(BN >> 3) << 17) | (ue8m0 << 23) |
-         (static_cast<uint32_t>(BM >> 7) << 27) | (sf_id << 29);
+         (static_cast<uint32_t>((2 * BM) >> 7) << 27) | (sf_id << 29);
 }
 
 struct GemmArgs {
-  const uint8_t* sfa;
-  const uint8_t* sfb;
   const uint16_t* bias;  // nullable
   const float* ga;       // NVFP4: per-tensor scales in the scale tails
   const float* gb;
-  int M, N, K;
-  int tiles_n, num_tiles, nk;
-  int sf_nct;          // 4-column scale tiles per row (K / block / 4)
-  int sfb_row_tiles;   // ceil(N / 128)
+  int M, N;
+  int tiles_n, num_pairs, nk;
+  int kchunks;  // 128-byte K chunks in total (the last stage may hold fewer than kChunks)
   int* status;
 };
 
 template <int FMT>
 __global__ void __launch_bounds__(threads_of<FMT>(), 1)
     gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
+                const __grid_constant__ CUtensorMap mapSfa, const __grid_constant__ CUtensorMap mapSfb,
                 const __grid_constant__ CUtensorMap mapOut, const GemmArgs args) {
   using C = Cfg<FMT>;
   using L = Smem<FMT>;
@@ -130,110 +150,149 @@ __global__ void __launch_bounds__(threads_of<FMT>(), 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::bar_off);
-  uint64_t* full_bar = bars;
-  uint64_t* empty_bar = bars + S;
-  uint64_t* sf_ready = bars + 2 * S;
-  uint64_t* tmem_full = bars + 3 * S;
-  uint64_t* tmem_empty = bars + 3 * S + 1;
-  uint64_t* drain_bar = bars + 3 * S + 2;     // MMA issuer's outstanding work
-  uint64_t* sf_drain_bar = bars + 3 * S + 3;  // scale-factor copiers' outstanding work
+  uint64_t* full_bar = bars;                  // leader: both CTAs' operands of a stage landed
+  uint64_t* empty_bar = bars + S;             // the pair's MMAs are done with a stage
+  uint64_t* sf_ready = bars + 2 * S;          // leader: the stage's scale factors are in both TMEMs
+  uint64_t* tmem_full = bars + 3 * S;         // the accumulator of a tile is complete
+  uint64_t* tmem_empty = bars + 3 * S + 1;    // leader: both CTAs drained their accumulator
+  uint64_t* drain_bar = bars + 3 * S + 2;     // leader: MMA issuer's outstanding work
+  uint64_t* sf_drain_bar = bars + 3 * S + 3;  // leader: scale-factor copiers' outstanding work
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L::misc_off);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::misc_off + 4);
 
   const uint32_t warp = threadIdx.x >> 5;
   const uint32_t lane = threadIdx.x & 31u;
+  const uint32_t rank = cluster_rank();
+  const bool leader = (rank == 0);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
-      mbar_init(&sf_ready[s], C::kSfWarps);
+      mbar_init(&sf_ready[s], C::kSfWarps > 0 ? C::kSfWarps : 1);
     }
     mbar_init(tmem_full, 1);
-    mbar_init(tmem_empty, kNumEpiWarps);
+    mbar_init(tmem_empty, 2 * kNumEpiWarps);
     mbar_init(drain_bar, 1);
-    mbar_init(sf_drain_bar, C::kSfWarps);
+    mbar_init(sf_drain_bar, C::kSfWarps > 0 ? C::kSfWarps : 1);
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&mapA);
     prefetch_tmap(&mapB);
+    prefetch_tmap(&mapSfa);
+    prefetch_tmap(&mapSfb);
     prefetch_tmap(&mapOut);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_holder, kTmemCols);
-    tmem_relinquish();
+    tmem_alloc_pair(tmem_holder, kTmemCols);  // one warp in each CTA, collectively
+    tmem_relinquish_pair();
   }
   tc_fence_before();
   __syncthreads();
+  cluster_sync_all();  // barriers of both CTAs initialised before any remote arrival
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
+  // Copy scale atoms [first, first + count) of a stage (A atoms first, then the B atoms of the
+  // two 128-row halves) from each CTA's shared memory into the stage's TMEM slot of each CTA.
+  auto copy_stage_scales = [&](int stage, int kb, int first, int count) {
+    (void)kb;
+    const uint32_t sfa_t = tmem_base + kAccCols + stage * sf_cols<FMT>();
+    const uint32_t sfb_t = sfa_t + 4 * C::kAtoms;
+    const uint32_t sfa_s = smem_u32(smem + L::sfa_off + stage * L::kSfaBytes);
+    const uint32_t sfb_s = smem_u32(smem + L::sfb_off + stage * L::kSfbBytes);
+#pragma unroll
+    for (int c = 0; c < count; ++c) {
+      const int i = first + c;
+      if (i < C::kAtoms) {
+        tc_cp_pair_32x128b_warpx4(sfa_t + 4 * i, smem_desc(sfa_s + 512 * i, 128, 128, kSwizzleNone));
+      } else {
+        const int j = i - C::kAtoms, at = j >> 1, h = j & 1;
+        tc_cp_pair_32x128b_warpx4(sfb_t + 8 * at + 4 * h, smem_desc(sfb_s + h * L::kSfaBytes + 512 * at, 128, 128, kSwizzleNone));
+      }
+    }
+  };
+  const int first_pair = static_cast<int>(cluster_id_x());
+  const int pair_stride = static_cast<int>(num_clusters_x());
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------------ TMA producer
+    // Boxes reaching past M, N or K are zero-filled by TMA and still deliver their full byte
+    // count, so every stage of every CTA brings exactly kStageBytes.
+    constexpr uint32_t kStageBytes = L::kABytes + L::kBBytes + L::kSfaBytes + L::kSfbBytes;
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < args.num_tiles && ok; tile += gridDim.x) {
-      const int m_blk = tile / args.tiles_n, n_blk = tile % args.tiles_n;
+    for (int pt = first_pair; pt < args.num_pairs && ok; pt += pair_stride) {
+      const int m_blk = 2 * (pt / args.tiles_n) + static_cast<int>(rank);
+      const int n_blk = pt % args.tiles_n;
       for (int kb = 0; kb < args.nk; ++kb) {
         if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1u, abort_flag, args.status)) {
           ok = false;
           break;
         }
-        const bool hi_ok = (2 * n_blk + 1) < args.sfb_row_tiles;
-        const uint32_t bytes = kABytes + kBBytes + L::kSfaBytes + (hi_ok ? 2 : 1) * (L::kSfaBytes);
-        mbar_arrive_expect_tx(&full_bar[stage], bytes);
-        tma_load_2d(smem + L::a_off + stage * kABytes, &mapA, &full_bar[stage], kb * kRowBytes, m_blk * BM);
-        tma_load_2d(smem + L::b_off + stage * kBBytes, &mapB, &full_bar[stage], kb * kRowBytes, n_blk * BN);
-        const int64_t atom_a = static_cast<int64_t>(m_blk) * args.sf_nct + static_cast<int64_t>(kb) * C::kAtoms;
-        bulk_load(smem + L::sfa_off + stage * L::kSfaBytes, args.sfa + atom_a * 512, L::kSfaBytes, &full_bar[stage]);
-        for (int h = 0; h < (hi_ok ? 2 : 1); ++h) {
-          const int64_t atom_b =
-              static_cast<int64_t>(2 * n_blk + h) * args.sf_nct + static_cast<int64_t>(kb) * C::kAtoms;
-          bulk_load(smem + L::sfb_off + stage * L::kSfbBytes + h * L::kSfaBytes, args.sfb + atom_b * 512,
-                    L::kSfaBytes, &full_bar[stage]);
-        }
+        if (leader) mbar_arrive_expect_tx(&full_bar[stage], 2 * kStageBytes);
+        const uint32_t bar = smem_u32(&full_bar[stage]) & ~kClusterRankBit;  // the leader's full[stage]
+        tma_load_3d_to_leader(smem + L::a_off + stage * L::kABytes, &mapA, bar, 0, m_blk * BM, kb * C::kChunks);
+        tma_load_3d_to_leader(smem + L::b_off + stage * L::kBBytes, &mapB, bar, 0,
+                              n_blk * BN + static_cast<int>(rank) * BNH, kb * C::kChunks);
+        tma_load_3d_to_leader(smem + L::sfa_off + stage * L::kSfaBytes, &mapSfa, bar, 0, kb * C::kAtoms, m_blk);
+        tma_load_3d_to_leader(smem + L::sfb_off + stage * L::kSfbBytes, &mapSfb, bar, 0, kb * C::kAtoms, 2 * n_blk);
         if (++stage == S) {
           stage = 0;
           phase ^= 1u;
         }
       }
     }
-  } else if (warp == 1 && lane == 0) {
-    // ------------------------------------------------------------------ MMA issuer
+  } else if (warp == 1 && lane == 0 && leader) {
+    // ------------------------------------------------------------------ MMA issuer (leader)
     // Every tcgen05 instruction and every mbarrier wait costs the issuing thread a few dozen
-    // cycles; one MMA of 128 x 256 takes 128 tensor cycles. The issuer therefore does only the
-    // waits, the four MMAs and the commit of each stage (the scale-factor copies run on their
-    // own warps), with descriptors precomputed so that each MMA is a couple of adds.
+    // cycles; one 2-SM MMA of 256 x 256 takes 128 tensor cycles. The issuer does only the
+    // wait, the four MMAs and the commit of each stage; the scale-factor copiers waited for
+    // both CTAs' operands before signalling sf_ready.
     int stage = 0;
     uint32_t phase = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
     const uint64_t adesc0 = smem_desc(smem_u32(smem + L::a_off), 16, 1024, kSwizzle128B);
     const uint64_t bdesc0 = smem_desc(smem_u32(smem + L::b_off), 16, 1024, kSwizzle128B);
-    for (int tile = blockIdx.x; tile < args.num_tiles && ok; tile += gridDim.x) {
-      // wait until the epilogue has drained the accumulator of the previous tile
+    for (int pt = first_pair; pt < args.num_pairs && ok; pt += pair_stride) {
+      // wait until both CTAs' epilogues have drained the accumulator of the previous tile
       if (!mbar_wait_bounded(tmem_empty, acc_phase ^ 1u, abort_flag, args.status)) break;
       acc_phase ^= 1u;
       tc_fence_after();
       for (int kb = 0; kb < args.nk; ++kb) {
-        // operands landed (full) and this stage's scale factors are in TMEM (sf_ready)
-        if (!mbar_wait_bounded(&full_bar[stage], phase, abort_flag, args.status) ||
-            !mbar_wait_bounded(&sf_ready[stage], phase, abort_flag, args.status)) {
-          ok = false;
-          break;
+        if constexpr (C::kSfWarps == 0) {
+          // both CTAs' operands of the stage landed: copy the scales, then the MMAs
+          if (!mbar_wait_bounded(&full_bar[stage], phase, abort_flag, args.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          copy_stage_scales(stage, kb, 0, 3 * C::kAtoms);
+        } else {
+          if (!mbar_wait_bounded(&sf_ready[stage], phase, abort_flag, args.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
         }
-        tc_fence_after();
-        const uint32_t sfa_t = tmem_base + kAccCols + stage * C::kSfCols;
+        const int nmma = 4 * min(C::kChunks, args.kchunks - kb * C::kChunks);
+        const uint32_t sfa_t = tmem_base + kAccCols + stage * sf_cols<FMT>();
         const uint32_t sfb_t = sfa_t + 4 * C::kAtoms;
         // start-address field of the descriptors is in 16-byte units (stays below 2^14)
-        const uint64_t adesc = adesc0 + static_cast<uint64_t>((stage * kABytes) >> 4);
-        const uint64_t bdesc = bdesc0 + static_cast<uint64_t>((stage * kBBytes) >> 4);
+        const uint64_t adesc = adesc0 + static_cast<uint64_t>((stage * L::kABytes) >> 4);
+        const uint64_t bdesc = bdesc0 + static_cast<uint64_t>((stage * L::kBBytes) >> 4);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
+        for (int k = 0; k < 4 * C::kChunks; ++k) {
+          if (k >= nmma) break;
+          // K chunk k / 4 (its own 16 KB swizzle block), 32 bytes into it per MMA
+          const uint64_t koff = static_cast<uint64_t>((k >> 2) * ((BM * kChunkBytes) >> 4) + 2 * (k & 3));
+          const uint64_t kboff = static_cast<uint64_t>((k >> 2) * ((BNH * kChunkBytes) >> 4) + 2 * (k & 3));
           uint32_t sfa = sfa_t, sfb = sfb_t, id = 0;
           if constexpr (FMT == BSQ_MXFP8) {
-            id = k;  // byte k of each 32-bit scale cell: K block k of this stage
+            sfa += 4 * (k >> 2);  // one scale of 32 K per MMA: byte k % 4 of atom k / 4
+            sfb += 8 * (k >> 2);
+            id = k & 3;
           } else if constexpr (FMT == BSQ_NVFP4) {
             sfa += 4 * k;  // one atom (4 scales of 16 K) per MMA
             sfb += 8 * k;
@@ -242,56 +301,42 @@ __global__ void __launch_bounds__(threads_of<FMT>(), 1)
             sfb += 8 * (k >> 1);
             id = 2 * (k & 1);
           }
-          tc_mma_block_scaled<FMT>(tmem_base, adesc + 2 * k, bdesc + 2 * k, make_idesc<FMT>(id), sfa, sfb,
-                                   (kb | k) != 0 ? 1u : 0u);
+          tc_mma_pair<FMT>(tmem_base, adesc + koff, bdesc + kboff, make_idesc<FMT>(id), sfa, sfb,
+                           (kb | k) != 0 ? 1u : 0u);
         }
-        tc_commit(&empty_bar[stage]);  // the stage is free once these MMAs have read it
+        tc_commit_pair_mc(&empty_bar[stage], 0x3);  // both CTAs' stage is free once these MMAs read it
         if (++stage == S) {
           stage = 0;
           phase ^= 1u;
         }
       }
-      if (ok) tc_commit(tmem_full);  // accumulator complete
+      if (ok) tc_commit_pair_mc(tmem_full, 0x3);  // both CTAs' accumulators complete
     }
     // every tensor-core operation of this thread must finish before TMEM is released
-    tc_commit(drain_bar);
+    tc_commit_pair(drain_bar);
     mbar_wait_bounded(drain_bar, 0, nullptr, args.status);
-  } else if (warp >= 2 && warp < first_epi_warp<FMT>()) {
-    // ------------------------------------------------------------------ scale-factor copiers
-    // Each of the kSfWarps warps copies its share of the stage's 512-byte scale atoms from
-    // shared memory into the stage's TMEM slot, then commits onto sf_ready[stage] (count
-    // kSfWarps): the commit arrives once the copies are done.
+  } else if (warp >= 2 && warp < static_cast<uint32_t>(first_epi_warp<FMT>()) && leader) {
+    // ------------------------------------------------------------------ scale-factor copiers (leader)
+    // Each of the kSfWarps warps copies its share of the stage's 512-byte scale atoms into the
+    // stage's TMEM slot of BOTH CTAs (each from its own shared memory), after both CTAs'
+    // operands of the stage have landed, then commits onto sf_ready[stage].
     if (lane == 0) {
       constexpr int kCps = 3 * C::kAtoms;  // A atoms, then B atoms (two 128-row halves each)
-      constexpr int kPer = kCps / C::kSfWarps;
-      static_assert(kCps % C::kSfWarps == 0, "scale copies split evenly");
-      const int first = (warp - 2) * kPer;
+      constexpr int kPer = kCps / (C::kSfWarps > 0 ? C::kSfWarps : 1);
+      static_assert(C::kSfWarps == 0 || kCps % C::kSfWarps == 0, "scale copies split evenly");
+      const int first = (static_cast<int>(warp) - 2) * kPer;
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < args.num_tiles && ok; tile += gridDim.x) {
+      for (int pt = first_pair; pt < args.num_pairs && ok; pt += pair_stride) {
         for (int kb = 0; kb < args.nk; ++kb) {
           if (!mbar_wait_bounded(&full_bar[stage], phase, abort_flag, args.status)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t sfa_t = tmem_base + kAccCols + stage * C::kSfCols;
-          const uint32_t sfb_t = sfa_t + 4 * C::kAtoms;
-          const uint32_t sfa_s = smem_u32(smem + L::sfa_off + stage * L::kSfaBytes);
-          const uint32_t sfb_s = smem_u32(smem + L::sfb_off + stage * L::kSfbBytes);
-#pragma unroll
-          for (int c = 0; c < kPer; ++c) {
-            const int i = first + c;
-            if (i < C::kAtoms) {
-              tc_cp_32x128b_warpx4(sfa_t + 4 * i, smem_desc(sfa_s + 512 * i, 128, 128, kSwizzleNone));
-            } else {
-              const int j = i - C::kAtoms, at = j >> 1, h = j & 1;
-              tc_cp_32x128b_warpx4(sfb_t + 8 * at + 4 * h,
-                                   smem_desc(sfb_s + h * L::kSfaBytes + 512 * at, 128, 128, kSwizzleNone));
-            }
-          }
-          tc_commit(&sf_ready[stage]);
+          copy_stage_scales(stage, kb, first, kPer);
+          tc_commit_pair(&sf_ready[stage]);
           if (++stage == S) {
             stage = 0;
             phase ^= 1u;
@@ -299,21 +344,23 @@ __global__ void __launch_bounds__(threads_of<FMT>(), 1)
         }
       }
       // the copies must be finished before TMEM is released
-      tc_commit(sf_drain_bar);
+      tc_commit_pair(sf_drain_bar);
       mbar_wait_bounded(sf_drain_bar, 0, nullptr, args.status);
     }
-  } else if (warp >= first_epi_warp<FMT>()) {
-    // ------------------------------------------------------------------ epilogue
+  } else if (warp >= static_cast<uint32_t>(first_epi_warp<FMT>())) {
+    // ------------------------------------------------------------------ epilogue (both CTAs)
     const uint32_t e = warp - first_epi_warp<FMT>();  // 0..7
     const uint32_t quad = warp & 3u;                  // TMEM lane quadrant this warp may access
     const uint32_t half = e >> 2;
-    uint8_t* stage_buf = smem + L::epi_off + e * kEpiChunkBytes;
+    uint8_t* stage_buf = smem + L::epi_off + e * L::kEpiChunkBytes;
     float* bias_s = reinterpret_cast<float*>(smem + L::bias_off) + e * 128;
+    const uint32_t tmem_empty_leader = mapa_shared(smem_u32(tmem_empty), 0);
     float alpha = 1.0f;
     if constexpr (FMT == BSQ_NVFP4) alpha = __fmul_rn(*args.ga, *args.gb);
     uint32_t acc_phase = 0;
-    for (int tile = blockIdx.x; tile < args.num_tiles; tile += gridDim.x) {
-      const int m_blk = tile / args.tiles_n, n_blk = tile % args.tiles_n;
+    for (int pt = first_pair; pt < args.num_pairs; pt += pair_stride) {
+      const int m_blk = 2 * (pt / args.tiles_n) + static_cast<int>(rank);
+      const int n_blk = pt % args.tiles_n;
       const int n0 = n_blk * BN + half * 128;
       const int m0 = m_blk * BM + quad * 32;
       // bias of this warp's 128 columns (zero past N or without bias)
@@ -335,17 +382,19 @@ __global__ void __launch_bounds__(threads_of<FMT>(), 1)
       tmem_ld_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(tmem_empty);  // accumulator may be overwritten now
+      if (lane == 0) mbar_arrive_remote(tmem_empty_leader);  // accumulator may be overwritten now
 
+      constexpr int EC = C::kEpiCols;  // 32 or 16 columns (64 or 32 bytes) per store chunk
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
+      for (int j = 0; j < 128 / EC; ++j) {
         if (lane == 0) bulk_wait_group_read0();  // staging buffer free again
         __syncwarp();
-        uint32_t packed[16];
+        uint32_t packed[EC / 2];
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const float b0 = bias_s[32 * j + 2 * c], b1 = bias_s[32 * j + 2 * c + 1];
-          float v0 = __uint_as_float(acc[j][2 * c]), v1 = __uint_as_float(acc[j][2 * c + 1]);
+        for (int c = 0; c < EC / 2; ++c) {
+          const int col = EC * j + 2 * c;  // column within this warp's 128
+          const float b0 = bias_s[col], b1 = bias_s[col + 1];
+          float v0 = __uint_as_float(acc[col >> 5][col & 31]), v1 = __uint_as_float(acc[col >> 5][(col + 1) & 31]);
           if constexpr (FMT == BSQ_NVFP4) {
             v0 = __fmaf_rn(v0, alpha, b0);
             v1 = __fmaf_rn(v1, alpha, b1);
@@ -356,16 +405,18 @@ __global__ void __launch_bounds__(threads_of<FMT>(), 1)
           __nv_bfloat162 p = __floats2bfloat162_rn(v0, v1);
           packed[c] = *reinterpret_cast<uint32_t*>(&p);
         }
-        // row `lane` of the 32 x 32 chunk, 64 bytes, 16-byte pieces swizzled (64-byte mode)
+        // row `lane` of the 32 x EC chunk in 16-byte pieces; the TMA swizzle (64B or 32B mode)
+        // XORs the piece index with address bits 7.. so that a quarter-warp hits distinct banks
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const uint32_t phys = (static_cast<uint32_t>(q) ^ ((lane >> 1) & 3u)) << 4;
-          *reinterpret_cast<uint4*>(stage_buf + lane * 64 + phys) =
+        for (int q = 0; q < EC / 8; ++q) {
+          const uint32_t sw = (EC == 32) ? ((lane >> 1) & 3u) : ((lane >> 2) & 1u);
+          const uint32_t phys = (static_cast<uint32_t>(q) ^ sw) << 4;
+          *reinterpret_cast<uint4*>(stage_buf + lane * (EC * 2) + phys) =
               make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
         }
         fence_proxy_async_smem();
         __syncwarp();
-        const int x = n0 + 32 * j;
+        const int x = n0 + EC * j;
         if (lane == 0 && x < args.N && m0 < args.M) {
           tma_store_2d(&mapOut, stage_buf, x, m0);
           bulk_commit_group();
@@ -377,9 +428,10 @@ __global__ void __launch_bounds__(threads_of<FMT>(), 1)
 
   tc_fence_before();
   __syncthreads();
+  cluster_sync_all();  // neither CTA leaves while its peer may still touch its barriers or TMEM
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, kTmemCols);
+    tmem_dealloc_pair(tmem_base, kTmemCols);
   }
 }
 
@@ -402,6 +454,35 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
+// View of a rows x kbytes K-major operand as (128 bytes of a K chunk, rows, K chunks).
+bool make_map_3d_chunks(CUtensorMap* map, const void* base, uint64_t kbytes, uint64_t rows, uint32_t box_rows,
+                        uint32_t box_chunks) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kChunkBytes), rows, kbytes / kChunkBytes};
+  const cuuint64_t strides[2] = {kbytes, static_cast<cuuint64_t>(kChunkBytes)};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(kChunkBytes), box_rows, box_chunks};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// View of a tiled scale buffer as (128 words of a 512-byte atom, atoms of a row tile, row
+// tiles); a box of (128, atoms, tiles) brings that many whole atoms in one copy.
+bool make_map_scales(CUtensorMap* map, const void* base, uint64_t atoms_per_tile, uint64_t row_tiles,
+                     uint32_t box_atoms, uint32_t box_tiles) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[3] = {128, atoms_per_tile, row_tiles};
+  const cuuint64_t strides[2] = {512, atoms_per_tile * 512};
+  const cuuint32_t box[3] = {128, box_atoms, box_tiles};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool make_map_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
                  uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
   EncodeTiledFn fn = encode_fn();
@@ -414,44 +495,67 @@ bool make_map_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uin
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+cudaLaunchConfig_t pair_launch_config(cudaLaunchAttribute* attr, int clusters, int threads, int smem,
+                                      cudaStream_t stream) {
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * clusters);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+
 template <int FMT>
 int run_gemm(const void* A, const void* A_scales, const void* B, const void* B_scales, const void* bias, void* out,
              int64_t M, int64_t N, int64_t K, cudaStream_t stream, const DeviceInfo& dev) {
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
+  static int max_clusters = 0;
   std::call_once(attr_once, [] {
     attr_err = cudaFuncSetAttribute(gemm_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<FMT>::alloc);
+    if (attr_err != cudaSuccess) return;
+    cudaLaunchAttribute at[1];
+    cudaLaunchConfig_t cfg = pair_launch_config(at, 1, threads_of<FMT>(), Smem<FMT>::alloc, nullptr);
+    attr_err = cudaOccupancyMaxActiveClusters(&max_clusters, gemm_kernel<FMT>, &cfg);
+    if (attr_err == cudaSuccess && max_clusters < 1) attr_err = cudaErrorInvalidConfiguration;
   });
   if (attr_err != cudaSuccess) return BSQ_ERR_LAUNCH;
 
   const uint64_t kbytes = (FMT == BSQ_MXFP8) ? static_cast<uint64_t>(K) : static_cast<uint64_t>(K) / 2;
-  CUtensorMap mA, mB, mOut;
-  if (!make_map_2d(&mA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, kbytes, M, kbytes, kRowBytes, BM,
-                   CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_map_2d(&mB, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, kbytes, N, kbytes, kRowBytes, BN,
-                   CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_map_2d(&mOut, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, out, N, M, static_cast<uint64_t>(N) * 2, 32, 32,
-                   CU_TENSOR_MAP_SWIZZLE_64B))
+  CUtensorMap mA, mB, mSfa, mSfb, mOut;
+  constexpr int EC = Cfg<FMT>::kEpiCols;
+  if (!make_map_3d_chunks(&mA, A, kbytes, M, BM, Cfg<FMT>::kChunks) ||
+      !make_map_3d_chunks(&mB, B, kbytes, N, BNH, Cfg<FMT>::kChunks) ||
+      !make_map_scales(&mSfa, A_scales, static_cast<uint64_t>(ceil_div(K / block_size(FMT), 4)),
+                       static_cast<uint64_t>(ceil_div(M, 128)), Cfg<FMT>::kAtoms, 1) ||
+      !make_map_scales(&mSfb, B_scales, static_cast<uint64_t>(ceil_div(K / block_size(FMT), 4)),
+                       static_cast<uint64_t>(ceil_div(N, 128)), Cfg<FMT>::kAtoms, 2) ||
+      !make_map_2d(&mOut, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, out, N, M, static_cast<uint64_t>(N) * 2, EC, 32,
+                   EC == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B))
     return BSQ_ERR_LAUNCH;
 
   GemmArgs a{};
-  a.sfa = static_cast<const uint8_t*>(A_scales);
-  a.sfb = static_cast<const uint8_t*>(B_scales);
   a.bias = static_cast<const uint16_t*>(bias);
-  a.ga = reinterpret_cast<const float*>(a.sfa + scales_body_bytes(FMT, M, K));
-  a.gb = reinterpret_cast<const float*>(a.sfb + scales_body_bytes(FMT, N, K));
+  a.ga = reinterpret_cast<const float*>(static_cast<const uint8_t*>(A_scales) + scales_body_bytes(FMT, M, K));
+  a.gb = reinterpret_cast<const float*>(static_cast<const uint8_t*>(B_scales) + scales_body_bytes(FMT, N, K));
   a.M = static_cast<int>(M);
   a.N = static_cast<int>(N);
-  a.K = static_cast<int>(K);
-  const int tiles_m = static_cast<int>(ceil_div(M, BM));
   a.tiles_n = static_cast<int>(ceil_div(N, BN));
-  a.num_tiles = tiles_m * a.tiles_n;
-  a.nk = static_cast<int>(K / Cfg<FMT>::kKElems);
-  a.sf_nct = static_cast<int>(K / block_size(FMT) / 4);
-  a.sfb_row_tiles = static_cast<int>(ceil_div(N, 128));
+  a.num_pairs = static_cast<int>(ceil_div(ceil_div(M, BM), 2)) * a.tiles_n;
+  a.kchunks = static_cast<int>(kbytes / kChunkBytes);
+  a.nk = static_cast<int>(ceil_div(a.kchunks, Cfg<FMT>::kChunks));
   a.status = dev.status;
-  const int grid = std::min(a.num_tiles, dev.num_sms);
-  gemm_kernel<FMT><<<grid, threads_of<FMT>(), Smem<FMT>::alloc, stream>>>(mA, mB, mOut, a);
+  const int clusters = std::min(a.num_pairs, std::min(max_clusters, dev.num_sms / 2));
+
+  cudaLaunchAttribute at[1];
+  cudaLaunchConfig_t cfg = pair_launch_config(at, clusters, threads_of<FMT>(), Smem<FMT>::alloc, stream);
+  if (cudaLaunchKernelEx(&cfg, gemm_kernel<FMT>, mA, mB, mSfa, mSfb, mOut, a) != cudaSuccess) return BSQ_ERR_LAUNCH;
   return cudaGetLastError() == cudaSuccess ? BSQ_OK : BSQ_ERR_LAUNCH;
 }
 

@@ -125,3 +125,16 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     assert bsq.device_status() == 0                           # read-and-clear
     # the context is still usable
     test_gemm_oracle_operands("mxfp8", 128, 256, 256)
+
+
+@pytest.mark.parametrize("fmt,K", [("mxfp8", 384), ("mxfp8", 640), ("mxfp4", 256), ("mxfp4", 768), ("nvfp4", 768)])
+def test_gemm_partial_last_stage(fmt, K):
+    """K that leaves the last pipeline stage with a single 128-byte K chunk."""
+    bsq = _bsq()
+    M, N = 300, 512
+    a = random_matrix(M, K, seed=K, dist="student_t4")
+    b = random_matrix(N, K, seed=K + 1, std=0.02)
+    qa, qb = oracle.quantize(fmt, a), oracle.quantize(fmt, b)
+    out = bsq.gemm(_qtensor_from_oracle(qa), _qtensor_from_oracle(qb), None)
+    assert bsq.device_status() == 0
+    check_gemm_rows(bf16_to_f64(out), qa, qb, None, np.arange(M), "%s K=%d" % (fmt, K))
