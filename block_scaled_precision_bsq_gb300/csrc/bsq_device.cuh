@@ -28,6 +28,16 @@ __device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31u; }
 
 __device__ __forceinline__ bool elect_lane0() { return (threadIdx.x & 31u) == 0u; }
 
+// One lane of the (converged) warp, chosen by elect.sync. The warp's other lanes keep running the
+// same loop, so addresses and descriptors computed there stay warp-uniform.
+__device__ __forceinline__ bool elect_one_sync() {
+  uint32_t pred;
+  asm volatile(
+      "{\n\t.reg .b32 r;\n\t.reg .pred p;\n\telect.sync r|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 // ---------------------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
@@ -79,6 +89,12 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   }
 }
 
+// Whole-warp form of mbar_wait_bounded: every lane waits (bounded) and the warp agrees on the
+// outcome, so a timeout seen by any lane sends the whole warp down the same path.
+__device__ __forceinline__ bool mbar_wait_bounded_warp(uint64_t* bar, uint32_t parity, volatile int* abort, int* status) {
+  return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity, abort, status)) != 0;
+}
+
 // ---------------------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_load_2d(void* smem_dst, const void* tmap, uint64_t* bar, int32_t x, int32_t y) {
   asm volatile(
@@ -116,6 +132,15 @@ __device__ __forceinline__ void tma_load_3d_to_leader(void* smem_dst, const void
       "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, "
       "%4, %5}], [%2];" ::"r"(smem_u32(smem_dst)),
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(leader_bar), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+// 2-D form of tma_load_3d_to_leader.
+__device__ __forceinline__ void tma_load_2d_to_leader(void* smem_dst, const void* tmap, uint32_t leader_bar, int32_t x,
+                                                      int32_t y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, "
+      "%4}], [%2];" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(leader_bar), "r"(x), "r"(y)
       : "memory");
 }
 constexpr uint32_t kClusterRankBit = 1u << 24;

@@ -12,21 +12,24 @@
 // rows of A and its 128-row half of B: 32 KB per stage per SM for the same 512 cycles.
 //
 // Design (a (2,1,1) cluster per SM pair, persistent over 256 x 256 tiles; rank 0 = leader):
-//   warp 0      (both CTAs) TMA producer: own A rows, own half of the B rows (K chunks of
-//               128 bytes, 128-byte swizzle, K-major), own A scale atoms and all B scale atoms
-//               of the tile, into a kStages ring. Every copy is a 3-D tensor copy in its
-//               .cta_group::2 form, completing on the LEADER's full[] barrier, which expects
-//               the bytes of both CTAs: the leader learns that the whole stage landed without
-//               any relay between the CTAs.
-//   warp 1      leader: TMEM owner and MMA issuer (tcgen05.mma.cta_group::2, M=256 N=256), one
-//               commit per stage multicast to both CTAs' empty[] barriers, one per tile to
-//               both CTAs' tmem_full.
-//   warps 2..   leader (formats with many scale atoms): scale-factor copiers
-//               (tcgen05.cp.cta_group::2: each CTA's TMEM gets its own shared-memory atoms),
-//               committing onto sf_ready[].
-//   last 8      (both CTAs) epilogue: drain the CTA's 128 x 256 fp32 accumulator, alpha + bias,
-//               bf16, 64B-swizzled staging, TMA store; tell the leader (tmem_empty, 16
+//   warp 0      (both CTAs) TMA producer: per stage one 128-byte K chunk of the CTA's A rows
+//               and of its half of the B rows (128-byte swizzle, K-major), the CTA's A scale
+//               atoms and all B scale atoms of the tile, into a kStages ring. Every copy is a
+//               tensor copy in its .cta_group::2 form, completing on the LEADER's full[]
+//               barrier, which expects the bytes of both CTAs: the leader learns that the
+//               whole stage landed without any relay between the CTAs.
+//   warp 1      leader: TMEM owner and MMA issuer. The whole warp runs the loop (operands
+//               stay warp-uniform) and one elected lane issues, per stage, the scale-factor
+//               copies into the stage's TMEM slot of both CTAs (tcgen05.cp.cta_group::2: each
+//               CTA's TMEM gets its own shared-memory atoms), the four MMAs
+//               (tcgen05.mma.cta_group::2, M=256 N=256) and one commit multicast to both
+//               CTAs' empty[] barriers; one commit per tile to both CTAs' tmem_full.
+//   warps 2..9  (both CTAs) epilogue: drain the CTA's 128 x 256 fp32 accumulator, alpha +
+//               bias, bf16, swizzled staging, TMA store; tell the leader (tmem_empty, 16
 //               arrivals) as soon as the accumulator has been read.
+// Measured on GB300 (clock64 instrumentation): each tcgen05 instruction costs the issuing
+// thread a few dozen cycles, so the issue loop holds nothing else; in one thread the tensor
+// pipe keeps copies and MMAs in order, so a stage's scales need no extra barrier.
 // Every mbarrier wait is bounded (%globaltimer); on a timeout the kernel records
 // BSQ_ERR_TIMEOUT in the device status word, the roles leave their loops, outstanding
 // tensor-core work is waited for and TMEM is released after a final cluster barrier.
@@ -44,57 +47,44 @@
 namespace bsq {
 namespace {
 
-constexpr int BM = 128;         // rows of A per CTA (256 per pair)
-constexpr int BN = 256;         // columns of the output tile (both CTAs)
+constexpr int BM = 128;           // rows of A per CTA (256 per pair)
+constexpr int BN = 256;           // columns of the output tile (both CTAs)
 constexpr int BNH = BN / 2;       // rows of B held per CTA
-constexpr int kChunkBytes = 128;  // one 128-byte swizzle span of K per row
+constexpr int kChunkBytes = 128;  // K bytes per stage: one 128-byte swizzle span per row
+constexpr int kMmasPerStage = 4;  // 32 K bytes per MMA
 constexpr int kNumEpiWarps = 8;
+constexpr int kFirstEpiWarp = 2;
+constexpr int kThreads = (kFirstEpiWarp + kNumEpiWarps) * 32;
 constexpr int kAccCols = BN;  // fp32 accumulator columns in TMEM
 constexpr uint32_t kTmemCols = 512;
 
-// Per format: kChunks 128-byte K chunks per stage (loaded as one 3-D TMA box per operand:
-// measured TMA cost falls with fewer, larger operations), kKElems K elements per stage,
-// kAtoms 512-byte scale atoms per 128 rows per stage, kSfCols TMEM columns of one stage's
-// scale slot (4 per A atom, 8 per B atom), kEpiCols output columns per epilogue store chunk.
+// Per format: kStages stages in the ring, kAtoms 512-byte scale atoms per 128 rows per stage
+// (4 scale columns of 128 rows each), kEpiCols output columns per epilogue store chunk. A
+// stage's scale slot in TMEM takes 4 columns per A atom and 8 per B atom (two 128-row halves).
 template <int FMT>
 struct Cfg;
 template <>
-struct Cfg<BSQ_MXFP8> {  // 256 K per stage = 8 MMAs of K 32; 8 UE8M0 scales per row per stage
-  static constexpr int kChunks = 2, kStages = 3, kKElems = 256, kAtoms = 2, kSfWarps = 0, kEpiCols = 32;
+struct Cfg<BSQ_MXFP8> {  // 128 K per stage = 4 MMAs of K 32, one UE8M0 scale each
+  static constexpr int kStages = 6, kAtoms = 1, kEpiCols = 32;
 };
 template <>
-struct Cfg<BSQ_NVFP4> {  // 256 K per stage = 4 MMAs of K 64; 16 E4M3 scales per row per stage
-  static constexpr int kChunks = 1, kStages = 5, kKElems = 256, kAtoms = 4, kSfWarps = 2, kEpiCols = 32;
+struct Cfg<BSQ_NVFP4> {  // 256 K per stage = 4 MMAs of K 64, four E4M3 scales (one atom) each
+  static constexpr int kStages = 5, kAtoms = 4, kEpiCols = 32;
 };
 template <>
-struct Cfg<BSQ_MXFP4> {  // 512 K per stage = 8 MMAs of K 64; 16 UE8M0 scales per row per stage
-  static constexpr int kChunks = 2, kStages = 3, kKElems = 512, kAtoms = 4, kSfWarps = 1, kEpiCols = 16;
+struct Cfg<BSQ_MXFP4> {  // 256 K per stage = 4 MMAs of K 64, two UE8M0 scales each
+  static constexpr int kStages = 6, kAtoms = 2, kEpiCols = 16;
 };
 template <int FMT>
 __host__ __device__ constexpr int sf_cols() {
   return 12 * Cfg<FMT>::kAtoms;
 }
 
-// Warp roles: 0 TMA producer, 1 MMA issuer (leader), 2 .. 1 + kSfWarps
-// scale-factor copiers (leader), then kNumEpiWarps epilogue warps. With kSfWarps = 0 the MMA
-// issuer copies the scale factors itself, right before the stage's MMAs: in one thread the
-// tensor pipe keeps them in order, with no extra barrier hop (a copier warp's copies queue
-// behind the MMAs already issued and delay the next stage). Formats whose copies would not
-// fit in the issuer's time budget (12 copies per stage) use copier warps.
-template <int FMT>
-__host__ __device__ constexpr int first_epi_warp() {
-  return 2 + Cfg<FMT>::kSfWarps;
-}
-template <int FMT>
-__host__ __device__ constexpr int threads_of() {
-  return (first_epi_warp<FMT>() + kNumEpiWarps) * 32;
-}
-
 template <int FMT>
 struct Smem {
   static constexpr int S = Cfg<FMT>::kStages;
-  static constexpr int kABytes = Cfg<FMT>::kChunks * BM * kChunkBytes;   // own 128 rows of A
-  static constexpr int kBBytes = Cfg<FMT>::kChunks * BNH * kChunkBytes;  // own 128-row half of B
+  static constexpr int kABytes = BM * kChunkBytes;   // own 128 rows of A
+  static constexpr int kBBytes = BNH * kChunkBytes;  // own 128-row half of B
   static constexpr int kSfaBytes = Cfg<FMT>::kAtoms * 512;      // this CTA's 128 A rows
   static constexpr int kSfbBytes = 2 * Cfg<FMT>::kAtoms * 512;  // all 256 B rows of the tile
   static constexpr int kEpiChunkBytes = 32 * Cfg<FMT>::kEpiCols * 2;
@@ -105,7 +95,7 @@ struct Smem {
   static constexpr int epi_off = ((sfb_off + S * kSfbBytes) + 1023) / 1024 * 1024;
   static constexpr int bias_off = epi_off + kNumEpiWarps * kEpiChunkBytes;
   static constexpr int bar_off = bias_off + kNumEpiWarps * 128 * 4;
-  static constexpr int kNumBars = 3 * S + 4;
+  static constexpr int kNumBars = 2 * S + 3;
   static constexpr int misc_off = bar_off + kNumBars * 8;
   static constexpr int total = misc_off + 16;
   static constexpr int alloc = total + 1024;  // slack for aligning the base to 1024
@@ -134,13 +124,13 @@ struct GemmArgs {
   const float* ga;       // NVFP4: per-tensor scales in the scale tails
   const float* gb;
   int M, N;
-  int tiles_n, num_pairs, nk;
-  int kchunks;  // 128-byte K chunks in total (the last stage may hold fewer than kChunks)
+  int tiles_n, num_pairs;
+  int nk;  // stages per tile: K bytes / 128
   int* status;
 };
 
 template <int FMT>
-__global__ void __launch_bounds__(threads_of<FMT>(), 1)
+__global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
                 const __grid_constant__ CUtensorMap mapSfa, const __grid_constant__ CUtensorMap mapSfb,
                 const __grid_constant__ CUtensorMap mapOut, const GemmArgs args) {
@@ -150,13 +140,11 @@ __global__ void __launch_bounds__(threads_of<FMT>(), 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::bar_off);
-  uint64_t* full_bar = bars;                  // leader: both CTAs' operands of a stage landed
-  uint64_t* empty_bar = bars + S;             // the pair's MMAs are done with a stage
-  uint64_t* sf_ready = bars + 2 * S;          // leader: the stage's scale factors are in both TMEMs
-  uint64_t* tmem_full = bars + 3 * S;         // the accumulator of a tile is complete
-  uint64_t* tmem_empty = bars + 3 * S + 1;    // leader: both CTAs drained their accumulator
-  uint64_t* drain_bar = bars + 3 * S + 2;     // leader: MMA issuer's outstanding work
-  uint64_t* sf_drain_bar = bars + 3 * S + 3;  // leader: scale-factor copiers' outstanding work
+  uint64_t* full_bar = bars;                // leader: both CTAs' operands of a stage landed
+  uint64_t* empty_bar = bars + S;           // the pair's MMAs are done with a stage
+  uint64_t* tmem_full = bars + 2 * S;       // the accumulator of a tile is complete
+  uint64_t* tmem_empty = bars + 2 * S + 1;  // leader: both CTAs drained their accumulator
+  uint64_t* drain_bar = bars + 2 * S + 2;   // leader: MMA issuer's outstanding work
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L::misc_off);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::misc_off + 4);
 
@@ -169,12 +157,10 @@ __global__ void __launch_bounds__(threads_of<FMT>(), 1)
     for (int s = 0; s < S; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
-      mbar_init(&sf_ready[s], C::kSfWarps > 0 ? C::kSfWarps : 1);
     }
     mbar_init(tmem_full, 1);
     mbar_init(tmem_empty, 2 * kNumEpiWarps);
     mbar_init(drain_bar, 1);
-    mbar_init(sf_drain_bar, C::kSfWarps > 0 ? C::kSfWarps : 1);
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&mapA);
@@ -192,32 +178,13 @@ __global__ void __launch_bounds__(threads_of<FMT>(), 1)
   cluster_sync_all();  // barriers of both CTAs initialised before any remote arrival
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
-  // Copy scale atoms [first, first + count) of a stage (A atoms first, then the B atoms of the
-  // two 128-row halves) from each CTA's shared memory into the stage's TMEM slot of each CTA.
-  auto copy_stage_scales = [&](int stage, int kb, int first, int count) {
-    (void)kb;
-    const uint32_t sfa_t = tmem_base + kAccCols + stage * sf_cols<FMT>();
-    const uint32_t sfb_t = sfa_t + 4 * C::kAtoms;
-    const uint32_t sfa_s = smem_u32(smem + L::sfa_off + stage * L::kSfaBytes);
-    const uint32_t sfb_s = smem_u32(smem + L::sfb_off + stage * L::kSfbBytes);
-#pragma unroll
-    for (int c = 0; c < count; ++c) {
-      const int i = first + c;
-      if (i < C::kAtoms) {
-        tc_cp_pair_32x128b_warpx4(sfa_t + 4 * i, smem_desc(sfa_s + 512 * i, 128, 128, kSwizzleNone));
-      } else {
-        const int j = i - C::kAtoms, at = j >> 1, h = j & 1;
-        tc_cp_pair_32x128b_warpx4(sfb_t + 8 * at + 4 * h, smem_desc(sfb_s + h * L::kSfaBytes + 512 * at, 128, 128, kSwizzleNone));
-      }
-    }
-  };
   const int first_pair = static_cast<int>(cluster_id_x());
   const int pair_stride = static_cast<int>(num_clusters_x());
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------------ TMA producer
-    // Boxes reaching past M, N or K are zero-filled by TMA and still deliver their full byte
-    // count, so every stage of every CTA brings exactly kStageBytes.
+    // Boxes reaching past M, N or the scale atoms are zero-filled by TMA and still deliver
+    // their full byte count, so every stage of every CTA brings exactly kStageBytes.
     constexpr uint32_t kStageBytes = L::kABytes + L::kBBytes + L::kSfaBytes + L::kSfbBytes;
     int stage = 0;
     uint32_t phase = 0;
@@ -232,9 +199,9 @@ __global__ void __launch_bounds__(threads_of<FMT>(), 1)
         }
         if (leader) mbar_arrive_expect_tx(&full_bar[stage], 2 * kStageBytes);
         const uint32_t bar = smem_u32(&full_bar[stage]) & ~kClusterRankBit;  // the leader's full[stage]
-        tma_load_3d_to_leader(smem + L::a_off + stage * L::kABytes, &mapA, bar, 0, m_blk * BM, kb * C::kChunks);
-        tma_load_3d_to_leader(smem + L::b_off + stage * L::kBBytes, &mapB, bar, 0,
-                              n_blk * BN + static_cast<int>(rank) * BNH, kb * C::kChunks);
+        tma_load_2d_to_leader(smem + L::a_off + stage * L::kABytes, &mapA, bar, kb * kChunkBytes, m_blk * BM);
+        tma_load_2d_to_leader(smem + L::b_off + stage * L::kBBytes, &mapB, bar, kb * kChunkBytes,
+                              n_blk * BN + static_cast<int>(rank) * BNH);
         tma_load_3d_to_leader(smem + L::sfa_off + stage * L::kSfaBytes, &mapSfa, bar, 0, kb * C::kAtoms, m_blk);
         tma_load_3d_to_leader(smem + L::sfb_off + stage * L::kSfbBytes, &mapSfb, bar, 0, kb * C::kAtoms, 2 * n_blk);
         if (++stage == S) {
@@ -243,113 +210,84 @@ __global__ void __launch_bounds__(threads_of<FMT>(), 1)
         }
       }
     }
-  } else if (warp == 1 && lane == 0 && leader) {
+  } else if (warp == 1 && leader) {
     // ------------------------------------------------------------------ MMA issuer (leader)
-    // Every tcgen05 instruction and every mbarrier wait costs the issuing thread a few dozen
-    // cycles; one 2-SM MMA of 256 x 256 takes 128 tensor cycles. The issuer does only the
-    // wait, the four MMAs and the commit of each stage; the scale-factor copiers waited for
-    // both CTAs' operands before signalling sf_ready.
+    const bool issuer = elect_one_sync();
     int stage = 0;
     uint32_t phase = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
-    const uint64_t adesc0 = smem_desc(smem_u32(smem + L::a_off), 16, 1024, kSwizzle128B);
-    const uint64_t bdesc0 = smem_desc(smem_u32(smem + L::b_off), 16, 1024, kSwizzle128B);
+    const uint32_t a_s0 = smem_u32(smem + L::a_off);
+    const uint32_t b_s0 = smem_u32(smem + L::b_off);
+    const uint32_t sfa_s0 = smem_u32(smem + L::sfa_off);
+    const uint32_t sfb_s0 = smem_u32(smem + L::sfb_off);
+    const uint32_t sf_t0 = tmem_base + kAccCols;
     for (int pt = first_pair; pt < args.num_pairs && ok; pt += pair_stride) {
       // wait until both CTAs' epilogues have drained the accumulator of the previous tile
-      if (!mbar_wait_bounded(tmem_empty, acc_phase ^ 1u, abort_flag, args.status)) break;
+      if (!mbar_wait_bounded_warp(tmem_empty, acc_phase ^ 1u, abort_flag, args.status)) break;
       acc_phase ^= 1u;
       tc_fence_after();
       for (int kb = 0; kb < args.nk; ++kb) {
-        if constexpr (C::kSfWarps == 0) {
-          // both CTAs' operands of the stage landed: copy the scales, then the MMAs
-          if (!mbar_wait_bounded(&full_bar[stage], phase, abort_flag, args.status)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          copy_stage_scales(stage, kb, 0, 3 * C::kAtoms);
-        } else {
-          if (!mbar_wait_bounded(&sf_ready[stage], phase, abort_flag, args.status)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
+        // both CTAs' operands of the stage landed
+        if (!mbar_wait_bounded_warp(&full_bar[stage], phase, abort_flag, args.status)) {
+          ok = false;
+          break;
         }
-        const int nmma = 4 * min(C::kChunks, args.kchunks - kb * C::kChunks);
-        const uint32_t sfa_t = tmem_base + kAccCols + stage * sf_cols<FMT>();
+        tc_fence_after();
+        const uint32_t sfa_t = sf_t0 + stage * sf_cols<FMT>();
         const uint32_t sfb_t = sfa_t + 4 * C::kAtoms;
-        // start-address field of the descriptors is in 16-byte units (stays below 2^14)
-        const uint64_t adesc = adesc0 + static_cast<uint64_t>((stage * L::kABytes) >> 4);
-        const uint64_t bdesc = bdesc0 + static_cast<uint64_t>((stage * L::kBBytes) >> 4);
+        const uint32_t sfa_s = sfa_s0 + stage * L::kSfaBytes;
+        const uint32_t sfb_s = sfb_s0 + stage * L::kSfbBytes;
+        const uint64_t adesc = smem_desc(a_s0 + stage * L::kABytes, 16, 1024, kSwizzle128B);
+        const uint64_t bdesc = smem_desc(b_s0 + stage * L::kBBytes, 16, 1024, kSwizzle128B);
+        if (issuer) {
+          // scale atoms into the stage's TMEM slot of both CTAs (A atoms, then the B atoms of
+          // the two 128-row halves); in this thread's order they land before the MMAs read them
 #pragma unroll
-        for (int k = 0; k < 4 * C::kChunks; ++k) {
-          if (k >= nmma) break;
-          // K chunk k / 4 (its own 16 KB swizzle block), 32 bytes into it per MMA
-          const uint64_t koff = static_cast<uint64_t>((k >> 2) * ((BM * kChunkBytes) >> 4) + 2 * (k & 3));
-          const uint64_t kboff = static_cast<uint64_t>((k >> 2) * ((BNH * kChunkBytes) >> 4) + 2 * (k & 3));
-          uint32_t sfa = sfa_t, sfb = sfb_t, id = 0;
-          if constexpr (FMT == BSQ_MXFP8) {
-            sfa += 4 * (k >> 2);  // one scale of 32 K per MMA: byte k % 4 of atom k / 4
-            sfb += 8 * (k >> 2);
-            id = k & 3;
-          } else if constexpr (FMT == BSQ_NVFP4) {
-            sfa += 4 * k;  // one atom (4 scales of 16 K) per MMA
-            sfb += 8 * k;
-          } else {
-            sfa += 4 * (k >> 1);  // two scales of 32 K per MMA: bytes {0,1} or {2,3}
-            sfb += 8 * (k >> 1);
-            id = 2 * (k & 1);
+          for (int i = 0; i < C::kAtoms; ++i)
+            tc_cp_pair_32x128b_warpx4(sfa_t + 4 * i, smem_desc(sfa_s + 512 * i, 128, 128, kSwizzleNone));
+#pragma unroll
+          for (int i = 0; i < 2 * C::kAtoms; ++i) {
+            const int at = i >> 1, h = i & 1;
+            tc_cp_pair_32x128b_warpx4(sfb_t + 8 * at + 4 * h,
+                                      smem_desc(sfb_s + h * L::kSfaBytes + 512 * at, 128, 128, kSwizzleNone));
           }
-          tc_mma_pair<FMT>(tmem_base, adesc + koff, bdesc + kboff, make_idesc<FMT>(id), sfa, sfb,
-                           (kb | k) != 0 ? 1u : 0u);
+#pragma unroll
+          for (int k = 0; k < kMmasPerStage; ++k) {
+            // 32 bytes of K per MMA within the 128-byte swizzle span (descriptor start
+            // addresses are in 16-byte units)
+            uint32_t sfa = sfa_t, sfb = sfb_t, id = 0;
+            if constexpr (FMT == BSQ_MXFP8) {
+              id = k;  // one scale of 32 K per MMA: byte k of the stage's atom
+            } else if constexpr (FMT == BSQ_NVFP4) {
+              sfa += 4 * k;  // one atom (4 scales of 16 K) per MMA
+              sfb += 8 * k;
+            } else {
+              sfa += 4 * (k >> 1);  // two scales of 32 K per MMA: bytes {0,1} or {2,3}
+              sfb += 8 * (k >> 1);
+              id = 2 * (k & 1);
+            }
+            tc_mma_pair<FMT>(tmem_base, adesc + 2 * k, bdesc + 2 * k, make_idesc<FMT>(id), sfa, sfb,
+                             (k > 0 || kb > 0) ? 1u : 0u);
+          }
+          tc_commit_pair_mc(&empty_bar[stage], 0x3);  // both CTAs' stage is free once these MMAs read it
         }
-        tc_commit_pair_mc(&empty_bar[stage], 0x3);  // both CTAs' stage is free once these MMAs read it
+        __syncwarp();
         if (++stage == S) {
           stage = 0;
           phase ^= 1u;
         }
       }
-      if (ok) tc_commit_pair_mc(tmem_full, 0x3);  // both CTAs' accumulators complete
+      if (ok && issuer) tc_commit_pair_mc(tmem_full, 0x3);  // both CTAs' accumulators complete
+      __syncwarp();
     }
-    // every tensor-core operation of this thread must finish before TMEM is released
-    tc_commit_pair(drain_bar);
+    // every tensor-core operation of the issuing lane must finish before TMEM is released
+    if (issuer) tc_commit_pair(drain_bar);
+    __syncwarp();
     mbar_wait_bounded(drain_bar, 0, nullptr, args.status);
-  } else if (warp >= 2 && warp < static_cast<uint32_t>(first_epi_warp<FMT>()) && leader) {
-    // ------------------------------------------------------------------ scale-factor copiers (leader)
-    // Each of the kSfWarps warps copies its share of the stage's 512-byte scale atoms into the
-    // stage's TMEM slot of BOTH CTAs (each from its own shared memory), after both CTAs'
-    // operands of the stage have landed, then commits onto sf_ready[stage].
-    if (lane == 0) {
-      constexpr int kCps = 3 * C::kAtoms;  // A atoms, then B atoms (two 128-row halves each)
-      constexpr int kPer = kCps / (C::kSfWarps > 0 ? C::kSfWarps : 1);
-      static_assert(C::kSfWarps == 0 || kCps % C::kSfWarps == 0, "scale copies split evenly");
-      const int first = (static_cast<int>(warp) - 2) * kPer;
-      int stage = 0;
-      uint32_t phase = 0;
-      bool ok = true;
-      for (int pt = first_pair; pt < args.num_pairs && ok; pt += pair_stride) {
-        for (int kb = 0; kb < args.nk; ++kb) {
-          if (!mbar_wait_bounded(&full_bar[stage], phase, abort_flag, args.status)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          copy_stage_scales(stage, kb, first, kPer);
-          tc_commit_pair(&sf_ready[stage]);
-          if (++stage == S) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-      }
-      // the copies must be finished before TMEM is released
-      tc_commit_pair(sf_drain_bar);
-      mbar_wait_bounded(sf_drain_bar, 0, nullptr, args.status);
-    }
-  } else if (warp >= static_cast<uint32_t>(first_epi_warp<FMT>())) {
+  } else if (warp >= static_cast<uint32_t>(kFirstEpiWarp)) {
     // ------------------------------------------------------------------ epilogue (both CTAs)
-    const uint32_t e = warp - first_epi_warp<FMT>();  // 0..7
+    const uint32_t e = warp - kFirstEpiWarp;  // 0..7
     const uint32_t quad = warp & 3u;                  // TMEM lane quadrant this warp may access
     const uint32_t half = e >> 2;
     uint8_t* stage_buf = smem + L::epi_off + e * L::kEpiChunkBytes;
@@ -454,20 +392,6 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// View of a rows x kbytes K-major operand as (128 bytes of a K chunk, rows, K chunks).
-bool make_map_3d_chunks(CUtensorMap* map, const void* base, uint64_t kbytes, uint64_t rows, uint32_t box_rows,
-                        uint32_t box_chunks) {
-  EncodeTiledFn fn = encode_fn();
-  if (fn == nullptr) return false;
-  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kChunkBytes), rows, kbytes / kChunkBytes};
-  const cuuint64_t strides[2] = {kbytes, static_cast<cuuint64_t>(kChunkBytes)};
-  const cuuint32_t box[3] = {static_cast<cuuint32_t>(kChunkBytes), box_rows, box_chunks};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 // View of a tiled scale buffer as (128 words of a 512-byte atom, atoms of a row tile, row
 // tiles); a box of (128, atoms, tiles) brings that many whole atoms in one copy.
 bool make_map_scales(CUtensorMap* map, const void* base, uint64_t atoms_per_tile, uint64_t row_tiles,
@@ -521,7 +445,7 @@ int run_gemm(const void* A, const void* A_scales, const void* B, const void* B_s
     attr_err = cudaFuncSetAttribute(gemm_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<FMT>::alloc);
     if (attr_err != cudaSuccess) return;
     cudaLaunchAttribute at[1];
-    cudaLaunchConfig_t cfg = pair_launch_config(at, 1, threads_of<FMT>(), Smem<FMT>::alloc, nullptr);
+    cudaLaunchConfig_t cfg = pair_launch_config(at, 1, kThreads, Smem<FMT>::alloc, nullptr);
     attr_err = cudaOccupancyMaxActiveClusters(&max_clusters, gemm_kernel<FMT>, &cfg);
     if (attr_err == cudaSuccess && max_clusters < 1) attr_err = cudaErrorInvalidConfiguration;
   });
@@ -530,8 +454,8 @@ int run_gemm(const void* A, const void* A_scales, const void* B, const void* B_s
   const uint64_t kbytes = (FMT == BSQ_MXFP8) ? static_cast<uint64_t>(K) : static_cast<uint64_t>(K) / 2;
   CUtensorMap mA, mB, mSfa, mSfb, mOut;
   constexpr int EC = Cfg<FMT>::kEpiCols;
-  if (!make_map_3d_chunks(&mA, A, kbytes, M, BM, Cfg<FMT>::kChunks) ||
-      !make_map_3d_chunks(&mB, B, kbytes, N, BNH, Cfg<FMT>::kChunks) ||
+  if (!make_map_2d(&mA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, kbytes, M, kbytes, kChunkBytes, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map_2d(&mB, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, kbytes, N, kbytes, kChunkBytes, BNH, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_map_scales(&mSfa, A_scales, static_cast<uint64_t>(ceil_div(K / block_size(FMT), 4)),
                        static_cast<uint64_t>(ceil_div(M, 128)), Cfg<FMT>::kAtoms, 1) ||
       !make_map_scales(&mSfb, B_scales, static_cast<uint64_t>(ceil_div(K / block_size(FMT), 4)),
@@ -548,13 +472,12 @@ int run_gemm(const void* A, const void* A_scales, const void* B, const void* B_s
   a.N = static_cast<int>(N);
   a.tiles_n = static_cast<int>(ceil_div(N, BN));
   a.num_pairs = static_cast<int>(ceil_div(ceil_div(M, BM), 2)) * a.tiles_n;
-  a.kchunks = static_cast<int>(kbytes / kChunkBytes);
-  a.nk = static_cast<int>(ceil_div(a.kchunks, Cfg<FMT>::kChunks));
+  a.nk = static_cast<int>(kbytes / kChunkBytes);
   a.status = dev.status;
   const int clusters = std::min(a.num_pairs, std::min(max_clusters, dev.num_sms / 2));
 
   cudaLaunchAttribute at[1];
-  cudaLaunchConfig_t cfg = pair_launch_config(at, clusters, threads_of<FMT>(), Smem<FMT>::alloc, stream);
+  cudaLaunchConfig_t cfg = pair_launch_config(at, clusters, kThreads, Smem<FMT>::alloc, stream);
   if (cudaLaunchKernelEx(&cfg, gemm_kernel<FMT>, mA, mB, mSfa, mSfb, mOut, a) != cudaSuccess) return BSQ_ERR_LAUNCH;
   return cudaGetLastError() == cudaSuccess ? BSQ_OK : BSQ_ERR_LAUNCH;
 }
