@@ -103,7 +103,7 @@ int bsq_quantize(int fmt_flags, const void* src, int64_t rows, int64_t cols, voi
   const bool given = (flags & BSQ_FLAG_GLOBAL_GIVEN) != 0;
   if (fmt == BSQ_NVFP4 && given && global_scale == nullptr) return fail(BSQ_ERR_ARG);
   if (fmt != BSQ_NVFP4 && given) return fail(BSQ_ERR_ARG);
-  if (cols % bsq::block_size(fmt) != 0) return fail(BSQ_ERR_SHAPE);
+  if (cols % bsq::block_size(fmt) != 0 || rows > INT32_MAX || cols > INT32_MAX) return fail(BSQ_ERR_SHAPE);
   if (!aligned16(src) || !aligned16(codes) || !aligned16(scales)) return fail(BSQ_ERR_ALIGN);
   if (global_scale != nullptr && (reinterpret_cast<uintptr_t>(global_scale) & 3u)) return fail(BSQ_ERR_ALIGN);
   const bsq::DeviceInfo* dev = bsq::current_device();

@@ -59,21 +59,22 @@ constexpr int kAccCols = BN;  // fp32 accumulator columns in TMEM
 constexpr uint32_t kTmemCols = 512;
 
 // Per format: kStages stages in the ring, kAtoms 512-byte scale atoms per 128 rows per stage
-// (4 scale columns of 128 rows each), kEpiCols output columns per epilogue store chunk. A
+// (4 scale columns of 128 rows each), kEpiCols output columns per epilogue store chunk and
+// kEpiBufs staging buffers per epilogue warp (stores in flight per warp). A
 // stage's scale slot in TMEM takes 4 columns per A atom and 8 per B atom (two 128-row halves).
 template <int FMT>
 struct Cfg;
 template <>
 struct Cfg<BSQ_MXFP8> {  // 128 K per stage = 4 MMAs of K 32, one UE8M0 scale each
-  static constexpr int kStages = 6, kAtoms = 1, kEpiCols = 32;
+  static constexpr int kStages = 6, kAtoms = 1, kEpiCols = 32, kEpiBufs = 1;
 };
 template <>
 struct Cfg<BSQ_NVFP4> {  // 256 K per stage = 4 MMAs of K 64, four E4M3 scales (one atom) each
-  static constexpr int kStages = 5, kAtoms = 4, kEpiCols = 32;
+  static constexpr int kStages = 5, kAtoms = 4, kEpiCols = 32, kEpiBufs = 1;
 };
 template <>
 struct Cfg<BSQ_MXFP4> {  // 256 K per stage = 4 MMAs of K 64, two UE8M0 scales each
-  static constexpr int kStages = 6, kAtoms = 2, kEpiCols = 16;
+  static constexpr int kStages = 6, kAtoms = 2, kEpiCols = 16, kEpiBufs = 1;
 };
 template <int FMT>
 __host__ __device__ constexpr int sf_cols() {
@@ -93,7 +94,7 @@ struct Smem {
   static constexpr int sfa_off = b_off + S * kBBytes;
   static constexpr int sfb_off = sfa_off + S * kSfaBytes;
   static constexpr int epi_off = ((sfb_off + S * kSfbBytes) + 1023) / 1024 * 1024;
-  static constexpr int bias_off = epi_off + kNumEpiWarps * kEpiChunkBytes;
+  static constexpr int bias_off = epi_off + kNumEpiWarps * Cfg<FMT>::kEpiBufs * kEpiChunkBytes;
   static constexpr int bar_off = bias_off + kNumEpiWarps * 128 * 4;
   static constexpr int kNumBars = 2 * S + 3;
   static constexpr int misc_off = bar_off + kNumBars * 8;
@@ -290,7 +291,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t e = warp - kFirstEpiWarp;  // 0..7
     const uint32_t quad = warp & 3u;                  // TMEM lane quadrant this warp may access
     const uint32_t half = e >> 2;
-    uint8_t* stage_buf = smem + L::epi_off + e * L::kEpiChunkBytes;
+    constexpr int NB = C::kEpiBufs;
+    uint8_t* stage_base = smem + L::epi_off + e * NB * L::kEpiChunkBytes;
+    uint32_t nstores = 0;  // stores issued by this warp: staging buffer nstores % NB is next
     float* bias_s = reinterpret_cast<float*>(smem + L::bias_off) + e * 128;
     const uint32_t tmem_empty_leader = mapa_shared(smem_u32(tmem_empty), 0);
     float alpha = 1.0f;
@@ -325,7 +328,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr int EC = C::kEpiCols;  // 32 or 16 columns (64 or 32 bytes) per store chunk
 #pragma unroll
       for (int j = 0; j < 128 / EC; ++j) {
-        if (lane == 0) bulk_wait_group_read0();  // staging buffer free again
+        const int x = n0 + EC * j;
+        if (x >= args.N || m0 >= args.M) break;  // nothing of this chunk is stored (warp-uniform)
+        uint8_t* stage_buf = stage_base + (nstores % NB) * L::kEpiChunkBytes;
+        if (lane == 0) bulk_wait_group_read<NB - 1>();  // the store that last used this buffer has read it
         __syncwarp();
         uint32_t packed[EC / 2];
 #pragma unroll
@@ -354,11 +360,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         fence_proxy_async_smem();
         __syncwarp();
-        const int x = n0 + EC * j;
-        if (lane == 0 && x < args.N && m0 < args.M) {
+        if (lane == 0) {
           tma_store_2d(&mapOut, stage_buf, x, m0);
           bulk_commit_group();
         }
+        ++nstores;
       }
     }
     if (lane == 0) bulk_wait_group0();

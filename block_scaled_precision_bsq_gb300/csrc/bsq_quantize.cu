@@ -8,14 +8,20 @@
 // the BF16 ledger blog section 5.4; 6 for e2m1). The UE8M0 exponent of a block is
 // floor(log2(amax)) - emax with emax the exponent of the element format's top binade.
 //
-// Work mapping: one warp quantizes a 256-element segment of one row per step, each lane
-// 8 consecutive elements (one 16-byte bf16 load). A 1x32 block is 4 lanes, a 1x16 block 2
-// lanes; block maxima come from two (one) xor-shuffles. Each warp keeps kUnroll segments
-// of loads in flight. Codes leave as one 8-byte (E4M3) or 4-byte (e2m1) store per lane,
-// i.e. 256 or 128 contiguous bytes per warp. The scales of 4 consecutive blocks of a row
-// are 4 contiguous bytes in the tiled layout (128 rows x 4 columns per 512-byte tile, row
-// r at byte (r % 32) * 16 + ((r / 32) % 4) * 4), so each group of 4 scales is gathered with
-// shuffles and written as one 32-bit word.
+// Work mapping (two CTAs per SM, persistent). The source is cut into chunks of whole rows
+// (or, for rows longer than a chunk, row pieces of whole 512-element segments); a chunk is
+// contiguous in memory and comes in with one 1-D TMA bulk copy. A producer thread per CTA
+// keeps a ring of up to kRing chunk buffers in flight -- for a 22 MB matrix that is nearly
+// every chunk of the SM's share, requested at kernel start -- and the consumer warps (dealt
+// warp steps round-robin over the CTA's chunks) quantize a chunk straight
+// from shared memory, walking it as one flat array: each warp step covers 512 consecutive
+// elements, each lane 16 (one 32-byte piece; rows are multiples of 16 elements long, so a
+// piece never straddles two rows). A 1x32 block is then 2 lanes (one xor-shuffle for its
+// maximum), a 1x16 block 1 lane. Codes leave as one 16-byte (E4M3) or 8-byte (e2m1) store per
+// lane; each block's scale byte is stored at its place in the tiled layout (128 rows x 4
+// columns per 512-byte tile, row r at byte (r % 32) * 16 + ((r / 32) % 4) * 4), the lane of
+// a row's last block also zeroing the padding columns of that 4-column group. Scale bytes of
+// the padding rows of the last row tile are written as zeros by the kernel itself.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -27,35 +33,47 @@
 namespace bsq {
 namespace {
 
-constexpr int kThreads = 256;
-// Resident CTAs per SM (and so the register budget: 65536 / (256 * n)). fp32 sources and
-// NVFP4 hold more live values per lane.
-template <int FMT, bool F32>
-__host__ __device__ constexpr int ctas_per_sm() {
-  return F32 ? 2 : (FMT == BSQ_NVFP4 ? 3 : 4);
-}
-constexpr int kUnroll = 4;
-constexpr int kSeg = 256;  // elements per warp step
+constexpr int kThreads = 512;          // warp 0: TMA producer (lane 0); warps 1..15: consumers
+constexpr int kConsumerWarps = kThreads / 32 - 1;
+constexpr int kLaneElems = 16;         // elements per lane per step
+constexpr int kSeg = 32 * kLaneElems;   // elements per warp step
+constexpr int kRing = 6;                // chunk buffers per CTA
+constexpr int kCtasPerSm = 2;           // two resident CTAs: twice the warps to hide latency
+constexpr int kChunkMax = 16384;        // bytes per chunk buffer
+constexpr int kChunkMin = 4096;         // smallest chunk worth a copy (small tensors)
+constexpr int kAmaxThreads = 256;
 
 enum NvMode { kMx = 0, kNvComputed = 1, kNvGiven = 2 };
 
 struct QuantArgs {
-  const void* src;
+  const uint8_t* src;
   int64_t rows, cols;
   uint8_t* codes;
   uint8_t* scales;
   uint32_t* tail;       // NVFP4: {g, amax bits, 0, 0}
   const float* g_in;    // NVFP4 given-scale mode
   float* g_out;         // NVFP4 computed mode (nullable)
-  int64_t segs_per_row;
-  int64_t total_segs;
   int64_t nsc;          // scale columns per row
   int64_t nct;          // 4-column scale tiles per row
+  // chunking: either `rows_per_chunk` whole rows (cspan == cols) or one row piece of `cspan`
+  // elements (rows_per_chunk == 1, chunks_per_row pieces per row)
+  int64_t rows_per_chunk;
+  int64_t cspan;
+  int64_t chunks_per_row;
+  int64_t nchunks;
+  uint32_t cols_magic;  // floor(2^32 / cols) + 1: f / cols == umulhi(f, cols_magic) for f * cols < 2^32
+  int* status;
 };
+
+__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
 
 template <bool F32>
 struct Loaded {
-  uint4 v[F32 ? 2 : 1];
+  uint4 v[F32 ? 4 : 2];  // 16 elements
 };
 
 __device__ __forceinline__ float e4m3_to_f32(uint32_t c) {
@@ -64,28 +82,38 @@ __device__ __forceinline__ float e4m3_to_f32(uint32_t c) {
   return __uint_as_float(((E + 120u) << 23) | (m << 20));
 }
 
-// 8 source elements of one lane -> fp32 values and the max of their magnitude bits
+// 16 source elements of one lane -> fp32 values and the max of their magnitude bits
 // (bf16: 15-bit magnitudes, fp32: 31-bit magnitudes; both order like the values).
 template <bool F32>
-__device__ __forceinline__ void unpack8(const Loaded<F32>& L, float (&x)[8], uint32_t& mag_max) {
-  uint32_t mm = 0;
+__device__ __forceinline__ void unpack16(const Loaded<F32>& L, float (&x)[16], uint32_t& mag_max) {
   if constexpr (F32) {
-    const uint32_t w[8] = {L.v[0].x, L.v[0].y, L.v[0].z, L.v[0].w, L.v[1].x, L.v[1].y, L.v[1].z, L.v[1].w};
+    uint32_t mm = 0;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      x[i] = __uint_as_float(w[i]);
-      mm = max(mm, w[i] & 0x7FFFFFFFu);
+    for (int q = 0; q < 4; ++q) {
+      const uint32_t w[4] = {L.v[q].x, L.v[q].y, L.v[q].z, L.v[q].w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        x[4 * q + i] = __uint_as_float(w[i]);
+        mm = max(mm, w[i] & 0x7FFFFFFFu);
+      }
     }
+    mag_max = mm;
   } else {
-    const uint32_t w[4] = {L.v[0].x, L.v[0].y, L.v[0].z, L.v[0].w};
+    uint32_t m = 0;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      x[2 * i] = __uint_as_float(w[i] << 16);
-      x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-      mm = max(mm, max(w[i] & 0x7FFFu, (w[i] >> 16) & 0x7FFFu));
+    for (int q = 0; q < 2; ++q) {
+      const uint32_t w[4] = {L.v[q].x, L.v[q].y, L.v[q].z, L.v[q].w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        x[8 * q + 2 * i] = __uint_as_float(w[i] << 16);
+        x[8 * q + 2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+      }
+      // both 15-bit magnitudes of a word at once (unsigned 16-bit lanes)
+      m = max_u16x2(m, max_u16x2(max_u16x2(w[0] & 0x7FFF7FFFu, w[1] & 0x7FFF7FFFu),
+                                 max_u16x2(w[2] & 0x7FFF7FFFu, w[3] & 0x7FFF7FFFu)));
     }
+    mag_max = max(m & 0xFFFFu, m >> 16);
   }
-  mag_max = mm;
 }
 
 template <bool F32>
@@ -103,149 +131,204 @@ __device__ __forceinline__ int64_t scale_word_offset(int64_t r, int64_t c4, int6
   return ((r >> 7) * nct + (c4 >> 2)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4;
 }
 
-template <int FMT, bool F32, int NV>
-__global__ void __launch_bounds__(kThreads, (ctas_per_sm<FMT, F32>())) quantize_kernel(QuantArgs a) {
-  constexpr bool kFp4 = (FMT != BSQ_MXFP8);
-  constexpr int kLanesPerBlock = (FMT == BSQ_NVFP4) ? 2 : 4;
+// Quantize the 16 elements of one lane: `x` its values, `mag` the magnitude bits of the
+// lane's block (already reduced over the block's lanes). Writes the codes to `codes_dst` (16
+// E4M3 bytes or 8 e2m1 bytes) and returns the block's scale byte.
+template <int FMT, bool F32>
+__device__ __forceinline__ uint32_t quantize16(const float (&x)[16], uint32_t mag, float g, float six_g,
+                                               uint8_t* codes_dst) {
   constexpr uint32_t kEmax = (FMT == BSQ_MXFP8) ? 8u : 2u;
-  const uint32_t lane = threadIdx.x & 31u;
-  const int64_t warp = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
-  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * kThreads) >> 5;
-
-  float g = 0.f, six_g = 0.f;
-  if constexpr (NV != kMx) {
-    if constexpr (NV == kNvComputed) {
-      g = __fdiv_rn(__uint_as_float(a.tail[1]), 2688.0f);  // amax / (6 * 448)
-    } else {
-      g = *a.g_in;
-    }
-    six_g = __fmul_rn(6.0f, g);
-    if (blockIdx.x == 0 && threadIdx.x == 0) {
-      a.tail[0] = __float_as_uint(g);
-      if constexpr (NV == kNvComputed) {
-        if (a.g_out != nullptr) *a.g_out = g;
+  uint32_t sbyte;
+  if constexpr (FMT == BSQ_NVFP4) {
+    uint32_t scode = 0;
+    if (g != 0.0f) scode = cvt_e4m3x2(__fdiv_rn(mag_to_f32<F32>(mag), six_g), 0.0f) & 0xFFu;
+    sbyte = scode;
+    const float sc = e4m3_to_f32(scode);
+    const float sg = __fmul_rn(sc, g);
+    uint32_t w[2] = {0, 0};
+#pragma unroll
+    for (int i = 0; i < 16; i += 2) {
+      uint32_t c;
+      if (sc == 0.0f) {
+        c = ((__float_as_uint(x[i]) >> 31) << 3) | ((__float_as_uint(x[i + 1]) >> 31) << 7);
+      } else {
+        c = cvt_e2m1x2(__fdiv_rn(x[i], sg), __fdiv_rn(x[i + 1], sg));
       }
+      w[i >> 3] |= c << (4 * (i & 7));
+    }
+    *reinterpret_cast<uint2*>(codes_dst) = make_uint2(w[0], w[1]);
+  } else {
+    const uint32_t ef = exp_field<F32>(mag);
+    sbyte = ef > kEmax ? ef - kEmax : 0u;
+    const float mul = __uint_as_float((254u - sbyte) << 23);  // 2^(127 - sbyte), exact
+    float y[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) y[i] = x[i] * mul;
+    if constexpr (FMT == BSQ_MXFP8) {
+      uint32_t w[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) w[i] = cvt_e4m3x4(y[4 * i], y[4 * i + 1], y[4 * i + 2], y[4 * i + 3]);
+      *reinterpret_cast<uint4*>(codes_dst) = make_uint4(w[0], w[1], w[2], w[3]);
+    } else {
+      *reinterpret_cast<uint2*>(codes_dst) = make_uint2(cvt_e2m1x8(y), cvt_e2m1x8(y + 8));
     }
   }
-  uint32_t run_max = 0;  // NVFP4 given-scale mode: running magnitude max for the tail
+  return sbyte;
+}
 
-  // Work unit: one batch = up to kUnroll consecutive 256-element segments of one row. Warps
-  // walk the batches with a grid stride and prefetch the next batch's loads before working
-  // on the current one, so every warp keeps two batches of 16-byte loads in flight.
-  const uint32_t bpr = static_cast<uint32_t>((a.segs_per_row + kUnroll - 1) / kUnroll);
-  const uint32_t total = static_cast<uint32_t>(a.rows) * bpr;
-  auto load_batch = [&](uint32_t b, Loaded<F32> (&dst)[kUnroll]) {
-    const uint32_t row = b / bpr;
-    const int64_t seg0 = static_cast<int64_t>(b - row * bpr) * kUnroll;
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int64_t k0 = (seg0 + u) * kSeg + lane * 8;
-      if (k0 < a.cols) {
-        const int64_t e = static_cast<int64_t>(row) * a.cols + k0;
-        if constexpr (F32) {
-          const uint4* p = reinterpret_cast<const uint4*>(static_cast<const float*>(a.src) + e);
-          dst[u].v[0] = __ldcs(p);
-          dst[u].v[1] = __ldcs(p + 1);
-        } else {
-          dst[u].v[0] = __ldcs(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.src) + e));
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < (F32 ? 2 : 1); ++i) dst[u].v[i] = make_uint4(0, 0, 0, 0);
-      }
+template <int FMT, bool F32, int NV>
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) quantize_kernel(QuantArgs a) {
+  constexpr int kEsize = F32 ? 4 : 2;
+  extern __shared__ uint8_t q_smem_raw[];
+  uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(q_smem_raw) + 127) & ~uintptr_t(127));
+  __shared__ uint64_t full_bar[kRing], empty_bar[kRing];
+  __shared__ int abort_flag;
+  const uint32_t warp = threadIdx.x >> 5;
+  const uint32_t lane = threadIdx.x & 31u;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kRing; ++i) {
+      mbar_init(&full_bar[i], 1);
+      mbar_init(&empty_bar[i], kConsumerWarps);
+    }
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  // chunk c -> first row, rows, first column, columns
+  auto chunk_geom = [&](int64_t c, int64_t& r0, int64_t& nr, int64_t& c0, int64_t& nc) {
+    if (a.chunks_per_row > 1) {
+      r0 = c / a.chunks_per_row;
+      c0 = (c - r0 * a.chunks_per_row) * a.cspan;
+      nr = 1;
+      nc = min(a.cspan, a.cols - c0);
+    } else {
+      r0 = c * a.rows_per_chunk;
+      nr = min(a.rows_per_chunk, a.rows - r0);
+      c0 = 0;
+      nc = a.cols;
     }
   };
-  Loaded<F32> cur[kUnroll], nxt[kUnroll];
-  uint32_t b = static_cast<uint32_t>(warp);
-  if (b < total) load_batch(b, cur);
-  for (; b < total; b += static_cast<uint32_t>(nwarps)) {
-    const uint32_t bn = b + static_cast<uint32_t>(nwarps);
-    if (bn < total) load_batch(bn, nxt);
-    const uint32_t row = b / bpr;
-    const int64_t seg0 = static_cast<int64_t>(b - row * bpr) * kUnroll;
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      if (seg0 + u >= a.segs_per_row) break;  // warp-uniform
-      const int64_t brow = row;
-      const int64_t bk0 = (seg0 + u) * kSeg + lane * 8;
-      const bool blive = bk0 < a.cols;
-      float x[8];
-      uint32_t mag;
-      unpack8<F32>(cur[u], x, mag);
-      // block maximum across the lanes of one block
-      mag = max(mag, __shfl_xor_sync(0xFFFFFFFFu, mag, 1));
-      if (kLanesPerBlock == 4) mag = max(mag, __shfl_xor_sync(0xFFFFFFFFu, mag, 2));
-      if constexpr (NV == kNvGiven) run_max = max(run_max, mag);
 
-      uint32_t sbyte;
-      uint32_t code_lo = 0, code_hi = 0;
-      if constexpr (FMT == BSQ_NVFP4) {
-        uint32_t scode = 0;
-        if (g != 0.0f) scode = cvt_e4m3x2(__fdiv_rn(mag_to_f32<F32>(mag), six_g), 0.0f) & 0xFFu;
-        sbyte = scode;
-        const float s = e4m3_to_f32(scode);
-        const float sg = __fmul_rn(s, g);
-#pragma unroll
-        for (int i = 0; i < 8; i += 2) {
-          uint32_t c;
-          if (s == 0.0f) {
-            c = ((__float_as_uint(x[i]) >> 31) << 3) | ((__float_as_uint(x[i + 1]) >> 31) << 7);
-          } else {
-            c = cvt_e2m1x2(__fdiv_rn(x[i], sg), __fdiv_rn(x[i + 1], sg));
-          }
-          code_lo |= c << (4 * i);
-        }
-      } else {
-        const uint32_t ef = exp_field<F32>(mag);
-        sbyte = ef > kEmax ? ef - kEmax : 0u;
-        const float mul = __uint_as_float((254u - sbyte) << 23);  // 2^(127 - sbyte), exact
-        if constexpr (FMT == BSQ_MXFP8) {
-          code_lo = cvt_e4m3x2(x[0] * mul, x[1] * mul) | (cvt_e4m3x2(x[2] * mul, x[3] * mul) << 16);
-          code_hi = cvt_e4m3x2(x[4] * mul, x[5] * mul) | (cvt_e4m3x2(x[6] * mul, x[7] * mul) << 16);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 8; i += 2) code_lo |= cvt_e2m1x2(x[i] * mul, x[i + 1] * mul) << (4 * i);
-        }
-      }
-
-      if (blive) {
-        const int64_t e = brow * a.cols + bk0;
-        if constexpr (kFp4) {
-          *reinterpret_cast<uint32_t*>(a.codes + (e >> 1)) = code_lo;
-        } else {
-          *reinterpret_cast<uint2*>(a.codes + e) = make_uint2(code_lo, code_hi);
-        }
-      } else {
-        sbyte = 0;  // padding scale columns of a partial segment hold 0
-      }
-      // gather 4 consecutive block scales into one word: blocks are kLanesPerBlock lanes apart
-      const uint32_t s1 = __shfl_down_sync(0xFFFFFFFFu, sbyte, kLanesPerBlock);
-      const uint32_t s2 = __shfl_down_sync(0xFFFFFFFFu, sbyte, 2 * kLanesPerBlock);
-      const uint32_t s3 = __shfl_down_sync(0xFFFFFFFFu, sbyte, 3 * kLanesPerBlock);
-      if ((lane % (4 * kLanesPerBlock)) == 0) {
-        const int64_t seg_k0 = bk0 - lane * 8;
-        const int64_t c4 = seg_k0 / (FMT == BSQ_NVFP4 ? 16 : 32) + lane / kLanesPerBlock;
-        if (c4 < a.nsc) {
-          const uint32_t word = sbyte | (s1 << 8) | (s2 << 16) | (s3 << 24);
-          *reinterpret_cast<uint32_t*>(a.scales + scale_word_offset(brow, c4, a.nct)) = word;
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int64_t c = blockIdx.x; c < a.nchunks; c += gridDim.x) {
+        if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1u, &abort_flag, a.status)) break;
+        int64_t r0, nr, c0, nc;
+        chunk_geom(c, r0, nr, c0, nc);
+        const uint32_t bytes = static_cast<uint32_t>(nr * nc * kEsize);
+        mbar_arrive_expect_tx(&full_bar[stage], bytes);
+        bulk_load(ring + stage * kChunkMax, a.src + (r0 * a.cols + c0) * kEsize, bytes, &full_bar[stage]);
+        if (++stage == kRing) {
+          stage = 0;
+          phase ^= 1u;
         }
       }
     }
+  } else {
+    // ------------------------------------------------------------ consumers
+    float g = 0.f, six_g = 0.f;
+    if constexpr (NV != kMx) {
+      if constexpr (NV == kNvComputed) {
+        g = __fdiv_rn(__uint_as_float(a.tail[1]), 2688.0f);  // amax / (6 * 448)
+      } else {
+        g = *a.g_in;
+      }
+      six_g = __fmul_rn(6.0f, g);
+      if (blockIdx.x == 0 && threadIdx.x == 32) {
+        a.tail[0] = __float_as_uint(g);
+        if constexpr (NV == kNvComputed) {
+          if (a.g_out != nullptr) *a.g_out = g;
+        }
+      }
+    }
+    uint32_t run_max = 0;  // NVFP4 given-scale mode: running magnitude max for the tail
+    const int cw = static_cast<int>(warp) - 1;
+    // Warp steps are dealt round-robin over the concatenation of the CTA's chunks (not per
+    // chunk), so that a chunk whose step count is not a multiple of the warp count does not
+    // give the same warps an extra step every time. `lead`: this warp's first step in the
+    // current chunk.
+    uint32_t lead = static_cast<uint32_t>(cw);
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int64_t c = blockIdx.x; c < a.nchunks; c += gridDim.x) {
+      if (!mbar_wait_bounded_warp(&full_bar[stage], phase, &abort_flag, a.status)) break;
+      int64_t r0, nr, c0, nc;
+      chunk_geom(c, r0, nr, c0, nc);
+      const uint8_t* buf = ring + stage * kChunkMax;
+      // the chunk as one flat array of nr * nc elements; lane piece f = 16 elements
+      const uint32_t flat = static_cast<uint32_t>(nr * nc);
+      const uint64_t elem0 = static_cast<uint64_t>(r0) * static_cast<uint64_t>(a.cols) + static_cast<uint64_t>(c0);
+      const uint32_t steps = (flat + kSeg - 1) / kSeg;
+      for (uint32_t base = lead * kSeg; base < flat; base += kConsumerWarps * kSeg) {
+        const uint32_t f = base + lane * kLaneElems;
+        const bool live = f < flat;
+        Loaded<F32> in;
+        if (live) {
+          const uint4* p = reinterpret_cast<const uint4*>(buf + f * kEsize);
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) cur[u] = nxt[u];
+          for (int i = 0; i < (F32 ? 4 : 2); ++i) in.v[i] = p[i];
+        } else {
+#pragma unroll
+          for (int i = 0; i < (F32 ? 4 : 2); ++i) in.v[i] = make_uint4(0, 0, 0, 0);
+        }
+        float x[16];
+        uint32_t mag;
+        unpack16<F32>(in, x, mag);
+        if constexpr (FMT != BSQ_NVFP4) mag = max(mag, __shfl_xor_sync(0xFFFFFFFFu, mag, 1));  // 1x32 block = 2 lanes
+        if constexpr (NV == kNvGiven) run_max = max(run_max, mag);
+        if (live) {
+          const uint64_t e = elem0 + f;
+          const uint32_t sbyte = quantize16<FMT, F32>(x, mag, g, six_g, a.codes + (FMT == BSQ_MXFP8 ? e : e >> 1));
+          if (FMT == BSQ_NVFP4 || (lane & 1u) == 0) {
+            // row and scale column of this block (32-bit: rows and columns stay below 2^31,
+            // and the number of 512-byte scale tiles below 2^32)
+            const uint32_t rr = nr > 1 ? __umulhi(f, a.cols_magic) : 0u;
+            const uint32_t row = static_cast<uint32_t>(r0) + rr;
+            const uint32_t col = static_cast<uint32_t>(c0) + (f - rr * static_cast<uint32_t>(nc));
+            const uint32_t sc = col >> (FMT == BSQ_NVFP4 ? 4 : 5);
+            const uint32_t tile = (row >> 7) * static_cast<uint32_t>(a.nct) + (sc >> 2);
+            uint8_t* sp = a.scales + static_cast<uint64_t>(tile) * 512 +
+                          (((row & 31u) << 4) | (((row >> 5) & 3u) << 2) | (sc & 3u));
+            *sp = static_cast<uint8_t>(sbyte);
+            if (sc + 1 == static_cast<uint32_t>(a.nsc)) {
+              // padding columns of the row's last 4-column group read 0
+              for (uint32_t j = (sc & 3u) + 1; j < 4; ++j) sp[j - (sc & 3u)] = 0;
+            }
+          }
+        }
+      }
+      // first step in the next chunk: continue the round-robin where this chunk ended
+      lead = (lead + (kConsumerWarps - steps % kConsumerWarps)) % kConsumerWarps;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty_bar[stage]);
+      if (++stage == kRing) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+
+    if constexpr (NV == kNvGiven) {
+      // per-warp maximum of |x| -> tail word 1 (the amax of this tensor)
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) run_max = max(run_max, __shfl_xor_sync(0xFFFFFFFFu, run_max, o));
+      if (lane == 0 && run_max != 0) atomicMax(&a.tail[1], __float_as_uint(mag_to_f32<F32>(run_max)));
+    }
   }
 
-  if constexpr (NV == kNvGiven) {
-    // per-CTA maximum of |x| -> tail word 1 (the amax of this tensor)
-    __shared__ uint32_t red[kThreads / 32];
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) run_max = max(run_max, __shfl_xor_sync(0xFFFFFFFFu, run_max, o));
-    if (lane == 0) red[threadIdx.x >> 5] = run_max;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      uint32_t m = 0;
-      for (int i = 0; i < kThreads / 32; ++i) m = max(m, red[i]);
-      atomicMax(&a.tail[1], __float_as_uint(mag_to_f32<F32>(m)));
+  // scale bytes of the padding rows of the last row tile read 0
+  const int64_t pad_rows = (128 - a.rows % 128) % 128;
+  if (pad_rows > 0) {
+    const int64_t words = pad_rows * a.nct;
+    const int64_t r_first = a.rows;
+    for (int64_t w = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; w < words;
+         w += static_cast<int64_t>(gridDim.x) * kThreads) {
+      const int64_t r = r_first + w / a.nct, t = w % a.nct;
+      *reinterpret_cast<uint32_t*>(a.scales + scale_word_offset(r, 4 * t, a.nct)) = 0u;
     }
   }
 }
@@ -254,11 +337,11 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<FMT, F32>())) quantize_
 // (non-negative floats order like their bit patterns). Reads use the default cache policy
 // so that the quantize pass that follows finds the tensor in L2 when it fits.
 template <bool F32>
-__global__ void __launch_bounds__(kThreads) amax_kernel(const uint4* src, int64_t nvec, uint32_t* out) {
+__global__ void __launch_bounds__(kAmaxThreads) amax_kernel(const uint4* src, int64_t nvec, uint32_t* out) {
   constexpr int kU = 4;
   uint32_t m = 0;
-  const int64_t tid = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
-  const int64_t nthr = static_cast<int64_t>(gridDim.x) * kThreads;
+  const int64_t tid = static_cast<int64_t>(blockIdx.x) * kAmaxThreads + threadIdx.x;
+  const int64_t nthr = static_cast<int64_t>(gridDim.x) * kAmaxThreads;
   for (int64_t i = tid; i < nvec; i += nthr * kU) {
     uint4 v[kU];
 #pragma unroll
@@ -279,21 +362,26 @@ __global__ void __launch_bounds__(kThreads) amax_kernel(const uint4* src, int64_
       }
     }
   }
-  __shared__ uint32_t red[kThreads / 32];
+  __shared__ uint32_t red[kAmaxThreads / 32];
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
   __syncthreads();
   if (threadIdx.x == 0) {
     uint32_t b = 0;
-    for (int i = 0; i < kThreads / 32; ++i) b = max(b, red[i]);
+    for (int i = 0; i < kAmaxThreads / 32; ++i) b = max(b, red[i]);
     atomicMax(out, F32 ? b : (b << 16));
   }
 }
 
+constexpr int kQuantSmem = kRing * kChunkMax + 128;
+
 template <int FMT, bool F32, int NV>
 cudaError_t launch_q(const QuantArgs& a, int grid, cudaStream_t stream) {
-  quantize_kernel<FMT, F32, NV><<<grid, kThreads, 0, stream>>>(a);
+  static cudaError_t attr = cudaFuncSetAttribute(quantize_kernel<FMT, F32, NV>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kQuantSmem);
+  if (attr != cudaSuccess) return attr;
+  quantize_kernel<FMT, F32, NV><<<grid, kThreads, kQuantSmem, stream>>>(a);
   return cudaGetLastError();
 }
 
@@ -302,45 +390,48 @@ cudaError_t launch_q(const QuantArgs& a, int grid, cudaStream_t stream) {
 int launch_quantize(int fmt, bool src_f32, bool global_given, const void* src, int64_t rows, int64_t cols,
                     void* codes, void* scales, float* global_scale, cudaStream_t stream, const DeviceInfo& dev) {
   QuantArgs a{};
-  a.src = src;
+  a.src = static_cast<const uint8_t*>(src);
   a.rows = rows;
   a.cols = cols;
   a.codes = static_cast<uint8_t*>(codes);
   a.scales = static_cast<uint8_t*>(scales);
   a.nsc = cols / block_size(fmt);
   a.nct = ceil_div(a.nsc, 4);
-  a.segs_per_row = ceil_div(cols, kSeg);
-  a.total_segs = rows * a.segs_per_row;
+  a.status = dev.status;
+  a.cols_magic = static_cast<uint32_t>((uint64_t{1} << 32) / static_cast<uint64_t>(cols) + 1);
+  const int64_t esize = src_f32 ? 4 : 2;
+  const int64_t row_bytes = cols * esize;
   const int64_t body = scales_body_bytes(fmt, rows, cols);
 
-  // Padding scale bytes must read 0. Padding columns of real rows are written (as zero
-  // bytes inside the last scale word of a row); padding rows of the last row tile are not,
-  // so that tile row is cleared first.
-  cudaError_t err = cudaSuccess;
-  if (rows % 128 != 0) {
-    const int64_t last = (rows / 128) * a.nct * 512;
-    err = cudaMemsetAsync(a.scales + last, 0, static_cast<size_t>(body - last), stream);
+  // Chunk size: at most one ring buffer, and small enough that every SM gets a few chunks
+  // (a 5 MB matrix is then still spread over all SMs and copied in parallel).
+  const int64_t total_bytes = rows * row_bytes;
+  const int64_t target =
+      std::max<int64_t>(kChunkMin, std::min<int64_t>(kChunkMax, total_bytes / (4 * kCtasPerSm * static_cast<int64_t>(dev.num_sms))));
+  if (row_bytes <= target) {
+    a.rows_per_chunk = target / row_bytes;
+    a.cspan = cols;
+    a.chunks_per_row = 1;
+    a.nchunks = ceil_div(rows, a.rows_per_chunk);
+  } else {
+    a.rows_per_chunk = 1;
+    a.cspan = std::max<int64_t>(1, kChunkMax / (esize * kSeg)) * kSeg;  // whole segments per piece
+    a.chunks_per_row = ceil_div(cols, a.cspan);
+    a.nchunks = rows * a.chunks_per_row;
   }
-  if (err != cudaSuccess) return BSQ_ERR_LAUNCH;
+  const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(a.nchunks, kCtasPerSm * dev.num_sms)));
 
-  // Persistent grid: as many CTAs as stay resident (a second wave would serialise a kernel
-  // that lasts only a few microseconds), never more than there are batches of work.
-  const int64_t batches = rows * ceil_div(a.segs_per_row, kUnroll);
-  const int per_sm = fmt == BSQ_NVFP4 ? (src_f32 ? ctas_per_sm<BSQ_NVFP4, true>() : ctas_per_sm<BSQ_NVFP4, false>())
-                                      : (src_f32 ? ctas_per_sm<BSQ_MXFP8, true>() : ctas_per_sm<BSQ_MXFP8, false>());
-  const int64_t max_grid = static_cast<int64_t>(dev.num_sms) * per_sm;
-  const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(ceil_div(batches, kThreads / 32), max_grid)));
-
+  cudaError_t err = cudaSuccess;
   if (fmt == BSQ_NVFP4) {
     a.tail = reinterpret_cast<uint32_t*>(a.scales + body);
     a.g_in = global_scale;
     a.g_out = global_scale;
     if (cudaMemsetAsync(a.tail, 0, 16, stream) != cudaSuccess) return BSQ_ERR_LAUNCH;
     if (!global_given) {
-      const int64_t nvec = rows * cols * (src_f32 ? 4 : 2) / 16;
-      const int agrid = static_cast<int>(std::min<int64_t>(ceil_div(nvec, kThreads * 4), max_grid));
-      if (src_f32) amax_kernel<true><<<agrid, kThreads, 0, stream>>>(static_cast<const uint4*>(src), nvec, a.tail + 1);
-      else amax_kernel<false><<<agrid, kThreads, 0, stream>>>(static_cast<const uint4*>(src), nvec, a.tail + 1);
+      const int64_t nvec = rows * cols * esize / 16;
+      const int agrid = static_cast<int>(std::min<int64_t>(ceil_div(nvec, kAmaxThreads * 4), dev.num_sms * 8));
+      if (src_f32) amax_kernel<true><<<agrid, kAmaxThreads, 0, stream>>>(static_cast<const uint4*>(src), nvec, a.tail + 1);
+      else amax_kernel<false><<<agrid, kAmaxThreads, 0, stream>>>(static_cast<const uint4*>(src), nvec, a.tail + 1);
       if (cudaGetLastError() != cudaSuccess) return BSQ_ERR_LAUNCH;
       err = src_f32 ? launch_q<BSQ_NVFP4, true, kNvComputed>(a, grid, stream)
                     : launch_q<BSQ_NVFP4, false, kNvComputed>(a, grid, stream);

@@ -93,7 +93,8 @@ size_t bsq_scales_bytes(int fmt, int64_t rows, int64_t cols);
  *          [-127, 127], amax = 0 -> -127; scale byte e + 127; code = RNE_sat(x * 2^-e).
  *   NVFP4  s = E4M3 RNE_sat(bamax / (6 g)); code = e2m1 RNE_sat(x / (s g)), each step one
  *          IEEE fp32 operation; s = 0 gives zero codes carrying the sign of x.
- * Shapes: cols % 32 == 0 (MX) or cols % 16 == 0 (NVFP4), else BSQ_ERR_SHAPE; any rows >= 1.
+ * Shapes: cols % 32 == 0 (MX) or cols % 16 == 0 (NVFP4), rows and cols below 2^31, else
+ * BSQ_ERR_SHAPE; any rows >= 1.
  * Codes and scales are bit-exact functions of the input (no dependence on launch shape).
  */
 int bsq_quantize(int fmt_flags, const void* src, int64_t rows, int64_t cols, void* codes, void* scales,

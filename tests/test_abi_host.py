@@ -63,6 +63,8 @@ def test_argument_errors_before_any_cuda_call(bsq):
     assert bsq.bsq_quantize(bsq.MXFP8, p, 0, 32, p, p) == bsq.ERR_ARG
     assert bsq.bsq_quantize(bsq.MXFP8, p, 4, 48, p, p) == bsq.ERR_SHAPE                # 48 % 32
     assert bsq.bsq_quantize(bsq.NVFP4, p, 4, 40, p, p) == bsq.ERR_SHAPE                # 40 % 16
+    assert bsq.bsq_quantize(bsq.MXFP8, p, 1 << 31, 32, p, p) == bsq.ERR_SHAPE          # rows >= 2^31
+    assert bsq.bsq_quantize(bsq.MXFP8, p, 4, 1 << 31, p, p) == bsq.ERR_SHAPE           # cols >= 2^31
     assert bsq.bsq_quantize(bsq.NVFP4 | bsq.FLAG_GLOBAL_GIVEN, p, 4, 32, p, p, None) == bsq.ERR_ARG
     assert bsq.bsq_quantize(bsq.MXFP8 | bsq.FLAG_GLOBAL_GIVEN, p, 4, 32, p, p, p) == bsq.ERR_ARG
     assert bsq.bsq_quantize(bsq.MXFP8, p + 8, 4, 32, p, p) == bsq.ERR_ALIGN
