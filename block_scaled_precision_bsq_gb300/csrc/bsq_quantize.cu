@@ -65,12 +65,6 @@ struct QuantArgs {
   int* status;
 };
 
-__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
-}
-
 template <bool F32>
 struct Loaded {
   uint4 v[F32 ? 4 : 2];  // 16 elements
@@ -82,24 +76,20 @@ __device__ __forceinline__ float e4m3_to_f32(uint32_t c) {
   return __uint_as_float(((E + 120u) << 23) | (m << 20));
 }
 
-// 16 source elements of one lane -> fp32 values and the max of their magnitude bits
-// (bf16: 15-bit magnitudes, fp32: 31-bit magnitudes; both order like the values).
+// 16 source elements of one lane -> fp32 values and their largest magnitude. The maximum
+// starts at 0 and skips NaN (fmaxf returns the other operand), as a block maximum taken with
+// "if (|x| > amax) amax = |x|" does.
 template <bool F32>
-__device__ __forceinline__ void unpack16(const Loaded<F32>& L, float (&x)[16], uint32_t& mag_max) {
+__device__ __forceinline__ void unpack16(const Loaded<F32>& L, float (&x)[16], float& amax) {
   if constexpr (F32) {
-    uint32_t mm = 0;
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      const uint32_t w[4] = {L.v[q].x, L.v[q].y, L.v[q].z, L.v[q].w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        x[4 * q + i] = __uint_as_float(w[i]);
-        mm = max(mm, w[i] & 0x7FFFFFFFu);
-      }
+      x[4 * q + 0] = __uint_as_float(L.v[q].x);
+      x[4 * q + 1] = __uint_as_float(L.v[q].y);
+      x[4 * q + 2] = __uint_as_float(L.v[q].z);
+      x[4 * q + 3] = __uint_as_float(L.v[q].w);
     }
-    mag_max = mm;
   } else {
-    uint32_t m = 0;
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
       const uint32_t w[4] = {L.v[q].x, L.v[q].y, L.v[q].z, L.v[q].w};
@@ -108,22 +98,14 @@ __device__ __forceinline__ void unpack16(const Loaded<F32>& L, float (&x)[16], u
         x[8 * q + 2 * i] = __uint_as_float(w[i] << 16);
         x[8 * q + 2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
       }
-      // both 15-bit magnitudes of a word at once (unsigned 16-bit lanes)
-      m = max_u16x2(m, max_u16x2(max_u16x2(w[0] & 0x7FFF7FFFu, w[1] & 0x7FFF7FFFu),
-                                 max_u16x2(w[2] & 0x7FFF7FFFu, w[3] & 0x7FFF7FFFu)));
     }
-    mag_max = max(m & 0xFFFFu, m >> 16);
   }
-}
-
-template <bool F32>
-__device__ __forceinline__ uint32_t exp_field(uint32_t mag) {
-  return F32 ? (mag >> 23) : (mag >> 7);
-}
-
-template <bool F32>
-__device__ __forceinline__ float mag_to_f32(uint32_t mag) {
-  return F32 ? __uint_as_float(mag) : __uint_as_float(mag << 16);
+  float m[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) m[i] = fmaxf(fabsf(x[2 * i]), fabsf(x[2 * i + 1]));
+#pragma unroll
+  for (int i = 0; i < 4; ++i) m[i] = fmaxf(m[i], m[i + 4]);
+  amax = fmaxf(fmaxf(0.0f, fmaxf(m[0], m[2])), fmaxf(m[1], m[3]));
 }
 
 // Byte offset of the 32-bit scale word holding scale columns [c4, c4 + 4) of row r.
@@ -131,17 +113,17 @@ __device__ __forceinline__ int64_t scale_word_offset(int64_t r, int64_t c4, int6
   return ((r >> 7) * nct + (c4 >> 2)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4;
 }
 
-// Quantize the 16 elements of one lane: `x` its values, `mag` the magnitude bits of the
+// Quantize the 16 elements of one lane: `x` its values, `amax` the largest magnitude of the
 // lane's block (already reduced over the block's lanes). Writes the codes to `codes_dst` (16
 // E4M3 bytes or 8 e2m1 bytes) and returns the block's scale byte.
-template <int FMT, bool F32>
-__device__ __forceinline__ uint32_t quantize16(const float (&x)[16], uint32_t mag, float g, float six_g,
+template <int FMT>
+__device__ __forceinline__ uint32_t quantize16(const float (&x)[16], float amax, float g, float six_g,
                                                uint8_t* codes_dst) {
   constexpr uint32_t kEmax = (FMT == BSQ_MXFP8) ? 8u : 2u;
   uint32_t sbyte;
   if constexpr (FMT == BSQ_NVFP4) {
     uint32_t scode = 0;
-    if (g != 0.0f) scode = cvt_e4m3x2(__fdiv_rn(mag_to_f32<F32>(mag), six_g), 0.0f) & 0xFFu;
+    if (g != 0.0f) scode = cvt_e4m3x2(__fdiv_rn(amax, six_g), 0.0f) & 0xFFu;
     sbyte = scode;
     const float sc = e4m3_to_f32(scode);
     const float sg = __fmul_rn(sc, g);
@@ -158,7 +140,7 @@ __device__ __forceinline__ uint32_t quantize16(const float (&x)[16], uint32_t ma
     }
     *reinterpret_cast<uint2*>(codes_dst) = make_uint2(w[0], w[1]);
   } else {
-    const uint32_t ef = exp_field<F32>(mag);
+    const uint32_t ef = __float_as_uint(amax) >> 23;  // biased exponent of the block maximum
     sbyte = ef > kEmax ? ef - kEmax : 0u;
     const float mul = __uint_as_float((254u - sbyte) << 23);  // 2^(127 - sbyte), exact
     float y[16];
@@ -246,7 +228,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) quantize_kernel(QuantArg
         }
       }
     }
-    uint32_t run_max = 0;  // NVFP4 given-scale mode: running magnitude max for the tail
+    uint32_t run_max = 0;  // NVFP4 given-scale mode: running max |x| (fp32 bits) for the tail
     const int cw = static_cast<int>(warp) - 1;
     // Warp steps are dealt round-robin over the concatenation of the CTA's chunks (not per
     // chunk), so that a chunk whose step count is not a multiple of the warp count does not
@@ -277,13 +259,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) quantize_kernel(QuantArg
           for (int i = 0; i < (F32 ? 4 : 2); ++i) in.v[i] = make_uint4(0, 0, 0, 0);
         }
         float x[16];
-        uint32_t mag;
-        unpack16<F32>(in, x, mag);
-        if constexpr (FMT != BSQ_NVFP4) mag = max(mag, __shfl_xor_sync(0xFFFFFFFFu, mag, 1));  // 1x32 block = 2 lanes
-        if constexpr (NV == kNvGiven) run_max = max(run_max, mag);
+        float amax;
+        unpack16<F32>(in, x, amax);
+        if constexpr (FMT != BSQ_NVFP4) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));  // 1x32 block = 2 lanes
+        if constexpr (NV == kNvGiven) run_max = max(run_max, __float_as_uint(amax));
         if (live) {
           const uint64_t e = elem0 + f;
-          const uint32_t sbyte = quantize16<FMT, F32>(x, mag, g, six_g, a.codes + (FMT == BSQ_MXFP8 ? e : e >> 1));
+          const uint32_t sbyte = quantize16<FMT>(x, amax, g, six_g, a.codes + (FMT == BSQ_MXFP8 ? e : e >> 1));
           if (FMT == BSQ_NVFP4 || (lane & 1u) == 0) {
             // row and scale column of this block (32-bit: rows and columns stay below 2^31,
             // and the number of 512-byte scale tiles below 2^32)
@@ -316,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) quantize_kernel(QuantArg
       // per-warp maximum of |x| -> tail word 1 (the amax of this tensor)
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) run_max = max(run_max, __shfl_xor_sync(0xFFFFFFFFu, run_max, o));
-      if (lane == 0 && run_max != 0) atomicMax(&a.tail[1], __float_as_uint(mag_to_f32<F32>(run_max)));
+      if (lane == 0 && run_max != 0) atomicMax(&a.tail[1], run_max);
     }
   }
 
@@ -333,13 +315,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) quantize_kernel(QuantArg
   }
 }
 
-// Tensor amax (NVFP4 computed-scale mode): max |x| -> atomicMax on the fp32 bits at `out`
-// (non-negative floats order like their bit patterns). Reads use the default cache policy
-// so that the quantize pass that follows finds the tensor in L2 when it fits.
+// Tensor amax (NVFP4 computed-scale mode): max |x| over the tensor, NaN skipped like the block
+// maxima -> atomicMax on the fp32 bits at `out` (non-negative floats order like their bit
+// patterns). Reads use the default cache policy so that the quantize pass that follows finds
+// the tensor in L2 when it fits.
 template <bool F32>
 __global__ void __launch_bounds__(kAmaxThreads) amax_kernel(const uint4* src, int64_t nvec, uint32_t* out) {
   constexpr int kU = 4;
-  uint32_t m = 0;
+  float m = 0.0f;
   const int64_t tid = static_cast<int64_t>(blockIdx.x) * kAmaxThreads + threadIdx.x;
   const int64_t nthr = static_cast<int64_t>(gridDim.x) * kAmaxThreads;
   for (int64_t i = tid; i < nvec; i += nthr * kU) {
@@ -355,22 +338,22 @@ __global__ void __launch_bounds__(kAmaxThreads) amax_kernel(const uint4* src, in
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         if constexpr (F32) {
-          m = max(m, w[q] & 0x7FFFFFFFu);
+          m = fmaxf(m, fabsf(__uint_as_float(w[q])));
         } else {
-          m = max(m, max(w[q] & 0x7FFFu, (w[q] >> 16) & 0x7FFFu));
+          m = fmaxf(m, fmaxf(fabsf(__uint_as_float(w[q] << 16)), fabsf(__uint_as_float(w[q] & 0xFFFF0000u))));
         }
       }
     }
   }
-  __shared__ uint32_t red[kAmaxThreads / 32];
+  __shared__ float red[kAmaxThreads / 32];
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
   __syncthreads();
   if (threadIdx.x == 0) {
-    uint32_t b = 0;
-    for (int i = 0; i < kAmaxThreads / 32; ++i) b = max(b, red[i]);
-    atomicMax(out, F32 ? b : (b << 16));
+    float b = 0.0f;
+    for (int i = 0; i < kAmaxThreads / 32; ++i) b = fmaxf(b, red[i]);
+    atomicMax(out, __float_as_uint(b));
   }
 }
 
