@@ -28,6 +28,14 @@ __device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31u; }
 
 __device__ __forceinline__ bool elect_lane0() { return (threadIdx.x & 31u) == 0u; }
 
+// Programmatic dependent launch. A kernel launched with programmatic stream serialization
+// may start while the previous kernel in the stream is still running; grid_dependency_wait()
+// blocks until that kernel has completed and its memory operations are visible, so every
+// global read of inputs and every global write must come after it. launch_dependents() lets
+// the next kernel in the stream be launched (it waits the same way before touching memory).
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // One lane of the (converged) warp, chosen by elect.sync. The warp's other lanes keep running the
 // same loop, so addresses and descriptors computed there stay warp-uniform.
 __device__ __forceinline__ bool elect_one_sync() {

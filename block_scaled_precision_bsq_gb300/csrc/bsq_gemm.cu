@@ -178,6 +178,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   cluster_sync_all();  // barriers of both CTAs initialised before any remote arrival
   tc_fence_after();
+  launch_dependents();
+  grid_dependency_wait();  // the operands (and the output buffer) may belong to the previous kernel until here
   const uint32_t tmem_base = *tmem_holder;
   const int first_pair = static_cast<int>(cluster_id_x());
   const int pair_stride = static_cast<int>(num_clusters_x());
@@ -425,19 +427,24 @@ bool make_map_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uin
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Launch as (2,1,1) clusters; with programmatic stream serialization the kernel may be
+// launched while the previous kernel in the stream finishes (it waits for it before touching
+// memory). `attr` holds two entries.
 cudaLaunchConfig_t pair_launch_config(cudaLaunchAttribute* attr, int clusters, int threads, int smem,
                                       cudaStream_t stream) {
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * clusters);
   cfg.blockDim = dim3(threads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cfg;
 }
 
@@ -450,7 +457,7 @@ int run_gemm(const void* A, const void* A_scales, const void* B, const void* B_s
   std::call_once(attr_once, [] {
     attr_err = cudaFuncSetAttribute(gemm_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<FMT>::alloc);
     if (attr_err != cudaSuccess) return;
-    cudaLaunchAttribute at[1];
+    cudaLaunchAttribute at[2];
     cudaLaunchConfig_t cfg = pair_launch_config(at, 1, kThreads, Smem<FMT>::alloc, nullptr);
     attr_err = cudaOccupancyMaxActiveClusters(&max_clusters, gemm_kernel<FMT>, &cfg);
     if (attr_err == cudaSuccess && max_clusters < 1) attr_err = cudaErrorInvalidConfiguration;
@@ -482,7 +489,7 @@ int run_gemm(const void* A, const void* A_scales, const void* B, const void* B_s
   a.status = dev.status;
   const int clusters = std::min(a.num_pairs, std::min(max_clusters, dev.num_sms / 2));
 
-  cudaLaunchAttribute at[1];
+  cudaLaunchAttribute at[2];
   cudaLaunchConfig_t cfg = pair_launch_config(at, clusters, kThreads, Smem<FMT>::alloc, stream);
   if (cudaLaunchKernelEx(&cfg, gemm_kernel<FMT>, mA, mB, mSfa, mSfb, mOut, a) != cudaSuccess) return BSQ_ERR_LAUNCH;
   return cudaGetLastError() == cudaSuccess ? BSQ_OK : BSQ_ERR_LAUNCH;

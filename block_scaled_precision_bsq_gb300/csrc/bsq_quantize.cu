@@ -177,6 +177,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) quantize_kernel(QuantArg
     fence_mbar_init();
   }
   __syncthreads();
+  launch_dependents();
+  grid_dependency_wait();  // inputs and outputs may belong to the previous kernel until here
 
   // chunk c -> first row, rows, first column, columns
   auto chunk_geom = [&](int64_t c, int64_t& r0, int64_t& nr, int64_t& c0, int64_t& nc) {
@@ -364,8 +366,19 @@ cudaError_t launch_q(const QuantArgs& a, int grid, cudaStream_t stream) {
   static cudaError_t attr = cudaFuncSetAttribute(quantize_kernel<FMT, F32, NV>,
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, kQuantSmem);
   if (attr != cudaSuccess) return attr;
-  quantize_kernel<FMT, F32, NV><<<grid, kThreads, kQuantSmem, stream>>>(a);
-  return cudaGetLastError();
+  // programmatic dependent launch: the kernel may be launched while the previous kernel in
+  // the stream finishes; it waits for it (grid_dependency_wait) before touching memory
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kQuantSmem;
+  cfg.stream = stream;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, quantize_kernel<FMT, F32, NV>, a);
 }
 
 }  // namespace
