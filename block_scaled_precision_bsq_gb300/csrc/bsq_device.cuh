@@ -13,6 +13,7 @@ namespace bsq {
 // Longest time any mbarrier wait may take before the kernel gives up (nanoseconds of
 // %globaltimer). A healthy wait in these kernels lasts microseconds.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr uint32_t kWaitSuspendHintNs = 20000;  // one suspended try_wait: at most 20 us
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -76,6 +77,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity
   return ok != 0;
 }
 
+// try_wait with a suspend-time hint: a waiting thread sleeps until the phase completes (or
+// the hint expires) instead of spinning and taking issue slots from the working warps.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar_addr, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar_addr), "r"(parity), "r"(kWaitSuspendHintNs)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait until the phase with the given parity has completed. Gives up when `*abort` becomes
 // non-zero (another role gave up) or after `limit_ns`; on a timeout it raises `*abort`,
 // records BSQ_ERR_TIMEOUT in the device status word and returns false.
@@ -85,8 +100,8 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   if (mbar_try_wait(addr, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(addr, parity)) return true;
-    if ((it & 63u) == 0u) {
+    if (mbar_try_wait_sleep(addr, parity)) return true;
+    if ((it & 7u) == 0u) {
       if (abort != nullptr && *abort) return false;
       if (globaltimer_ns() - t0 > limit_ns) {
         if (abort != nullptr) *abort = 1;
