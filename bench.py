@@ -2,7 +2,8 @@
 """Benchmark of the block-scaled linear layer on GB300.
 
 One step = the whole hot path over one batch: quantize the activations A (M x K) and the
-weights B (N x K) along K, then the block-scaled GEMM with the fused bias + bf16 epilogue.
+weights B (N x K) along K (one batched launch), then the block-scaled GEMM with the fused
+bias + bf16 epilogue.
 Default workload: ViT-B/16 MLP fc1 at training shape in MXFP8 (M = 14336, K = 768,
 N = 3072). Inputs are seeded synthetic data resident in HBM; the L2 cache is flushed (a
 256 MB write) between timed steps and every step is timed with CUDA events on the stream
@@ -273,8 +274,8 @@ def run_gpu(args, rank: int, world: int):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
     def quantize_layer(L, s):
-        bsq.quantize(L["g"].fmt, L["a"], out=L["qa"], stream=s)
-        bsq.quantize(L["g"].fmt, L["b"], out=L["qb"], stream=s)
+        # activations and weights of the layer in one launch (bsq_quantize_batch)
+        bsq.quantize_many(L["g"].fmt, [L["a"], L["b"]], outs=[L["qa"], L["qb"]], stream=s)
 
     def gemm_layer(L, s):
         bsq.gemm(L["qa"], L["qb"], L["bias"], out=L["out"], stream=s)
@@ -309,8 +310,9 @@ def run_gpu(args, rank: int, world: int):
         evs[-1][2].synchronize()
         return [(e[0].elapsed_time(e[1]), e[1].elapsed_time(e[2])) for e in evs]
 
-    # our kernels per step: 2 quantize (+1 amax pass each for NVFP4) + 1 GEMM per layer
-    launches_per_step = sum(3 + (2 if L["g"].fmt == NVFP4 else 0) for L in layers)
+    # our kernels per step and layer: 1 batched quantize (+1 amax pass per matrix for NVFP4)
+    # + 1 GEMM
+    launches_per_step = sum(2 + (2 if L["g"].fmt == NVFP4 else 0) for L in layers)
 
     for _ in range(args.warmup):
         step()
@@ -395,8 +397,7 @@ def run_gpu(args, rank: int, world: int):
         s_cmp.wait_event(B["in_done"])
         s_cmp.wait_event(B["out_done"])  # result of the step two back copied out
         for L, D in zip(layers, B["L"]):
-            bsq.quantize(L["g"].fmt, D["a"], out=D["qa"], stream=s_cmp)
-            bsq.quantize(L["g"].fmt, D["b"], out=D["qb"], stream=s_cmp)
+            bsq.quantize_many(L["g"].fmt, [D["a"], D["b"]], outs=[D["qa"], D["qb"]], stream=s_cmp)
             bsq.gemm(D["qa"], D["qb"], D["bias"], out=D["out"], stream=s_cmp)
         B["cmp_done"].record(s_cmp)
         with torch.cuda.stream(s_out):

@@ -39,6 +39,17 @@ _lib.bsq_scales_bytes.restype = ctypes.c_size_t
 _lib.bsq_scales_bytes.argtypes = [_int, _i64, _i64]
 _lib.bsq_quantize.restype = _int
 _lib.bsq_quantize.argtypes = [_int, _vp, _i64, _i64, _vp, _vp, _vp, _vp]
+MAX_BATCH = 8
+
+
+class QuantItem(ctypes.Structure):
+    """bsq_quant_item of bsq.h."""
+    _fields_ = [("src", _vp), ("rows", _i64), ("cols", _i64), ("codes", _vp), ("scales", _vp),
+                ("global_scale", ctypes.POINTER(ctypes.c_float))]
+
+
+_lib.bsq_quantize_batch.restype = _int
+_lib.bsq_quantize_batch.argtypes = [_int, _int, ctypes.POINTER(QuantItem), _vp]
 _lib.bsq_gemm.restype = _int
 _lib.bsq_gemm.argtypes = [_int, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp]
 _lib.bsq_get_device_status.restype = _int
@@ -49,8 +60,8 @@ _lib.bsq_last_error.restype = _int
 _lib.bsq_strerror.restype = ctypes.c_char_p
 _lib.bsq_strerror.argtypes = [_int]
 
-EXPORTS = ("bsq_codes_bytes", "bsq_scales_bytes", "bsq_quantize", "bsq_gemm", "bsq_get_device_status",
-           "bsq_selftest_timeout", "bsq_last_error", "bsq_strerror")
+EXPORTS = ("bsq_codes_bytes", "bsq_scales_bytes", "bsq_quantize", "bsq_quantize_batch", "bsq_gemm",
+           "bsq_get_device_status", "bsq_selftest_timeout", "bsq_last_error", "bsq_strerror")
 
 Ptr = Union[int, None, torch.Tensor]
 
@@ -94,6 +105,17 @@ def bsq_quantize(fmt_flags: int, src: Ptr, rows: int, cols: int, codes: Ptr, sca
                  global_scale: Ptr = None, stream=None) -> int:
     return int(_lib.bsq_quantize(int(fmt_flags), _p(src), rows, cols, _p(codes), _p(scales), _p(global_scale),
                                  _stream(stream)))
+
+
+def bsq_quantize_batch(fmt_flags: int, items, stream=None) -> int:
+    """items: sequence of (src, rows, cols, codes, scales, global_scale) tuples (pointers or
+    tensors, as bsq_quantize takes them)."""
+    arr = (QuantItem * max(1, len(items)))()
+    for i, (src, rows, cols, codes, scales, gs) in enumerate(items):
+        g = _p(gs)
+        arr[i] = QuantItem(_p(src), rows, cols, _p(codes), _p(scales),
+                           ctypes.cast(g, ctypes.POINTER(ctypes.c_float)) if g else None)
+    return int(_lib.bsq_quantize_batch(int(fmt_flags), len(items), arr, _stream(stream)))
 
 
 def bsq_gemm(fmt, A: Ptr, A_scales: Ptr, B: Ptr, B_scales: Ptr, bias: Ptr, out: Ptr, M: int, N: int, K: int,
@@ -162,6 +184,28 @@ def quantize(fmt, x: torch.Tensor, global_scale: Optional[torch.Tensor] = None, 
     if global_scale is not None:
         q.global_scale = global_scale
     return q
+
+
+def quantize_many(fmt, xs, outs=None, stream=None):
+    """Quantize several contiguous 2-D CUDA matrices of one dtype (bf16 or fp32) in one launch
+    (bsq_quantize_batch); NVFP4 computes each matrix's own g. Returns a list of QTensor."""
+    f = _fmt(fmt)
+    assert 1 <= len(xs) <= MAX_BATCH, "1..%d matrices per call" % MAX_BATCH
+    dt = xs[0].dtype
+    for x in xs:
+        assert x.is_cuda and x.is_contiguous() and x.dim() == 2 and x.dtype == dt, \
+            "matrices must be contiguous 2-D CUDA tensors of one dtype"
+    flags = f
+    if dt == torch.float32:
+        flags |= FLAG_SRC_F32
+    elif dt != torch.bfloat16:
+        raise TypeError("matrices must be bfloat16 or float32")
+    qs = list(outs) if outs is not None else [empty_qtensor(f, x.shape[0], x.shape[1], x.device) for x in xs]
+    items = [(x, x.shape[0], x.shape[1], q.codes, q.scales, q.global_scale) for x, q in zip(xs, qs)]
+    rc = bsq_quantize_batch(flags, items, stream)
+    if rc != OK:
+        raise BsqError(rc, "bsq_quantize_batch")
+    return qs
 
 
 def gemm(qa: QTensor, qb: QTensor, bias: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,

@@ -93,25 +93,45 @@ size_t bsq_scales_bytes(int fmt, int64_t rows, int64_t cols) {
   return static_cast<size_t>(fmt == BSQ_NVFP4 ? body + 16 : body);
 }
 
-int bsq_quantize(int fmt_flags, const void* src, int64_t rows, int64_t cols, void* codes, void* scales,
-                 float* global_scale, bsq_stream_t stream) {
+namespace {
+// Validation shared by bsq_quantize and bsq_quantize_batch; BSQ_OK or the error code.
+int check_quant_item(int fmt, bool given, const bsq_quant_item& it) {
+  if (it.src == nullptr || it.codes == nullptr || it.scales == nullptr || it.rows <= 0 || it.cols <= 0)
+    return BSQ_ERR_ARG;
+  if (fmt == BSQ_NVFP4 && given && it.global_scale == nullptr) return BSQ_ERR_ARG;
+  if (it.cols % bsq::block_size(fmt) != 0 || it.rows > INT32_MAX || it.cols > INT32_MAX) return BSQ_ERR_SHAPE;
+  if (!aligned16(it.src) || !aligned16(it.codes) || !aligned16(it.scales)) return BSQ_ERR_ALIGN;
+  if (it.global_scale != nullptr && (reinterpret_cast<uintptr_t>(it.global_scale) & 3u)) return BSQ_ERR_ALIGN;
+  return BSQ_OK;
+}
+}  // namespace
+
+int bsq_quantize_batch(int fmt_flags, int count, const bsq_quant_item* items, bsq_stream_t stream) {
   const int fmt = fmt_flags & BSQ_FMT_MASK;
   const int flags = fmt_flags & ~BSQ_FMT_MASK;
   if (fmt != BSQ_MXFP8 && fmt != BSQ_NVFP4 && fmt != BSQ_MXFP4) return fail(BSQ_ERR_ARG);
   if (flags & ~(BSQ_FLAG_SRC_F32 | BSQ_FLAG_GLOBAL_GIVEN)) return fail(BSQ_ERR_ARG);
-  if (src == nullptr || codes == nullptr || scales == nullptr || rows <= 0 || cols <= 0) return fail(BSQ_ERR_ARG);
+  if (items == nullptr || count < 1 || count > BSQ_MAX_BATCH) return fail(BSQ_ERR_ARG);
   const bool given = (flags & BSQ_FLAG_GLOBAL_GIVEN) != 0;
-  if (fmt == BSQ_NVFP4 && given && global_scale == nullptr) return fail(BSQ_ERR_ARG);
   if (fmt != BSQ_NVFP4 && given) return fail(BSQ_ERR_ARG);
-  if (cols % bsq::block_size(fmt) != 0 || rows > INT32_MAX || cols > INT32_MAX) return fail(BSQ_ERR_SHAPE);
-  if (!aligned16(src) || !aligned16(codes) || !aligned16(scales)) return fail(BSQ_ERR_ALIGN);
-  if (global_scale != nullptr && (reinterpret_cast<uintptr_t>(global_scale) & 3u)) return fail(BSQ_ERR_ALIGN);
+  bsq_quant_item local[BSQ_MAX_BATCH];
+  for (int i = 0; i < count; ++i) {
+    const int st = check_quant_item(fmt, given, items[i]);
+    if (st != BSQ_OK) return fail(st);
+    local[i] = items[i];
+    if (fmt != BSQ_NVFP4) local[i].global_scale = nullptr;
+  }
   const bsq::DeviceInfo* dev = bsq::current_device();
   if (dev == nullptr) return fail(BSQ_ERR_ARCH);
-  const int st = bsq::launch_quantize(fmt, (flags & BSQ_FLAG_SRC_F32) != 0, given, src, rows, cols, codes, scales,
-                                      fmt == BSQ_NVFP4 ? global_scale : nullptr, reinterpret_cast<cudaStream_t>(stream),
-                                      *dev);
+  const int st = bsq::launch_quantize_batch(fmt, (flags & BSQ_FLAG_SRC_F32) != 0, given, count, local,
+                                            reinterpret_cast<cudaStream_t>(stream), *dev);
   return st == BSQ_OK ? BSQ_OK : fail(st);
+}
+
+int bsq_quantize(int fmt_flags, const void* src, int64_t rows, int64_t cols, void* codes, void* scales,
+                 float* global_scale, bsq_stream_t stream) {
+  const bsq_quant_item item = {src, rows, cols, codes, scales, global_scale};
+  return bsq_quantize_batch(fmt_flags, 1, &item, stream);
 }
 
 int bsq_gemm(int fmt, const void* A, const void* A_scales, const void* B, const void* B_scales,

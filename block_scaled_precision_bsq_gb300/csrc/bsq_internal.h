@@ -4,6 +4,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "bsq.h"
+
 namespace bsq {
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -27,8 +29,10 @@ struct DeviceInfo {
 // usable device. Thread-safe.
 const DeviceInfo* current_device();
 
-int launch_quantize(int fmt, bool src_f32, bool global_given, const void* src, int64_t rows, int64_t cols,
-                    void* codes, void* scales, float* global_scale, cudaStream_t stream, const DeviceInfo& dev);
+// Items already validated (shapes, alignment); count in [1, BSQ_MAX_BATCH].
+using QuantItem = bsq_quant_item;
+int launch_quantize_batch(int fmt, bool src_f32, bool global_given, int count, const QuantItem* items,
+                          cudaStream_t stream, const DeviceInfo& dev);
 
 int launch_gemm(int fmt, const void* A, const void* A_scales, const void* B, const void* B_scales, const void* bias,
                 void* out, int64_t M, int64_t N, int64_t K, cudaStream_t stream, const DeviceInfo& dev);

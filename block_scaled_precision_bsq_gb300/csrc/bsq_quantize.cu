@@ -42,6 +42,7 @@ constexpr int kCtasPerSm = 2;           // two resident CTAs: twice the warps to
 constexpr int kChunkMax = 16384;        // bytes per chunk buffer
 constexpr int kChunkMin = 4096;         // smallest chunk worth a copy (small tensors)
 constexpr int kAmaxThreads = 256;
+constexpr int kMaxBatch = BSQ_MAX_BATCH;
 
 enum NvMode { kMx = 0, kNvComputed = 1, kNvGiven = 2 };
 
@@ -62,6 +63,14 @@ struct QuantArgs {
   int64_t chunks_per_row;
   int64_t nchunks;
   uint32_t cols_magic;  // floor(2^32 / cols) + 1: f / cols == umulhi(f, cols_magic) for f * cols < 2^32
+};
+
+// Up to kMaxBatch matrices of one format and source type quantized by one launch: their
+// chunk lists are concatenated, matrix t owning global chunks [chunk_start[t], chunk_start[t+1]).
+struct QuantBatch {
+  int n;
+  int64_t chunk_start[kMaxBatch + 1];
+  QuantArgs t[kMaxBatch];
   int* status;
 };
 
@@ -159,7 +168,7 @@ __device__ __forceinline__ uint32_t quantize16(const float (&x)[16], float amax,
 }
 
 template <int FMT, bool F32, int NV>
-__global__ void __launch_bounds__(kThreads, kCtasPerSm) quantize_kernel(QuantArgs a) {
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) quantize_kernel(const __grid_constant__ QuantBatch batch) {
   constexpr int kEsize = F32 ? 4 : 2;
   extern __shared__ uint8_t q_smem_raw[];
   uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(q_smem_raw) + 127) & ~uintptr_t(127));
@@ -180,8 +189,16 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) quantize_kernel(QuantArg
   launch_dependents();
   grid_dependency_wait();  // inputs and outputs may belong to the previous kernel until here
 
-  // chunk c -> first row, rows, first column, columns
-  auto chunk_geom = [&](int64_t c, int64_t& r0, int64_t& nr, int64_t& c0, int64_t& nc) {
+  const int64_t nchunks = batch.chunk_start[batch.n];
+  // global chunk c -> its matrix and local chunk index
+  auto chunk_owner = [&](int64_t c, int64_t& local) {
+    int t = 0;
+    while (t + 1 < batch.n && c >= batch.chunk_start[t + 1]) ++t;
+    local = c - batch.chunk_start[t];
+    return t;
+  };
+  // local chunk c of matrix a -> first row, rows, first column, columns
+  auto chunk_geom = [&](const QuantArgs& a, int64_t c, int64_t& r0, int64_t& nr, int64_t& c0, int64_t& nc) {
     if (a.chunks_per_row > 1) {
       r0 = c / a.chunks_per_row;
       c0 = (c - r0 * a.chunks_per_row) * a.cspan;
@@ -200,10 +217,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) quantize_kernel(QuantArg
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
-      for (int64_t c = blockIdx.x; c < a.nchunks; c += gridDim.x) {
-        if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1u, &abort_flag, a.status)) break;
+      for (int64_t c = blockIdx.x; c < nchunks; c += gridDim.x) {
+        if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1u, &abort_flag, batch.status)) break;
+        int64_t local;
+        const QuantArgs& a = batch.t[chunk_owner(c, local)];
         int64_t r0, nr, c0, nc;
-        chunk_geom(c, r0, nr, c0, nc);
+        chunk_geom(a, local, r0, nr, c0, nc);
         const uint32_t bytes = static_cast<uint32_t>(nr * nc * kEsize);
         mbar_arrive_expect_tx(&full_bar[stage], bytes);
         bulk_load(ring + stage * kChunkMax, a.src + (r0 * a.cols + c0) * kEsize, bytes, &full_bar[stage]);
@@ -215,22 +234,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) quantize_kernel(QuantArg
     }
   } else {
     // ------------------------------------------------------------ consumers
+    uint32_t run_max = 0;  // NVFP4 given-scale mode: running max |x| (fp32 bits) of matrix `cur`
+    int cur = -1;          // matrix of the previous chunk
     float g = 0.f, six_g = 0.f;
-    if constexpr (NV != kMx) {
-      if constexpr (NV == kNvComputed) {
-        g = __fdiv_rn(__uint_as_float(a.tail[1]), 2688.0f);  // amax / (6 * 448)
-      } else {
-        g = *a.g_in;
-      }
-      six_g = __fmul_rn(6.0f, g);
-      if (blockIdx.x == 0 && threadIdx.x == 32) {
-        a.tail[0] = __float_as_uint(g);
-        if constexpr (NV == kNvComputed) {
-          if (a.g_out != nullptr) *a.g_out = g;
-        }
-      }
-    }
-    uint32_t run_max = 0;  // NVFP4 given-scale mode: running max |x| (fp32 bits) for the tail
     const int cw = static_cast<int>(warp) - 1;
     // Warp steps are dealt round-robin over the concatenation of the CTA's chunks (not per
     // chunk), so that a chunk whose step count is not a multiple of the warp count does not
@@ -239,10 +245,39 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) quantize_kernel(QuantArg
     uint32_t lead = static_cast<uint32_t>(cw);
     int stage = 0;
     uint32_t phase = 0;
-    for (int64_t c = blockIdx.x; c < a.nchunks; c += gridDim.x) {
-      if (!mbar_wait_bounded_warp(&full_bar[stage], phase, &abort_flag, a.status)) break;
+    for (int64_t c = blockIdx.x; c < nchunks; c += gridDim.x) {
+      if (!mbar_wait_bounded_warp(&full_bar[stage], phase, &abort_flag, batch.status)) break;
+      int64_t local;
+      const int t = chunk_owner(c, local);
+      const QuantArgs& a = batch.t[t];
+      if (t != cur) {
+        if constexpr (NV == kNvGiven) {
+          // the previous matrix's share of |x| maxima -> its tail word 1
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) run_max = max(run_max, __shfl_xor_sync(0xFFFFFFFFu, run_max, o));
+          if (cur >= 0 && lane == 0 && run_max != 0) atomicMax(&batch.t[cur].tail[1], run_max);
+          run_max = 0;
+        }
+        cur = t;
+        if constexpr (NV != kMx) {
+          if constexpr (NV == kNvComputed) {
+            g = __fdiv_rn(__uint_as_float(a.tail[1]), 2688.0f);  // amax / (6 * 448)
+          } else {
+            g = *a.g_in;
+          }
+          six_g = __fmul_rn(6.0f, g);
+        }
+      }
+      if constexpr (NV != kMx) {
+        if (local == 0 && warp == 1 && lane == 0) {
+          a.tail[0] = __float_as_uint(g);
+          if constexpr (NV == kNvComputed) {
+            if (a.g_out != nullptr) *a.g_out = g;
+          }
+        }
+      }
       int64_t r0, nr, c0, nc;
-      chunk_geom(c, r0, nr, c0, nc);
+      chunk_geom(a, local, r0, nr, c0, nc);
       const uint8_t* buf = ring + stage * kChunkMax;
       // the chunk as one flat array of nr * nc elements; lane piece f = 16 elements
       const uint32_t flat = static_cast<uint32_t>(nr * nc);
@@ -297,22 +332,23 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) quantize_kernel(QuantArg
     }
 
     if constexpr (NV == kNvGiven) {
-      // per-warp maximum of |x| -> tail word 1 (the amax of this tensor)
+      // the last matrix's share of |x| maxima -> its tail word 1
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) run_max = max(run_max, __shfl_xor_sync(0xFFFFFFFFu, run_max, o));
-      if (lane == 0 && run_max != 0) atomicMax(&a.tail[1], run_max);
+      if (cur >= 0 && lane == 0 && run_max != 0) atomicMax(&batch.t[cur].tail[1], run_max);
     }
   }
 
-  // scale bytes of the padding rows of the last row tile read 0
-  const int64_t pad_rows = (128 - a.rows % 128) % 128;
-  if (pad_rows > 0) {
+  // scale bytes of the padding rows of each matrix's last row tile read 0
+  for (int m = 0; m < batch.n; ++m) {
+    const QuantArgs& a = batch.t[m];
+    const int64_t pad_rows = (128 - a.rows % 128) % 128;
+    if (pad_rows == 0) continue;
     const int64_t words = pad_rows * a.nct;
-    const int64_t r_first = a.rows;
     for (int64_t w = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; w < words;
          w += static_cast<int64_t>(gridDim.x) * kThreads) {
-      const int64_t r = r_first + w / a.nct, t = w % a.nct;
-      *reinterpret_cast<uint32_t*>(a.scales + scale_word_offset(r, 4 * t, a.nct)) = 0u;
+      const int64_t r = a.rows + w / a.nct, tc = w % a.nct;
+      *reinterpret_cast<uint32_t*>(a.scales + scale_word_offset(r, 4 * tc, a.nct)) = 0u;
     }
   }
 }
@@ -362,7 +398,7 @@ __global__ void __launch_bounds__(kAmaxThreads) amax_kernel(const uint4* src, in
 constexpr int kQuantSmem = kRing * kChunkMax + 128;
 
 template <int FMT, bool F32, int NV>
-cudaError_t launch_q(const QuantArgs& a, int grid, cudaStream_t stream) {
+cudaError_t launch_q(const QuantBatch& b, int grid, cudaStream_t stream) {
   static cudaError_t attr = cudaFuncSetAttribute(quantize_kernel<FMT, F32, NV>,
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, kQuantSmem);
   if (attr != cudaSuccess) return attr;
@@ -378,67 +414,81 @@ cudaError_t launch_q(const QuantArgs& a, int grid, cudaStream_t stream) {
   cfg.stream = stream;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, quantize_kernel<FMT, F32, NV>, a);
+  return cudaLaunchKernelEx(&cfg, quantize_kernel<FMT, F32, NV>, b);
 }
 
 }  // namespace
 
-int launch_quantize(int fmt, bool src_f32, bool global_given, const void* src, int64_t rows, int64_t cols,
-                    void* codes, void* scales, float* global_scale, cudaStream_t stream, const DeviceInfo& dev) {
-  QuantArgs a{};
-  a.src = static_cast<const uint8_t*>(src);
-  a.rows = rows;
-  a.cols = cols;
-  a.codes = static_cast<uint8_t*>(codes);
-  a.scales = static_cast<uint8_t*>(scales);
-  a.nsc = cols / block_size(fmt);
-  a.nct = ceil_div(a.nsc, 4);
-  a.status = dev.status;
-  a.cols_magic = static_cast<uint32_t>((uint64_t{1} << 32) / static_cast<uint64_t>(cols) + 1);
+int launch_quantize_batch(int fmt, bool src_f32, bool global_given, int count, const QuantItem* items,
+                          cudaStream_t stream, const DeviceInfo& dev) {
+  if (count < 1 || count > kMaxBatch) return BSQ_ERR_ARG;
   const int64_t esize = src_f32 ? 4 : 2;
-  const int64_t row_bytes = cols * esize;
-  const int64_t body = scales_body_bytes(fmt, rows, cols);
-
+  QuantBatch b{};
+  b.n = count;
+  b.status = dev.status;
   // Chunk size: at most one ring buffer, and small enough that every SM gets a few chunks
   // (a 5 MB matrix is then still spread over all SMs and copied in parallel).
-  const int64_t total_bytes = rows * row_bytes;
-  const int64_t target =
-      std::max<int64_t>(kChunkMin, std::min<int64_t>(kChunkMax, total_bytes / (4 * kCtasPerSm * static_cast<int64_t>(dev.num_sms))));
-  if (row_bytes <= target) {
-    a.rows_per_chunk = target / row_bytes;
-    a.cspan = cols;
-    a.chunks_per_row = 1;
-    a.nchunks = ceil_div(rows, a.rows_per_chunk);
-  } else {
-    a.rows_per_chunk = 1;
-    a.cspan = std::max<int64_t>(1, kChunkMax / (esize * kSeg)) * kSeg;  // whole segments per piece
-    a.chunks_per_row = ceil_div(cols, a.cspan);
-    a.nchunks = rows * a.chunks_per_row;
+  int64_t total_bytes = 0;
+  for (int i = 0; i < count; ++i) total_bytes += items[i].rows * items[i].cols * esize;
+  const int64_t target = std::max<int64_t>(
+      kChunkMin, std::min<int64_t>(kChunkMax, total_bytes / (4 * kCtasPerSm * static_cast<int64_t>(dev.num_sms))));
+  b.chunk_start[0] = 0;
+  for (int i = 0; i < count; ++i) {
+    const QuantItem& it = items[i];
+    QuantArgs& a = b.t[i];
+    a.src = static_cast<const uint8_t*>(it.src);
+    a.rows = it.rows;
+    a.cols = it.cols;
+    a.codes = static_cast<uint8_t*>(it.codes);
+    a.scales = static_cast<uint8_t*>(it.scales);
+    a.nsc = it.cols / block_size(fmt);
+    a.nct = ceil_div(a.nsc, 4);
+    a.cols_magic = static_cast<uint32_t>((uint64_t{1} << 32) / static_cast<uint64_t>(it.cols) + 1);
+    const int64_t row_bytes = it.cols * esize;
+    if (row_bytes <= target) {
+      a.rows_per_chunk = target / row_bytes;
+      a.cspan = it.cols;
+      a.chunks_per_row = 1;
+      a.nchunks = ceil_div(it.rows, a.rows_per_chunk);
+    } else {
+      a.rows_per_chunk = 1;
+      a.cspan = std::max<int64_t>(1, kChunkMax / (esize * kSeg)) * kSeg;  // whole segments per piece
+      a.chunks_per_row = ceil_div(it.cols, a.cspan);
+      a.nchunks = it.rows * a.chunks_per_row;
+    }
+    b.chunk_start[i + 1] = b.chunk_start[i] + a.nchunks;
+    if (fmt == BSQ_NVFP4) {
+      a.tail = reinterpret_cast<uint32_t*>(a.scales + scales_body_bytes(fmt, it.rows, it.cols));
+      a.g_in = it.global_scale;
+      a.g_out = it.global_scale;
+    }
   }
-  const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(a.nchunks, kCtasPerSm * dev.num_sms)));
+  const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(b.chunk_start[count], kCtasPerSm * dev.num_sms)));
 
   cudaError_t err = cudaSuccess;
   if (fmt == BSQ_NVFP4) {
-    a.tail = reinterpret_cast<uint32_t*>(a.scales + body);
-    a.g_in = global_scale;
-    a.g_out = global_scale;
-    if (cudaMemsetAsync(a.tail, 0, 16, stream) != cudaSuccess) return BSQ_ERR_LAUNCH;
+    for (int i = 0; i < count; ++i) {
+      const QuantArgs& a = b.t[i];
+      if (cudaMemsetAsync(a.tail, 0, 16, stream) != cudaSuccess) return BSQ_ERR_LAUNCH;
+      if (!global_given) {
+        const int64_t nvec = a.rows * a.cols * esize / 16;
+        const int agrid = static_cast<int>(std::min<int64_t>(ceil_div(nvec, kAmaxThreads * 4), dev.num_sms * 8));
+        if (src_f32) amax_kernel<true><<<agrid, kAmaxThreads, 0, stream>>>(reinterpret_cast<const uint4*>(a.src), nvec, a.tail + 1);
+        else amax_kernel<false><<<agrid, kAmaxThreads, 0, stream>>>(reinterpret_cast<const uint4*>(a.src), nvec, a.tail + 1);
+        if (cudaGetLastError() != cudaSuccess) return BSQ_ERR_LAUNCH;
+      }
+    }
     if (!global_given) {
-      const int64_t nvec = rows * cols * esize / 16;
-      const int agrid = static_cast<int>(std::min<int64_t>(ceil_div(nvec, kAmaxThreads * 4), dev.num_sms * 8));
-      if (src_f32) amax_kernel<true><<<agrid, kAmaxThreads, 0, stream>>>(static_cast<const uint4*>(src), nvec, a.tail + 1);
-      else amax_kernel<false><<<agrid, kAmaxThreads, 0, stream>>>(static_cast<const uint4*>(src), nvec, a.tail + 1);
-      if (cudaGetLastError() != cudaSuccess) return BSQ_ERR_LAUNCH;
-      err = src_f32 ? launch_q<BSQ_NVFP4, true, kNvComputed>(a, grid, stream)
-                    : launch_q<BSQ_NVFP4, false, kNvComputed>(a, grid, stream);
+      err = src_f32 ? launch_q<BSQ_NVFP4, true, kNvComputed>(b, grid, stream)
+                    : launch_q<BSQ_NVFP4, false, kNvComputed>(b, grid, stream);
     } else {
-      err = src_f32 ? launch_q<BSQ_NVFP4, true, kNvGiven>(a, grid, stream)
-                    : launch_q<BSQ_NVFP4, false, kNvGiven>(a, grid, stream);
+      err = src_f32 ? launch_q<BSQ_NVFP4, true, kNvGiven>(b, grid, stream)
+                    : launch_q<BSQ_NVFP4, false, kNvGiven>(b, grid, stream);
     }
   } else if (fmt == BSQ_MXFP8) {
-    err = src_f32 ? launch_q<BSQ_MXFP8, true, kMx>(a, grid, stream) : launch_q<BSQ_MXFP8, false, kMx>(a, grid, stream);
+    err = src_f32 ? launch_q<BSQ_MXFP8, true, kMx>(b, grid, stream) : launch_q<BSQ_MXFP8, false, kMx>(b, grid, stream);
   } else {
-    err = src_f32 ? launch_q<BSQ_MXFP4, true, kMx>(a, grid, stream) : launch_q<BSQ_MXFP4, false, kMx>(a, grid, stream);
+    err = src_f32 ? launch_q<BSQ_MXFP4, true, kMx>(b, grid, stream) : launch_q<BSQ_MXFP4, false, kMx>(b, grid, stream);
   }
   return err == cudaSuccess ? BSQ_OK : BSQ_ERR_LAUNCH;
 }

@@ -101,6 +101,28 @@ int bsq_quantize(int fmt_flags, const void* src, int64_t rows, int64_t cols, voi
                  float* global_scale, bsq_stream_t stream);
 
 /*
+ * bsq_quantize_batch: bsq_quantize applied to `count` matrices (1 <= count <= BSQ_MAX_BATCH)
+ * in one kernel launch, e.g. a layer's activations and weights together. Every item is
+ * validated as in bsq_quantize (its own rows, cols, buffers; global_scale as bsq_quantize's
+ * argument) and the whole batch shares fmt_flags (one format, one source type, one
+ * NVFP4 scale mode). Results are identical, byte for byte, to `count` bsq_quantize calls.
+ * `items` is a host array read during the call only. The batching is an engineering entry
+ * point (fewer launches for small matrices); the method itself has no counterpart.
+ * Errors: BSQ_ERR_ARG if count is out of range or items is NULL, otherwise the first error
+ * any item would give bsq_quantize; nothing is enqueued on an argument error.
+ */
+#define BSQ_MAX_BATCH 8
+typedef struct {
+  const void* src;     /* rows x cols bf16 or fp32 (per fmt_flags) */
+  int64_t rows, cols;
+  void* codes;         /* bsq_codes_bytes(fmt, rows, cols) bytes, written */
+  void* scales;        /* bsq_scales_bytes(fmt, rows, cols) bytes, written */
+  float* global_scale; /* NVFP4 only, as bsq_quantize's global_scale; NULL otherwise */
+} bsq_quant_item;
+
+int bsq_quantize_batch(int fmt_flags, int count, const bsq_quant_item* items, bsq_stream_t stream);
+
+/*
  * bsq_gemm: out[m, n] = bf16_rn(alpha * sum_k Ahat[m,k] * Bhat[n,k] + bias[n]).
  *   A, A_scales  M x K operand as written by bsq_quantize(fmt, ..., M, K, ...).
  *   B, B_scales  N x K operand (the nn.Linear weight layout) from bsq_quantize(fmt, ..., N, K, ...).

@@ -64,6 +64,12 @@ def test_argument_errors_before_any_cuda_call(bsq):
     assert bsq.bsq_quantize(bsq.MXFP8, p, 4, 48, p, p) == bsq.ERR_SHAPE                # 48 % 32
     assert bsq.bsq_quantize(bsq.NVFP4, p, 4, 40, p, p) == bsq.ERR_SHAPE                # 40 % 16
     assert bsq.bsq_quantize(bsq.MXFP8, p, 1 << 31, 32, p, p) == bsq.ERR_SHAPE          # rows >= 2^31
+    good = (p, 4, 64, p, p, None)
+    assert bsq.bsq_quantize_batch(bsq.MXFP8, []) == bsq.ERR_ARG                        # count 0
+    assert bsq.bsq_quantize_batch(bsq.MXFP8, [good] * 9) == bsq.ERR_ARG                # count > 8
+    assert bsq.bsq_quantize_batch(bsq.MXFP8, [good, (p, 4, 48, p, p, None)]) == bsq.ERR_SHAPE  # item 2
+    assert bsq.bsq_quantize_batch(bsq.MXFP8, [good, (p + 8, 4, 64, p, p, None)]) == bsq.ERR_ALIGN
+    assert bsq.bsq_quantize_batch(bsq.NVFP4 | bsq.FLAG_GLOBAL_GIVEN, [good]) == bsq.ERR_ARG  # no g
     assert bsq.bsq_quantize(bsq.MXFP8, p, 4, 1 << 31, p, p) == bsq.ERR_SHAPE           # cols >= 2^31
     assert bsq.bsq_quantize(bsq.NVFP4 | bsq.FLAG_GLOBAL_GIVEN, p, 4, 32, p, p, None) == bsq.ERR_ARG
     assert bsq.bsq_quantize(bsq.MXFP8 | bsq.FLAG_GLOBAL_GIVEN, p, 4, 32, p, p, p) == bsq.ERR_ARG

@@ -101,3 +101,41 @@ def test_full_size_workload_quantize(name):
             seen.add(key)
             _compare(g.fmt, make(g), label="%s %s %s" % (name, g.name, kind))
             torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("fmt", ["mxfp8", "nvfp4", "mxfp4"])
+@pytest.mark.parametrize("f32", [False, True])
+def test_batch_equals_single_calls_and_oracle(fmt, f32):
+    """bsq_quantize_batch over matrices of different shapes (ragged rows, a row longer than a
+    chunk) gives the bytes of one bsq_quantize call per matrix, and those of the oracle."""
+    bsq = _bsq()
+    shapes = [(300, 768), (7, 96), (129, 8192), (1, 32), (1000, 1024)]
+    xs_np = [random_matrix(r, c, seed=40 + i, dist="student_t4", src_f32=f32) for i, (r, c) in enumerate(shapes)]
+    xs = [to_dev(x) for x in xs_np]
+    many = bsq.quantize_many(fmt, xs)
+    assert bsq.device_status() == 0
+    for x, x_np, qm in zip(xs, xs_np, many):
+        q1 = bsq.quantize(fmt, x)
+        assert torch.equal(qm.codes, q1.codes) and torch.equal(qm.scales, q1.scales)
+        o = oracle.quantize(fmt, x_np)
+        assert np.array_equal(qm.codes.cpu().numpy(), o.codes)
+        assert np.array_equal(qm.scales.cpu().numpy(), o.tiled_scales())
+        if fmt == "nvfp4":
+            assert qm.global_scale.item() == o.g
+
+
+def test_batch_nvfp4_given_scales():
+    bsq = _bsq()
+    xs_np = [random_matrix(64, 256, seed=50, dist="normal"), random_matrix(200, 512, seed=51, dist="student_t4")]
+    gs = [0.01, 0.003]
+    xs = [to_dev(x) for x in xs_np]
+    outs = [bsq.empty_qtensor("nvfp4", x.shape[0], x.shape[1]) for x in xs]
+    for q, g in zip(outs, gs):
+        q.global_scale.fill_(g)
+    items = [(x, x.shape[0], x.shape[1], q.codes, q.scales, q.global_scale) for x, q in zip(xs, outs)]
+    assert bsq.bsq_quantize_batch(bsq.NVFP4 | bsq.FLAG_GLOBAL_GIVEN, items) == bsq.OK
+    assert bsq.device_status() == 0
+    for x_np, q, g in zip(xs_np, outs, gs):
+        o = oracle.quantize("nvfp4", x_np, global_scale=g)
+        assert np.array_equal(q.codes.cpu().numpy(), o.codes)
+        assert np.array_equal(q.scales.cpu().numpy(), o.tiled_scales())
