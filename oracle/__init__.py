@@ -72,6 +72,12 @@ def lib() -> ctypes.CDLL:
         L.orc_decode.argtypes = [ctypes.c_int, u8p, u8p, i64, i64, f64p]
         L.orc_gemm.restype = ctypes.c_int
         L.orc_gemm.argtypes = [f64p, f64p, vp, i64, i64, i64, ctypes.c_double, i64, i64, f64p, vp]
+        L.orc_gelu_erf.restype = ctypes.c_int
+        L.orc_gelu_erf.argtypes = [f64p, f64p, i64]
+        L.orc_quantize_mx_f64.restype = ctypes.c_int
+        L.orc_quantize_mx_f64.argtypes = [ctypes.c_int, f64p, i64, i64, u8p, u8p]
+        L.orc_encode_array.restype = ctypes.c_int
+        L.orc_encode_array.argtypes = [ctypes.c_int, f64p, i64, u8p]
         L.orc_num_threads.restype = ctypes.c_int
         L.orc_set_num_threads.argtypes = [ctypes.c_int]
         _lib = L
@@ -228,3 +234,42 @@ def reference_linear(fmt, a_src: np.ndarray, b_src: np.ndarray, bias: Optional[n
     alpha = qa.g * qb.g if qa.fmt == NVFP4 else 1.0
     out, ab = gemm(qa.decode(), qb.decode(), bias, alpha, rows)
     return qa, qb, out, ab
+
+
+def gelu_erf(v: np.ndarray) -> np.ndarray:
+    """Exact-erf GELU in fp64 (reading R8)."""
+    v = np.ascontiguousarray(v, dtype=np.float64)
+    out = np.empty_like(v)
+    st = lib().orc_gelu_erf(_ptr(v), _ptr(out), v.size)
+    if st:
+        raise ValueError("oracle gelu failed: %d" % st)
+    return out
+
+
+def quantize_mx_f64(fmt, y: np.ndarray) -> Quantized:
+    """MX quantization (rule R2) of fp64 values y (rows x cols)."""
+    f = _fmt(fmt)
+    assert f in (MXFP8, MXFP4)
+    y = np.ascontiguousarray(y, dtype=np.float64)
+    rows, cols = y.shape
+    codes = np.zeros(codes_bytes(f, rows, cols), dtype=np.uint8)
+    scales = np.zeros((rows, cols // 32), dtype=np.uint8)
+    st = lib().orc_quantize_mx_f64(f, _ptr(y), rows, cols, _ptr(codes), _ptr(scales))
+    if st:
+        raise ValueError("oracle quantize failed: %d" % st)
+    return Quantized(f, rows, cols, codes, scales)
+
+
+def encode_array(elem: str, v: np.ndarray) -> np.ndarray:
+    """Element codes (one per byte) of fp64 values: elem 'e4m3' or 'e2m1' (rule R1)."""
+    v = np.ascontiguousarray(v, dtype=np.float64)
+    out = np.empty(v.shape, dtype=np.uint8)
+    st = lib().orc_encode_array(0 if elem == "e4m3" else 1, _ptr(v), v.size, _ptr(out))
+    if st:
+        raise ValueError("oracle encode failed: %d" % st)
+    return out
+
+
+def gelu_quantize_reference(fmt, y: np.ndarray) -> Quantized:
+    """The fused fc1 step of reading R8 on the unrounded GEMM values y: MX(GELU(y))."""
+    return quantize_mx_f64(fmt, gelu_erf(y))

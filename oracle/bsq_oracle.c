@@ -39,6 +39,11 @@
  *   R6  GEMM: y[m,n] = alpha * sum_k Ahat[m,k] * Bhat[n,k] + bias[n] in fp64, kept unrounded;
  *       alpha = g_A * g_B for NVFP4 (the block-scaled sum is formed first), 1 otherwise.
  *   R7  Non-finite inputs are outside the contract; the quantizers reject them.
+ *   R8  Producer-fused quantization of a fc1 output ([LT] section 4.3: the MXFP8 stack's fc1
+ *       epilogue quantizes the GELU output straight into fc2's operand): the value
+ *       quantized is GELU(alpha * acc + bias) with GELU in its exact erf form
+ *       0.5 v (1 + erf(v / sqrt 2)), taken before any bf16 rounding, then the MX rule R2
+ *       along the output row. Here y is the unrounded fp64 value of R6.
  *
  * Pins (tests that tie this code to something other than itself) are in the test suite:
  * exhaustive decode tables against two independent float8/float4 libraries, encoders
@@ -397,5 +402,72 @@ int orc_gemm(const double* A, const double* B, const uint16_t* bias, int64_t M, 
             if (abs_out) abs_out[(m - row0) * N + n] = fabs(alpha) * acc_abs;
         }
     }
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------------------
+ * Producer-fused quantization of a fc1 output for fc2 ("lightly-train - DINOv3 + EoMT on
+ * RTX 5090" README, section 4.3: in the MXFP8 stack the fc1 epilogue quantizes the GELU
+ * output directly into fc2's operand), reading R8.
+ * ---------------------------------------------------------------------------------- */
+
+/* out[i] = GELU(v[i]) = v * Phi(v) = 0.5 * v * (1 + erf(v / sqrt 2)), fp64, evaluated as
+ * 0.5 * v * erfc(-v / sqrt 2) (libm erfc): the same function without the cancellation of
+ * 1 + erf(.) for negative v, where GELU is tiny but not zero. */
+int orc_gelu_erf(const double* v, double* out, int64_t n) {
+    int64_t i;
+    if (!v || !out || n < 0) return ORC_ERR_ARG;
+#pragma omp parallel for schedule(static)
+    for (i = 0; i < n; ++i) out[i] = 0.5 * v[i] * erfc(-v[i] / sqrt(2.0));
+    return ORC_OK;
+}
+
+/* MX quantization (reading R2) of fp64 values: y rows x cols, cols % 32 == 0, finite.
+ * codes: MXFP8 rows*cols bytes, MXFP4 rows*cols/2 bytes; scales: plain rows x (cols/32). */
+int orc_quantize_mx_f64(int fmt, const double* y, int64_t rows, int64_t cols, uint8_t* codes, uint8_t* scales) {
+    int64_t nsc, r, i;
+    int emax_elem;
+    if (!y || !codes || !scales || rows <= 0 || cols <= 0) return ORC_ERR_ARG;
+    if (fmt != ORC_MXFP8 && fmt != ORC_MXFP4) return ORC_ERR_ARG;
+    if (cols % 32) return ORC_ERR_SHAPE;
+    for (i = 0; i < rows * cols; ++i)
+        if (!isfinite(y[i])) return ORC_ERR_NONFINITE;
+    nsc = cols / 32;
+    emax_elem = fmt == ORC_MXFP8 ? 8 : 2;
+#pragma omp parallel for schedule(static)
+    for (r = 0; r < rows; ++r) {
+        int64_t b;
+        for (b = 0; b < nsc; ++b) {
+            int64_t k, base = r * cols + b * 32;
+            double amax = 0.0;
+            int e, ex;
+            for (k = 0; k < 32; ++k) {
+                double a = fabs(y[base + k]);
+                if (a > amax) amax = a;
+            }
+            if (amax == 0.0) {
+                e = -127;
+            } else {
+                (void)frexp(amax, &ex);
+                e = (ex - 1) - emax_elem;
+                if (e < -127) e = -127;
+                if (e > 127) e = 127;
+            }
+            scales[r * nsc + b] = (uint8_t)(e + 127);
+            for (k = 0; k < 32; ++k) {
+                double v = ldexp(y[base + k], -e);
+                unsigned code = fmt == ORC_MXFP8 ? orc_encode_e4m3(v) : orc_encode_e2m1(v);
+                put_code(fmt, codes, base + k, code);
+            }
+        }
+    }
+    return ORC_OK;
+}
+
+/* Element encoders over an array: elem 0 = E4M3, 1 = e2m1 (one code per byte). */
+int orc_encode_array(int elem, const double* v, int64_t n, uint8_t* out) {
+    int64_t i;
+    if (!v || !out || n < 0 || (elem != 0 && elem != 1)) return ORC_ERR_ARG;
+    for (i = 0; i < n; ++i) out[i] = (uint8_t)(elem == 0 ? orc_encode_e4m3(v[i]) : orc_encode_e2m1(v[i]));
     return ORC_OK;
 }
