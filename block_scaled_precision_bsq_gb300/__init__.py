@@ -52,6 +52,10 @@ _lib.bsq_quantize_batch.restype = _int
 _lib.bsq_quantize_batch.argtypes = [_int, _int, ctypes.POINTER(QuantItem), _vp]
 _lib.bsq_gemm.restype = _int
 _lib.bsq_gemm.argtypes = [_int, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp]
+_lib.bsq_gemm_gelu.restype = _int
+_lib.bsq_gemm_gelu.argtypes = [_int, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp]
+_lib.bsq_gemm_gelu_quantize.restype = _int
+_lib.bsq_gemm_gelu_quantize.argtypes = [_int, _vp, _vp, _vp, _vp, _vp, _int, _vp, _vp, _i64, _i64, _i64, _vp]
 _lib.bsq_get_device_status.restype = _int
 _lib.bsq_get_device_status.argtypes = [_vp]
 _lib.bsq_selftest_timeout.restype = _int
@@ -61,7 +65,8 @@ _lib.bsq_strerror.restype = ctypes.c_char_p
 _lib.bsq_strerror.argtypes = [_int]
 
 EXPORTS = ("bsq_codes_bytes", "bsq_scales_bytes", "bsq_quantize", "bsq_quantize_batch", "bsq_gemm",
-           "bsq_get_device_status", "bsq_selftest_timeout", "bsq_last_error", "bsq_strerror")
+           "bsq_gemm_gelu", "bsq_gemm_gelu_quantize", "bsq_get_device_status", "bsq_selftest_timeout",
+           "bsq_last_error", "bsq_strerror")
 
 Ptr = Union[int, None, torch.Tensor]
 
@@ -122,6 +127,18 @@ def bsq_gemm(fmt, A: Ptr, A_scales: Ptr, B: Ptr, B_scales: Ptr, bias: Ptr, out: 
              stream=None) -> int:
     return int(_lib.bsq_gemm(_fmt(fmt), _p(A), _p(A_scales), _p(B), _p(B_scales), _p(bias), _p(out), M, N, K,
                              _stream(stream)))
+
+
+def bsq_gemm_gelu(fmt, A: Ptr, A_scales: Ptr, B: Ptr, B_scales: Ptr, bias: Ptr, out: Ptr, M: int, N: int,
+                  K: int, stream=None) -> int:
+    return int(_lib.bsq_gemm_gelu(_fmt(fmt), _p(A), _p(A_scales), _p(B), _p(B_scales), _p(bias), _p(out), M, N, K,
+                                  _stream(stream)))
+
+
+def bsq_gemm_gelu_quantize(fmt, A: Ptr, A_scales: Ptr, B: Ptr, B_scales: Ptr, bias: Ptr, out_fmt, out_codes: Ptr,
+                           out_scales: Ptr, M: int, N: int, K: int, stream=None) -> int:
+    return int(_lib.bsq_gemm_gelu_quantize(_fmt(fmt), _p(A), _p(A_scales), _p(B), _p(B_scales), _p(bias),
+                                           _fmt(out_fmt), _p(out_codes), _p(out_scales), M, N, K, _stream(stream)))
 
 
 def bsq_get_device_status(stream=None) -> int:
@@ -221,6 +238,34 @@ def gemm(qa: QTensor, qb: QTensor, bias: Optional[torch.Tensor] = None, out: Opt
     if rc != OK:
         raise BsqError(rc, "bsq_gemm")
     return out
+
+
+def gemm_gelu(qa: QTensor, qb: QTensor, bias: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
+              stream=None) -> torch.Tensor:
+    """out[M, N] = bf16(GELU(alpha * A_hat . B_hat^T + bias)), GELU in its erf form."""
+    assert qa.fmt == qb.fmt and qa.cols == qb.cols
+    M, K, N = qa.rows, qa.cols, qb.rows
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=qa.codes.device)
+    rc = bsq_gemm_gelu(qa.fmt, qa.codes, qa.scales, qb.codes, qb.scales, bias, out, M, N, K, stream)
+    if rc != OK:
+        raise BsqError(rc, "bsq_gemm_gelu")
+    return out
+
+
+def gemm_gelu_quantize(qa: QTensor, qb: QTensor, bias: Optional[torch.Tensor] = None, out_fmt="mxfp8",
+                       out: Optional[QTensor] = None, stream=None) -> QTensor:
+    """GELU(alpha * A_hat . B_hat^T + bias) quantized along N into out_fmt (MXFP8 / MXFP4) in the
+    GEMM's epilogue: an M x N operand, laid out as quantize() lays it out."""
+    assert qa.fmt == qb.fmt and qa.cols == qb.cols
+    M, K, N = qa.rows, qa.cols, qb.rows
+    of = _fmt(out_fmt)
+    q = out if out is not None else empty_qtensor(of, M, N, qa.codes.device)
+    rc = bsq_gemm_gelu_quantize(qa.fmt, qa.codes, qa.scales, qb.codes, qb.scales, bias, of, q.codes, q.scales,
+                                M, N, K, stream)
+    if rc != OK:
+        raise BsqError(rc, "bsq_gemm_gelu_quantize")
+    return q
 
 
 def linear(fmt, x: torch.Tensor, w: torch.Tensor, bias: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:

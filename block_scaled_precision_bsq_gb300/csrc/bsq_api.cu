@@ -134,22 +134,57 @@ int bsq_quantize(int fmt_flags, const void* src, int64_t rows, int64_t cols, voi
   return bsq_quantize_batch(fmt_flags, 1, &item, stream);
 }
 
-int bsq_gemm(int fmt, const void* A, const void* A_scales, const void* B, const void* B_scales,
-             const void* bias_bf16, void* out_bf16, int64_t M, int64_t N, int64_t K, bsq_stream_t stream) {
-  if (fmt != BSQ_MXFP8 && fmt != BSQ_NVFP4 && fmt != BSQ_MXFP4) return fail(BSQ_ERR_ARG);
-  if (A == nullptr || A_scales == nullptr || B == nullptr || B_scales == nullptr || out_bf16 == nullptr)
-    return fail(BSQ_ERR_ARG);
-  if (M <= 0 || N <= 0 || K <= 0) return fail(BSQ_ERR_ARG);
-  if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return fail(BSQ_ERR_SHAPE);
-  if (K % (fmt == BSQ_MXFP8 ? 128 : 256) != 0 || N % 8 != 0) return fail(BSQ_ERR_SHAPE);
-  if (!aligned16(A) || !aligned16(A_scales) || !aligned16(B) || !aligned16(B_scales) || !aligned16(out_bf16))
-    return fail(BSQ_ERR_ALIGN);
-  if (bias_bf16 != nullptr && (reinterpret_cast<uintptr_t>(bias_bf16) & 1u)) return fail(BSQ_ERR_ALIGN);
+namespace {
+// Validation shared by the GEMM entry points; BSQ_OK or the error code.
+int check_gemm(int fmt, const void* A, const void* A_scales, const void* B, const void* B_scales,
+               const void* bias_bf16, const void* out, int64_t M, int64_t N, int64_t K) {
+  if (fmt != BSQ_MXFP8 && fmt != BSQ_NVFP4 && fmt != BSQ_MXFP4) return BSQ_ERR_ARG;
+  if (A == nullptr || A_scales == nullptr || B == nullptr || B_scales == nullptr || out == nullptr) return BSQ_ERR_ARG;
+  if (M <= 0 || N <= 0 || K <= 0) return BSQ_ERR_ARG;
+  if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return BSQ_ERR_SHAPE;
+  if (K % (fmt == BSQ_MXFP8 ? 128 : 256) != 0 || N % 8 != 0) return BSQ_ERR_SHAPE;
+  if (!aligned16(A) || !aligned16(A_scales) || !aligned16(B) || !aligned16(B_scales) || !aligned16(out))
+    return BSQ_ERR_ALIGN;
+  if (bias_bf16 != nullptr && (reinterpret_cast<uintptr_t>(bias_bf16) & 1u)) return BSQ_ERR_ALIGN;
+  return BSQ_OK;
+}
+
+int gemm_common(int fmt, int epi, const void* A, const void* A_scales, const void* B, const void* B_scales,
+                const void* bias_bf16, void* out, void* out_scales, int64_t M, int64_t N, int64_t K,
+                bsq_stream_t stream) {
   const bsq::DeviceInfo* dev = bsq::current_device();
   if (dev == nullptr) return fail(BSQ_ERR_ARCH);
-  const int st = bsq::launch_gemm(fmt, A, A_scales, B, B_scales, bias_bf16, out_bf16, M, N, K,
+  const int st = bsq::launch_gemm(fmt, epi, A, A_scales, B, B_scales, bias_bf16, out, out_scales, M, N, K,
                                   reinterpret_cast<cudaStream_t>(stream), *dev);
   return st == BSQ_OK ? BSQ_OK : fail(st);
+}
+}  // namespace
+
+int bsq_gemm(int fmt, const void* A, const void* A_scales, const void* B, const void* B_scales,
+             const void* bias_bf16, void* out_bf16, int64_t M, int64_t N, int64_t K, bsq_stream_t stream) {
+  const int st = check_gemm(fmt, A, A_scales, B, B_scales, bias_bf16, out_bf16, M, N, K);
+  if (st != BSQ_OK) return fail(st);
+  return gemm_common(fmt, 0, A, A_scales, B, B_scales, bias_bf16, out_bf16, nullptr, M, N, K, stream);
+}
+
+int bsq_gemm_gelu(int fmt, const void* A, const void* A_scales, const void* B, const void* B_scales,
+                  const void* bias_bf16, void* out_bf16, int64_t M, int64_t N, int64_t K, bsq_stream_t stream) {
+  const int st = check_gemm(fmt, A, A_scales, B, B_scales, bias_bf16, out_bf16, M, N, K);
+  if (st != BSQ_OK) return fail(st);
+  return gemm_common(fmt, 1, A, A_scales, B, B_scales, bias_bf16, out_bf16, nullptr, M, N, K, stream);
+}
+
+int bsq_gemm_gelu_quantize(int fmt, const void* A, const void* A_scales, const void* B, const void* B_scales,
+                           const void* bias_bf16, int out_fmt, void* out_codes, void* out_scales, int64_t M,
+                           int64_t N, int64_t K, bsq_stream_t stream) {
+  if (out_fmt != BSQ_MXFP8 && out_fmt != BSQ_MXFP4) return fail(BSQ_ERR_ARG);
+  if (out_scales == nullptr) return fail(BSQ_ERR_ARG);
+  int st = check_gemm(fmt, A, A_scales, B, B_scales, bias_bf16, out_codes, M, N, K);
+  if (st != BSQ_OK) return fail(st);
+  if (N % 32 != 0) return fail(BSQ_ERR_SHAPE);
+  if (!aligned16(out_scales)) return fail(BSQ_ERR_ALIGN);
+  return gemm_common(fmt, out_fmt == BSQ_MXFP8 ? 2 : 3, A, A_scales, B, B_scales, bias_bf16, out_codes, out_scales,
+                     M, N, K, stream);
 }
 
 int bsq_get_device_status(bsq_stream_t stream) {

@@ -120,8 +120,20 @@ __host__ __device__ constexpr uint32_t make_idesc(uint32_t sf_id) {
          (static_cast<uint32_t>((2 * BM) >> 7) << 27) | (sf_id << 29);
 }
 
+// Epilogue modes. kEpiBf16: out = bf16(v), v = alpha * acc + bias. kEpiGeluBf16: out =
+// bf16(GELU(v)) (the "fc1 + GELU" epilogue every stack of the "lightly-train - DINOv3 + EoMT on
+// RTX 5090" README fuses, section 4.3). kEpiGeluMxfp8 / kEpiGeluMxfp4: GELU(v) quantized along
+// the output row straight into MX codes and tiled scales, the fc2 operand (the MXFP8 stack's
+// fc1 epilogue, same section); bytes laid out as bsq_quantize writes them. GELU is the exact
+// erf form, evaluated as 0.5 v erfc(-v / sqrt 2) (no cancellation for negative v).
+enum EpiMode { kEpiBf16 = 0, kEpiGeluBf16 = 1, kEpiGeluMxfp8 = 2, kEpiGeluMxfp4 = 3 };
+
+__device__ __forceinline__ float gelu_erf(float v) { return 0.5f * v * erfcf(-v * 0.7071067811865476f); }
+
 struct GemmArgs {
   const uint16_t* bias;  // nullable
+  uint8_t* qscales;      // quantized epilogues: tiled scales of the M x N output
+  int q_nct;             // quantized epilogues: 4-column scale tiles per output row (N / 128, rounded up)
   const float* ga;       // NVFP4: per-tensor scales in the scale tails
   const float* gb;
   int M, N;
@@ -130,7 +142,7 @@ struct GemmArgs {
   int* status;
 };
 
-template <int FMT>
+template <int FMT, int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
                 const __grid_constant__ CUtensorMap mapSfa, const __grid_constant__ CUtensorMap mapSfb,
@@ -327,37 +339,93 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive_remote(tmem_empty_leader);  // accumulator may be overwritten now
 
-      constexpr int EC = C::kEpiCols;  // 32 or 16 columns (64 or 32 bytes) per store chunk
+      // the epilogue value of column c of this warp's 128: alpha * acc + bias (and GELU)
+      auto value = [&](int c) {
+        float v = __uint_as_float(acc[c >> 5][c & 31]);
+        if constexpr (FMT == BSQ_NVFP4) {
+          v = __fmaf_rn(v, alpha, bias_s[c]);
+        } else {
+          v = __fadd_rn(v, bias_s[c]);
+        }
+        if constexpr (EPI != kEpiBf16) v = gelu_erf(v);
+        return v;
+      };
+      // quantized epilogues: all 128 values first (in place), one MX block per 32 columns (the
+      // MX rule: exponent of the block's largest magnitude minus that of the element format's
+      // top binade), scale word of the row's four blocks stored in the tiled layout (zero for
+      // the padding rows of the tile)
+      constexpr bool kQuant = (EPI == kEpiGeluMxfp8 || EPI == kEpiGeluMxfp4);
+      float mul[4] = {1.0f, 1.0f, 1.0f, 1.0f};
+      if constexpr (kQuant) {
 #pragma unroll
-      for (int j = 0; j < 128 / EC; ++j) {
-        const int x = n0 + EC * j;
-        if (x >= args.N || m0 >= args.M) break;  // nothing of this chunk is stored (warp-uniform)
+        for (int c = 0; c < 128; ++c) acc[c >> 5][c & 31] = __float_as_uint(value(c));
+        constexpr uint32_t kEmax = (EPI == kEpiGeluMxfp8) ? 8u : 2u;
+        uint32_t word = 0;
+#pragma unroll
+        for (int bk = 0; bk < 4; ++bk) {
+          float amax = 0.0f;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(__uint_as_float(acc[bk][i])));
+          const uint32_t ef = __float_as_uint(amax) >> 23;
+          const uint32_t sbyte = ef > kEmax ? ef - kEmax : 0u;
+          mul[bk] = __uint_as_float((254u - sbyte) << 23);  // 2^(127 - sbyte), exact
+          word |= sbyte << (8 * bk);
+        }
+        // rows of the padded output tiles only: with an odd number of 128-row tiles the last
+        // pair's second CTA computes a tile that lies wholly past them
+        const uint32_t r = static_cast<uint32_t>(m0) + lane;
+        if (n0 < args.N && (r >> 7) < (static_cast<uint32_t>(args.M) + 127u) >> 7) {
+          const uint64_t off = (static_cast<uint64_t>(r >> 7) * static_cast<uint64_t>(args.q_nct) +
+                                static_cast<uint64_t>(n0 >> 7)) * 512 + (r & 31u) * 16 + ((r >> 5) & 3u) * 4;
+          *reinterpret_cast<uint32_t*>(args.qscales + off) = r < static_cast<uint32_t>(args.M) ? word : 0u;
+        }
+      }
+
+      // store: chunks of 32 rows x RB bytes through the staging buffer and TMA
+      constexpr int EC = C::kEpiCols;
+      constexpr int RB = EC * 2;  // bytes of a staged row: 64 or 32
+      constexpr int kRowBytes = (EPI == kEpiGeluMxfp8) ? 128 : (EPI == kEpiGeluMxfp4 ? 64 : 256);
+      const int row_units = (EPI == kEpiGeluMxfp4) ? (args.N >> 1) : args.N;  // TMA x extent of a row
+#pragma unroll
+      for (int j = 0; j < kRowBytes / RB; ++j) {
+        int x;  // first TMA x coordinate of the chunk (bf16 elements or code bytes)
+        if constexpr (EPI == kEpiBf16 || EPI == kEpiGeluBf16) x = n0 + (RB / 2) * j;
+        else if constexpr (EPI == kEpiGeluMxfp8) x = n0 + RB * j;
+        else x = (n0 >> 1) + RB * j;
+        if (x >= row_units || m0 >= args.M) break;  // nothing of this chunk is stored (warp-uniform)
         uint8_t* stage_buf = stage_base + (nstores % NB) * L::kEpiChunkBytes;
         if (lane == 0) bulk_wait_group_read<NB - 1>();  // the store that last used this buffer has read it
         __syncwarp();
-        uint32_t packed[EC / 2];
+        uint32_t packed[RB / 4];
 #pragma unroll
-        for (int c = 0; c < EC / 2; ++c) {
-          const int col = EC * j + 2 * c;  // column within this warp's 128
-          const float b0 = bias_s[col], b1 = bias_s[col + 1];
-          float v0 = __uint_as_float(acc[col >> 5][col & 31]), v1 = __uint_as_float(acc[col >> 5][(col + 1) & 31]);
-          if constexpr (FMT == BSQ_NVFP4) {
-            v0 = __fmaf_rn(v0, alpha, b0);
-            v1 = __fmaf_rn(v1, alpha, b1);
+        for (int c = 0; c < RB / 4; ++c) {
+          if constexpr (EPI == kEpiBf16 || EPI == kEpiGeluBf16) {
+            const int col = (RB / 2) * j + 2 * c;  // two bf16 per word
+            __nv_bfloat162 p = __floats2bfloat162_rn(value(col), value(col + 1));
+            packed[c] = *reinterpret_cast<uint32_t*>(&p);
+          } else if constexpr (EPI == kEpiGeluMxfp8) {
+            const int col = RB * j + 4 * c;  // four E4M3 codes per word, one block
+            const float m = mul[col >> 5];
+            packed[c] = cvt_e4m3x4(__uint_as_float(acc[col >> 5][col & 31]) * m,
+                                   __uint_as_float(acc[col >> 5][(col + 1) & 31]) * m,
+                                   __uint_as_float(acc[col >> 5][(col + 2) & 31]) * m,
+                                   __uint_as_float(acc[col >> 5][(col + 3) & 31]) * m);
           } else {
-            v0 = __fadd_rn(v0, b0);
-            v1 = __fadd_rn(v1, b1);
+            const int col = 2 * RB * j + 8 * c;  // eight e2m1 codes per word, one block
+            const float m = mul[col >> 5];
+            float y[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) y[i] = __uint_as_float(acc[col >> 5][(col + i) & 31]) * m;
+            packed[c] = cvt_e2m1x8(y);
           }
-          __nv_bfloat162 p = __floats2bfloat162_rn(v0, v1);
-          packed[c] = *reinterpret_cast<uint32_t*>(&p);
         }
-        // row `lane` of the 32 x EC chunk in 16-byte pieces; the TMA swizzle (64B or 32B mode)
+        // row `lane` of the 32 x RB chunk in 16-byte pieces; the TMA swizzle (64B or 32B mode)
         // XORs the piece index with address bits 7.. so that a quarter-warp hits distinct banks
 #pragma unroll
-        for (int q = 0; q < EC / 8; ++q) {
-          const uint32_t sw = (EC == 32) ? ((lane >> 1) & 3u) : ((lane >> 2) & 1u);
+        for (int q = 0; q < RB / 16; ++q) {
+          const uint32_t sw = (RB == 64) ? ((lane >> 1) & 3u) : ((lane >> 2) & 1u);
           const uint32_t phys = (static_cast<uint32_t>(q) ^ sw) << 4;
-          *reinterpret_cast<uint4*>(stage_buf + lane * (EC * 2) + phys) =
+          *reinterpret_cast<uint4*>(stage_buf + lane * RB + phys) =
               make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
         }
         fence_proxy_async_smem();
@@ -448,18 +516,19 @@ cudaLaunchConfig_t pair_launch_config(cudaLaunchAttribute* attr, int clusters, i
   return cfg;
 }
 
-template <int FMT>
+template <int FMT, int EPI>
 int run_gemm(const void* A, const void* A_scales, const void* B, const void* B_scales, const void* bias, void* out,
-             int64_t M, int64_t N, int64_t K, cudaStream_t stream, const DeviceInfo& dev) {
+             void* out_scales, int64_t M, int64_t N, int64_t K, cudaStream_t stream, const DeviceInfo& dev) {
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
   static int max_clusters = 0;
   std::call_once(attr_once, [] {
-    attr_err = cudaFuncSetAttribute(gemm_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<FMT>::alloc);
+    attr_err = cudaFuncSetAttribute(gemm_kernel<FMT, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    Smem<FMT>::alloc);
     if (attr_err != cudaSuccess) return;
     cudaLaunchAttribute at[2];
     cudaLaunchConfig_t cfg = pair_launch_config(at, 1, kThreads, Smem<FMT>::alloc, nullptr);
-    attr_err = cudaOccupancyMaxActiveClusters(&max_clusters, gemm_kernel<FMT>, &cfg);
+    attr_err = cudaOccupancyMaxActiveClusters(&max_clusters, gemm_kernel<FMT, EPI>, &cfg);
     if (attr_err == cudaSuccess && max_clusters < 1) attr_err = cudaErrorInvalidConfiguration;
   });
   if (attr_err != cudaSuccess) return BSQ_ERR_LAUNCH;
@@ -467,18 +536,28 @@ int run_gemm(const void* A, const void* A_scales, const void* B, const void* B_s
   const uint64_t kbytes = (FMT == BSQ_MXFP8) ? static_cast<uint64_t>(K) : static_cast<uint64_t>(K) / 2;
   CUtensorMap mA, mB, mSfa, mSfb, mOut;
   constexpr int EC = Cfg<FMT>::kEpiCols;
-  if (!make_map_2d(&mA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, kbytes, M, kbytes, kChunkBytes, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+  const CUtensorMapSwizzle osw = EC == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
+  bool ok_out;
+  if constexpr (EPI == kEpiBf16 || EPI == kEpiGeluBf16) {
+    ok_out = make_map_2d(&mOut, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, out, N, M, static_cast<uint64_t>(N) * 2, EC, 32, osw);
+  } else {
+    // code bytes of an output row: N (E4M3) or N / 2 (e2m1); staged rows of 2 * EC bytes
+    const uint64_t rb = (EPI == kEpiGeluMxfp8) ? static_cast<uint64_t>(N) : static_cast<uint64_t>(N) / 2;
+    ok_out = make_map_2d(&mOut, CU_TENSOR_MAP_DATA_TYPE_UINT8, out, rb, M, rb, 2 * EC, 32, osw);
+  }
+  if (!ok_out ||
+      !make_map_2d(&mA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, kbytes, M, kbytes, kChunkBytes, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_map_2d(&mB, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, kbytes, N, kbytes, kChunkBytes, BNH, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_map_scales(&mSfa, A_scales, static_cast<uint64_t>(ceil_div(K / block_size(FMT), 4)),
                        static_cast<uint64_t>(ceil_div(M, 128)), Cfg<FMT>::kAtoms, 1) ||
       !make_map_scales(&mSfb, B_scales, static_cast<uint64_t>(ceil_div(K / block_size(FMT), 4)),
-                       static_cast<uint64_t>(ceil_div(N, 128)), Cfg<FMT>::kAtoms, 2) ||
-      !make_map_2d(&mOut, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, out, N, M, static_cast<uint64_t>(N) * 2, EC, 32,
-                   EC == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B))
+                       static_cast<uint64_t>(ceil_div(N, 128)), Cfg<FMT>::kAtoms, 2))
     return BSQ_ERR_LAUNCH;
 
   GemmArgs a{};
   a.bias = static_cast<const uint16_t*>(bias);
+  a.qscales = static_cast<uint8_t*>(out_scales);
+  a.q_nct = static_cast<int>(ceil_div(N / 32, 4));
   a.ga = reinterpret_cast<const float*>(static_cast<const uint8_t*>(A_scales) + scales_body_bytes(FMT, M, K));
   a.gb = reinterpret_cast<const float*>(static_cast<const uint8_t*>(B_scales) + scales_body_bytes(FMT, N, K));
   a.M = static_cast<int>(M);
@@ -491,21 +570,41 @@ int run_gemm(const void* A, const void* A_scales, const void* B, const void* B_s
 
   cudaLaunchAttribute at[2];
   cudaLaunchConfig_t cfg = pair_launch_config(at, clusters, kThreads, Smem<FMT>::alloc, stream);
-  if (cudaLaunchKernelEx(&cfg, gemm_kernel<FMT>, mA, mB, mSfa, mSfb, mOut, a) != cudaSuccess) return BSQ_ERR_LAUNCH;
+  if (cudaLaunchKernelEx(&cfg, gemm_kernel<FMT, EPI>, mA, mB, mSfa, mSfb, mOut, a) != cudaSuccess)
+    return BSQ_ERR_LAUNCH;
   return cudaGetLastError() == cudaSuccess ? BSQ_OK : BSQ_ERR_LAUNCH;
+}
+
+template <int FMT>
+int run_gemm_epi(int epi, const void* A, const void* A_scales, const void* B, const void* B_scales, const void* bias,
+                 void* out, void* out_scales, int64_t M, int64_t N, int64_t K, cudaStream_t stream,
+                 const DeviceInfo& dev) {
+  switch (epi) {
+    case kEpiBf16:
+      return run_gemm<FMT, kEpiBf16>(A, A_scales, B, B_scales, bias, out, out_scales, M, N, K, stream, dev);
+    case kEpiGeluBf16:
+      return run_gemm<FMT, kEpiGeluBf16>(A, A_scales, B, B_scales, bias, out, out_scales, M, N, K, stream, dev);
+    case kEpiGeluMxfp8:
+      return run_gemm<FMT, kEpiGeluMxfp8>(A, A_scales, B, B_scales, bias, out, out_scales, M, N, K, stream, dev);
+    case kEpiGeluMxfp4:
+      return run_gemm<FMT, kEpiGeluMxfp4>(A, A_scales, B, B_scales, bias, out, out_scales, M, N, K, stream, dev);
+    default:
+      return BSQ_ERR_ARG;
+  }
 }
 
 }  // namespace
 
-int launch_gemm(int fmt, const void* A, const void* A_scales, const void* B, const void* B_scales, const void* bias,
-                void* out, int64_t M, int64_t N, int64_t K, cudaStream_t stream, const DeviceInfo& dev) {
+int launch_gemm(int fmt, int epi, const void* A, const void* A_scales, const void* B, const void* B_scales,
+                const void* bias, void* out, void* out_scales, int64_t M, int64_t N, int64_t K, cudaStream_t stream,
+                const DeviceInfo& dev) {
   switch (fmt) {
     case BSQ_MXFP8:
-      return run_gemm<BSQ_MXFP8>(A, A_scales, B, B_scales, bias, out, M, N, K, stream, dev);
+      return run_gemm_epi<BSQ_MXFP8>(epi, A, A_scales, B, B_scales, bias, out, out_scales, M, N, K, stream, dev);
     case BSQ_NVFP4:
-      return run_gemm<BSQ_NVFP4>(A, A_scales, B, B_scales, bias, out, M, N, K, stream, dev);
+      return run_gemm_epi<BSQ_NVFP4>(epi, A, A_scales, B, B_scales, bias, out, out_scales, M, N, K, stream, dev);
     case BSQ_MXFP4:
-      return run_gemm<BSQ_MXFP4>(A, A_scales, B, B_scales, bias, out, M, N, K, stream, dev);
+      return run_gemm_epi<BSQ_MXFP4>(epi, A, A_scales, B, B_scales, bias, out, out_scales, M, N, K, stream, dev);
     default:
       return BSQ_ERR_ARG;
   }

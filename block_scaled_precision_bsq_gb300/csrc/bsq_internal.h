@@ -34,8 +34,11 @@ using QuantItem = bsq_quant_item;
 int launch_quantize_batch(int fmt, bool src_f32, bool global_given, int count, const QuantItem* items,
                           cudaStream_t stream, const DeviceInfo& dev);
 
-int launch_gemm(int fmt, const void* A, const void* A_scales, const void* B, const void* B_scales, const void* bias,
-                void* out, int64_t M, int64_t N, int64_t K, cudaStream_t stream, const DeviceInfo& dev);
+// epi: 0 bf16 out, 1 GELU -> bf16, 2 GELU -> MXFP8 codes + scales, 3 GELU -> MXFP4 (out_scales
+// used by 2 and 3 only).
+int launch_gemm(int fmt, int epi, const void* A, const void* A_scales, const void* B, const void* B_scales,
+                const void* bias, void* out, void* out_scales, int64_t M, int64_t N, int64_t K, cudaStream_t stream,
+                const DeviceInfo& dev);
 
 int launch_selftest_timeout(int64_t limit_ns, cudaStream_t stream, const DeviceInfo& dev);
 

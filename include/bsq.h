@@ -138,6 +138,33 @@ int bsq_gemm(int fmt, const void* A, const void* A_scales, const void* B, const 
              const void* bias_bf16, void* out_bf16, int64_t M, int64_t N, int64_t K, bsq_stream_t stream);
 
 /*
+ * bsq_gemm_gelu: as bsq_gemm with out = bf16_rn(GELU(v)), v = alpha * sum_k Ahat Bhat + bias
+ * in fp32, GELU the exact erf form 0.5 v (1 + erf(v / sqrt 2)) evaluated in fp32 (the "fc1 +
+ * GELU" epilogue of every stack in the "lightly-train - DINOv3 + EoMT on RTX 5090" README,
+ * section 4.3). Arguments, shapes and errors as bsq_gemm.
+ */
+int bsq_gemm_gelu(int fmt, const void* A, const void* A_scales, const void* B, const void* B_scales,
+                  const void* bias_bf16, void* out_bf16, int64_t M, int64_t N, int64_t K, bsq_stream_t stream);
+
+/*
+ * bsq_gemm_gelu_quantize: the producer-fused fc1 of the README's MXFP8 stack (section 4.3: the
+ * fc1 epilogue quantizes the GELU output straight into fc2's operand). y = GELU(v) as in
+ * bsq_gemm_gelu, kept in fp32, then quantized along each output row with the MX rule of
+ * bsq_quantize into out_fmt (BSQ_MXFP8 or BSQ_MXFP4):
+ *   out_codes   bsq_codes_bytes(out_fmt, M, N) bytes, written;
+ *   out_scales  bsq_scales_bytes(out_fmt, M, N) bytes (tiled layout, padding zero), written.
+ * The pair is exactly an M x N operand as bsq_quantize(out_fmt, y, M, N) lays it out, ready
+ * as fc2's A. Codes and scales are the MX quantization of the kernel's fp32 y, which differs
+ * from the exact value by the fp32 accumulation and GELU rounding; a code differs from the
+ * exact value's code only where that value lies within this error of a rounding boundary.
+ * Shapes: as bsq_gemm, and N % 32 == 0. Errors: as bsq_gemm; BSQ_ERR_ARG for another out_fmt
+ * or a NULL out_scales; BSQ_ERR_ALIGN for an unaligned out_scales.
+ */
+int bsq_gemm_gelu_quantize(int fmt, const void* A, const void* A_scales, const void* B, const void* B_scales,
+                           const void* bias_bf16, int out_fmt, void* out_codes, void* out_scales, int64_t M,
+                           int64_t N, int64_t K, bsq_stream_t stream);
+
+/*
  * bsq_get_device_status: synchronise `stream`, then read and clear the current device's
  * status word. Returns BSQ_OK, BSQ_ERR_TIMEOUT (a kernel's bounded wait on an mbarrier
  * gave up; that kernel returned early and its outputs are incomplete) or BSQ_ERR_LAUNCH

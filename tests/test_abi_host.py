@@ -78,6 +78,12 @@ def test_argument_errors_before_any_cuda_call(bsq):
     assert bsq.bsq_gemm(bsq.MXFP8, p, p, p, p, None, p, 128, 256, 96) == bsq.ERR_SHAPE    # K % 128
     assert bsq.bsq_gemm(bsq.NVFP4, p, p, p, p, None, p, 128, 256, 128) == bsq.ERR_SHAPE   # K % 256
     assert bsq.bsq_gemm(bsq.MXFP4, p, p, p, p, None, p, 128, 260, 256) == bsq.ERR_SHAPE   # N % 8
+    assert bsq.bsq_gemm_gelu(bsq.MXFP8, p, p, p, p, None, p, 128, 256, 96) == bsq.ERR_SHAPE  # K % 128
+    gq = bsq.bsq_gemm_gelu_quantize
+    assert gq(bsq.MXFP8, p, p, p, p, None, bsq.NVFP4, p, p, 128, 256, 256) == bsq.ERR_ARG      # out fmt
+    assert gq(bsq.MXFP8, p, p, p, p, None, bsq.MXFP8, p, None, 128, 256, 256) == bsq.ERR_ARG   # no scales
+    assert gq(bsq.MXFP8, p, p, p, p, None, bsq.MXFP8, p, p, 128, 264, 256) == bsq.ERR_SHAPE   # N % 32
+    assert gq(bsq.MXFP8, p, p, p, p, None, bsq.MXFP4, p, p + 4, 128, 256, 256) == bsq.ERR_ALIGN
     assert bsq.bsq_gemm(bsq.MXFP8, p, p, p, p, None, None, 128, 256, 256) == bsq.ERR_ARG
     assert bsq.bsq_gemm(bsq.MXFP8, p, p + 4, p, p, None, p, 128, 256, 256) == bsq.ERR_ALIGN
     assert bsq.bsq_gemm(bsq.MXFP8, p, p, p, p, p + 1, p, 128, 256, 256) == bsq.ERR_ALIGN
