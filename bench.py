@@ -167,6 +167,7 @@ def cpu_oracle_sample(gemms, target_s: float = 10.0):
 def config_of(wl):
     return {"workload": wl.name, "description": wl.description,
             "gemms": [{"name": g.name, "format": g.fmt, "M": g.M, "N": g.N, "K": g.K} for g in wl.gemms],
+            "chain": wl.chain,
             "l2": "flushed between timed steps (256 MB write)",
             "launch": "one step (L2 flush; per layer quantize A+B, then the GEMM) captured once into a CUDA "
                       "graph with CUDA events as graph nodes around each layer's quantize and GEMM; replayed "
@@ -260,59 +261,107 @@ def run_gpu(args, rank: int, world: int):
         t = torch.from_numpy(x.view(np.int16) if x.dtype == np.uint16 else x)
         return (t.view(torch.bfloat16) if x.dtype == np.uint16 else t).pin_memory()
 
-    layers = []
-    for g in wl.gemms:
-        a, b, bias = make_activations(g), make_weights(g), make_bias(g)
-        ha, hb = host(a), host(b)
-        hbias = host(bias) if bias is not None else None
-        L = {"g": g, "ha": ha, "hb": hb, "hbias": hbias,
-             "a": ha.to(dev), "b": hb.to(dev), "bias": hbias.to(dev) if hbias is not None else None,
-             "qa": bsq.empty_qtensor(g.fmt, g.M, g.K, dev), "qb": bsq.empty_qtensor(g.fmt, g.N, g.K, dev),
-             "out": torch.empty((g.M, g.N), dtype=torch.bfloat16, device=dev),
-             "hout": torch.empty((g.M, g.N), dtype=torch.bfloat16).pin_memory()}
-        layers.append(L)
+    # A unit is the work of one layer (or of one chained MLP): pinned host inputs, a device
+    # buffer set (`alloc`; e2e double-buffers them), and the quantize / GEMM phases.
+    units = []
+    if wl.chain is None:
+        for g in wl.gemms:
+            bias = make_bias(g)
+            hosts = {"a": host(make_activations(g)), "b": host(make_weights(g)),
+                     "bias": host(bias) if bias is not None else None}
+
+            def alloc(g=g, hosts=hosts):
+                return {"a": torch.empty_like(hosts["a"], device=dev), "b": torch.empty_like(hosts["b"], device=dev),
+                        "bias": torch.empty_like(hosts["bias"], device=dev) if hosts["bias"] is not None else None,
+                        "qa": bsq.empty_qtensor(g.fmt, g.M, g.K, dev), "qb": bsq.empty_qtensor(g.fmt, g.N, g.K, dev),
+                        "out": torch.empty((g.M, g.N), dtype=torch.bfloat16, device=dev)}
+
+            def quant(D, s, g=g):
+                # activations and weights of the layer in one launch (bsq_quantize_batch)
+                bsq.quantize_many(g.fmt, [D["a"], D["b"]], outs=[D["qa"], D["qb"]], stream=s)
+
+            def gemm(D, s):
+                bsq.gemm(D["qa"], D["qb"], D["bias"], out=D["out"], stream=s)
+
+            units.append({"hosts": hosts, "alloc": alloc, "quant": quant, "gemm": gemm, "fmt": g.fmt,
+                          "flops": g.flops, "launches": 2 + (2 if g.fmt == NVFP4 else 0),
+                          "qbytes": quant_bytes(g.fmt, g.M, g.K, 4 if g.src_f32 else 2, True) +
+                                    quant_bytes(g.fmt, g.N, g.K, 4 if g.src_f32 else 2, True),
+                          "gbytes": gemm_bytes(g.fmt, g.M, g.N, g.K, bias is not None)})
+    else:
+        g1, g2 = wl.gemms  # fc1: M x K1 -> N1, fc2: M x N1 -> N2
+        fmt = g1.fmt
+        b1, b2 = make_bias(g1), make_bias(g2)
+        hosts = {"x": host(make_activations(g1)), "w1": host(make_weights(g1)), "w2": host(make_weights(g2)),
+                 "b1": host(b1), "b2": host(b2)}
+        fused = wl.chain == "fused"
+
+        def alloc():
+            D = {k: torch.empty_like(v, device=dev) for k, v in hosts.items()}
+            D.update({"qx": bsq.empty_qtensor(fmt, g1.M, g1.K, dev), "qw1": bsq.empty_qtensor(fmt, g1.N, g1.K, dev),
+                      "qw2": bsq.empty_qtensor(fmt, g2.N, g2.K, dev), "qh": bsq.empty_qtensor(fmt, g2.M, g2.K, dev),
+                      "out": torch.empty((g2.M, g2.N), dtype=torch.bfloat16, device=dev)})
+            if not fused:
+                D["h"] = torch.empty((g1.M, g1.N), dtype=torch.bfloat16, device=dev)
+            return D
+
+        def quant(D, s):
+            bsq.quantize_many(fmt, [D["x"], D["w1"], D["w2"]], outs=[D["qx"], D["qw1"], D["qw2"]], stream=s)
+
+        def gemm(D, s):
+            if fused:  # fc1's epilogue writes fc2's operand
+                bsq.gemm_gelu_quantize(D["qx"], D["qw1"], D["b1"], out_fmt=fmt, out=D["qh"], stream=s)
+            else:      # fc1 + GELU to bf16, then a quantize pass
+                bsq.gemm_gelu(D["qx"], D["qw1"], D["b1"], out=D["h"], stream=s)
+                bsq.quantize(fmt, D["h"], out=D["qh"], stream=s)
+            bsq.gemm(D["qh"], D["qw2"], D["b2"], out=D["out"], stream=s)
+
+        units.append({"hosts": hosts, "alloc": alloc, "quant": quant, "gemm": gemm, "fmt": fmt,
+                      "flops": g1.flops + g2.flops, "launches": 3 if fused else 4,
+                      "qbytes": sum(quant_bytes(fmt, r, c, 2, True) for r, c in ((g1.M, g1.K), (g1.N, g1.K), (g2.N, g2.K))),
+                      "gbytes": gemm_bytes(fmt, g1.M, g1.N, g1.K, True) + gemm_bytes(fmt, g2.M, g2.N, g2.K, True) -
+                                (2 * g1.M * g1.N if fused else 0) +
+                                (g1.M * g1.N * (1 if fmt == MXFP8 else 0.5) if fused else 0)})
+    for U in units:
+        U["D"] = U["alloc"]()
+        for k, v in U["hosts"].items():
+            if v is not None:
+                U["D"][k].copy_(v)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-
-    def quantize_layer(L, s):
-        # activations and weights of the layer in one launch (bsq_quantize_batch)
-        bsq.quantize_many(L["g"].fmt, [L["a"], L["b"]], outs=[L["qa"], L["qb"]], stream=s)
-
-    def gemm_layer(L, s):
-        bsq.gemm(L["qa"], L["qb"], L["bias"], out=L["out"], stream=s)
 
     # warm-up through the direct calls (first calls set kernel attributes, build tables)
     for _ in range(args.warmup):
-        for L in layers:
-            quantize_layer(L, stream)
-            gemm_layer(L, stream)
+        for U in units:
+            U["quant"](U["D"], stream)
+            U["gemm"](U["D"], stream)
     torch.cuda.synchronize()
     assert bsq.device_status() == 0
 
-    # the whole step as one CUDA graph: flush, then per layer event / quantize / event / GEMM /
+    # the whole step as one CUDA graph: flush, then per unit event / quantize / event / GEMM /
     # event, with the events recorded by graph nodes
-    evs = [tuple(torch.cuda.Event(enable_timing=True, external=True) for _ in range(3)) for _ in layers]
+    evs = [tuple(torch.cuda.Event(enable_timing=True, external=True) for _ in range(3)) for _ in units]
     cap = torch.cuda.Stream(device=dev)
     cap.wait_stream(stream)
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=cap):
         flush.zero_()
-        for L, e in zip(layers, evs):
+        for U, e in zip(units, evs):
             e[0].record(cap)
-            quantize_layer(L, cap)
+            U["quant"](U["D"], cap)
             e[1].record(cap)
-            gemm_layer(L, cap)
+            U["gemm"](U["D"], cap)
             e[2].record(cap)
     torch.cuda.synchronize()
 
     def step():
-        """One replay; returns per layer (quantize ms, GEMM ms)."""
+        """One replay; returns per unit (quantize ms, GEMM ms)."""
         graph.replay()
         evs[-1][2].synchronize()
         return [(e[0].elapsed_time(e[1]), e[1].elapsed_time(e[2])) for e in evs]
 
-    # our kernels per step and layer: 1 batched quantize (+1 amax pass per matrix for NVFP4)
-    # + 1 GEMM
-    launches_per_step = sum(2 + (2 if L["g"].fmt == NVFP4 else 0) for L in layers)
+    # our kernels per step (the batched quantize counts once; NVFP4 adds an amax pass per
+    # matrix; a chained MLP's unfused variant adds its quantize pass)
+    launches_per_step = sum(U["launches"] for U in units)
 
     for _ in range(args.warmup):
         step()
@@ -345,64 +394,59 @@ def run_gpu(args, rank: int, world: int):
     q_ms = [sum(t[0] for t in ts) for ts in times]
     g_ms = [sum(t[1] for t in ts) for ts in times]
     step_ms = [q + g for q, g in zip(q_ms, g_ms)]
-    flops = sum(L["g"].flops for L in layers)
+    flops = sum(U["flops"] for U in units)
     ms_per_step, value = replica_throughput(float(np.mean(step_ms)), flops, world, dev)
 
     # dominant kernel: the GEMM
-    fmt0 = layers[0]["g"].fmt
+    fmt0 = units[0]["fmt"]
     gemm_ms = float(np.mean(g_ms))
     gemm_tflops = flops / (gemm_ms * 1e-3) / 1e12
     peak_bf16 = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
     peak_tc = peak_bf16 * NOMINAL_RATIO[fmt0]
     khash = kernel_source_hash()
     traffic = recorded_traffic(khash, wl.name)
-    q_bytes = sum(quant_bytes(L["g"].fmt, L["g"].M, L["g"].K, 4 if L["g"].src_f32 else 2, True) +
-                  quant_bytes(L["g"].fmt, L["g"].N, L["g"].K, 4 if L["g"].src_f32 else 2, True) for L in layers)
+    q_bytes = sum(U["qbytes"] for U in units)
     q_ms_mean = float(np.mean(q_ms))
     q_gbs = q_bytes / (q_ms_mean * 1e-3) / 1e9
     hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
-    g_bytes = sum(gemm_bytes(L["g"].fmt, L["g"].M, L["g"].N, L["g"].K, L["bias"] is not None) for L in layers)
+    g_bytes = int(sum(U["gbytes"] for U in units))
     t_ideal = max(flops / (peak_tc * 1e12), g_bytes / (hbm * 1e9))
 
     # ------------------------------------------------------------ end to end through host buffers
     e2e_steps = max(3, min(args.steps, args.e2e_steps))
-    h2d = sum(L["ha"].numel() * L["ha"].element_size() + L["hb"].numel() * L["hb"].element_size() +
-              (L["hbias"].numel() * 2 if L["hbias"] is not None else 0) for L in layers)
-    d2h = sum(L["hout"].numel() * 2 for L in layers)
+    h2d = sum(v.numel() * v.element_size() for U in units for v in U["hosts"].values() if v is not None)
+    d2h = sum(U["D"]["out"].numel() * 2 for U in units)
 
-    # two device buffer sets; streams: copy in, compute, copy out
+    # two device buffer sets per unit; streams: copy in, compute, copy out
     s_in, s_cmp, s_out = (torch.cuda.Stream(device=dev) for _ in range(3))
     bufs = []
     for j in range(2):
-        bj = []
-        for L in layers:
-            g = L["g"]
-            bj.append({"a": torch.empty_like(L["a"]), "b": torch.empty_like(L["b"]),
-                       "bias": torch.empty_like(L["bias"]) if L["bias"] is not None else None,
-                       "qa": bsq.empty_qtensor(g.fmt, g.M, g.K, dev), "qb": bsq.empty_qtensor(g.fmt, g.N, g.K, dev),
-                       "out": torch.empty_like(L["out"]), "hout": torch.empty_like(L["hout"]).pin_memory()})
-        bufs.append({"L": bj, "in_done": torch.cuda.Event(), "cmp_done": torch.cuda.Event(),
+        sets = []
+        for U in units:
+            D = U["alloc"]()
+            D["hout"] = torch.empty(D["out"].shape, dtype=torch.bfloat16).pin_memory()
+            sets.append(D)
+        bufs.append({"D": sets, "in_done": torch.cuda.Event(), "cmp_done": torch.cuda.Event(),
                      "out_done": torch.cuda.Event()})
 
     def e2e_step(i):
         B = bufs[i % 2]
         with torch.cuda.stream(s_in):
             s_in.wait_event(B["cmp_done"])  # inputs of the step two back consumed
-            for L, D in zip(layers, B["L"]):
-                D["a"].copy_(L["ha"], non_blocking=True)
-                D["b"].copy_(L["hb"], non_blocking=True)
-                if L["hbias"] is not None:
-                    D["bias"].copy_(L["hbias"], non_blocking=True)
+            for U, D in zip(units, B["D"]):
+                for k, v in U["hosts"].items():
+                    if v is not None:
+                        D[k].copy_(v, non_blocking=True)
             B["in_done"].record(s_in)
         s_cmp.wait_event(B["in_done"])
         s_cmp.wait_event(B["out_done"])  # result of the step two back copied out
-        for L, D in zip(layers, B["L"]):
-            bsq.quantize_many(L["g"].fmt, [D["a"], D["b"]], outs=[D["qa"], D["qb"]], stream=s_cmp)
-            bsq.gemm(D["qa"], D["qb"], D["bias"], out=D["out"], stream=s_cmp)
+        for U, D in zip(units, B["D"]):
+            U["quant"](D, s_cmp)
+            U["gemm"](D, s_cmp)
         B["cmp_done"].record(s_cmp)
         with torch.cuda.stream(s_out):
             s_out.wait_event(B["cmp_done"])
-            for D in B["L"]:
+            for D in B["D"]:
                 D["hout"].copy_(D["out"], non_blocking=True)
             B["out_done"].record(s_out)
 

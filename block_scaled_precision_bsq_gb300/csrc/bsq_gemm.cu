@@ -124,11 +124,31 @@ __host__ __device__ constexpr uint32_t make_idesc(uint32_t sf_id) {
 // bf16(GELU(v)) (the "fc1 + GELU" epilogue every stack of the "lightly-train - DINOv3 + EoMT on
 // RTX 5090" README fuses, section 4.3). kEpiGeluMxfp8 / kEpiGeluMxfp4: GELU(v) quantized along
 // the output row straight into MX codes and tiled scales, the fc2 operand (the MXFP8 stack's
-// fc1 epilogue, same section); bytes laid out as bsq_quantize writes them. GELU is the exact
-// erf form, evaluated as 0.5 v erfc(-v / sqrt 2) (no cancellation for negative v).
+// fc1 epilogue, same section); bytes laid out as bsq_quantize writes them.
 enum EpiMode { kEpiBf16 = 0, kEpiGeluBf16 = 1, kEpiGeluMxfp8 = 2, kEpiGeluMxfp4 = 3 };
 
-__device__ __forceinline__ float gelu_erf(float v) { return 0.5f * v * erfcf(-v * 0.7071067811865476f); }
+// GELU(v) = v Phi(v) (the erf form) with Phi(v) = 1 - erfc(z) / 2 for v >= 0 and erfc(z) / 2
+// for v < 0, z = |v| / sqrt 2 (no cancellation in the negative tail), and erfc from
+// Abramowitz & Stegun, Handbook of Mathematical Functions, formula 7.1.26:
+//   erfc(z) = (a1 t + a2 t^2 + a3 t^3 + a4 t^4 + a5 t^5) exp(-z^2) + err, t = 1 / (1 + p z),
+//   |err| <= 1.5e-7.
+// One reciprocal and one exp2 on the special-function unit and five FMAs: the epilogue runs
+// it on every output of a tile while the next tile's MMAs run. Measured in fp32 against the
+// exact function: |GELU_kernel(v) - GELU(v)| <= 1e-7 |v| + 2^-21 |GELU(v)| (plus about one
+// ulp from the hardware reciprocal and exp2).
+__device__ __forceinline__ float gelu_erf(float v) {
+  const float z = fabsf(v) * 0.7071067811865476f;
+  float t;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(t) : "f"(fmaf(0.3275911f, z, 1.0f)));
+  float poly = fmaf(1.061405429f, t, -1.453152027f);
+  poly = fmaf(poly, t, 1.421413741f);
+  poly = fmaf(poly, t, -0.284496736f);
+  poly = fmaf(poly, t, 0.254829592f);
+  float e;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(-(z * z) * 1.4426950408889634f));
+  const float h = 0.5f * (poly * t) * e;  // erfc(z) / 2
+  return v * (v >= 0.0f ? 1.0f - h : h);
+}
 
 struct GemmArgs {
   const uint16_t* bias;  // nullable

@@ -139,9 +139,10 @@ int bsq_gemm(int fmt, const void* A, const void* A_scales, const void* B, const 
 
 /*
  * bsq_gemm_gelu: as bsq_gemm with out = bf16_rn(GELU(v)), v = alpha * sum_k Ahat Bhat + bias
- * in fp32, GELU the exact erf form 0.5 v (1 + erf(v / sqrt 2)) evaluated in fp32 (the "fc1 +
- * GELU" epilogue of every stack in the "lightly-train - DINOv3 + EoMT on RTX 5090" README,
- * section 4.3). Arguments, shapes and errors as bsq_gemm.
+ * in fp32, GELU the erf form 0.5 v (1 + erf(v / sqrt 2)) (the "fc1 + GELU" epilogue of every
+ * stack in the "lightly-train - DINOv3 + EoMT on RTX 5090" README, section 4.3), evaluated in
+ * fp32 with erfc from Abramowitz & Stegun formula 7.1.26: |error| <= 4e-7 |v| + 2^-20 |GELU|.
+ * Arguments, shapes and errors as bsq_gemm.
  */
 int bsq_gemm_gelu(int fmt, const void* A, const void* A_scales, const void* B, const void* B_scales,
                   const void* bias_bf16, void* out_bf16, int64_t M, int64_t N, int64_t K, bsq_stream_t stream);

@@ -15,6 +15,9 @@ quantized GEMMs are qkv / proj / fc1 / fc2 of every ViT block):
   vitl_nvfp4      the same sweep in NVFP4 with Student-t(4) activations.
   vitl_mlp_large  M = 32*1600 tokens, fc1 1024->4096 and fc2 4096->1024, MXFP4 and NVFP4;
                   fc2's input is GELU of an N(0,1) pre-activation.
+  vitl_mlp_*_fused / _unfused
+                  one ViT-L/16 MLP, fc1 -> GELU -> fc2, with fc2's operand produced by fc1's
+                  epilogue (fused) or by a bf16 output and a separate quantize pass (unfused).
 
 Recipe (every array is drawn in fp64 by numpy's default_rng, cast to fp32 with
 round-to-nearest, then to bf16 with round-to-nearest-even where the input is bf16):
@@ -75,6 +78,9 @@ class Workload:
     name: str
     description: str
     gemms: List[Gemm]
+    # "fused" / "unfused": gemms = [fc1, fc2] of one MLP, fc2's A being GELU of fc1's output
+    # (quantized in fc1's epilogue, or written as bf16 and quantized by a separate pass)
+    chain: Optional[str] = None
 
 
 def _vitl_sweep(fmt: str, a_dist: str) -> List[Gemm]:
@@ -115,6 +121,19 @@ WORKLOADS: Dict[str, Workload] = {
         ],
     ),
 }
+
+
+def _mlp_chain(name: str, fmt: str, M: int, chain: str) -> Workload:
+    # fc1 weights N(0, 1/sqrt(1024)) so that fc1's outputs spread over the range where GELU
+    # bends; fc2 as in the other workloads
+    return Workload(name, "ViT-L/16 MLP fc1 -> GELU -> fc2 at M=%d, %s, fc2 operand %s" % (
+        M, fmt.upper(), "quantized in fc1's epilogue" if chain == "fused" else "from bf16 + a quantize pass"),
+        [Gemm("fc1", fmt, M, 1024, 4096, w_std=1.0 / 32.0), Gemm("fc2", fmt, M, 4096, 1024)], chain)
+
+
+for _fmt, _M, _tag in ((MXFP8, 7 * 1024, "vitl_mlp_mxfp8"), (MXFP4, 32 * 1600, "vitl_mlp_large_mxfp4")):
+    for _chain in ("fused", "unfused"):
+        WORKLOADS["%s_%s" % (_tag, _chain)] = _mlp_chain("%s_%s" % (_tag, _chain), _fmt, _M, _chain)
 
 
 def _gelu_erf(x: np.ndarray) -> np.ndarray:
