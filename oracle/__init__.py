@@ -78,6 +78,8 @@ def lib() -> ctypes.CDLL:
         L.orc_quantize_mx_f64.argtypes = [ctypes.c_int, f64p, i64, i64, u8p, u8p]
         L.orc_encode_array.restype = ctypes.c_int
         L.orc_encode_array.argtypes = [ctypes.c_int, f64p, i64, u8p]
+        L.orc_layernorm.restype = ctypes.c_int
+        L.orc_layernorm.argtypes = [vp, ctypes.c_int, vp, vp, ctypes.c_double, i64, i64, f64p]
         L.orc_num_threads.restype = ctypes.c_int
         L.orc_set_num_threads.argtypes = [ctypes.c_int]
         _lib = L
@@ -273,3 +275,21 @@ def encode_array(elem: str, v: np.ndarray) -> np.ndarray:
 def gelu_quantize_reference(fmt, y: np.ndarray) -> Quantized:
     """The fused fc1 step of reading R8 on the unrounded GEMM values y: MX(GELU(y))."""
     return quantize_mx_f64(fmt, gelu_erf(y))
+
+
+def layernorm(x: np.ndarray, gamma: np.ndarray, beta: np.ndarray, eps: float) -> np.ndarray:
+    """Row LayerNorm in fp64 (reading R9): x bf16 bits (uint16) or fp32; gamma, beta bf16 bits."""
+    x, is_f32 = _src(x)
+    rows, cols = x.shape
+    gamma = np.ascontiguousarray(gamma, dtype=np.uint16)
+    beta = np.ascontiguousarray(beta, dtype=np.uint16)
+    out = np.empty((rows, cols), dtype=np.float64)
+    st = lib().orc_layernorm(_ptr(x), is_f32, _ptr(gamma), _ptr(beta), float(eps), rows, cols, _ptr(out))
+    if st:
+        raise ValueError("oracle layernorm failed: %d" % st)
+    return out
+
+
+def layernorm_quantize_reference(fmt, x: np.ndarray, gamma: np.ndarray, beta: np.ndarray, eps: float) -> Quantized:
+    """The fused LN step of reading R9: MX(LayerNorm(x))."""
+    return quantize_mx_f64(fmt, layernorm(x, gamma, beta, eps))

@@ -44,6 +44,10 @@
  *       quantized is GELU(alpha * acc + bias) with GELU in its exact erf form
  *       0.5 v (1 + erf(v / sqrt 2)), taken before any bf16 rounding, then the MX rule R2
  *       along the output row. Here y is the unrounded fp64 value of R6.
+ *   R9  Producer-fused quantization of a LayerNorm output ([LT] section 4.3: the MXFP8 stack
+ *       merges LN and quantization into one kernel): y = (x - mean) / sqrt(var + eps) * gamma
+ *       + beta per row, mean and biased variance over the row (the usual LayerNorm), gamma and
+ *       beta bf16, taken before any bf16 rounding, then the MX rule R2 along the row.
  *
  * Pins (tests that tie this code to something other than itself) are in the test suite:
  * exhaustive decode tables against two independent float8/float4 libraries, encoders
@@ -469,5 +473,33 @@ int orc_encode_array(int elem, const double* v, int64_t n, uint8_t* out) {
     int64_t i;
     if (!v || !out || n < 0 || (elem != 0 && elem != 1)) return ORC_ERR_ARG;
     for (i = 0; i < n; ++i) out[i] = (uint8_t)(elem == 0 ? orc_encode_e4m3(v[i]) : orc_encode_e2m1(v[i]));
+    return ORC_OK;
+}
+
+/* LayerNorm of each row of a bf16 / fp32 rows x cols matrix in fp64 (reading R9):
+ * out[r, c] = (x[r, c] - mean_r) / sqrt(var_r + eps) * gamma[c] + beta[c], mean_r and the
+ * biased variance var_r over the row; gamma, beta: cols bf16 bits. */
+int orc_layernorm(const void* src, int src_f32, const uint16_t* gamma, const uint16_t* beta, double eps,
+                  int64_t rows, int64_t cols, double* out) {
+    int64_t r, st;
+    if (!src || !gamma || !beta || !out || rows <= 0 || cols <= 0 || eps < 0.0) return ORC_ERR_ARG;
+    st = check_finite(src, src_f32, rows * cols);
+    if (st) return (int)st;
+#pragma omp parallel for schedule(static)
+    for (r = 0; r < rows; ++r) {
+        double mean = 0.0, var = 0.0, rstd;
+        int64_t c;
+        for (c = 0; c < cols; ++c) mean += (double)load_src(src, src_f32, r * cols + c);
+        mean /= (double)cols;
+        for (c = 0; c < cols; ++c) {
+            double d = (double)load_src(src, src_f32, r * cols + c) - mean;
+            var += d * d;
+        }
+        var /= (double)cols;
+        rstd = 1.0 / sqrt(var + eps);
+        for (c = 0; c < cols; ++c)
+            out[r * cols + c] = ((double)load_src(src, src_f32, r * cols + c) - mean) * rstd *
+                                    (double)orc_bf16_to_f32(gamma[c]) + (double)orc_bf16_to_f32(beta[c]);
+    }
     return ORC_OK;
 }
