@@ -50,6 +50,8 @@ class QuantItem(ctypes.Structure):
 
 _lib.bsq_quantize_batch.restype = _int
 _lib.bsq_quantize_batch.argtypes = [_int, _int, ctypes.POINTER(QuantItem), _vp]
+_lib.bsq_layernorm_quantize.restype = _int
+_lib.bsq_layernorm_quantize.argtypes = [_int, _vp, _vp, _vp, ctypes.c_float, _i64, _i64, _vp, _vp, _vp]
 _lib.bsq_gemm.restype = _int
 _lib.bsq_gemm.argtypes = [_int, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp]
 _lib.bsq_gemm_gelu.restype = _int
@@ -64,7 +66,8 @@ _lib.bsq_last_error.restype = _int
 _lib.bsq_strerror.restype = ctypes.c_char_p
 _lib.bsq_strerror.argtypes = [_int]
 
-EXPORTS = ("bsq_codes_bytes", "bsq_scales_bytes", "bsq_quantize", "bsq_quantize_batch", "bsq_gemm",
+EXPORTS = ("bsq_codes_bytes", "bsq_scales_bytes", "bsq_quantize", "bsq_quantize_batch", "bsq_layernorm_quantize",
+           "bsq_gemm",
            "bsq_gemm_gelu", "bsq_gemm_gelu_quantize", "bsq_get_device_status", "bsq_selftest_timeout",
            "bsq_last_error", "bsq_strerror")
 
@@ -121,6 +124,12 @@ def bsq_quantize_batch(fmt_flags: int, items, stream=None) -> int:
         arr[i] = QuantItem(_p(src), rows, cols, _p(codes), _p(scales),
                            ctypes.cast(g, ctypes.POINTER(ctypes.c_float)) if g else None)
     return int(_lib.bsq_quantize_batch(int(fmt_flags), len(items), arr, _stream(stream)))
+
+
+def bsq_layernorm_quantize(fmt_flags: int, src: Ptr, gamma: Ptr, beta: Ptr, eps: float, rows: int, cols: int,
+                           codes: Ptr, scales: Ptr, stream=None) -> int:
+    return int(_lib.bsq_layernorm_quantize(int(fmt_flags), _p(src), _p(gamma), _p(beta), float(eps), rows, cols,
+                                           _p(codes), _p(scales), _stream(stream)))
 
 
 def bsq_gemm(fmt, A: Ptr, A_scales: Ptr, B: Ptr, B_scales: Ptr, bias: Ptr, out: Ptr, M: int, N: int, K: int,
@@ -223,6 +232,24 @@ def quantize_many(fmt, xs, outs=None, stream=None):
     if rc != OK:
         raise BsqError(rc, "bsq_quantize_batch")
     return qs
+
+
+def layernorm_quantize(fmt, x: torch.Tensor, gamma: torch.Tensor, beta: torch.Tensor, eps: float = 1e-6,
+                       out: Optional[QTensor] = None, stream=None) -> QTensor:
+    """Row LayerNorm (gamma, beta bf16) of a contiguous bf16 / fp32 CUDA matrix, quantized along
+    the row into MXFP8 / MXFP4 in the same kernel."""
+    f = _fmt(fmt)
+    assert x.is_cuda and x.is_contiguous() and x.dim() == 2, "x must be a contiguous 2-D CUDA tensor"
+    rows, cols = x.shape
+    assert gamma.dtype == torch.bfloat16 and beta.dtype == torch.bfloat16 and gamma.numel() == cols == beta.numel()
+    flags = f | (FLAG_SRC_F32 if x.dtype == torch.float32 else 0)
+    if x.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("x must be bfloat16 or float32")
+    q = out if out is not None else empty_qtensor(f, rows, cols, x.device)
+    rc = bsq_layernorm_quantize(flags, x, gamma, beta, eps, rows, cols, q.codes, q.scales, stream)
+    if rc != OK:
+        raise BsqError(rc, "bsq_layernorm_quantize")
+    return q
 
 
 def gemm(qa: QTensor, qb: QTensor, bias: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,

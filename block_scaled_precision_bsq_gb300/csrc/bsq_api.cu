@@ -2,6 +2,7 @@
 // properties, the device status word, and dispatch to the kernel launchers.
 #include <cuda_runtime.h>
 
+#include <cmath>
 #include <cstdint>
 #include <mutex>
 
@@ -125,6 +126,27 @@ int bsq_quantize_batch(int fmt_flags, int count, const bsq_quant_item* items, bs
   if (dev == nullptr) return fail(BSQ_ERR_ARCH);
   const int st = bsq::launch_quantize_batch(fmt, (flags & BSQ_FLAG_SRC_F32) != 0, given, count, local,
                                             reinterpret_cast<cudaStream_t>(stream), *dev);
+  return st == BSQ_OK ? BSQ_OK : fail(st);
+}
+
+int bsq_layernorm_quantize(int fmt_flags, const void* src, const void* gamma_bf16, const void* beta_bf16, float eps,
+                           int64_t rows, int64_t cols, void* codes, void* scales, bsq_stream_t stream) {
+  const int fmt = fmt_flags & BSQ_FMT_MASK;
+  const int flags = fmt_flags & ~BSQ_FMT_MASK;
+  if (fmt != BSQ_MXFP8 && fmt != BSQ_MXFP4) return fail(BSQ_ERR_ARG);
+  if (flags & ~BSQ_FLAG_SRC_F32) return fail(BSQ_ERR_ARG);
+  if (gamma_bf16 == nullptr || beta_bf16 == nullptr || !(eps >= 0.0f) || !(eps < INFINITY)) return fail(BSQ_ERR_ARG);
+  const bsq_quant_item item = {src, rows, cols, codes, scales, nullptr};
+  int st = check_quant_item(fmt, false, item);
+  if (st != BSQ_OK) return fail(st);
+  const bool f32 = (flags & BSQ_FLAG_SRC_F32) != 0;
+  if (cols * (f32 ? 4 : 2) > 16384) return fail(BSQ_ERR_SHAPE);
+  if (!aligned16(gamma_bf16) || !aligned16(beta_bf16)) return fail(BSQ_ERR_ALIGN);
+  const bsq::DeviceInfo* dev = bsq::current_device();
+  if (dev == nullptr) return fail(BSQ_ERR_ARCH);
+  st = bsq::launch_layernorm_quantize(fmt, f32, item, static_cast<const uint16_t*>(gamma_bf16),
+                                      static_cast<const uint16_t*>(beta_bf16), eps,
+                                      reinterpret_cast<cudaStream_t>(stream), *dev);
   return st == BSQ_OK ? BSQ_OK : fail(st);
 }
 

@@ -34,6 +34,11 @@ using QuantItem = bsq_quant_item;
 int launch_quantize_batch(int fmt, bool src_f32, bool global_given, int count, const QuantItem* items,
                           cudaStream_t stream, const DeviceInfo& dev);
 
+// Row LayerNorm then MX quantization of one matrix (fmt MXFP8 / MXFP4); rows must fit a chunk
+// (BSQ_ERR_SHAPE otherwise).
+int launch_layernorm_quantize(int fmt, bool src_f32, const QuantItem& item, const uint16_t* gamma,
+                              const uint16_t* beta, float eps, cudaStream_t stream, const DeviceInfo& dev);
+
 // epi: 0 bf16 out, 1 GELU -> bf16, 2 GELU -> MXFP8 codes + scales, 3 GELU -> MXFP4 (out_scales
 // used by 2 and 3 only).
 int launch_gemm(int fmt, int epi, const void* A, const void* A_scales, const void* B, const void* B_scales,

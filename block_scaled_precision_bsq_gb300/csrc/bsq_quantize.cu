@@ -43,6 +43,7 @@ constexpr int kChunkMax = 16384;        // bytes per chunk buffer
 constexpr int kChunkMin = 4096;         // smallest chunk worth a copy (small tensors)
 constexpr int kAmaxThreads = 256;
 constexpr int kMaxBatch = BSQ_MAX_BATCH;
+constexpr int kLnMaxRows = kChunkMax / (32 * 2);  // rows of a chunk: rows of at least 32 bf16
 
 enum NvMode { kMx = 0, kNvComputed = 1, kNvGiven = 2 };
 
@@ -63,6 +64,10 @@ struct QuantArgs {
   int64_t chunks_per_row;
   int64_t nchunks;
   uint32_t cols_magic;  // floor(2^32 / cols) + 1: f / cols == umulhi(f, cols_magic) for f * cols < 2^32
+  // LayerNorm mode: y = (x - mean) / sqrt(var + eps) * gamma + beta per row before quantizing
+  const uint16_t* gamma;  // cols bf16
+  const uint16_t* beta;   // cols bf16
+  float eps;
 };
 
 // Up to kMaxBatch matrices of one format and source type quantized by one launch: their
@@ -167,13 +172,17 @@ __device__ __forceinline__ uint32_t quantize16(const float (&x)[16], float amax,
   return sbyte;
 }
 
-template <int FMT, bool F32, int NV>
+template <int FMT, bool F32, int NV, bool LN>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) quantize_kernel(const __grid_constant__ QuantBatch batch) {
   constexpr int kEsize = F32 ? 4 : 2;
   extern __shared__ uint8_t q_smem_raw[];
   uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(q_smem_raw) + 127) & ~uintptr_t(127));
   __shared__ uint64_t full_bar[kRing], empty_bar[kRing];
   __shared__ int abort_flag;
+  // LayerNorm mode: row mean / rstd of a chunk (double-buffered by chunk parity) and, per
+  // parity, a barrier the consumer warps pass once the chunk's statistics are written
+  __shared__ float ln_stats[LN ? 4 * kLnMaxRows : 1];
+  __shared__ uint64_t ln_bar[2];
   const uint32_t warp = threadIdx.x >> 5;
   const uint32_t lane = threadIdx.x & 31u;
 
@@ -182,6 +191,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) quantize_kernel(const __
       mbar_init(&full_bar[i], 1);
       mbar_init(&empty_bar[i], kConsumerWarps);
     }
+    mbar_init(&ln_bar[0], kConsumerWarps);
+    mbar_init(&ln_bar[1], kConsumerWarps);
     abort_flag = 0;
     fence_mbar_init();
   }
@@ -245,7 +256,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) quantize_kernel(const __
     uint32_t lead = static_cast<uint32_t>(cw);
     int stage = 0;
     uint32_t phase = 0;
-    for (int64_t c = blockIdx.x; c < nchunks; c += gridDim.x) {
+    uint32_t ln_phase = 0;  // bit p: phase of ln_bar[p]
+    uint32_t it = 0;        // chunk iteration of this CTA
+    for (int64_t c = blockIdx.x; c < nchunks; c += gridDim.x, ++it) {
       if (!mbar_wait_bounded_warp(&full_bar[stage], phase, &abort_flag, batch.status)) break;
       int64_t local;
       const int t = chunk_owner(c, local);
@@ -283,6 +296,46 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) quantize_kernel(const __
       const uint32_t flat = static_cast<uint32_t>(nr * nc);
       const uint64_t elem0 = static_cast<uint64_t>(r0) * static_cast<uint64_t>(a.cols) + static_cast<uint64_t>(c0);
       const uint32_t steps = (flat + kSeg - 1) / kSeg;
+      const uint32_t pb = it & 1u;
+      if constexpr (LN) {
+        // phase 1: mean and rstd of the chunk's rows (whole rows: c0 = 0, nc = cols), one warp
+        // per row, two passes over the row in shared memory, fp32, butterfly warp sums
+        const int nci = static_cast<int>(nc);
+        const int pieces = nci * kEsize / 16;  // 16-byte pieces of a row
+        for (int rr = cw; rr < static_cast<int>(nr); rr += kConsumerWarps) {
+          const uint4* rowp = reinterpret_cast<const uint4*>(buf + static_cast<size_t>(rr) * nci * kEsize);
+          auto piece_sum = [&](float mean, bool sq) {
+            float acc_s = 0.0f;
+            for (int q = static_cast<int>(lane); q < pieces; q += 32) {
+              const uint4 v = rowp[q];
+              const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                if constexpr (F32) {
+                  const float d = __uint_as_float(w[i]) - mean;
+                  acc_s += sq ? d * d : d;
+                } else {
+                  const float d0 = __uint_as_float(w[i] << 16) - mean, d1 = __uint_as_float(w[i] & 0xFFFF0000u) - mean;
+                  acc_s += sq ? d0 * d0 + d1 * d1 : d0 + d1;
+                }
+              }
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) acc_s += __shfl_xor_sync(0xFFFFFFFFu, acc_s, o);
+            return acc_s;
+          };
+          const float mean = __fdiv_rn(piece_sum(0.0f, false), static_cast<float>(nci));
+          const float var = __fdiv_rn(piece_sum(mean, true), static_cast<float>(nci));
+          if (lane == 0) {
+            ln_stats[(2 * pb) * kLnMaxRows + rr] = mean;
+            ln_stats[(2 * pb + 1) * kLnMaxRows + rr] = __fdiv_rn(1.0f, __fsqrt_rn(var + a.eps));
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ln_bar[pb]);
+        if (!mbar_wait_bounded_warp(&ln_bar[pb], (ln_phase >> pb) & 1u, &abort_flag, batch.status)) break;
+        ln_phase ^= 1u << pb;
+      }
       for (uint32_t base = lead * kSeg; base < flat; base += kConsumerWarps * kSeg) {
         const uint32_t f = base + lane * kLaneElems;
         const bool live = f < flat;
@@ -298,6 +351,30 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) quantize_kernel(const __
         float x[16];
         float amax;
         unpack16<F32>(in, x, amax);
+        if constexpr (LN) {
+          // phase 2: y = (x - mean) * rstd * gamma + beta for this lane's 16 columns of row rr
+          // lanes past the chunk's end (live false) read row 0: their values are never stored
+          const uint32_t rr = (live && nr > 1) ? __umulhi(f, a.cols_magic) : 0u;
+          const uint32_t col = live ? f - rr * static_cast<uint32_t>(nc) : 0u;
+          const float mean = ln_stats[(2 * pb) * kLnMaxRows + rr], rstd = ln_stats[(2 * pb + 1) * kLnMaxRows + rr];
+          const uint4* gp = reinterpret_cast<const uint4*>(a.gamma + col);
+          const uint4* bp = reinterpret_cast<const uint4*>(a.beta + col);
+          amax = 0.0f;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const uint4 gv = __ldg(gp + h), bv = __ldg(bp + h);
+            const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w}, bw[4] = {bv.x, bv.y, bv.z, bv.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              float& y0 = x[8 * h + 2 * i];
+              float& y1 = x[8 * h + 2 * i + 1];
+              y0 = __fadd_rn(__fmul_rn(__fmul_rn(y0 - mean, rstd), __uint_as_float(gw[i] << 16)), __uint_as_float(bw[i] << 16));
+              y1 = __fadd_rn(__fmul_rn(__fmul_rn(y1 - mean, rstd), __uint_as_float(gw[i] & 0xFFFF0000u)),
+                             __uint_as_float(bw[i] & 0xFFFF0000u));
+              amax = fmaxf(amax, fmaxf(fabsf(y0), fabsf(y1)));
+            }
+          }
+        }
         if constexpr (FMT != BSQ_NVFP4) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));  // 1x32 block = 2 lanes
         if constexpr (NV == kNvGiven) run_max = max(run_max, __float_as_uint(amax));
         if (live) {
@@ -397,9 +474,9 @@ __global__ void __launch_bounds__(kAmaxThreads) amax_kernel(const uint4* src, in
 
 constexpr int kQuantSmem = kRing * kChunkMax + 128;
 
-template <int FMT, bool F32, int NV>
+template <int FMT, bool F32, int NV, bool LN = false>
 cudaError_t launch_q(const QuantBatch& b, int grid, cudaStream_t stream) {
-  static cudaError_t attr = cudaFuncSetAttribute(quantize_kernel<FMT, F32, NV>,
+  static cudaError_t attr = cudaFuncSetAttribute(quantize_kernel<FMT, F32, NV, LN>,
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, kQuantSmem);
   if (attr != cudaSuccess) return attr;
   // programmatic dependent launch: the kernel may be launched while the previous kernel in
@@ -414,16 +491,14 @@ cudaError_t launch_q(const QuantBatch& b, int grid, cudaStream_t stream) {
   cfg.stream = stream;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, quantize_kernel<FMT, F32, NV>, b);
+  return cudaLaunchKernelEx(&cfg, quantize_kernel<FMT, F32, NV, LN>, b);
 }
 
 }  // namespace
 
-int launch_quantize_batch(int fmt, bool src_f32, bool global_given, int count, const QuantItem* items,
-                          cudaStream_t stream, const DeviceInfo& dev) {
-  if (count < 1 || count > kMaxBatch) return BSQ_ERR_ARG;
+// The batch's chunking (chunk size, per-matrix chunk counts) and per-matrix arguments.
+void build_batch(QuantBatch& b, int fmt, bool src_f32, int count, const QuantItem* items, const DeviceInfo& dev) {
   const int64_t esize = src_f32 ? 4 : 2;
-  QuantBatch b{};
   b.n = count;
   b.status = dev.status;
   // Chunk size: at most one ring buffer, and small enough that every SM gets a few chunks
@@ -463,6 +538,14 @@ int launch_quantize_batch(int fmt, bool src_f32, bool global_given, int count, c
       a.g_out = it.global_scale;
     }
   }
+}
+
+int launch_quantize_batch(int fmt, bool src_f32, bool global_given, int count, const QuantItem* items,
+                          cudaStream_t stream, const DeviceInfo& dev) {
+  if (count < 1 || count > kMaxBatch) return BSQ_ERR_ARG;
+  const int64_t esize = src_f32 ? 4 : 2;
+  QuantBatch b{};
+  build_batch(b, fmt, src_f32, count, items, dev);
   const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(b.chunk_start[count], kCtasPerSm * dev.num_sms)));
 
   cudaError_t err = cudaSuccess;
@@ -489,6 +572,24 @@ int launch_quantize_batch(int fmt, bool src_f32, bool global_given, int count, c
     err = src_f32 ? launch_q<BSQ_MXFP8, true, kMx>(b, grid, stream) : launch_q<BSQ_MXFP8, false, kMx>(b, grid, stream);
   } else {
     err = src_f32 ? launch_q<BSQ_MXFP4, true, kMx>(b, grid, stream) : launch_q<BSQ_MXFP4, false, kMx>(b, grid, stream);
+  }
+  return err == cudaSuccess ? BSQ_OK : BSQ_ERR_LAUNCH;
+}
+
+int launch_layernorm_quantize(int fmt, bool src_f32, const QuantItem& item, const uint16_t* gamma,
+                              const uint16_t* beta, float eps, cudaStream_t stream, const DeviceInfo& dev) {
+  QuantBatch b{};
+  build_batch(b, fmt, src_f32, 1, &item, dev);
+  if (b.t[0].chunks_per_row != 1 || b.t[0].rows_per_chunk > kLnMaxRows) return BSQ_ERR_SHAPE;  // whole rows only
+  b.t[0].gamma = gamma;
+  b.t[0].beta = beta;
+  b.t[0].eps = eps;
+  const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(b.chunk_start[1], kCtasPerSm * dev.num_sms)));
+  cudaError_t err;
+  if (fmt == BSQ_MXFP8) {
+    err = src_f32 ? launch_q<BSQ_MXFP8, true, kMx, true>(b, grid, stream) : launch_q<BSQ_MXFP8, false, kMx, true>(b, grid, stream);
+  } else {
+    err = src_f32 ? launch_q<BSQ_MXFP4, true, kMx, true>(b, grid, stream) : launch_q<BSQ_MXFP4, false, kMx, true>(b, grid, stream);
   }
   return err == cudaSuccess ? BSQ_OK : BSQ_ERR_LAUNCH;
 }

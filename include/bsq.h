@@ -111,6 +111,26 @@ int bsq_quantize(int fmt_flags, const void* src, int64_t rows, int64_t cols, voi
  * Errors: BSQ_ERR_ARG if count is out of range or items is NULL, otherwise the first error
  * any item would give bsq_quantize; nothing is enqueued on an argument error.
  */
+/*
+ * bsq_layernorm_quantize: the LayerNorm + quantization kernel of the README's MXFP8 stack
+ * ("lightly-train - DINOv3 + EoMT on RTX 5090" README, section 4.3: LN and quantization merged
+ * into one kernel). Per row r of a rows x cols matrix:
+ *   y[r, c] = (x[r, c] - mean_r) / sqrt(var_r + eps) * gamma[c] + beta[c]
+ * with mean_r and the biased variance var_r over the row, in fp32, then y (kept in fp32)
+ * quantized along the row as bsq_quantize does: codes and tiled scales of an MX format.
+ *   fmt_flags   BSQ_MXFP8 or BSQ_MXFP4, optionally | BSQ_FLAG_SRC_F32
+ *   gamma_bf16, beta_bf16   cols bf16 values each, 16-byte aligned
+ *   eps         >= 0
+ * Codes and scales are the MX quantization of the kernel's fp32 y; a code differs from that of
+ * the exact value only where the exact value lies within the fp32 rounding of the statistics
+ * and the affine step of a rounding boundary.
+ * Shapes: as bsq_quantize for MX, and a row of at most 16384 bytes (cols <= 8192 bf16 or 4096
+ * fp32), else BSQ_ERR_SHAPE. Errors: BSQ_ERR_ARG for another format or flag, NULL gamma /
+ * beta or a negative or non-finite eps; otherwise as bsq_quantize.
+ */
+int bsq_layernorm_quantize(int fmt_flags, const void* src, const void* gamma_bf16, const void* beta_bf16, float eps,
+                           int64_t rows, int64_t cols, void* codes, void* scales, bsq_stream_t stream);
+
 #define BSQ_MAX_BATCH 8
 typedef struct {
   const void* src;     /* rows x cols bf16 or fp32 (per fmt_flags) */

@@ -79,6 +79,12 @@ def test_argument_errors_before_any_cuda_call(bsq):
     assert bsq.bsq_gemm(bsq.NVFP4, p, p, p, p, None, p, 128, 256, 128) == bsq.ERR_SHAPE   # K % 256
     assert bsq.bsq_gemm(bsq.MXFP4, p, p, p, p, None, p, 128, 260, 256) == bsq.ERR_SHAPE   # N % 8
     assert bsq.bsq_gemm_gelu(bsq.MXFP8, p, p, p, p, None, p, 128, 256, 96) == bsq.ERR_SHAPE  # K % 128
+    ln = bsq.bsq_layernorm_quantize
+    assert ln(bsq.NVFP4, p, p, p, 1e-6, 4, 64, p, p) == bsq.ERR_ARG          # MX formats only
+    assert ln(bsq.MXFP8, p, None, p, 1e-6, 4, 64, p, p) == bsq.ERR_ARG       # gamma
+    assert ln(bsq.MXFP8, p, p, p, -1.0, 4, 64, p, p) == bsq.ERR_ARG          # eps < 0
+    assert ln(bsq.MXFP8, p, p, p, 1e-6, 4, 8224, p, p) == bsq.ERR_SHAPE      # row > 16 KB
+    assert ln(bsq.MXFP8, p, p + 2, p, 1e-6, 4, 64, p, p) == bsq.ERR_ALIGN    # gamma alignment
     gq = bsq.bsq_gemm_gelu_quantize
     assert gq(bsq.MXFP8, p, p, p, p, None, bsq.NVFP4, p, p, 128, 256, 256) == bsq.ERR_ARG      # out fmt
     assert gq(bsq.MXFP8, p, p, p, p, None, bsq.MXFP8, p, None, 128, 256, 256) == bsq.ERR_ARG   # no scales

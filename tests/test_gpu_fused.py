@@ -13,14 +13,11 @@ import pytest
 import torch
 
 import oracle
-from tests.gpu_util import bf16_to_f64, check_gemm_rows, decode_rows, sample_rows, to_dev
+from tests.gpu_util import (bf16_to_f64, check_gemm_rows, check_mx_band, decode_rows, element_codes, plain_scales,
+                            sample_rows, to_dev)
 from workloads import f32_to_bf16_bits, random_matrix
 
 pytestmark = pytest.mark.gpu
-
-E4M3 = np.array([oracle.decode_e4m3(c) for c in range(256)])
-E2M1 = np.array([oracle.decode_e2m1(c) for c in range(16)])
-
 
 def _bsq():
     import block_scaled_precision_bsq_gb300 as bsq
@@ -42,53 +39,10 @@ def _gpu_operands(bsq, fmt, a, w, bias):
     return bsq.quantize(fmt, to_dev(a)), bsq.quantize(fmt, to_dev(w)), to_dev(bias)
 
 
-def _plain_scales(tiled: np.ndarray, rows: int, cols: int) -> np.ndarray:
-    nsc = cols // 32
-    off = np.array([[oracle.scale_tiled_offset(r, c, nsc) for c in range(nsc)] for r in range(rows)])
-    return tiled[off]
-
-
-def _element_codes(out_fmt, codes: np.ndarray, rows: int, cols: int) -> np.ndarray:
-    if out_fmt == "mxfp8":
-        return codes.reshape(rows, cols)
-    c = codes.reshape(rows, cols // 2)
-    out = np.empty((rows, cols), dtype=np.uint8)
-    out[:, 0::2] = c & 0xF
-    out[:, 1::2] = c >> 4
-    return out
-
-
-def _mx_exponent(amax: np.ndarray, emax: int) -> np.ndarray:
-    m, ex = np.frexp(amax)
-    e = np.where(amax > 0, ex - 1 - emax, -127)
-    return np.clip(e, -127, 127)
-
-
-def check_fused(out_fmt, codes_el: np.ndarray, scales_plain: np.ndarray, y: np.ndarray, absum: np.ndarray):
-    rows, cols = y.shape
-    emax = 8 if out_fmt == "mxfp8" else 2
-    tbl = E4M3 if out_fmt == "mxfp8" else E2M1
+def check_fused(out_fmt, codes_el, scales_plain, y, absum):
     G = oracle.gelu_erf(y)
     band = 1.13 * (2.0 ** -16 * np.abs(y) + 1e-5 * absum) + 4e-7 * np.abs(y) + 2.0 ** -20 * np.abs(G) + 1e-30
-    Gb, Bb = np.abs(G).reshape(rows, -1, 32), band.reshape(rows, -1, 32)
-    e_lo = _mx_exponent(np.maximum(Gb - Bb, 0).max(-1), emax)
-    e_hi = _mx_exponent((Gb + Bb).max(-1), emax)
-    e_gpu = scales_plain.astype(np.int64) - 127
-    assert ((e_lo <= e_gpu) & (e_gpu <= e_hi)).all(), "block scales outside the band"
-    scale = np.repeat(np.exp2(e_gpu.astype(np.float64)), 32, axis=1)
-    elem = "e4m3" if out_fmt == "mxfp8" else "e2m1"
-    d_lo = tbl[oracle.encode_array(elem, (G - band) / scale)]
-    d_hi = tbl[oracle.encode_array(elem, (G + band) / scale)]
-    d = tbl[codes_el]
-    bad = ~((d_lo <= d) & (d <= d_hi))
-    assert not bad.any(), "%d of %d codes outside the band (first at %s)" % (
-        int(bad.sum()), bad.size, np.unravel_index(int(np.argmax(bad)), bad.shape))
-    ref = oracle.quantize_mx_f64(out_fmt, G)
-    ref_codes = _element_codes(out_fmt, ref.codes, rows, cols)
-    code_match = float((ref_codes == codes_el).mean())
-    scale_match = float((ref.scales == scales_plain).mean())
-    assert code_match >= 0.99 and scale_match >= 0.99, (code_match, scale_match)
-    return code_match, scale_match
+    return check_mx_band(out_fmt, codes_el, scales_plain, G, band)
 
 
 @pytest.mark.parametrize("fmt", ["mxfp8", "nvfp4", "mxfp4"])
@@ -117,12 +71,12 @@ def test_gemm_gelu_quantize(fmt, out_fmt, M, N, K):
     assert bsq.device_status() == 0
     codes = q.codes.cpu().numpy()
     tiled = q.scales.cpu().numpy()
-    plain = _plain_scales(tiled, M, N)
+    plain = plain_scales(tiled, M, N)
     # layout: the tiled buffer is exactly the oracle's tiling of these scales (zero padding)
     assert np.array_equal(tiled, oracle.tile_scales(out_fmt, plain, M, N))
     idx = np.arange(M)
     y, absum = oracle.gemm(decode_rows(qa, idx), qw.decode(), bias, qa.g * qw.g if fmt == "nvfp4" else 1.0)
-    check_fused(out_fmt, _element_codes(out_fmt, codes, M, N), plain, y, absum)
+    check_fused(out_fmt, element_codes(out_fmt, codes, M, N), plain, y, absum)
 
 
 @pytest.mark.parametrize("fmt,out_fmt", [("mxfp8", "mxfp8"), ("mxfp4", "mxfp4")])
@@ -139,7 +93,7 @@ def test_fused_output_feeds_fc2(fmt, out_fmt):
     out = bsq.gemm(h, gw2, None)
     assert bsq.device_status() == 0
     codes = h.codes.cpu().numpy()
-    plain = _plain_scales(h.scales.cpu().numpy(), M, N1)
+    plain = plain_scales(h.scales.cpu().numpy(), M, N1)
     qh = oracle.Quantized(oracle._fmt(out_fmt), M, N1, codes, plain)
     idx = sample_rows(M)
     check_gemm_rows(bf16_to_f64(out)[idx], qh, oracle.quantize(out_fmt, w2), None, idx, "fc2 on fused fc1")
