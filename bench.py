@@ -43,7 +43,8 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from workloads import MXFP8, NVFP4, MXFP4, WORKLOADS, make_activations, make_bias, make_weights  # noqa: E402
+from workloads import (MXFP8, NVFP4, MXFP4, WORKLOADS, make_activations, make_bias,  # noqa: E402
+                       make_layernorm_affine, make_weights)
 
 METRIC = "block-scaled GEMM TFLOPS (% dense FP8/FP4 peak); quantize GB/s (% HBM)"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -294,7 +295,11 @@ def run_gpu(args, rank: int, world: int):
         b1, b2 = make_bias(g1), make_bias(g2)
         hosts = {"x": host(make_activations(g1)), "w1": host(make_weights(g1)), "w2": host(make_weights(g2)),
                  "b1": host(b1), "b2": host(b2)}
-        fused = wl.chain == "fused"
+        fused = wl.chain in ("fused", "ln_fused")
+        ln = wl.chain == "ln_fused"
+        if ln:
+            lg, lb = make_layernorm_affine(g1.K, g1.seed)
+            hosts.update({"ln_g": host(lg), "ln_b": host(lb)})
 
         def alloc():
             D = {k: torch.empty_like(v, device=dev) for k, v in hosts.items()}
@@ -306,7 +311,11 @@ def run_gpu(args, rank: int, world: int):
             return D
 
         def quant(D, s):
-            bsq.quantize_many(fmt, [D["x"], D["w1"], D["w2"]], outs=[D["qx"], D["qw1"], D["qw2"]], stream=s)
+            if ln:  # LayerNorm + quantize of the activations in one kernel, the weights batched
+                bsq.layernorm_quantize(fmt, D["x"], D["ln_g"], D["ln_b"], 1e-6, out=D["qx"], stream=s)
+                bsq.quantize_many(fmt, [D["w1"], D["w2"]], outs=[D["qw1"], D["qw2"]], stream=s)
+            else:
+                bsq.quantize_many(fmt, [D["x"], D["w1"], D["w2"]], outs=[D["qx"], D["qw1"], D["qw2"]], stream=s)
 
         def gemm(D, s):
             if fused:  # fc1's epilogue writes fc2's operand
@@ -317,7 +326,7 @@ def run_gpu(args, rank: int, world: int):
             bsq.gemm(D["qh"], D["qw2"], D["b2"], out=D["out"], stream=s)
 
         units.append({"hosts": hosts, "alloc": alloc, "quant": quant, "gemm": gemm, "fmt": fmt,
-                      "flops": g1.flops + g2.flops, "launches": 3 if fused else 4,
+                      "flops": g1.flops + g2.flops, "launches": (4 if ln else 3) if fused else 4,
                       "qbytes": sum(quant_bytes(fmt, r, c, 2, True) for r, c in ((g1.M, g1.K), (g1.N, g1.K), (g2.N, g2.K))),
                       "gbytes": gemm_bytes(fmt, g1.M, g1.N, g1.K, True) + gemm_bytes(fmt, g2.M, g2.N, g2.K, True) -
                                 (2 * g1.M * g1.N if fused else 0) +

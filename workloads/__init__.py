@@ -79,7 +79,9 @@ class Workload:
     description: str
     gemms: List[Gemm]
     # "fused" / "unfused": gemms = [fc1, fc2] of one MLP, fc2's A being GELU of fc1's output
-    # (quantized in fc1's epilogue, or written as bf16 and quantized by a separate pass)
+    # (quantized in fc1's epilogue, or written as bf16 and quantized by a separate pass);
+    # "ln_fused": as "fused", with fc1's A = LayerNorm of the activations, quantized by the
+    # LN + quantize kernel
     chain: Optional[str] = None
 
 
@@ -126,13 +128,14 @@ WORKLOADS: Dict[str, Workload] = {
 def _mlp_chain(name: str, fmt: str, M: int, chain: str) -> Workload:
     # fc1 weights N(0, 1/sqrt(1024)) so that fc1's outputs spread over the range where GELU
     # bends; fc2 as in the other workloads
-    return Workload(name, "ViT-L/16 MLP fc1 -> GELU -> fc2 at M=%d, %s, fc2 operand %s" % (
-        M, fmt.upper(), "quantized in fc1's epilogue" if chain == "fused" else "from bf16 + a quantize pass"),
+    return Workload(name, "ViT-L/16 MLP %sfc1 -> GELU -> fc2 at M=%d, %s, fc2 operand %s" % (
+        "LN -> " if chain == "ln_fused" else "", M, fmt.upper(),
+        "from bf16 + a quantize pass" if chain == "unfused" else "quantized in fc1's epilogue"),
         [Gemm("fc1", fmt, M, 1024, 4096, w_std=1.0 / 32.0), Gemm("fc2", fmt, M, 4096, 1024)], chain)
 
 
 for _fmt, _M, _tag in ((MXFP8, 7 * 1024, "vitl_mlp_mxfp8"), (MXFP4, 32 * 1600, "vitl_mlp_large_mxfp4")):
-    for _chain in ("fused", "unfused"):
+    for _chain in ("fused", "unfused", "ln_fused"):
         WORKLOADS["%s_%s" % (_tag, _chain)] = _mlp_chain("%s_%s" % (_tag, _chain), _fmt, _M, _chain)
 
 
@@ -202,3 +205,11 @@ def random_matrix(rows: int, cols: int, seed: int, std: float = 1.0, dist: str =
     else:
         x = rng.standard_normal((rows, cols)) * std
     return _store(x, src_f32)
+
+
+def make_layernorm_affine(cols: int, seed: int = 0):
+    """LayerNorm gamma ~ 1 + N(0, 0.1) and beta ~ N(0, 0.1), bf16 bit patterns (stream seed + 4)."""
+    rng = np.random.default_rng(seed + 4)
+    g = f32_to_bf16_bits((1.0 + 0.1 * rng.standard_normal(cols)).astype(np.float32))
+    b = f32_to_bf16_bits((0.1 * rng.standard_normal(cols)).astype(np.float32))
+    return g, b
