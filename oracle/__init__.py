@@ -80,6 +80,13 @@ def lib() -> ctypes.CDLL:
         L.orc_encode_array.argtypes = [ctypes.c_int, f64p, i64, u8p]
         L.orc_layernorm.restype = ctypes.c_int
         L.orc_layernorm.argtypes = [vp, ctypes.c_int, vp, vp, ctypes.c_double, i64, i64, f64p]
+        L.orc_philox4x32_10.restype = None
+        L.orc_philox4x32_10.argtypes = [vp, vp, vp]
+        L.orc_encode_sr_array.restype = ctypes.c_int
+        L.orc_encode_sr_array.argtypes = [ctypes.c_int, f64p, f64p, i64, u8p]
+        L.orc_quantize_mx_dual.restype = ctypes.c_int
+        L.orc_quantize_mx_dual.argtypes = [ctypes.c_int, vp, ctypes.c_int, i64, i64, ctypes.c_int, ctypes.c_uint64,
+                                           u8p, u8p, u8p, u8p]
         L.orc_num_threads.restype = ctypes.c_int
         L.orc_set_num_threads.argtypes = [ctypes.c_int]
         _lib = L
@@ -293,3 +300,40 @@ def layernorm(x: np.ndarray, gamma: np.ndarray, beta: np.ndarray, eps: float) ->
 def layernorm_quantize_reference(fmt, x: np.ndarray, gamma: np.ndarray, beta: np.ndarray, eps: float) -> Quantized:
     """The fused LN step of reading R9: MX(LayerNorm(x))."""
     return quantize_mx_f64(fmt, layernorm(x, gamma, beta, eps))
+
+
+def philox4x32_10(counter, key) -> Tuple[int, int, int, int]:
+    """Philox4x32-10 of a 4 x 32-bit counter and a 2 x 32-bit key (reading R10)."""
+    c = np.ascontiguousarray(counter, dtype=np.uint32)
+    k = np.ascontiguousarray(key, dtype=np.uint32)
+    out = np.zeros(4, dtype=np.uint32)
+    lib().orc_philox4x32_10(_ptr(c), _ptr(k), _ptr(out))
+    return tuple(int(v) for v in out)
+
+
+def encode_sr_array(elem: str, v: np.ndarray, u: np.ndarray) -> np.ndarray:
+    """Stochastically rounded element codes (reading R10): up iff frac(|v| / spacing) > u."""
+    v = np.ascontiguousarray(v, dtype=np.float64)
+    u = np.ascontiguousarray(u, dtype=np.float64)
+    out = np.empty(v.shape, dtype=np.uint8)
+    st = lib().orc_encode_sr_array(0 if elem == "e4m3" else 1, _ptr(v), _ptr(u), v.size, _ptr(out))
+    if st:
+        raise ValueError("oracle encode failed: %d" % st)
+    return out
+
+
+def quantize_dual(fmt, x: np.ndarray, stochastic: bool = False, seed: int = 0) -> Tuple[Quantized, Quantized]:
+    """Dual-layout MX quantization (reading R10): (row-wise R x C, column-wise C x R)."""
+    f = _fmt(fmt)
+    assert f in (MXFP8, MXFP4)
+    x, is_f32 = _src(x)
+    R, C = x.shape
+    rc = np.zeros(codes_bytes(f, R, C), dtype=np.uint8)
+    rs = np.zeros((R, C // 32), dtype=np.uint8)
+    cc = np.zeros(codes_bytes(f, C, R), dtype=np.uint8)
+    cs = np.zeros((C, R // 32), dtype=np.uint8)
+    st = lib().orc_quantize_mx_dual(f, _ptr(x), is_f32, R, C, 1 if stochastic else 0, int(seed) & (2 ** 64 - 1),
+                                    _ptr(rc), _ptr(rs), _ptr(cc), _ptr(cs))
+    if st:
+        raise ValueError("oracle dual quantize failed: %d" % st)
+    return Quantized(f, R, C, rc, rs), Quantized(f, C, R, cc, cs)

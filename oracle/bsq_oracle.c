@@ -48,6 +48,17 @@
  *       merges LN and quantization into one kernel): y = (x - mean) / sqrt(var + eps) * gamma
  *       + beta per row, mean and biased variance over the row (the usual LayerNorm), gamma and
  *       beta bf16, taken before any bf16 rounding, then the MX rule R2 along the row.
+ *   R10 Dual-layout quantization for the backward GEMMs ([LT] section 4.3 / the training path
+ *       of the pages: dgrad needs dY along N and W along N, wgrad dY and X along M): one
+ *       matrix R x C gives the row-wise MX operand (along C, R x C) and the column-wise one
+ *       stored transposed (C x R, quantized along R), each with the MX rule R2.
+ *       Stochastic rounding (for gradients) replaces RNE in R1: with q = |v| / spacing (the
+ *       element format's spacing at v's binade, subnormal spacing below the smallest normal),
+ *       the magnitude rounds up iff frac(q) > u, u = (r >> 8) * 2^-24; |v| >= max still
+ *       saturates. r is word (i mod 4) of Philox4x32-10 (Salmon et al., "Parallel Random
+ *       Numbers: As Easy as 1, 2, 3", SC'11) at counter (floor(i/4) low 32 bits, high 32 bits,
+ *       layout, 0) and key (seed low, seed high), i the element's index in its layout's order
+ *       (row layout r * C + c, column layout c * R + r), layout 0 = row, 1 = column.
  *
  * Pins (tests that tie this code to something other than itself) are in the test suite:
  * exhaustive decode tables against two independent float8/float4 libraries, encoders
@@ -501,5 +512,145 @@ int orc_layernorm(const void* src, int src_f32, const uint16_t* gamma, const uin
             out[r * cols + c] = ((double)load_src(src, src_f32, r * cols + c) - mean) * rstd *
                                     (double)orc_bf16_to_f32(gamma[c]) + (double)orc_bf16_to_f32(beta[c]);
     }
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------------------
+ * Dual-layout quantization with optional stochastic rounding (reading R10).
+ * ---------------------------------------------------------------------------------- */
+
+/* Philox4x32-10 (Salmon et al. SC'11): 10 rounds of the Philox S-box on a 4 x 32-bit counter
+ * with a 2 x 32-bit key, the key bumped by the Weyl constants after every round. */
+void orc_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]) {
+    uint32_t c0 = ctr[0], c1 = ctr[1], c2 = ctr[2], c3 = ctr[3], k0 = key[0], k1 = key[1];
+    int rnd;
+    for (rnd = 0; rnd < 10; ++rnd) {
+        uint64_t p0 = (uint64_t)0xD2511F53u * c0, p1 = (uint64_t)0xCD9E8D57u * c2;
+        uint32_t hi0 = (uint32_t)(p0 >> 32), lo0 = (uint32_t)p0, hi1 = (uint32_t)(p1 >> 32), lo1 = (uint32_t)p1;
+        c0 = hi1 ^ c1 ^ k0;
+        c1 = lo1;
+        c2 = hi0 ^ c3 ^ k1;
+        c3 = lo0;
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+    }
+    out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
+}
+
+/* The 32-bit random word of element i of a layout (reading R10). */
+static uint32_t sr_word(uint64_t seed, int layout, uint64_t i) {
+    uint32_t ctr[4], key[2], out[4];
+    uint64_t g = i >> 2;
+    ctr[0] = (uint32_t)g; ctr[1] = (uint32_t)(g >> 32); ctr[2] = (uint32_t)layout; ctr[3] = 0;
+    key[0] = (uint32_t)seed; key[1] = (uint32_t)(seed >> 32);
+    orc_philox4x32_10(ctr, key, out);
+    return out[i & 3];
+}
+
+/* Stochastic rounding of v to E4M3 (elem 0) or e2m1 (elem 1) with the uniform u in [0, 1):
+ * the magnitude steps up iff frac(|v| / spacing) > u; saturating. */
+static unsigned encode_sr(double v, int elem, double u) {
+    const int mbits = elem == 0 ? 3 : 1, emin = elem == 0 ? -6 : 0;
+    const double maxval = elem == 0 ? 448.0 : 6.0;
+    const unsigned maxcode = elem == 0 ? 0x7Eu : 0x7u, signpos = elem == 0 ? 7u : 3u;
+    unsigned sign = signbit(v) ? 1u : 0u, mag;
+    double a = fabs(v);
+    if (a >= maxval) {
+        mag = maxcode;
+    } else {
+        int ex = 0, E;
+        double q, fl;
+        if (a == 0.0) {
+            E = emin;
+        } else {
+            (void)frexp(a, &ex);
+            E = ex - 1;
+            if (E < emin) E = emin;
+        }
+        q = ldexp(a, mbits - E); /* exact */
+        fl = floor(q);
+        mag = ((unsigned)(E - emin) << mbits) + (unsigned)fl + ((q - fl) > u ? 1u : 0u);
+        if (mag > maxcode) mag = maxcode;
+    }
+    return (sign << signpos) | mag;
+}
+
+int orc_encode_sr_array(int elem, const double* v, const double* u, int64_t n, uint8_t* out) {
+    int64_t i;
+    if (!v || !u || !out || n < 0 || (elem != 0 && elem != 1)) return ORC_ERR_ARG;
+    for (i = 0; i < n; ++i) out[i] = (uint8_t)encode_sr(v[i], elem, u[i]);
+    return ORC_OK;
+}
+
+/* One MX block of 32 values at stride `step` in `x` (fp64): scale byte (rule R2) and codes,
+ * RNE or stochastic with the words of elements base_index + k (k = 0..31) of `layout`. */
+static uint8_t mx_block(int fmt, const double* x, int64_t step, int sr, uint64_t seed, int layout,
+                        uint64_t base_index, unsigned codes[32]) {
+    const int emax_elem = fmt == ORC_MXFP8 ? 8 : 2, elem = fmt == ORC_MXFP8 ? 0 : 1;
+    double amax = 0.0;
+    int k, e, ex;
+    for (k = 0; k < 32; ++k) {
+        double a = fabs(x[k * step]);
+        if (a > amax) amax = a;
+    }
+    if (amax == 0.0) {
+        e = -127;
+    } else {
+        (void)frexp(amax, &ex);
+        e = (ex - 1) - emax_elem;
+        if (e < -127) e = -127;
+        if (e > 127) e = 127;
+    }
+    for (k = 0; k < 32; ++k) {
+        double v = ldexp(x[k * step], -e);
+        if (sr) {
+            double u = ldexp((double)(sr_word(seed, layout, base_index + (uint64_t)k) >> 8), -24);
+            codes[k] = encode_sr(v, elem, u);
+        } else {
+            codes[k] = elem == 0 ? orc_encode_e4m3(v) : orc_encode_e2m1(v);
+        }
+    }
+    return (uint8_t)(e + 127);
+}
+
+/* Dual-layout MX quantization (reading R10) of a bf16 / fp32 R x C matrix (R % 32 == 0 and
+ * C % 32 == 0): row codes R x C (MXFP8 bytes / MXFP4 nibbles) with plain row scales R x C/32,
+ * column codes C x R (the transpose, quantized along R) with plain scales C x R/32. */
+int orc_quantize_mx_dual(int fmt, const void* src, int src_f32, int64_t R, int64_t C, int sr, uint64_t seed,
+                         uint8_t* row_codes, uint8_t* row_scales, uint8_t* col_codes, uint8_t* col_scales) {
+    double* x;
+    int64_t i, r, c;
+    int st;
+    if (!src || !row_codes || !row_scales || !col_codes || !col_scales || R <= 0 || C <= 0) return ORC_ERR_ARG;
+    if (fmt != ORC_MXFP8 && fmt != ORC_MXFP4) return ORC_ERR_ARG;
+    if (R % 32 || C % 32) return ORC_ERR_SHAPE;
+    st = check_finite(src, src_f32, R * C);
+    if (st) return st;
+    x = (double*)malloc((size_t)(R * C) * sizeof(double));
+    if (!x) return ORC_ERR_ARG;
+    for (i = 0; i < R * C; ++i) x[i] = (double)load_src(src, src_f32, i);
+#pragma omp parallel for schedule(static)
+    for (r = 0; r < R; ++r) {
+        int64_t b;
+        unsigned codes[32];
+        int k;
+        for (b = 0; b < C / 32; ++b) {
+            row_scales[r * (C / 32) + b] =
+                mx_block(fmt, x + r * C + b * 32, 1, sr, seed, 0, (uint64_t)(r * C + b * 32), codes);
+            for (k = 0; k < 32; ++k) put_code(fmt, row_codes, r * C + b * 32 + k, codes[k]);
+        }
+    }
+#pragma omp parallel for schedule(static)
+    for (c = 0; c < C; ++c) {
+        int64_t b;
+        unsigned codes[32];
+        int k;
+        for (b = 0; b < R / 32; ++b) {
+            col_scales[c * (R / 32) + b] =
+                mx_block(fmt, x + (b * 32) * C + c, C, sr, seed, 1, (uint64_t)(c * R + b * 32), codes);
+            for (k = 0; k < 32; ++k) put_code(fmt, col_codes, c * R + b * 32 + k, codes[k]);
+        }
+    }
+    free(x);
     return ORC_OK;
 }

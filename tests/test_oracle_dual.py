@@ -1,0 +1,93 @@
+"""Pins of the oracle's dual-layout quantizer and stochastic rounding (reading R10): Philox's
+published known-answer vectors, stochastic rounding against brute-force neighbours and exact
+unbiasedness, and the round-to-nearest dual quantizer against the pinned quantizer applied to
+the matrix and to its transpose."""
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from tests.bruteforce import value_table
+from workloads import f32_to_bf16_bits
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "philox4x32_10_kat.txt")
+
+
+def test_philox_known_answers():
+    n = 0
+    for line in open(GOLDEN):
+        if line.startswith("#") or not line.strip():
+            continue
+        w = [int(t, 16) for t in line.split()]
+        assert oracle.philox4x32_10(w[0:4], w[4:6]) == tuple(w[6:10])
+        n += 1
+    assert n == 3
+
+
+def _neighbours(v, mags):
+    """Largest representable magnitude <= |v| and smallest >= |v| (brute force over the table)."""
+    a = abs(v)
+    lo = mags[mags <= a].max()
+    hi = mags[mags >= a].min() if a <= mags.max() else mags.max()
+    return lo, hi
+
+
+@pytest.mark.parametrize("elem", ["e4m3", "e2m1"])
+def test_sr_extremes_are_round_up_and_truncation(elem):
+    # the value tables come from the decoders, which are pinned to two float8/float4 libraries
+    if elem == "e4m3":
+        _, mags = value_table(oracle.decode_e4m3, 256, 0x80)
+    else:
+        _, mags = value_table(oracle.decode_e2m1, 16, 0x8)
+    rng = np.random.default_rng(11)
+    vmax = 448.0 if elem == "e4m3" else 6.0
+    v = np.concatenate([rng.uniform(-vmax, vmax, 3000), rng.uniform(-1, 1, 1000) * 2.0 ** -6])
+    v = f32_to_bf16_bits(v.astype(np.float32)).astype(np.uint32) << 16
+    v = v.view(np.float32).astype(np.float64)
+    dec = oracle.decode_e4m3 if elem == "e4m3" else oracle.decode_e2m1
+    up = oracle.encode_sr_array(elem, v, np.zeros_like(v))
+    down = oracle.encode_sr_array(elem, v, np.full_like(v, 1.0 - 2.0 ** -24))
+    for x, cu, cd in zip(v, up, down):
+        lo, hi = _neighbours(x, mags)
+        assert abs(dec(int(cu))) == hi and abs(dec(int(cd))) == lo
+        assert (x < 0) == (dec(int(cu)) < 0 or (dec(int(cu)) == 0 and np.signbit(dec(int(cu)))))
+
+
+def test_sr_is_exactly_unbiased_on_dyadic_values():
+    # v with few fractional bits relative to its spacing: the mean over a full grid of u is v
+    rng = np.random.default_rng(12)
+    v = (rng.integers(-400 * 8, 400 * 8, 200) / 8.0).astype(np.float64)  # multiples of 1/8 in (-400, 400)
+    k = 12
+    u = np.arange(2 ** k) / 2.0 ** k
+    for x in v:
+        codes = oracle.encode_sr_array("e4m3", np.full(u.shape, x), u)
+        mean = np.mean([oracle.decode_e4m3(int(c)) for c in codes])
+        assert mean == x
+
+
+@pytest.mark.parametrize("fmt", ["mxfp8", "mxfp4"])
+def test_dual_rne_equals_pinned_quantizer(fmt):
+    rng = np.random.default_rng(13)
+    x = f32_to_bf16_bits((rng.standard_t(4, size=(96, 160)) * 2.0).astype(np.float32))
+    row, col = oracle.quantize_dual(fmt, x)
+    a = oracle.quantize(fmt, x)
+    t = oracle.quantize(fmt, np.ascontiguousarray(x.T))
+    assert np.array_equal(row.codes, a.codes) and np.array_equal(row.scales, a.scales)
+    assert np.array_equal(col.codes, t.codes) and np.array_equal(col.scales, t.scales)
+
+
+def test_dual_sr_steps_at_most_one_code_and_depends_on_seed():
+    rng = np.random.default_rng(14)
+    x = f32_to_bf16_bits(rng.standard_normal((64, 128)).astype(np.float32))
+    rne_row, rne_col = oracle.quantize_dual("mxfp8", x)
+    s1_row, s1_col = oracle.quantize_dual("mxfp8", x, stochastic=True, seed=7)
+    s2_row, _ = oracle.quantize_dual("mxfp8", x, stochastic=True, seed=8)
+    assert np.array_equal(s1_row.scales, rne_row.scales) and np.array_equal(s1_col.scales, rne_col.scales)
+    # same sign, magnitude codes within one step of the RNE code
+    for a, b in ((s1_row, rne_row), (s1_col, rne_col)):
+        d = (a.codes & 0x7F).astype(int) - (b.codes & 0x7F).astype(int)
+        assert np.abs(d).max() <= 1
+    assert not np.array_equal(s1_row.codes, s2_row.codes)
+    s1_again, _ = oracle.quantize_dual("mxfp8", x, stochastic=True, seed=7)
+    assert np.array_equal(s1_again.codes, s1_row.codes)
