@@ -23,6 +23,7 @@ LIB_PATH = os.path.join(_HERE, "libbsq.so")
 MXFP8, NVFP4, MXFP4 = 1, 2, 3
 FLAG_SRC_F32 = 0x100
 FLAG_GLOBAL_GIVEN = 0x200
+FLAG_STOCHASTIC = 0x400
 FORMATS = {"mxfp8": MXFP8, "nvfp4": NVFP4, "mxfp4": MXFP4}
 
 OK, ERR_ARG, ERR_SHAPE, ERR_ALIGN, ERR_ARCH, ERR_LAUNCH, ERR_TIMEOUT = 0, -1, -2, -3, -4, -5, -6
@@ -53,6 +54,8 @@ _lib.bsq_quantize_batch.argtypes = [_int, _int, ctypes.POINTER(QuantItem), _vp]
 _lib.bsq_layernorm_quantize.restype = _int
 _lib.bsq_layernorm_quantize.argtypes = [_int, _vp, _vp, _vp, ctypes.c_float, _i64, _i64, _vp, _vp, _vp]
 _lib.bsq_gemm.restype = _int
+_lib.bsq_quantize_dual.argtypes = [_int, _vp, _i64, _i64, ctypes.c_uint64, _vp, _vp, _vp, _vp, _vp]
+_lib.bsq_quantize_dual.restype = _int
 _lib.bsq_gemm.argtypes = [_int, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp]
 _lib.bsq_gemm_gelu.restype = _int
 _lib.bsq_gemm_gelu.argtypes = [_int, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp]
@@ -67,7 +70,7 @@ _lib.bsq_strerror.restype = ctypes.c_char_p
 _lib.bsq_strerror.argtypes = [_int]
 
 EXPORTS = ("bsq_codes_bytes", "bsq_scales_bytes", "bsq_quantize", "bsq_quantize_batch", "bsq_layernorm_quantize",
-           "bsq_gemm",
+           "bsq_quantize_dual", "bsq_gemm",
            "bsq_gemm_gelu", "bsq_gemm_gelu_quantize", "bsq_get_device_status", "bsq_selftest_timeout",
            "bsq_last_error", "bsq_strerror")
 
@@ -130,6 +133,12 @@ def bsq_layernorm_quantize(fmt_flags: int, src: Ptr, gamma: Ptr, beta: Ptr, eps:
                            codes: Ptr, scales: Ptr, stream=None) -> int:
     return int(_lib.bsq_layernorm_quantize(int(fmt_flags), _p(src), _p(gamma), _p(beta), float(eps), rows, cols,
                                            _p(codes), _p(scales), _stream(stream)))
+
+
+def bsq_quantize_dual(fmt_flags: int, src: Ptr, rows: int, cols: int, seed: int, row_codes: Ptr, row_scales: Ptr,
+                      col_codes: Ptr, col_scales: Ptr, stream=None) -> int:
+    return int(_lib.bsq_quantize_dual(int(fmt_flags), _p(src), rows, cols, int(seed) & (2 ** 64 - 1), _p(row_codes),
+                                      _p(row_scales), _p(col_codes), _p(col_scales), _stream(stream)))
 
 
 def bsq_gemm(fmt, A: Ptr, A_scales: Ptr, B: Ptr, B_scales: Ptr, bias: Ptr, out: Ptr, M: int, N: int, K: int,
@@ -250,6 +259,23 @@ def layernorm_quantize(fmt, x: torch.Tensor, gamma: torch.Tensor, beta: torch.Te
     if rc != OK:
         raise BsqError(rc, "bsq_layernorm_quantize")
     return q
+
+
+def quantize_dual(fmt, x: torch.Tensor, stochastic: bool = False, seed: int = 0, out=None, stream=None):
+    """Both MX operands of a contiguous bf16 / fp32 CUDA matrix X (R x C, multiples of 32) in one
+    launch: (row-wise QTensor R x C, column-wise QTensor C x R = X^T quantized along R), with
+    round-to-nearest-even or Philox-keyed stochastic rounding."""
+    f = _fmt(fmt)
+    assert x.is_cuda and x.is_contiguous() and x.dim() == 2, "x must be a contiguous 2-D CUDA tensor"
+    if x.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("x must be bfloat16 or float32")
+    rows, cols = x.shape
+    flags = f | (FLAG_SRC_F32 if x.dtype == torch.float32 else 0) | (FLAG_STOCHASTIC if stochastic else 0)
+    qr, qc = out if out is not None else (empty_qtensor(f, rows, cols, x.device), empty_qtensor(f, cols, rows, x.device))
+    rc = bsq_quantize_dual(flags, x, rows, cols, seed, qr.codes, qr.scales, qc.codes, qc.scales, stream)
+    if rc != OK:
+        raise BsqError(rc, "bsq_quantize_dual")
+    return qr, qc
 
 
 def gemm(qa: QTensor, qb: QTensor, bias: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,

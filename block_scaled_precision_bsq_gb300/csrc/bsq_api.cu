@@ -156,6 +156,27 @@ int bsq_quantize(int fmt_flags, const void* src, int64_t rows, int64_t cols, voi
   return bsq_quantize_batch(fmt_flags, 1, &item, stream);
 }
 
+int bsq_quantize_dual(int fmt_flags, const void* src, int64_t rows, int64_t cols, uint64_t seed, void* row_codes,
+                      void* row_scales, void* col_codes, void* col_scales, bsq_stream_t stream) {
+  const int fmt = fmt_flags & BSQ_FMT_MASK;
+  const int flags = fmt_flags & ~BSQ_FMT_MASK;
+  if (fmt != BSQ_MXFP8 && fmt != BSQ_MXFP4) return fail(BSQ_ERR_ARG);
+  if (flags & ~(BSQ_FLAG_SRC_F32 | BSQ_FLAG_STOCHASTIC)) return fail(BSQ_ERR_ARG);
+  if (src == nullptr || row_codes == nullptr || row_scales == nullptr || col_codes == nullptr ||
+      col_scales == nullptr || rows <= 0 || cols <= 0)
+    return fail(BSQ_ERR_ARG);
+  if (rows % 32 != 0 || cols % 32 != 0 || rows > INT32_MAX || cols > INT32_MAX) return fail(BSQ_ERR_SHAPE);
+  if (!aligned16(src) || !aligned16(row_codes) || !aligned16(row_scales) || !aligned16(col_codes) ||
+      !aligned16(col_scales))
+    return fail(BSQ_ERR_ALIGN);
+  const bsq::DeviceInfo* dev = bsq::current_device();
+  if (dev == nullptr) return fail(BSQ_ERR_ARCH);
+  const int st = bsq::launch_quantize_dual(fmt, (flags & BSQ_FLAG_SRC_F32) != 0, (flags & BSQ_FLAG_STOCHASTIC) != 0,
+                                           seed, src, rows, cols, row_codes, row_scales, col_codes, col_scales,
+                                           reinterpret_cast<cudaStream_t>(stream), *dev);
+  return st == BSQ_OK ? BSQ_OK : fail(st);
+}
+
 namespace {
 // Validation shared by the GEMM entry points; BSQ_OK or the error code.
 int check_gemm(int fmt, const void* A, const void* A_scales, const void* B, const void* B_scales,

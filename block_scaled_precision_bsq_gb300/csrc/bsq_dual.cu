@@ -1,0 +1,415 @@
+// bsq_dual.cu -- dual-layout MX quantization for the backward GEMMs: one R x C bf16 / fp32
+// matrix gives both its row-wise operand (quantized along C, R x C) and its column-wise one
+// (quantized along R, stored transposed as C x R), each with codes and tiled scales, in one pass
+// over the source. With stochastic rounding the element rounding is the gradient form: the
+// magnitude steps up from the grid point below iff frac(|v| / spacing) > u, u a uniform draw
+// from Philox4x32-10 (Salmon, Moraes, Dror and Shaw, "Parallel Random Numbers: As Easy as 1,
+// 2, 3", SC'11) keyed by the seed and counting over the element's index in its layout.
+//
+// Why dual: dgrad (dX = dY W) contracts over N and wgrad (dW = dY^T X) over M, so the backward
+// pass needs dY quantized along both of its dimensions, W along N and X along M ("lightly-train
+// - DINOv3 + EoMT on RTX 5090" README, section 4.3, the quantized training stack). Reading the
+// source once and writing both layouts costs 2 + 2 bytes per bf16 element (MXFP8) against 2 x
+// (2 + 1) for two quantizer calls over the source and its transpose.
+//
+// Work mapping (two CTAs per SM, persistent over tiles). A tile is 128 columns x kRows rows
+// (128 for bf16, 64 for fp32: 32 KB), loaded by one 2-D TMA copy into a 3-deep ring; tiles past
+// the matrix edge read zeros. Every tile covers exactly one 512-byte scale tile of the row
+// layout and one (bf16) or half of one (fp32) of the column layout, so the kernel writes every
+// scale byte, padding included (zero blocks give scale byte 0), and no buffer needs clearing.
+//   row pass     each lane takes one 16-byte piece (8 bf16 / 4 fp32) of a row: a warp reads
+//                512 contiguous bytes (conflict-free); a 32-element block is 4 / 8 lanes
+//                (xor-shuffles for its maximum) and the row's four scale bytes are OR-ed into
+//                one 32-bit word by two more shuffles, stored by the row's first lane.
+//   column pass  each thread takes one column and 64 / 32 rows of the tile: the warp reads 32
+//                consecutive columns of one row per load (conflict-free), the thread reduces
+//                its 32-row blocks alone and writes each block's 32 codes as contiguous bytes
+//                of the transposed operand (full 32-byte sectors) and its scale bytes.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+
+#include "bsq_device.cuh"
+#include "bsq_internal.h"
+
+namespace bsq {
+namespace {
+
+constexpr int kDCols = 128;          // tile columns
+constexpr int kDTileBytes = 32768;   // one tile of source
+constexpr int kDStages = 3;
+constexpr int kDConsumerWarps = 8;   // warps 1..8; warp 0 lane 0 is the TMA producer
+constexpr int kDThreads = 32 * (kDConsumerWarps + 1);
+constexpr int kDCtasPerSm = 2;
+constexpr int kDSmem = kDStages * kDTileBytes + 128;
+
+struct DualArgs {
+  int64_t rows, cols;  // R, C
+  uint8_t* row_codes;
+  uint8_t* row_scales;
+  uint8_t* col_codes;
+  uint8_t* col_scales;
+  int64_t tiles_c;  // 128-column tiles
+  int64_t ntiles;
+  int64_t nct_row;  // 512-byte scale tiles per 128-row group, row layout: ceil(C / 128)
+  int64_t nct_col;  // same for the column layout (C rows, R / 32 scale columns): ceil(R / 128)
+  uint32_t seed_lo, seed_hi;
+  int* status;
+};
+
+// Philox4x32-10 of the SC'11 paper: ten rounds of two 32 x 32 -> 64-bit products mixed into
+// the other two counter words and the key, the key bumped by the Weyl constants after every
+// round.
+__device__ __forceinline__ uint4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3, uint32_t k0,
+                                               uint32_t k1) {
+#pragma unroll
+  for (int i = 0; i < 10; ++i) {
+    const uint32_t hi0 = __umulhi(0xD2511F53u, c0), lo0 = 0xD2511F53u * c0;
+    const uint32_t hi1 = __umulhi(0xCD9E8D57u, c2), lo1 = 0xCD9E8D57u * c2;
+    c0 = hi1 ^ c1 ^ k0;
+    c1 = lo1;
+    c2 = hi0 ^ c3 ^ k1;
+    c3 = lo0;
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+  return make_uint4(c0, c1, c2, c3);
+}
+
+// The four random words of elements 4g .. 4g+3 of a layout (0 = row, 1 = column).
+__device__ __forceinline__ uint4 sr_words(uint64_t g, uint32_t layout, const DualArgs& a) {
+  return philox4x32_10(static_cast<uint32_t>(g), static_cast<uint32_t>(g >> 32), layout, 0u, a.seed_lo, a.seed_hi);
+}
+
+// Block scale byte of the MX rule: floor(log2(amax)) - emax, clamped at -127, plus 127.
+template <int FMT>
+__device__ __forceinline__ uint32_t mx_scale_byte(float amax) {
+  constexpr uint32_t kEmax = (FMT == BSQ_MXFP8) ? 8u : 2u;
+  const uint32_t ef = __float_as_uint(amax) >> 23;
+  return ef > kEmax ? ef - kEmax : 0u;
+}
+
+// 2^(127 - sbyte) = 1 / scale, exact.
+__device__ __forceinline__ float mx_inv_scale(uint32_t sbyte) { return __uint_as_float((254u - sbyte) << 23); }
+
+// Stochastic rounding of y = x / scale (exact in fp32 unless it fell below fp32's range) to an
+// E4M3 (MXFP8) or e2m1 code with the random word r: q = |y| / spacing at y's binade (the
+// subnormal spacing below the smallest normal), magnitude floor(q) + (frac(q) > u) with
+// u = (r >> 8) 2^-24, saturating at the largest finite value. All steps are exact in fp32.
+template <int FMT>
+__device__ __forceinline__ uint32_t sr_code(float y, float x, uint32_t r) {
+  constexpr uint32_t kM = (FMT == BSQ_MXFP8) ? 3u : 1u;         // mantissa bits
+  constexpr uint32_t kEminB = (FMT == BSQ_MXFP8) ? 121u : 127u;  // biased exponent of the lowest normal binade
+  constexpr float kMax = (FMT == BSQ_MXFP8) ? 448.0f : 6.0f;
+  constexpr uint32_t kMaxCode = (FMT == BSQ_MXFP8) ? 0x7Eu : 0x7u;
+  constexpr uint32_t kSign = (FMT == BSQ_MXFP8) ? 7u : 3u;
+  const float av = fabsf(y);
+  const uint32_t eb = max(__float_as_uint(av) >> 23, kEminB);
+  const float q = av * __uint_as_float((254u + kM - eb) << 23);
+  const float fl = floorf(q);
+  const uint32_t rr = r >> 8;
+  const float u = __uint2float_rn(rr) * 5.9604644775390625e-08f;  // rr * 2^-24
+  // y == 0 for x != 0 only when x / scale underflowed fp32: its true fraction is positive and
+  // below 2^-24, so it steps up exactly when u == 0
+  const bool up = (q - fl > u) || (rr == 0u && av == 0.0f && x != 0.0f);
+  uint32_t mag = ((eb - kEminB) << kM) + static_cast<uint32_t>(fl) + (up ? 1u : 0u);
+  mag = av >= kMax ? kMaxCode : mag;
+  return ((__float_as_uint(y) >> 31) << kSign) | mag;
+}
+
+// Codes of n (a multiple of 4, <= 8 for e2m1 words) consecutive elements y[0..n) packed into
+// `w`: E4M3 one byte each (element i in byte i of w[i / 4]), e2m1 one nibble each (element i in
+// bits 4i of w[0]). RNE, or stochastic with words rw[i].
+template <int FMT, bool SR, int N>
+__device__ __forceinline__ void encode_n(const float* y, const float* x, const uint32_t* rw, uint32_t* w) {
+  if constexpr (FMT == BSQ_MXFP8) {
+#pragma unroll
+    for (int j = 0; j < N / 4; ++j) {
+      if constexpr (SR) {
+        w[j] = sr_code<FMT>(y[4 * j], x[4 * j], rw[4 * j]) | (sr_code<FMT>(y[4 * j + 1], x[4 * j + 1], rw[4 * j + 1]) << 8) |
+               (sr_code<FMT>(y[4 * j + 2], x[4 * j + 2], rw[4 * j + 2]) << 16) |
+               (sr_code<FMT>(y[4 * j + 3], x[4 * j + 3], rw[4 * j + 3]) << 24);
+      } else {
+        w[j] = cvt_e4m3x4(y[4 * j], y[4 * j + 1], y[4 * j + 2], y[4 * j + 3]);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < (N + 7) / 8; ++j) {
+      constexpr int kn = N < 8 ? N : 8;
+      if constexpr (SR) {
+        uint32_t v = 0;
+#pragma unroll
+        for (int i = 0; i < kn; ++i) v |= sr_code<FMT>(y[8 * j + i], x[8 * j + i], rw[8 * j + i]) << (4 * i);
+        w[j] = v;
+      } else if constexpr (kn == 8) {
+        w[j] = cvt_e2m1x8(y + 8 * j);
+      } else {
+        w[j] = cvt_e2m1x2(y[8 * j], y[8 * j + 1]) | (cvt_e2m1x2(y[8 * j + 2], y[8 * j + 3]) << 8);
+      }
+    }
+  }
+}
+
+template <int FMT, bool F32, bool SR>
+__global__ void __launch_bounds__(kDThreads, kDCtasPerSm)
+    dual_kernel(const __grid_constant__ CUtensorMap src_map, const DualArgs a) {
+  constexpr int kEsize = F32 ? 4 : 2;
+  constexpr int kRows = kDTileBytes / (kDCols * kEsize);  // 128 bf16, 64 fp32
+  constexpr int V = 16 / kEsize;                           // elements of a 16-byte piece
+  constexpr int LB = 32 / V;                               // lanes of a 32-element block
+  constexpr int kRowSteps = kDTileBytes / 16 / 32 / kDConsumerWarps;  // row-pass steps per warp
+  constexpr int kColBlocks = kRows / 32 / 2;  // column-pass 32-row blocks per thread (2 bf16, 1 fp32)
+  constexpr bool kFp8 = (FMT == BSQ_MXFP8);
+  extern __shared__ uint8_t d_smem_raw[];
+  uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(d_smem_raw) + 127) & ~uintptr_t(127));
+  __shared__ uint64_t full_bar[kDStages], empty_bar[kDStages];
+  __shared__ int abort_flag;
+  const uint32_t warp = threadIdx.x >> 5;
+  const uint32_t lane = threadIdx.x & 31u;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kDStages; ++i) {
+      mbar_init(&full_bar[i], 1);
+      mbar_init(&empty_bar[i], kDConsumerWarps);
+    }
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  launch_dependents();
+  grid_dependency_wait();  // the source and outputs may belong to the previous kernel until here
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tmap(&src_map);
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int64_t t = blockIdx.x; t < a.ntiles; t += gridDim.x) {
+        if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1u, &abort_flag, a.status)) break;
+        const int64_t ti = t / a.tiles_c, tj = t - ti * a.tiles_c;
+        mbar_arrive_expect_tx(&full_bar[stage], kDTileBytes);
+        tma_load_2d(ring + stage * kDTileBytes, &src_map, &full_bar[stage], static_cast<int32_t>(tj * kDCols),
+                    static_cast<int32_t>(ti * kRows));
+        if (++stage == kDStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const int cw = static_cast<int>(warp) - 1;
+  const int ct = static_cast<int>(threadIdx.x) - 32;  // 0 .. 255
+  const int64_t R = a.rows, C = a.cols;
+  int stage = 0;
+  uint32_t phase = 0;
+  for (int64_t t = blockIdx.x; t < a.ntiles; t += gridDim.x) {
+    if (!mbar_wait_bounded_warp(&full_bar[stage], phase, &abort_flag, a.status)) break;
+    const int64_t ti = t / a.tiles_c, tj = t - ti * a.tiles_c;
+    const int64_t r0 = ti * kRows, c0 = tj * kDCols;
+    const uint8_t* tile = ring + stage * kDTileBytes;
+
+    // ---- row pass: pieces of 16 bytes, the warp's 32 pieces contiguous
+#pragma unroll 2
+    for (int s = 0; s < kRowSteps; ++s) {
+      const int f = (s * kDConsumerWarps + cw) * 32 + static_cast<int>(lane);
+      const int e0 = f * V;
+      const int rr = e0 / kDCols, cc = e0 % kDCols;
+      const uint4 v = *reinterpret_cast<const uint4*>(tile + f * 16);
+      float x[V];
+      if constexpr (F32) {
+        x[0] = __uint_as_float(v.x);
+        x[1] = __uint_as_float(v.y);
+        x[2] = __uint_as_float(v.z);
+        x[3] = __uint_as_float(v.w);
+      } else {
+        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          x[2 * i] = __uint_as_float(wv[i] << 16);
+          x[2 * i + 1] = __uint_as_float(wv[i] & 0xFFFF0000u);
+        }
+      }
+      float amax = 0.0f;
+#pragma unroll
+      for (int i = 0; i < V; ++i) amax = fmaxf(amax, fabsf(x[i]));
+#pragma unroll
+      for (int o = 1; o < LB; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+      const uint32_t sbyte = mx_scale_byte<FMT>(amax);
+      const float mul = mx_inv_scale(sbyte);
+      float y[V];
+#pragma unroll
+      for (int i = 0; i < V; ++i) y[i] = x[i] * mul;
+      const int64_t r = r0 + rr, c = c0 + cc;
+      uint32_t rw[V];
+      if constexpr (SR) {
+        const uint64_t i0 = static_cast<uint64_t>(r) * static_cast<uint64_t>(C) + static_cast<uint64_t>(c);
+#pragma unroll
+        for (int gq = 0; gq < V / 4; ++gq) {
+          const uint4 q = sr_words((i0 >> 2) + gq, 0u, a);
+          rw[4 * gq] = q.x;
+          rw[4 * gq + 1] = q.y;
+          rw[4 * gq + 2] = q.z;
+          rw[4 * gq + 3] = q.w;
+        }
+      }
+      uint32_t w[kFp8 ? V / 4 : 1];
+      encode_n<FMT, SR, V>(y, x, rw, w);
+      if (r < R && c < C) {
+        const int64_t idx = r * C + c;
+        if constexpr (kFp8) {
+          if constexpr (V == 8) *reinterpret_cast<uint2*>(a.row_codes + idx) = make_uint2(w[0], w[1]);
+          else *reinterpret_cast<uint32_t*>(a.row_codes + idx) = w[0];
+        } else {
+          if constexpr (V == 8) *reinterpret_cast<uint32_t*>(a.row_codes + idx / 2) = w[0];
+          else *reinterpret_cast<uint16_t*>(a.row_codes + idx / 2) = static_cast<uint16_t>(w[0]);
+        }
+      }
+      // the row's four scale bytes -> one word (block b of the row in byte b)
+      uint32_t sw = sbyte << (8 * (cc / 32));
+      sw |= __shfl_xor_sync(0xFFFFFFFFu, sw, LB);
+      sw |= __shfl_xor_sync(0xFFFFFFFFu, sw, 2 * LB);
+      if ((lane & (4 * LB - 1)) == 0) {
+        const int64_t off = ((r >> 7) * a.nct_row + tj) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4;
+        *reinterpret_cast<uint32_t*>(a.row_scales + off) = sw;
+      }
+    }
+
+    // ---- column pass: one column, kColBlocks blocks of 32 rows per thread
+    {
+      const int cc = ct & (kDCols - 1);
+      const int g = ct >> 7;
+      const int64_t c = c0 + cc;
+      uint32_t sbytes = 0;
+#pragma unroll 1
+      for (int bb = 0; bb < kColBlocks; ++bb) {
+        const int rb = (g * kColBlocks + bb) * 32;
+        float x[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          if constexpr (F32) {
+            x[k] = *reinterpret_cast<const float*>(tile + ((rb + k) * kDCols + cc) * 4);
+          } else {
+            x[k] = __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(tile + ((rb + k) * kDCols + cc) * 2)) << 16);
+          }
+        }
+        float m[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) m[i] = fmaxf(fmaxf(fabsf(x[4 * i]), fabsf(x[4 * i + 1])), fmaxf(fabsf(x[4 * i + 2]), fabsf(x[4 * i + 3])));
+#pragma unroll
+        for (int i = 0; i < 4; ++i) m[i] = fmaxf(m[i], m[i + 4]);
+        const float amax = fmaxf(fmaxf(0.0f, fmaxf(m[0], m[1])), fmaxf(m[2], m[3]));
+        const uint32_t sbyte = mx_scale_byte<FMT>(amax);
+        sbytes |= sbyte << (8 * bb);
+        const float mul = mx_inv_scale(sbyte);
+        const int64_t r = r0 + rb;
+        if (c < C && r < R) {
+          float y[32];
+#pragma unroll
+          for (int k = 0; k < 32; ++k) y[k] = x[k] * mul;
+          uint32_t rw[SR ? 32 : 1];
+          if constexpr (SR) {
+            const uint64_t i0 = static_cast<uint64_t>(c) * static_cast<uint64_t>(R) + static_cast<uint64_t>(r);
+#pragma unroll
+            for (int gq = 0; gq < 8; ++gq) {
+              const uint4 q = sr_words((i0 >> 2) + gq, 1u, a);
+              rw[4 * gq] = q.x;
+              rw[4 * gq + 1] = q.y;
+              rw[4 * gq + 2] = q.z;
+              rw[4 * gq + 3] = q.w;
+            }
+          }
+          const int64_t idx = c * R + r;
+          if constexpr (kFp8) {
+            uint32_t w[8];
+            encode_n<FMT, SR, 32>(y, x, rw, w);
+            uint4* dst = reinterpret_cast<uint4*>(a.col_codes + idx);
+            dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+            dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+          } else {
+            uint32_t w[4];
+            encode_n<FMT, SR, 32>(y, x, rw, w);
+            *reinterpret_cast<uint4*>(a.col_codes + idx / 2) = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        }
+      }
+      // scale bytes of column c: row c of the column layout, scale columns (r0 % 128) / 32 + ..
+      const int64_t off = (tj * a.nct_col + (r0 >> 7)) * 512 + (cc & 31) * 16 + ((cc >> 5) & 3) * 4 +
+                          ((r0 & 127) >> 5) + g * kColBlocks;
+      if constexpr (kColBlocks == 2) *reinterpret_cast<uint16_t*>(a.col_scales + off) = static_cast<uint16_t>(sbytes);
+      else a.col_scales[off] = static_cast<uint8_t>(sbytes);
+    }
+
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty_bar[stage]);
+    if (++stage == kDStages) {
+      stage = 0;
+      phase ^= 1u;
+    }
+  }
+}
+
+template <int FMT, bool F32, bool SR>
+cudaError_t launch_d(const CUtensorMap& map, const DualArgs& a, int grid, cudaStream_t stream) {
+  static cudaError_t attr =
+      cudaFuncSetAttribute(dual_kernel<FMT, F32, SR>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDSmem);
+  if (attr != cudaSuccess) return attr;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kDThreads);
+  cfg.dynamicSmemBytes = kDSmem;
+  cfg.stream = stream;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, dual_kernel<FMT, F32, SR>, map, a);
+}
+
+template <int FMT>
+cudaError_t launch_d_fmt(bool f32, bool sr, const CUtensorMap& map, const DualArgs& a, int grid, cudaStream_t stream) {
+  if (f32) return sr ? launch_d<FMT, true, true>(map, a, grid, stream) : launch_d<FMT, true, false>(map, a, grid, stream);
+  return sr ? launch_d<FMT, false, true>(map, a, grid, stream) : launch_d<FMT, false, false>(map, a, grid, stream);
+}
+
+}  // namespace
+
+int launch_quantize_dual(int fmt, bool src_f32, bool stochastic, uint64_t seed, const void* src, int64_t rows,
+                         int64_t cols, void* row_codes, void* row_scales, void* col_codes, void* col_scales,
+                         cudaStream_t stream, const DeviceInfo& dev) {
+  const int64_t esize = src_f32 ? 4 : 2;
+  const int64_t tile_rows = kDTileBytes / (kDCols * esize);
+  DualArgs a{};
+  a.rows = rows;
+  a.cols = cols;
+  a.row_codes = static_cast<uint8_t*>(row_codes);
+  a.row_scales = static_cast<uint8_t*>(row_scales);
+  a.col_codes = static_cast<uint8_t*>(col_codes);
+  a.col_scales = static_cast<uint8_t*>(col_scales);
+  a.tiles_c = ceil_div(cols, kDCols);
+  // row tiles cover the rows padded to 128, so that every scale byte of both layouts is written
+  a.ntiles = (ceil_div(rows, 128) * 128 / tile_rows) * a.tiles_c;
+  a.nct_row = ceil_div(cols, 128);
+  a.nct_col = ceil_div(rows, 128);
+  a.seed_lo = static_cast<uint32_t>(seed);
+  a.seed_hi = static_cast<uint32_t>(seed >> 32);
+  a.status = dev.status;
+  CUtensorMap map;
+  if (!make_map_2d(&map, src_f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, src,
+                   static_cast<uint64_t>(cols), static_cast<uint64_t>(rows), static_cast<uint64_t>(cols * esize), kDCols,
+                   static_cast<uint32_t>(tile_rows), CU_TENSOR_MAP_SWIZZLE_NONE))
+    return BSQ_ERR_LAUNCH;
+  const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(a.ntiles, kDCtasPerSm * dev.num_sms)));
+  const cudaError_t err = fmt == BSQ_MXFP8 ? launch_d_fmt<BSQ_MXFP8>(src_f32, stochastic, map, a, grid, stream)
+                                           : launch_d_fmt<BSQ_MXFP4>(src_f32, stochastic, map, a, grid, stream);
+  return err == cudaSuccess ? BSQ_OK : BSQ_ERR_LAUNCH;
+}
+
+}  // namespace bsq

@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "bsq.h"
@@ -29,6 +30,18 @@ struct DeviceInfo {
 // usable device. Thread-safe.
 const DeviceInfo* current_device();
 
+// cuTensorMapEncodeTiled, obtained once through the runtime's driver entry-point query
+// (nullptr if unavailable).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_fn();
+
+// 2-D tensor map over `outer` rows of `inner` elements (row pitch `row_bytes`), box
+// box_inner x box_outer, zero fill out of bounds. False if the encoder refused.
+bool make_map_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
+                 uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw);
+
 // Items already validated (shapes, alignment); count in [1, BSQ_MAX_BATCH].
 using QuantItem = bsq_quant_item;
 int launch_quantize_batch(int fmt, bool src_f32, bool global_given, int count, const QuantItem* items,
@@ -38,6 +51,12 @@ int launch_quantize_batch(int fmt, bool src_f32, bool global_given, int count, c
 // (BSQ_ERR_SHAPE otherwise).
 int launch_layernorm_quantize(int fmt, bool src_f32, const QuantItem& item, const uint16_t* gamma,
                               const uint16_t* beta, float eps, cudaStream_t stream, const DeviceInfo& dev);
+
+// Dual-layout MX quantization (fmt MXFP8 / MXFP4) of one rows x cols matrix, arguments
+// validated (rows, cols multiples of 32).
+int launch_quantize_dual(int fmt, bool src_f32, bool stochastic, uint64_t seed, const void* src, int64_t rows,
+                         int64_t cols, void* row_codes, void* row_scales, void* col_codes, void* col_scales,
+                         cudaStream_t stream, const DeviceInfo& dev);
 
 // epi: 0 bf16 out, 1 GELU -> bf16, 2 GELU -> MXFP8 codes + scales, 3 GELU -> MXFP4 (out_scales
 // used by 2 and 3 only).

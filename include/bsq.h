@@ -46,6 +46,7 @@ typedef enum { BSQ_MXFP8 = 1, BSQ_NVFP4 = 2, BSQ_MXFP4 = 3 } bsq_format;
 #define BSQ_FLAG_GLOBAL_GIVEN 0x200 /* NVFP4: read g from *global_scale instead of computing it
                                        (a static or delayed per-tensor scale, README sections
                                        4.3 and 5.5) */
+#define BSQ_FLAG_STOCHASTIC 0x400   /* bsq_quantize_dual: stochastic rounding of the elements */
 
 /* Status codes. */
 #define BSQ_OK 0
@@ -101,17 +102,6 @@ int bsq_quantize(int fmt_flags, const void* src, int64_t rows, int64_t cols, voi
                  float* global_scale, bsq_stream_t stream);
 
 /*
- * bsq_quantize_batch: bsq_quantize applied to `count` matrices (1 <= count <= BSQ_MAX_BATCH)
- * in one kernel launch, e.g. a layer's activations and weights together. Every item is
- * validated as in bsq_quantize (its own rows, cols, buffers; global_scale as bsq_quantize's
- * argument) and the whole batch shares fmt_flags (one format, one source type, one
- * NVFP4 scale mode). Results are identical, byte for byte, to `count` bsq_quantize calls.
- * `items` is a host array read during the call only. The batching is an engineering entry
- * point (fewer launches for small matrices); the method itself has no counterpart.
- * Errors: BSQ_ERR_ARG if count is out of range or items is NULL, otherwise the first error
- * any item would give bsq_quantize; nothing is enqueued on an argument error.
- */
-/*
  * bsq_layernorm_quantize: the LayerNorm + quantization kernel of the README's MXFP8 stack
  * ("lightly-train - DINOv3 + EoMT on RTX 5090" README, section 4.3: LN and quantization merged
  * into one kernel). Per row r of a rows x cols matrix:
@@ -140,7 +130,48 @@ typedef struct {
   float* global_scale; /* NVFP4 only, as bsq_quantize's global_scale; NULL otherwise */
 } bsq_quant_item;
 
+/*
+ * bsq_quantize_batch: bsq_quantize applied to `count` matrices (1 <= count <= BSQ_MAX_BATCH)
+ * in one kernel launch, e.g. a layer's activations and weights together. Every item is
+ * validated as in bsq_quantize (its own rows, cols, buffers; global_scale as bsq_quantize's
+ * argument) and the whole batch shares fmt_flags (one format, one source type, one
+ * NVFP4 scale mode). Results are identical, byte for byte, to `count` bsq_quantize calls.
+ * `items` is a host array read during the call only. The batching is an engineering entry
+ * point (fewer launches for small matrices); the method itself has no counterpart.
+ * Errors: BSQ_ERR_ARG if count is out of range or items is NULL, otherwise the first error
+ * any item would give bsq_quantize; nothing is enqueued on an argument error.
+ */
 int bsq_quantize_batch(int fmt_flags, int count, const bsq_quant_item* items, bsq_stream_t stream);
+
+/*
+ * bsq_quantize_dual: dual-layout MX quantization for the backward GEMMs ("lightly-train -
+ * DINOv3 + EoMT on RTX 5090" README, section 4.3, the quantized training stack): dgrad
+ * contracts dY over N and wgrad over M, so dY is needed quantized along both of its dimensions
+ * (and W along N, X along M). From one rows x cols matrix X, in one pass over it:
+ *   row_codes, row_scales  the operand bsq_quantize(fmt, X, rows, cols) writes (blocks along
+ *                          cols), sized bsq_codes_bytes / bsq_scales_bytes(fmt, rows, cols);
+ *   col_codes, col_scales  the operand of X^T (cols x rows, blocks along rows), as
+ *                          bsq_quantize(fmt, X^T, cols, rows) would write it, sized
+ *                          bsq_codes_bytes / bsq_scales_bytes(fmt, cols, rows).
+ * All four are written, scale padding included.
+ *   fmt_flags  BSQ_MXFP8 or BSQ_MXFP4, | BSQ_FLAG_SRC_F32 (fp32 source, default bf16),
+ *              | BSQ_FLAG_STOCHASTIC.
+ * Block scales follow the MX rule of bsq_quantize. Without BSQ_FLAG_STOCHASTIC the elements
+ * round to nearest even (seed ignored); both layouts are then byte-identical to the two
+ * bsq_quantize calls. With it (the gradient rounding of quantized training), for v = x / scale:
+ * q = |v| / spacing, the spacing of the element format at |v|'s binade (its subnormal step
+ * below the smallest normal); |code| = floor(q) + (frac(q) > u), saturating at the largest
+ * finite value (448, 6); u = (r >> 8) * 2^-24 with r word (i mod 4) of Philox4x32-10 (Salmon
+ * et al., "Parallel Random Numbers: As Easy as 1, 2, 3", SC'11) at counter {floor(i/4) low 32
+ * bits, high 32 bits, layout, 0} and key {seed low 32 bits, high 32 bits}; i = r * cols + c in
+ * the row layout (layout 0), c * rows + r in the column layout (layout 1). E[code value] = v
+ * below saturation, and the codes are a function of (X, seed) alone.
+ * Shapes: rows % 32 == 0 and cols % 32 == 0, both below 2^31, else BSQ_ERR_SHAPE.
+ * Errors: BSQ_ERR_ARG for another format or flag, a NULL buffer or a non-positive size;
+ * BSQ_ERR_ALIGN for a pointer not 16-byte aligned.
+ */
+int bsq_quantize_dual(int fmt_flags, const void* src, int64_t rows, int64_t cols, uint64_t seed, void* row_codes,
+                      void* row_scales, void* col_codes, void* col_scales, bsq_stream_t stream);
 
 /*
  * bsq_gemm: out[m, n] = bf16_rn(alpha * sum_k Ahat[m,k] * Bhat[n,k] + bias[n]).

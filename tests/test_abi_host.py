@@ -94,5 +94,16 @@ def test_argument_errors_before_any_cuda_call(bsq):
     assert bsq.bsq_gemm(bsq.MXFP8, p, p + 4, p, p, None, p, 128, 256, 256) == bsq.ERR_ALIGN
     assert bsq.bsq_gemm(bsq.MXFP8, p, p, p, p, p + 1, p, 128, 256, 256) == bsq.ERR_ALIGN
     assert bsq.bsq_selftest_timeout(10, None) == bsq.ERR_ARG
+    dq = bsq.bsq_quantize_dual
+    assert dq(bsq.NVFP4, p, 64, 64, 0, p, p, p, p) == bsq.ERR_ARG                  # MX formats only
+    assert dq(bsq.MXFP8 | bsq.FLAG_GLOBAL_GIVEN, p, 64, 64, 0, p, p, p, p) == bsq.ERR_ARG  # flag
+    assert dq(bsq.MXFP8, p, 64, 64, 0, p, p, None, p) == bsq.ERR_ARG               # col codes
+    assert dq(bsq.MXFP8, p, 0, 64, 0, p, p, p, p) == bsq.ERR_ARG                   # rows
+    assert dq(bsq.MXFP8, p, 48, 64, 0, p, p, p, p) == bsq.ERR_SHAPE                # rows % 32
+    assert dq(bsq.MXFP4 | bsq.FLAG_STOCHASTIC, p, 64, 80, 0, p, p, p, p) == bsq.ERR_SHAPE  # cols % 32
+    assert dq(bsq.MXFP8, p, 1 << 31, 64, 0, p, p, p, p) == bsq.ERR_SHAPE           # rows >= 2^31
+    assert dq(bsq.MXFP8, p, 64, 64, 0, p, p, p, p + 8) == bsq.ERR_ALIGN            # col scales
+    assert dq(bsq.MXFP8 | bsq.FLAG_SRC_F32 | bsq.FLAG_STOCHASTIC, p + 4, 64, 64, 2 ** 64 - 1, p, p, p, p) == \
+        bsq.ERR_ALIGN
     assert bsq.bsq_strerror(bsq.ERR_TIMEOUT).startswith("a kernel")
     assert bsq.bsq_strerror(12345) == "unknown status"
