@@ -44,7 +44,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 from workloads import (MXFP8, NVFP4, MXFP4, WORKLOADS, make_activations, make_bias,  # noqa: E402
-                       make_layernorm_affine, make_weights)
+                       make_layernorm_affine, make_output_grad, make_weights)
 
 METRIC = "block-scaled GEMM TFLOPS (% dense FP8/FP4 peak); quantize GB/s (% HBM)"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -69,6 +69,13 @@ def quant_bytes(fmt: str, rows: int, cols: int, src_bytes: int, computed_global:
     scales = n // (16 if fmt == NVFP4 else 32)
     reads = n * src_bytes * (2 if (fmt == NVFP4 and computed_global) else 1)
     return reads + codes + scales
+
+
+def dual_bytes(fmt: str, rows: int, cols: int, src_bytes: int) -> int:
+    """Algorithmic bytes of one dual-layout MX quantization: the source read once, codes and
+    scales of both layouts written."""
+    n = rows * cols
+    return n * src_bytes + 2 * (n if fmt == MXFP8 else n // 2) + 2 * (n // 32)
 
 
 def gemm_bytes(fmt: str, M: int, N: int, K: int, bias: bool) -> int:
@@ -142,6 +149,42 @@ def _oracle_linear_rows(g, rows: int) -> float:
     return time.perf_counter() - t0
 
 
+def _oracle_train_rows(g, rows: int, sr: bool) -> float:
+    """One training step of the layer on the first `rows` tokens: dual quantization of X, W and
+    dY, then forward, dgrad and wgrad (the latter summing over the `rows` tokens only)."""
+    import oracle
+
+    x, w, dy, bias = make_activations(g, rows=rows), make_weights(g), make_output_grad(g, rows=rows), make_bias(g)
+    t0 = time.perf_counter()
+    xr, xc = oracle.quantize_dual(g.fmt, x)
+    wr, wc = oracle.quantize_dual(g.fmt, w)
+    dr, dc = oracle.quantize_dual(g.fmt, dy, stochastic=sr, seed=1)
+    oracle.gemm(xr.decode(), wr.decode(), bias, 1.0, want_abs=False)
+    oracle.gemm(dr.decode(), wc.decode(), None, 1.0, want_abs=False)
+    oracle.gemm(dc.decode(), xc.decode(), None, 1.0, want_abs=False)
+    return time.perf_counter() - t0
+
+
+def cpu_oracle_train_sample(wl, target_s: float = 10.0):
+    """The training step's oracle on R leading tokens (R a multiple of 32), R calibrated from two
+    runs to take about `target_s` seconds. Returns (TFLOP/s, seconds, cores, description)."""
+    import oracle
+
+    g = wl.gemms[0]
+    t32, t160 = _oracle_train_rows(g, 32, wl.grad_sr), _oracle_train_rows(g, 160, wl.grad_sr)
+    per_row = max((t160 - t32) / 128.0, 1e-9)
+    fixed = max(t32 - 32 * per_row, 0.0)
+    rows = int(min(g.M, max(32, (target_s - fixed) / per_row))) // 32 * 32
+    secs = _oracle_train_rows(g, rows, wl.grad_sr)
+    desc = ("oracle training step on %d of %d tokens: dual quantization of X (R rows), W and dY (R rows), "
+            "decode, fp64 forward, dgrad and wgrad GEMMs" % (rows, g.M))
+    return 3 * 2 * rows * g.N * g.K / secs / 1e12, secs, oracle.num_threads(), desc
+
+
+def oracle_sample(wl, target_s: float):
+    return cpu_oracle_train_sample(wl, target_s) if wl.chain == "train" else cpu_oracle_sample(wl.gemms, target_s)
+
+
 def cpu_oracle_sample(gemms, target_s: float = 10.0):
     """Time the CPU oracle (as it stands, all host cores) on a bounded sample of the workload:
     for each GEMM, quantize R rows of A and all of B, decode, fp64 GEMM of those R rows, with R
@@ -169,6 +212,7 @@ def config_of(wl):
     return {"workload": wl.name, "description": wl.description,
             "gemms": [{"name": g.name, "format": g.fmt, "M": g.M, "N": g.N, "K": g.K} for g in wl.gemms],
             "chain": wl.chain,
+            "grad_rounding": ("stochastic (Philox4x32-10)" if wl.grad_sr else "nearest even") if wl.chain == "train" else None,
             "l2": "flushed between timed steps (256 MB write)",
             "launch": "one step (L2 flush; per layer quantize A+B, then the GEMM) captured once into a CUDA "
                       "graph with CUDA events as graph nodes around each layer's quantize and GEMM; replayed "
@@ -184,12 +228,12 @@ def run_reference(args, rank: int, world: int):
     import oracle
 
     oracle.build()
-    cpu_oracle_sample(wl.gemms, target_s=0.5)  # warm-up: page in the inputs and the library
+    oracle_sample(wl, target_s=0.5)  # warm-up: page in the inputs and the library
     vals, secs_total = [], 0.0
     steps = max(1, min(args.steps, 3))
     cores, desc = None, ""
     for _ in range(steps):
-        v, secs, cores, desc = cpu_oracle_sample(wl.gemms, target_s=args.cpu_seconds)
+        v, secs, cores, desc = oracle_sample(wl, target_s=args.cpu_seconds)
         vals.append(v)
         secs_total += secs
     value = statistics.median(vals)
@@ -289,6 +333,38 @@ def run_gpu(args, rank: int, world: int):
                           "qbytes": quant_bytes(g.fmt, g.M, g.K, 4 if g.src_f32 else 2, True) +
                                     quant_bytes(g.fmt, g.N, g.K, 4 if g.src_f32 else 2, True),
                           "gbytes": gemm_bytes(g.fmt, g.M, g.N, g.K, bias is not None)})
+    elif wl.chain == "train":
+        g = wl.gemms[0]
+        fmt, M, K, N = g.fmt, g.M, g.K, g.N
+        hosts = {"x": host(make_activations(g)), "w": host(make_weights(g)), "bias": host(make_bias(g)),
+                 "dy": host(make_output_grad(g))}
+
+        def alloc():
+            D = {k: torch.empty_like(v, device=dev) for k, v in hosts.items()}
+            D.update({"qx": (bsq.empty_qtensor(fmt, M, K, dev), bsq.empty_qtensor(fmt, K, M, dev)),
+                      "qw": (bsq.empty_qtensor(fmt, N, K, dev), bsq.empty_qtensor(fmt, K, N, dev)),
+                      "qdy": (bsq.empty_qtensor(fmt, M, N, dev), bsq.empty_qtensor(fmt, N, M, dev)),
+                      "out": torch.empty((M, N), dtype=torch.bfloat16, device=dev),
+                      "dx": torch.empty((M, K), dtype=torch.bfloat16, device=dev),
+                      "dw": torch.empty((N, K), dtype=torch.bfloat16, device=dev)})
+            return D
+
+        def quant(D, s):
+            # both layouts of X, W and dY, each in one pass over its source
+            bsq.quantize_dual(fmt, D["x"], out=D["qx"], stream=s)
+            bsq.quantize_dual(fmt, D["w"], out=D["qw"], stream=s)
+            bsq.quantize_dual(fmt, D["dy"], stochastic=wl.grad_sr, seed=1, out=D["qdy"], stream=s)
+
+        def gemm(D, s):
+            bsq.gemm(D["qx"][0], D["qw"][0], D["bias"], out=D["out"], stream=s)  # Y = X W^T + b
+            bsq.gemm(D["qdy"][0], D["qw"][1], None, out=D["dx"], stream=s)       # dX = dY W
+            bsq.gemm(D["qdy"][1], D["qx"][1], None, out=D["dw"], stream=s)       # dW = dY^T X
+
+        units.append({"hosts": hosts, "alloc": alloc, "quant": quant, "gemm": gemm, "fmt": fmt,
+                      "flops": 3 * g.flops, "launches": 6, "outs": ("out", "dx", "dw"),
+                      "qbytes": dual_bytes(fmt, M, K, 2) + dual_bytes(fmt, N, K, 2) + dual_bytes(fmt, M, N, 2),
+                      "gbytes": gemm_bytes(fmt, M, N, K, True) + gemm_bytes(fmt, M, K, N, False) +
+                                gemm_bytes(fmt, N, K, M, False)})
     else:
         g1, g2 = wl.gemms  # fc1: M x K1 -> N1, fc2: M x N1 -> N2
         fmt = g1.fmt
@@ -424,7 +500,7 @@ def run_gpu(args, rank: int, world: int):
     # ------------------------------------------------------------ end to end through host buffers
     e2e_steps = max(3, min(args.steps, args.e2e_steps))
     h2d = sum(v.numel() * v.element_size() for U in units for v in U["hosts"].values() if v is not None)
-    d2h = sum(U["D"]["out"].numel() * 2 for U in units)
+    d2h = sum(U["D"][k].numel() * 2 for U in units for k in U.get("outs", ("out",)))
 
     # two device buffer sets per unit; streams: copy in, compute, copy out
     s_in, s_cmp, s_out = (torch.cuda.Stream(device=dev) for _ in range(3))
@@ -433,7 +509,8 @@ def run_gpu(args, rank: int, world: int):
         sets = []
         for U in units:
             D = U["alloc"]()
-            D["hout"] = torch.empty(D["out"].shape, dtype=torch.bfloat16).pin_memory()
+            for k in U.get("outs", ("out",)):
+                D["h" + k] = torch.empty(D[k].shape, dtype=torch.bfloat16).pin_memory()
             sets.append(D)
         bufs.append({"D": sets, "in_done": torch.cuda.Event(), "cmp_done": torch.cuda.Event(),
                      "out_done": torch.cuda.Event()})
@@ -455,8 +532,9 @@ def run_gpu(args, rank: int, world: int):
         B["cmp_done"].record(s_cmp)
         with torch.cuda.stream(s_out):
             s_out.wait_event(B["cmp_done"])
-            for D in B["D"]:
-                D["hout"].copy_(D["out"], non_blocking=True)
+            for U, D in zip(units, B["D"]):
+                for k in U.get("outs", ("out",)):
+                    D["h" + k].copy_(D[k], non_blocking=True)
             B["out_done"].record(s_out)
 
     for i in range(2):
@@ -495,7 +573,7 @@ def run_gpu(args, rank: int, world: int):
         "kernel_source_hash": khash,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, secs, cores, desc = cpu_oracle_sample(wl.gemms, target_s=args.cpu_seconds)
+        v, secs, cores, desc = oracle_sample(wl, target_s=args.cpu_seconds)
         line["cpu_baseline"] = {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc,
                                 "seconds": secs}
     if rank == 0:

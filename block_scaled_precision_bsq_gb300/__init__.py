@@ -326,5 +326,16 @@ def linear(fmt, x: torch.Tensor, w: torch.Tensor, bias: Optional[torch.Tensor] =
     return gemm(quantize(fmt, x, stream=stream), quantize(fmt, w, stream=stream), bias, stream=stream)
 
 
+def linear_backward(dy: torch.Tensor, x_col: QTensor, w_col: QTensor, stochastic: bool = False, seed: int = 0,
+                    stream=None):
+    """The two backward GEMMs of a block-scaled linear layer: dY (M x N, bf16 / fp32) is
+    quantized in both layouts in one pass, then dX = dY . W (dY row-wise against W column-wise,
+    M x K) and dW = dY^T . X (dY column-wise against X column-wise, N x K), both bf16 with fp32
+    accumulation. x_col / w_col are the column-wise operands of X (M x K) and W (N x K) from
+    quantize_dual (K x M and K x N). Returns (dX, dW)."""
+    dy_row, dy_col = quantize_dual(x_col.fmt, dy, stochastic=stochastic, seed=seed, stream=stream)
+    return gemm(dy_row, w_col, stream=stream), gemm(dy_col, x_col, stream=stream)
+
+
 def device_status(stream=None) -> int:
     return bsq_get_device_status(stream)

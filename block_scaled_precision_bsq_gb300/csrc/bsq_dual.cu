@@ -23,8 +23,21 @@
 //                one 32-bit word by two more shuffles, stored by the row's first lane.
 //   column pass  each thread takes one column and 64 / 32 rows of the tile: the warp reads 32
 //                consecutive columns of one row per load (conflict-free), the thread reduces
-//                its 32-row blocks alone and writes each block's 32 codes as contiguous bytes
-//                of the transposed operand (full 32-byte sectors) and its scale bytes.
+//                its 32-row blocks alone and puts each block's codes into a shared-memory
+//                staging tile laid out as the transposed operand's 128 rows (one per source
+//                column), swizzled so that 8 lanes on 8 rows hit 8 different bank groups; one
+//                2-D TMA store per tile then writes the staging tile as whole lines. Direct
+//                stores from this layout touch 32 lines per warp instruction and were the
+//                kernel's top stall (measured on GB300).
+// The staging tile is reused once the previous tile's store has read it (bulk wait_group.read
+// by the issuing thread before a named barrier of the consumer warps); that barrier also
+// reduces the consumers' full-barrier outcomes, so a timeout sends every consumer warp out of
+// the loop together.
+//
+// Stochastic rounding runs on the fp32 bits of v (exact): for a normal target binade it adds
+// the complement of the top D bits of the random word below the kept mantissa and truncates,
+// D = 23 - mantissa bits, which rounds up exactly when frac(q) > u; only targets in the
+// element format's subnormal range take a 64-bit compare.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -43,7 +56,12 @@ constexpr int kDStages = 3;
 constexpr int kDConsumerWarps = 8;   // warps 1..8; warp 0 lane 0 is the TMA producer
 constexpr int kDThreads = 32 * (kDConsumerWarps + 1);
 constexpr int kDCtasPerSm = 2;
-constexpr int kDSmem = kDStages * kDTileBytes + 128;
+constexpr int kDStageBytes = 16384;  // transposed codes of one tile (at most 128 x 128 bytes)
+// dynamic shared memory: staging tile (1024-byte aligned for the swizzled TMA store), input
+// ring, barriers; nothing static, so that two CTAs fit on an SM
+constexpr int kDRingOff = kDStageBytes;
+constexpr int kDBarOff = kDRingOff + kDStages * kDTileBytes;
+constexpr int kDSmem = kDBarOff + 128;
 
 struct DualArgs {
   int64_t rows, cols;  // R, C
@@ -66,12 +84,12 @@ __device__ __forceinline__ uint4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_
                                                uint32_t k1) {
 #pragma unroll
   for (int i = 0; i < 10; ++i) {
-    const uint32_t hi0 = __umulhi(0xD2511F53u, c0), lo0 = 0xD2511F53u * c0;
-    const uint32_t hi1 = __umulhi(0xCD9E8D57u, c2), lo1 = 0xCD9E8D57u * c2;
-    c0 = hi1 ^ c1 ^ k0;
-    c1 = lo1;
-    c2 = hi0 ^ c3 ^ k1;
-    c3 = lo0;
+    const uint64_t p0 = static_cast<uint64_t>(0xD2511F53u) * c0;  // one widening multiply each
+    const uint64_t p1 = static_cast<uint64_t>(0xCD9E8D57u) * c2;
+    c0 = static_cast<uint32_t>(p1 >> 32) ^ c1 ^ k0;
+    c1 = static_cast<uint32_t>(p1);
+    c2 = static_cast<uint32_t>(p0 >> 32) ^ c3 ^ k1;
+    c3 = static_cast<uint32_t>(p0);
     k0 += 0x9E3779B9u;
     k1 += 0xBB67AE85u;
   }
@@ -97,65 +115,102 @@ __device__ __forceinline__ float mx_inv_scale(uint32_t sbyte) { return __uint_as
 // Stochastic rounding of y = x / scale (exact in fp32 unless it fell below fp32's range) to an
 // E4M3 (MXFP8) or e2m1 code with the random word r: q = |y| / spacing at y's binade (the
 // subnormal spacing below the smallest normal), magnitude floor(q) + (frac(q) > u) with
-// u = (r >> 8) 2^-24, saturating at the largest finite value. All steps are exact in fp32.
+// u = (r >> 8) 2^-24, saturating at the largest finite value. Integer arithmetic on the fp32
+// bits, exact.
 template <int FMT>
 __device__ __forceinline__ uint32_t sr_code(float y, float x, uint32_t r) {
   constexpr uint32_t kM = (FMT == BSQ_MXFP8) ? 3u : 1u;         // mantissa bits
+  constexpr uint32_t D = 23u - kM;                              // fp32 mantissa bits below the kept ones
   constexpr uint32_t kEminB = (FMT == BSQ_MXFP8) ? 121u : 127u;  // biased exponent of the lowest normal binade
-  constexpr float kMax = (FMT == BSQ_MXFP8) ? 448.0f : 6.0f;
   constexpr uint32_t kMaxCode = (FMT == BSQ_MXFP8) ? 0x7Eu : 0x7u;
   constexpr uint32_t kSign = (FMT == BSQ_MXFP8) ? 7u : 3u;
-  const float av = fabsf(y);
-  const uint32_t eb = max(__float_as_uint(av) >> 23, kEminB);
-  const float q = av * __uint_as_float((254u + kM - eb) << 23);
-  const float fl = floorf(q);
-  const uint32_t rr = r >> 8;
-  const float u = __uint2float_rn(rr) * 5.9604644775390625e-08f;  // rr * 2^-24
-  // y == 0 for x != 0 only when x / scale underflowed fp32: its true fraction is positive and
-  // below 2^-24, so it steps up exactly when u == 0
-  const bool up = (q - fl > u) || (rr == 0u && av == 0.0f && x != 0.0f);
-  uint32_t mag = ((eb - kEminB) << kM) + static_cast<uint32_t>(fl) + (up ? 1u : 0u);
-  mag = av >= kMax ? kMaxCode : mag;
-  return ((__float_as_uint(y) >> 31) << kSign) | mag;
-}
-
-// Codes of n (a multiple of 4, <= 8 for e2m1 words) consecutive elements y[0..n) packed into
-// `w`: E4M3 one byte each (element i in byte i of w[i / 4]), e2m1 one nibble each (element i in
-// bits 4i of w[0]). RNE, or stochastic with words rw[i].
-template <int FMT, bool SR, int N>
-__device__ __forceinline__ void encode_n(const float* y, const float* x, const uint32_t* rw, uint32_t* w) {
-  if constexpr (FMT == BSQ_MXFP8) {
-#pragma unroll
-    for (int j = 0; j < N / 4; ++j) {
-      if constexpr (SR) {
-        w[j] = sr_code<FMT>(y[4 * j], x[4 * j], rw[4 * j]) | (sr_code<FMT>(y[4 * j + 1], x[4 * j + 1], rw[4 * j + 1]) << 8) |
-               (sr_code<FMT>(y[4 * j + 2], x[4 * j + 2], rw[4 * j + 2]) << 16) |
-               (sr_code<FMT>(y[4 * j + 3], x[4 * j + 3], rw[4 * j + 3]) << 24);
-      } else {
-        w[j] = cvt_e4m3x4(y[4 * j], y[4 * j + 1], y[4 * j + 2], y[4 * j + 3]);
-      }
-    }
+  const uint32_t yb = __float_as_uint(y);
+  const uint32_t b = yb & 0x7FFFFFFFu;
+  uint32_t mag;
+  if (b >= (kEminB << 23)) {
+    // q's fraction is the low D mantissa bits t: up iff t > r >> (32 - D), i.e. iff
+    // t + (2^D - 1 - (r >> (32 - D))) carries into the kept bits; the carry may move to the
+    // next binade, which is the next grid point
+    // (~r) >> (32 - D) = 2^D - 1 - (r >> (32 - D)); the exponent re-bias folds into the same add
+    mag = (b + ((1u << D) - 1u - ((kEminB - 1u) << 23)) - (r >> (32u - D))) >> D;
   } else {
-#pragma unroll
-    for (int j = 0; j < (N + 7) / 8; ++j) {
-      constexpr int kn = N < 8 ? N : 8;
-      if constexpr (SR) {
-        uint32_t v = 0;
-#pragma unroll
-        for (int i = 0; i < kn; ++i) v |= sr_code<FMT>(y[8 * j + i], x[8 * j + i], rw[8 * j + i]) << (4 * i);
-        w[j] = v;
-      } else if constexpr (kn == 8) {
-        w[j] = cvt_e2m1x8(y + 8 * j);
-      } else {
-        w[j] = cvt_e2m1x2(y[8 * j], y[8 * j + 1]) | (cvt_e2m1x2(y[8 * j + 2], y[8 * j + 3]) << 8);
-      }
+    // subnormal target: q = sig / 2^sh, sig the 24-bit significand of |y|
+    const uint32_t e = b >> 23;
+    uint32_t sig = e ? ((b & 0x7FFFFFu) | 0x800000u) : b;
+    const uint32_t sh = D + kEminB - max(e, 1u);  // > D
+    if (sh <= 24u) {
+      // the same carry trick on the significand, kept bits above sh
+      mag = (sig + ((~r) >> (32u - sh))) >> sh;
+    } else {
+      // q < 2^(24 - sh) <= 1/2: up iff (r >> 8) < ceil(sig / 2^(sh - 24)); past a shift of 24
+      // that ceiling is 1 for every positive sig. A y that underflowed to 0 from x != 0 is a
+      // positive value below every grid step and counts as sig = 1.
+      if (b == 0u && x != 0.0f) sig = 1u;
+      const uint32_t k = min(sh - 24u, 24u);
+      mag = (r >> 8) < ((sig + (1u << k) - 1u) >> k) ? 1u : 0u;
     }
   }
+  // from the largest finite value up the magnitude is at least kMaxCode; below it, at most
+  mag = min(mag, kMaxCode);
+  return ((yb >> 31) << kSign) | mag;
+}
+
+// Round-to-nearest-even codes of n (a multiple of 4, at most 8 for e2m1) consecutive elements
+// x[0..n) / scale, packed: E4M3 one byte each (element i in byte i % 4 of w[i / 4]), e2m1 one
+// nibble each (element i in bits 4i of w[0]).
+template <int FMT, int N>
+__device__ __forceinline__ void rne_codes(const float* x, float mul, uint32_t* w) {
+  if constexpr (FMT == BSQ_MXFP8) {
+#pragma unroll
+    for (int j = 0; j < N / 4; ++j)
+      w[j] = cvt_e4m3x4(x[4 * j] * mul, x[4 * j + 1] * mul, x[4 * j + 2] * mul, x[4 * j + 3] * mul);
+  } else if constexpr (N == 8) {
+    float y[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) y[i] = x[i] * mul;
+    w[0] = cvt_e2m1x8(y);
+  } else {
+    w[0] = cvt_e2m1x2(x[0] * mul, x[1] * mul) | (cvt_e2m1x2(x[2] * mul, x[3] * mul) << 8);
+  }
+}
+
+// Stochastic codes of the four elements x[0..4) / scale with the random words q (element i takes
+// word i), packed as rne_codes packs four: E4M3 one word, e2m1 the low 16 bits.
+template <int FMT>
+__device__ __forceinline__ uint32_t sr_codes4(const float* x, float mul, uint4 q) {
+  constexpr int kBits = (FMT == BSQ_MXFP8) ? 8 : 4;
+  return sr_code<FMT>(x[0] * mul, x[0], q.x) | (sr_code<FMT>(x[1] * mul, x[1], q.y) << kBits) |
+         (sr_code<FMT>(x[2] * mul, x[2], q.z) << (2 * kBits)) | (sr_code<FMT>(x[3] * mul, x[3], q.w) << (3 * kBits));
+}
+
+// Named barriers of the consumer warps (ids 1 and 2; 0 is __syncthreads).
+__device__ __forceinline__ bool consumers_and_sync(bool p) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.and.pred q, 1, %2, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(p)), "n"(32 * kDConsumerWarps)
+      : "memory");
+  return r != 0;
+}
+__device__ __forceinline__ void consumers_sync() {
+  asm volatile("bar.sync 2, %0;" ::"n"(32 * kDConsumerWarps) : "memory");
+}
+
+// Byte offset in the staging tile of logical byte `b` of row `row` (rows of S bytes), with the
+// TMA swizzle of an S-byte box row: 16-byte chunk bits [4, 4 + log2(S / 16)) XOR-ed with the
+// address bits from 7 up (the staging tile is 1024-byte aligned).
+template <int S>
+__device__ __forceinline__ uint32_t staging_offset(uint32_t row, uint32_t b) {
+  constexpr uint32_t kMask = S / 16 - 1;  // 7 (128 B), 3 (64 B), 1 (32 B)
+  const uint32_t off = row * S + b;
+  return off ^ (((off >> 7) & kMask) << 4);
 }
 
 template <int FMT, bool F32, bool SR>
 __global__ void __launch_bounds__(kDThreads, kDCtasPerSm)
-    dual_kernel(const __grid_constant__ CUtensorMap src_map, const DualArgs a) {
+    dual_kernel(const __grid_constant__ CUtensorMap src_map, const __grid_constant__ CUtensorMap col_map,
+                const DualArgs a) {
   constexpr int kEsize = F32 ? 4 : 2;
   constexpr int kRows = kDTileBytes / (kDCols * kEsize);  // 128 bf16, 64 fp32
   constexpr int V = 16 / kEsize;                           // elements of a 16-byte piece
@@ -163,19 +218,28 @@ __global__ void __launch_bounds__(kDThreads, kDCtasPerSm)
   constexpr int kRowSteps = kDTileBytes / 16 / 32 / kDConsumerWarps;  // row-pass steps per warp
   constexpr int kColBlocks = kRows / 32 / 2;  // column-pass 32-row blocks per thread (2 bf16, 1 fp32)
   constexpr bool kFp8 = (FMT == BSQ_MXFP8);
-  extern __shared__ uint8_t d_smem_raw[];
-  uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(d_smem_raw) + 127) & ~uintptr_t(127));
-  __shared__ uint64_t full_bar[kDStages], empty_bar[kDStages];
-  __shared__ int abort_flag;
+  constexpr int kBlockCodeBytes = kFp8 ? 32 : 16;        // codes of a 32-element block
+  constexpr int S = kRows * kBlockCodeBytes / 32;        // staging row: the tile's rows of one column
+  extern __shared__ __align__(1024) uint8_t d_smem[];
+  uint8_t* staging = d_smem;
+  uint8_t* ring = d_smem + kDRingOff;
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(d_smem + kDBarOff);
+  uint64_t* empty_bar = full_bar + kDStages;
+  int* abort_flag = reinterpret_cast<int*>(empty_bar + kDStages);
   const uint32_t warp = threadIdx.x >> 5;
   const uint32_t lane = threadIdx.x & 31u;
 
+  // the swizzled staging tile needs a 1024-byte aligned address (uniform: every thread leaves)
+  if (smem_u32(d_smem) & 1023u) {
+    if (threadIdx.x == 0) atomicCAS(a.status, 0, BSQ_ERR_LAUNCH);
+    return;
+  }
   if (threadIdx.x == 0) {
     for (int i = 0; i < kDStages; ++i) {
       mbar_init(&full_bar[i], 1);
       mbar_init(&empty_bar[i], kDConsumerWarps);
     }
-    abort_flag = 0;
+    *abort_flag = 0;
     fence_mbar_init();
   }
   __syncthreads();
@@ -189,7 +253,7 @@ __global__ void __launch_bounds__(kDThreads, kDCtasPerSm)
       int stage = 0;
       uint32_t phase = 0;
       for (int64_t t = blockIdx.x; t < a.ntiles; t += gridDim.x) {
-        if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1u, &abort_flag, a.status)) break;
+        if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1u, abort_flag, a.status)) break;
         const int64_t ti = t / a.tiles_c, tj = t - ti * a.tiles_c;
         mbar_arrive_expect_tx(&full_bar[stage], kDTileBytes);
         tma_load_2d(ring + stage * kDTileBytes, &src_map, &full_bar[stage], static_cast<int32_t>(tj * kDCols),
@@ -206,80 +270,86 @@ __global__ void __launch_bounds__(kDThreads, kDCtasPerSm)
   // -------------------------------------------------------------- consumers
   const int cw = static_cast<int>(warp) - 1;
   const int ct = static_cast<int>(threadIdx.x) - 32;  // 0 .. 255
+  const bool issuer = ct == 0;                         // issues the staging tile's TMA stores
+  if (issuer) prefetch_tmap(&col_map);
   const int64_t R = a.rows, C = a.cols;
+  bool stored = false;
   int stage = 0;
   uint32_t phase = 0;
   for (int64_t t = blockIdx.x; t < a.ntiles; t += gridDim.x) {
-    if (!mbar_wait_bounded_warp(&full_bar[stage], phase, &abort_flag, a.status)) break;
+    const bool ok = mbar_wait_bounded_warp(&full_bar[stage], phase, abort_flag, a.status);
     const int64_t ti = t / a.tiles_c, tj = t - ti * a.tiles_c;
     const int64_t r0 = ti * kRows, c0 = tj * kDCols;
     const uint8_t* tile = ring + stage * kDTileBytes;
 
     // ---- row pass: pieces of 16 bytes, the warp's 32 pieces contiguous
+    if (ok) {
 #pragma unroll 2
-    for (int s = 0; s < kRowSteps; ++s) {
-      const int f = (s * kDConsumerWarps + cw) * 32 + static_cast<int>(lane);
-      const int e0 = f * V;
-      const int rr = e0 / kDCols, cc = e0 % kDCols;
-      const uint4 v = *reinterpret_cast<const uint4*>(tile + f * 16);
-      float x[V];
-      if constexpr (F32) {
-        x[0] = __uint_as_float(v.x);
-        x[1] = __uint_as_float(v.y);
-        x[2] = __uint_as_float(v.z);
-        x[3] = __uint_as_float(v.w);
-      } else {
-        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          x[2 * i] = __uint_as_float(wv[i] << 16);
-          x[2 * i + 1] = __uint_as_float(wv[i] & 0xFFFF0000u);
-        }
-      }
-      float amax = 0.0f;
-#pragma unroll
-      for (int i = 0; i < V; ++i) amax = fmaxf(amax, fabsf(x[i]));
-#pragma unroll
-      for (int o = 1; o < LB; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
-      const uint32_t sbyte = mx_scale_byte<FMT>(amax);
-      const float mul = mx_inv_scale(sbyte);
-      float y[V];
-#pragma unroll
-      for (int i = 0; i < V; ++i) y[i] = x[i] * mul;
-      const int64_t r = r0 + rr, c = c0 + cc;
-      uint32_t rw[V];
-      if constexpr (SR) {
-        const uint64_t i0 = static_cast<uint64_t>(r) * static_cast<uint64_t>(C) + static_cast<uint64_t>(c);
-#pragma unroll
-        for (int gq = 0; gq < V / 4; ++gq) {
-          const uint4 q = sr_words((i0 >> 2) + gq, 0u, a);
-          rw[4 * gq] = q.x;
-          rw[4 * gq + 1] = q.y;
-          rw[4 * gq + 2] = q.z;
-          rw[4 * gq + 3] = q.w;
-        }
-      }
-      uint32_t w[kFp8 ? V / 4 : 1];
-      encode_n<FMT, SR, V>(y, x, rw, w);
-      if (r < R && c < C) {
-        const int64_t idx = r * C + c;
-        if constexpr (kFp8) {
-          if constexpr (V == 8) *reinterpret_cast<uint2*>(a.row_codes + idx) = make_uint2(w[0], w[1]);
-          else *reinterpret_cast<uint32_t*>(a.row_codes + idx) = w[0];
+      for (int s = 0; s < kRowSteps; ++s) {
+        const int f = (s * kDConsumerWarps + cw) * 32 + static_cast<int>(lane);
+        const int e0 = f * V;
+        const int rr = e0 / kDCols, cc = e0 % kDCols;
+        const uint4 v = *reinterpret_cast<const uint4*>(tile + f * 16);
+        float x[V];
+        if constexpr (F32) {
+          x[0] = __uint_as_float(v.x);
+          x[1] = __uint_as_float(v.y);
+          x[2] = __uint_as_float(v.z);
+          x[3] = __uint_as_float(v.w);
         } else {
-          if constexpr (V == 8) *reinterpret_cast<uint32_t*>(a.row_codes + idx / 2) = w[0];
-          else *reinterpret_cast<uint16_t*>(a.row_codes + idx / 2) = static_cast<uint16_t>(w[0]);
+          const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            x[2 * i] = __uint_as_float(wv[i] << 16);
+            x[2 * i + 1] = __uint_as_float(wv[i] & 0xFFFF0000u);
+          }
         }
-      }
-      // the row's four scale bytes -> one word (block b of the row in byte b)
-      uint32_t sw = sbyte << (8 * (cc / 32));
-      sw |= __shfl_xor_sync(0xFFFFFFFFu, sw, LB);
-      sw |= __shfl_xor_sync(0xFFFFFFFFu, sw, 2 * LB);
-      if ((lane & (4 * LB - 1)) == 0) {
-        const int64_t off = ((r >> 7) * a.nct_row + tj) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4;
-        *reinterpret_cast<uint32_t*>(a.row_scales + off) = sw;
+        float amax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < V; ++i) amax = fmaxf(amax, fabsf(x[i]));
+#pragma unroll
+        for (int o = 1; o < LB; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+        const uint32_t sbyte = mx_scale_byte<FMT>(amax);
+        const float mul = mx_inv_scale(sbyte);
+        const int64_t r = r0 + rr, c = c0 + cc;
+        uint32_t w[kFp8 ? V / 4 : 1];
+        if constexpr (SR) {
+          const uint64_t g0 = (static_cast<uint64_t>(r) * static_cast<uint64_t>(C) + static_cast<uint64_t>(c)) >> 2;
+          if constexpr (kFp8) {
+#pragma unroll
+            for (int gq = 0; gq < V / 4; ++gq) w[gq] = sr_codes4<FMT>(x + 4 * gq, mul, sr_words(g0 + gq, 0u, a));
+          } else {
+            w[0] = 0;
+#pragma unroll
+            for (int gq = 0; gq < V / 4; ++gq) w[0] |= sr_codes4<FMT>(x + 4 * gq, mul, sr_words(g0 + gq, 0u, a)) << (16 * gq);
+          }
+        } else {
+          rne_codes<FMT, V>(x, mul, w);
+        }
+        if (r < R && c < C) {
+          const int64_t idx = r * C + c;
+          if constexpr (kFp8) {
+            if constexpr (V == 8) *reinterpret_cast<uint2*>(a.row_codes + idx) = make_uint2(w[0], w[1]);
+            else *reinterpret_cast<uint32_t*>(a.row_codes + idx) = w[0];
+          } else {
+            if constexpr (V == 8) *reinterpret_cast<uint32_t*>(a.row_codes + idx / 2) = w[0];
+            else *reinterpret_cast<uint16_t*>(a.row_codes + idx / 2) = static_cast<uint16_t>(w[0]);
+          }
+        }
+        // the row's four scale bytes -> one word (block b of the row in byte b)
+        uint32_t sw = sbyte << (8 * (cc / 32));
+        sw |= __shfl_xor_sync(0xFFFFFFFFu, sw, LB);
+        sw |= __shfl_xor_sync(0xFFFFFFFFu, sw, 2 * LB);
+        if ((lane & (4 * LB - 1)) == 0) {
+          const int64_t off = ((r >> 7) * a.nct_row + tj) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4;
+          *reinterpret_cast<uint32_t*>(a.row_scales + off) = sw;
+        }
       }
     }
+
+    // the previous tile's store has read the staging tile; every consumer saw its full barrier
+    if (issuer && stored) bulk_wait_group_read<0>();
+    if (!consumers_and_sync(ok)) break;
 
     // ---- column pass: one column, kColBlocks blocks of 32 rows per thread
     {
@@ -296,48 +366,39 @@ __global__ void __launch_bounds__(kDThreads, kDCtasPerSm)
           if constexpr (F32) {
             x[k] = *reinterpret_cast<const float*>(tile + ((rb + k) * kDCols + cc) * 4);
           } else {
-            x[k] = __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(tile + ((rb + k) * kDCols + cc) * 2)) << 16);
+            x[k] = __uint_as_float(
+                static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(tile + ((rb + k) * kDCols + cc) * 2)) << 16);
           }
         }
         float m[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) m[i] = fmaxf(fmaxf(fabsf(x[4 * i]), fabsf(x[4 * i + 1])), fmaxf(fabsf(x[4 * i + 2]), fabsf(x[4 * i + 3])));
+        for (int i = 0; i < 8; ++i)
+          m[i] = fmaxf(fmaxf(fabsf(x[4 * i]), fabsf(x[4 * i + 1])), fmaxf(fabsf(x[4 * i + 2]), fabsf(x[4 * i + 3])));
 #pragma unroll
         for (int i = 0; i < 4; ++i) m[i] = fmaxf(m[i], m[i + 4]);
         const float amax = fmaxf(fmaxf(0.0f, fmaxf(m[0], m[1])), fmaxf(m[2], m[3]));
         const uint32_t sbyte = mx_scale_byte<FMT>(amax);
         sbytes |= sbyte << (8 * bb);
         const float mul = mx_inv_scale(sbyte);
-        const int64_t r = r0 + rb;
-        if (c < C && r < R) {
-          float y[32];
+        uint32_t w[kFp8 ? 8 : 4];
+        if constexpr (SR) {
+          const uint64_t g0 = (static_cast<uint64_t>(c) * static_cast<uint64_t>(R) + static_cast<uint64_t>(r0 + rb)) >> 2;
 #pragma unroll
-          for (int k = 0; k < 32; ++k) y[k] = x[k] * mul;
-          uint32_t rw[SR ? 32 : 1];
-          if constexpr (SR) {
-            const uint64_t i0 = static_cast<uint64_t>(c) * static_cast<uint64_t>(R) + static_cast<uint64_t>(r);
+          for (int gq = 0; gq < 8; ++gq) {
+            const uint32_t v4 = sr_codes4<FMT>(x + 4 * gq, mul, sr_words(g0 + gq, 1u, a));
+            if constexpr (kFp8) w[gq] = v4;
+            else if (gq & 1) w[gq >> 1] |= v4 << 16;
+            else w[gq >> 1] = v4;
+          }
+        } else {
 #pragma unroll
-            for (int gq = 0; gq < 8; ++gq) {
-              const uint4 q = sr_words((i0 >> 2) + gq, 1u, a);
-              rw[4 * gq] = q.x;
-              rw[4 * gq + 1] = q.y;
-              rw[4 * gq + 2] = q.z;
-              rw[4 * gq + 3] = q.w;
-            }
-          }
-          const int64_t idx = c * R + r;
-          if constexpr (kFp8) {
-            uint32_t w[8];
-            encode_n<FMT, SR, 32>(y, x, rw, w);
-            uint4* dst = reinterpret_cast<uint4*>(a.col_codes + idx);
-            dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-            dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-          } else {
-            uint32_t w[4];
-            encode_n<FMT, SR, 32>(y, x, rw, w);
-            *reinterpret_cast<uint4*>(a.col_codes + idx / 2) = make_uint4(w[0], w[1], w[2], w[3]);
-          }
+          for (int j = 0; j < (kFp8 ? 8 : 4); ++j) rne_codes<FMT, kFp8 ? 4 : 8>(x + (kFp8 ? 4 : 8) * j, mul, w + j);
         }
+        // codes -> staging row cc, bytes [rb * kBlockCodeBytes / 32, + kBlockCodeBytes)
+        const uint32_t b0 = static_cast<uint32_t>(rb * kBlockCodeBytes / 32);
+        *reinterpret_cast<uint4*>(staging + staging_offset<S>(cc, b0)) = make_uint4(w[0], w[1], w[2], w[3]);
+        if constexpr (kFp8)
+          *reinterpret_cast<uint4*>(staging + staging_offset<S>(cc, b0 + 16)) = make_uint4(w[4], w[5], w[6], w[7]);
       }
       // scale bytes of column c: row c of the column layout, scale columns (r0 % 128) / 32 + ..
       const int64_t off = (tj * a.nct_col + (r0 >> 7)) * 512 + (cc & 31) * 16 + ((cc >> 5) & 3) * 4 +
@@ -346,17 +407,29 @@ __global__ void __launch_bounds__(kDThreads, kDCtasPerSm)
       else a.col_scales[off] = static_cast<uint8_t>(sbytes);
     }
 
+    // every read of the tile is done: release it to the producer
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty_bar[stage]);
+    // staging complete and visible to the async proxy -> one TMA store of the transposed codes
+    // (rows of the column layout beyond C and bytes beyond R are clipped by the tensor map)
+    fence_proxy_async_smem();
+    consumers_sync();
+    if (issuer && r0 < R) {
+      tma_store_2d(&col_map, staging, static_cast<int32_t>(r0 * kBlockCodeBytes / 32), static_cast<int32_t>(c0));
+      bulk_commit_group();
+      stored = true;
+    }
     if (++stage == kDStages) {
       stage = 0;
       phase ^= 1u;
     }
   }
+  if (issuer && stored) bulk_wait_group0();  // the last stores have completed
 }
 
 template <int FMT, bool F32, bool SR>
-cudaError_t launch_d(const CUtensorMap& map, const DualArgs& a, int grid, cudaStream_t stream) {
+cudaError_t launch_d(const CUtensorMap& src_map, const CUtensorMap& col_map, const DualArgs& a, int grid,
+                     cudaStream_t stream) {
   static cudaError_t attr =
       cudaFuncSetAttribute(dual_kernel<FMT, F32, SR>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDSmem);
   if (attr != cudaSuccess) return attr;
@@ -370,13 +443,18 @@ cudaError_t launch_d(const CUtensorMap& map, const DualArgs& a, int grid, cudaSt
   cfg.stream = stream;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, dual_kernel<FMT, F32, SR>, map, a);
+  return cudaLaunchKernelEx(&cfg, dual_kernel<FMT, F32, SR>, src_map, col_map, a);
 }
 
 template <int FMT>
-cudaError_t launch_d_fmt(bool f32, bool sr, const CUtensorMap& map, const DualArgs& a, int grid, cudaStream_t stream) {
-  if (f32) return sr ? launch_d<FMT, true, true>(map, a, grid, stream) : launch_d<FMT, true, false>(map, a, grid, stream);
-  return sr ? launch_d<FMT, false, true>(map, a, grid, stream) : launch_d<FMT, false, false>(map, a, grid, stream);
+cudaError_t launch_d_fmt(bool f32, bool sr, const CUtensorMap& src_map, const CUtensorMap& col_map,
+                         const DualArgs& a, int grid, cudaStream_t stream) {
+  if (f32) {
+    return sr ? launch_d<FMT, true, true>(src_map, col_map, a, grid, stream)
+              : launch_d<FMT, true, false>(src_map, col_map, a, grid, stream);
+  }
+  return sr ? launch_d<FMT, false, true>(src_map, col_map, a, grid, stream)
+            : launch_d<FMT, false, false>(src_map, col_map, a, grid, stream);
 }
 
 }  // namespace
@@ -401,14 +479,25 @@ int launch_quantize_dual(int fmt, bool src_f32, bool stochastic, uint64_t seed, 
   a.seed_lo = static_cast<uint32_t>(seed);
   a.seed_hi = static_cast<uint32_t>(seed >> 32);
   a.status = dev.status;
-  CUtensorMap map;
+  CUtensorMap map, col_map;
   if (!make_map_2d(&map, src_f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, src,
                    static_cast<uint64_t>(cols), static_cast<uint64_t>(rows), static_cast<uint64_t>(cols * esize), kDCols,
                    static_cast<uint32_t>(tile_rows), CU_TENSOR_MAP_SWIZZLE_NONE))
     return BSQ_ERR_LAUNCH;
+  // the column-layout codes as `cols` rows of R code bytes (MXFP8) or R / 2 (MXFP4); a box is
+  // one tile's staging: 128 rows of tile_rows codes
+  const int64_t code_row = fmt == BSQ_MXFP8 ? rows : rows / 2;
+  const uint32_t box_inner = static_cast<uint32_t>(fmt == BSQ_MXFP8 ? tile_rows : tile_rows / 2);
+  const CUtensorMapSwizzle sw = box_inner == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
+                                : box_inner == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                  : CU_TENSOR_MAP_SWIZZLE_32B;
+  if (!make_map_2d(&col_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, col_codes, static_cast<uint64_t>(code_row),
+                   static_cast<uint64_t>(cols), static_cast<uint64_t>(code_row), box_inner, kDCols, sw))
+    return BSQ_ERR_LAUNCH;
   const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(a.ntiles, kDCtasPerSm * dev.num_sms)));
-  const cudaError_t err = fmt == BSQ_MXFP8 ? launch_d_fmt<BSQ_MXFP8>(src_f32, stochastic, map, a, grid, stream)
-                                           : launch_d_fmt<BSQ_MXFP4>(src_f32, stochastic, map, a, grid, stream);
+  const cudaError_t err = fmt == BSQ_MXFP8
+                              ? launch_d_fmt<BSQ_MXFP8>(src_f32, stochastic, map, col_map, a, grid, stream)
+                              : launch_d_fmt<BSQ_MXFP4>(src_f32, stochastic, map, col_map, a, grid, stream);
   return err == cudaSuccess ? BSQ_OK : BSQ_ERR_LAUNCH;
 }
 

@@ -1,0 +1,66 @@
+"""GPU parity of the backward GEMMs of a block-scaled linear layer against the CPU oracle:
+dgrad dX = dY . W (dY quantized along N, W along N: its column-wise layout) and wgrad
+dW = dY^T . X (dY and X quantized along M: their column-wise layouts), every operand from the
+dual-layout quantizer, the output gradient with stochastic rounding. Operands bit-identical to
+the oracle's; outputs within |gpu - y| <= 2^-7 |y| + 1e-5 sum_k |a b| of the oracle's fp64
+GEMM on them."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests.gpu_util import check_gemm_rows, sample_rows, to_dev
+from workloads import Gemm, MXFP8, make_activations, make_output_grad, make_weights
+
+pytestmark = pytest.mark.gpu
+
+
+def _bsq():
+    import block_scaled_precision_bsq_gb300 as bsq
+
+    return bsq
+
+
+def _same(got, want, what):
+    codes = got.codes.cpu().numpy()
+    assert np.array_equal(codes, want.codes), "%s codes differ in %d bytes" % (what, int((codes != want.codes).sum()))
+    assert np.array_equal(got.scales.cpu().numpy(), want.tiled_scales()), "%s scales differ" % what
+
+
+def _run(fmt, M, K, N, sr, seed, full_rows=False):
+    bsq = _bsq()
+    g = Gemm("layer", fmt, M, K, N, seed=seed)
+    x, w, dy = make_activations(g), make_weights(g), make_output_grad(g)
+    xr, xc = bsq.quantize_dual(fmt, to_dev(x))
+    wr, wc = bsq.quantize_dual(fmt, to_dev(w))
+    dx, dw = bsq.linear_backward(to_dev(dy), xc, wc, stochastic=sr, seed=seed + 99)
+    torch.cuda.synchronize()
+    assert bsq.device_status() == 0
+    ox = oracle.quantize_dual(fmt, x)
+    ow = oracle.quantize_dual(fmt, w)
+    ody = oracle.quantize_dual(fmt, dy, stochastic=sr, seed=seed + 99)
+    _same(xc, ox[1], "X column-wise")
+    _same(wc, ow[1], "W column-wise")
+    dyr, dyc = bsq.quantize_dual(fmt, to_dev(dy), stochastic=sr, seed=seed + 99)
+    _same(dyr, ody[0], "dY row-wise")
+    _same(dyc, ody[1], "dY column-wise")
+    rows_dx = np.arange(M) if full_rows else sample_rows(M, seed=1)
+    rows_dw = np.arange(N) if full_rows else sample_rows(N, seed=2)
+    dx_np = dx.float().cpu().numpy().astype(np.float64)[rows_dx]
+    dw_np = dw.float().cpu().numpy().astype(np.float64)[rows_dw]
+    check_gemm_rows(dx_np, ody[0], ow[1], None, rows_dx, "dgrad")
+    check_gemm_rows(dw_np, ody[1], ox[1], None, rows_dw, "wgrad")
+
+
+# dgrad contracts over N and wgrad over M, so both are multiples of 128 (the MXFP8 GEMM's K
+# step); output tiles of 256 x 256 are ragged in every case
+@pytest.mark.parametrize("M,K,N", [(128, 128, 128), (384, 256, 640), (640, 416, 384)])
+@pytest.mark.parametrize("sr", [False, True])
+def test_backward_mxfp8_matches_oracle(M, K, N, sr):
+    _run(MXFP8, M, K, N, sr, seed=M + K + N, full_rows=True)
+
+
+def test_backward_full_size_vitb_fc1():
+    """ViT-B/16 fc1 at training shape (M = 14336 tokens, K = 768, N = 3072): dgrad is
+    14336 x 768 over N = 3072, wgrad 3072 x 768 over M = 14336; sampled rows."""
+    _run(MXFP8, 14336, 768, 3072, True, seed=0)

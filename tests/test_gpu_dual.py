@@ -69,6 +69,11 @@ def test_dual_special_values(fmt, src_f32):
     x[96:128, :] *= 1e-39 if src_f32 else 1e-40          # subnormal sources
     x[128:160, 128:160] = np.ldexp(1.0, 100) * rng.standard_normal((32, 32))
     x[5, 130] = -0.0
+    # one huge element per block, the rest 2^-40 smaller: codes far below the element format's
+    # subnormal spacing (stochastic rounding then steps up only when u is 0)
+    x[0:64, 160:192] = rng.standard_normal((64, 32)) * 2.0 ** -20
+    x[0, 160:192] = 2.0 ** 20
+    x[32:64, 160] = -(2.0 ** 20)
     data = x.astype(np.float32) if src_f32 else f32_to_bf16_bits(x.astype(np.float32))
     for sr in (False, True):
         _check(fmt, data, sr, seed=3, label="%s special f32=%d sr=%d" % (fmt, src_f32, sr))

@@ -18,6 +18,10 @@ quantized GEMMs are qkv / proj / fc1 / fc2 of every ViT block):
   vitl_mlp_*_fused / _unfused
                   one ViT-L/16 MLP, fc1 -> GELU -> fc2, with fc2's operand produced by fc1's
                   epilogue (fused) or by a bf16 output and a separate quantize pass (unfused).
+  vitb_fc1_mxfp8_train[_sr]
+                  one training step of the ViT-B/16 fc1 layer at training shape: forward,
+                  dgrad (dX = dY W) and wgrad (dW = dY^T X), every operand from the dual-layout
+                  quantizer; the output gradient dY rounded to nearest or stochastically.
 
 Recipe (every array is drawn in fp64 by numpy's default_rng, cast to fp32 with
 round-to-nearest, then to bf16 with round-to-nearest-even where the input is bf16):
@@ -25,6 +29,7 @@ round-to-nearest, then to bf16 with round-to-nearest-even where the input is bf1
   * activations N(0,1) (t(4) for the NVFP4 sweep); 0.5 % of the K channels,
     round(0.005 * K) of them picked without replacement from A's stream, scaled x20;
   * weights N(0, 0.02), bias N(0, 0.01);
+  * output gradient dY[M, N] N(0, 1e-3) from stream seed + 5 (training workloads);
   * tiny case: round(0.01 * M * K) entries of A picked without replacement, scaled x50.
 """
 from __future__ import annotations
@@ -81,8 +86,10 @@ class Workload:
     # "fused" / "unfused": gemms = [fc1, fc2] of one MLP, fc2's A being GELU of fc1's output
     # (quantized in fc1's epilogue, or written as bf16 and quantized by a separate pass);
     # "ln_fused": as "fused", with fc1's A = LayerNorm of the activations, quantized by the
-    # LN + quantize kernel
+    # LN + quantize kernel; "train": gemms = [the layer], one training step (forward, dgrad,
+    # wgrad) with dual-layout operands
     chain: Optional[str] = None
+    grad_sr: bool = False  # "train": stochastic rounding of the output gradient
 
 
 def _vitl_sweep(fmt: str, a_dist: str) -> List[Gemm]:
@@ -139,6 +146,14 @@ for _fmt, _M, _tag in ((MXFP8, 7 * 1024, "vitl_mlp_mxfp8"), (MXFP4, 32 * 1600, "
         WORKLOADS["%s_%s" % (_tag, _chain)] = _mlp_chain("%s_%s" % (_tag, _chain), _fmt, _M, _chain)
 
 
+for _sr in (False, True):
+    _n = "vitb_fc1_mxfp8_train" + ("_sr" if _sr else "")
+    WORKLOADS[_n] = Workload(
+        _n, "ViT-B/16 MLP fc1 training step (forward, dgrad, wgrad) at M=14336, K=768, N=3072, MXFP8, "
+            "dual-layout operands, output gradient rounded %s" % ("stochastically" if _sr else "to nearest even"),
+        [Gemm("fc1", MXFP8, 14 * 1024, 768, 3072)], "train", _sr)
+
+
 def _gelu_erf(x: np.ndarray) -> np.ndarray:
     # exact erf form of GELU, fp64; part of the input recipe for fc2's activations
     from scipy.special import erf
@@ -183,6 +198,14 @@ def make_weights(g: Gemm) -> np.ndarray:
     rng = np.random.default_rng(g.seed + 1)
     w = rng.standard_normal((g.N, g.K)) * g.w_std
     return _store(w, g.src_f32)
+
+
+def make_output_grad(g: Gemm, rows: Optional[int] = None, std: float = 1e-3) -> np.ndarray:
+    """dY[M, N], the gradient of the layer's output (bf16 bits, or fp32 for fp32 layers); `rows`
+    < M draws only the leading rows of the same stream."""
+    rng = np.random.default_rng(g.seed + 5)
+    M = g.M if rows is None else rows
+    return _store(rng.standard_normal((M, g.N)) * std, g.src_f32)
 
 
 def make_bias(g: Gemm) -> Optional[np.ndarray]:
