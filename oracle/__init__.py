@@ -88,6 +88,9 @@ def lib() -> ctypes.CDLL:
         L.orc_quantize_mx_dual.argtypes = [ctypes.c_int, vp, ctypes.c_int, i64, i64, ctypes.c_int, ctypes.c_uint64,
                                            u8p, u8p, u8p, u8p]
         L.orc_num_threads.restype = ctypes.c_int
+        L.orc_quantize_nv_dual.restype = ctypes.c_int
+        L.orc_quantize_nv_dual.argtypes = [vp, ctypes.c_int, i64, i64, ctypes.c_int, ctypes.c_float, ctypes.c_int,
+                                           ctypes.c_uint64, u8p, u8p, u8p, u8p, vp, vp]
         L.orc_set_num_threads.argtypes = [ctypes.c_int]
         _lib = L
     return _lib
@@ -322,17 +325,32 @@ def encode_sr_array(elem: str, v: np.ndarray, u: np.ndarray) -> np.ndarray:
     return out
 
 
-def quantize_dual(fmt, x: np.ndarray, stochastic: bool = False, seed: int = 0) -> Tuple[Quantized, Quantized]:
-    """Dual-layout MX quantization (reading R10): (row-wise R x C, column-wise C x R)."""
+def quantize_dual(fmt, x: np.ndarray, stochastic: bool = False, seed: int = 0,
+                  global_scale: Optional[float] = None) -> Tuple[Quantized, Quantized]:
+    """Dual-layout quantization (readings R10, R11): (row-wise R x C, column-wise C x R). NVFP4
+    shares one per-tensor scale between the layouts (computed, or `global_scale`)."""
     f = _fmt(fmt)
-    assert f in (MXFP8, MXFP4)
     x, is_f32 = _src(x)
     R, C = x.shape
+    bs = block_size(f)
     rc = np.zeros(codes_bytes(f, R, C), dtype=np.uint8)
-    rs = np.zeros((R, C // 32), dtype=np.uint8)
+    rs = np.zeros((R, C // bs), dtype=np.uint8)
     cc = np.zeros(codes_bytes(f, C, R), dtype=np.uint8)
-    cs = np.zeros((C, R // 32), dtype=np.uint8)
-    st = lib().orc_quantize_mx_dual(f, _ptr(x), is_f32, R, C, 1 if stochastic else 0, int(seed) & (2 ** 64 - 1),
+    cs = np.zeros((C, R // bs), dtype=np.uint8)
+    seed = int(seed) & (2 ** 64 - 1)
+    if f == NVFP4:
+        g = np.zeros(1, np.float32)
+        amax = np.zeros(1, np.float32)
+        st = lib().orc_quantize_nv_dual(_ptr(x), is_f32, R, C, 0 if global_scale is None else 1,
+                                        0.0 if global_scale is None else float(global_scale),
+                                        1 if stochastic else 0, seed, _ptr(rc), _ptr(rs), _ptr(cc), _ptr(cs),
+                                        _ptr(g), _ptr(amax))
+        if st:
+            raise ValueError("oracle dual quantize failed: %d" % st)
+        return (Quantized(f, R, C, rc, rs, float(g[0]), float(amax[0])),
+                Quantized(f, C, R, cc, cs, float(g[0]), float(amax[0])))
+    assert global_scale is None
+    st = lib().orc_quantize_mx_dual(f, _ptr(x), is_f32, R, C, 1 if stochastic else 0, seed,
                                     _ptr(rc), _ptr(rs), _ptr(cc), _ptr(cs))
     if st:
         raise ValueError("oracle dual quantize failed: %d" % st)

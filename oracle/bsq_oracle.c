@@ -59,6 +59,12 @@
  *       Numbers: As Easy as 1, 2, 3", SC'11) at counter (floor(i/4) low 32 bits, high 32 bits,
  *       layout, 0) and key (seed low, seed high), i the element's index in its layout's order
  *       (row layout r * C + c, column layout c * R + r), layout 0 = row, 1 = column.
+ *   R11 Dual-layout NVFP4 (the pages' fused FP4 quantizer writes NVFP4 codes for both
+ *       layouts; [LT] section 4.3 training stack P3, dY with stochastic rounding): one per-tensor
+ *       g for the whole matrix (R3: fp32(amax / 2688), or a given g), shared by both layouts;
+ *       each layout applies R3 along its rows (1x16 blocks). With stochastic rounding the
+ *       element y = fp32(x / fp32(s g)) of R3 rounds by the rule of R10 (e2m1, the same Philox
+ *       words and element indices); s = 0 still gives signed zero codes.
  *
  * Pins (tests that tie this code to something other than itself) are in the test suite:
  * exhaustive decode tables against two independent float8/float4 libraries, encoders
@@ -652,5 +658,92 @@ int orc_quantize_mx_dual(int fmt, const void* src, int src_f32, int64_t R, int64
         }
     }
     free(x);
+    return ORC_OK;
+}
+
+/* One NVFP4 block of 16 values at stride `step` of `x` (R3 with the shared g and 6 g): E4M3
+ * scale code and e2m1 codes, round-to-nearest or stochastic with the words of elements
+ * base_index + k of `layout` (R11). */
+static uint8_t nv_block(const float* x, int64_t step, float g, float six_g, int sr, uint64_t seed, int layout,
+                        uint64_t base_index, unsigned codes[16]) {
+    float bamax = 0.0f, q, s, sg;
+    unsigned s_code;
+    int k;
+    for (k = 0; k < 16; ++k) {
+        float a = fabsf(x[k * step]);
+        if (a > bamax) bamax = a;
+    }
+    if (g == 0.0f) {
+        s_code = 0;
+    } else {
+        q = bamax / six_g;                           /* fp32 division */
+        s_code = orc_encode_e4m3((double)q) & 0x7Fu;
+    }
+    s = (float)orc_decode_e4m3(s_code);              /* exact in fp32 */
+    sg = s * g;                                      /* fp32 multiplication */
+    for (k = 0; k < 16; ++k) {
+        float xv = x[k * step];
+        if (s == 0.0f) {
+            codes[k] = signbit(xv) ? 0x8u : 0x0u;
+        } else {
+            float y = xv / sg;                       /* fp32 division */
+            if (sr) {
+                double u = ldexp((double)(sr_word(seed, layout, base_index + (uint64_t)k) >> 8), -24);
+                codes[k] = encode_sr((double)y, 1, u);
+            } else {
+                codes[k] = orc_encode_e2m1((double)y);
+            }
+        }
+    }
+    return (uint8_t)s_code;
+}
+
+/* Dual-layout NVFP4 (reading R11) of a bf16 / fp32 R x C matrix (R % 16 == 0, C % 16 == 0):
+ * row codes R x C with plain E4M3 scales R x C/16, column codes C x R (the transpose,
+ * quantized along R) with plain scales C x R/16; g_out / amax_out receive the shared
+ * per-tensor scale and the tensor's amax. */
+int orc_quantize_nv_dual(const void* src, int src_f32, int64_t R, int64_t C, int global_given, float g_in, int sr,
+                         uint64_t seed, uint8_t* row_codes, uint8_t* row_scales, uint8_t* col_codes,
+                         uint8_t* col_scales, float* g_out, float* amax_out) {
+    float* x;
+    float amax, g, six_g;
+    int64_t i, r, c;
+    int st;
+    if (!src || !row_codes || !row_scales || !col_codes || !col_scales || R <= 0 || C <= 0) return ORC_ERR_ARG;
+    if (R % 16 || C % 16) return ORC_ERR_SHAPE;
+    st = check_finite(src, src_f32, R * C);
+    if (st) return st;
+    if (global_given && !(isfinite(g_in) && g_in >= 0.0f)) return ORC_ERR_ARG;
+    amax = orc_tensor_amax(src, src_f32, R * C);
+    g = global_given ? g_in : amax / 2688.0f; /* one fp32 division, 2688 = 6 * 448 */
+    six_g = 6.0f * g;                          /* one fp32 multiplication */
+    x = (float*)malloc((size_t)(R * C) * sizeof(float));
+    if (!x) return ORC_ERR_ARG;
+    for (i = 0; i < R * C; ++i) x[i] = load_src(src, src_f32, i);
+#pragma omp parallel for schedule(static)
+    for (r = 0; r < R; ++r) {
+        int64_t b;
+        unsigned codes[16];
+        int k;
+        for (b = 0; b < C / 16; ++b) {
+            row_scales[r * (C / 16) + b] =
+                nv_block(x + r * C + b * 16, 1, g, six_g, sr, seed, 0, (uint64_t)(r * C + b * 16), codes);
+            for (k = 0; k < 16; ++k) put_code(ORC_NVFP4, row_codes, r * C + b * 16 + k, codes[k]);
+        }
+    }
+#pragma omp parallel for schedule(static)
+    for (c = 0; c < C; ++c) {
+        int64_t b;
+        unsigned codes[16];
+        int k;
+        for (b = 0; b < R / 16; ++b) {
+            col_scales[c * (R / 16) + b] =
+                nv_block(x + (b * 16) * C + c, C, g, six_g, sr, seed, 1, (uint64_t)(c * R + b * 16), codes);
+            for (k = 0; k < 16; ++k) put_code(ORC_NVFP4, col_codes, c * R + b * 16 + k, codes[k]);
+        }
+    }
+    free(x);
+    if (g_out) *g_out = g;
+    if (amax_out) *amax_out = amax;
     return ORC_OK;
 }

@@ -91,3 +91,84 @@ def test_dual_sr_steps_at_most_one_code_and_depends_on_seed():
     assert not np.array_equal(s1_row.codes, s2_row.codes)
     s1_again, _ = oracle.quantize_dual("mxfp8", x, stochastic=True, seed=7)
     assert np.array_equal(s1_again.codes, s1_row.codes)
+
+
+def test_sr_e2m1_is_exactly_unbiased_on_dyadic_values():
+    rng = np.random.default_rng(15)
+    v = (rng.integers(-6 * 8, 6 * 8, 120) / 8.0).astype(np.float64)  # multiples of 1/8 in (-6, 6)
+    u = np.arange(2 ** 12) / 2.0 ** 12
+    for x in v:
+        codes = oracle.encode_sr_array("e2m1", np.full(u.shape, x), u)
+        assert np.mean([oracle.decode_e2m1(int(c)) for c in codes]) == x
+
+
+@pytest.mark.parametrize("given", [None, 0.0021])
+def test_dual_nvfp4_rne_equals_pinned_quantizer(given):
+    """Round to nearest: the two layouts are the pinned NVFP4 quantizer applied to X and to X^T
+    with the same per-tensor scale (the tensor's amax, or the given scale)."""
+    rng = np.random.default_rng(16)
+    x = f32_to_bf16_bits((rng.standard_t(4, size=(96, 160)) * 3.0).astype(np.float32))
+    row, col = oracle.quantize_dual("nvfp4", x, global_scale=given)
+    a = oracle.quantize("nvfp4", x, global_scale=given)
+    t = oracle.quantize("nvfp4", np.ascontiguousarray(x.T), global_scale=given)
+    for got, want in ((row, a), (col, t)):
+        assert np.array_equal(got.codes, want.codes) and np.array_equal(got.scales, want.scales)
+        assert got.g == want.g and got.amax == want.amax
+        assert np.array_equal(got.tiled_scales(), want.tiled_scales())
+
+
+def _nibble(codes, i):
+    return (int(codes[i // 2]) >> (4 * (i % 2))) & 0xF
+
+
+@pytest.mark.parametrize("fmt", ["mxfp8", "mxfp4", "nvfp4"])
+def test_dual_sr_takes_each_elements_own_word(fmt):
+    """Stochastic codes equal the pinned encoder applied to the element's scaled value v with
+    u from the Philox word the reading assigns to the element (counter floor(i/4) and layout,
+    key = seed, word i mod 4; i = r C + c in the row layout, c R + r in the column layout),
+    and v taken from the round-to-nearest dual quantizer's scales (which rounding leaves
+    alone)."""
+    rng = np.random.default_rng(17)
+    R, C, seed = 64, 96, 0x1234_5678_9ABC_DEF0
+    x = f32_to_bf16_bits((rng.standard_normal((R, C)) * 3.0).astype(np.float32))
+    xf = (x.astype(np.uint32) << 16).view(np.float32)
+    rne = oracle.quantize_dual(fmt, x)
+    sr = oracle.quantize_dual(fmt, x, stochastic=True, seed=seed)
+    elem = "e4m3" if fmt == "mxfp8" else "e2m1"
+    bs = 16 if fmt == "nvfp4" else 32
+    for layout, (q_rne, q_sr) in enumerate(zip(rne, sr)):
+        rows, cols = q_sr.rows, q_sr.cols
+        for _ in range(300):
+            r, c = int(rng.integers(rows)), int(rng.integers(cols))
+            src = xf[r, c] if layout == 0 else xf[c, r]
+            sb = int(q_rne.scales[r, c // bs])
+            if fmt == "nvfp4":
+                sg = np.float32(oracle.decode_e4m3(sb)) * np.float32(q_rne.g)
+                if sg == 0:
+                    continue
+                v = float(np.float32(src) / sg)
+            else:
+                v = float(src) * 2.0 ** (127 - sb)
+            i = r * cols + c
+            words = oracle.philox4x32_10([(i // 4) & 0xFFFFFFFF, (i // 4) >> 32, layout, 0],
+                                         [seed & 0xFFFFFFFF, seed >> 32])
+            u = (words[i % 4] >> 8) * 2.0 ** -24
+            want = int(oracle.encode_sr_array(elem, np.array([v]), np.array([u]))[0])
+            got = int(q_sr.codes[i]) if fmt == "mxfp8" else _nibble(q_sr.codes, i)
+            assert got == want, (fmt, layout, r, c, v, u, got, want)
+
+
+def test_dual_nvfp4_sr_steps_at_most_one_code():
+    rng = np.random.default_rng(18)
+    x = f32_to_bf16_bits(rng.standard_t(4, size=(64, 128)).astype(np.float32))
+    rne = oracle.quantize_dual("nvfp4", x)
+    s1 = oracle.quantize_dual("nvfp4", x, stochastic=True, seed=3)
+    s2 = oracle.quantize_dual("nvfp4", x, stochastic=True, seed=4)
+    for a, b in zip(s1, rne):
+        assert np.array_equal(a.scales, b.scales) and a.g == b.g
+        lo_a, hi_a = a.codes & 0xF, a.codes >> 4
+        lo_b, hi_b = b.codes & 0xF, b.codes >> 4
+        for p, q in ((lo_a, lo_b), (hi_a, hi_b)):
+            assert np.array_equal(p & 0x8, q & 0x8)  # the sign of x in both
+            assert np.abs((p & 0x7).astype(int) - (q & 0x7).astype(int)).max() <= 1
+    assert not np.array_equal(s1[0].codes, s2[0].codes)
