@@ -54,7 +54,7 @@ _lib.bsq_quantize_batch.argtypes = [_int, _int, ctypes.POINTER(QuantItem), _vp]
 _lib.bsq_layernorm_quantize.restype = _int
 _lib.bsq_layernorm_quantize.argtypes = [_int, _vp, _vp, _vp, ctypes.c_float, _i64, _i64, _vp, _vp, _vp]
 _lib.bsq_gemm.restype = _int
-_lib.bsq_quantize_dual.argtypes = [_int, _vp, _i64, _i64, ctypes.c_uint64, _vp, _vp, _vp, _vp, _vp]
+_lib.bsq_quantize_dual.argtypes = [_int, _vp, _i64, _i64, ctypes.c_uint64, _vp, _vp, _vp, _vp, _vp, _vp]
 _lib.bsq_quantize_dual.restype = _int
 _lib.bsq_gemm.argtypes = [_int, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp]
 _lib.bsq_gemm_gelu.restype = _int
@@ -136,9 +136,10 @@ def bsq_layernorm_quantize(fmt_flags: int, src: Ptr, gamma: Ptr, beta: Ptr, eps:
 
 
 def bsq_quantize_dual(fmt_flags: int, src: Ptr, rows: int, cols: int, seed: int, row_codes: Ptr, row_scales: Ptr,
-                      col_codes: Ptr, col_scales: Ptr, stream=None) -> int:
+                      col_codes: Ptr, col_scales: Ptr, global_scale: Ptr = None, stream=None) -> int:
     return int(_lib.bsq_quantize_dual(int(fmt_flags), _p(src), rows, cols, int(seed) & (2 ** 64 - 1), _p(row_codes),
-                                      _p(row_scales), _p(col_codes), _p(col_scales), _stream(stream)))
+                                      _p(row_scales), _p(col_codes), _p(col_scales), _p(global_scale),
+                                      _stream(stream)))
 
 
 def bsq_gemm(fmt, A: Ptr, A_scales: Ptr, B: Ptr, B_scales: Ptr, bias: Ptr, out: Ptr, M: int, N: int, K: int,
@@ -261,10 +262,12 @@ def layernorm_quantize(fmt, x: torch.Tensor, gamma: torch.Tensor, beta: torch.Te
     return q
 
 
-def quantize_dual(fmt, x: torch.Tensor, stochastic: bool = False, seed: int = 0, out=None, stream=None):
-    """Both MX operands of a contiguous bf16 / fp32 CUDA matrix X (R x C, multiples of 32) in one
+def quantize_dual(fmt, x: torch.Tensor, stochastic: bool = False, seed: int = 0,
+                  global_scale: Optional[torch.Tensor] = None, out=None, stream=None):
+    """Both operands of a contiguous bf16 / fp32 CUDA matrix X (R x C, multiples of 32) in one
     launch: (row-wise QTensor R x C, column-wise QTensor C x R = X^T quantized along R), with
-    round-to-nearest-even or Philox-keyed stochastic rounding."""
+    round-to-nearest-even or Philox-keyed stochastic rounding. NVFP4 shares one per-tensor
+    scale between the layouts: computed from X, or `global_scale` (a one-element fp32 tensor)."""
     f = _fmt(fmt)
     assert x.is_cuda and x.is_contiguous() and x.dim() == 2, "x must be a contiguous 2-D CUDA tensor"
     if x.dtype not in (torch.float32, torch.bfloat16):
@@ -272,9 +275,16 @@ def quantize_dual(fmt, x: torch.Tensor, stochastic: bool = False, seed: int = 0,
     rows, cols = x.shape
     flags = f | (FLAG_SRC_F32 if x.dtype == torch.float32 else 0) | (FLAG_STOCHASTIC if stochastic else 0)
     qr, qc = out if out is not None else (empty_qtensor(f, rows, cols, x.device), empty_qtensor(f, cols, rows, x.device))
-    rc = bsq_quantize_dual(flags, x, rows, cols, seed, qr.codes, qr.scales, qc.codes, qc.scales, stream)
+    g = qr.global_scale
+    if global_scale is not None:
+        flags |= FLAG_GLOBAL_GIVEN
+        g = global_scale
+    rc = bsq_quantize_dual(flags, x, rows, cols, seed, qr.codes, qr.scales, qc.codes, qc.scales, g, stream)
     if rc != OK:
         raise BsqError(rc, "bsq_quantize_dual")
+    if f == NVFP4:
+        qr.global_scale = g
+        qc.global_scale = g
     return qr, qc
 
 

@@ -157,11 +157,13 @@ int bsq_quantize(int fmt_flags, const void* src, int64_t rows, int64_t cols, voi
 }
 
 int bsq_quantize_dual(int fmt_flags, const void* src, int64_t rows, int64_t cols, uint64_t seed, void* row_codes,
-                      void* row_scales, void* col_codes, void* col_scales, bsq_stream_t stream) {
+                      void* row_scales, void* col_codes, void* col_scales, float* global_scale, bsq_stream_t stream) {
   const int fmt = fmt_flags & BSQ_FMT_MASK;
   const int flags = fmt_flags & ~BSQ_FMT_MASK;
-  if (fmt != BSQ_MXFP8 && fmt != BSQ_MXFP4) return fail(BSQ_ERR_ARG);
-  if (flags & ~(BSQ_FLAG_SRC_F32 | BSQ_FLAG_STOCHASTIC)) return fail(BSQ_ERR_ARG);
+  if (fmt != BSQ_MXFP8 && fmt != BSQ_NVFP4 && fmt != BSQ_MXFP4) return fail(BSQ_ERR_ARG);
+  if (flags & ~(BSQ_FLAG_SRC_F32 | BSQ_FLAG_STOCHASTIC | BSQ_FLAG_GLOBAL_GIVEN)) return fail(BSQ_ERR_ARG);
+  const bool given = (flags & BSQ_FLAG_GLOBAL_GIVEN) != 0;
+  if (given && (fmt != BSQ_NVFP4 || global_scale == nullptr)) return fail(BSQ_ERR_ARG);
   if (src == nullptr || row_codes == nullptr || row_scales == nullptr || col_codes == nullptr ||
       col_scales == nullptr || rows <= 0 || cols <= 0)
     return fail(BSQ_ERR_ARG);
@@ -169,10 +171,13 @@ int bsq_quantize_dual(int fmt_flags, const void* src, int64_t rows, int64_t cols
   if (!aligned16(src) || !aligned16(row_codes) || !aligned16(row_scales) || !aligned16(col_codes) ||
       !aligned16(col_scales))
     return fail(BSQ_ERR_ALIGN);
+  if (fmt == BSQ_NVFP4 && global_scale != nullptr && (reinterpret_cast<uintptr_t>(global_scale) & 3u))
+    return fail(BSQ_ERR_ALIGN);
   const bsq::DeviceInfo* dev = bsq::current_device();
   if (dev == nullptr) return fail(BSQ_ERR_ARCH);
   const int st = bsq::launch_quantize_dual(fmt, (flags & BSQ_FLAG_SRC_F32) != 0, (flags & BSQ_FLAG_STOCHASTIC) != 0,
-                                           seed, src, rows, cols, row_codes, row_scales, col_codes, col_scales,
+                                           given, seed, src, rows, cols, row_codes, row_scales, col_codes, col_scales,
+                                           fmt == BSQ_NVFP4 ? global_scale : nullptr,
                                            reinterpret_cast<cudaStream_t>(stream), *dev);
   return st == BSQ_OK ? BSQ_OK : fail(st);
 }

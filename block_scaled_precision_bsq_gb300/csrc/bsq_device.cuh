@@ -402,6 +402,13 @@ __device__ __forceinline__ void tc_mma_pair<3>(uint32_t d, uint64_t a, uint64_t 
 }
 
 // ---------------------------------------------------------------------------- conversions
+// E4M3 code (sign bit ignored) -> its fp32 value, exact.
+__device__ __forceinline__ float e4m3_to_f32(uint32_t c) {
+  const uint32_t E = (c >> 3) & 15u, m = c & 7u;
+  if (E == 0u) return static_cast<float>(m) * 0.001953125f;  // m * 2^-9, exact
+  return __uint_as_float(((E + 120u) << 23) | (m << 20));
+}
+
 // Two fp32 -> two E4M3 codes (round to nearest even, saturate to +-448); `lo` lands in
 // bits 0..7 of the result, `hi` in bits 8..15.
 __device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {

@@ -71,9 +71,14 @@ struct DualArgs {
   uint8_t* col_scales;
   int64_t tiles_c;  // 128-column tiles
   int64_t ntiles;
-  int64_t nct_row;  // 512-byte scale tiles per 128-row group, row layout: ceil(C / 128)
-  int64_t nct_col;  // same for the column layout (C rows, R / 32 scale columns): ceil(R / 128)
+  int64_t nct_row;  // 512-byte scale tiles per 128-row group, row layout: ceil(C / (4 * block))
+  int64_t nct_col;  // same for the column layout (C rows, R / block scale columns): ceil(R / (4 * block))
   uint32_t seed_lo, seed_hi;
+  // NVFP4: the per-tensor scale g, shared by both layouts; {g, amax} tails after each scale body
+  uint32_t* row_tail;
+  uint32_t* col_tail;
+  const float* g_in;  // given mode (else g = amax / 2688 from row_tail[1], put there beforehand)
+  float* g_out;       // computed mode: receives g (nullable)
   int* status;
 };
 
@@ -155,32 +160,72 @@ __device__ __forceinline__ uint32_t sr_code(float y, float x, uint32_t r) {
   return ((yb >> 31) << kSign) | mag;
 }
 
+// The value a code encodes, x / scale: MX x * (1 / scale) (exact), NVFP4 fp32(x / fp32(s g)).
+template <int FMT>
+__device__ __forceinline__ float scaled(float x, float f) {
+  if constexpr (FMT == BSQ_NVFP4) return __fdiv_rn(x, f);
+  else return x * f;
+}
+
 // Round-to-nearest-even codes of n (a multiple of 4, at most 8 for e2m1) consecutive elements
-// x[0..n) / scale, packed: E4M3 one byte each (element i in byte i % 4 of w[i / 4]), e2m1 one
-// nibble each (element i in bits 4i of w[0]).
+// x[0..n) with the block factor f, packed: E4M3 one byte each (element i in byte i % 4 of
+// w[i / 4]), e2m1 one nibble each (element i in bits 4i of w[0]).
 template <int FMT, int N>
-__device__ __forceinline__ void rne_codes(const float* x, float mul, uint32_t* w) {
+__device__ __forceinline__ void rne_codes(const float* x, float f, uint32_t* w) {
   if constexpr (FMT == BSQ_MXFP8) {
 #pragma unroll
     for (int j = 0; j < N / 4; ++j)
-      w[j] = cvt_e4m3x4(x[4 * j] * mul, x[4 * j + 1] * mul, x[4 * j + 2] * mul, x[4 * j + 3] * mul);
+      w[j] = cvt_e4m3x4(x[4 * j] * f, x[4 * j + 1] * f, x[4 * j + 2] * f, x[4 * j + 3] * f);
   } else if constexpr (N == 8) {
     float y[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) y[i] = x[i] * mul;
+    for (int i = 0; i < 8; ++i) y[i] = scaled<FMT>(x[i], f);
     w[0] = cvt_e2m1x8(y);
   } else {
-    w[0] = cvt_e2m1x2(x[0] * mul, x[1] * mul) | (cvt_e2m1x2(x[2] * mul, x[3] * mul) << 8);
+    w[0] = cvt_e2m1x2(scaled<FMT>(x[0], f), scaled<FMT>(x[1], f)) |
+           (cvt_e2m1x2(scaled<FMT>(x[2], f), scaled<FMT>(x[3], f)) << 8);
   }
 }
 
-// Stochastic codes of the four elements x[0..4) / scale with the random words q (element i takes
-// word i), packed as rne_codes packs four: E4M3 one word, e2m1 the low 16 bits.
+// Stochastic codes of the four elements x[0..4) with the block factor f and the random words q
+// (element i takes word i), packed as rne_codes packs four: E4M3 one word, e2m1 the low 16 bits.
+// MX passes x for sr_code's underflow test (the MX value x / scale is exact unless it leaves
+// fp32's range); NVFP4 rounds the fp32 quotient itself, so the quotient stands in for x.
 template <int FMT>
-__device__ __forceinline__ uint32_t sr_codes4(const float* x, float mul, uint4 q) {
+__device__ __forceinline__ uint32_t sr_codes4(const float* x, float f, uint4 q) {
   constexpr int kBits = (FMT == BSQ_MXFP8) ? 8 : 4;
-  return sr_code<FMT>(x[0] * mul, x[0], q.x) | (sr_code<FMT>(x[1] * mul, x[1], q.y) << kBits) |
-         (sr_code<FMT>(x[2] * mul, x[2], q.z) << (2 * kBits)) | (sr_code<FMT>(x[3] * mul, x[3], q.w) << (3 * kBits));
+  const uint32_t qq[4] = {q.x, q.y, q.z, q.w};
+  uint32_t w = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float y = scaled<FMT>(x[i], f);
+    w |= sr_code<FMT>(y, FMT == BSQ_NVFP4 ? y : x[i], qq[i]) << (kBits * i);
+  }
+  return w;
+}
+
+// Codes of a zero NVFP4 block scale: zeros carrying the sign of each element (n <= 8).
+template <int N>
+__device__ __forceinline__ uint32_t sign_codes(const float* x) {
+  uint32_t w = 0;
+#pragma unroll
+  for (int i = 0; i < N; ++i) w |= (__float_as_uint(x[i]) >> 31) << (4 * i + 3);
+  return w;
+}
+
+// Block scale from the block maximum: MX the UE8M0 byte and 1 / scale; NVFP4 the E4M3 code of
+// fp32(amax / fp32(6 g)) and fp32(s g) (0 when s is 0: the block's codes are signed zeros).
+template <int FMT>
+__device__ __forceinline__ uint32_t block_scale(float amax, float g, float six_g, float& f) {
+  if constexpr (FMT == BSQ_NVFP4) {
+    const uint32_t sc = g != 0.0f ? (cvt_e4m3x2(__fdiv_rn(amax, six_g), 0.0f) & 0xFFu) : 0u;
+    f = __fmul_rn(e4m3_to_f32(sc), g);
+    return sc;
+  } else {
+    const uint32_t sb = mx_scale_byte<FMT>(amax);
+    f = mx_inv_scale(sb);
+    return sb;
+  }
 }
 
 // Named barriers of the consumer warps (ids 1 and 2; 0 is __syncthreads).
@@ -211,15 +256,18 @@ template <int FMT, bool F32, bool SR>
 __global__ void __launch_bounds__(kDThreads, kDCtasPerSm)
     dual_kernel(const __grid_constant__ CUtensorMap src_map, const __grid_constant__ CUtensorMap col_map,
                 const DualArgs a) {
+  constexpr bool kNv = (FMT == BSQ_NVFP4);
+  constexpr bool kFp8 = (FMT == BSQ_MXFP8);
+  constexpr int BS = kNv ? 16 : 32;                        // block size
   constexpr int kEsize = F32 ? 4 : 2;
   constexpr int kRows = kDTileBytes / (kDCols * kEsize);  // 128 bf16, 64 fp32
   constexpr int V = 16 / kEsize;                           // elements of a 16-byte piece
-  constexpr int LB = 32 / V;                               // lanes of a 32-element block
+  constexpr int LB = BS / V;                               // lanes of a block in the row pass
   constexpr int kRowSteps = kDTileBytes / 16 / 32 / kDConsumerWarps;  // row-pass steps per warp
-  constexpr int kColBlocks = kRows / 32 / 2;  // column-pass 32-row blocks per thread (2 bf16, 1 fp32)
-  constexpr bool kFp8 = (FMT == BSQ_MXFP8);
-  constexpr int kBlockCodeBytes = kFp8 ? 32 : 16;        // codes of a 32-element block
-  constexpr int S = kRows * kBlockCodeBytes / 32;        // staging row: the tile's rows of one column
+  constexpr int kColUnits = kRows / 32 / 2;  // column-pass 32-row units per thread (2 bf16, 1 fp32)
+  constexpr int kUnitScales = 32 / BS;       // scale bytes of a 32-row unit
+  constexpr int kUnitCodeBytes = kFp8 ? 32 : 16;           // codes of a 32-element unit
+  constexpr int S = kRows * kUnitCodeBytes / 32;           // staging row: the tile's rows of one column
   extern __shared__ __align__(1024) uint8_t d_smem[];
   uint8_t* staging = d_smem;
   uint8_t* ring = d_smem + kDRingOff;
@@ -273,6 +321,21 @@ __global__ void __launch_bounds__(kDThreads, kDCtasPerSm)
   const bool issuer = ct == 0;                         // issues the staging tile's TMA stores
   if (issuer) prefetch_tmap(&col_map);
   const int64_t R = a.rows, C = a.cols;
+  // NVFP4 per-tensor scale (both layouts): given, or amax / 2688 with amax in the row tail
+  float g = 0.0f, six_g = 0.0f;
+  if constexpr (kNv) {
+    g = a.g_in != nullptr ? *a.g_in : __fdiv_rn(__uint_as_float(a.row_tail[1]), 2688.0f);
+    six_g = __fmul_rn(6.0f, g);
+    if (blockIdx.x == 0 && ct == 0) {
+      a.row_tail[0] = __float_as_uint(g);
+      a.col_tail[0] = __float_as_uint(g);
+      if (a.g_in == nullptr) {
+        a.col_tail[1] = a.row_tail[1];
+        if (a.g_out != nullptr) *a.g_out = g;
+      }
+    }
+  }
+  uint32_t run_max = 0;  // NVFP4 given mode: this thread's largest |x| (fp32 bits) for the tails
   bool stored = false;
   int stage = 0;
   uint32_t phase = 0;
@@ -307,24 +370,27 @@ __global__ void __launch_bounds__(kDThreads, kDCtasPerSm)
         float amax = 0.0f;
 #pragma unroll
         for (int i = 0; i < V; ++i) amax = fmaxf(amax, fabsf(x[i]));
+        if constexpr (kNv) run_max = max(run_max, __float_as_uint(amax));
 #pragma unroll
         for (int o = 1; o < LB; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
-        const uint32_t sbyte = mx_scale_byte<FMT>(amax);
-        const float mul = mx_inv_scale(sbyte);
+        float bf;
+        const uint32_t sbyte = block_scale<FMT>(amax, g, six_g, bf);
         const int64_t r = r0 + rr, c = c0 + cc;
         uint32_t w[kFp8 ? V / 4 : 1];
-        if constexpr (SR) {
+        if (kNv && bf == 0.0f) {
+          w[0] = sign_codes<V>(x);
+        } else if constexpr (SR) {
           const uint64_t g0 = (static_cast<uint64_t>(r) * static_cast<uint64_t>(C) + static_cast<uint64_t>(c)) >> 2;
           if constexpr (kFp8) {
 #pragma unroll
-            for (int gq = 0; gq < V / 4; ++gq) w[gq] = sr_codes4<FMT>(x + 4 * gq, mul, sr_words(g0 + gq, 0u, a));
+            for (int gq = 0; gq < V / 4; ++gq) w[gq] = sr_codes4<FMT>(x + 4 * gq, bf, sr_words(g0 + gq, 0u, a));
           } else {
             w[0] = 0;
 #pragma unroll
-            for (int gq = 0; gq < V / 4; ++gq) w[0] |= sr_codes4<FMT>(x + 4 * gq, mul, sr_words(g0 + gq, 0u, a)) << (16 * gq);
+            for (int gq = 0; gq < V / 4; ++gq) w[0] |= sr_codes4<FMT>(x + 4 * gq, bf, sr_words(g0 + gq, 0u, a)) << (16 * gq);
           }
         } else {
-          rne_codes<FMT, V>(x, mul, w);
+          rne_codes<FMT, V>(x, bf, w);
         }
         if (r < R && c < C) {
           const int64_t idx = r * C + c;
@@ -336,12 +402,13 @@ __global__ void __launch_bounds__(kDThreads, kDCtasPerSm)
             else *reinterpret_cast<uint16_t*>(a.row_codes + idx / 2) = static_cast<uint16_t>(w[0]);
           }
         }
-        // the row's four scale bytes -> one word (block b of the row in byte b)
-        uint32_t sw = sbyte << (8 * (cc / 32));
+        // four consecutive block scales of the row -> one word (block b of the group in byte b)
+        uint32_t sw = sbyte << (8 * ((cc / BS) & 3));
         sw |= __shfl_xor_sync(0xFFFFFFFFu, sw, LB);
         sw |= __shfl_xor_sync(0xFFFFFFFFu, sw, 2 * LB);
-        if ((lane & (4 * LB - 1)) == 0) {
-          const int64_t off = ((r >> 7) * a.nct_row + tj) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4;
+        const int64_t grp = c / (4 * BS);  // 4-scale-column group of the row layout
+        if ((lane & (4 * LB - 1)) == 0 && grp < a.nct_row) {
+          const int64_t off = ((r >> 7) * a.nct_row + grp) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4;
           *reinterpret_cast<uint32_t*>(a.row_scales + off) = sw;
         }
       }
@@ -351,15 +418,15 @@ __global__ void __launch_bounds__(kDThreads, kDCtasPerSm)
     if (issuer && stored) bulk_wait_group_read<0>();
     if (!consumers_and_sync(ok)) break;
 
-    // ---- column pass: one column, kColBlocks blocks of 32 rows per thread
+    // ---- column pass: one column, kColUnits units of 32 rows per thread
     {
       const int cc = ct & (kDCols - 1);
-      const int g = ct >> 7;
+      const int gh = ct >> 7;
       const int64_t c = c0 + cc;
       uint32_t sbytes = 0;
 #pragma unroll 1
-      for (int bb = 0; bb < kColBlocks; ++bb) {
-        const int rb = (g * kColBlocks + bb) * 32;
+      for (int bb = 0; bb < kColUnits; ++bb) {
+        const int rb = (gh * kColUnits + bb) * 32;
         float x[32];
 #pragma unroll
         for (int k = 0; k < 32; ++k) {
@@ -370,41 +437,57 @@ __global__ void __launch_bounds__(kDThreads, kDCtasPerSm)
                 static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(tile + ((rb + k) * kDCols + cc) * 2)) << 16);
           }
         }
-        float m[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          m[i] = fmaxf(fmaxf(fabsf(x[4 * i]), fabsf(x[4 * i + 1])), fmaxf(fabsf(x[4 * i + 2]), fabsf(x[4 * i + 3])));
-#pragma unroll
-        for (int i = 0; i < 4; ++i) m[i] = fmaxf(m[i], m[i + 4]);
-        const float amax = fmaxf(fmaxf(0.0f, fmaxf(m[0], m[1])), fmaxf(m[2], m[3]));
-        const uint32_t sbyte = mx_scale_byte<FMT>(amax);
-        sbytes |= sbyte << (8 * bb);
-        const float mul = mx_inv_scale(sbyte);
         uint32_t w[kFp8 ? 8 : 4];
-        if constexpr (SR) {
-          const uint64_t g0 = (static_cast<uint64_t>(c) * static_cast<uint64_t>(R) + static_cast<uint64_t>(r0 + rb)) >> 2;
+        const uint64_t g0 = (static_cast<uint64_t>(c) * static_cast<uint64_t>(R) + static_cast<uint64_t>(r0 + rb)) >> 2;
 #pragma unroll
-          for (int gq = 0; gq < 8; ++gq) {
-            const uint32_t v4 = sr_codes4<FMT>(x + 4 * gq, mul, sr_words(g0 + gq, 1u, a));
-            if constexpr (kFp8) w[gq] = v4;
-            else if (gq & 1) w[gq >> 1] |= v4 << 16;
-            else w[gq >> 1] = v4;
+        for (int h = 0; h < kUnitScales; ++h) {  // the unit's blocks: 1 (MX) or 2 (NVFP4) of BS rows
+          const float* xb = x + h * BS;
+          float m[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            m[i] = 0.0f;
+#pragma unroll
+            for (int k = i; k < BS; k += 4) m[i] = fmaxf(m[i], fabsf(xb[k]));
           }
-        } else {
+          const float amax = fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
+          float bf;
+          const uint32_t sbyte = block_scale<FMT>(amax, g, six_g, bf);
+          sbytes |= sbyte << (8 * (bb * kUnitScales + h));
+          constexpr int kWords = BS * (kFp8 ? 8 : 4) / 32;  // code words of one block
+          uint32_t* wb = w + h * kWords;
+          if (kNv && bf == 0.0f) {
+            wb[0] = sign_codes<8>(xb);
+            wb[1] = sign_codes<8>(xb + 8);
+          } else if constexpr (SR) {
 #pragma unroll
-          for (int j = 0; j < (kFp8 ? 8 : 4); ++j) rne_codes<FMT, kFp8 ? 4 : 8>(x + (kFp8 ? 4 : 8) * j, mul, w + j);
+            for (int gq = 0; gq < BS / 4; ++gq) {
+              const uint32_t v4 = sr_codes4<FMT>(xb + 4 * gq, bf, sr_words(g0 + h * (BS / 4) + gq, 1u, a));
+              if constexpr (kFp8) wb[gq] = v4;
+              else if (gq & 1) wb[gq >> 1] |= v4 << 16;
+              else wb[gq >> 1] = v4;
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < kWords; ++j) rne_codes<FMT, kFp8 ? 4 : 8>(xb + (kFp8 ? 4 : 8) * j, bf, wb + j);
+          }
         }
-        // codes -> staging row cc, bytes [rb * kBlockCodeBytes / 32, + kBlockCodeBytes)
-        const uint32_t b0 = static_cast<uint32_t>(rb * kBlockCodeBytes / 32);
+        // codes -> staging row cc, bytes [rb * kUnitCodeBytes / 32, + kUnitCodeBytes)
+        const uint32_t b0 = static_cast<uint32_t>(rb * kUnitCodeBytes / 32);
         *reinterpret_cast<uint4*>(staging + staging_offset<S>(cc, b0)) = make_uint4(w[0], w[1], w[2], w[3]);
         if constexpr (kFp8)
           *reinterpret_cast<uint4*>(staging + staging_offset<S>(cc, b0 + 16)) = make_uint4(w[4], w[5], w[6], w[7]);
       }
-      // scale bytes of column c: row c of the column layout, scale columns (r0 % 128) / 32 + ..
-      const int64_t off = (tj * a.nct_col + (r0 >> 7)) * 512 + (cc & 31) * 16 + ((cc >> 5) & 3) * 4 +
-                          ((r0 & 127) >> 5) + g * kColBlocks;
-      if constexpr (kColBlocks == 2) *reinterpret_cast<uint16_t*>(a.col_scales + off) = static_cast<uint16_t>(sbytes);
-      else a.col_scales[off] = static_cast<uint8_t>(sbytes);
+      // scale bytes of column c: row c of the column layout, scale columns from rt / BS on
+      const int64_t rt = r0 + gh * kColUnits * 32;
+      const int64_t grp = rt / (4 * BS);
+      constexpr int kBytes = kColUnits * kUnitScales;  // 1, 2 or 4, never crossing a word
+      if (grp < a.nct_col) {
+        const int64_t off =
+            (tj * a.nct_col + grp) * 512 + (cc & 31) * 16 + ((cc >> 5) & 3) * 4 + (rt / BS) % 4;
+        if constexpr (kBytes == 4) *reinterpret_cast<uint32_t*>(a.col_scales + off) = sbytes;
+        else if constexpr (kBytes == 2) *reinterpret_cast<uint16_t*>(a.col_scales + off) = static_cast<uint16_t>(sbytes);
+        else a.col_scales[off] = static_cast<uint8_t>(sbytes);
+      }
     }
 
     // every read of the tile is done: release it to the producer
@@ -415,13 +498,23 @@ __global__ void __launch_bounds__(kDThreads, kDCtasPerSm)
     fence_proxy_async_smem();
     consumers_sync();
     if (issuer && r0 < R) {
-      tma_store_2d(&col_map, staging, static_cast<int32_t>(r0 * kBlockCodeBytes / 32), static_cast<int32_t>(c0));
+      tma_store_2d(&col_map, staging, static_cast<int32_t>(r0 * kUnitCodeBytes / 32), static_cast<int32_t>(c0));
       bulk_commit_group();
       stored = true;
     }
     if (++stage == kDStages) {
       stage = 0;
       phase ^= 1u;
+    }
+  }
+  if constexpr (kNv) {
+    if (a.g_in != nullptr) {  // given mode: this tensor's amax into both tails
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) run_max = max(run_max, __shfl_xor_sync(0xFFFFFFFFu, run_max, o));
+      if (lane == 0 && run_max != 0) {
+        atomicMax(&a.row_tail[1], run_max);
+        atomicMax(&a.col_tail[1], run_max);
+      }
     }
   }
   if (issuer && stored) bulk_wait_group0();  // the last stores have completed
@@ -459,11 +552,12 @@ cudaError_t launch_d_fmt(bool f32, bool sr, const CUtensorMap& src_map, const CU
 
 }  // namespace
 
-int launch_quantize_dual(int fmt, bool src_f32, bool stochastic, uint64_t seed, const void* src, int64_t rows,
-                         int64_t cols, void* row_codes, void* row_scales, void* col_codes, void* col_scales,
-                         cudaStream_t stream, const DeviceInfo& dev) {
+int launch_quantize_dual(int fmt, bool src_f32, bool stochastic, bool global_given, uint64_t seed, const void* src,
+                         int64_t rows, int64_t cols, void* row_codes, void* row_scales, void* col_codes,
+                         void* col_scales, float* global_scale, cudaStream_t stream, const DeviceInfo& dev) {
   const int64_t esize = src_f32 ? 4 : 2;
   const int64_t tile_rows = kDTileBytes / (kDCols * esize);
+  const int64_t bs = block_size(fmt);
   DualArgs a{};
   a.rows = rows;
   a.cols = cols;
@@ -474,17 +568,27 @@ int launch_quantize_dual(int fmt, bool src_f32, bool stochastic, uint64_t seed, 
   a.tiles_c = ceil_div(cols, kDCols);
   // row tiles cover the rows padded to 128, so that every scale byte of both layouts is written
   a.ntiles = (ceil_div(rows, 128) * 128 / tile_rows) * a.tiles_c;
-  a.nct_row = ceil_div(cols, 128);
-  a.nct_col = ceil_div(rows, 128);
+  a.nct_row = ceil_div(cols, 4 * bs);
+  a.nct_col = ceil_div(rows, 4 * bs);
   a.seed_lo = static_cast<uint32_t>(seed);
   a.seed_hi = static_cast<uint32_t>(seed >> 32);
   a.status = dev.status;
+  if (fmt == BSQ_NVFP4) {
+    a.row_tail = reinterpret_cast<uint32_t*>(a.row_scales + scales_body_bytes(fmt, rows, cols));
+    a.col_tail = reinterpret_cast<uint32_t*>(a.col_scales + scales_body_bytes(fmt, cols, rows));
+    a.g_in = global_given ? global_scale : nullptr;
+    a.g_out = global_given ? nullptr : global_scale;
+    if (cudaMemsetAsync(a.row_tail, 0, 16, stream) != cudaSuccess) return BSQ_ERR_LAUNCH;
+    if (cudaMemsetAsync(a.col_tail, 0, 16, stream) != cudaSuccess) return BSQ_ERR_LAUNCH;
+    if (!global_given && launch_amax(src, src_f32, rows * cols, a.row_tail + 1, stream, dev) != BSQ_OK)
+      return BSQ_ERR_LAUNCH;
+  }
   CUtensorMap map, col_map;
   if (!make_map_2d(&map, src_f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, src,
                    static_cast<uint64_t>(cols), static_cast<uint64_t>(rows), static_cast<uint64_t>(cols * esize), kDCols,
                    static_cast<uint32_t>(tile_rows), CU_TENSOR_MAP_SWIZZLE_NONE))
     return BSQ_ERR_LAUNCH;
-  // the column-layout codes as `cols` rows of R code bytes (MXFP8) or R / 2 (MXFP4); a box is
+  // the column-layout codes as `cols` rows of R code bytes (MXFP8) or R / 2 (4-bit); a box is
   // one tile's staging: 128 rows of tile_rows codes
   const int64_t code_row = fmt == BSQ_MXFP8 ? rows : rows / 2;
   const uint32_t box_inner = static_cast<uint32_t>(fmt == BSQ_MXFP8 ? tile_rows : tile_rows / 2);
@@ -495,9 +599,10 @@ int launch_quantize_dual(int fmt, bool src_f32, bool stochastic, uint64_t seed, 
                    static_cast<uint64_t>(cols), static_cast<uint64_t>(code_row), box_inner, kDCols, sw))
     return BSQ_ERR_LAUNCH;
   const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(a.ntiles, kDCtasPerSm * dev.num_sms)));
-  const cudaError_t err = fmt == BSQ_MXFP8
-                              ? launch_d_fmt<BSQ_MXFP8>(src_f32, stochastic, map, col_map, a, grid, stream)
-                              : launch_d_fmt<BSQ_MXFP4>(src_f32, stochastic, map, col_map, a, grid, stream);
+  cudaError_t err;
+  if (fmt == BSQ_MXFP8) err = launch_d_fmt<BSQ_MXFP8>(src_f32, stochastic, map, col_map, a, grid, stream);
+  else if (fmt == BSQ_MXFP4) err = launch_d_fmt<BSQ_MXFP4>(src_f32, stochastic, map, col_map, a, grid, stream);
+  else err = launch_d_fmt<BSQ_NVFP4>(src_f32, stochastic, map, col_map, a, grid, stream);
   return err == cudaSuccess ? BSQ_OK : BSQ_ERR_LAUNCH;
 }
 

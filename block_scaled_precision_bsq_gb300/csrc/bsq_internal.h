@@ -47,16 +47,22 @@ using QuantItem = bsq_quant_item;
 int launch_quantize_batch(int fmt, bool src_f32, bool global_given, int count, const QuantItem* items,
                           cudaStream_t stream, const DeviceInfo& dev);
 
+// Largest |x| of `elems` bf16 / fp32 values (elems * size a multiple of 16 bytes), atomically
+// max-ed into *out as fp32 bits (out must hold 0 or an earlier maximum).
+int launch_amax(const void* src, bool src_f32, int64_t elems, uint32_t* out, cudaStream_t stream,
+                const DeviceInfo& dev);
+
 // Row LayerNorm then MX quantization of one matrix (fmt MXFP8 / MXFP4); rows must fit a chunk
 // (BSQ_ERR_SHAPE otherwise).
 int launch_layernorm_quantize(int fmt, bool src_f32, const QuantItem& item, const uint16_t* gamma,
                               const uint16_t* beta, float eps, cudaStream_t stream, const DeviceInfo& dev);
 
-// Dual-layout MX quantization (fmt MXFP8 / MXFP4) of one rows x cols matrix, arguments
-// validated (rows, cols multiples of 32).
-int launch_quantize_dual(int fmt, bool src_f32, bool stochastic, uint64_t seed, const void* src, int64_t rows,
-                         int64_t cols, void* row_codes, void* row_scales, void* col_codes, void* col_scales,
-                         cudaStream_t stream, const DeviceInfo& dev);
+// Dual-layout quantization (MXFP8 / MXFP4 / NVFP4) of one rows x cols matrix, arguments
+// validated (rows, cols multiples of 32). NVFP4: global_scale as bsq_quantize's (given mode
+// when global_given).
+int launch_quantize_dual(int fmt, bool src_f32, bool stochastic, bool global_given, uint64_t seed, const void* src,
+                         int64_t rows, int64_t cols, void* row_codes, void* row_scales, void* col_codes,
+                         void* col_scales, float* global_scale, cudaStream_t stream, const DeviceInfo& dev);
 
 // epi: 0 bf16 out, 1 GELU -> bf16, 2 GELU -> MXFP8 codes + scales, 3 GELU -> MXFP4 (out_scales
 // used by 2 and 3 only).

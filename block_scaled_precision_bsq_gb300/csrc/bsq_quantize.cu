@@ -84,12 +84,6 @@ struct Loaded {
   uint4 v[F32 ? 4 : 2];  // 16 elements
 };
 
-__device__ __forceinline__ float e4m3_to_f32(uint32_t c) {
-  const uint32_t E = (c >> 3) & 15u, m = c & 7u;
-  if (E == 0u) return static_cast<float>(m) * 0.001953125f;  // m * 2^-9, exact
-  return __uint_as_float(((E + 120u) << 23) | (m << 20));
-}
-
 // 16 source elements of one lane -> fp32 values and their largest magnitude. The maximum
 // starts at 0 and skips NaN (fmaxf returns the other operand), as a block maximum taken with
 // "if (|x| > amax) amax = |x|" does.
@@ -496,6 +490,15 @@ cudaError_t launch_q(const QuantBatch& b, int grid, cudaStream_t stream) {
 
 }  // namespace
 
+int launch_amax(const void* src, bool src_f32, int64_t elems, uint32_t* out, cudaStream_t stream,
+                const DeviceInfo& dev) {
+  const int64_t nvec = elems * (src_f32 ? 4 : 2) / 16;
+  const int agrid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(ceil_div(nvec, kAmaxThreads * 4), dev.num_sms * 8)));
+  if (src_f32) amax_kernel<true><<<agrid, kAmaxThreads, 0, stream>>>(static_cast<const uint4*>(src), nvec, out);
+  else amax_kernel<false><<<agrid, kAmaxThreads, 0, stream>>>(static_cast<const uint4*>(src), nvec, out);
+  return cudaGetLastError() == cudaSuccess ? BSQ_OK : BSQ_ERR_LAUNCH;
+}
+
 // The batch's chunking (chunk size, per-matrix chunk counts) and per-matrix arguments.
 void build_batch(QuantBatch& b, int fmt, bool src_f32, int count, const QuantItem* items, const DeviceInfo& dev) {
   const int64_t esize = src_f32 ? 4 : 2;
@@ -553,13 +556,8 @@ int launch_quantize_batch(int fmt, bool src_f32, bool global_given, int count, c
     for (int i = 0; i < count; ++i) {
       const QuantArgs& a = b.t[i];
       if (cudaMemsetAsync(a.tail, 0, 16, stream) != cudaSuccess) return BSQ_ERR_LAUNCH;
-      if (!global_given) {
-        const int64_t nvec = a.rows * a.cols * esize / 16;
-        const int agrid = static_cast<int>(std::min<int64_t>(ceil_div(nvec, kAmaxThreads * 4), dev.num_sms * 8));
-        if (src_f32) amax_kernel<true><<<agrid, kAmaxThreads, 0, stream>>>(reinterpret_cast<const uint4*>(a.src), nvec, a.tail + 1);
-        else amax_kernel<false><<<agrid, kAmaxThreads, 0, stream>>>(reinterpret_cast<const uint4*>(a.src), nvec, a.tail + 1);
-        if (cudaGetLastError() != cudaSuccess) return BSQ_ERR_LAUNCH;
-      }
+      if (!global_given && launch_amax(a.src, src_f32, a.rows * a.cols, a.tail + 1, stream, dev) != BSQ_OK)
+        return BSQ_ERR_LAUNCH;
     }
     if (!global_given) {
       err = src_f32 ? launch_q<BSQ_NVFP4, true, kNvComputed>(b, grid, stream)

@@ -144,34 +144,41 @@ typedef struct {
 int bsq_quantize_batch(int fmt_flags, int count, const bsq_quant_item* items, bsq_stream_t stream);
 
 /*
- * bsq_quantize_dual: dual-layout MX quantization for the backward GEMMs ("lightly-train -
- * DINOv3 + EoMT on RTX 5090" README, section 4.3, the quantized training stack): dgrad
- * contracts dY over N and wgrad over M, so dY is needed quantized along both of its dimensions
- * (and W along N, X along M). From one rows x cols matrix X, in one pass over it:
+ * bsq_quantize_dual: dual-layout quantization for the backward GEMMs ("lightly-train - DINOv3 +
+ * EoMT on RTX 5090" README, section 4.3, the quantized training stacks: dgrad contracts dY
+ * over N and wgrad over M, so dY is needed quantized along both of its dimensions, W along N
+ * and X along M; the README's fused FP4 quantizer writes both layouts from one read). From one
+ * rows x cols matrix X, in one pass over it:
  *   row_codes, row_scales  the operand bsq_quantize(fmt, X, rows, cols) writes (blocks along
  *                          cols), sized bsq_codes_bytes / bsq_scales_bytes(fmt, rows, cols);
  *   col_codes, col_scales  the operand of X^T (cols x rows, blocks along rows), as
  *                          bsq_quantize(fmt, X^T, cols, rows) would write it, sized
  *                          bsq_codes_bytes / bsq_scales_bytes(fmt, cols, rows).
  * All four are written, scale padding included.
- *   fmt_flags  BSQ_MXFP8 or BSQ_MXFP4, | BSQ_FLAG_SRC_F32 (fp32 source, default bf16),
- *              | BSQ_FLAG_STOCHASTIC.
- * Block scales follow the MX rule of bsq_quantize. Without BSQ_FLAG_STOCHASTIC the elements
+ *   fmt_flags     BSQ_MXFP8, BSQ_MXFP4 or BSQ_NVFP4, | BSQ_FLAG_SRC_F32 (fp32 source, default
+ *                 bf16), | BSQ_FLAG_STOCHASTIC, | BSQ_FLAG_GLOBAL_GIVEN (NVFP4 only).
+ *   global_scale  NVFP4: one fp32 in device memory, as bsq_quantize's argument (receives the
+ *                 computed g, may be NULL; or, with BSQ_FLAG_GLOBAL_GIVEN, supplies g). The one
+ *                 g serves both layouts; both scale tails hold {g, amax of X}. Ignored for MX.
+ * Block scales follow the rules of bsq_quantize. Without BSQ_FLAG_STOCHASTIC the elements
  * round to nearest even (seed ignored); both layouts are then byte-identical to the two
- * bsq_quantize calls. With it (the gradient rounding of quantized training), for v = x / scale:
+ * bsq_quantize calls (NVFP4 with the same g). With it (the gradient rounding of quantized
+ * training), for v = the element's quotient (MX: x / scale, exact; NVFP4: fp32(x / fp32(s g))):
  * q = |v| / spacing, the spacing of the element format at |v|'s binade (its subnormal step
  * below the smallest normal); |code| = floor(q) + (frac(q) > u), saturating at the largest
  * finite value (448, 6); u = (r >> 8) * 2^-24 with r word (i mod 4) of Philox4x32-10 (Salmon
  * et al., "Parallel Random Numbers: As Easy as 1, 2, 3", SC'11) at counter {floor(i/4) low 32
  * bits, high 32 bits, layout, 0} and key {seed low 32 bits, high 32 bits}; i = r * cols + c in
  * the row layout (layout 0), c * rows + r in the column layout (layout 1). E[code value] = v
- * below saturation, and the codes are a function of (X, seed) alone.
+ * below saturation, and the codes are a function of (X, seed) alone. An NVFP4 block whose
+ * scale is 0 gives signed zero codes either way.
  * Shapes: rows % 32 == 0 and cols % 32 == 0, both below 2^31, else BSQ_ERR_SHAPE.
- * Errors: BSQ_ERR_ARG for another format or flag, a NULL buffer or a non-positive size;
- * BSQ_ERR_ALIGN for a pointer not 16-byte aligned.
+ * Errors: BSQ_ERR_ARG for an unknown format or flag, BSQ_FLAG_GLOBAL_GIVEN without NVFP4 or
+ * without global_scale, a NULL buffer or a non-positive size; BSQ_ERR_ALIGN for a buffer not
+ * 16-byte aligned or a global_scale not 4-byte aligned.
  */
 int bsq_quantize_dual(int fmt_flags, const void* src, int64_t rows, int64_t cols, uint64_t seed, void* row_codes,
-                      void* row_scales, void* col_codes, void* col_scales, bsq_stream_t stream);
+                      void* row_scales, void* col_codes, void* col_scales, float* global_scale, bsq_stream_t stream);
 
 /*
  * bsq_gemm: out[m, n] = bf16_rn(alpha * sum_k Ahat[m,k] * Bhat[n,k] + bias[n]).

@@ -91,6 +91,8 @@ def lib() -> ctypes.CDLL:
         L.orc_quantize_nv_dual.restype = ctypes.c_int
         L.orc_quantize_nv_dual.argtypes = [vp, ctypes.c_int, i64, i64, ctypes.c_int, ctypes.c_float, ctypes.c_int,
                                            ctypes.c_uint64, u8p, u8p, u8p, u8p, vp, vp]
+        L.orc_delayed_global_scale.restype = ctypes.c_float
+        L.orc_delayed_global_scale.argtypes = [ctypes.c_float, ctypes.c_float]
         L.orc_set_num_threads.argtypes = [ctypes.c_int]
         _lib = L
     return _lib
@@ -355,3 +357,8 @@ def quantize_dual(fmt, x: np.ndarray, stochastic: bool = False, seed: int = 0,
     if st:
         raise ValueError("oracle dual quantize failed: %d" % st)
     return Quantized(f, R, C, rc, rs), Quantized(f, C, R, cc, cs)
+
+
+def delayed_global_scale(amax_prev: float, headroom: float) -> float:
+    """Delayed per-tensor NVFP4 scale (reading R12): fp32(fp32(amax_prev * headroom) / 2688)."""
+    return float(lib().orc_delayed_global_scale(float(amax_prev), float(headroom)))

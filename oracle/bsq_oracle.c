@@ -65,6 +65,10 @@
  *       each layout applies R3 along its rows (1x16 blocks). With stochastic rounding the
  *       element y = fp32(x / fp32(s g)) of R3 rounds by the rule of R10 (e2m1, the same Philox
  *       words and element indices); s = 0 still gives signed zero codes.
+ *   R12 Delayed per-tensor scale ([LT] section 5.5: the amax found while quantizing a tensor
+ *       in one step, times a headroom factor H, gives the next step's scale without an extra
+ *       pass; H = 32 for dY): g_next = fp32(fp32(amax_prev * H) / 2688), amax_prev the amax
+ *       recorded by the previous NVFP4 quantization of the tensor.
  *
  * Pins (tests that tie this code to something other than itself) are in the test suite:
  * exhaustive decode tables against two independent float8/float4 libraries, encoders
@@ -746,4 +750,10 @@ int orc_quantize_nv_dual(const void* src, int src_f32, int64_t R, int64_t C, int
     if (g_out) *g_out = g;
     if (amax_out) *amax_out = amax;
     return ORC_OK;
+}
+
+/* Delayed per-tensor NVFP4 scale (reading R12): two fp32 operations. */
+float orc_delayed_global_scale(float amax_prev, float headroom) {
+    float a = amax_prev * headroom; /* fp32 multiplication */
+    return a / 2688.0f;             /* fp32 division */
 }

@@ -95,8 +95,10 @@ def test_argument_errors_before_any_cuda_call(bsq):
     assert bsq.bsq_gemm(bsq.MXFP8, p, p, p, p, p + 1, p, 128, 256, 256) == bsq.ERR_ALIGN
     assert bsq.bsq_selftest_timeout(10, None) == bsq.ERR_ARG
     dq = bsq.bsq_quantize_dual
-    assert dq(bsq.NVFP4, p, 64, 64, 0, p, p, p, p) == bsq.ERR_ARG                  # MX formats only
-    assert dq(bsq.MXFP8 | bsq.FLAG_GLOBAL_GIVEN, p, 64, 64, 0, p, p, p, p) == bsq.ERR_ARG  # flag
+    assert dq(7, p, 64, 64, 0, p, p, p, p) == bsq.ERR_ARG                          # format
+    assert dq(bsq.MXFP8 | bsq.FLAG_GLOBAL_GIVEN, p, 64, 64, 0, p, p, p, p, p) == bsq.ERR_ARG  # MX given g
+    assert dq(bsq.NVFP4 | bsq.FLAG_GLOBAL_GIVEN, p, 64, 64, 0, p, p, p, p, None) == bsq.ERR_ARG  # no g
+    assert dq(bsq.NVFP4, p, 64, 64, 0, p, p, p, p, p + 2) == bsq.ERR_ALIGN          # g alignment
     assert dq(bsq.MXFP8, p, 64, 64, 0, p, p, None, p) == bsq.ERR_ARG               # col codes
     assert dq(bsq.MXFP8, p, 0, 64, 0, p, p, p, p) == bsq.ERR_ARG                   # rows
     assert dq(bsq.MXFP8, p, 48, 64, 0, p, p, p, p) == bsq.ERR_SHAPE                # rows % 32

@@ -21,10 +21,11 @@ def _bsq():
     return bsq
 
 
-def _check(fmt, x_np, stochastic, seed, label):
+def _check(fmt, x_np, stochastic, seed, label, global_scale=None):
     bsq = _bsq()
-    qr_o, qc_o = oracle.quantize_dual(fmt, x_np, stochastic=stochastic, seed=seed)
-    qr, qc = bsq.quantize_dual(fmt, to_dev(x_np), stochastic=stochastic, seed=seed)
+    qr_o, qc_o = oracle.quantize_dual(fmt, x_np, stochastic=stochastic, seed=seed, global_scale=global_scale)
+    gs = None if global_scale is None else torch.tensor([global_scale], dtype=torch.float32, device="cuda")
+    qr, qc = bsq.quantize_dual(fmt, to_dev(x_np), stochastic=stochastic, seed=seed, global_scale=gs)
     assert bsq.device_status() == 0
     for name, got, want in (("row", qr, qr_o), ("col", qc, qc_o)):
         codes = got.codes.cpu().numpy()
@@ -37,7 +38,7 @@ def _check(fmt, x_np, stochastic, seed, label):
     return qr, qc
 
 
-@pytest.mark.parametrize("fmt", ["mxfp8", "mxfp4"])
+@pytest.mark.parametrize("fmt", ["mxfp8", "mxfp4", "nvfp4"])
 @pytest.mark.parametrize("rows,cols", SHAPES)
 @pytest.mark.parametrize("stochastic", [False, True])
 def test_dual_bf16_matches_oracle(fmt, rows, cols, stochastic):
@@ -45,7 +46,7 @@ def test_dual_bf16_matches_oracle(fmt, rows, cols, stochastic):
     _check(fmt, x, stochastic, seed=rows * 1000 + cols, label="%s %dx%d sr=%d" % (fmt, rows, cols, stochastic))
 
 
-@pytest.mark.parametrize("fmt", ["mxfp8", "mxfp4"])
+@pytest.mark.parametrize("fmt", ["mxfp8", "mxfp4", "nvfp4"])
 @pytest.mark.parametrize("rows,cols", [(32, 64), (96, 160), (192, 416)])
 @pytest.mark.parametrize("stochastic", [False, True])
 def test_dual_fp32_matches_oracle(fmt, rows, cols, stochastic):
@@ -53,7 +54,7 @@ def test_dual_fp32_matches_oracle(fmt, rows, cols, stochastic):
     _check(fmt, x, stochastic, seed=7, label="%s f32 %dx%d sr=%d" % (fmt, rows, cols, stochastic))
 
 
-@pytest.mark.parametrize("fmt", ["mxfp8", "mxfp4"])
+@pytest.mark.parametrize("fmt", ["mxfp8", "mxfp4", "nvfp4"])
 @pytest.mark.parametrize("src_f32", [False, True])
 def test_dual_special_values(fmt, src_f32):
     """Zeros of both signs, all-zero blocks, exact grid points, values at and past saturation,
@@ -79,9 +80,10 @@ def test_dual_special_values(fmt, src_f32):
         _check(fmt, data, sr, seed=3, label="%s special f32=%d sr=%d" % (fmt, src_f32, sr))
 
 
-@pytest.mark.parametrize("fmt", ["mxfp8", "mxfp4"])
+@pytest.mark.parametrize("fmt", ["mxfp8", "mxfp4", "nvfp4"])
 def test_dual_rne_equals_two_quantizer_calls(fmt):
-    """Without stochastic rounding the two layouts are exactly bsq_quantize of X and of X^T."""
+    """Without stochastic rounding the two layouts are exactly bsq_quantize of X and of X^T
+    (NVFP4: both with the tensor's own per-tensor scale, which X and X^T share)."""
     bsq = _bsq()
     x = to_dev(random_matrix(288, 416, seed=1, dist="normal"))
     qr, qc = bsq.quantize_dual(fmt, x)
@@ -89,6 +91,15 @@ def test_dual_rne_equals_two_quantizer_calls(fmt):
     b = bsq.quantize(fmt, x.t().contiguous())
     assert torch.equal(qr.codes, a.codes) and torch.equal(qr.scales, a.scales)
     assert torch.equal(qc.codes, b.codes) and torch.equal(qc.scales, b.scales)
+
+
+@pytest.mark.parametrize("stochastic", [False, True])
+@pytest.mark.parametrize("g", [0.00123, 1.0, 0.0])
+def test_dual_nvfp4_given_scale(stochastic, g):
+    """A given per-tensor scale (the delayed scale of training): both layouts use it, and both
+    tails record it with the tensor's own amax; g = 0 gives signed zero codes everywhere."""
+    x = random_matrix(160, 288, seed=4, dist="student_t4")
+    _check("nvfp4", x, stochastic, seed=9, label="nvfp4 given g=%g sr=%d" % (g, stochastic), global_scale=g)
 
 
 def test_dual_seed_determines_the_codes():

@@ -172,3 +172,26 @@ def test_dual_nvfp4_sr_steps_at_most_one_code():
             assert np.array_equal(p & 0x8, q & 0x8)  # the sign of x in both
             assert np.abs((p & 0x7).astype(int) - (q & 0x7).astype(int)).max() <= 1
     assert not np.array_equal(s1[0].codes, s2[0].codes)
+
+
+def test_delayed_scale_with_unit_headroom_is_the_computed_scale():
+    """H = 1: the delayed scale from a tensor's recorded amax equals the scale the NVFP4
+    quantizer computes from that tensor (reading R3)."""
+    rng = np.random.default_rng(19)
+    for k in range(20):
+        x = f32_to_bf16_bits((rng.standard_t(3, size=(32, 64)) * 10.0 ** rng.uniform(-6, 6)).astype(np.float32))
+        q = oracle.quantize("nvfp4", x)
+        assert oracle.delayed_global_scale(q.amax, 1.0) == q.g
+
+
+def test_delayed_scale_power_of_two_headroom_scales_exactly():
+    """For H = 2^j the two rounded fp32 steps commute with the exact scaling: g(H) = 2^j g(1)."""
+    rng = np.random.default_rng(20)
+    for amax in np.float32(10.0) ** rng.uniform(-20, 20, 200).astype(np.float32):
+        g1 = oracle.delayed_global_scale(amax, 1.0)
+        for j in (1, 3, 5):
+            assert oracle.delayed_global_scale(amax, 2.0 ** j) == g1 * 2.0 ** j
+    # and a non-power-of-two headroom differs from scaling the computed g in some cases, i.e.
+    # the product is taken before the division
+    amax = np.float32(1.1)
+    assert oracle.delayed_global_scale(amax, 3.0) == np.float32(np.float32(amax * np.float32(3.0)) / np.float32(2688.0))
