@@ -71,11 +71,12 @@ def quant_bytes(fmt: str, rows: int, cols: int, src_bytes: int, computed_global:
     return reads + codes + scales
 
 
-def dual_bytes(fmt: str, rows: int, cols: int, src_bytes: int) -> int:
-    """Algorithmic bytes of one dual-layout MX quantization: the source read once, codes and
-    scales of both layouts written."""
+def dual_bytes(fmt: str, rows: int, cols: int, src_bytes: int, computed_global: bool = False) -> int:
+    """Algorithmic bytes of one dual-layout quantization: the source read once (twice for an
+    NVFP4 scale computed from the tensor's amax), codes and scales of both layouts written."""
     n = rows * cols
-    return n * src_bytes + 2 * (n if fmt == MXFP8 else n // 2) + 2 * (n // 32)
+    reads = 2 if (fmt == NVFP4 and computed_global) else 1
+    return reads * n * src_bytes + 2 * (n if fmt == MXFP8 else n // 2) + 2 * (n // (16 if fmt == NVFP4 else 32))
 
 
 def gemm_bytes(fmt: str, M: int, N: int, K: int, bias: bool) -> int:
@@ -159,9 +160,10 @@ def _oracle_train_rows(g, rows: int, sr: bool) -> float:
     xr, xc = oracle.quantize_dual(g.fmt, x)
     wr, wc = oracle.quantize_dual(g.fmt, w)
     dr, dc = oracle.quantize_dual(g.fmt, dy, stochastic=sr, seed=1)
-    oracle.gemm(xr.decode(), wr.decode(), bias, 1.0, want_abs=False)
-    oracle.gemm(dr.decode(), wc.decode(), None, 1.0, want_abs=False)
-    oracle.gemm(dc.decode(), xc.decode(), None, 1.0, want_abs=False)
+    nv = g.fmt == NVFP4  # alpha = g_A g_B
+    oracle.gemm(xr.decode(), wr.decode(), bias, xr.g * wr.g if nv else 1.0, want_abs=False)
+    oracle.gemm(dr.decode(), wc.decode(), None, dr.g * wc.g if nv else 1.0, want_abs=False)
+    oracle.gemm(dc.decode(), xc.decode(), None, dc.g * xc.g if nv else 1.0, want_abs=False)
     return time.perf_counter() - t0
 
 
@@ -213,6 +215,7 @@ def config_of(wl):
             "gemms": [{"name": g.name, "format": g.fmt, "M": g.M, "N": g.N, "K": g.K} for g in wl.gemms],
             "chain": wl.chain,
             "grad_rounding": ("stochastic (Philox4x32-10)" if wl.grad_sr else "nearest even") if wl.chain == "train" else None,
+            "grad_scale": ("delayed: previous step's amax x %g / 2688" % wl.grad_headroom) if wl.grad_headroom else None,
             "l2": "flushed between timed steps (256 MB write)",
             "launch": "one step (L2 flush; per layer quantize A+B, then the GEMM) captured once into a CUDA "
                       "graph with CUDA events as graph nodes around each layer's quantize and GEMM; replayed "
@@ -336,6 +339,7 @@ def run_gpu(args, rank: int, world: int):
     elif wl.chain == "train":
         g = wl.gemms[0]
         fmt, M, K, N = g.fmt, g.M, g.K, g.N
+        delayed = fmt == NVFP4 and wl.grad_headroom is not None
         hosts = {"x": host(make_activations(g)), "w": host(make_weights(g)), "bias": host(make_bias(g)),
                  "dy": host(make_output_grad(g))}
 
@@ -347,22 +351,35 @@ def run_gpu(args, rank: int, world: int):
                       "out": torch.empty((M, N), dtype=torch.bfloat16, device=dev),
                       "dx": torch.empty((M, K), dtype=torch.bfloat16, device=dev),
                       "dw": torch.empty((N, K), dtype=torch.bfloat16, device=dev)})
+            if delayed:
+                # the step before the first one: dY quantized with its own amax, so that the
+                # first timed step finds a recorded amax in the tail
+                D["g_dy"] = torch.empty(1, dtype=torch.float32, device=dev)
+                D["dy"].copy_(hosts["dy"])
+                bsq.quantize_dual(fmt, D["dy"], out=D["qdy"])
             return D
 
         def quant(D, s):
             # both layouts of X, W and dY, each in one pass over its source
             bsq.quantize_dual(fmt, D["x"], out=D["qx"], stream=s)
             bsq.quantize_dual(fmt, D["w"], out=D["qw"], stream=s)
-            bsq.quantize_dual(fmt, D["dy"], stochastic=wl.grad_sr, seed=1, out=D["qdy"], stream=s)
+            g_dy = None
+            if delayed:  # this step's scale from the amax the previous step recorded
+                g_dy = bsq.delayed_global_scale(D["qdy"][0], wl.grad_headroom, out=D["g_dy"], stream=s)
+            bsq.quantize_dual(fmt, D["dy"], stochastic=wl.grad_sr, seed=1, global_scale=g_dy, out=D["qdy"], stream=s)
 
         def gemm(D, s):
             bsq.gemm(D["qx"][0], D["qw"][0], D["bias"], out=D["out"], stream=s)  # Y = X W^T + b
             bsq.gemm(D["qdy"][0], D["qw"][1], None, out=D["dx"], stream=s)       # dX = dY W
             bsq.gemm(D["qdy"][1], D["qx"][1], None, out=D["dw"], stream=s)       # dW = dY^T X
 
+        nv = fmt == NVFP4
         units.append({"hosts": hosts, "alloc": alloc, "quant": quant, "gemm": gemm, "fmt": fmt,
-                      "flops": 3 * g.flops, "launches": 6, "outs": ("out", "dx", "dw"),
-                      "qbytes": dual_bytes(fmt, M, K, 2) + dual_bytes(fmt, N, K, 2) + dual_bytes(fmt, M, N, 2),
+                      "flops": 3 * g.flops, "outs": ("out", "dx", "dw"),
+                      # duals + GEMMs; NVFP4: amax passes of X and W, the delayed-scale kernel
+                      "launches": 6 + (2 if nv else 0) + (1 if delayed else 0) + (1 if nv and not delayed else 0),
+                      "qbytes": dual_bytes(fmt, M, K, 2, True) + dual_bytes(fmt, N, K, 2, True) +
+                                dual_bytes(fmt, M, N, 2, not delayed),
                       "gbytes": gemm_bytes(fmt, M, N, K, True) + gemm_bytes(fmt, M, K, N, False) +
                                 gemm_bytes(fmt, N, K, M, False)})
     else:

@@ -56,6 +56,8 @@ _lib.bsq_layernorm_quantize.argtypes = [_int, _vp, _vp, _vp, ctypes.c_float, _i6
 _lib.bsq_gemm.restype = _int
 _lib.bsq_quantize_dual.argtypes = [_int, _vp, _i64, _i64, ctypes.c_uint64, _vp, _vp, _vp, _vp, _vp, _vp]
 _lib.bsq_quantize_dual.restype = _int
+_lib.bsq_delayed_global_scale.argtypes = [_vp, _i64, _i64, ctypes.c_float, _vp, _vp]
+_lib.bsq_delayed_global_scale.restype = _int
 _lib.bsq_gemm.argtypes = [_int, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp]
 _lib.bsq_gemm_gelu.restype = _int
 _lib.bsq_gemm_gelu.argtypes = [_int, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp]
@@ -70,7 +72,7 @@ _lib.bsq_strerror.restype = ctypes.c_char_p
 _lib.bsq_strerror.argtypes = [_int]
 
 EXPORTS = ("bsq_codes_bytes", "bsq_scales_bytes", "bsq_quantize", "bsq_quantize_batch", "bsq_layernorm_quantize",
-           "bsq_quantize_dual", "bsq_gemm",
+           "bsq_quantize_dual", "bsq_delayed_global_scale", "bsq_gemm",
            "bsq_gemm_gelu", "bsq_gemm_gelu_quantize", "bsq_get_device_status", "bsq_selftest_timeout",
            "bsq_last_error", "bsq_strerror")
 
@@ -140,6 +142,12 @@ def bsq_quantize_dual(fmt_flags: int, src: Ptr, rows: int, cols: int, seed: int,
     return int(_lib.bsq_quantize_dual(int(fmt_flags), _p(src), rows, cols, int(seed) & (2 ** 64 - 1), _p(row_codes),
                                       _p(row_scales), _p(col_codes), _p(col_scales), _p(global_scale),
                                       _stream(stream)))
+
+
+def bsq_delayed_global_scale(prev_scales: Ptr, rows: int, cols: int, headroom: float, g_out: Ptr,
+                             stream=None) -> int:
+    return int(_lib.bsq_delayed_global_scale(_p(prev_scales), rows, cols, float(headroom), _p(g_out),
+                                             _stream(stream)))
 
 
 def bsq_gemm(fmt, A: Ptr, A_scales: Ptr, B: Ptr, B_scales: Ptr, bias: Ptr, out: Ptr, M: int, N: int, K: int,
@@ -286,6 +294,19 @@ def quantize_dual(fmt, x: torch.Tensor, stochastic: bool = False, seed: int = 0,
         qr.global_scale = g
         qc.global_scale = g
     return qr, qc
+
+
+def delayed_global_scale(prev: QTensor, headroom: float = 32.0, out: Optional[torch.Tensor] = None,
+                         stream=None) -> torch.Tensor:
+    """The next step's NVFP4 per-tensor scale from an earlier quantization `prev` of the tensor:
+    fp32(fp32(amax * headroom) / 2688) on the device, as a one-element fp32 tensor to pass as
+    `global_scale`."""
+    assert prev.fmt == NVFP4
+    g = out if out is not None else torch.empty(1, dtype=torch.float32, device=prev.scales.device)
+    rc = bsq_delayed_global_scale(prev.scales, prev.rows, prev.cols, headroom, g, stream)
+    if rc != OK:
+        raise BsqError(rc, "bsq_delayed_global_scale")
+    return g
 
 
 def gemm(qa: QTensor, qb: QTensor, bias: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,

@@ -182,6 +182,19 @@ int bsq_quantize_dual(int fmt_flags, const void* src, int64_t rows, int64_t cols
   return st == BSQ_OK ? BSQ_OK : fail(st);
 }
 
+int bsq_delayed_global_scale(const void* prev_scales, int64_t rows, int64_t cols, float headroom, float* g_out,
+                             bsq_stream_t stream) {
+  if (prev_scales == nullptr || g_out == nullptr || rows <= 0 || cols <= 0) return fail(BSQ_ERR_ARG);
+  if (!(headroom > 0.0f) || !(headroom < INFINITY)) return fail(BSQ_ERR_ARG);
+  if (cols % 16 != 0 || rows > INT32_MAX || cols > INT32_MAX) return fail(BSQ_ERR_SHAPE);
+  if (!aligned16(prev_scales) || (reinterpret_cast<uintptr_t>(g_out) & 3u)) return fail(BSQ_ERR_ALIGN);
+  const bsq::DeviceInfo* dev = bsq::current_device();
+  if (dev == nullptr) return fail(BSQ_ERR_ARCH);
+  const int st = bsq::launch_delayed_scale(prev_scales, rows, cols, headroom, g_out,
+                                           reinterpret_cast<cudaStream_t>(stream));
+  return st == BSQ_OK ? BSQ_OK : fail(st);
+}
+
 namespace {
 // Validation shared by the GEMM entry points; BSQ_OK or the error code.
 int check_gemm(int fmt, const void* A, const void* A_scales, const void* B, const void* B_scales,

@@ -52,6 +52,11 @@ int launch_quantize_batch(int fmt, bool src_f32, bool global_given, int count, c
 int launch_amax(const void* src, bool src_f32, int64_t elems, uint32_t* out, cudaStream_t stream,
                 const DeviceInfo& dev);
 
+// g_out = fp32(fp32(amax * headroom) / 2688), amax from the tail of an NVFP4 scale buffer of a
+// rows x cols matrix.
+int launch_delayed_scale(const void* prev_scales, int64_t rows, int64_t cols, float headroom, float* g_out,
+                         cudaStream_t stream);
+
 // Row LayerNorm then MX quantization of one matrix (fmt MXFP8 / MXFP4); rows must fit a chunk
 // (BSQ_ERR_SHAPE otherwise).
 int launch_layernorm_quantize(int fmt, bool src_f32, const QuantItem& item, const uint16_t* gamma,

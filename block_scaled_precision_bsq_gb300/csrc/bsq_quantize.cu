@@ -490,6 +490,33 @@ cudaError_t launch_q(const QuantBatch& b, int grid, cudaStream_t stream) {
 
 }  // namespace
 
+namespace {
+// Delayed per-tensor scale: g = fp32(fp32(amax_prev * headroom) / 2688), amax_prev from the tail
+// of an earlier NVFP4 quantization of the tensor.
+__global__ void delayed_scale_kernel(const uint32_t* tail, float headroom, float* g_out) {
+  grid_dependency_wait();
+  *g_out = __fdiv_rn(__fmul_rn(__uint_as_float(tail[1]), headroom), 2688.0f);
+  launch_dependents();
+}
+}  // namespace
+
+int launch_delayed_scale(const void* prev_scales, int64_t rows, int64_t cols, float headroom, float* g_out,
+                         cudaStream_t stream) {
+  const uint32_t* tail = reinterpret_cast<const uint32_t*>(static_cast<const uint8_t*>(prev_scales) +
+                                                           scales_body_bytes(BSQ_NVFP4, rows, cols));
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(1);
+  cfg.stream = stream;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, delayed_scale_kernel, tail, headroom, g_out) == cudaSuccess ? BSQ_OK
+                                                                                            : BSQ_ERR_LAUNCH;
+}
+
 int launch_amax(const void* src, bool src_f32, int64_t elems, uint32_t* out, cudaStream_t stream,
                 const DeviceInfo& dev) {
   const int64_t nvec = elems * (src_f32 ? 4 : 2) / 16;

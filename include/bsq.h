@@ -181,6 +181,27 @@ int bsq_quantize_dual(int fmt_flags, const void* src, int64_t rows, int64_t cols
                       void* row_scales, void* col_codes, void* col_scales, float* global_scale, bsq_stream_t stream);
 
 /*
+ * bsq_delayed_global_scale: the delayed NVFP4 per-tensor scale of quantized training
+ * ("lightly-train - DINOv3 + EoMT on RTX 5090" README, section 5.5: the amax found while a
+ * tensor is quantized in one step, times a headroom factor, is the next step's scale, so no
+ * step spends an extra pass over the tensor on its amax; the README's dY study settles on a
+ * headroom of 32). Enqueues one thread computing
+ *   *g_out = fp32(fp32(amax * headroom) / 2688)
+ * with amax the tail word of prev_scales, an NVFP4 scale buffer of a rows x cols matrix
+ * written by bsq_quantize / bsq_quantize_batch / bsq_quantize_dual (either layout's buffer:
+ * both tails hold the same amax). Pass g_out to the next quantization of the tensor with
+ * BSQ_FLAG_GLOBAL_GIVEN; that call records the new amax in its own tail. Reading the tail and
+ * writing g_out are ordered on `stream` only, with no host synchronisation.
+ *   prev_scales  bsq_scales_bytes(BSQ_NVFP4, rows, cols) bytes, 16-byte aligned
+ *   headroom     finite, > 0
+ *   g_out        one fp32 in device memory, 4-byte aligned
+ * Errors: BSQ_ERR_ARG (NULL pointer, non-positive size, bad headroom), BSQ_ERR_SHAPE (cols % 16,
+ * sizes >= 2^31), BSQ_ERR_ALIGN.
+ */
+int bsq_delayed_global_scale(const void* prev_scales, int64_t rows, int64_t cols, float headroom, float* g_out,
+                             bsq_stream_t stream);
+
+/*
  * bsq_gemm: out[m, n] = bf16_rn(alpha * sum_k Ahat[m,k] * Bhat[n,k] + bias[n]).
  *   A, A_scales  M x K operand as written by bsq_quantize(fmt, ..., M, K, ...).
  *   B, B_scales  N x K operand (the nn.Linear weight layout) from bsq_quantize(fmt, ..., N, K, ...).

@@ -94,6 +94,12 @@ def test_argument_errors_before_any_cuda_call(bsq):
     assert bsq.bsq_gemm(bsq.MXFP8, p, p + 4, p, p, None, p, 128, 256, 256) == bsq.ERR_ALIGN
     assert bsq.bsq_gemm(bsq.MXFP8, p, p, p, p, p + 1, p, 128, 256, 256) == bsq.ERR_ALIGN
     assert bsq.bsq_selftest_timeout(10, None) == bsq.ERR_ARG
+    ds = bsq.bsq_delayed_global_scale
+    assert ds(None, 64, 64, 32.0, p) == bsq.ERR_ARG
+    assert ds(p, 64, 64, 0.0, p) == bsq.ERR_ARG                                    # headroom
+    assert ds(p, 64, 64, float("inf"), p) == bsq.ERR_ARG
+    assert ds(p, 64, 40, 32.0, p) == bsq.ERR_SHAPE                                 # cols % 16
+    assert ds(p, 64, 64, 32.0, p + 2) == bsq.ERR_ALIGN                             # g_out
     dq = bsq.bsq_quantize_dual
     assert dq(7, p, 64, 64, 0, p, p, p, p) == bsq.ERR_ARG                          # format
     assert dq(bsq.MXFP8 | bsq.FLAG_GLOBAL_GIVEN, p, 64, 64, 0, p, p, p, p, p) == bsq.ERR_ARG  # MX given g

@@ -10,7 +10,7 @@ import torch
 
 import oracle
 from tests.gpu_util import check_gemm_rows, sample_rows, to_dev
-from workloads import Gemm, MXFP8, make_activations, make_output_grad, make_weights
+from workloads import Gemm, MXFP8, NVFP4, make_activations, make_output_grad, make_weights, random_matrix
 
 pytestmark = pytest.mark.gpu
 
@@ -34,6 +34,8 @@ def _run(fmt, M, K, N, sr, seed, full_rows=False):
     xr, xc = bsq.quantize_dual(fmt, to_dev(x))
     wr, wc = bsq.quantize_dual(fmt, to_dev(w))
     dx, dw = bsq.linear_backward(to_dev(dy), xc, wc, stochastic=sr, seed=seed + 99)
+    if fmt == NVFP4:  # the GEMM's alpha is g_A * g_B, read from the operands' tails
+        assert xc.global_scale is not None and wc.global_scale is not None
     torch.cuda.synchronize()
     assert bsq.device_status() == 0
     ox = oracle.quantize_dual(fmt, x)
@@ -58,6 +60,32 @@ def _run(fmt, M, K, N, sr, seed, full_rows=False):
 @pytest.mark.parametrize("sr", [False, True])
 def test_backward_mxfp8_matches_oracle(M, K, N, sr):
     _run(MXFP8, M, K, N, sr, seed=M + K + N, full_rows=True)
+
+
+# NVFP4 contracts in steps of 256
+@pytest.mark.parametrize("M,K,N", [(256, 256, 256), (512, 416, 768)])
+@pytest.mark.parametrize("sr", [False, True])
+def test_backward_nvfp4_matches_oracle(M, K, N, sr):
+    _run(NVFP4, M, K, N, sr, seed=M + K + N, full_rows=True)
+
+
+def test_delayed_scale_feeds_the_next_quantization():
+    """Step 1 quantizes dY with its own amax; the delayed scale (headroom 32) from step 1's tail
+    quantizes step 2's dY (stochastic): scale value and both layouts bit-exact against the
+    oracle, and step 2's tails record g and step 2's own amax."""
+    bsq = _bsq()
+    d1 = random_matrix(256, 384, seed=31, std=1e-3)
+    d2 = random_matrix(256, 384, seed=32, std=3e-3)
+    q1 = bsq.quantize_dual("nvfp4", to_dev(d1))
+    g2 = bsq.delayed_global_scale(q1[1], headroom=32.0)
+    o1 = oracle.quantize_dual("nvfp4", d1)
+    g2_want = oracle.delayed_global_scale(o1[0].amax, 32.0)
+    assert g2.item() == g2_want
+    q2 = bsq.quantize_dual("nvfp4", to_dev(d2), stochastic=True, seed=77, global_scale=g2)
+    assert bsq.device_status() == 0
+    o2 = oracle.quantize_dual("nvfp4", d2, stochastic=True, seed=77, global_scale=g2_want)
+    _same(q2[0], o2[0], "dY step 2 row-wise")
+    _same(q2[1], o2[1], "dY step 2 column-wise")
 
 
 def test_backward_full_size_vitb_fc1():

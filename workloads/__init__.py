@@ -22,6 +22,10 @@ quantized GEMMs are qkv / proj / fc1 / fc2 of every ViT block):
                   one training step of the ViT-B/16 fc1 layer at training shape: forward,
                   dgrad (dX = dY W) and wgrad (dW = dY^T X), every operand from the dual-layout
                   quantizer; the output gradient dY rounded to nearest or stochastically.
+  vitb_fc1_nvfp4_train_sr
+                  the same step in NVFP4 (the README's FP4 training path): X and W with their
+                  own per-tensor scales, dY stochastically rounded with the delayed scale of
+                  the previous step (headroom 32).
 
 Recipe (every array is drawn in fp64 by numpy's default_rng, cast to fp32 with
 round-to-nearest, then to bf16 with round-to-nearest-even where the input is bf16):
@@ -90,6 +94,7 @@ class Workload:
     # wgrad) with dual-layout operands
     chain: Optional[str] = None
     grad_sr: bool = False  # "train": stochastic rounding of the output gradient
+    grad_headroom: Optional[float] = None  # "train", NVFP4: dY's scale delayed by one step, this headroom
 
 
 def _vitl_sweep(fmt: str, a_dist: str) -> List[Gemm]:
@@ -152,6 +157,11 @@ for _sr in (False, True):
         _n, "ViT-B/16 MLP fc1 training step (forward, dgrad, wgrad) at M=14336, K=768, N=3072, MXFP8, "
             "dual-layout operands, output gradient rounded %s" % ("stochastically" if _sr else "to nearest even"),
         [Gemm("fc1", MXFP8, 14 * 1024, 768, 3072)], "train", _sr)
+WORKLOADS["vitb_fc1_nvfp4_train_sr"] = Workload(
+    "vitb_fc1_nvfp4_train_sr",
+    "ViT-B/16 MLP fc1 training step (forward, dgrad, wgrad) at M=14336, K=768, N=3072, NVFP4, dual-layout "
+    "operands; dY rounded stochastically with the previous step's amax times headroom 32 as its scale",
+    [Gemm("fc1", NVFP4, 14 * 1024, 768, 3072)], "train", True, 32.0)
 
 
 def _gelu_erf(x: np.ndarray) -> np.ndarray:
