@@ -267,11 +267,14 @@ def replica_throughput(ms_local: float, flops_per_rank: int, world: int, device=
 
 # ----------------------------------------------------------------------------------- GPU arm
 def kernel_source_hash() -> str:
+    """Hash of the sources the GEMM kernel is built from (its .cu, the shared device header and
+    the headers): the key of the recorded DRAM traffic."""
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "block_scaled_precision_bsq_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode() + f.read())
+    pkg = os.path.join(ROOT, "block_scaled_precision_bsq_gb300", "csrc")
+    for path in (os.path.join(pkg, "bsq_gemm.cu"), os.path.join(pkg, "bsq_device.cuh"),
+                 os.path.join(pkg, "bsq_internal.h"), os.path.join(ROOT, "include", "bsq.h")):
+        with open(path, "rb") as f:
+            h.update(os.path.basename(path).encode() + f.read())
     return h.hexdigest()[:16]
 
 
