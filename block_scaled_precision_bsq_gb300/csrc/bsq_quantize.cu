@@ -9,19 +9,20 @@
 // floor(log2(amax)) - emax with emax the exponent of the element format's top binade.
 //
 // Work mapping (two CTAs per SM, persistent). The source is cut into chunks of whole rows
-// (or, for rows longer than a chunk, row pieces of whole 512-element segments); a chunk is
+// (or, for rows longer than a chunk, row pieces of whole 1024-element segments); a chunk is
 // contiguous in memory and comes in with one 1-D TMA bulk copy. A producer thread per CTA
 // keeps a ring of up to kRing chunk buffers in flight -- for a 22 MB matrix that is nearly
 // every chunk of the SM's share, requested at kernel start -- and the consumer warps (dealt
-// warp steps round-robin over the CTA's chunks) quantize a chunk straight
-// from shared memory, walking it as one flat array: each warp step covers 512 consecutive
-// elements, each lane 16 (one 32-byte piece; rows are multiples of 16 elements long, so a
-// piece never straddles two rows). A 1x32 block is then 2 lanes (one xor-shuffle for its
-// maximum), a 1x16 block 1 lane. Codes leave as one 16-byte (E4M3) or 8-byte (e2m1) store per
-// lane; each block's scale byte is stored at its place in the tiled layout (128 rows x 4
-// columns per 512-byte tile, row r at byte (r % 32) * 16 + ((r / 32) % 4) * 4), the lane of
-// a row's last block also zeroing the padding columns of that 4-column group. Scale bytes of
-// the padding rows of the last row tile are written as zeros by the kernel itself.
+// warp steps round-robin over the CTA's chunks) quantize a chunk straight from shared memory,
+// walking it as one flat array: each warp step covers 1024 consecutive elements, each lane 32,
+// i.e. exactly one MX block or two NVFP4 blocks, so a lane finds its block maxima without any
+// shuffle and computes one scale position per block. Codes leave as 32 (E4M3) or 16 (e2m1)
+// contiguous bytes per lane; each block's scale byte is stored at its place in the tiled
+// layout (128 rows x 4 columns per 512-byte tile, row r at byte (r % 32) * 16 +
+// ((r / 32) % 4) * 4), the lane of a row's last block also zeroing the padding columns of that
+// 4-column group. Scale bytes of the padding rows of the last row tile are written as zeros by
+// the kernel itself. (A lane-per-16-elements version with shuffles for the block maxima spent
+// ~14 instructions per element against ~12 here.)
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -33,9 +34,9 @@
 namespace bsq {
 namespace {
 
-constexpr int kThreads = 512;          // warp 0: TMA producer (lane 0); warps 1..15: consumers
+constexpr int kThreads = 384;          // warp 0: TMA producer (lane 0); warps 1..11: consumers
 constexpr int kConsumerWarps = kThreads / 32 - 1;
-constexpr int kLaneElems = 16;         // elements per lane per step
+constexpr int kLaneElems = 32;         // elements per lane per step: one MX block, two NVFP4 blocks
 constexpr int kSeg = 32 * kLaneElems;   // elements per warp step
 constexpr int kRing = 6;                // chunk buffers per CTA
 constexpr int kCtasPerSm = 2;           // two resident CTAs: twice the warps to hide latency
@@ -79,41 +80,41 @@ struct QuantBatch {
   int* status;
 };
 
-template <bool F32>
-struct Loaded {
-  uint4 v[F32 ? 4 : 2];  // 16 elements
-};
-
-// 16 source elements of one lane -> fp32 values and their largest magnitude. The maximum
-// starts at 0 and skips NaN (fmaxf returns the other operand), as a block maximum taken with
-// "if (|x| > amax) amax = |x|" does.
-template <bool F32>
-__device__ __forceinline__ void unpack16(const Loaded<F32>& L, float (&x)[16], float& amax) {
+// The first N (16 or 32) source elements of one lane's piece (bf16 or fp32) -> fp32 values.
+template <bool F32, int N = 32>
+__device__ __forceinline__ void load32(const uint8_t* p, float* x) {
+  const uint4* q = reinterpret_cast<const uint4*>(p);
   if constexpr (F32) {
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      x[4 * q + 0] = __uint_as_float(L.v[q].x);
-      x[4 * q + 1] = __uint_as_float(L.v[q].y);
-      x[4 * q + 2] = __uint_as_float(L.v[q].z);
-      x[4 * q + 3] = __uint_as_float(L.v[q].w);
+    for (int i = 0; i < N / 4; ++i) {
+      const uint4 v = q[i];
+      x[4 * i + 0] = __uint_as_float(v.x);
+      x[4 * i + 1] = __uint_as_float(v.y);
+      x[4 * i + 2] = __uint_as_float(v.z);
+      x[4 * i + 3] = __uint_as_float(v.w);
     }
   } else {
 #pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      const uint32_t w[4] = {L.v[q].x, L.v[q].y, L.v[q].z, L.v[q].w};
+    for (int i = 0; i < N / 8; ++i) {
+      const uint4 v = q[i];
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        x[8 * q + 2 * i] = __uint_as_float(w[i] << 16);
-        x[8 * q + 2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+      for (int k = 0; k < 4; ++k) {
+        x[8 * i + 2 * k] = __uint_as_float(w[k] << 16);
+        x[8 * i + 2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
       }
     }
   }
-  float m[8];
+}
+
+// Largest |x[i]| over n values. The maximum starts at 0 and skips NaN (fmaxf returns the other
+// operand), as a block maximum taken with "if (|x| > amax) amax = |x|" does.
+template <int N>
+__device__ __forceinline__ float abs_max(const float* x) {
+  float m[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-  for (int i = 0; i < 8; ++i) m[i] = fmaxf(fabsf(x[2 * i]), fabsf(x[2 * i + 1]));
-#pragma unroll
-  for (int i = 0; i < 4; ++i) m[i] = fmaxf(m[i], m[i + 4]);
-  amax = fmaxf(fmaxf(0.0f, fmaxf(m[0], m[2])), fmaxf(m[1], m[3]));
+  for (int i = 0; i < N; ++i) m[i & 3] = fmaxf(m[i & 3], fabsf(x[i]));
+  return fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
 }
 
 // Byte offset of the 32-bit scale word holding scale columns [c4, c4 + 4) of row r.
@@ -121,49 +122,54 @@ __device__ __forceinline__ int64_t scale_word_offset(int64_t r, int64_t c4, int6
   return ((r >> 7) * nct + (c4 >> 2)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4;
 }
 
-// Quantize the 16 elements of one lane: `x` its values, `amax` the largest magnitude of the
-// lane's block (already reduced over the block's lanes). Writes the codes to `codes_dst` (16
-// E4M3 bytes or 8 e2m1 bytes) and returns the block's scale byte.
-template <int FMT>
-__device__ __forceinline__ uint32_t quantize16(const float (&x)[16], float amax, float g, float six_g,
-                                               uint8_t* codes_dst) {
-  constexpr uint32_t kEmax = (FMT == BSQ_MXFP8) ? 8u : 2u;
-  uint32_t sbyte;
-  if constexpr (FMT == BSQ_NVFP4) {
-    uint32_t scode = 0;
-    if (g != 0.0f) scode = cvt_e4m3x2(__fdiv_rn(amax, six_g), 0.0f) & 0xFFu;
-    sbyte = scode;
-    const float sc = e4m3_to_f32(scode);
-    const float sg = __fmul_rn(sc, g);
-    uint32_t w[2] = {0, 0};
+// Codes of 16 elements of one NVFP4 block with block maximum `amax` -> 8 bytes in w[0..1]; returns
+// the block's E4M3 scale code.
+__device__ __forceinline__ uint32_t nv_block16(const float* x, float amax, float g, float six_g, uint32_t* w) {
+  uint32_t scode = 0;
+  if (g != 0.0f) scode = cvt_e4m3x2(__fdiv_rn(amax, six_g), 0.0f) & 0xFFu;
+  const float sc = e4m3_to_f32(scode);
+  const float sg = __fmul_rn(sc, g);
+  w[0] = w[1] = 0;
 #pragma unroll
-    for (int i = 0; i < 16; i += 2) {
-      uint32_t c;
-      if (sc == 0.0f) {
-        c = ((__float_as_uint(x[i]) >> 31) << 3) | ((__float_as_uint(x[i + 1]) >> 31) << 7);
-      } else {
-        c = cvt_e2m1x2(__fdiv_rn(x[i], sg), __fdiv_rn(x[i + 1], sg));
-      }
-      w[i >> 3] |= c << (4 * (i & 7));
-    }
-    *reinterpret_cast<uint2*>(codes_dst) = make_uint2(w[0], w[1]);
-  } else {
-    const uint32_t ef = __float_as_uint(amax) >> 23;  // biased exponent of the block maximum
-    sbyte = ef > kEmax ? ef - kEmax : 0u;
-    const float mul = __uint_as_float((254u - sbyte) << 23);  // 2^(127 - sbyte), exact
-    float y[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) y[i] = x[i] * mul;
-    if constexpr (FMT == BSQ_MXFP8) {
-      uint32_t w[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) w[i] = cvt_e4m3x4(y[4 * i], y[4 * i + 1], y[4 * i + 2], y[4 * i + 3]);
-      *reinterpret_cast<uint4*>(codes_dst) = make_uint4(w[0], w[1], w[2], w[3]);
+  for (int i = 0; i < 16; i += 2) {
+    uint32_t c;
+    if (sc == 0.0f) {
+      c = ((__float_as_uint(x[i]) >> 31) << 3) | ((__float_as_uint(x[i + 1]) >> 31) << 7);
     } else {
-      *reinterpret_cast<uint2*>(codes_dst) = make_uint2(cvt_e2m1x8(y), cvt_e2m1x8(y + 8));
+      c = cvt_e2m1x2(__fdiv_rn(x[i], sg), __fdiv_rn(x[i + 1], sg));
     }
+    w[i >> 3] |= c << (4 * (i & 7));
   }
-  return sbyte;
+  return scode;
+}
+
+// Quantize the 32 elements of one lane: MX one block (scale byte returned in bits 0..7), NVFP4
+// two blocks (scale codes in bits 0..7 and 8..15). Codes go to w: 8 words (E4M3) or 4 (e2m1).
+template <int FMT>
+__device__ __forceinline__ uint32_t quantize32(const float (&x)[32], float g, float six_g, uint32_t* w) {
+  if constexpr (FMT == BSQ_NVFP4) {
+    const uint32_t s0 = nv_block16(x, abs_max<16>(x), g, six_g, w);
+    const uint32_t s1 = nv_block16(x + 16, abs_max<16>(x + 16), g, six_g, w + 2);
+    return s0 | (s1 << 8);
+  } else {
+    constexpr uint32_t kEmax = (FMT == BSQ_MXFP8) ? 8u : 2u;
+    const uint32_t ef = __float_as_uint(abs_max<32>(x)) >> 23;  // biased exponent of the block maximum
+    const uint32_t sbyte = ef > kEmax ? ef - kEmax : 0u;
+    const float mul = __uint_as_float((254u - sbyte) << 23);  // 2^(127 - sbyte), exact
+    if constexpr (FMT == BSQ_MXFP8) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) w[i] = cvt_e4m3x4(x[4 * i] * mul, x[4 * i + 1] * mul, x[4 * i + 2] * mul, x[4 * i + 3] * mul);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        float y[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) y[k] = x[8 * i + k] * mul;
+        w[i] = cvt_e2m1x8(y);
+      }
+    }
+    return sbyte;
+  }
 }
 
 template <int FMT, bool F32, int NV, bool LN>
@@ -332,30 +338,28 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) quantize_kernel(const __
       }
       for (uint32_t base = lead * kSeg; base < flat; base += kConsumerWarps * kSeg) {
         const uint32_t f = base + lane * kLaneElems;
+        // MX chunks hold whole 32-element blocks; an NVFP4 chunk may end half-way through a
+        // lane's piece (rows of 16k elements): then only its first block is live
         const bool live = f < flat;
-        Loaded<F32> in;
-        if (live) {
-          const uint4* p = reinterpret_cast<const uint4*>(buf + f * kEsize);
-#pragma unroll
-          for (int i = 0; i < (F32 ? 4 : 2); ++i) in.v[i] = p[i];
+        const bool live_hi = f + 16 < flat;
+        float x[32];
+        if (live_hi) {
+          load32<F32>(buf + f * kEsize, x);
         } else {
 #pragma unroll
-          for (int i = 0; i < (F32 ? 4 : 2); ++i) in.v[i] = make_uint4(0, 0, 0, 0);
+          for (int i = 0; i < 32; ++i) x[i] = 0.0f;
+          if (live) load32<F32, 16>(buf + f * kEsize, x);  // the first block only: nothing past the chunk is read
         }
-        float x[16];
-        float amax;
-        unpack16<F32>(in, x, amax);
         if constexpr (LN) {
-          // phase 2: y = (x - mean) * rstd * gamma + beta for this lane's 16 columns of row rr
+          // phase 2: y = (x - mean) * rstd * gamma + beta for this lane's 32 columns of row rr
           // lanes past the chunk's end (live false) read row 0: their values are never stored
           const uint32_t rr = (live && nr > 1) ? __umulhi(f, a.cols_magic) : 0u;
           const uint32_t col = live ? f - rr * static_cast<uint32_t>(nc) : 0u;
           const float mean = ln_stats[(2 * pb) * kLnMaxRows + rr], rstd = ln_stats[(2 * pb + 1) * kLnMaxRows + rr];
           const uint4* gp = reinterpret_cast<const uint4*>(a.gamma + col);
           const uint4* bp = reinterpret_cast<const uint4*>(a.beta + col);
-          amax = 0.0f;
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
+          for (int h = 0; h < 4; ++h) {
             const uint4 gv = __ldg(gp + h), bv = __ldg(bp + h);
             const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w}, bw[4] = {bv.x, bv.y, bv.z, bv.w};
 #pragma unroll
@@ -365,26 +369,40 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) quantize_kernel(const __
               y0 = __fadd_rn(__fmul_rn(__fmul_rn(y0 - mean, rstd), __uint_as_float(gw[i] << 16)), __uint_as_float(bw[i] << 16));
               y1 = __fadd_rn(__fmul_rn(__fmul_rn(y1 - mean, rstd), __uint_as_float(gw[i] & 0xFFFF0000u)),
                              __uint_as_float(bw[i] & 0xFFFF0000u));
-              amax = fmaxf(amax, fmaxf(fabsf(y0), fabsf(y1)));
             }
           }
         }
-        if constexpr (FMT != BSQ_NVFP4) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));  // 1x32 block = 2 lanes
-        if constexpr (NV == kNvGiven) run_max = max(run_max, __float_as_uint(amax));
+        if constexpr (NV == kNvGiven) run_max = max(run_max, __float_as_uint(abs_max<32>(x)));
         if (live) {
           const uint64_t e = elem0 + f;
-          const uint32_t sbyte = quantize16<FMT>(x, amax, g, six_g, a.codes + (FMT == BSQ_MXFP8 ? e : e >> 1));
-          if (FMT == BSQ_NVFP4 || (lane & 1u) == 0) {
-            // row and scale column of this block (32-bit: rows and columns stay below 2^31,
-            // and the number of 512-byte scale tiles below 2^32)
-            const uint32_t rr = nr > 1 ? __umulhi(f, a.cols_magic) : 0u;
+          uint32_t w[FMT == BSQ_MXFP8 ? 8 : 4];
+          const uint32_t sb = quantize32<FMT>(x, g, six_g, w);
+          if constexpr (FMT == BSQ_MXFP8) {
+            uint4* dst = reinterpret_cast<uint4*>(a.codes + e);
+            dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+            dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+          } else if constexpr (FMT == BSQ_MXFP4) {
+            *reinterpret_cast<uint4*>(a.codes + (e >> 1)) = make_uint4(w[0], w[1], w[2], w[3]);
+          } else {  // NVFP4 codes are only 8-byte aligned when rows are 16k elements long
+            uint2* dst = reinterpret_cast<uint2*>(a.codes + (e >> 1));
+            dst[0] = make_uint2(w[0], w[1]);
+            if (live_hi) dst[1] = make_uint2(w[2], w[3]);
+          }
+          // each block's scale byte at its place in the tiled layout (32-bit arithmetic: rows and
+          // columns stay below 2^31, the number of 512-byte scale tiles below 2^32)
+          constexpr int kBlocks = FMT == BSQ_NVFP4 ? 2 : 1;
+#pragma unroll
+          for (int h = 0; h < kBlocks; ++h) {
+            if (h == 1 && !live_hi) break;
+            const uint32_t fh = f + 16u * h;
+            const uint32_t rr = nr > 1 ? __umulhi(fh, a.cols_magic) : 0u;
             const uint32_t row = static_cast<uint32_t>(r0) + rr;
-            const uint32_t col = static_cast<uint32_t>(c0) + (f - rr * static_cast<uint32_t>(nc));
+            const uint32_t col = static_cast<uint32_t>(c0) + (fh - rr * static_cast<uint32_t>(nc));
             const uint32_t sc = col >> (FMT == BSQ_NVFP4 ? 4 : 5);
             const uint32_t tile = (row >> 7) * static_cast<uint32_t>(a.nct) + (sc >> 2);
             uint8_t* sp = a.scales + static_cast<uint64_t>(tile) * 512 +
                           (((row & 31u) << 4) | (((row >> 5) & 3u) << 2) | (sc & 3u));
-            *sp = static_cast<uint8_t>(sbyte);
+            *sp = static_cast<uint8_t>(sb >> (8 * h));
             if (sc + 1 == static_cast<uint32_t>(a.nsc)) {
               // padding columns of the row's last 4-column group read 0
               for (uint32_t j = (sc & 3u) + 1; j < 4; ++j) sp[j - (sc & 3u)] = 0;
@@ -573,7 +591,6 @@ void build_batch(QuantBatch& b, int fmt, bool src_f32, int count, const QuantIte
 int launch_quantize_batch(int fmt, bool src_f32, bool global_given, int count, const QuantItem* items,
                           cudaStream_t stream, const DeviceInfo& dev) {
   if (count < 1 || count > kMaxBatch) return BSQ_ERR_ARG;
-  const int64_t esize = src_f32 ? 4 : 2;
   QuantBatch b{};
   build_batch(b, fmt, src_f32, count, items, dev);
   const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(b.chunk_start[count], kCtasPerSm * dev.num_sms)));
