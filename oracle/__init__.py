@@ -93,6 +93,8 @@ def lib() -> ctypes.CDLL:
                                            ctypes.c_uint64, u8p, u8p, u8p, u8p, vp, vp]
         L.orc_delayed_global_scale.restype = ctypes.c_float
         L.orc_delayed_global_scale.argtypes = [ctypes.c_float, ctypes.c_float]
+        L.orc_convt2x2.restype = ctypes.c_int
+        L.orc_convt2x2.argtypes = [f64p, f64p, vp, i64, i64, i64, i64, i64, ctypes.c_double, ctypes.c_int, f64p]
         L.orc_set_num_threads.argtypes = [ctypes.c_int]
         _lib = L
     return _lib
@@ -362,3 +364,21 @@ def quantize_dual(fmt, x: np.ndarray, stochastic: bool = False, seed: int = 0,
 def delayed_global_scale(amax_prev: float, headroom: float) -> float:
     """Delayed per-tensor NVFP4 scale (reading R12): fp32(fp32(amax_prev * headroom) / 2688)."""
     return float(lib().orc_delayed_global_scale(float(amax_prev), float(headroom)))
+
+
+def convt2x2(A: np.ndarray, B: np.ndarray, bias: Optional[np.ndarray], batch: int, H: int, W: int,
+             alpha: float = 1.0, gelu: bool = False) -> np.ndarray:
+    """Transposed convolution, kernel 2, stride 2 (reading R13) from decoded fp64 operands:
+    A (batch*H*W) x Cin, B (4*Cout) x Cin (row (2 dy + dx) Cout + co), bias Cout bf16 bits or
+    None; returns batch x 2H x 2W x Cout fp64 (NHWC)."""
+    A = np.ascontiguousarray(A, dtype=np.float64)
+    B = np.ascontiguousarray(B, dtype=np.float64)
+    Cin = A.shape[1]
+    Cout = B.shape[0] // 4
+    assert A.shape[0] == batch * H * W and B.shape == (4 * Cout, Cin)
+    bias_arr = None if bias is None else np.ascontiguousarray(bias, dtype=np.uint16)
+    out = np.empty((batch, 2 * H, 2 * W, Cout), dtype=np.float64)
+    st = lib().orc_convt2x2(_ptr(A), _ptr(B), _ptr(bias_arr), batch, H, W, Cin, Cout, float(alpha),
+                            1 if gelu else 0, _ptr(out))
+    assert st == 0, st
+    return out

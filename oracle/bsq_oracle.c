@@ -69,6 +69,13 @@
  *       in one step, times a headroom factor H, gives the next step's scale without an extra
  *       pass; H = 32 for dY): g_next = fp32(fp32(amax_prev * H) / 2688), amax_prev the amax
  *       recorded by the previous NVFP4 quantization of the tensor.
+ *   R13 Head transposed convolutions ([LT] section 4.3: the head's two ScaleBlocks start with a
+ *       ConvT of kernel 2 and stride 2 that doubles the patch grid, and both ConvTs are quantized
+ *       GEMMs): out[b, 2h + dy, 2w + dx, co] = alpha * sum_ci A[(b, h, w), ci] * B[(2 dy + dx) *
+ *       C_out + co, ci] + bias[co], optionally GELU (the ScaleBlock's next step), A the NHWC
+ *       input as a (batch H W) x C_in operand, B the weight as a 4 C_out x C_in operand whose row
+ *       (2 dy + dx) C_out + co holds the kernel tap (dy, dx) of output channel co. Kernel and
+ *       stride 2 do not overlap, so every output pixel has exactly one input pixel.
  *
  * Pins (tests that tie this code to something other than itself) are in the test suite:
  * exhaustive decode tables against two independent float8/float4 libraries, encoders
@@ -756,4 +763,32 @@ int orc_quantize_nv_dual(const void* src, int src_f32, int64_t R, int64_t C, int
 float orc_delayed_global_scale(float amax_prev, float headroom) {
     float a = amax_prev * headroom; /* fp32 multiplication */
     return a / 2688.0f;             /* fp32 division */
+}
+
+/* Transposed convolution, kernel 2, stride 2 (reading R13), from decoded fp64 operands:
+ * A (batch*H*W) x Cin (NHWC input rows), B (4*Cout) x Cin, bias Cout bf16 bits (may be NULL),
+ * out batch x 2H x 2W x Cout fp64, written by the definition one output pixel at a time. */
+int orc_convt2x2(const double* A, const double* B, const uint16_t* bias, int64_t batch, int64_t H, int64_t W,
+                 int64_t Cin, int64_t Cout, double alpha, int gelu, double* out) {
+    int64_t b;
+    if (!A || !B || !out || batch <= 0 || H <= 0 || W <= 0 || Cin <= 0 || Cout <= 0) return ORC_ERR_ARG;
+#pragma omp parallel for schedule(static)
+    for (b = 0; b < batch; ++b) {
+        int64_t ho, wo, co, ci;
+        for (ho = 0; ho < 2 * H; ++ho) {
+            for (wo = 0; wo < 2 * W; ++wo) {
+                const int64_t h = ho / 2, dy = ho % 2, w = wo / 2, dx = wo % 2;
+                const double* a = A + ((b * H + h) * W + w) * Cin;
+                double* o = out + ((b * 2 * H + ho) * 2 * W + wo) * Cout;
+                for (co = 0; co < Cout; ++co) {
+                    const double* wt = B + ((2 * dy + dx) * Cout + co) * Cin;
+                    double acc = 0.0, v;
+                    for (ci = 0; ci < Cin; ++ci) acc += a[ci] * wt[ci];
+                    v = alpha * acc + (bias ? (double)orc_bf16_to_f32(bias[co]) : 0.0);
+                    o[co] = gelu ? 0.5 * v * erfc(-v / sqrt(2.0)) : v;
+                }
+            }
+        }
+    }
+    return ORC_OK;
 }
