@@ -140,9 +140,18 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------------------- oracle timing
+def _sample_rows(g, rows: int) -> int:
+    """Rows of A the oracle sample takes: for a transposed convolution whole image rows of the
+    first frame (a sub-image: kernel = stride = 2 has no halo)."""
+    if g.convt is not None:
+        return max(g.convt[2], min(rows, g.convt[1] * g.convt[2]) // g.convt[2] * g.convt[2])
+    return rows
+
+
 def _oracle_linear_rows(g, rows: int) -> float:
     import oracle
 
+    rows = _sample_rows(g, rows)
     a = make_activations(g, rows=rows) if g.a_dist != "normal_outlier50" else make_activations(g)
     b = make_weights(g)
     bias = make_bias(g)
@@ -150,7 +159,10 @@ def _oracle_linear_rows(g, rows: int) -> float:
     qa = oracle.quantize(g.fmt, a)
     qb = oracle.quantize(g.fmt, b)
     alpha = qa.g * qb.g if qa.fmt == oracle.NVFP4 else 1.0
-    oracle.gemm(qa.decode(), qb.decode(), bias, alpha, want_abs=False)
+    if g.convt is not None:
+        oracle.convt2x2(qa.decode(), qb.decode(), bias, 1, rows // g.convt[2], g.convt[2], alpha, gelu=True)
+    else:
+        oracle.gemm(qa.decode(), qb.decode(), bias, alpha, want_abs=False)
     return time.perf_counter() - t0
 
 
@@ -203,14 +215,19 @@ def cpu_oracle_sample(gemms, target_s: float = 10.0):
         rows = g.M
         if g.a_dist != "normal_outlier50":
             # t(R) = fixed (all of B) + R * per_row
-            t32, t160 = _oracle_linear_rows(g, 32), _oracle_linear_rows(g, 160)
-            per_row = max((t160 - t32) / 128.0, 1e-9)
-            fixed = max(t32 - 32 * per_row, 0.0)
+            r1, r2 = _sample_rows(g, 32), _sample_rows(g, 160)
+            if r2 == r1:
+                r2 = _sample_rows(g, 2 * r1)
+            t1, t2 = _oracle_linear_rows(g, r1), _oracle_linear_rows(g, r2)
+            per_row = max((t2 - t1) / max(r2 - r1, 1), 1e-9)
+            fixed = max(t1 - r1 * per_row, 0.0)
             rows = int(min(g.M, max(32, (target_s / len(gemms) - fixed) / per_row)))
+        rows = _sample_rows(g, rows)
         secs += _oracle_linear_rows(g, rows)
         flops += 2 * rows * g.N * g.K
         parts.append("%s: %d of %d rows" % (g.name, rows, g.M))
-    desc = "oracle quantize (R rows of A, all of B) + decode + fp64 GEMM of R rows; " + ", ".join(parts)
+    desc = ("oracle quantize (R rows of A, all of B) + decode + fp64 GEMM of R rows (transposed convolutions: "
+            "the sub-image of those rows, by definition); " + ", ".join(parts))
     return flops / secs / 1e12, secs, oracle.num_threads(), desc
 
 
@@ -330,14 +347,20 @@ def run_gpu(args, rank: int, world: int):
                 return {"a": torch.empty_like(hosts["a"], device=dev), "b": torch.empty_like(hosts["b"], device=dev),
                         "bias": torch.empty_like(hosts["bias"], device=dev) if hosts["bias"] is not None else None,
                         "qa": bsq.empty_qtensor(g.fmt, g.M, g.K, dev), "qb": bsq.empty_qtensor(g.fmt, g.N, g.K, dev),
-                        "out": torch.empty((g.M, g.N), dtype=torch.bfloat16, device=dev)}
+                        "out": torch.empty((g.M, g.N) if g.convt is None else
+                                           (g.convt[0], 2 * g.convt[1], 2 * g.convt[2], g.N // 4),
+                                           dtype=torch.bfloat16, device=dev)}
 
             def quant(D, s, g=g):
                 # activations and weights of the layer in one launch (bsq_quantize_batch)
                 bsq.quantize_many(g.fmt, [D["a"], D["b"]], outs=[D["qa"], D["qb"]], stream=s)
 
-            def gemm(D, s):
-                bsq.gemm(D["qa"], D["qb"], D["bias"], out=D["out"], stream=s)
+            def gemm(D, s, g=g):
+                if g.convt is not None:  # head transposed convolution, GELU fused (the ScaleBlock)
+                    b_, h_, w_ = g.convt
+                    bsq.convt2x2(D["qa"], D["qb"], b_, h_, w_, bias=D["bias"], gelu=True, out=D["out"], stream=s)
+                else:
+                    bsq.gemm(D["qa"], D["qb"], D["bias"], out=D["out"], stream=s)
 
             units.append({"hosts": hosts, "alloc": alloc, "quant": quant, "gemm": gemm, "fmt": g.fmt,
                           "flops": g.flops, "launches": 2 + (2 if g.fmt == NVFP4 else 0),

@@ -58,6 +58,8 @@ _lib.bsq_quantize_dual.argtypes = [_int, _vp, _i64, _i64, ctypes.c_uint64, _vp, 
 _lib.bsq_quantize_dual.restype = _int
 _lib.bsq_delayed_global_scale.argtypes = [_vp, _i64, _i64, ctypes.c_float, _vp, _vp]
 _lib.bsq_delayed_global_scale.restype = _int
+_lib.bsq_convt2x2.argtypes = [_int, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, _int, _vp]
+_lib.bsq_convt2x2.restype = _int
 _lib.bsq_gemm.argtypes = [_int, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp]
 _lib.bsq_gemm_gelu.restype = _int
 _lib.bsq_gemm_gelu.argtypes = [_int, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp]
@@ -73,7 +75,7 @@ _lib.bsq_strerror.argtypes = [_int]
 
 EXPORTS = ("bsq_codes_bytes", "bsq_scales_bytes", "bsq_quantize", "bsq_quantize_batch", "bsq_layernorm_quantize",
            "bsq_quantize_dual", "bsq_delayed_global_scale", "bsq_gemm",
-           "bsq_gemm_gelu", "bsq_gemm_gelu_quantize", "bsq_get_device_status", "bsq_selftest_timeout",
+           "bsq_gemm_gelu", "bsq_gemm_gelu_quantize", "bsq_convt2x2", "bsq_get_device_status", "bsq_selftest_timeout",
            "bsq_last_error", "bsq_strerror")
 
 Ptr = Union[int, None, torch.Tensor]
@@ -166,6 +168,12 @@ def bsq_gemm_gelu_quantize(fmt, A: Ptr, A_scales: Ptr, B: Ptr, B_scales: Ptr, bi
                            out_scales: Ptr, M: int, N: int, K: int, stream=None) -> int:
     return int(_lib.bsq_gemm_gelu_quantize(_fmt(fmt), _p(A), _p(A_scales), _p(B), _p(B_scales), _p(bias),
                                            _fmt(out_fmt), _p(out_codes), _p(out_scales), M, N, K, _stream(stream)))
+
+
+def bsq_convt2x2(fmt, A: Ptr, A_scales: Ptr, B: Ptr, B_scales: Ptr, bias: Ptr, out: Ptr, batch: int, H: int, W: int,
+                 C_in: int, C_out: int, gelu: bool = False, stream=None) -> int:
+    return int(_lib.bsq_convt2x2(_fmt(fmt), _p(A), _p(A_scales), _p(B), _p(B_scales), _p(bias), _p(out), batch, H, W,
+                                 C_in, C_out, 1 if gelu else 0, _stream(stream)))
 
 
 def bsq_get_device_status(stream=None) -> int:
@@ -366,6 +374,21 @@ def linear_backward(dy: torch.Tensor, x_col: QTensor, w_col: QTensor, stochastic
     quantize_dual (K x M and K x N). Returns (dX, dW)."""
     dy_row, dy_col = quantize_dual(x_col.fmt, dy, stochastic=stochastic, seed=seed, stream=stream)
     return gemm(dy_row, w_col, stream=stream), gemm(dy_col, x_col, stream=stream)
+
+
+def convt2x2(qx: QTensor, qw: QTensor, batch: int, H: int, W: int, bias: Optional[torch.Tensor] = None,
+             gelu: bool = False, out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Kernel-2 stride-2 transposed convolution of a quantized NHWC input (batch*H*W x C_in) with a
+    quantized 4*C_out x C_in weight (row (2 dy + dx) C_out + co): batch x 2H x 2W x C_out bf16."""
+    assert qx.fmt == qw.fmt and qx.cols == qw.cols and qx.rows == batch * H * W and qw.rows % 4 == 0
+    C_in, C_out = qx.cols, qw.rows // 4
+    if out is None:
+        out = torch.empty((batch, 2 * H, 2 * W, C_out), dtype=torch.bfloat16, device=qx.codes.device)
+    rc = bsq_convt2x2(qx.fmt, qx.codes, qx.scales, qw.codes, qw.scales, bias, out, batch, H, W, C_in, C_out, gelu,
+                      stream)
+    if rc != OK:
+        raise BsqError(rc, "bsq_convt2x2")
+    return out
 
 
 def device_status(stream=None) -> int:

@@ -248,6 +248,22 @@ int bsq_gemm_gelu_quantize(int fmt, const void* A, const void* A_scales, const v
                      M, N, K, stream);
 }
 
+int bsq_convt2x2(int fmt, const void* A, const void* A_scales, const void* B, const void* B_scales,
+                 const void* bias_bf16, void* out_bf16, int64_t batch, int64_t H, int64_t W, int64_t C_in,
+                 int64_t C_out, int gelu, bsq_stream_t stream) {
+  if (batch <= 0 || H <= 0 || W <= 0 || C_in <= 0 || C_out <= 0) return fail(BSQ_ERR_ARG);
+  if (batch * H > INT32_MAX || batch * H * W > INT32_MAX || 4 * C_out > INT32_MAX) return fail(BSQ_ERR_SHAPE);
+  if (C_out % 32 != 0 || (32 % W != 0 && W % 32 != 0)) return fail(BSQ_ERR_SHAPE);
+  const int64_t M = batch * H * W, N = 4 * C_out;
+  const int st = check_gemm(fmt, A, A_scales, B, B_scales, bias_bf16, out_bf16, M, N, C_in);
+  if (st != BSQ_OK) return fail(st);
+  const bsq::DeviceInfo* dev = bsq::current_device();
+  if (dev == nullptr) return fail(BSQ_ERR_ARCH);
+  const int rc = bsq::launch_gemm(fmt, gelu ? 5 : 4, A, A_scales, B, B_scales, bias_bf16, out_bf16, nullptr, M, N,
+                                  C_in, reinterpret_cast<cudaStream_t>(stream), *dev, W);
+  return rc == BSQ_OK ? BSQ_OK : fail(rc);
+}
+
 int bsq_get_device_status(bsq_stream_t stream) {
   const bsq::DeviceInfo* dev = bsq::current_device();
   if (dev == nullptr) return fail(BSQ_ERR_ARCH);

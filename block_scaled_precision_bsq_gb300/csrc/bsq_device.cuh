@@ -186,6 +186,16 @@ __device__ __forceinline__ void tma_store_2d(const void* tmap, const void* smem_
                : "memory");
 }
 
+// 5-D tile store (coordinates innermost first).
+__device__ __forceinline__ void tma_store_5d(const void* tmap, const void* smem_src, int32_t c0, int32_t c1,
+                                             int32_t c2, int32_t c3, int32_t c4) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4, %5, %6}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(tmap)),
+      "r"(smem_u32(smem_src)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
+      : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
 __device__ __forceinline__ void bulk_wait_group_read0() {

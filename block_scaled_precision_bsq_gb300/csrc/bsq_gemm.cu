@@ -124,8 +124,11 @@ __host__ __device__ constexpr uint32_t make_idesc(uint32_t sf_id) {
 // bf16(GELU(v)) (the "fc1 + GELU" epilogue every stack of the "lightly-train - DINOv3 + EoMT on
 // RTX 5090" README fuses, section 4.3). kEpiGeluMxfp8 / kEpiGeluMxfp4: GELU(v) quantized along
 // the output row straight into MX codes and tiled scales, the fc2 operand (the MXFP8 stack's
-// fc1 epilogue, same section); bytes laid out as bsq_quantize writes them.
-enum EpiMode { kEpiBf16 = 0, kEpiGeluBf16 = 1, kEpiGeluMxfp8 = 2, kEpiGeluMxfp4 = 3 };
+// fc1 epilogue, same section); bytes laid out as bsq_quantize writes them. kEpiConvT /
+// kEpiConvTGelu: the head's kernel-2 stride-2 transposed convolution (same README section: the
+// ScaleBlocks' ConvT, then GELU): column n = (2 dy + dx) C_out + co of output row (b, h, w) is
+// stored at pixel (b, 2h + dy, 2w + dx), channel co, of the NHWC output, with bias[co].
+enum EpiMode { kEpiBf16 = 0, kEpiGeluBf16 = 1, kEpiGeluMxfp8 = 2, kEpiGeluMxfp4 = 3, kEpiConvT = 4, kEpiConvTGelu = 5 };
 
 // GELU(v) = v Phi(v) (the erf form) with Phi(v) = 1 - erfc(z) / 2 for v >= 0 and erfc(z) / 2
 // for v < 0, z = |v| / sqrt 2 (no cancellation in the negative tail), and erfc from
@@ -159,6 +162,7 @@ struct GemmArgs {
   int M, N;
   int tiles_n, num_pairs;
   int nk;  // stages per tile: K bytes / 128
+  int cv_c, cv_w;  // ConvT epilogues: output channels C_out, input width W
   int* status;
 };
 
@@ -343,8 +347,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int n = n0 + 4 * lane + i;
+        const int bn = (EPI == kEpiConvT || EPI == kEpiConvTGelu) ? n % args.cv_c : n;  // ConvT: per channel
         bias_s[4 * lane + i] =
-            (args.bias != nullptr && n < args.N) ? __uint_as_float(static_cast<uint32_t>(args.bias[n]) << 16) : 0.0f;
+            (args.bias != nullptr && n < args.N) ? __uint_as_float(static_cast<uint32_t>(args.bias[bn]) << 16) : 0.0f;
       }
       __syncwarp();
       if (!mbar_wait_bounded(tmem_full, acc_phase, abort_flag, args.status)) break;
@@ -367,7 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
           v = __fadd_rn(v, bias_s[c]);
         }
-        if constexpr (EPI != kEpiBf16) v = gelu_erf(v);
+        if constexpr (EPI != kEpiBf16 && EPI != kEpiConvT) v = gelu_erf(v);
         return v;
       };
       // quantized epilogues: all 128 values first (in place), one MX block per 32 columns (the
@@ -408,8 +413,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int row_units = (EPI == kEpiGeluMxfp4) ? (args.N >> 1) : args.N;  // TMA x extent of a row
 #pragma unroll
       for (int j = 0; j < kRowBytes / RB; ++j) {
+        constexpr bool kBf16Out = (EPI == kEpiBf16 || EPI == kEpiGeluBf16 || EPI == kEpiConvT || EPI == kEpiConvTGelu);
         int x;  // first TMA x coordinate of the chunk (bf16 elements or code bytes)
-        if constexpr (EPI == kEpiBf16 || EPI == kEpiGeluBf16) x = n0 + (RB / 2) * j;
+        if constexpr (kBf16Out) x = n0 + (RB / 2) * j;
         else if constexpr (EPI == kEpiGeluMxfp8) x = n0 + RB * j;
         else x = (n0 >> 1) + RB * j;
         if (x >= row_units || m0 >= args.M) break;  // nothing of this chunk is stored (warp-uniform)
@@ -419,7 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t packed[RB / 4];
 #pragma unroll
         for (int c = 0; c < RB / 4; ++c) {
-          if constexpr (EPI == kEpiBf16 || EPI == kEpiGeluBf16) {
+          if constexpr (kBf16Out) {
             const int col = (RB / 2) * j + 2 * c;  // two bf16 per word
             __nv_bfloat162 p = __floats2bfloat162_rn(value(col), value(col + 1));
             packed[c] = *reinterpret_cast<uint32_t*>(&p);
@@ -451,7 +457,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          tma_store_2d(&mapOut, stage_buf, x, m0);
+          if constexpr (EPI == kEpiConvT || EPI == kEpiConvTGelu) {
+            // the chunk's 32 output rows are tokens m0.. (whole image rows when W divides 32, a
+            // 32-token piece of one image row when 32 divides W); its columns one tap (dy, dx)
+            const int tap = x / args.cv_c, co = x - tap * args.cv_c;
+            const int bh = m0 / args.cv_w, w0 = m0 - bh * args.cv_w;
+            tma_store_5d(&mapOut, stage_buf, co, tap & 1, w0, tap >> 1, bh);
+          } else {
+            tma_store_2d(&mapOut, stage_buf, x, m0);
+          }
           bulk_commit_group();
         }
         ++nstores;
@@ -538,9 +552,27 @@ cudaLaunchConfig_t pair_launch_config(cudaLaunchAttribute* attr, int clusters, i
   return cfg;
 }
 
+// NHWC output of a kernel-2 stride-2 transposed convolution as a 5-D tensor (channel co, dx, w,
+// dy, b * H + h), one box = one epilogue chunk: EC channels of one tap for 32 tokens.
+bool make_map_convt_out(CUtensorMap* map, void* out, int64_t cout, int64_t W, int64_t BH, uint32_t ec,
+                        CUtensorMapSwizzle sw) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[5] = {static_cast<cuuint64_t>(cout), 2, static_cast<cuuint64_t>(W), 2,
+                              static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[4] = {static_cast<cuuint64_t>(cout) * 2, static_cast<cuuint64_t>(cout) * 4,
+                                 static_cast<cuuint64_t>(W * cout) * 4, static_cast<cuuint64_t>(W * cout) * 8};
+  const uint32_t wb = static_cast<uint32_t>(std::min<int64_t>(W, 32));
+  const cuuint32_t box[5] = {ec, 1, wb, 1, 32 / wb};
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, out, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int FMT, int EPI>
 int run_gemm(const void* A, const void* A_scales, const void* B, const void* B_scales, const void* bias, void* out,
-             void* out_scales, int64_t M, int64_t N, int64_t K, cudaStream_t stream, const DeviceInfo& dev) {
+             void* out_scales, int64_t M, int64_t N, int64_t K, int64_t cv_w, cudaStream_t stream,
+             const DeviceInfo& dev) {
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
   static int max_clusters = 0;
@@ -560,7 +592,9 @@ int run_gemm(const void* A, const void* A_scales, const void* B, const void* B_s
   constexpr int EC = Cfg<FMT>::kEpiCols;
   const CUtensorMapSwizzle osw = EC == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
   bool ok_out;
-  if constexpr (EPI == kEpiBf16 || EPI == kEpiGeluBf16) {
+  if constexpr (EPI == kEpiConvT || EPI == kEpiConvTGelu) {
+    ok_out = make_map_convt_out(&mOut, out, N / 4, cv_w, M / cv_w, EC, osw);
+  } else if constexpr (EPI == kEpiBf16 || EPI == kEpiGeluBf16) {
     ok_out = make_map_2d(&mOut, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, out, N, M, static_cast<uint64_t>(N) * 2, EC, 32, osw);
   } else {
     // code bytes of an output row: N (E4M3) or N / 2 (e2m1); staged rows of 2 * EC bytes
@@ -587,6 +621,8 @@ int run_gemm(const void* A, const void* A_scales, const void* B, const void* B_s
   a.tiles_n = static_cast<int>(ceil_div(N, BN));
   a.num_pairs = static_cast<int>(ceil_div(ceil_div(M, BM), 2)) * a.tiles_n;
   a.nk = static_cast<int>(kbytes / kChunkBytes);
+  a.cv_c = static_cast<int>(N / 4);
+  a.cv_w = static_cast<int>(cv_w);
   a.status = dev.status;
   const int clusters = std::min(a.num_pairs, std::min(max_clusters, dev.num_sms / 2));
 
@@ -599,34 +635,33 @@ int run_gemm(const void* A, const void* A_scales, const void* B, const void* B_s
 
 template <int FMT>
 int run_gemm_epi(int epi, const void* A, const void* A_scales, const void* B, const void* B_scales, const void* bias,
-                 void* out, void* out_scales, int64_t M, int64_t N, int64_t K, cudaStream_t stream,
+                 void* out, void* out_scales, int64_t M, int64_t N, int64_t K, int64_t cv_w, cudaStream_t stream,
                  const DeviceInfo& dev) {
+#define BSQ_RUN(E) run_gemm<FMT, E>(A, A_scales, B, B_scales, bias, out, out_scales, M, N, K, cv_w, stream, dev)
   switch (epi) {
-    case kEpiBf16:
-      return run_gemm<FMT, kEpiBf16>(A, A_scales, B, B_scales, bias, out, out_scales, M, N, K, stream, dev);
-    case kEpiGeluBf16:
-      return run_gemm<FMT, kEpiGeluBf16>(A, A_scales, B, B_scales, bias, out, out_scales, M, N, K, stream, dev);
-    case kEpiGeluMxfp8:
-      return run_gemm<FMT, kEpiGeluMxfp8>(A, A_scales, B, B_scales, bias, out, out_scales, M, N, K, stream, dev);
-    case kEpiGeluMxfp4:
-      return run_gemm<FMT, kEpiGeluMxfp4>(A, A_scales, B, B_scales, bias, out, out_scales, M, N, K, stream, dev);
-    default:
-      return BSQ_ERR_ARG;
+    case kEpiBf16: return BSQ_RUN(kEpiBf16);
+    case kEpiGeluBf16: return BSQ_RUN(kEpiGeluBf16);
+    case kEpiGeluMxfp8: return BSQ_RUN(kEpiGeluMxfp8);
+    case kEpiGeluMxfp4: return BSQ_RUN(kEpiGeluMxfp4);
+    case kEpiConvT: return BSQ_RUN(kEpiConvT);
+    case kEpiConvTGelu: return BSQ_RUN(kEpiConvTGelu);
+    default: return BSQ_ERR_ARG;
   }
+#undef BSQ_RUN
 }
 
 }  // namespace
 
 int launch_gemm(int fmt, int epi, const void* A, const void* A_scales, const void* B, const void* B_scales,
                 const void* bias, void* out, void* out_scales, int64_t M, int64_t N, int64_t K, cudaStream_t stream,
-                const DeviceInfo& dev) {
+                const DeviceInfo& dev, int64_t convt_w) {
   switch (fmt) {
     case BSQ_MXFP8:
-      return run_gemm_epi<BSQ_MXFP8>(epi, A, A_scales, B, B_scales, bias, out, out_scales, M, N, K, stream, dev);
+      return run_gemm_epi<BSQ_MXFP8>(epi, A, A_scales, B, B_scales, bias, out, out_scales, M, N, K, convt_w, stream, dev);
     case BSQ_NVFP4:
-      return run_gemm_epi<BSQ_NVFP4>(epi, A, A_scales, B, B_scales, bias, out, out_scales, M, N, K, stream, dev);
+      return run_gemm_epi<BSQ_NVFP4>(epi, A, A_scales, B, B_scales, bias, out, out_scales, M, N, K, convt_w, stream, dev);
     case BSQ_MXFP4:
-      return run_gemm_epi<BSQ_MXFP4>(epi, A, A_scales, B, B_scales, bias, out, out_scales, M, N, K, stream, dev);
+      return run_gemm_epi<BSQ_MXFP4>(epi, A, A_scales, B, B_scales, bias, out, out_scales, M, N, K, convt_w, stream, dev);
     default:
       return BSQ_ERR_ARG;
   }

@@ -70,10 +70,11 @@ int launch_quantize_dual(int fmt, bool src_f32, bool stochastic, bool global_giv
                          void* col_scales, float* global_scale, cudaStream_t stream, const DeviceInfo& dev);
 
 // epi: 0 bf16 out, 1 GELU -> bf16, 2 GELU -> MXFP8 codes + scales, 3 GELU -> MXFP4 (out_scales
-// used by 2 and 3 only).
+// used by 2 and 3 only), 4 / 5 kernel-2 stride-2 transposed convolution to NHWC bf16 (without /
+// with GELU; N = 4 C_out, M = batch H W, convt_w = W).
 int launch_gemm(int fmt, int epi, const void* A, const void* A_scales, const void* B, const void* B_scales,
                 const void* bias, void* out, void* out_scales, int64_t M, int64_t N, int64_t K, cudaStream_t stream,
-                const DeviceInfo& dev);
+                const DeviceInfo& dev, int64_t convt_w = 1);
 
 int launch_selftest_timeout(int64_t limit_ns, cudaStream_t stream, const DeviceInfo& dev);
 

@@ -245,6 +245,32 @@ int bsq_gemm_gelu_quantize(int fmt, const void* A, const void* A_scales, const v
                            int64_t N, int64_t K, bsq_stream_t stream);
 
 /*
+ * bsq_convt2x2: the head's transposed convolution with kernel 2 and stride 2 as a block-scaled
+ * GEMM ("lightly-train - DINOv3 + EoMT on RTX 5090" README, section 4.3: the head's two
+ * ScaleBlocks (ConvT k2 s2 -> GELU -> depthwise 3x3 -> LN2D) upscale the patch grid, and ConvT1 /
+ * ConvT2 are two of the six quantized GEMM classes). Kernel = stride = 2: every output pixel has
+ * exactly one input pixel, so
+ *   out[b, 2h + dy, 2w + dx, co] = bf16(alpha * sum_ci Ahat[(b, h, w), ci] * Bhat[(2 dy + dx) C_out + co, ci]
+ *                                       + bias[co])        (GELU of it when gelu != 0)
+ * is one GEMM with N = 4 C_out whose epilogue stores each output column at its output pixel.
+ *   A, A_scales  the NHWC input, batch * H * W rows (tokens in (b, h, w) order) x C_in, as written
+ *                by bsq_quantize(fmt, ..., batch * H * W, C_in, ...)
+ *   B, B_scales  the weight as a 4 C_out x C_in operand: row (2 dy + dx) C_out + co holds tap
+ *                (dy, dx) of output channel co, i.e. W_torch[ci, co, dy, dx] of a PyTorch
+ *                ConvTranspose2d weight [C_in, C_out, 2, 2]
+ *   bias_bf16    C_out bf16 values or NULL
+ *   out_bf16     batch x 2H x 2W x C_out bf16 (NHWC), written
+ *   alpha        as bsq_gemm (NVFP4: g_A * g_B from the scale tails)
+ * GELU is the erf form evaluated as in bsq_gemm_gelu.
+ * Shapes: C_in as bsq_gemm's K (multiple of 128 MXFP8, 256 FP4); C_out % 32 == 0; W divides 32
+ * or 32 divides W (so that 32 consecutive tokens are whole image rows or part of one); batch *
+ * H * W below 2^31. Otherwise BSQ_ERR_SHAPE. Errors: as bsq_gemm.
+ */
+int bsq_convt2x2(int fmt, const void* A, const void* A_scales, const void* B, const void* B_scales,
+                 const void* bias_bf16, void* out_bf16, int64_t batch, int64_t H, int64_t W, int64_t C_in,
+                 int64_t C_out, int gelu, bsq_stream_t stream);
+
+/*
  * bsq_get_device_status: synchronise `stream`, then read and clear the current device's
  * status word. Returns BSQ_OK, BSQ_ERR_TIMEOUT (a kernel's bounded wait on an mbarrier
  * gave up; that kernel returned early and its outputs are incomplete) or BSQ_ERR_LAUNCH

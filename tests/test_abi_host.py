@@ -94,6 +94,13 @@ def test_argument_errors_before_any_cuda_call(bsq):
     assert bsq.bsq_gemm(bsq.MXFP8, p, p + 4, p, p, None, p, 128, 256, 256) == bsq.ERR_ALIGN
     assert bsq.bsq_gemm(bsq.MXFP8, p, p, p, p, p + 1, p, 128, 256, 256) == bsq.ERR_ALIGN
     assert bsq.bsq_selftest_timeout(10, None) == bsq.ERR_ARG
+    cv = bsq.bsq_convt2x2
+    assert cv(bsq.MXFP8, p, p, p, p, None, p, 0, 4, 4, 128, 64) == bsq.ERR_ARG           # batch
+    assert cv(bsq.MXFP8, p, p, p, p, None, p, 1, 4, 4, 128, 48) == bsq.ERR_SHAPE         # C_out % 32
+    assert cv(bsq.MXFP8, p, p, p, p, None, p, 1, 4, 48, 128, 64) == bsq.ERR_SHAPE        # W vs 32
+    assert cv(bsq.MXFP8, p, p, p, p, None, p, 1, 4, 4, 96, 64) == bsq.ERR_SHAPE          # C_in % 128
+    assert cv(bsq.NVFP4, p, p, p, p, None, p, 1, 4, 4, 128, 64) == bsq.ERR_SHAPE         # C_in % 256
+    assert cv(bsq.MXFP8, p, p + 4, p, p, None, p, 1, 4, 4, 128, 64) == bsq.ERR_ALIGN
     ds = bsq.bsq_delayed_global_scale
     assert ds(None, 64, 64, 32.0, p) == bsq.ERR_ARG
     assert ds(p, 64, 64, 0.0, p) == bsq.ERR_ARG                                    # headroom

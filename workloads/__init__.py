@@ -22,6 +22,10 @@ quantized GEMMs are qkv / proj / fc1 / fc2 of every ViT block):
                   one training step of the ViT-B/16 fc1 layer at training shape: forward,
                   dgrad (dX = dY W) and wgrad (dW = dY^T X), every operand from the dual-layout
                   quantizer; the output gradient dY rounded to nearest or stochastically.
+  eomt_head_vitl_mxfp8
+                  the head's two transposed convolutions (kernel 2, stride 2, ConvT -> GELU of
+                  the ScaleBlocks): 32x32 -> 64x64 and 64x64 -> 128x128 grids of a 512x512 frame
+                  (ViT-L/16: 1024 channels in and out), a batch of 8 frames.
   vitb_fc1_nvfp4_train_sr
                   the same step in NVFP4 (the README's FP4 training path): X and W with their
                   own per-tensor scales, dY stochastically rounded with the delayed scale of
@@ -76,6 +80,9 @@ class Gemm:
     w_std: float = 0.02
     bias_std: Optional[float] = 0.01  # None = zero bias
     seed: int = 0
+    # head transposed convolution (kernel 2, stride 2): (batch, H, W) of the NHWC input; then
+    # M = batch H W tokens, K = C_in, N = 4 C_out (weight rows (2 dy + dx) C_out + co), bias C_out
+    convt: Optional[tuple] = None
 
     @property
     def flops(self) -> int:
@@ -157,6 +164,12 @@ for _sr in (False, True):
         _n, "ViT-B/16 MLP fc1 training step (forward, dgrad, wgrad) at M=14336, K=768, N=3072, MXFP8, "
             "dual-layout operands, output gradient rounded %s" % ("stochastically" if _sr else "to nearest even"),
         [Gemm("fc1", MXFP8, 14 * 1024, 768, 3072)], "train", _sr)
+WORKLOADS["eomt_head_vitl_mxfp8"] = Workload(
+    "eomt_head_vitl_mxfp8",
+    "EoMT head transposed convolutions (k2 s2, GELU fused) of ViT-L/16 on 512x512 frames, batch 8, MXFP8: "
+    "ConvT1 32x32 -> 64x64, ConvT2 64x64 -> 128x128, 1024 channels",
+    [Gemm("convt1", MXFP8, 8 * 32 * 32, 1024, 4 * 1024, convt=(8, 32, 32)),
+     Gemm("convt2", MXFP8, 8 * 64 * 64, 1024, 4 * 1024, convt=(8, 64, 64))])
 WORKLOADS["vitb_fc1_nvfp4_train_sr"] = Workload(
     "vitb_fc1_nvfp4_train_sr",
     "ViT-B/16 MLP fc1 training step (forward, dgrad, wgrad) at M=14336, K=768, N=3072, NVFP4, dual-layout "
@@ -219,11 +232,12 @@ def make_output_grad(g: Gemm, rows: Optional[int] = None, std: float = 1e-3) -> 
 
 
 def make_bias(g: Gemm) -> Optional[np.ndarray]:
-    """bias[N] as uint16 bf16 bits, or None for a zero bias."""
+    """bias[N] (bias[C_out] for a transposed convolution) as uint16 bf16 bits, or None."""
     if g.bias_std is None:
         return None
     rng = np.random.default_rng(g.seed + 2)
-    return f32_to_bf16_bits((rng.standard_normal(g.N) * g.bias_std).astype(np.float32))
+    n = g.N // 4 if g.convt is not None else g.N
+    return f32_to_bf16_bits((rng.standard_normal(n) * g.bias_std).astype(np.float32))
 
 
 def random_matrix(rows: int, cols: int, seed: int, std: float = 1.0, dist: str = "normal",
