@@ -420,8 +420,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         else x = (n0 >> 1) + RB * j;
         if (x >= row_units || m0 >= args.M) break;  // nothing of this chunk is stored (warp-uniform)
         uint8_t* stage_buf = stage_base + (nstores % NB) * L::kEpiChunkBytes;
-        if (lane == 0) bulk_wait_group_read<NB - 1>();  // the store that last used this buffer has read it
-        __syncwarp();
         uint32_t packed[RB / 4];
 #pragma unroll
         for (int c = 0; c < RB / 4; ++c) {
@@ -445,6 +443,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             packed[c] = cvt_e2m1x8(y);
           }
         }
+        // the chunk's values are computed above while the store that last used this buffer may
+        // still be reading it; wait for that read only now
+        if (lane == 0) bulk_wait_group_read<NB - 1>();
+        __syncwarp();
         // row `lane` of the 32 x RB chunk in 16-byte pieces; the TMA swizzle (64B or 32B mode)
         // XORs the piece index with address bits 7.. so that a quarter-warp hits distinct banks
 #pragma unroll
