@@ -132,28 +132,37 @@ __device__ __forceinline__ uint32_t sr_code(float y, float x, uint32_t r) {
   const uint32_t yb = __float_as_uint(y);
   const uint32_t b = yb & 0x7FFFFFFFu;
   uint32_t mag;
-  if (b >= (kEminB << 23)) {
-    // q's fraction is the low D mantissa bits t: up iff t > r >> (32 - D), i.e. iff
-    // t + (2^D - 1 - (r >> (32 - D))) carries into the kept bits; the carry may move to the
-    // next binade, which is the next grid point
-    // (~r) >> (32 - D) = 2^D - 1 - (r >> (32 - D)); the exponent re-bias folds into the same add
-    mag = (b + ((1u << D) - 1u - ((kEminB - 1u) << 23)) - (r >> (32u - D))) >> D;
-  } else {
-    // subnormal target: q = sig / 2^sh, sig the 24-bit significand of |y|
+  // normal target binade: q's fraction is the low D mantissa bits t: up iff t > r >> (32 - D), i.e.
+  // iff t + (2^D - 1 - (r >> (32 - D))) carries into the kept bits; the carry may move to the next
+  // binade, which is the next grid point. (~r) >> (32 - D) = 2^D - 1 - (r >> (32 - D)), and the
+  // exponent re-bias folds into the same add.
+  auto normal_mag = [&]() { return (b + ((1u << D) - 1u - ((kEminB - 1u) << 23)) - (r >> (32u - D))) >> D; };
+  // subnormal target: q = sig / 2^sh, sig the 24-bit significand of |y|. sh <= 24: the same carry
+  // trick on the significand. sh > 24: q < 2^(24 - sh) <= 1/2 and up iff (r >> 8) <
+  // ceil(sig / 2^(sh - 24)), the shift capped at 24 (past it the ceiling is 1 for any positive
+  // sig). A y that underflowed to 0 from x != 0 is a positive value below every grid step and
+  // counts as sig = 1.
+  auto subnormal_mag = [&]() {
     const uint32_t e = b >> 23;
     uint32_t sig = e ? ((b & 0x7FFFFFu) | 0x800000u) : b;
+    if (b == 0u && x != 0.0f) sig = 1u;
     const uint32_t sh = D + kEminB - max(e, 1u);  // > D
-    if (sh <= 24u) {
-      // the same carry trick on the significand, kept bits above sh
-      mag = (sig + ((~r) >> (32u - sh))) >> sh;
-    } else {
-      // q < 2^(24 - sh) <= 1/2: up iff (r >> 8) < ceil(sig / 2^(sh - 24)); past a shift of 24
-      // that ceiling is 1 for every positive sig. A y that underflowed to 0 from x != 0 is a
-      // positive value below every grid step and counts as sig = 1.
-      if (b == 0u && x != 0.0f) sig = 1u;
-      const uint32_t k = min(sh - 24u, 24u);
-      mag = (r >> 8) < ((sig + (1u << k) - 1u) >> k) ? 1u : 0u;
-    }
+    const uint32_t sa = min(sh, 24u);
+    const uint32_t mag_a = (sig + ((~r) >> (32u - sa))) >> sa;
+    const uint32_t k = min(max(sh, 24u) - 24u, 24u);
+    const uint32_t mag_b = (r >> 8) < ((sig + (1u << k) - 1u) >> k) ? 1u : 0u;
+    return sh <= 24u ? mag_a : mag_b;
+  };
+  if constexpr (FMT == BSQ_MXFP8) {
+    // E4M3: values in the subnormal range are rare (a block's maximum sits 2^14 above it), so the
+    // branch is almost always warp-uniform
+    if (b < (kEminB << 23)) mag = subnormal_mag();
+    else mag = normal_mag();
+  } else {
+    // e2m1: |v| < 1 (the format's subnormal range) is common, so both forms are computed and
+    // selected instead of diverging
+    const uint32_t mn = normal_mag(), ms = subnormal_mag();
+    mag = b >= (kEminB << 23) ? mn : ms;
   }
   // from the largest finite value up the magnitude is at least kMaxCode; below it, at most
   mag = min(mag, kMaxCode);
