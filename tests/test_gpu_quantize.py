@@ -139,3 +139,52 @@ def test_batch_nvfp4_given_scales():
         o = oracle.quantize("nvfp4", x_np, global_scale=g)
         assert np.array_equal(q.codes.cpu().numpy(), o.codes)
         assert np.array_equal(q.scales.cpu().numpy(), o.tiled_scales())
+
+
+def _nudge(v, k):
+    """The float32 k ulps above (k > 0) or below v."""
+    v = np.float32(v)
+    for _ in range(abs(k)):
+        v = np.nextafter(v, np.float32(np.inf if k > 0 else -np.inf))
+    return v
+
+
+def _boundary_blocks(g32, seed):
+    """16 x 64 fp32: every 16-element block starts with its maximum amax = 6 s g (fixing the
+    block scale s), the other 15 elements have quotients x / (s g) on or within 3 ulps of the
+    e2m1 rounding boundaries."""
+    rng = np.random.default_rng(seed)
+    pairs = [(m, k) for m in (0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0) for k in range(-3, 4)]
+    rows = []
+    for r in range(16):
+        row = []
+        for b in range(4):
+            s_target = float(rng.choice([0.875, 1.125, 1.375, 3.25, 13.0, 0.3125]))
+            amax = np.float32(6.0 * s_target * g32)
+            sc = np.float32(oracle.decode_e4m3(oracle.encode_e4m3(float(amax / np.float32(np.float32(6.0) * np.float32(g32))))))
+            sg = np.float32(sc * np.float32(g32))
+            block = [amax]
+            for j in range(15):
+                m, k = pairs[(r * 60 + b * 15 + j) % len(pairs)]
+                block.append(_nudge(np.float32(np.float32(m) * sg), k))
+            signs = rng.choice([-1.0, 1.0], size=16).astype(np.float32)
+            signs[0] = 1.0
+            row.extend(np.array(block, dtype=np.float32) * signs)
+        rows.append(row)
+    return np.array(rows, dtype=np.float32)
+
+
+@pytest.mark.parametrize("g", [1.0 / 3.0, 0.0123, 7.77])
+def test_nvfp4_quotients_at_rounding_boundaries(g):
+    """Element quotients x / (s g) exactly on, and within three ulps of, every e2m1 rounding
+    boundary (0.25 ... 5): the codes must follow the IEEE quotient, which a reciprocal-multiply
+    alone would not get right there. The quantizer and the dual-layout quantizer (row layout)
+    against the oracle, with the per-tensor scale given."""
+    bsq = _bsq()
+    g32 = float(np.float32(g))
+    x = _boundary_blocks(g32, seed=int(g * 1000))
+    _compare("nvfp4", x, global_scale=g32, label="boundaries g=%g" % g)
+    xd = np.concatenate([x, x], axis=0)  # 32 rows for the dual kernel
+    qr, _ = oracle.quantize_dual("nvfp4", xd, global_scale=g32)
+    gr, _ = bsq.quantize_dual("nvfp4", to_dev(xd), global_scale=torch.tensor([g32], device="cuda"))
+    assert np.array_equal(gr.codes.cpu().numpy(), qr.codes)
