@@ -22,7 +22,8 @@
 // ((r / 32) % 4) * 4), the lane of a row's last block also zeroing the padding columns of that
 // 4-column group. Scale bytes of the padding rows of the last row tile are written as zeros by
 // the kernel itself. (A lane-per-16-elements version with shuffles for the block maxima spent
-// ~14 instructions per element against ~12 here.)
+// ~14 instructions per element against ~10 here.) In LayerNorm mode each warp instead owns whole
+// rows of a chunk: the row's statistics, then its affine step and quantization.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -179,10 +180,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) quantize_kernel(const __
   uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(q_smem_raw) + 127) & ~uintptr_t(127));
   __shared__ uint64_t full_bar[kRing], empty_bar[kRing];
   __shared__ int abort_flag;
-  // LayerNorm mode: row mean / rstd of a chunk (double-buffered by chunk parity) and, per
-  // parity, a barrier the consumer warps pass once the chunk's statistics are written
-  __shared__ float ln_stats[LN ? 4 * kLnMaxRows : 1];
-  __shared__ uint64_t ln_bar[2];
   const uint32_t warp = threadIdx.x >> 5;
   const uint32_t lane = threadIdx.x & 31u;
 
@@ -191,8 +188,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) quantize_kernel(const __
       mbar_init(&full_bar[i], 1);
       mbar_init(&empty_bar[i], kConsumerWarps);
     }
-    mbar_init(&ln_bar[0], kConsumerWarps);
-    mbar_init(&ln_bar[1], kConsumerWarps);
     abort_flag = 0;
     fence_mbar_init();
   }
@@ -256,9 +251,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) quantize_kernel(const __
     uint32_t lead = static_cast<uint32_t>(cw);
     int stage = 0;
     uint32_t phase = 0;
-    uint32_t ln_phase = 0;  // bit p: phase of ln_bar[p]
-    uint32_t it = 0;        // chunk iteration of this CTA
-    for (int64_t c = blockIdx.x; c < nchunks; c += gridDim.x, ++it) {
+    for (int64_t c = blockIdx.x; c < nchunks; c += gridDim.x) {
       if (!mbar_wait_bounded_warp(&full_bar[stage], phase, &abort_flag, batch.status)) break;
       int64_t local;
       const int t = chunk_owner(c, local);
@@ -292,22 +285,24 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) quantize_kernel(const __
       int64_t r0, nr, c0, nc;
       chunk_geom(a, local, r0, nr, c0, nc);
       const uint8_t* buf = ring + stage * kChunkMax;
-      // the chunk as one flat array of nr * nc elements; lane piece f = 16 elements
+      // the chunk as one flat array of nr * nc elements; lane piece f = 32 elements
       const uint32_t flat = static_cast<uint32_t>(nr * nc);
       const uint64_t elem0 = static_cast<uint64_t>(r0) * static_cast<uint64_t>(a.cols) + static_cast<uint64_t>(c0);
       const uint32_t steps = (flat + kSeg - 1) / kSeg;
-      const uint32_t pb = it & 1u;
       if constexpr (LN) {
-        // phase 1: mean and rstd of the chunk's rows (whole rows: c0 = 0, nc = cols), one warp
-        // per row, two passes over the row in shared memory, fp32, butterfly warp sums
+        // LayerNorm mode (whole rows, MX formats): each warp owns whole rows of the chunk, dealt
+        // round-robin over the CTA's chunks like the warp steps below (`lead` is this warp's first
+        // row here): the row's mean and rstd (fp32, two passes over the row in shared memory,
+        // butterfly warp sums), then y = (x - mean) * rstd * gamma + beta and the quantization of
+        // the row, 32 columns per lane -- no barrier between the warps
         const int nci = static_cast<int>(nc);
         const int pieces = nci * kEsize / 16;  // 16-byte pieces of a row
-        for (int rr = cw; rr < static_cast<int>(nr); rr += kConsumerWarps) {
-          const uint4* rowp = reinterpret_cast<const uint4*>(buf + static_cast<size_t>(rr) * nci * kEsize);
+        for (uint32_t rr = lead; rr < static_cast<uint32_t>(nr); rr += kConsumerWarps) {
+          const uint8_t* rowp = buf + static_cast<size_t>(rr) * nci * kEsize;
           auto piece_sum = [&](float mean, bool sq) {
             float acc_s = 0.0f;
             for (int q = static_cast<int>(lane); q < pieces; q += 32) {
-              const uint4 v = rowp[q];
+              const uint4 v = reinterpret_cast<const uint4*>(rowp)[q];
               const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
               for (int i = 0; i < 4; ++i) {
@@ -326,97 +321,114 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) quantize_kernel(const __
           };
           const float mean = __fdiv_rn(piece_sum(0.0f, false), static_cast<float>(nci));
           const float var = __fdiv_rn(piece_sum(mean, true), static_cast<float>(nci));
-          if (lane == 0) {
-            ln_stats[(2 * pb) * kLnMaxRows + rr] = mean;
-            ln_stats[(2 * pb + 1) * kLnMaxRows + rr] = __fdiv_rn(1.0f, __fsqrt_rn(var + a.eps));
-          }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&ln_bar[pb]);
-        if (!mbar_wait_bounded_warp(&ln_bar[pb], (ln_phase >> pb) & 1u, &abort_flag, batch.status)) break;
-        ln_phase ^= 1u << pb;
-      }
-      for (uint32_t base = lead * kSeg; base < flat; base += kConsumerWarps * kSeg) {
-        const uint32_t f = base + lane * kLaneElems;
-        // MX chunks hold whole 32-element blocks; an NVFP4 chunk may end half-way through a
-        // lane's piece (rows of 16k elements): then only its first block is live
-        const bool live = f < flat;
-        const bool live_hi = f + 16 < flat;
-        float x[32];
-        if (live_hi) {
-          load32<F32>(buf + f * kEsize, x);
-        } else {
+          const float rstd = __fdiv_rn(1.0f, __fsqrt_rn(var + a.eps));
+          const uint32_t row = static_cast<uint32_t>(r0) + rr;
+          for (int cc = static_cast<int>(lane) * kLaneElems; cc < nci; cc += 32 * kLaneElems) {
+            float x[32];
+            load32<F32>(rowp + cc * kEsize, x);
+            const uint4* gp = reinterpret_cast<const uint4*>(a.gamma + cc);
+            const uint4* bp = reinterpret_cast<const uint4*>(a.beta + cc);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) x[i] = 0.0f;
-          if (live) load32<F32, 16>(buf + f * kEsize, x);  // the first block only: nothing past the chunk is read
-        }
-        if constexpr (LN) {
-          // phase 2: y = (x - mean) * rstd * gamma + beta for this lane's 32 columns of row rr
-          // lanes past the chunk's end (live false) read row 0: their values are never stored
-          const uint32_t rr = (live && nr > 1) ? __umulhi(f, a.cols_magic) : 0u;
-          const uint32_t col = live ? f - rr * static_cast<uint32_t>(nc) : 0u;
-          const float mean = ln_stats[(2 * pb) * kLnMaxRows + rr], rstd = ln_stats[(2 * pb + 1) * kLnMaxRows + rr];
-          const uint4* gp = reinterpret_cast<const uint4*>(a.gamma + col);
-          const uint4* bp = reinterpret_cast<const uint4*>(a.beta + col);
+            for (int h = 0; h < 4; ++h) {
+              const uint4 gv = __ldg(gp + h), bv = __ldg(bp + h);
+              const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w}, bw[4] = {bv.x, bv.y, bv.z, bv.w};
 #pragma unroll
-          for (int h = 0; h < 4; ++h) {
-            const uint4 gv = __ldg(gp + h), bv = __ldg(bp + h);
-            const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w}, bw[4] = {bv.x, bv.y, bv.z, bv.w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              float& y0 = x[8 * h + 2 * i];
-              float& y1 = x[8 * h + 2 * i + 1];
-              y0 = __fadd_rn(__fmul_rn(__fmul_rn(y0 - mean, rstd), __uint_as_float(gw[i] << 16)), __uint_as_float(bw[i] << 16));
-              y1 = __fadd_rn(__fmul_rn(__fmul_rn(y1 - mean, rstd), __uint_as_float(gw[i] & 0xFFFF0000u)),
-                             __uint_as_float(bw[i] & 0xFFFF0000u));
+              for (int i = 0; i < 4; ++i) {
+                float& y0 = x[8 * h + 2 * i];
+                float& y1 = x[8 * h + 2 * i + 1];
+                y0 = __fadd_rn(__fmul_rn(__fmul_rn(y0 - mean, rstd), __uint_as_float(gw[i] << 16)),
+                               __uint_as_float(bw[i] << 16));
+                y1 = __fadd_rn(__fmul_rn(__fmul_rn(y1 - mean, rstd), __uint_as_float(gw[i] & 0xFFFF0000u)),
+                               __uint_as_float(bw[i] & 0xFFFF0000u));
+              }
             }
-          }
-        }
-        if constexpr (NV == kNvGiven) run_max = max(run_max, __float_as_uint(abs_max<32>(x)));
-        if (live) {
-          const uint64_t e = elem0 + f;
-          uint32_t w[FMT == BSQ_MXFP8 ? 8 : 4];
-          const uint32_t sb = quantize32<FMT>(x, g, six_g, w);
-          if constexpr (FMT == BSQ_MXFP8) {
-            uint4* dst = reinterpret_cast<uint4*>(a.codes + e);
-            dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-            dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-          } else if constexpr (FMT == BSQ_MXFP4) {
-            *reinterpret_cast<uint4*>(a.codes + (e >> 1)) = make_uint4(w[0], w[1], w[2], w[3]);
-          } else {  // NVFP4 codes are only 8-byte aligned when rows are 16k elements long
-            uint2* dst = reinterpret_cast<uint2*>(a.codes + (e >> 1));
-            dst[0] = make_uint2(w[0], w[1]);
-            if (live_hi) dst[1] = make_uint2(w[2], w[3]);
-          }
-          // each block's scale byte at its place in the tiled layout (32-bit arithmetic: rows and
-          // columns stay below 2^31, the number of 512-byte scale tiles below 2^32)
-          constexpr int kBlocks = FMT == BSQ_NVFP4 ? 2 : 1;
-#pragma unroll
-          for (int h = 0; h < kBlocks; ++h) {
-            if (h == 1 && !live_hi) break;
-            const uint32_t fh = f + 16u * h;
-            const uint32_t rr = nr > 1 ? __umulhi(fh, a.cols_magic) : 0u;
-            const uint32_t row = static_cast<uint32_t>(r0) + rr;
-            const uint32_t col = static_cast<uint32_t>(c0) + (fh - rr * static_cast<uint32_t>(nc));
-            const uint32_t sc = col >> (FMT == BSQ_NVFP4 ? 4 : 5);
-            const uint32_t tile = (row >> 7) * static_cast<uint32_t>(a.nct) + (sc >> 2);
-            uint8_t* sp = a.scales + static_cast<uint64_t>(tile) * 512 +
+            const uint64_t e = static_cast<uint64_t>(row) * static_cast<uint64_t>(a.cols) + static_cast<uint64_t>(cc);
+            uint32_t w[FMT == BSQ_MXFP8 ? 8 : 4];
+            const uint32_t sb = quantize32<FMT>(x, g, six_g, w);
+            if constexpr (FMT == BSQ_MXFP8) {
+              uint4* dst = reinterpret_cast<uint4*>(a.codes + e);
+              dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+              dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+            } else {
+              *reinterpret_cast<uint4*>(a.codes + (e >> 1)) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+            const uint32_t sc = static_cast<uint32_t>(cc) >> 5;
+            uint8_t* sp = a.scales + static_cast<uint64_t>((row >> 7) * static_cast<uint32_t>(a.nct) + (sc >> 2)) * 512 +
                           (((row & 31u) << 4) | (((row >> 5) & 3u) << 2) | (sc & 3u));
-            *sp = static_cast<uint8_t>(sb >> (8 * h));
+            *sp = static_cast<uint8_t>(sb);
             if (sc + 1 == static_cast<uint32_t>(a.nsc)) {
-              // padding columns of the row's last 4-column group read 0
               for (uint32_t j = (sc & 3u) + 1; j < 4; ++j) sp[j - (sc & 3u)] = 0;
             }
           }
         }
-      }
-      // first step in the next chunk: continue the round-robin where this chunk ended
-      lead = (lead + (kConsumerWarps - steps % kConsumerWarps)) % kConsumerWarps;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty_bar[stage]);
-      if (++stage == kRing) {
-        stage = 0;
-        phase ^= 1u;
+        lead = (lead + (kConsumerWarps - static_cast<uint32_t>(nr) % kConsumerWarps)) % kConsumerWarps;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty_bar[stage]);
+        if (++stage == kRing) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      } else {
+        for (uint32_t base = lead * kSeg; base < flat; base += kConsumerWarps * kSeg) {
+          const uint32_t f = base + lane * kLaneElems;
+          // MX chunks hold whole 32-element blocks; an NVFP4 chunk may end half-way through a
+          // lane's piece (rows of 16k elements): then only its first block is live
+          const bool live = f < flat;
+          const bool live_hi = f + 16 < flat;
+          float x[32];
+          if (live_hi) {
+            load32<F32>(buf + f * kEsize, x);
+          } else {
+  #pragma unroll
+            for (int i = 0; i < 32; ++i) x[i] = 0.0f;
+            if (live) load32<F32, 16>(buf + f * kEsize, x);  // the first block only: nothing past the chunk is read
+          }
+          if constexpr (NV == kNvGiven) run_max = max(run_max, __float_as_uint(abs_max<32>(x)));
+          if (live) {
+            const uint64_t e = elem0 + f;
+            uint32_t w[FMT == BSQ_MXFP8 ? 8 : 4];
+            const uint32_t sb = quantize32<FMT>(x, g, six_g, w);
+            if constexpr (FMT == BSQ_MXFP8) {
+              uint4* dst = reinterpret_cast<uint4*>(a.codes + e);
+              dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+              dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+            } else if constexpr (FMT == BSQ_MXFP4) {
+              *reinterpret_cast<uint4*>(a.codes + (e >> 1)) = make_uint4(w[0], w[1], w[2], w[3]);
+            } else {  // NVFP4 codes are only 8-byte aligned when rows are 16k elements long
+              uint2* dst = reinterpret_cast<uint2*>(a.codes + (e >> 1));
+              dst[0] = make_uint2(w[0], w[1]);
+              if (live_hi) dst[1] = make_uint2(w[2], w[3]);
+            }
+            // each block's scale byte at its place in the tiled layout (32-bit arithmetic: rows and
+            // columns stay below 2^31, the number of 512-byte scale tiles below 2^32)
+            constexpr int kBlocks = FMT == BSQ_NVFP4 ? 2 : 1;
+  #pragma unroll
+            for (int h = 0; h < kBlocks; ++h) {
+              if (h == 1 && !live_hi) break;
+              const uint32_t fh = f + 16u * h;
+              const uint32_t rr = nr > 1 ? __umulhi(fh, a.cols_magic) : 0u;
+              const uint32_t row = static_cast<uint32_t>(r0) + rr;
+              const uint32_t col = static_cast<uint32_t>(c0) + (fh - rr * static_cast<uint32_t>(nc));
+              const uint32_t sc = col >> (FMT == BSQ_NVFP4 ? 4 : 5);
+              const uint32_t tile = (row >> 7) * static_cast<uint32_t>(a.nct) + (sc >> 2);
+              uint8_t* sp = a.scales + static_cast<uint64_t>(tile) * 512 +
+                            (((row & 31u) << 4) | (((row >> 5) & 3u) << 2) | (sc & 3u));
+              *sp = static_cast<uint8_t>(sb >> (8 * h));
+              if (sc + 1 == static_cast<uint32_t>(a.nsc)) {
+                // padding columns of the row's last 4-column group read 0
+                for (uint32_t j = (sc & 3u) + 1; j < 4; ++j) sp[j - (sc & 3u)] = 0;
+              }
+            }
+          }
+        }
+        // first step in the next chunk: continue the round-robin where this chunk ended
+        lead = (lead + (kConsumerWarps - steps % kConsumerWarps)) % kConsumerWarps;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty_bar[stage]);
+        if (++stage == kRing) {
+          stage = 0;
+          phase ^= 1u;
+        }
       }
     }
 
