@@ -17,10 +17,11 @@
 // the matrix edge read zeros. Every tile covers exactly one 512-byte scale tile of the row
 // layout and one (bf16) or half of one (fp32) of the column layout, so the kernel writes every
 // scale byte, padding included (zero blocks give scale byte 0), and no buffer needs clearing.
-//   row pass     each lane takes one 16-byte piece (8 bf16 / 4 fp32) of a row: a warp reads
-//                512 contiguous bytes (conflict-free); a 32-element block is 4 / 8 lanes
-//                (xor-shuffles for its maximum) and the row's four scale bytes are OR-ed into
-//                one 32-bit word by two more shuffles, stored by the row's first lane.
+//   row pass     each lane takes 32 consecutive elements of a row -- one MX block, two NVFP4
+//                blocks -- so block maxima need no shuffle; four lanes cover a 128-column row,
+//                whose scale bytes are OR-ed into 32-bit words of the tiled layout by one or
+//                two shuffles. (With 16-byte pieces per lane and shuffles for the maxima the
+//                pass took ~12.6 instructions per element.)
 //   column pass  each thread takes one column and 64 / 32 rows of the tile: the warp reads 32
 //                consecutive columns of one row per load (conflict-free), the thread reduces
 //                its 32-row blocks alone and puts each block's codes into a shared-memory
@@ -270,9 +271,7 @@ __global__ void __launch_bounds__(kDThreads, kDCtasPerSm)
   constexpr int BS = kNv ? 16 : 32;                        // block size
   constexpr int kEsize = F32 ? 4 : 2;
   constexpr int kRows = kDTileBytes / (kDCols * kEsize);  // 128 bf16, 64 fp32
-  constexpr int V = 16 / kEsize;                           // elements of a 16-byte piece
-  constexpr int LB = BS / V;                               // lanes of a block in the row pass
-  constexpr int kRowSteps = kDTileBytes / 16 / 32 / kDConsumerWarps;  // row-pass steps per warp
+  constexpr int kRowSteps = kRows / 8 / kDConsumerWarps;  // row-pass steps per warp (8 rows each)
   constexpr int kColUnits = kRows / 32 / 2;  // column-pass 32-row units per thread (2 bf16, 1 fp32)
   constexpr int kUnitScales = 32 / BS;       // scale bytes of a 32-row unit
   constexpr int kUnitCodeBytes = kFp8 ? 32 : 16;           // codes of a 32-element unit
@@ -354,69 +353,93 @@ __global__ void __launch_bounds__(kDThreads, kDCtasPerSm)
     const int64_t r0 = ti * kRows, c0 = tj * kDCols;
     const uint8_t* tile = ring + stage * kDTileBytes;
 
-    // ---- row pass: pieces of 16 bytes, the warp's 32 pieces contiguous
+    // ---- row pass: each lane one 32-element piece of a row (one MX block, two NVFP4 blocks),
+    // four lanes per 128-column row, 8 rows per warp step
     if (ok) {
-#pragma unroll 2
+#pragma unroll 1
       for (int s = 0; s < kRowSteps; ++s) {
-        const int f = (s * kDConsumerWarps + cw) * 32 + static_cast<int>(lane);
-        const int e0 = f * V;
-        const int rr = e0 / kDCols, cc = e0 % kDCols;
-        const uint4 v = *reinterpret_cast<const uint4*>(tile + f * 16);
-        float x[V];
+        const int rr = (s * kDConsumerWarps + cw) * 8 + static_cast<int>(lane >> 2);
+        const int cc = static_cast<int>(lane & 3u) * 32;
+        float x[32];
+        const uint4* src = reinterpret_cast<const uint4*>(tile + (rr * kDCols + cc) * kEsize);
         if constexpr (F32) {
-          x[0] = __uint_as_float(v.x);
-          x[1] = __uint_as_float(v.y);
-          x[2] = __uint_as_float(v.z);
-          x[3] = __uint_as_float(v.w);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const uint4 v = src[i];
+            x[4 * i] = __uint_as_float(v.x);
+            x[4 * i + 1] = __uint_as_float(v.y);
+            x[4 * i + 2] = __uint_as_float(v.z);
+            x[4 * i + 3] = __uint_as_float(v.w);
+          }
         } else {
-          const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            x[2 * i] = __uint_as_float(wv[i] << 16);
-            x[2 * i + 1] = __uint_as_float(wv[i] & 0xFFFF0000u);
+            const uint4 v = src[i];
+            const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              x[8 * i + 2 * k] = __uint_as_float(wv[k] << 16);
+              x[8 * i + 2 * k + 1] = __uint_as_float(wv[k] & 0xFFFF0000u);
+            }
           }
         }
-        float amax = 0.0f;
-#pragma unroll
-        for (int i = 0; i < V; ++i) amax = fmaxf(amax, fabsf(x[i]));
-        if constexpr (kNv) run_max = max(run_max, __float_as_uint(amax));
-#pragma unroll
-        for (int o = 1; o < LB; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
-        float bf;
-        const uint32_t sbyte = block_scale<FMT>(amax, g, six_g, bf);
         const int64_t r = r0 + rr, c = c0 + cc;
-        uint32_t w[kFp8 ? V / 4 : 1];
-        if (kNv && bf == 0.0f) {
-          w[0] = sign_codes<V>(x);
-        } else if constexpr (SR) {
-          const uint64_t g0 = (static_cast<uint64_t>(r) * static_cast<uint64_t>(C) + static_cast<uint64_t>(c)) >> 2;
-          if constexpr (kFp8) {
+        constexpr int kBlocks = 32 / BS;               // 1 (MX) or 2 (NVFP4)
+        constexpr int kWords = kFp8 ? 8 : 4;           // code words of the piece
+        constexpr int kBlockWords = kWords / kBlocks;  // code words of one block
+        uint32_t w[kWords];
+        uint32_t sbytes = 0;
+        const uint64_t g0 = (static_cast<uint64_t>(r) * static_cast<uint64_t>(C) + static_cast<uint64_t>(c)) >> 2;
 #pragma unroll
-            for (int gq = 0; gq < V / 4; ++gq) w[gq] = sr_codes4<FMT>(x + 4 * gq, bf, sr_words(g0 + gq, 0u, a));
+        for (int h = 0; h < kBlocks; ++h) {
+          const float* xb = x + h * BS;
+          float m[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+          for (int k = 0; k < BS; ++k) m[k & 3] = fmaxf(m[k & 3], fabsf(xb[k]));
+          const float amax = fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
+          if constexpr (kNv) run_max = max(run_max, __float_as_uint(amax));
+          float bf;
+          sbytes |= block_scale<FMT>(amax, g, six_g, bf) << (8 * h);
+          uint32_t* wb = w + h * kBlockWords;
+          if (kNv && bf == 0.0f) {
+            wb[0] = sign_codes<8>(xb);
+            wb[1] = sign_codes<8>(xb + 8);
+          } else if constexpr (SR) {
+#pragma unroll
+            for (int gq = 0; gq < BS / 4; ++gq) {
+              const uint32_t v4 = sr_codes4<FMT>(xb + 4 * gq, bf, sr_words(g0 + h * (BS / 4) + gq, 0u, a));
+              if constexpr (kFp8) wb[gq] = v4;
+              else if (gq & 1) wb[gq >> 1] |= v4 << 16;
+              else wb[gq >> 1] = v4;
+            }
           } else {
-            w[0] = 0;
 #pragma unroll
-            for (int gq = 0; gq < V / 4; ++gq) w[0] |= sr_codes4<FMT>(x + 4 * gq, bf, sr_words(g0 + gq, 0u, a)) << (16 * gq);
+            for (int j = 0; j < kBlockWords; ++j) rne_codes<FMT, kFp8 ? 4 : 8>(xb + (kFp8 ? 4 : 8) * j, bf, wb + j);
           }
-        } else {
-          rne_codes<FMT, V>(x, bf, w);
         }
         if (r < R && c < C) {
           const int64_t idx = r * C + c;
           if constexpr (kFp8) {
-            if constexpr (V == 8) *reinterpret_cast<uint2*>(a.row_codes + idx) = make_uint2(w[0], w[1]);
-            else *reinterpret_cast<uint32_t*>(a.row_codes + idx) = w[0];
+            uint4* dst = reinterpret_cast<uint4*>(a.row_codes + idx);
+            dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+            dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
           } else {
-            if constexpr (V == 8) *reinterpret_cast<uint32_t*>(a.row_codes + idx / 2) = w[0];
-            else *reinterpret_cast<uint16_t*>(a.row_codes + idx / 2) = static_cast<uint16_t>(w[0]);
+            *reinterpret_cast<uint4*>(a.row_codes + idx / 2) = make_uint4(w[0], w[1], w[2], w[3]);
           }
         }
-        // four consecutive block scales of the row -> one word (block b of the group in byte b)
-        uint32_t sw = sbyte << (8 * ((cc / BS) & 3));
-        sw |= __shfl_xor_sync(0xFFFFFFFFu, sw, LB);
-        sw |= __shfl_xor_sync(0xFFFFFFFFu, sw, 2 * LB);
+        // the row's scale bytes -> 32-bit words of the tiled layout: MX one word (lane b of the
+        // row holds byte b), NVFP4 two words (lanes 2k and 2k + 1 hold word k)
+        uint32_t sw;
+        if constexpr (kNv) {
+          sw = sbytes << (16 * (lane & 1u));
+          sw |= __shfl_xor_sync(0xFFFFFFFFu, sw, 1);
+        } else {
+          sw = sbytes << (8 * (lane & 3u));
+          sw |= __shfl_xor_sync(0xFFFFFFFFu, sw, 1);
+          sw |= __shfl_xor_sync(0xFFFFFFFFu, sw, 2);
+        }
         const int64_t grp = c / (4 * BS);  // 4-scale-column group of the row layout
-        if ((lane & (4 * LB - 1)) == 0 && grp < a.nct_row) {
+        if ((lane & (kNv ? 1u : 3u)) == 0 && grp < a.nct_row) {
           const int64_t off = ((r >> 7) * a.nct_row + grp) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4;
           *reinterpret_cast<uint32_t*>(a.row_scales + off) = sw;
         }
