@@ -75,6 +75,9 @@ struct DualArgs {
   int64_t nct_row;  // 512-byte scale tiles per 128-row group, row layout: ceil(C / (4 * block))
   int64_t nct_col;  // same for the column layout (C rows, R / block scale columns): ceil(R / (4 * block))
   uint32_t seed_lo, seed_hi;
+  // Philox round keys, computed on the host: keys[2i] = seed_lo + i * 0x9E3779B9, keys[2i + 1] =
+  // seed_hi + i * 0xBB67AE85 (kernel parameters, so every round XORs a constant-bank operand)
+  uint32_t keys[20];
   // NVFP4: the per-tensor scale g, shared by both layouts; {g, amax} tails after each scale body
   uint32_t* row_tail;
   uint32_t* col_tail;
@@ -84,27 +87,25 @@ struct DualArgs {
 };
 
 // Philox4x32-10 of the SC'11 paper: ten rounds of two 32 x 32 -> 64-bit products mixed into
-// the other two counter words and the key, the key bumped by the Weyl constants after every
-// round.
-__device__ __forceinline__ uint4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3, uint32_t k0,
-                                               uint32_t k1) {
+// the other two counter words and the round key (the key bumped by the Weyl constants after every
+// round: the caller's precomputed keys[2i], keys[2i + 1]).
+__device__ __forceinline__ uint4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3,
+                                               const uint32_t* keys) {
 #pragma unroll
   for (int i = 0; i < 10; ++i) {
     const uint64_t p0 = static_cast<uint64_t>(0xD2511F53u) * c0;  // one widening multiply each
     const uint64_t p1 = static_cast<uint64_t>(0xCD9E8D57u) * c2;
-    c0 = static_cast<uint32_t>(p1 >> 32) ^ c1 ^ k0;
+    c0 = static_cast<uint32_t>(p1 >> 32) ^ c1 ^ keys[2 * i];
     c1 = static_cast<uint32_t>(p1);
-    c2 = static_cast<uint32_t>(p0 >> 32) ^ c3 ^ k1;
+    c2 = static_cast<uint32_t>(p0 >> 32) ^ c3 ^ keys[2 * i + 1];
     c3 = static_cast<uint32_t>(p0);
-    k0 += 0x9E3779B9u;
-    k1 += 0xBB67AE85u;
   }
   return make_uint4(c0, c1, c2, c3);
 }
 
 // The four random words of elements 4g .. 4g+3 of a layout (0 = row, 1 = column).
 __device__ __forceinline__ uint4 sr_words(uint64_t g, uint32_t layout, const DualArgs& a) {
-  return philox4x32_10(static_cast<uint32_t>(g), static_cast<uint32_t>(g >> 32), layout, 0u, a.seed_lo, a.seed_hi);
+  return philox4x32_10(static_cast<uint32_t>(g), static_cast<uint32_t>(g >> 32), layout, 0u, a.keys);
 }
 
 // Block scale byte of the MX rule: floor(log2(amax)) - emax, clamped at -127, plus 127.
@@ -604,6 +605,10 @@ int launch_quantize_dual(int fmt, bool src_f32, bool stochastic, bool global_giv
   a.nct_col = ceil_div(rows, 4 * bs);
   a.seed_lo = static_cast<uint32_t>(seed);
   a.seed_hi = static_cast<uint32_t>(seed >> 32);
+  for (int i = 0; i < 10; ++i) {
+    a.keys[2 * i] = a.seed_lo + static_cast<uint32_t>(i) * 0x9E3779B9u;
+    a.keys[2 * i + 1] = a.seed_hi + static_cast<uint32_t>(i) * 0xBB67AE85u;
+  }
   a.status = dev.status;
   if (fmt == BSQ_NVFP4) {
     a.row_tail = reinterpret_cast<uint32_t*>(a.row_scales + scales_body_bytes(fmt, rows, cols));
