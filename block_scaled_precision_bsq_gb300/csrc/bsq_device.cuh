@@ -157,6 +157,15 @@ __device__ __forceinline__ void tma_load_3d_to_leader(void* smem_dst, const void
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(leader_bar), "r"(x), "r"(y), "r"(z)
       : "memory");
 }
+// The same 3-D load with an L2 cache policy (createpolicy) on the global reads.
+__device__ __forceinline__ void tma_load_3d_to_leader(void* smem_dst, const void* tmap, uint32_t leader_bar, int32_t x,
+                                                      int32_t y, int32_t z, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(leader_bar), "r"(x), "r"(y), "r"(z), "l"(policy)
+      : "memory");
+}
 // 2-D form of tma_load_3d_to_leader.
 __device__ __forceinline__ void tma_load_2d_to_leader(void* smem_dst, const void* tmap, uint32_t leader_bar, int32_t x,
                                                       int32_t y) {
@@ -166,7 +175,23 @@ __device__ __forceinline__ void tma_load_2d_to_leader(void* smem_dst, const void
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(leader_bar), "r"(x), "r"(y)
       : "memory");
 }
+// The same 2-D load with an L2 cache policy (createpolicy) on the global reads.
+__device__ __forceinline__ void tma_load_2d_to_leader(void* smem_dst, const void* tmap, uint32_t leader_bar, int32_t x,
+                                                      int32_t y, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(leader_bar), "r"(x), "r"(y), "l"(policy)
+      : "memory");
+}
 constexpr uint32_t kClusterRankBit = 1u << 24;
+
+// L2 policy that keeps the lines it covers resident ahead of normally cached lines.
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
 
 // Contiguous global -> shared copy delivered to the same offset in every CTA of `mask`, each
 // destination CTA's mbarrier (same offset) receiving the complete_tx.

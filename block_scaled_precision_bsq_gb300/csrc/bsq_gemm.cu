@@ -225,6 +225,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Boxes reaching past M, N or the scale atoms are zero-filled by TMA and still deliver
     // their full byte count, so every stage of every CTA brings exactly kStageBytes.
     constexpr uint32_t kStageBytes = L::kABytes + L::kBBytes + L::kSfaBytes + L::kSfbBytes;
+    // every row block of A (codes and scales) is read by tiles_n tiles and every column block of
+    // B by all row blocks: keep the operands in L2 ahead of the output lines the epilogue streams
+    // through it (measured: 4-6 % faster on the ViT shapes than default caching)
+    const uint64_t keep = l2_policy_evict_last();
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
@@ -238,11 +242,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (leader) mbar_arrive_expect_tx(&full_bar[stage], 2 * kStageBytes);
         const uint32_t bar = smem_u32(&full_bar[stage]) & ~kClusterRankBit;  // the leader's full[stage]
-        tma_load_2d_to_leader(smem + L::a_off + stage * L::kABytes, &mapA, bar, kb * kChunkBytes, m_blk * BM);
+        tma_load_2d_to_leader(smem + L::a_off + stage * L::kABytes, &mapA, bar, kb * kChunkBytes, m_blk * BM, keep);
         tma_load_2d_to_leader(smem + L::b_off + stage * L::kBBytes, &mapB, bar, kb * kChunkBytes,
-                              n_blk * BN + static_cast<int>(rank) * BNH);
-        tma_load_3d_to_leader(smem + L::sfa_off + stage * L::kSfaBytes, &mapSfa, bar, 0, kb * C::kAtoms, m_blk);
-        tma_load_3d_to_leader(smem + L::sfb_off + stage * L::kSfbBytes, &mapSfb, bar, 0, kb * C::kAtoms, 2 * n_blk);
+                              n_blk * BN + static_cast<int>(rank) * BNH, keep);
+        tma_load_3d_to_leader(smem + L::sfa_off + stage * L::kSfaBytes, &mapSfa, bar, 0, kb * C::kAtoms, m_blk, keep);
+        tma_load_3d_to_leader(smem + L::sfb_off + stage * L::kSfbBytes, &mapSfb, bar, 0, kb * C::kAtoms, 2 * n_blk,
+                              keep);
         if (++stage == S) {
           stage = 0;
           phase ^= 1u;
