@@ -74,7 +74,9 @@ struct Cfg<BSQ_NVFP4> {  // 256 K per stage = 4 MMAs of K 64, four E4M3 scales (
 };
 template <>
 struct Cfg<BSQ_MXFP4> {  // 256 K per stage = 4 MMAs of K 64, two UE8M0 scales each
-  static constexpr int kStages = 6, kAtoms = 2, kEpiCols = 16, kEpiBufs = 1;
+  // 5 stages leave room for 32-column store chunks: at K = 1024 (2048 MMA cycles per tile) the
+  // epilogue's store round trips bound the tile, and halving their number beats a sixth stage
+  static constexpr int kStages = 5, kAtoms = 2, kEpiCols = 32, kEpiBufs = 1;
 };
 template <int FMT>
 __host__ __device__ constexpr int sf_cols() {
