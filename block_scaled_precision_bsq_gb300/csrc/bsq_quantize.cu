@@ -8,7 +8,7 @@
 // the BF16 ledger blog section 5.4; 6 for e2m1). The UE8M0 exponent of a block is
 // floor(log2(amax)) - emax with emax the exponent of the element format's top binade.
 //
-// Work mapping (two CTAs per SM, persistent). The source is cut into chunks of whole rows
+// Work mapping (four CTAs per SM, persistent). The source is cut into chunks of whole rows
 // (or, for rows longer than a chunk, row pieces of whole 1024-element segments); a chunk is
 // contiguous in memory and comes in with one 1-D TMA bulk copy. A producer thread per CTA
 // keeps a ring of up to kRing chunk buffers in flight -- for a 22 MB matrix that is nearly
@@ -35,12 +35,12 @@
 namespace bsq {
 namespace {
 
-constexpr int kThreads = 384;          // warp 0: TMA producer (lane 0); warps 1..11: consumers
+constexpr int kThreads = 256;          // warp 0: TMA producer (lane 0); warps 1..7: consumers
 constexpr int kConsumerWarps = kThreads / 32 - 1;
 constexpr int kLaneElems = 32;         // elements per lane per step: one MX block, two NVFP4 blocks
 constexpr int kSeg = 32 * kLaneElems;   // elements per warp step
-constexpr int kRing = 6;                // chunk buffers per CTA
-constexpr int kCtasPerSm = 2;           // two resident CTAs: twice the warps to hide latency
+constexpr int kRing = 3;                // chunk buffers per CTA
+constexpr int kCtasPerSm = 4;           // four resident CTAs (28 consumer warps per SM) to hide latency
 constexpr int kChunkMax = 16384;        // bytes per chunk buffer
 constexpr int kChunkMin = 4096;         // smallest chunk worth a copy (small tensors)
 constexpr int kAmaxThreads = 256;
