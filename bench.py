@@ -528,8 +528,8 @@ def run_gpu(args, rank: int, world: int):
         gpu_index = os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local]
     else:
         gpu_index = str(local)
-    out_dir = os.path.join(ROOT, "gpurun_out") if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else \
-        os.path.join(ROOT, "_build")
+    # the nvidia-smi clock log of the timed region: BSQ_CLOCKS_DIR if set, else the build folder
+    out_dir = os.environ.get("BSQ_CLOCKS_DIR") or os.path.join(ROOT, "_build")
     os.makedirs(out_dir, exist_ok=True)
     sampler = ClockSampler(gpu_index, os.path.join(out_dir, "clocks_rank%d.csv" % rank))
     time.sleep(0.3)
