@@ -202,15 +202,40 @@ __device__ __forceinline__ void rne_codes(const float* x, float f, uint32_t* w) 
 // (element i takes word i), packed as rne_codes packs four: E4M3 one word, e2m1 the low 16 bits.
 // MX passes x for sr_code's underflow test (the MX value x / scale is exact unless it leaves
 // fp32's range); NVFP4 rounds the fp32 quotient itself, so the quotient stands in for x.
+// E4M3 tests the range once per four elements: when all four scaled values lie in the normal
+// range (all but ~1 % of groups: the subnormal range sits 2^14 below a block's maximum), each
+// code is sr_code's normal-range carry form without a branch per element; otherwise sr_code.
 template <int FMT>
 __device__ __forceinline__ uint32_t sr_codes4(const float* x, float f, uint4 q) {
   constexpr int kBits = (FMT == BSQ_MXFP8) ? 8 : 4;
   const uint32_t qq[4] = {q.x, q.y, q.z, q.w};
   uint32_t w = 0;
+  if constexpr (FMT == BSQ_MXFP8) {
+    float y[4];
+    uint32_t bmin = 0xFFFFFFFFu;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float y = scaled<FMT>(x[i], f);
-    w |= sr_code<FMT>(y, FMT == BSQ_NVFP4 ? y : x[i], qq[i]) << (kBits * i);
+    for (int i = 0; i < 4; ++i) {
+      y[i] = scaled<FMT>(x[i], f);
+      bmin = min(bmin, __float_as_uint(y[i]) & 0x7FFFFFFFu);
+    }
+    if (bmin >= (121u << 23)) {  // 2^-6, the smallest normal E4M3 magnitude
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t yb = __float_as_uint(y[i]);
+        const uint32_t b = yb & 0x7FFFFFFFu;
+        const uint32_t mag = min((b + ((1u << 20) - 1u - (120u << 23)) - (qq[i] >> 12)) >> 20, 0x7Eu);
+        w |= (((yb >> 31) << 7) | mag) << (8 * i);
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) w |= sr_code<FMT>(y[i], x[i], qq[i]) << (8 * i);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float y = scaled<FMT>(x[i], f);
+      w |= sr_code<FMT>(y, FMT == BSQ_NVFP4 ? y : x[i], qq[i]) << (kBits * i);
+    }
   }
   return w;
 }
