@@ -292,9 +292,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) quantize_kernel(const __
       if constexpr (LN) {
         // LayerNorm mode (whole rows, MX formats): each warp owns whole rows of the chunk, dealt
         // round-robin over the CTA's chunks like the warp steps below (`lead` is this warp's first
-        // row here): the row's mean and rstd (fp32, two passes over the row in shared memory,
-        // butterfly warp sums), then y = (x - mean) * rstd * gamma + beta and the quantization of
-        // the row, 32 columns per lane -- no barrier between the warps
+        // row here): the row's mean and rstd (fp32, two passes over the row -- in registers for
+        // rows of at most 1024 elements, else in shared memory -- with butterfly warp sums), then
+        // y = (x - mean) * rstd * gamma + beta and the quantization of the row, 32 columns per
+        // lane -- no barrier between the warps
         const int nci = static_cast<int>(nc);
         const int pieces = nci * kEsize / 16;  // 16-byte pieces of a row
         for (uint32_t rr = lead; rr < static_cast<uint32_t>(nr); rr += kConsumerWarps) {
@@ -319,13 +320,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) quantize_kernel(const __
             for (int o = 16; o > 0; o >>= 1) acc_s += __shfl_xor_sync(0xFFFFFFFFu, acc_s, o);
             return acc_s;
           };
-          const float mean = __fdiv_rn(piece_sum(0.0f, false), static_cast<float>(nci));
-          const float var = __fdiv_rn(piece_sum(mean, true), static_cast<float>(nci));
-          const float rstd = __fdiv_rn(1.0f, __fsqrt_rn(var + a.eps));
           const uint32_t row = static_cast<uint32_t>(r0) + rr;
-          for (int cc = static_cast<int>(lane) * kLaneElems; cc < nci; cc += 32 * kLaneElems) {
-            float x[32];
-            load32<F32>(rowp + cc * kEsize, x);
+          // y = (x - mean) * rstd * gamma + beta for the 32 elements at column cc (x holds the
+          // source values), then their MX block: codes and scale byte
+          auto finish = [&](int cc, float (&x)[32], float mean, float rstd) {
             const uint4* gp = reinterpret_cast<const uint4*>(a.gamma + cc);
             const uint4* bp = reinterpret_cast<const uint4*>(a.beta + cc);
 #pragma unroll
@@ -358,6 +356,50 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) quantize_kernel(const __
             *sp = static_cast<uint8_t>(sb);
             if (sc + 1 == static_cast<uint32_t>(a.nsc)) {
               for (uint32_t j = (sc & 3u) + 1; j < 4; ++j) sp[j - (sc & 3u)] = 0;
+            }
+          };
+          if (nci <= 32 * kLaneElems) {
+            // rows of at most 1024 elements: each lane reads its 32 elements from shared memory
+            // once and keeps them in registers for both statistics passes and the quantization
+            const int cc = static_cast<int>(lane) * kLaneElems;
+            const bool act = cc < nci;
+            float x[32];
+            if (act) {
+              load32<F32>(rowp + cc * kEsize, x);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) x[i] = 0.0f;
+            }
+            float p4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+            for (int i = 0; i < 32; ++i) p4[i & 3] += x[i];
+            float acc_s = (p4[0] + p4[1]) + (p4[2] + p4[3]);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) acc_s += __shfl_xor_sync(0xFFFFFFFFu, acc_s, o);
+            const float mean = __fdiv_rn(acc_s, static_cast<float>(nci));
+#pragma unroll
+            for (int i = 0; i < 4; ++i) p4[i] = 0.0f;
+            if (act) {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) {
+                const float d = x[i] - mean;
+                p4[i & 3] += d * d;
+              }
+            }
+            acc_s = (p4[0] + p4[1]) + (p4[2] + p4[3]);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) acc_s += __shfl_xor_sync(0xFFFFFFFFu, acc_s, o);
+            const float var = __fdiv_rn(acc_s, static_cast<float>(nci));
+            const float rstd = __fdiv_rn(1.0f, __fsqrt_rn(var + a.eps));
+            if (act) finish(cc, x, mean, rstd);
+          } else {
+            const float mean = __fdiv_rn(piece_sum(0.0f, false), static_cast<float>(nci));
+            const float var = __fdiv_rn(piece_sum(mean, true), static_cast<float>(nci));
+            const float rstd = __fdiv_rn(1.0f, __fsqrt_rn(var + a.eps));
+            for (int cc = static_cast<int>(lane) * kLaneElems; cc < nci; cc += 32 * kLaneElems) {
+              float x[32];
+              load32<F32>(rowp + cc * kEsize, x);
+              finish(cc, x, mean, rstd);
             }
           }
         }
