@@ -371,6 +371,9 @@ def run_gpu(args, rank: int, world: int):
         g = wl.gemms[0]
         fmt, M, K, N = g.fmt, g.M, g.K, g.N
         delayed = fmt == NVFP4 and wl.grad_headroom is not None
+        # dW = dY^T X: N x K over the M tokens, K cut into the library's number of ranges
+        dw_splits = bsq.bsq_gemm_splitk_splits(fmt, N, K, M)
+        assert dw_splits >= 1
         hosts = {"x": host(make_activations(g)), "w": host(make_weights(g)), "bias": host(make_bias(g)),
                  "dy": host(make_output_grad(g))}
 
@@ -381,7 +384,8 @@ def run_gpu(args, rank: int, world: int):
                       "qdy": (bsq.empty_qtensor(fmt, M, N, dev), bsq.empty_qtensor(fmt, N, M, dev)),
                       "out": torch.empty((M, N), dtype=torch.bfloat16, device=dev),
                       "dx": torch.empty((M, K), dtype=torch.bfloat16, device=dev),
-                      "dw": torch.empty((N, K), dtype=torch.bfloat16, device=dev)})
+                      "dw": torch.empty((N, K), dtype=torch.bfloat16, device=dev),
+                      "ws": torch.empty(dw_splits * N * K if dw_splits > 1 else 4, dtype=torch.float32, device=dev)})
             if delayed:
                 # the step before the first one: dY quantized with its own amax, so that the
                 # first timed step finds a recorded amax in the tail
@@ -402,13 +406,15 @@ def run_gpu(args, rank: int, world: int):
         def gemm(D, s):
             bsq.gemm(D["qx"][0], D["qw"][0], D["bias"], out=D["out"], stream=s)  # Y = X W^T + b
             bsq.gemm(D["qdy"][0], D["qw"][1], None, out=D["dx"], stream=s)       # dX = dY W
-            bsq.gemm(D["qdy"][1], D["qx"][1], None, out=D["dw"], stream=s)       # dW = dY^T X
+            bsq.gemm_splitk(D["qdy"][1], D["qx"][1], None, splits=dw_splits, workspace=D["ws"], out=D["dw"],
+                            stream=s)                                            # dW = dY^T X
 
         nv = fmt == NVFP4
         units.append({"hosts": hosts, "alloc": alloc, "quant": quant, "gemm": gemm, "fmt": fmt,
                       "flops": 3 * g.flops, "outs": ("out", "dx", "dw"),
-                      # duals + GEMMs; NVFP4: amax passes of X and W, the delayed-scale kernel
-                      "launches": 6 + (2 if nv else 0) + (1 if delayed else 0) + (1 if nv and not delayed else 0),
+                      # duals + GEMMs (+ the split-K sum); NVFP4: amax passes of X and W, the delayed-scale kernel
+                      "launches": 6 + (1 if dw_splits > 1 else 0) + (2 if nv else 0) + (1 if delayed else 0) +
+                                  (1 if nv and not delayed else 0),
                       "qbytes": dual_bytes(fmt, M, K, 2, True) + dual_bytes(fmt, N, K, 2, True) +
                                 dual_bytes(fmt, M, N, 2, not delayed),
                       "gbytes": gemm_bytes(fmt, M, N, K, True) + gemm_bytes(fmt, M, K, N, False) +

@@ -61,6 +61,10 @@ _lib.bsq_delayed_global_scale.restype = _int
 _lib.bsq_convt2x2.argtypes = [_int, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, _int, _vp]
 _lib.bsq_convt2x2.restype = _int
 _lib.bsq_gemm.argtypes = [_int, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp]
+_lib.bsq_gemm_splitk.restype = _int
+_lib.bsq_gemm_splitk.argtypes = [_int, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _vp, ctypes.c_size_t, _vp]
+_lib.bsq_gemm_splitk_splits.restype = _int
+_lib.bsq_gemm_splitk_splits.argtypes = [_int, _i64, _i64, _i64]
 _lib.bsq_gemm_gelu.restype = _int
 _lib.bsq_gemm_gelu.argtypes = [_int, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp]
 _lib.bsq_gemm_gelu_quantize.restype = _int
@@ -74,7 +78,7 @@ _lib.bsq_strerror.restype = ctypes.c_char_p
 _lib.bsq_strerror.argtypes = [_int]
 
 EXPORTS = ("bsq_codes_bytes", "bsq_scales_bytes", "bsq_quantize", "bsq_quantize_batch", "bsq_layernorm_quantize",
-           "bsq_quantize_dual", "bsq_delayed_global_scale", "bsq_gemm",
+           "bsq_quantize_dual", "bsq_delayed_global_scale", "bsq_gemm", "bsq_gemm_splitk", "bsq_gemm_splitk_splits",
            "bsq_gemm_gelu", "bsq_gemm_gelu_quantize", "bsq_convt2x2", "bsq_get_device_status", "bsq_selftest_timeout",
            "bsq_last_error", "bsq_strerror")
 
@@ -156,6 +160,16 @@ def bsq_gemm(fmt, A: Ptr, A_scales: Ptr, B: Ptr, B_scales: Ptr, bias: Ptr, out: 
              stream=None) -> int:
     return int(_lib.bsq_gemm(_fmt(fmt), _p(A), _p(A_scales), _p(B), _p(B_scales), _p(bias), _p(out), M, N, K,
                              _stream(stream)))
+
+
+def bsq_gemm_splitk(fmt, A: Ptr, A_scales: Ptr, B: Ptr, B_scales: Ptr, bias: Ptr, out: Ptr, M: int, N: int, K: int,
+                    splits: int, workspace: Ptr, workspace_bytes: int, stream=None) -> int:
+    return int(_lib.bsq_gemm_splitk(_fmt(fmt), _p(A), _p(A_scales), _p(B), _p(B_scales), _p(bias), _p(out), M, N, K,
+                                    splits, _p(workspace), workspace_bytes, _stream(stream)))
+
+
+def bsq_gemm_splitk_splits(fmt, M: int, N: int, K: int) -> int:
+    return int(_lib.bsq_gemm_splitk_splits(_fmt(fmt), M, N, K))
 
 
 def bsq_gemm_gelu(fmt, A: Ptr, A_scales: Ptr, B: Ptr, B_scales: Ptr, bias: Ptr, out: Ptr, M: int, N: int,
@@ -332,6 +346,31 @@ def gemm(qa: QTensor, qb: QTensor, bias: Optional[torch.Tensor] = None, out: Opt
     return out
 
 
+def gemm_splitk(qa: QTensor, qb: QTensor, bias: Optional[torch.Tensor] = None, splits: Optional[int] = None,
+                workspace: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
+                stream=None) -> torch.Tensor:
+    """gemm() with K cut into `splits` ranges (default: the library's choice for the shape), the
+    fp32 partial sums in `workspace` (splits x M x N fp32; allocated here when not given)."""
+    assert qa.fmt == qb.fmt and qa.cols == qb.cols
+    M, K, N = qa.rows, qa.cols, qb.rows
+    if splits is None:
+        splits = bsq_gemm_splitk_splits(qa.fmt, M, N, K)
+        if splits < 0:
+            raise BsqError(splits, "bsq_gemm_splitk_splits")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=qa.codes.device)
+    if bias is not None:
+        assert bias.dtype == torch.bfloat16 and bias.numel() == N and bias.is_contiguous()
+    if workspace is None and splits > 1:
+        workspace = torch.empty(splits * M * N, dtype=torch.float32, device=qa.codes.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = bsq_gemm_splitk(qa.fmt, qa.codes, qa.scales, qb.codes, qb.scales, bias, out, M, N, K, splits, workspace,
+                         ws_bytes, stream)
+    if rc != OK:
+        raise BsqError(rc, "bsq_gemm_splitk")
+    return out
+
+
 def gemm_gelu(qa: QTensor, qb: QTensor, bias: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
               stream=None) -> torch.Tensor:
     """out[M, N] = bf16(GELU(alpha * A_hat . B_hat^T + bias)), GELU in its erf form."""
@@ -371,9 +410,10 @@ def linear_backward(dy: torch.Tensor, x_col: QTensor, w_col: QTensor, stochastic
     quantized in both layouts in one pass, then dX = dY . W (dY row-wise against W column-wise,
     M x K) and dW = dY^T . X (dY column-wise against X column-wise, N x K), both bf16 with fp32
     accumulation. x_col / w_col are the column-wise operands of X (M x K) and W (N x K) from
-    quantize_dual (K x M and K x N). Returns (dX, dW)."""
+    quantize_dual (K x M and K x N). dW (few output tiles, K = the token count) goes through
+    gemm_splitk with the library's split count. Returns (dX, dW)."""
     dy_row, dy_col = quantize_dual(x_col.fmt, dy, stochastic=stochastic, seed=seed, stream=stream)
-    return gemm(dy_row, w_col, stream=stream), gemm(dy_col, x_col, stream=stream)
+    return gemm(dy_row, w_col, stream=stream), gemm_splitk(dy_col, x_col, stream=stream)
 
 
 def convt2x2(qx: QTensor, qw: QTensor, batch: int, H: int, W: int, bias: Optional[torch.Tensor] = None,

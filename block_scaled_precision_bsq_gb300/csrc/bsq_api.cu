@@ -3,6 +3,7 @@
 #include <cuda_runtime.h>
 
 #include <cmath>
+#include <algorithm>
 #include <cstdint>
 #include <mutex>
 
@@ -226,6 +227,39 @@ int bsq_gemm(int fmt, const void* A, const void* A_scales, const void* B, const 
   const int st = check_gemm(fmt, A, A_scales, B, B_scales, bias_bf16, out_bf16, M, N, K);
   if (st != BSQ_OK) return fail(st);
   return gemm_common(fmt, 0, A, A_scales, B, B_scales, bias_bf16, out_bf16, nullptr, M, N, K, stream);
+}
+
+int bsq_gemm_splitk(int fmt, const void* A, const void* A_scales, const void* B, const void* B_scales,
+                    const void* bias_bf16, void* out_bf16, int64_t M, int64_t N, int64_t K, int splits,
+                    void* workspace, size_t workspace_bytes, bsq_stream_t stream) {
+  const int st = check_gemm(fmt, A, A_scales, B, B_scales, bias_bf16, out_bf16, M, N, K);
+  if (st != BSQ_OK) return fail(st);
+  const int64_t stages = K / (fmt == BSQ_MXFP8 ? 128 : 256);
+  if (splits < 1 || splits > 8 || splits > stages) return fail(BSQ_ERR_ARG);
+  if (splits == 1) return gemm_common(fmt, 0, A, A_scales, B, B_scales, bias_bf16, out_bf16, nullptr, M, N, K, stream);
+  if (workspace == nullptr || workspace_bytes / 4 / static_cast<size_t>(splits) / static_cast<size_t>(M) <
+                                  static_cast<size_t>(N))
+    return fail(BSQ_ERR_ARG);
+  if (!aligned16(workspace)) return fail(BSQ_ERR_ALIGN);
+  const bsq::DeviceInfo* dev = bsq::current_device();
+  if (dev == nullptr) return fail(BSQ_ERR_ARCH);
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int rc = bsq::launch_gemm(fmt, 6, A, A_scales, B, B_scales, nullptr, workspace, nullptr, M, N, K, s, *dev, 1, splits);
+  if (rc == BSQ_OK)
+    rc = bsq::launch_splitk_finalize(fmt, static_cast<const float*>(workspace), splits, M, N, K, bias_bf16, A_scales,
+                                     B_scales, out_bf16, s, *dev);
+  return rc == BSQ_OK ? BSQ_OK : fail(rc);
+}
+
+int bsq_gemm_splitk_splits(int fmt, int64_t M, int64_t N, int64_t K) {
+  if (fmt != BSQ_MXFP8 && fmt != BSQ_NVFP4 && fmt != BSQ_MXFP4) return fail(BSQ_ERR_ARG);
+  if (M <= 0 || N <= 0 || K <= 0) return fail(BSQ_ERR_ARG);
+  const bsq::DeviceInfo* dev = bsq::current_device();
+  if (dev == nullptr) return fail(BSQ_ERR_ARCH);
+  const int64_t tiles = bsq::ceil_div(bsq::ceil_div(M, 128), 2) * bsq::ceil_div(N, 256);
+  const int64_t stages = K / (fmt == BSQ_MXFP8 ? 128 : 256);
+  const int64_t s = std::min<int64_t>(std::min<int64_t>(dev->num_sms / 2 / tiles, 8), stages / 8);
+  return static_cast<int>(std::max<int64_t>(s, 1));
 }
 
 int bsq_gemm_gelu(int fmt, const void* A, const void* A_scales, const void* B, const void* B_scales,

@@ -130,7 +130,29 @@ __host__ __device__ constexpr uint32_t make_idesc(uint32_t sf_id) {
 // kEpiConvTGelu: the head's kernel-2 stride-2 transposed convolution (same README section: the
 // ScaleBlocks' ConvT, then GELU): column n = (2 dy + dx) C_out + co of output row (b, h, w) is
 // stored at pixel (b, 2h + dy, 2w + dx), channel co, of the NHWC output, with bias[co].
-enum EpiMode { kEpiBf16 = 0, kEpiGeluBf16 = 1, kEpiGeluMxfp8 = 2, kEpiGeluMxfp4 = 3, kEpiConvT = 4, kEpiConvTGelu = 5 };
+// kEpiF32Partial: split-K -- K is cut into `splits` equal ranges of stages, the work units are
+// (tile, range) pairs, and each unit stores its raw fp32 accumulator (no alpha, no bias) into
+// slice `range` of an fp32 workspace of splits x M x N; splitk_finalize_kernel sums the slices.
+// For shapes with fewer tiles than SM pairs and a long K (the weight gradient dW = dY^T X:
+// M, N the weight's shape, K the token count), where one unit per tile leaves SMs idle.
+enum EpiMode {
+  kEpiBf16 = 0,
+  kEpiGeluBf16 = 1,
+  kEpiGeluMxfp8 = 2,
+  kEpiGeluMxfp4 = 3,
+  kEpiConvT = 4,
+  kEpiConvTGelu = 5,
+  kEpiF32Partial = 6
+};
+
+// 3-D tile store (coordinates innermost first).
+__device__ __forceinline__ void tma_store_3d(const void* tmap, const void* smem_src, int32_t c0, int32_t c1,
+                                             int32_t c2) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(tmap)),
+               "r"(smem_u32(smem_src)), "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
 
 // Packed fp32 pairs for the epilogue: two values in one 64-bit operand (`lo` in bits 0..31) of
 // the f32x2 instructions, each lane rounded to nearest even exactly like the scalar operation.
@@ -201,6 +223,7 @@ struct GemmArgs {
   const float* gb;
   int M, N;
   int tiles_n, num_pairs;
+  int splits, num_units;  // split-K ranges (1 outside kEpiF32Partial); work units = num_pairs * splits
   int nk;  // stages per tile: K bytes / 128
   int cv_c, cv_w;  // ConvT epilogues: output channels C_out, input width W
   int* status;
@@ -272,10 +295,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    for (int pt = first_pair; pt < args.num_pairs && ok; pt += pair_stride) {
+    for (int u = first_pair; u < args.num_units && ok; u += pair_stride) {
+      const int split = u / args.num_pairs, pt = u - split * args.num_pairs;
       const int m_blk = 2 * (pt / args.tiles_n) + static_cast<int>(rank);
       const int n_blk = pt % args.tiles_n;
-      for (int kb = 0; kb < args.nk; ++kb) {
+      const int kb1 = (split + 1) * args.nk / args.splits;
+      for (int kb = split * args.nk / args.splits; kb < kb1; ++kb) {
         if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1u, abort_flag, args.status)) {
           ok = false;
           break;
@@ -306,12 +331,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sfa_s0 = smem_u32(smem + L::sfa_off);
     const uint32_t sfb_s0 = smem_u32(smem + L::sfb_off);
     const uint32_t sf_t0 = tmem_base + kAccCols;
-    for (int pt = first_pair; pt < args.num_pairs && ok; pt += pair_stride) {
+    for (int u = first_pair; u < args.num_units && ok; u += pair_stride) {
+      const int split = u / args.num_pairs;
+      const int kb0 = split * args.nk / args.splits, kb1 = (split + 1) * args.nk / args.splits;
       // wait until both CTAs' epilogues have drained the accumulator of the previous tile
       if (!mbar_wait_bounded_warp(tmem_empty, acc_phase ^ 1u, abort_flag, args.status)) break;
       acc_phase ^= 1u;
       tc_fence_after();
-      for (int kb = 0; kb < args.nk; ++kb) {
+      for (int kb = kb0; kb < kb1; ++kb) {
         // both CTAs' operands of the stage landed
         if (!mbar_wait_bounded_warp(&full_bar[stage], phase, abort_flag, args.status)) {
           ok = false;
@@ -352,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               id = 2 * (k & 1);
             }
             tc_mma_pair<FMT>(tmem_base, adesc + 2 * k, bdesc + 2 * k, make_idesc<FMT>(id), sfa, sfb,
-                             (k > 0 || kb > 0) ? 1u : 0u);
+                             (k > 0 || kb > kb0) ? 1u : 0u);
           }
           tc_commit_pair_mc(&empty_bar[stage], 0x3);  // both CTAs' stage is free once these MMAs read it
         }
@@ -382,7 +409,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     float alpha = 1.0f;
     if constexpr (FMT == BSQ_NVFP4) alpha = __fmul_rn(*args.ga, *args.gb);
     uint32_t acc_phase = 0;
-    for (int pt = first_pair; pt < args.num_pairs; pt += pair_stride) {
+    for (int u = first_pair; u < args.num_units; u += pair_stride) {
+      const int split = u / args.num_pairs, pt = u - split * args.num_pairs;
       const int m_blk = 2 * (pt / args.tiles_n) + static_cast<int>(rank);
       const int n_blk = pt % args.tiles_n;
       const int n0 = n_blk * BN + half * 128;
@@ -460,13 +488,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       // store: chunks of 32 rows x RB bytes through the staging buffer and TMA
       constexpr int EC = C::kEpiCols;
       constexpr int RB = EC * 2;  // bytes of a staged row: 64 or 32
-      constexpr int kRowBytes = (EPI == kEpiGeluMxfp8) ? 128 : (EPI == kEpiGeluMxfp4 ? 64 : 256);
+      constexpr int kRowBytes =
+          (EPI == kEpiF32Partial) ? 512 : (EPI == kEpiGeluMxfp8) ? 128 : (EPI == kEpiGeluMxfp4 ? 64 : 256);
       const int row_units = (EPI == kEpiGeluMxfp4) ? (args.N >> 1) : args.N;  // TMA x extent of a row
 #pragma unroll
       for (int j = 0; j < kRowBytes / RB; ++j) {
         constexpr bool kBf16Out = (EPI == kEpiBf16 || EPI == kEpiGeluBf16 || EPI == kEpiConvT || EPI == kEpiConvTGelu);
         int x;  // first TMA x coordinate of the chunk (bf16 elements or code bytes)
         if constexpr (kBf16Out) x = n0 + (RB / 2) * j;
+        else if constexpr (EPI == kEpiF32Partial) x = n0 + (RB / 4) * j;  // fp32 elements
         else if constexpr (EPI == kEpiGeluMxfp8) x = n0 + RB * j;
         else x = (n0 >> 1) + RB * j;
         if (x >= row_units || m0 >= args.M) break;  // nothing of this chunk is stored (warp-uniform)
@@ -480,6 +510,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             value2(col, lo, hi);
             __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
             packed[c] = *reinterpret_cast<uint32_t*>(&p);
+          } else if constexpr (EPI == kEpiF32Partial) {
+            const int col = (RB / 4) * j + c;  // the raw fp32 accumulator
+            packed[c] = acc[col >> 5][col & 31];
           } else if constexpr (EPI == kEpiGeluMxfp8) {
             const int col = RB * j + 4 * c;  // four E4M3 codes per word, one block
             const float m = mul[col >> 5];
@@ -518,6 +551,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int tap = x / args.cv_c, co = x - tap * args.cv_c;
             const int bh = m0 / args.cv_w, w0 = m0 - bh * args.cv_w;
             tma_store_5d(&mapOut, stage_buf, co, tap & 1, w0, tap >> 1, bh);
+          } else if constexpr (EPI == kEpiF32Partial) {
+            tma_store_3d(&mapOut, stage_buf, x, m0, split);  // slice `split` of the workspace
           } else {
             tma_store_2d(&mapOut, stage_buf, x, m0);
           }
@@ -624,9 +659,23 @@ bool make_map_convt_out(CUtensorMap* map, void* out, int64_t cout, int64_t W, in
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The split-K workspace: `splits` slices of M x N fp32, row-major, as a 3-D tensor (n, m, slice);
+// one box = one epilogue chunk of 16 columns x 32 rows (64-byte rows, 64-byte swizzle).
+bool make_map_partial(CUtensorMap* map, void* ws, int64_t M, int64_t N, int splits) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M), static_cast<cuuint64_t>(splits)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(N) * 4, static_cast<cuuint64_t>(M * N) * 4};
+  const cuuint32_t box[3] = {16, 32, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ws, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int FMT, int EPI>
 int run_gemm(const void* A, const void* A_scales, const void* B, const void* B_scales, const void* bias, void* out,
-             void* out_scales, int64_t M, int64_t N, int64_t K, int64_t cv_w, cudaStream_t stream,
+             void* out_scales, int64_t M, int64_t N, int64_t K, int64_t cv_w, int splits, cudaStream_t stream,
              const DeviceInfo& dev) {
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
@@ -647,7 +696,10 @@ int run_gemm(const void* A, const void* A_scales, const void* B, const void* B_s
   constexpr int EC = Cfg<FMT>::kEpiCols;
   const CUtensorMapSwizzle osw = EC == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
   bool ok_out;
-  if constexpr (EPI == kEpiConvT || EPI == kEpiConvTGelu) {
+  if constexpr (EPI == kEpiF32Partial) {
+    static_assert(EC == 32, "fp32 partial chunks are 16 columns = 64-byte rows, the staging of 32 bf16 columns");
+    ok_out = make_map_partial(&mOut, out, M, N, splits);
+  } else if constexpr (EPI == kEpiConvT || EPI == kEpiConvTGelu) {
     ok_out = make_map_convt_out(&mOut, out, N / 4, cv_w, M / cv_w, EC, osw);
   } else if constexpr (EPI == kEpiBf16 || EPI == kEpiGeluBf16) {
     ok_out = make_map_2d(&mOut, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, out, N, M, static_cast<uint64_t>(N) * 2, EC, 32, osw);
@@ -678,8 +730,10 @@ int run_gemm(const void* A, const void* A_scales, const void* B, const void* B_s
   a.nk = static_cast<int>(kbytes / kChunkBytes);
   a.cv_c = static_cast<int>(N / 4);
   a.cv_w = static_cast<int>(cv_w);
+  a.splits = (EPI == kEpiF32Partial) ? splits : 1;
+  a.num_units = a.num_pairs * a.splits;
   a.status = dev.status;
-  const int clusters = std::min(a.num_pairs, std::min(max_clusters, dev.num_sms / 2));
+  const int clusters = std::min(a.num_units, std::min(max_clusters, dev.num_sms / 2));
 
   cudaLaunchAttribute at[2];
   cudaLaunchConfig_t cfg = pair_launch_config(at, clusters, kThreads, Smem<FMT>::alloc, stream);
@@ -688,11 +742,50 @@ int run_gemm(const void* A, const void* A_scales, const void* B, const void* B_s
   return cudaGetLastError() == cudaSuccess ? BSQ_OK : BSQ_ERR_LAUNCH;
 }
 
+// out[m, n] = bf16(fmaf(sum_s ws[s][m][n], alpha, bias[n])): the split-K partial sums added in
+// slice order, then the GEMM's own epilogue arithmetic (alpha = g_A g_B for NVFP4; for MX alpha
+// is 1 and the fma is the plain add acc + bias). Eight consecutive columns per thread (N % 8 == 0).
+__global__ void __launch_bounds__(256)
+    splitk_finalize_kernel(const float* ws, int splits, int64_t mn, int N, const uint16_t* bias, const float* ga,
+                           const float* gb, uint16_t* out) {
+  grid_dependency_wait();  // the partial sums come from the previous kernel
+  const float alpha = ga != nullptr ? __fmul_rn(*ga, *gb) : 1.0f;
+  const int64_t n8 = mn / 8;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t e = i * 8;
+    float v[8];
+    {
+      const float4* p = reinterpret_cast<const float4*>(ws + e);
+      const float4 a = p[0], b = p[1];
+      v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    }
+    for (int sl = 1; sl < splits; ++sl) {
+      const float4* p = reinterpret_cast<const float4*>(ws + sl * mn + e);
+      const float4 a = p[0], b = p[1];
+      const float t[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int k = 0; k < 8; ++k) v[k] = __fadd_rn(v[k], t[k]);
+    }
+    const int n = static_cast<int>(e % N);
+    uint32_t w[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float b0 = bias != nullptr ? __uint_as_float(static_cast<uint32_t>(bias[n + 2 * k]) << 16) : 0.0f;
+      const float b1 = bias != nullptr ? __uint_as_float(static_cast<uint32_t>(bias[n + 2 * k + 1]) << 16) : 0.0f;
+      __nv_bfloat162 h = __floats2bfloat162_rn(__fmaf_rn(v[2 * k], alpha, b0), __fmaf_rn(v[2 * k + 1], alpha, b1));
+      w[k] = *reinterpret_cast<uint32_t*>(&h);
+    }
+    *reinterpret_cast<uint4*>(out + e) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+  launch_dependents();
+}
+
 template <int FMT>
 int run_gemm_epi(int epi, const void* A, const void* A_scales, const void* B, const void* B_scales, const void* bias,
-                 void* out, void* out_scales, int64_t M, int64_t N, int64_t K, int64_t cv_w, cudaStream_t stream,
-                 const DeviceInfo& dev) {
-#define BSQ_RUN(E) run_gemm<FMT, E>(A, A_scales, B, B_scales, bias, out, out_scales, M, N, K, cv_w, stream, dev)
+                 void* out, void* out_scales, int64_t M, int64_t N, int64_t K, int64_t cv_w, int splits,
+                 cudaStream_t stream, const DeviceInfo& dev) {
+#define BSQ_RUN(E) run_gemm<FMT, E>(A, A_scales, B, B_scales, bias, out, out_scales, M, N, K, cv_w, splits, stream, dev)
   switch (epi) {
     case kEpiBf16: return BSQ_RUN(kEpiBf16);
     case kEpiGeluBf16: return BSQ_RUN(kEpiGeluBf16);
@@ -700,6 +793,7 @@ int run_gemm_epi(int epi, const void* A, const void* A_scales, const void* B, co
     case kEpiGeluMxfp4: return BSQ_RUN(kEpiGeluMxfp4);
     case kEpiConvT: return BSQ_RUN(kEpiConvT);
     case kEpiConvTGelu: return BSQ_RUN(kEpiConvTGelu);
+    case kEpiF32Partial: return BSQ_RUN(kEpiF32Partial);
     default: return BSQ_ERR_ARG;
   }
 #undef BSQ_RUN
@@ -709,17 +803,46 @@ int run_gemm_epi(int epi, const void* A, const void* A_scales, const void* B, co
 
 int launch_gemm(int fmt, int epi, const void* A, const void* A_scales, const void* B, const void* B_scales,
                 const void* bias, void* out, void* out_scales, int64_t M, int64_t N, int64_t K, cudaStream_t stream,
-                const DeviceInfo& dev, int64_t convt_w) {
+                const DeviceInfo& dev, int64_t convt_w, int splits) {
   switch (fmt) {
     case BSQ_MXFP8:
-      return run_gemm_epi<BSQ_MXFP8>(epi, A, A_scales, B, B_scales, bias, out, out_scales, M, N, K, convt_w, stream, dev);
+      return run_gemm_epi<BSQ_MXFP8>(epi, A, A_scales, B, B_scales, bias, out, out_scales, M, N, K, convt_w, splits,
+                                     stream, dev);
     case BSQ_NVFP4:
-      return run_gemm_epi<BSQ_NVFP4>(epi, A, A_scales, B, B_scales, bias, out, out_scales, M, N, K, convt_w, stream, dev);
+      return run_gemm_epi<BSQ_NVFP4>(epi, A, A_scales, B, B_scales, bias, out, out_scales, M, N, K, convt_w, splits,
+                                     stream, dev);
     case BSQ_MXFP4:
-      return run_gemm_epi<BSQ_MXFP4>(epi, A, A_scales, B, B_scales, bias, out, out_scales, M, N, K, convt_w, stream, dev);
+      return run_gemm_epi<BSQ_MXFP4>(epi, A, A_scales, B, B_scales, bias, out, out_scales, M, N, K, convt_w, splits,
+                                     stream, dev);
     default:
       return BSQ_ERR_ARG;
   }
+}
+
+int launch_splitk_finalize(int fmt, const float* ws, int splits, int64_t M, int64_t N, int64_t K, const void* bias,
+                           const void* A_scales, const void* B_scales, void* out, cudaStream_t stream,
+                           const DeviceInfo& dev) {
+  const float* ga = nullptr;
+  const float* gb = nullptr;
+  if (fmt == BSQ_NVFP4) {
+    ga = reinterpret_cast<const float*>(static_cast<const uint8_t*>(A_scales) + scales_body_bytes(fmt, M, K));
+    gb = reinterpret_cast<const float*>(static_cast<const uint8_t*>(B_scales) + scales_body_bytes(fmt, N, K));
+  }
+  const int64_t n8 = M * N / 8;
+  const int64_t blocks = std::min<int64_t>(ceil_div(n8, 256), static_cast<int64_t>(dev.num_sms) * 8);
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(std::max<int64_t>(blocks, 1)));
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, splitk_finalize_kernel, ws, splits, M * N, static_cast<int>(N),
+                         static_cast<const uint16_t*>(bias), ga, gb, static_cast<uint16_t*>(out)) != cudaSuccess)
+    return BSQ_ERR_LAUNCH;
+  return cudaGetLastError() == cudaSuccess ? BSQ_OK : BSQ_ERR_LAUNCH;
 }
 
 }  // namespace bsq

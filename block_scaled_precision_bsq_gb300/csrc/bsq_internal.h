@@ -71,10 +71,17 @@ int launch_quantize_dual(int fmt, bool src_f32, bool stochastic, bool global_giv
 
 // epi: 0 bf16 out, 1 GELU -> bf16, 2 GELU -> MXFP8 codes + scales, 3 GELU -> MXFP4 (out_scales
 // used by 2 and 3 only), 4 / 5 kernel-2 stride-2 transposed convolution to NHWC bf16 (without /
-// with GELU; N = 4 C_out, M = batch H W, convt_w = W).
+// with GELU; N = 4 C_out, M = batch H W, convt_w = W), 6 split-K partial sums: `out` is an fp32
+// workspace of splits x M x N (slice s = K stages [s nk / splits, (s + 1) nk / splits), raw
+// accumulator; 1 <= splits <= K stages).
 int launch_gemm(int fmt, int epi, const void* A, const void* A_scales, const void* B, const void* B_scales,
                 const void* bias, void* out, void* out_scales, int64_t M, int64_t N, int64_t K, cudaStream_t stream,
-                const DeviceInfo& dev, int64_t convt_w = 1);
+                const DeviceInfo& dev, int64_t convt_w = 1, int splits = 1);
+
+// out_bf16 = bf16(alpha * sum of the workspace's slices + bias), after launch_gemm epi 6.
+int launch_splitk_finalize(int fmt, const float* ws, int splits, int64_t M, int64_t N, int64_t K, const void* bias,
+                           const void* A_scales, const void* B_scales, void* out, cudaStream_t stream,
+                           const DeviceInfo& dev);
 
 int launch_selftest_timeout(int64_t limit_ns, cudaStream_t stream, const DeviceInfo& dev);
 

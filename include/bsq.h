@@ -217,6 +217,37 @@ int bsq_gemm(int fmt, const void* A, const void* A_scales, const void* B, const 
              const void* bias_bf16, void* out_bf16, int64_t M, int64_t N, int64_t K, bsq_stream_t stream);
 
 /*
+ * bsq_gemm_splitk: bsq_gemm's result computed with the K dimension cut into `splits` equal
+ * ranges of K stages (128 K for MXFP8, 256 for NVFP4 / MXFP4), each (output tile, range) pair
+ * one unit of work, for shapes with fewer 256 x 256 output tiles than the GPU has SM pairs and
+ * a long K: the weight gradient dW = dY^T X of a linear layer ("lightly-train - DINOv3 + EoMT
+ * on RTX 5090" README, section 4.3: the training stacks' wgrad GEMM; M, N the weight's shape, K
+ * the token count) has 36 tiles for 76 SM pairs at ViT-B/16 fc1. The method has no split-K of
+ * its own: this is an engineering entry point. Each unit stores its raw fp32 sum into slice r
+ * of `workspace`; a second kernel adds the slices in order (deterministic) and applies alpha,
+ * the bias and the bf16 rounding as bsq_gemm does. The fp32 sum therefore rounds in a different
+ * order than bsq_gemm's (within the same tolerance).
+ *   splits           1..8 and at most the number of K stages; 1 is bsq_gemm itself
+ *   workspace        splits * M * N fp32 in device memory, 16-byte aligned, owned by the caller;
+ *                    overwritten, no initial contents needed; unused when splits == 1
+ *   workspace_bytes  its size, at least splits * M * N * 4 (else BSQ_ERR_ARG)
+ * Other arguments, shapes and errors as bsq_gemm; two launches on `stream`.
+ */
+int bsq_gemm_splitk(int fmt, const void* A, const void* A_scales, const void* B, const void* B_scales,
+                    const void* bias_bf16, void* out_bf16, int64_t M, int64_t N, int64_t K, int splits,
+                    void* workspace, size_t workspace_bytes, bsq_stream_t stream);
+
+/*
+ * bsq_gemm_splitk_splits: the number of K ranges bsq_gemm_splitk should use on the current
+ * device for an M x N x K product: floor(SM pairs / output tiles of 256 x 256), at most 8 and at
+ * most K stages / 8 (each range keeps at least 8 stages of the operand pipeline), at least 1 --
+ * 2 for ViT-B/16 fc1's weight gradient (36 tiles, 76 SM pairs), 1 for every forward GEMM of the
+ * ViT shapes. Returns the count, or a negative error (BSQ_ERR_ARG for an unknown format or a
+ * non-positive size, BSQ_ERR_ARCH without a usable device).
+ */
+int bsq_gemm_splitk_splits(int fmt, int64_t M, int64_t N, int64_t K);
+
+/*
  * bsq_gemm_gelu: as bsq_gemm with out = bf16_rn(GELU(v)), v = alpha * sum_k Ahat Bhat + bias
  * in fp32, GELU the erf form 0.5 v (1 + erf(v / sqrt 2)) (the "fc1 + GELU" epilogue of every
  * stack in the "lightly-train - DINOv3 + EoMT on RTX 5090" README, section 4.3), evaluated in
