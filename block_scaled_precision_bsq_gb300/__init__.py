@@ -63,6 +63,8 @@ _lib.bsq_convt2x2.restype = _int
 _lib.bsq_gemm.argtypes = [_int, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp]
 _lib.bsq_gemm_splitk.restype = _int
 _lib.bsq_gemm_splitk.argtypes = [_int, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _vp, ctypes.c_size_t, _vp]
+_lib.bsq_gemm_splitk_scratch.restype = _int
+_lib.bsq_gemm_splitk_scratch.argtypes = [_int, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _vp]
 _lib.bsq_gemm_splitk_splits.restype = _int
 _lib.bsq_gemm_splitk_splits.argtypes = [_int, _i64, _i64, _i64]
 _lib.bsq_gemm_gelu.restype = _int
@@ -79,6 +81,7 @@ _lib.bsq_strerror.argtypes = [_int]
 
 EXPORTS = ("bsq_codes_bytes", "bsq_scales_bytes", "bsq_quantize", "bsq_quantize_batch", "bsq_layernorm_quantize",
            "bsq_quantize_dual", "bsq_delayed_global_scale", "bsq_gemm", "bsq_gemm_splitk", "bsq_gemm_splitk_splits",
+           "bsq_gemm_splitk_scratch",
            "bsq_gemm_gelu", "bsq_gemm_gelu_quantize", "bsq_convt2x2", "bsq_get_device_status", "bsq_selftest_timeout",
            "bsq_last_error", "bsq_strerror")
 
@@ -166,6 +169,12 @@ def bsq_gemm_splitk(fmt, A: Ptr, A_scales: Ptr, B: Ptr, B_scales: Ptr, bias: Ptr
                     splits: int, workspace: Ptr, workspace_bytes: int, stream=None) -> int:
     return int(_lib.bsq_gemm_splitk(_fmt(fmt), _p(A), _p(A_scales), _p(B), _p(B_scales), _p(bias), _p(out), M, N, K,
                                     splits, _p(workspace), workspace_bytes, _stream(stream)))
+
+
+def bsq_gemm_splitk_scratch(fmt, A: Ptr, A_scales: Ptr, B: Ptr, B_scales: Ptr, bias: Ptr, out: Ptr, M: int, N: int,
+                            K: int, splits: int, stream=None) -> int:
+    return int(_lib.bsq_gemm_splitk_scratch(_fmt(fmt), _p(A), _p(A_scales), _p(B), _p(B_scales), _p(bias), _p(out),
+                                            M, N, K, splits, _stream(stream)))
 
 
 def bsq_gemm_splitk_splits(fmt, M: int, N: int, K: int) -> int:

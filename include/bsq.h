@@ -248,6 +248,25 @@ int bsq_gemm_splitk(int fmt, const void* A, const void* A_scales, const void* B,
 int bsq_gemm_splitk_splits(int fmt, int64_t M, int64_t N, int64_t K);
 
 /*
+ * bsq_gemm_splitk_scratch: bsq_gemm_splitk with the workspace taken from a fixed 64 MiB device
+ * array inside the library instead of a caller buffer, so that a call allocates nothing. The
+ * pages describe no counterpart: an engineering entry point.
+ *   - The array is placed with the library's device module, once per device; its address is
+ *     looked up once per device. No call allocates or frees memory.
+ *   - Limit: splits * M * N * 4 bytes <= 64 MiB; a larger request fails with BSQ_ERR_ARG, as
+ *     bsq_gemm_splitk does with too small a workspace (splits == 1 needs none).
+ *   - Nothing needs to start at zero: each call overwrites the part of the array it uses before
+ *     reading it.
+ *   - The array is shared by every caller in the process on that device: calls that can overlap
+ *     in time (on different streams, or from different host threads) race on it; the caller
+ *     orders them.
+ * Other arguments, results and errors as bsq_gemm_splitk.
+ */
+int bsq_gemm_splitk_scratch(int fmt, const void* A, const void* A_scales, const void* B, const void* B_scales,
+                            const void* bias_bf16, void* out_bf16, int64_t M, int64_t N, int64_t K, int splits,
+                            bsq_stream_t stream);
+
+/*
  * bsq_gemm_gelu: as bsq_gemm with out = bf16_rn(GELU(v)), v = alpha * sum_k Ahat Bhat + bias
  * in fp32, GELU the erf form 0.5 v (1 + erf(v / sqrt 2)) (the "fc1 + GELU" epilogue of every
  * stack in the "lightly-train - DINOv3 + EoMT on RTX 5090" README, section 4.3), evaluated in
