@@ -8,7 +8,7 @@
 // the BF16 ledger blog section 5.4; 6 for e2m1). The UE8M0 exponent of a block is
 // floor(log2(amax)) - emax with emax the exponent of the element format's top binade.
 //
-// Work mapping (four CTAs per SM, persistent). The source is cut into chunks of whole rows
+// Work mapping (four CTAs per SM for MX, two for NVFP4; persistent). The source is cut into chunks of whole rows
 // (or, for rows longer than a chunk, row pieces of whole 1024-element segments); a chunk is
 // contiguous in memory and comes in with one 1-D TMA bulk copy. A producer thread per CTA
 // keeps a ring of up to kRing chunk buffers in flight -- for a 22 MB matrix that is nearly
@@ -35,12 +35,8 @@
 namespace bsq {
 namespace {
 
-constexpr int kThreads = 256;          // warp 0: TMA producer (lane 0); warps 1..7: consumers
-constexpr int kConsumerWarps = kThreads / 32 - 1;
 constexpr int kLaneElems = 32;         // elements per lane per step: one MX block, two NVFP4 blocks
 constexpr int kSeg = 32 * kLaneElems;   // elements per warp step
-constexpr int kRing = 3;                // chunk buffers per CTA
-constexpr int kCtasPerSm = 4;           // four resident CTAs (28 consumer warps per SM) to hide latency
 constexpr int kChunkMax = 16384;        // bytes per chunk buffer
 constexpr int kChunkMin = 4096;         // smallest chunk worth a copy (small tensors)
 constexpr int kAmaxThreads = 256;
@@ -48,6 +44,20 @@ constexpr int kMaxBatch = BSQ_MAX_BATCH;
 constexpr int kLnMaxRows = kChunkMax / (32 * 2);  // rows of a chunk: rows of at least 32 bf16
 
 enum NvMode { kMx = 0, kNvComputed = 1, kNvGiven = 2 };
+
+// Occupancy per format (warp 0's lane 0 is the TMA producer, the other warps consume): MX, four
+// resident CTAs of 256 threads with a 3-chunk ring each (28 consumer warps per SM to hide
+// latency, 64 registers); NVFP4, whose IEEE divisions need more registers, two CTAs of 384
+// threads with a 6-chunk ring (72 registers; at 64 it spilled and ran 8-15 % slower).
+template <bool NV>
+struct QCfg {
+  static constexpr int kThreads = NV ? 384 : 256;
+  static constexpr int kCtasPerSm = NV ? 2 : 4;
+  static constexpr int kRing = NV ? 6 : 3;
+  static constexpr int kConsumerWarps = kThreads / 32 - 1;
+  static constexpr int kSmem = kRing * kChunkMax + 128;
+};
+inline int ctas_per_sm(int fmt) { return fmt == BSQ_NVFP4 ? QCfg<true>::kCtasPerSm : QCfg<false>::kCtasPerSm; }
 
 struct QuantArgs {
   const uint8_t* src;
@@ -174,7 +184,11 @@ __device__ __forceinline__ uint32_t quantize32(const float (&x)[32], float g, fl
 }
 
 template <int FMT, bool F32, int NV, bool LN>
-__global__ void __launch_bounds__(kThreads, kCtasPerSm) quantize_kernel(const __grid_constant__ QuantBatch batch) {
+__global__ void __launch_bounds__(QCfg<NV != kMx>::kThreads, QCfg<NV != kMx>::kCtasPerSm)
+    quantize_kernel(const __grid_constant__ QuantBatch batch) {
+  constexpr int kThreads = QCfg<NV != kMx>::kThreads;
+  constexpr int kRing = QCfg<NV != kMx>::kRing;
+  constexpr int kConsumerWarps = QCfg<NV != kMx>::kConsumerWarps;
   constexpr int kEsize = F32 ? 4 : 2;
   extern __shared__ uint8_t q_smem_raw[];
   uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(q_smem_raw) + 127) & ~uintptr_t(127));
@@ -538,12 +552,11 @@ __global__ void __launch_bounds__(kAmaxThreads) amax_kernel(const uint4* src, in
   }
 }
 
-constexpr int kQuantSmem = kRing * kChunkMax + 128;
-
 template <int FMT, bool F32, int NV, bool LN = false>
 cudaError_t launch_q(const QuantBatch& b, int grid, cudaStream_t stream) {
+  using Q = QCfg<NV != kMx>;
   static cudaError_t attr = cudaFuncSetAttribute(quantize_kernel<FMT, F32, NV, LN>,
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kQuantSmem);
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, Q::kSmem);
   if (attr != cudaSuccess) return attr;
   // programmatic dependent launch: the kernel may be launched while the previous kernel in
   // the stream finishes; it waits for it (grid_dependency_wait) before touching memory
@@ -552,8 +565,8 @@ cudaError_t launch_q(const QuantBatch& b, int grid, cudaStream_t stream) {
   at[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kQuantSmem;
+  cfg.blockDim = dim3(Q::kThreads);
+  cfg.dynamicSmemBytes = Q::kSmem;
   cfg.stream = stream;
   cfg.attrs = at;
   cfg.numAttrs = 1;
@@ -608,7 +621,7 @@ void build_batch(QuantBatch& b, int fmt, bool src_f32, int count, const QuantIte
   int64_t total_bytes = 0;
   for (int i = 0; i < count; ++i) total_bytes += items[i].rows * items[i].cols * esize;
   const int64_t target = std::max<int64_t>(
-      kChunkMin, std::min<int64_t>(kChunkMax, total_bytes / (4 * kCtasPerSm * static_cast<int64_t>(dev.num_sms))));
+      kChunkMin, std::min<int64_t>(kChunkMax, total_bytes / (4 * ctas_per_sm(fmt) * static_cast<int64_t>(dev.num_sms))));
   b.chunk_start[0] = 0;
   for (int i = 0; i < count; ++i) {
     const QuantItem& it = items[i];
@@ -647,7 +660,8 @@ int launch_quantize_batch(int fmt, bool src_f32, bool global_given, int count, c
   if (count < 1 || count > kMaxBatch) return BSQ_ERR_ARG;
   QuantBatch b{};
   build_batch(b, fmt, src_f32, count, items, dev);
-  const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(b.chunk_start[count], kCtasPerSm * dev.num_sms)));
+  const int grid =
+      static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(b.chunk_start[count], ctas_per_sm(fmt) * dev.num_sms)));
 
   cudaError_t err = cudaSuccess;
   if (fmt == BSQ_NVFP4) {
@@ -680,7 +694,8 @@ int launch_layernorm_quantize(int fmt, bool src_f32, const QuantItem& item, cons
   b.t[0].gamma = gamma;
   b.t[0].beta = beta;
   b.t[0].eps = eps;
-  const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(b.chunk_start[1], kCtasPerSm * dev.num_sms)));
+  const int grid =
+      static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(b.chunk_start[1], ctas_per_sm(fmt) * dev.num_sms)));
   cudaError_t err;
   if (fmt == BSQ_MXFP8) {
     err = src_f32 ? launch_q<BSQ_MXFP8, true, kMx, true>(b, grid, stream) : launch_q<BSQ_MXFP8, false, kMx, true>(b, grid, stream);
