@@ -138,3 +138,24 @@ def test_gemm_partial_last_stage(fmt, K):
     out = bsq.gemm(_qtensor_from_oracle(qa), _qtensor_from_oracle(qb), None)
     assert bsq.device_status() == 0
     check_gemm_rows(bf16_to_f64(out), qa, qb, None, np.arange(M), "%s K=%d" % (fmt, K))
+
+
+@pytest.mark.parametrize("fmt", ["mxfp8", "nvfp4", "mxfp4"])
+@pytest.mark.parametrize("M,N", [(1, 8), (33, 24), (130, 136), (257, 8)])
+def test_gemm_narrow_n_and_single_stage_k(fmt, M, N):
+    """The smallest legal shapes: N of 8 (one 16-byte bf16 row piece; the tile's store boxes
+    clip at N), ragged M across the pair's two CTAs, and K of one pipeline stage (128 for MXFP8,
+    256 for the FP4 formats); the output buffer is pre-filled so that a store past N or M shows."""
+    bsq = _bsq()
+    K = 128 if fmt == "mxfp8" else 256
+    a = random_matrix(M, K, seed=M * 7 + N, dist="student_t4")
+    b = random_matrix(N, K, seed=N * 5 + M, std=0.02)
+    bias = f32_to_bf16_bits(np.random.default_rng(M + N).standard_normal(N).astype(np.float32) * 0.1)
+    qa, qb = oracle.quantize(fmt, a), oracle.quantize(fmt, b)
+    # a guard region after the M x N output must stay untouched
+    buf = torch.full((M * N + 4096,), 12345, dtype=torch.int16, device="cuda")
+    out = buf[: M * N].view(torch.bfloat16).view(M, N)
+    bsq.gemm(_qtensor_from_oracle(qa), _qtensor_from_oracle(qb), to_dev(bias), out=out)
+    assert bsq.device_status() == 0
+    assert bool((buf[M * N:] == 12345).all())
+    check_gemm_rows(bf16_to_f64(out), qa, qb, bias, np.arange(M), "%s %dx%dx%d" % (fmt, M, N, K))
