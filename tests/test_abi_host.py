@@ -120,5 +120,20 @@ def test_argument_errors_before_any_cuda_call(bsq):
     assert dq(bsq.MXFP8, p, 64, 64, 0, p, p, p, p + 8) == bsq.ERR_ALIGN            # col scales
     assert dq(bsq.MXFP8 | bsq.FLAG_SRC_F32 | bsq.FLAG_STOCHASTIC, p + 4, 64, 64, 2 ** 64 - 1, p, p, p, p) == \
         bsq.ERR_ALIGN
+    sk = bsq.bsq_gemm_splitk
+    ws = 2 * 128 * 256 * 4
+    assert sk(bsq.MXFP8, p, p, p, p, None, p, 128, 256, 96, 2, p, ws) == bsq.ERR_SHAPE       # K % 128
+    assert sk(bsq.MXFP8, p, p, p, p, None, p, 128, 260, 1024, 2, p, ws) == bsq.ERR_SHAPE     # N % 8
+    assert sk(bsq.MXFP8, p, p, p, p, None, p, 128, 256, 1024, 0, p, ws) == bsq.ERR_ARG       # splits
+    assert sk(bsq.MXFP8, p, p, p, p, None, p, 128, 256, 1024, 9, p, ws) == bsq.ERR_ARG
+    assert sk(bsq.NVFP4, p, p, p, p, None, p, 128, 256, 512, 3, p, 3 * ws) == bsq.ERR_ARG    # 2 K stages
+    assert sk(bsq.MXFP8, p, p, p, p, None, p, 128, 256, 1024, 2, None, ws) == bsq.ERR_ARG    # no workspace
+    assert sk(bsq.MXFP8, p, p, p, p, None, p, 128, 256, 1024, 2, p, ws - 1) == bsq.ERR_ARG   # too small
+    assert sk(bsq.MXFP8, p, p, p, p, None, p, 128, 256, 1024, 2, p + 8, ws) == bsq.ERR_ALIGN
+    assert bsq.bsq_gemm_splitk_splits(7, 128, 256, 1024) == bsq.ERR_ARG
+    assert bsq.bsq_gemm_splitk_splits(bsq.MXFP8, 128, 0, 1024) == bsq.ERR_ARG
+    sc = bsq.bsq_gemm_splitk_scratch
+    assert sc(bsq.MXFP8, p, p, p, p, None, p, 128, 256, 96, 2) == bsq.ERR_SHAPE              # K % 128
+    assert sc(bsq.MXFP8, p, p, p, p, None, p, 128, 256, 1024, 9) == bsq.ERR_ARG              # splits
     assert bsq.bsq_strerror(bsq.ERR_TIMEOUT).startswith("a kernel")
     assert bsq.bsq_strerror(12345) == "unknown status"
