@@ -103,9 +103,14 @@ __device__ __forceinline__ uint4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_
   return make_uint4(c0, c1, c2, c3);
 }
 
-// The four random words of elements 4g .. 4g+3 of a layout (0 = row, 1 = column).
-__device__ __forceinline__ uint4 sr_words(uint64_t g, uint32_t layout, const DualArgs& a) {
-  return philox4x32_10(static_cast<uint32_t>(g), static_cast<uint32_t>(g >> 32), layout, 0u, a.keys);
+// The random bits of elements 8g .. 8g+7 of a layout (0 = row, 1 = column): element 8g + j takes
+// the 16-bit half j mod 2 (low first) of Philox word j / 2 at counter g, returned in the top half
+// of its 32-bit r (lower bits zero, so sr_code's u = (r >> 8) 2^-24 is that half times 2^-16);
+// lo holds elements 8g .. 8g+3, hi elements 8g+4 .. 8g+7.
+__device__ __forceinline__ void sr_words8(uint64_t g, uint32_t layout, const DualArgs& a, uint4& lo, uint4& hi) {
+  const uint4 w = philox4x32_10(static_cast<uint32_t>(g), static_cast<uint32_t>(g >> 32), layout, 0u, a.keys);
+  lo = make_uint4(w.x << 16, w.x & 0xFFFF0000u, w.y << 16, w.y & 0xFFFF0000u);
+  hi = make_uint4(w.z << 16, w.z & 0xFFFF0000u, w.w << 16, w.w & 0xFFFF0000u);
 }
 
 // Block scale byte of the MX rule: floor(log2(amax)) - emax, clamped at -127, plus 127.
@@ -120,10 +125,10 @@ __device__ __forceinline__ uint32_t mx_scale_byte(float amax) {
 __device__ __forceinline__ float mx_inv_scale(uint32_t sbyte) { return __uint_as_float((254u - sbyte) << 23); }
 
 // Stochastic rounding of y = x / scale (exact in fp32 unless it fell below fp32's range) to an
-// E4M3 (MXFP8) or e2m1 code with the random word r: q = |y| / spacing at y's binade (the
-// subnormal spacing below the smallest normal), magnitude floor(q) + (frac(q) > u) with
-// u = (r >> 8) 2^-24, saturating at the largest finite value. Integer arithmetic on the fp32
-// bits, exact.
+// E4M3 (MXFP8) or e2m1 code with the random bits r (the element's 16 bits in the top half, the
+// low half zero): q = |y| / spacing at y's binade (the subnormal spacing below the smallest
+// normal), magnitude floor(q) + (frac(q) > u) with u = (r >> 8) 2^-24 = (r >> 16) 2^-16,
+// saturating at the largest finite value. Exact.
 template <int FMT>
 __device__ __forceinline__ uint32_t sr_code(float y, float x, uint32_t r) {
   constexpr uint32_t kM = (FMT == BSQ_MXFP8) ? 3u : 1u;         // mantissa bits
@@ -139,21 +144,16 @@ __device__ __forceinline__ uint32_t sr_code(float y, float x, uint32_t r) {
   // binade, which is the next grid point. (~r) >> (32 - D) = 2^D - 1 - (r >> (32 - D)), and the
   // exponent re-bias folds into the same add.
   auto normal_mag = [&]() { return (b + ((1u << D) - 1u - ((kEminB - 1u) << 23)) - (r >> (32u - D))) >> D; };
-  // subnormal target: q = sig / 2^sh, sig the 24-bit significand of |y|. sh <= 24: the same carry
-  // trick on the significand. sh > 24: q < 2^(24 - sh) <= 1/2 and up iff (r >> 8) <
-  // ceil(sig / 2^(sh - 24)), the shift capped at 24 (past it the ceiling is 1 for any positive
-  // sig). A y that underflowed to 0 from x != 0 is a positive value below every grid step and
-  // counts as sig = 1.
+  // subnormal target: q = |y| / 2^-S (S = 9 for E4M3, 1 for e2m1) < 2^kM, and frac(q) > u iff
+  // ceil(frac(q) 2^16) > h (u = h 2^-16, h = r >> 16), so floor(q) + (frac(q) > u) =
+  // (ceil(q 2^16) + 2^16 - 1 - h) >> 16. ceil(|y| 2^(S + 16)) is a round-up add of 2^23 to the
+  // exact product (below 2^(kM + 16), fp32 denormals included), read off the sum's bits. A y
+  // that underflowed to 0 from x != 0 is a positive value below every step: ceiling 1.
   auto subnormal_mag = [&]() {
-    const uint32_t e = b >> 23;
-    uint32_t sig = e ? ((b & 0x7FFFFFu) | 0x800000u) : b;
-    if (b == 0u && x != 0.0f) sig = 1u;
-    const uint32_t sh = D + kEminB - max(e, 1u);  // > D
-    const uint32_t sa = min(sh, 24u);
-    const uint32_t mag_a = (sig + ((~r) >> (32u - sa))) >> sa;
-    const uint32_t k = min(max(sh, 24u) - 24u, 24u);
-    const uint32_t mag_b = (r >> 8) < ((sig + (1u << k) - 1u) >> k) ? 1u : 0u;
-    return sh <= 24u ? mag_a : mag_b;
+    constexpr float kScale = (FMT == BSQ_MXFP8) ? 33554432.0f : 131072.0f;  // 2^25, 2^17
+    uint32_t c = __float_as_uint(__fadd_ru(__fmul_rn(__uint_as_float(b), kScale), 8388608.0f)) - 0x4B000000u;
+    if (b == 0u && x != 0.0f) c = 1u;
+    return (c + 0xFFFFu - (r >> 16)) >> 16;
   };
   if constexpr (FMT == BSQ_MXFP8) {
     // E4M3: values in the subnormal range are rare (a block's maximum sits 2^14 above it), so the
@@ -415,7 +415,7 @@ __global__ void __launch_bounds__(kDThreads, kDCtasPerSm)
         constexpr int kBlockWords = kWords / kBlocks;  // code words of one block
         uint32_t w[kWords];
         uint32_t sbytes = 0;
-        const uint64_t g0 = (static_cast<uint64_t>(r) * static_cast<uint64_t>(C) + static_cast<uint64_t>(c)) >> 2;
+        const uint64_t g0 = (static_cast<uint64_t>(r) * static_cast<uint64_t>(C) + static_cast<uint64_t>(c)) >> 3;
 #pragma unroll
         for (int h = 0; h < kBlocks; ++h) {
           const float* xb = x + h * BS;
@@ -432,11 +432,17 @@ __global__ void __launch_bounds__(kDThreads, kDCtasPerSm)
             wb[1] = sign_codes<8>(xb + 8);
           } else if constexpr (SR) {
 #pragma unroll
-            for (int gq = 0; gq < BS / 4; ++gq) {
-              const uint32_t v4 = sr_codes4<FMT>(xb + 4 * gq, bf, sr_words(g0 + h * (BS / 4) + gq, 0u, a));
-              if constexpr (kFp8) wb[gq] = v4;
-              else if (gq & 1) wb[gq >> 1] |= v4 << 16;
-              else wb[gq >> 1] = v4;
+            for (int go = 0; go < BS / 8; ++go) {
+              uint4 rlo, rhi;
+              sr_words8(g0 + h * (BS / 8) + go, 0u, a, rlo, rhi);
+              const uint32_t v0 = sr_codes4<FMT>(xb + 8 * go, bf, rlo);
+              const uint32_t v1 = sr_codes4<FMT>(xb + 8 * go + 4, bf, rhi);
+              if constexpr (kFp8) {
+                wb[2 * go] = v0;
+                wb[2 * go + 1] = v1;
+              } else {
+                wb[go] = v0 | (v1 << 16);
+              }
             }
           } else {
 #pragma unroll
@@ -496,7 +502,7 @@ __global__ void __launch_bounds__(kDThreads, kDCtasPerSm)
           }
         }
         uint32_t w[kFp8 ? 8 : 4];
-        const uint64_t g0 = (static_cast<uint64_t>(c) * static_cast<uint64_t>(R) + static_cast<uint64_t>(r0 + rb)) >> 2;
+        const uint64_t g0 = (static_cast<uint64_t>(c) * static_cast<uint64_t>(R) + static_cast<uint64_t>(r0 + rb)) >> 3;
 #pragma unroll
         for (int h = 0; h < kUnitScales; ++h) {  // the unit's blocks: 1 (MX) or 2 (NVFP4) of BS rows
           const float* xb = x + h * BS;
@@ -518,11 +524,17 @@ __global__ void __launch_bounds__(kDThreads, kDCtasPerSm)
             wb[1] = sign_codes<8>(xb + 8);
           } else if constexpr (SR) {
 #pragma unroll
-            for (int gq = 0; gq < BS / 4; ++gq) {
-              const uint32_t v4 = sr_codes4<FMT>(xb + 4 * gq, bf, sr_words(g0 + h * (BS / 4) + gq, 1u, a));
-              if constexpr (kFp8) wb[gq] = v4;
-              else if (gq & 1) wb[gq >> 1] |= v4 << 16;
-              else wb[gq >> 1] = v4;
+            for (int go = 0; go < BS / 8; ++go) {
+              uint4 rlo, rhi;
+              sr_words8(g0 + h * (BS / 8) + go, 1u, a, rlo, rhi);
+              const uint32_t v0 = sr_codes4<FMT>(xb + 8 * go, bf, rlo);
+              const uint32_t v1 = sr_codes4<FMT>(xb + 8 * go + 4, bf, rhi);
+              if constexpr (kFp8) {
+                wb[2 * go] = v0;
+                wb[2 * go + 1] = v1;
+              } else {
+                wb[go] = v0 | (v1 << 16);
+              }
             }
           } else {
 #pragma unroll

@@ -166,11 +166,13 @@ int bsq_quantize_batch(int fmt_flags, int count, const bsq_quant_item* items, bs
  * training), for v = the element's quotient (MX: x / scale, exact; NVFP4: fp32(x / fp32(s g))):
  * q = |v| / spacing, the spacing of the element format at |v|'s binade (its subnormal step
  * below the smallest normal); |code| = floor(q) + (frac(q) > u), saturating at the largest
- * finite value (448, 6); u = (r >> 8) * 2^-24 with r word (i mod 4) of Philox4x32-10 (Salmon
- * et al., "Parallel Random Numbers: As Easy as 1, 2, 3", SC'11) at counter {floor(i/4) low 32
- * bits, high 32 bits, layout, 0} and key {seed low 32 bits, high 32 bits}; i = r * cols + c in
- * the row layout (layout 0), c * rows + r in the column layout (layout 1). E[code value] = v
- * below saturation, and the codes are a function of (X, seed) alone. An NVFP4 block whose
+ * finite value (448, 6); u = h * 2^-16 with h the 16-bit half i mod 2 (low half first) of word
+ * (i mod 8) / 2 of Philox4x32-10 (Salmon et al., "Parallel Random Numbers: As Easy as 1, 2, 3",
+ * SC'11) at counter {floor(i/8) low 32 bits, high 32 bits, layout, 0} and key {seed low 32 bits,
+ * high 32 bits}; i = r * cols + c in the row layout (layout 0), c * rows + r in the column
+ * layout (layout 1). E[code value] = v below saturation wherever frac(q) has at most 16 bits
+ * (every bf16 X whose quotient lies in the format's normal range), otherwise within 2^-16 of a
+ * spacing; the codes are a function of (X, seed) alone. An NVFP4 block whose
  * scale is 0 gives signed zero codes either way.
  * Shapes: rows % 32 == 0 and cols % 32 == 0, both below 2^31, else BSQ_ERR_SHAPE.
  * Errors: BSQ_ERR_ARG for an unknown format or flag, BSQ_FLAG_GLOBAL_GIVEN without NVFP4 or

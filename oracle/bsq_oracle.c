@@ -54,11 +54,14 @@
  *       stored transposed (C x R, quantized along R), each with the MX rule R2.
  *       Stochastic rounding (for gradients) replaces RNE in R1: with q = |v| / spacing (the
  *       element format's spacing at v's binade, subnormal spacing below the smallest normal),
- *       the magnitude rounds up iff frac(q) > u, u = (r >> 8) * 2^-24; |v| >= max still
- *       saturates. r is word (i mod 4) of Philox4x32-10 (Salmon et al., "Parallel Random
- *       Numbers: As Easy as 1, 2, 3", SC'11) at counter (floor(i/4) low 32 bits, high 32 bits,
- *       layout, 0) and key (seed low, seed high), i the element's index in its layout's order
- *       (row layout r * C + c, column layout c * R + r), layout 0 = row, 1 = column.
+ *       the magnitude rounds up iff frac(q) > u, u = h * 2^-16; |v| >= max still saturates.
+ *       h is the 16-bit half (i mod 2: 0 = low, 1 = high) of word ((i mod 8) / 2) of
+ *       Philox4x32-10 (Salmon et al., "Parallel Random Numbers: As Easy as 1, 2, 3", SC'11) at
+ *       counter (floor(i/8) low 32 bits, high 32 bits, layout, 0) and key (seed low, seed high),
+ *       i the element's index in its layout's order (row layout r * C + c, column layout
+ *       c * R + r), layout 0 = row, 1 = column. 16 bits exceed the fraction any bf16 value
+ *       keeps below an E4M3 or e2m1 code of the normal range, so E[code] = v there exactly;
+ *       for longer fractions (fp32 sources, NVFP4 quotients) the bias is below 2^-16 spacing.
  *   R11 Dual-layout NVFP4 (the pages' fused FP4 quantizer writes NVFP4 codes for both
  *       layouts; [LT] section 4.3 training stack P3, dY with stochastic rounding): one per-tensor
  *       g for the whole matrix (R3: fp32(amax / 2688), or a given g), shared by both layouts;
@@ -554,14 +557,16 @@ void orc_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t ou
     out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
 }
 
-/* The 32-bit random word of element i of a layout (reading R10). */
-static uint32_t sr_word(uint64_t seed, int layout, uint64_t i) {
-    uint32_t ctr[4], key[2], out[4];
-    uint64_t g = i >> 2;
+/* The uniform u = h * 2^-16 of element i of a layout (reading R10): h the 16-bit half
+ * (i mod 2) of word ((i mod 8) / 2) of Philox4x32-10 at counter floor(i / 8). */
+static double sr_u(uint64_t seed, int layout, uint64_t i) {
+    uint32_t ctr[4], key[2], out[4], h;
+    uint64_t g = i >> 3;
     ctr[0] = (uint32_t)g; ctr[1] = (uint32_t)(g >> 32); ctr[2] = (uint32_t)layout; ctr[3] = 0;
     key[0] = (uint32_t)seed; key[1] = (uint32_t)(seed >> 32);
     orc_philox4x32_10(ctr, key, out);
-    return out[i & 3];
+    h = (i & 1) ? out[(i & 7) >> 1] >> 16 : out[(i & 7) >> 1] & 0xFFFFu;
+    return ldexp((double)h, -16);
 }
 
 /* Stochastic rounding of v to E4M3 (elem 0) or e2m1 (elem 1) with the uniform u in [0, 1):
@@ -621,7 +626,7 @@ static uint8_t mx_block(int fmt, const double* x, int64_t step, int sr, uint64_t
     for (k = 0; k < 32; ++k) {
         double v = ldexp(x[k * step], -e);
         if (sr) {
-            double u = ldexp((double)(sr_word(seed, layout, base_index + (uint64_t)k) >> 8), -24);
+            double u = sr_u(seed, layout, base_index + (uint64_t)k);
             codes[k] = encode_sr(v, elem, u);
         } else {
             codes[k] = elem == 0 ? orc_encode_e4m3(v) : orc_encode_e2m1(v);
@@ -699,7 +704,7 @@ static uint8_t nv_block(const float* x, int64_t step, float g, float six_g, int 
         } else {
             float y = xv / sg;                       /* fp32 division */
             if (sr) {
-                double u = ldexp((double)(sr_word(seed, layout, base_index + (uint64_t)k) >> 8), -24);
+                double u = sr_u(seed, layout, base_index + (uint64_t)k);
                 codes[k] = encode_sr((double)y, 1, u);
             } else {
                 codes[k] = orc_encode_e2m1((double)y);

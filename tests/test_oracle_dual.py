@@ -66,6 +66,34 @@ def test_sr_is_exactly_unbiased_on_dyadic_values():
         assert mean == x
 
 
+@pytest.mark.parametrize("elem", ["e4m3", "e2m1"])
+def test_sr_mean_over_all_16_bit_u_is_exact_or_within_bound(elem):
+    """Reading R10 draws u on the grid h 2^-16: the mean code over all 2^16 values of h equals v
+    exactly when frac(|v| / spacing) has at most 16 bits (normal and subnormal targets), and
+    exceeds |v| by less than 2^-16 spacing when the fraction is longer (P(up) =
+    ceil(frac 2^16) / 2^16)."""
+    rng = np.random.default_rng(19)
+    dec = oracle.decode_e4m3 if elem == "e4m3" else oracle.decode_e2m1
+    # (start, end, spacing) of the subnormal range and of normal binades
+    ranges = ([(0.0, 2.0 ** -6, 2.0 ** -9), (2.0 ** -6, 2.0 ** -5, 2.0 ** -9), (1.0, 2.0, 2.0 ** -3),
+               (256.0, 448.0, 32.0)] if elem == "e4m3" else
+              [(0.0, 1.0, 0.5), (1.0, 2.0, 0.5), (2.0, 4.0, 1.0), (4.0, 6.0, 2.0)])
+    u = np.arange(2 ** 16) / 2.0 ** 16
+    for start, end, spacing in ranges:
+        steps = int(round((end - start) / spacing))
+        for _ in range(6):
+            q16 = int(rng.integers(0, steps * 2 ** 16))            # 16 fractional bits: exact
+            v = start + q16 * spacing * 2.0 ** -16
+            sgn = -1.0 if rng.integers(2) else 1.0
+            codes = oracle.encode_sr_array(elem, np.full(u.shape, sgn * v), u)
+            assert np.mean([dec(int(c)) for c in codes]) == sgn * v, (elem, v)
+            q20 = int(rng.integers(0, steps * 2 ** 20)) | 1        # 20 fractional bits
+            w = start + q20 * spacing * 2.0 ** -20
+            codes = oracle.encode_sr_array(elem, np.full(u.shape, w), u)
+            m = np.mean([dec(int(c)) for c in codes])
+            assert 0.0 < m - w < spacing * 2.0 ** -16, (elem, w, m)
+
+
 @pytest.mark.parametrize("fmt", ["mxfp8", "mxfp4"])
 def test_dual_rne_equals_pinned_quantizer(fmt):
     rng = np.random.default_rng(13)
@@ -124,8 +152,9 @@ def _nibble(codes, i):
 @pytest.mark.parametrize("fmt", ["mxfp8", "mxfp4", "nvfp4"])
 def test_dual_sr_takes_each_elements_own_word(fmt):
     """Stochastic codes equal the pinned encoder applied to the element's scaled value v with
-    u from the Philox word the reading assigns to the element (counter floor(i/4) and layout,
-    key = seed, word i mod 4; i = r C + c in the row layout, c R + r in the column layout),
+    u from the 16 Philox bits the reading assigns to the element (counter floor(i/8) and
+    layout, key = seed, half i mod 2 of word (i mod 8) / 2; i = r C + c in the row layout,
+    c R + r in the column layout),
     and v taken from the round-to-nearest dual quantizer's scales (which rounding leaves
     alone)."""
     rng = np.random.default_rng(17)
@@ -150,9 +179,9 @@ def test_dual_sr_takes_each_elements_own_word(fmt):
             else:
                 v = float(src) * 2.0 ** (127 - sb)
             i = r * cols + c
-            words = oracle.philox4x32_10([(i // 4) & 0xFFFFFFFF, (i // 4) >> 32, layout, 0],
+            words = oracle.philox4x32_10([(i // 8) & 0xFFFFFFFF, (i // 8) >> 32, layout, 0],
                                          [seed & 0xFFFFFFFF, seed >> 32])
-            u = (words[i % 4] >> 8) * 2.0 ** -24
+            u = ((words[(i % 8) // 2] >> (16 * (i % 2))) & 0xFFFF) * 2.0 ** -16
             want = int(oracle.encode_sr_array(elem, np.array([v]), np.array([u]))[0])
             got = int(q_sr.codes[i]) if fmt == "mxfp8" else _nibble(q_sr.codes, i)
             assert got == want, (fmt, layout, r, c, v, u, got, want)
