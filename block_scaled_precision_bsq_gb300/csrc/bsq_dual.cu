@@ -2,9 +2,10 @@
 // matrix gives both its row-wise operand (quantized along C, R x C) and its column-wise one
 // (quantized along R, stored transposed as C x R), each with codes and tiled scales, in one pass
 // over the source. With stochastic rounding the element rounding is the gradient form: the
-// magnitude steps up from the grid point below iff frac(|v| / spacing) > u, u a uniform draw
-// from Philox4x32-10 (Salmon, Moraes, Dror and Shaw, "Parallel Random Numbers: As Easy as 1,
-// 2, 3", SC'11) keyed by the seed and counting over the element's index in its layout.
+// magnitude steps up from the grid point below iff frac(|v| / spacing) > u, u = h 2^-16 with h
+// 16 bits of Philox4x32-10 (Salmon, Moraes, Dror and Shaw, "Parallel Random Numbers: As Easy as
+// 1, 2, 3", SC'11) keyed by the seed, one call per 8 elements counting over the element's index
+// in its layout.
 //
 // Why dual: dgrad (dX = dY W) contracts over N and wgrad (dW = dY^T X) over M, so the backward
 // pass needs dY quantized along both of its dimensions, W along N and X along M ("lightly-train
@@ -36,9 +37,9 @@
 // the loop together.
 //
 // Stochastic rounding runs on the fp32 bits of v (exact): for a normal target binade it adds
-// the complement of the top D bits of the random word below the kept mantissa and truncates,
-// D = 23 - mantissa bits, which rounds up exactly when frac(q) > u; only targets in the
-// element format's subnormal range take a 64-bit compare.
+// the complement of the random bits, aligned below the kept mantissa, and truncates, which
+// rounds up exactly when frac(q) > u; a target in the element format's subnormal range takes
+// the fixed-point form (ceil(q 2^16) + 2^16 - 1 - h) >> 16.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -198,8 +199,9 @@ __device__ __forceinline__ void rne_codes(const float* x, float f, uint32_t* w) 
   }
 }
 
-// Stochastic codes of the four elements x[0..4) with the block factor f and the random words q
-// (element i takes word i), packed as rne_codes packs four: E4M3 one word, e2m1 the low 16 bits.
+// Stochastic codes of the four elements x[0..4) with the block factor f and the random bits q
+// (element i takes q's component i: its 16 bits in the top half), packed as rne_codes packs
+// four: E4M3 one word, e2m1 the low 16 bits.
 // MX passes x for sr_code's underflow test (the MX value x / scale is exact unless it leaves
 // fp32's range); NVFP4 rounds the fp32 quotient itself, so the quotient stands in for x.
 // E4M3 tests the range once per four elements: when all four scaled values lie in the normal
