@@ -104,14 +104,13 @@ __device__ __forceinline__ uint4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_
   return make_uint4(c0, c1, c2, c3);
 }
 
-// The random bits of elements 8g .. 8g+7 of a layout (0 = row, 1 = column): element 8g + j takes
-// the 16-bit half j mod 2 (low first) of Philox word j / 2 at counter g, returned in the top half
-// of its 32-bit r (lower bits zero, so sr_code's u = (r >> 8) 2^-24 is that half times 2^-16);
+// The random bits h (u = h 2^-16) of elements 8g .. 8g+7 of a layout (0 = row, 1 = column):
+// element 8g + j takes the 16-bit half j mod 2 (low first) of Philox word j / 2 at counter g;
 // lo holds elements 8g .. 8g+3, hi elements 8g+4 .. 8g+7.
 __device__ __forceinline__ void sr_words8(uint64_t g, uint32_t layout, const DualArgs& a, uint4& lo, uint4& hi) {
   const uint4 w = philox4x32_10(static_cast<uint32_t>(g), static_cast<uint32_t>(g >> 32), layout, 0u, a.keys);
-  lo = make_uint4(w.x << 16, w.x & 0xFFFF0000u, w.y << 16, w.y & 0xFFFF0000u);
-  hi = make_uint4(w.z << 16, w.z & 0xFFFF0000u, w.w << 16, w.w & 0xFFFF0000u);
+  lo = make_uint4(w.x & 0xFFFFu, w.x >> 16, w.y & 0xFFFFu, w.y >> 16);
+  hi = make_uint4(w.z & 0xFFFFu, w.z >> 16, w.w & 0xFFFFu, w.w >> 16);
 }
 
 // Block scale byte of the MX rule: floor(log2(amax)) - emax, clamped at -127, plus 127.
@@ -126,12 +125,11 @@ __device__ __forceinline__ uint32_t mx_scale_byte(float amax) {
 __device__ __forceinline__ float mx_inv_scale(uint32_t sbyte) { return __uint_as_float((254u - sbyte) << 23); }
 
 // Stochastic rounding of y = x / scale (exact in fp32 unless it fell below fp32's range) to an
-// E4M3 (MXFP8) or e2m1 code with the random bits r (the element's 16 bits in the top half, the
-// low half zero): q = |y| / spacing at y's binade (the subnormal spacing below the smallest
-// normal), magnitude floor(q) + (frac(q) > u) with u = (r >> 8) 2^-24 = (r >> 16) 2^-16,
-// saturating at the largest finite value. Exact.
+// E4M3 (MXFP8) or e2m1 code with the element's 16 random bits h: q = |y| / spacing at y's
+// binade (the subnormal spacing below the smallest normal), magnitude floor(q) + (frac(q) > u)
+// with u = h 2^-16, saturating at the largest finite value. Exact.
 template <int FMT>
-__device__ __forceinline__ uint32_t sr_code(float y, float x, uint32_t r) {
+__device__ __forceinline__ uint32_t sr_code(float y, float x, uint32_t h) {
   constexpr uint32_t kM = (FMT == BSQ_MXFP8) ? 3u : 1u;         // mantissa bits
   constexpr uint32_t D = 23u - kM;                              // fp32 mantissa bits below the kept ones
   constexpr uint32_t kEminB = (FMT == BSQ_MXFP8) ? 121u : 127u;  // biased exponent of the lowest normal binade
@@ -140,13 +138,13 @@ __device__ __forceinline__ uint32_t sr_code(float y, float x, uint32_t r) {
   const uint32_t yb = __float_as_uint(y);
   const uint32_t b = yb & 0x7FFFFFFFu;
   uint32_t mag;
-  // normal target binade: q's fraction is the low D mantissa bits t: up iff t > r >> (32 - D), i.e.
-  // iff t + (2^D - 1 - (r >> (32 - D))) carries into the kept bits; the carry may move to the next
-  // binade, which is the next grid point. (~r) >> (32 - D) = 2^D - 1 - (r >> (32 - D)), and the
-  // exponent re-bias folds into the same add.
-  auto normal_mag = [&]() { return (b + ((1u << D) - 1u - ((kEminB - 1u) << 23)) - (r >> (32u - D))) >> D; };
+  // normal target binade: q's fraction is the low D mantissa bits t, and u in units of 2^-D is
+  // h 2^(D - 16): up iff t > h 2^(D - 16), i.e. iff t + (2^D - 1 - h 2^(D - 16)) carries into the
+  // kept bits; the carry may move to the next binade, which is the next grid point. The exponent
+  // re-bias folds into the same add.
+  auto normal_mag = [&]() { return (b + ((1u << D) - 1u - ((kEminB - 1u) << 23)) - (h << (D - 16u))) >> D; };
   // subnormal target: q = |y| / 2^-S (S = 9 for E4M3, 1 for e2m1) < 2^kM, and frac(q) > u iff
-  // ceil(frac(q) 2^16) > h (u = h 2^-16, h = r >> 16), so floor(q) + (frac(q) > u) =
+  // ceil(frac(q) 2^16) > h, so floor(q) + (frac(q) > u) =
   // (ceil(q 2^16) + 2^16 - 1 - h) >> 16. ceil(|y| 2^(S + 16)) is a round-up add of 2^23 to the
   // exact product (below 2^(kM + 16), fp32 denormals included), read off the sum's bits. A y
   // that underflowed to 0 from x != 0 is a positive value below every step: ceiling 1.
@@ -154,7 +152,7 @@ __device__ __forceinline__ uint32_t sr_code(float y, float x, uint32_t r) {
     constexpr float kScale = (FMT == BSQ_MXFP8) ? 33554432.0f : 131072.0f;  // 2^25, 2^17
     uint32_t c = __float_as_uint(__fadd_ru(__fmul_rn(__uint_as_float(b), kScale), 8388608.0f)) - 0x4B000000u;
     if (b == 0u && x != 0.0f) c = 1u;
-    return (c + 0xFFFFu - (r >> 16)) >> 16;
+    return (c + 0xFFFFu - h) >> 16;
   };
   if constexpr (FMT == BSQ_MXFP8) {
     // E4M3: values in the subnormal range are rare (a block's maximum sits 2^14 above it), so the
@@ -200,8 +198,8 @@ __device__ __forceinline__ void rne_codes(const float* x, float f, uint32_t* w) 
 }
 
 // Stochastic codes of the four elements x[0..4) with the block factor f and the random bits q
-// (element i takes q's component i: its 16 bits in the top half), packed as rne_codes packs
-// four: E4M3 one word, e2m1 the low 16 bits.
+// (element i takes q's component i, 16 bits), packed as rne_codes packs four: E4M3 one word,
+// e2m1 the low 16 bits.
 // MX passes x for sr_code's underflow test (the MX value x / scale is exact unless it leaves
 // fp32's range); NVFP4 rounds the fp32 quotient itself, so the quotient stands in for x.
 // E4M3 tests the range once per four elements: when all four scaled values lie in the normal
@@ -225,7 +223,7 @@ __device__ __forceinline__ uint32_t sr_codes4(const float* x, float f, uint4 q) 
       for (int i = 0; i < 4; ++i) {
         const uint32_t yb = __float_as_uint(y[i]);
         const uint32_t b = yb & 0x7FFFFFFFu;
-        const uint32_t mag = min((b + ((1u << 20) - 1u - (120u << 23)) - (qq[i] >> 12)) >> 20, 0x7Eu);
+        const uint32_t mag = min((b + ((1u << 20) - 1u - (120u << 23)) - (qq[i] << 4)) >> 20, 0x7Eu);
         w |= (((yb >> 31) << 7) | mag) << (8 * i);
       }
     } else {
