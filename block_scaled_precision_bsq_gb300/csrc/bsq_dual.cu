@@ -151,7 +151,10 @@ __device__ __forceinline__ uint32_t sr_code(float y, float x, uint32_t h) {
   auto subnormal_mag = [&]() {
     constexpr float kScale = (FMT == BSQ_MXFP8) ? 33554432.0f : 131072.0f;  // 2^25, 2^17
     uint32_t c = __float_as_uint(__fadd_ru(__fmul_rn(__uint_as_float(b), kScale), 8388608.0f)) - 0x4B000000u;
-    if (b == 0u && x != 0.0f) c = 1u;
+    // (NVFP4 passes the quotient itself as x, so there b == 0 implies x == 0)
+    if constexpr (FMT != BSQ_NVFP4) {
+      if (b == 0u && x != 0.0f) c = 1u;
+    }
     return (c + 0xFFFFu - h) >> 16;
   };
   if constexpr (FMT == BSQ_MXFP8) {
