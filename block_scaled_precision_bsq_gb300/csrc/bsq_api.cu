@@ -19,7 +19,6 @@ __device__ int g_status_word;
 
 namespace {
 
-constexpr int kMaxDevices = 64;
 DeviceInfo g_dev[kMaxDevices];
 std::once_flag g_dev_once[kMaxDevices];
 thread_local int t_last_error = 0;
@@ -47,6 +46,8 @@ __global__ void selftest_timeout_kernel(int64_t limit_ns, int* status) {
 }
 
 }  // namespace
+
+int record_error(int code) { return fail(code); }
 
 const DeviceInfo* current_device() {
   int dev = -1;

@@ -595,9 +595,11 @@ __global__ void __launch_bounds__(kDThreads, kDCtasPerSm)
 
 template <int FMT, bool F32, bool SR>
 cudaError_t launch_d(const CUtensorMap& src_map, const CUtensorMap& col_map, const DualArgs& a, int grid,
-                     cudaStream_t stream) {
-  static cudaError_t attr =
-      cudaFuncSetAttribute(dual_kernel<FMT, F32, SR>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDSmem);
+                     cudaStream_t stream, int device) {
+  static PerDevice<cudaError_t> setup;  // the shared-memory opt-in holds per device
+  const cudaError_t attr = setup.run(device, [] {
+    return cudaFuncSetAttribute(dual_kernel<FMT, F32, SR>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDSmem);
+  });
   if (attr != cudaSuccess) return attr;
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -614,13 +616,13 @@ cudaError_t launch_d(const CUtensorMap& src_map, const CUtensorMap& col_map, con
 
 template <int FMT>
 cudaError_t launch_d_fmt(bool f32, bool sr, const CUtensorMap& src_map, const CUtensorMap& col_map,
-                         const DualArgs& a, int grid, cudaStream_t stream) {
+                         const DualArgs& a, int grid, cudaStream_t stream, int device) {
   if (f32) {
-    return sr ? launch_d<FMT, true, true>(src_map, col_map, a, grid, stream)
-              : launch_d<FMT, true, false>(src_map, col_map, a, grid, stream);
+    return sr ? launch_d<FMT, true, true>(src_map, col_map, a, grid, stream, device)
+              : launch_d<FMT, true, false>(src_map, col_map, a, grid, stream, device);
   }
-  return sr ? launch_d<FMT, false, true>(src_map, col_map, a, grid, stream)
-            : launch_d<FMT, false, false>(src_map, col_map, a, grid, stream);
+  return sr ? launch_d<FMT, false, true>(src_map, col_map, a, grid, stream, device)
+            : launch_d<FMT, false, false>(src_map, col_map, a, grid, stream, device);
 }
 
 }  // namespace
@@ -677,9 +679,9 @@ int launch_quantize_dual(int fmt, bool src_f32, bool stochastic, bool global_giv
     return BSQ_ERR_LAUNCH;
   const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(a.ntiles, kDCtasPerSm * dev.num_sms)));
   cudaError_t err;
-  if (fmt == BSQ_MXFP8) err = launch_d_fmt<BSQ_MXFP8>(src_f32, stochastic, map, col_map, a, grid, stream);
-  else if (fmt == BSQ_MXFP4) err = launch_d_fmt<BSQ_MXFP4>(src_f32, stochastic, map, col_map, a, grid, stream);
-  else err = launch_d_fmt<BSQ_NVFP4>(src_f32, stochastic, map, col_map, a, grid, stream);
+  if (fmt == BSQ_MXFP8) err = launch_d_fmt<BSQ_MXFP8>(src_f32, stochastic, map, col_map, a, grid, stream, dev.device);
+  else if (fmt == BSQ_MXFP4) err = launch_d_fmt<BSQ_MXFP4>(src_f32, stochastic, map, col_map, a, grid, stream, dev.device);
+  else err = launch_d_fmt<BSQ_NVFP4>(src_f32, stochastic, map, col_map, a, grid, stream, dev.device);
   return err == cudaSuccess ? BSQ_OK : BSQ_ERR_LAUNCH;
 }
 

@@ -677,19 +677,24 @@ template <int FMT, int EPI>
 int run_gemm(const void* A, const void* A_scales, const void* B, const void* B_scales, const void* bias, void* out,
              void* out_scales, int64_t M, int64_t N, int64_t K, int64_t cv_w, int splits, cudaStream_t stream,
              const DeviceInfo& dev) {
-  static std::once_flag attr_once;
-  static cudaError_t attr_err = cudaSuccess;
-  static int max_clusters = 0;
-  std::call_once(attr_once, [] {
-    attr_err = cudaFuncSetAttribute(gemm_kernel<FMT, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    Smem<FMT>::alloc);
-    if (attr_err != cudaSuccess) return;
+  // per device: the shared-memory opt-in and the number of co-resident clusters (0 = unusable)
+  static PerDevice<int> setup;
+  const int max_clusters = setup.run(dev.device, [] {
+    if (cudaFuncSetAttribute(gemm_kernel<FMT, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<FMT>::alloc) !=
+        cudaSuccess) {
+      cudaGetLastError();
+      return 0;
+    }
     cudaLaunchAttribute at[2];
     cudaLaunchConfig_t cfg = pair_launch_config(at, 1, kThreads, Smem<FMT>::alloc, nullptr);
-    attr_err = cudaOccupancyMaxActiveClusters(&max_clusters, gemm_kernel<FMT, EPI>, &cfg);
-    if (attr_err == cudaSuccess && max_clusters < 1) attr_err = cudaErrorInvalidConfiguration;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_kernel<FMT, EPI>, &cfg) != cudaSuccess) {
+      cudaGetLastError();
+      return 0;
+    }
+    return n;
   });
-  if (attr_err != cudaSuccess) return BSQ_ERR_LAUNCH;
+  if (max_clusters < 1) return BSQ_ERR_LAUNCH;
 
   const uint64_t kbytes = (FMT == BSQ_MXFP8) ? static_cast<uint64_t>(K) : static_cast<uint64_t>(K) / 2;
   CUtensorMap mA, mB, mSfa, mSfb, mOut;

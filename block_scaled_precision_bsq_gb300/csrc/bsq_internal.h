@@ -4,6 +4,7 @@
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <mutex>
 
 #include "bsq.h"
 
@@ -29,6 +30,24 @@ struct DeviceInfo {
 // Current device's cached properties (and the status word's address); nullptr when no
 // usable device. Thread-safe.
 const DeviceInfo* current_device();
+
+// Kernel attributes (the dynamic shared-memory opt-in) and occupancy queries hold per device, so
+// each kernel instance does its setup once per device: PerDevice<T> keeps one flag and one
+// result per device index, and run(device, f) calls f() the first time that device asks.
+constexpr int kMaxDevices = 64;
+template <typename T>
+struct PerDevice {
+  std::once_flag once[kMaxDevices];
+  T value[kMaxDevices] = {};
+  template <typename F>
+  const T& run(int device, F&& f) {
+    std::call_once(once[device], [&] { value[device] = f(); });
+    return value[device];
+  }
+};
+
+// Record `code` as the calling thread's last error (bsq_last_error) and return it.
+int record_error(int code);
 
 // cuTensorMapEncodeTiled, obtained once through the runtime's driver entry-point query
 // (nullptr if unavailable).

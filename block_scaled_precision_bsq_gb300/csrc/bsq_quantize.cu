@@ -553,10 +553,13 @@ __global__ void __launch_bounds__(kAmaxThreads) amax_kernel(const uint4* src, in
 }
 
 template <int FMT, bool F32, int NV, bool LN = false>
-cudaError_t launch_q(const QuantBatch& b, int grid, cudaStream_t stream) {
+cudaError_t launch_q(const QuantBatch& b, int grid, cudaStream_t stream, int device) {
   using Q = QCfg<NV != kMx>;
-  static cudaError_t attr = cudaFuncSetAttribute(quantize_kernel<FMT, F32, NV, LN>,
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, Q::kSmem);
+  static PerDevice<cudaError_t> setup;  // the shared-memory opt-in holds per device
+  const cudaError_t attr = setup.run(device, [] {
+    return cudaFuncSetAttribute(quantize_kernel<FMT, F32, NV, LN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                Q::kSmem);
+  });
   if (attr != cudaSuccess) return attr;
   // programmatic dependent launch: the kernel may be launched while the previous kernel in
   // the stream finishes; it waits for it (grid_dependency_wait) before touching memory
@@ -672,16 +675,16 @@ int launch_quantize_batch(int fmt, bool src_f32, bool global_given, int count, c
         return BSQ_ERR_LAUNCH;
     }
     if (!global_given) {
-      err = src_f32 ? launch_q<BSQ_NVFP4, true, kNvComputed>(b, grid, stream)
-                    : launch_q<BSQ_NVFP4, false, kNvComputed>(b, grid, stream);
+      err = src_f32 ? launch_q<BSQ_NVFP4, true, kNvComputed>(b, grid, stream, dev.device)
+                    : launch_q<BSQ_NVFP4, false, kNvComputed>(b, grid, stream, dev.device);
     } else {
-      err = src_f32 ? launch_q<BSQ_NVFP4, true, kNvGiven>(b, grid, stream)
-                    : launch_q<BSQ_NVFP4, false, kNvGiven>(b, grid, stream);
+      err = src_f32 ? launch_q<BSQ_NVFP4, true, kNvGiven>(b, grid, stream, dev.device)
+                    : launch_q<BSQ_NVFP4, false, kNvGiven>(b, grid, stream, dev.device);
     }
   } else if (fmt == BSQ_MXFP8) {
-    err = src_f32 ? launch_q<BSQ_MXFP8, true, kMx>(b, grid, stream) : launch_q<BSQ_MXFP8, false, kMx>(b, grid, stream);
+    err = src_f32 ? launch_q<BSQ_MXFP8, true, kMx>(b, grid, stream, dev.device) : launch_q<BSQ_MXFP8, false, kMx>(b, grid, stream, dev.device);
   } else {
-    err = src_f32 ? launch_q<BSQ_MXFP4, true, kMx>(b, grid, stream) : launch_q<BSQ_MXFP4, false, kMx>(b, grid, stream);
+    err = src_f32 ? launch_q<BSQ_MXFP4, true, kMx>(b, grid, stream, dev.device) : launch_q<BSQ_MXFP4, false, kMx>(b, grid, stream, dev.device);
   }
   return err == cudaSuccess ? BSQ_OK : BSQ_ERR_LAUNCH;
 }
@@ -698,9 +701,9 @@ int launch_layernorm_quantize(int fmt, bool src_f32, const QuantItem& item, cons
       static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(b.chunk_start[1], ctas_per_sm(fmt) * dev.num_sms)));
   cudaError_t err;
   if (fmt == BSQ_MXFP8) {
-    err = src_f32 ? launch_q<BSQ_MXFP8, true, kMx, true>(b, grid, stream) : launch_q<BSQ_MXFP8, false, kMx, true>(b, grid, stream);
+    err = src_f32 ? launch_q<BSQ_MXFP8, true, kMx, true>(b, grid, stream, dev.device) : launch_q<BSQ_MXFP8, false, kMx, true>(b, grid, stream, dev.device);
   } else {
-    err = src_f32 ? launch_q<BSQ_MXFP4, true, kMx, true>(b, grid, stream) : launch_q<BSQ_MXFP4, false, kMx, true>(b, grid, stream);
+    err = src_f32 ? launch_q<BSQ_MXFP4, true, kMx, true>(b, grid, stream, dev.device) : launch_q<BSQ_MXFP4, false, kMx, true>(b, grid, stream, dev.device);
   }
   return err == cudaSuccess ? BSQ_OK : BSQ_ERR_LAUNCH;
 }

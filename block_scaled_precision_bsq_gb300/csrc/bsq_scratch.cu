@@ -22,7 +22,7 @@ namespace {
 constexpr size_t kScratchBytes = size_t{64} << 20;  // 64 MiB: splits * M * N * 4 bytes at most
 static __device__ __align__(256) unsigned char g_splitk_scratch[kScratchBytes];
 
-constexpr int kMaxDevices = 64;
+using bsq::kMaxDevices;
 std::once_flag g_scratch_once[kMaxDevices];
 void* g_scratch_addr[kMaxDevices];
 
@@ -33,7 +33,12 @@ void* scratch_address() {
   const int d = dev->device;
   std::call_once(g_scratch_once[d], [d] {
     void* p = nullptr;
-    g_scratch_addr[d] = cudaGetSymbolAddress(&p, g_splitk_scratch) == cudaSuccess ? p : nullptr;
+    if (cudaGetSymbolAddress(&p, g_splitk_scratch) == cudaSuccess) {
+      g_scratch_addr[d] = p;
+    } else {
+      g_scratch_addr[d] = nullptr;
+      cudaGetLastError();  // the failed lookup leaves no error pending for a later launch check
+    }
   });
   return g_scratch_addr[d];
 }
@@ -44,6 +49,9 @@ int bsq_gemm_splitk_scratch(int fmt, const void* A, const void* A_scales, const 
                             const void* bias_bf16, void* out_bf16, int64_t M, int64_t N, int64_t K, int splits,
                             bsq_stream_t stream) {
   void* ws = scratch_address();
+  // a usable device whose array could not be found: say so rather than report a workspace too
+  // small (without a usable device bsq_gemm_splitk itself returns the argument or device error)
+  if (ws == nullptr && splits > 1 && bsq::current_device() != nullptr) return bsq::record_error(BSQ_ERR_LAUNCH);
   return bsq_gemm_splitk(fmt, A, A_scales, B, B_scales, bias_bf16, out_bf16, M, N, K, splits, ws,
                          ws != nullptr ? kScratchBytes : 0, stream);
 }

@@ -62,11 +62,16 @@ typedef enum { BSQ_MXFP8 = 1, BSQ_NVFP4 = 2, BSQ_MXFP4 = 3 } bsq_format;
  *   MXFP8: rows * cols bytes (one E4M3 code per byte).
  *   NVFP4, MXFP4: rows * cols / 2 bytes; element 2j in the low nibble of byte j, 2j+1 in
  *   the high nibble. Returns 0 for invalid arguments.
+ * Source: the element widths of the README's section 2 number-format table (8-bit E4M3,
+ * 4-bit e2m1). The nibble order is a convention: the pages are silent on it.
  */
 size_t bsq_codes_bytes(int fmt, int64_t rows, int64_t cols);
 
 /*
  * bsq_scales_bytes: size of the scale buffer of a rows x cols matrix.
+ * Source: the block sizes and scale types of the README's section 2 number-format table
+ * (one 8-bit scale per 1x32 block for MX, per 1x16 block for NVFP4). The tiled layout below
+ * is a convention; the pages are silent on how scales are laid out in memory.
  * Block scales are stored in tiles of 128 rows x 4 scale columns (512 bytes): the scale of
  * row r and block column c lives in tile (r / 128) * ceil(nsc / 4) + c / 4 at byte
  * (r % 32) * 16 + ((r / 32) % 4) * 4 + c % 4, nsc = cols / block size. Rows are padded to
@@ -205,6 +210,10 @@ int bsq_delayed_global_scale(const void* prev_scales, int64_t rows, int64_t cols
 
 /*
  * bsq_gemm: out[m, n] = bf16_rn(alpha * sum_k Ahat[m,k] * Bhat[n,k] + bias[n]).
+ * Source: "lightly-train - DINOv3 + EoMT on RTX 5090" README, section 2 (the block-scaled
+ * MXFP8 / NVFP4 / MXFP4 GEMM formats and their tensor-core rates) and section 4.3 (qkv, proj,
+ * fc1, fc2 of every block run as these GEMMs, bias fused into the epilogue). Ahat, Bhat are the
+ * decoded operands: code value times its block scale (times g for NVFP4, folded into alpha).
  *   A, A_scales  M x K operand as written by bsq_quantize(fmt, ..., M, K, ...).
  *   B, B_scales  N x K operand (the nn.Linear weight layout) from bsq_quantize(fmt, ..., N, K, ...).
  *   bias_bf16    N bf16 values, or NULL for no bias.

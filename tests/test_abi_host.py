@@ -137,3 +137,19 @@ def test_argument_errors_before_any_cuda_call(bsq):
     assert sc(bsq.MXFP8, p, p, p, p, None, p, 128, 256, 1024, 9) == bsq.ERR_ARG              # splits
     assert bsq.bsq_strerror(bsq.ERR_TIMEOUT).startswith("a kernel")
     assert bsq.bsq_strerror(12345) == "unknown status"
+
+
+def test_no_multicast_bulk_or_tensor_copy_in_the_sources():
+    """No bulk or tensor copy (load, store or reduce) in the library's sources uses cluster
+    multicast: every CTA loads its own tiles. The tcgen05.commit multicast (an mbarrier signal
+    to both CTAs of a pair, not a memory copy) is the only multicast form allowed."""
+    csrc = os.path.join(ROOT, "block_scaled_precision_bsq_gb300", "csrc")
+    offenders = []
+    for name in sorted(os.listdir(csrc)):
+        if not name.endswith((".cu", ".cuh", ".h")):
+            continue
+        text = open(os.path.join(csrc, name)).read()
+        for m in re.finditer(r'"[^"\n]*multicast::cluster[^"\n]*"', text):
+            if "cp.async.bulk" in m.group(0) or "tcgen05.commit" not in m.group(0):
+                offenders.append("%s: %s" % (name, m.group(0)))
+    assert not offenders, offenders

@@ -89,9 +89,11 @@ def test_nvfp4_all_zero_tensor():
     assert gq.global_scale.item() == 0.0
 
 
-@pytest.mark.parametrize("name", ["vitb_fc1_mxfp8", "vitl_mxfp8", "vitl_nvfp4", "vitl_mlp_large"])
+@pytest.mark.parametrize("name", ["tiny_mxfp8", "vitb_fc1_mxfp8", "vitl_mxfp8", "vitl_nvfp4", "vitl_mlp_large"])
 def test_full_size_workload_quantize(name):
-    """Every activation and weight tensor of the workload, at full size, bit-exact."""
+    """Every activation and weight tensor of the workload, at full size, bit-exact: codes,
+    tiled scales with their padding and (NVFP4) the tail. The tiny case quantizes its fp32
+    sources (A 128 x 256 with 1 % of the entries x50, B 256 x 256) along K."""
     seen = set()
     for g in WORKLOADS[name].gemms:
         for kind, make in (("A", make_activations), ("B", make_weights)):

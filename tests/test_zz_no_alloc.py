@@ -54,3 +54,22 @@ def test_scratch_one_range_and_size_limit():
     want = bsq.gemm(qa, qb, bias)
     assert torch.equal(out.view(torch.int16), want.view(torch.int16))
     assert bsq.device_status() == 0
+
+
+def test_scratch_request_that_fills_the_array_exactly():
+    """2 x 4096 x 2048 fp32 partial sums are exactly the array's 64 MiB: the last slice's top edge
+    is the array's last byte. The result must equal the caller-workspace split-K bit for bit; a
+    request 8 columns wider no longer fits and is refused before anything is enqueued."""
+    bsq = _bsq()
+    M, N, K, splits = 4096, 2048, 256, 2
+    assert splits * M * N * 4 == 64 << 20
+    qa, qb, bias = _operands("mxfp8", M, N, K, 4)
+    want = bsq.gemm_splitk(qa, qb, bias, splits=splits)
+    got = torch.empty_like(want)
+    assert _scratch(qa, qb, bias, got, splits) == bsq.OK
+    assert bsq.device_status() == 0
+    assert torch.equal(got.view(torch.int16), want.view(torch.int16))
+    qa2, qb2, bias2 = _operands("mxfp8", M, N + 8, K, 5)
+    out2 = torch.empty(M, N + 8, dtype=torch.bfloat16, device="cuda")
+    assert _scratch(qa2, qb2, bias2, out2, splits) == bsq.ERR_ARG
+    assert bsq.device_status() == 0
