@@ -1,27 +1,33 @@
 #!/usr/bin/env python3
 """Benchmark of the block-scaled linear layer on GB300.
 
-One step = the whole hot path over one batch: quantize the activations A (M x K) and the
-weights B (N x K) along K (one batched launch), then the block-scaled GEMM with the fused
-bias + bf16 epilogue.
-Default workload: ViT-B/16 MLP fc1 at training shape in MXFP8 (M = 14336, K = 768,
-N = 3072). Inputs are seeded synthetic data resident in HBM; the L2 cache is flushed (a
-256 MB write) between timed steps and every step is timed with CUDA events on the stream
-the kernels run on. One step (the L2 flush, an event, every layer's quantize and GEMM back to
-back, an event) is captured once into a CUDA graph with the events as graph nodes and replayed
-every timed step, so host launch overhead cannot open gaps inside the timed interval and the
-library kernels overlap each other's prologue and tail through programmatic dependent launch,
-as they do in a layer sequence; the kernels are exactly those the direct library calls launch.
-The per-kernel times behind `roofline` and `quantize` come from a second graph of the same
-step with events around each kernel (an event between two kernels serialises them), replayed
-after the timed loop.
+One step = the whole hot path over one batch: for every linear layer of the workload, quantize
+its activations A (M x K) and weights B (N x K) along K (one batched launch), then the
+block-scaled GEMM with the fused bias + bf16 epilogue.
+Default workload: the largest single-GPU configuration, the ViT-L/16 MLP at M = 51200 tokens
+(32 frames of 640 x 640): fc1 (K = 1024, N = 4096) and fc2 (K = 4096, N = 1024, its A a bf16
+GELU output) in MXFP4 and in NVFP4 (per-tensor scale from the tensor's amax), four layers per
+step. Inputs are seeded synthetic data resident in HBM; the L2 cache is flushed (a 256 MB write)
+between timed steps and every step is timed with CUDA events on the stream the kernels run on.
+One step (the L2 flush, an event, every layer's quantize and GEMM back to back, an event) is
+captured once into a CUDA graph with the events as graph nodes and replayed every timed step,
+so host launch overhead cannot open gaps inside the timed interval and the library kernels
+overlap each other's prologue and tail through programmatic dependent launch, as they do in a
+layer sequence; the kernels are exactly those the direct library calls launch. The per-kernel
+times behind `roofline`, `gemms` and `quantize` come from a second graph of the same step with
+events around each layer's quantize and GEMM (an event between two kernels serialises them),
+replayed after the timed loop.
 
-Printed JSON line: value = TFLOP/s of the whole step (2 M N K per GEMM); `roofline` for
-the dominant kernel (the GEMM) against the measured bf16 tensor peak times the nominal
-FP8 (x2) or FP4 (x6) ratio; `quantize` = the quantizer kernels' algorithmic GB/s against
-the measured HBM copy bandwidth; `e2e` = the same metric through the C ABI with pinned
-host buffers and the host<->device copies inside the timed region; `cpu_baseline` = the
-CPU oracle timed on a bounded sample of the same workload.
+Printed JSON line: value = TFLOP/s of the whole step (2 M N K per GEMM); `gemms` = one entry per
+layer (GEMM time, TFLOP/s, fraction of the format's peak: the measured bf16 tensor peak times the
+nominal FP8 (x2) or FP4 (x6) ratio, and of the 4.5 / 9 PF dense peaks the target is stated
+against, and of the attainable roofline); `quantize` = the quantizer kernels' algorithmic GB/s
+against the measured HBM copy bandwidth; `roofline` = the kernel class (GEMM or quantizer) with
+the larger share of the step; `e2e` = the same metric through the C ABI with pinned host buffers
+and the host<->device copies inside the timed region; `cpu_baseline` = the CPU oracle timed on a
+bounded sample of the same workload, with its quantize-only GB/s on one thread and on all cores;
+`other_configs` = the other configurations of the study (the tiny fp32 check, ViT-B/16 fc1,
+the ViT-L/16 MXFP8 and NVFP4 sweeps) timed per layer in the same run, for reference only.
 
 `e2e` goes through the Python API call by call (no graphs): per step the pinned host inputs
 are copied in, quantized, multiplied and the bf16 result is copied back; consecutive steps
@@ -53,6 +59,10 @@ from workloads import (MXFP8, NVFP4, MXFP4, WORKLOADS, make_activations, make_bi
 METRIC = "block-scaled GEMM TFLOPS (% dense FP8/FP4 peak); quantize GB/s (% HBM)"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 NOMINAL_RATIO = {MXFP8: 4.5 / 2.25, NVFP4: 13.5 / 2.25, MXFP4: 13.5 / 2.25}
+# the dense peaks the target of the study is stated against (TFLOP/s)
+STATED_PEAK = {MXFP8: 4500.0, NVFP4: 9000.0, MXFP4: 9000.0}
+HEADLINE = "vitl_mlp_large"
+OTHER_CONFIGS = ("tiny_mxfp8", "vitb_fc1_mxfp8", "vitl_mxfp8", "vitl_nvfp4")
 L2_FLUSH_BYTES = 256 << 20
 FMT_NAME = {MXFP8: "mxfp8", NVFP4: "nvfp4", MXFP4: "mxfp4"}
 
@@ -231,6 +241,48 @@ def cpu_oracle_sample(gemms, target_s: float = 10.0):
     return flops / secs / 1e12, secs, oracle.num_threads(), desc
 
 
+def cpu_quantize_sample(wl, target_s: float = 3.0):
+    """The oracle's quantizer alone (as it stands) on the largest activation matrix of each format
+    of the workload: R leading rows, R calibrated to about `target_s` seconds, timed once with one
+    thread and once with all host cores. GB/s on the algorithmic bytes the GPU quantizer is
+    measured on (source read once, twice for an NVFP4 scale computed from the tensor's amax;
+    codes and scales written). Returns a dict for cpu_baseline."""
+    import oracle
+
+    by_fmt = {}
+    for g in wl.gemms:
+        if g.fmt not in by_fmt or g.M * g.K > by_fmt[g.fmt].M * by_fmt[g.fmt].K:
+            by_fmt[g.fmt] = g
+    cores = oracle.num_threads()
+    out = {"unit": "GB/s", "cores": cores}
+    try:
+        for nthreads, key in ((1, "one_thread"), (cores, "all_cores")):
+            oracle.set_num_threads(nthreads)
+            nbytes, secs, parts = 0, 0.0, []
+            for fmt, g in sorted(by_fmt.items()):
+                eb = 4 if g.src_f32 else 2
+                full = g.a_dist == "normal_outlier50"  # the tiny case is drawn whole
+                r0 = g.M if full else min(g.M, 64)
+                x = make_activations(g) if full else make_activations(g, rows=r0)
+                t0 = time.perf_counter()
+                oracle.quantize(fmt, x)
+                t = max(time.perf_counter() - t0, 1e-6)
+                rows = r0 if full else int(min(g.M, max(r0, r0 * target_s / len(by_fmt) / t)))
+                if rows != r0:
+                    x = make_activations(g, rows=rows)
+                    t0 = time.perf_counter()
+                    oracle.quantize(fmt, x)
+                    t = time.perf_counter() - t0
+                nbytes += quant_bytes(fmt, rows, g.K, eb, True)
+                secs += t
+                parts.append("%s %d of %d rows x %d" % (fmt, rows, g.M, g.K))
+            out[key] = nbytes / secs / 1e9
+            out[key + "_sample"] = ", ".join(parts)
+    finally:
+        oracle.set_num_threads(cores)
+    return out
+
+
 def config_of(wl):
     return {"workload": wl.name, "description": wl.description,
             "gemms": [{"name": g.name, "format": g.fmt, "M": g.M, "N": g.N, "K": g.K} for g in wl.gemms],
@@ -289,59 +341,51 @@ def replica_throughput(ms_local: float, flops_per_rank: int, world: int, device=
 
 # ----------------------------------------------------------------------------------- GPU arm
 def kernel_source_hash() -> str:
-    """Hash of the sources the GEMM kernel is built from (its .cu, the shared device header and
-    the headers): the key of the recorded DRAM traffic."""
+    """Hash of every kernel source of the library (csrc/*.cu, *.cuh, *.h) and the public header:
+    the key of the recorded DRAM traffic, so that any kernel change invalidates the record."""
     h = hashlib.sha256()
     pkg = os.path.join(ROOT, "block_scaled_precision_bsq_gb300", "csrc")
-    for path in (os.path.join(pkg, "bsq_gemm.cu"), os.path.join(pkg, "bsq_device.cuh"),
-                 os.path.join(pkg, "bsq_internal.h"), os.path.join(ROOT, "include", "bsq.h")):
+    paths = sorted(os.path.join(pkg, n) for n in os.listdir(pkg) if n.endswith((".cu", ".cuh", ".h")))
+    for path in paths + [os.path.join(ROOT, "include", "bsq.h")]:
         with open(path, "rb") as f:
             h.update(os.path.basename(path).encode() + f.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(kernel_hash: str, workload: str):
-    """DRAM bytes per GEMM launch from the committed ncu summary, if it was taken on the
-    current kernel sources; otherwise None."""
+def recorded_traffic(kernel_hash: str, workload: str, kernel: str):
+    """DRAM bytes per step of `kernel`'s launches (read + write, from the committed ncu summary
+    `profiles/traffic.json`), if the capture was taken on the current kernel sources; else None."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         d = json.load(f)
-    e = d.get(workload)
+    e = d.get(workload, {}).get(kernel)
     if not e or e.get("kernel_source_hash") != kernel_hash:
         return None
-    return e.get("gemm_dram_bytes_per_launch")
+    return e.get("dram_bytes_per_step")
 
 
-def run_gpu(args, rank: int, world: int):
+def _host(x):
+    """A numpy input (uint16 = bf16 bits, or fp32) as a pinned host tensor."""
     import torch
 
-    import __graft_entry__ as ge
+    t = torch.from_numpy(x.view(np.int16) if x.dtype == np.uint16 else x)
+    return (t.view(torch.bfloat16) if x.dtype == np.uint16 else t).pin_memory()
 
-    ge.build()
-    import block_scaled_precision_bsq_gb300 as bsq
 
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    stream = torch.cuda.current_stream()
-    wl = WORKLOADS[args.workload]
-    peaks, peak_src = load_peaks()
+def build_units(wl, bsq, dev):
+    """The step of workload `wl` as units: one per linear layer (or one per chained MLP /
+    training step). A unit holds its pinned host inputs, an `alloc` making one device buffer set
+    (e2e double-buffers them), its quantize and GEMM phases, and its flops / algorithmic bytes."""
+    import torch
 
-    # ------------------------------------------------------------ inputs, resident in HBM
-    def host(x):
-        t = torch.from_numpy(x.view(np.int16) if x.dtype == np.uint16 else x)
-        return (t.view(torch.bfloat16) if x.dtype == np.uint16 else t).pin_memory()
-
-    # A unit is the work of one layer (or of one chained MLP): pinned host inputs, a device
-    # buffer set (`alloc`; e2e double-buffers them), and the quantize / GEMM phases.
     units = []
     if wl.chain is None:
         for g in wl.gemms:
             bias = make_bias(g)
-            hosts = {"a": host(make_activations(g)), "b": host(make_weights(g)),
-                     "bias": host(bias) if bias is not None else None}
+            hosts = {"a": _host(make_activations(g)), "b": _host(make_weights(g)),
+                     "bias": _host(bias) if bias is not None else None}
 
             def alloc(g=g, hosts=hosts):
                 return {"a": torch.empty_like(hosts["a"], device=dev), "b": torch.empty_like(hosts["b"], device=dev),
@@ -362,8 +406,8 @@ def run_gpu(args, rank: int, world: int):
                 else:
                     bsq.gemm(D["qa"], D["qb"], D["bias"], out=D["out"], stream=s)
 
-            units.append({"hosts": hosts, "alloc": alloc, "quant": quant, "gemm": gemm, "fmt": g.fmt,
-                          "flops": g.flops, "launches": 2 + (2 if g.fmt == NVFP4 else 0),
+            units.append({"name": g.name, "gemms": [g], "hosts": hosts, "alloc": alloc, "quant": quant, "gemm": gemm,
+                          "fmt": g.fmt, "flops": g.flops, "launches": 2 + (2 if g.fmt == NVFP4 else 0),
                           "qbytes": quant_bytes(g.fmt, g.M, g.K, 4 if g.src_f32 else 2, True) +
                                     quant_bytes(g.fmt, g.N, g.K, 4 if g.src_f32 else 2, True),
                           "gbytes": gemm_bytes(g.fmt, g.M, g.N, g.K, bias is not None)})
@@ -374,8 +418,8 @@ def run_gpu(args, rank: int, world: int):
         # dW = dY^T X: N x K over the M tokens, K cut into the library's number of ranges
         dw_splits = bsq.bsq_gemm_splitk_splits(fmt, N, K, M)
         assert dw_splits >= 1
-        hosts = {"x": host(make_activations(g)), "w": host(make_weights(g)), "bias": host(make_bias(g)),
-                 "dy": host(make_output_grad(g))}
+        hosts = {"x": _host(make_activations(g)), "w": _host(make_weights(g)), "bias": _host(make_bias(g)),
+                 "dy": _host(make_output_grad(g))}
 
         def alloc():
             D = {k: torch.empty_like(v, device=dev) for k, v in hosts.items()}
@@ -410,8 +454,8 @@ def run_gpu(args, rank: int, world: int):
                             stream=s)                                            # dW = dY^T X
 
         nv = fmt == NVFP4
-        units.append({"hosts": hosts, "alloc": alloc, "quant": quant, "gemm": gemm, "fmt": fmt,
-                      "flops": 3 * g.flops, "outs": ("out", "dx", "dw"),
+        units.append({"name": "train_step", "gemms": [g, g, g], "hosts": hosts, "alloc": alloc, "quant": quant,
+                      "gemm": gemm, "fmt": fmt, "flops": 3 * g.flops, "outs": ("out", "dx", "dw"),
                       # duals + GEMMs (+ the split-K sum); NVFP4: amax passes of X and W, the delayed-scale kernel
                       "launches": 6 + (1 if dw_splits > 1 else 0) + (2 if nv else 0) + (1 if delayed else 0) +
                                   (1 if nv and not delayed else 0),
@@ -423,13 +467,13 @@ def run_gpu(args, rank: int, world: int):
         g1, g2 = wl.gemms  # fc1: M x K1 -> N1, fc2: M x N1 -> N2
         fmt = g1.fmt
         b1, b2 = make_bias(g1), make_bias(g2)
-        hosts = {"x": host(make_activations(g1)), "w1": host(make_weights(g1)), "w2": host(make_weights(g2)),
-                 "b1": host(b1), "b2": host(b2)}
+        hosts = {"x": _host(make_activations(g1)), "w1": _host(make_weights(g1)), "w2": _host(make_weights(g2)),
+                 "b1": _host(b1), "b2": _host(b2)}
         fused = wl.chain in ("fused", "ln_fused")
         ln = wl.chain == "ln_fused"
         if ln:
             lg, lb = make_layernorm_affine(g1.K, g1.seed)
-            hosts.update({"ln_g": host(lg), "ln_b": host(lb)})
+            hosts.update({"ln_g": _host(lg), "ln_b": _host(lb)})
 
         def alloc():
             D = {k: torch.empty_like(v, device=dev) for k, v in hosts.items()}
@@ -455,8 +499,8 @@ def run_gpu(args, rank: int, world: int):
                 bsq.quantize(fmt, D["h"], out=D["qh"], stream=s)
             bsq.gemm(D["qh"], D["qw2"], D["b2"], out=D["out"], stream=s)
 
-        units.append({"hosts": hosts, "alloc": alloc, "quant": quant, "gemm": gemm, "fmt": fmt,
-                      "flops": g1.flops + g2.flops, "launches": (4 if ln else 3) if fused else 4,
+        units.append({"name": "mlp", "gemms": [g1, g2], "hosts": hosts, "alloc": alloc, "quant": quant, "gemm": gemm,
+                      "fmt": fmt, "flops": g1.flops + g2.flops, "launches": (4 if ln else 3) if fused else 4,
                       "qbytes": sum(quant_bytes(fmt, r, c, 2, True) for r, c in ((g1.M, g1.K), (g1.N, g1.K), (g2.N, g2.K))),
                       "gbytes": gemm_bytes(fmt, g1.M, g1.N, g1.K, True) + gemm_bytes(fmt, g2.M, g2.N, g2.K, True) -
                                 (2 * g1.M * g1.N if fused else 0) +
@@ -466,6 +510,125 @@ def run_gpu(args, rank: int, world: int):
         for k, v in U["hosts"].items():
             if v is not None:
                 U["D"][k].copy_(v)
+    return units
+
+
+class StepGraphs:
+    """Two CUDA graphs of one step, events recorded by graph nodes:
+     - the step graph (timed loop, `value`): flush, event, every unit's quantize and GEMM back
+       to back, event. Consecutive library kernels overlap their prologue with the previous
+       kernel's tail (programmatic dependent launch), as in a real layer sequence;
+     - the split graph (per-kernel times): flush, then per unit event / quantize / event / GEMM /
+       event. An event between two kernels serialises them and blocks the overlap, so this graph
+       is replayed after the timed loop, not in it."""
+
+    def __init__(self, units, flush, dev):
+        import torch
+
+        cap = torch.cuda.Stream(device=dev)
+        cap.wait_stream(torch.cuda.current_stream())
+        self.step_evs = tuple(torch.cuda.Event(enable_timing=True, external=True) for _ in range(2))
+        self.step_graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.step_graph, stream=cap):
+            flush.zero_()
+            self.step_evs[0].record(cap)
+            for U in units:
+                U["quant"](U["D"], cap)
+                U["gemm"](U["D"], cap)
+            self.step_evs[1].record(cap)
+        self.evs = [tuple(torch.cuda.Event(enable_timing=True, external=True) for _ in range(3)) for _ in units]
+        self.split_graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.split_graph, stream=cap):
+            flush.zero_()
+            for U, e in zip(units, self.evs):
+                e[0].record(cap)
+                U["quant"](U["D"], cap)
+                e[1].record(cap)
+                U["gemm"](U["D"], cap)
+                e[2].record(cap)
+        torch.cuda.synchronize()
+
+    def step(self):
+        """One replay of the step graph; returns its ms."""
+        self.step_graph.replay()
+        self.step_evs[1].synchronize()
+        return self.step_evs[0].elapsed_time(self.step_evs[1])
+
+    def split_step(self):
+        """One replay of the split graph; returns per unit (quantize ms, GEMM ms)."""
+        self.split_graph.replay()
+        self.evs[-1][2].synchronize()
+        return [(e[0].elapsed_time(e[1]), e[1].elapsed_time(e[2])) for e in self.evs]
+
+
+def per_unit_entries(units, split, peaks, peak_src):
+    """One entry per unit from the split-graph samples: the GEMM phase's time, TFLOP/s and
+    fractions of peak (measured bf16 x nominal format ratio, the stated dense peak, the
+    attainable roofline max(flops / peak, bytes / HBM)) and the quantize phase's GB/s."""
+    hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    bf16 = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    out = []
+    for i, U in enumerate(units):
+        g_ms = float(np.mean([t[i][1] for t in split]))
+        q_ms = float(np.mean([t[i][0] for t in split]))
+        peak = bf16 * NOMINAL_RATIO[U["fmt"]]
+        tflops = U["flops"] / (g_ms * 1e-3) / 1e12
+        t_ideal = max(U["flops"] / (peak * 1e12), U["gbytes"] / (hbm * 1e9))
+        out.append({"name": U["name"], "format": FMT_NAME[U["fmt"]],
+                    "shape": [{"M": g.M, "N": g.N, "K": g.K} for g in U["gemms"]],
+                    "gemm_ms": g_ms, "tflops": tflops, "peak": peak, "frac": tflops / peak,
+                    "frac_stated": tflops / STATED_PEAK[U["fmt"]], "attainable_frac": t_ideal / (g_ms * 1e-3),
+                    "quantize_ms": q_ms, "quantize_gbs": U["qbytes"] / (q_ms * 1e-3) / 1e9,
+                    "quantize_frac": U["qbytes"] / (q_ms * 1e-3) / 1e9 / hbm})
+    return out
+
+
+def time_other_config(name, bsq, dev, flush, peaks, peak_src, reps):
+    """A configuration other than the headline: its step's split graph, per-unit entries."""
+    import torch
+
+    wl = WORKLOADS[name]
+    units = build_units(wl, bsq, dev)
+    for _ in range(3):
+        for U in units:
+            U["quant"](U["D"], torch.cuda.current_stream())
+            U["gemm"](U["D"], torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    graphs = StepGraphs(units, flush, dev)
+    for _ in range(3):
+        graphs.split_step()
+    split = [graphs.split_step() for _ in range(reps)]
+    steps = [graphs.step() for _ in range(reps)]
+    assert bsq.device_status() == 0
+    flops = sum(U["flops"] for U in units)
+    ms = float(np.mean(steps))
+    entry = {"workload": name, "description": wl.description, "ms_per_step": ms,
+             "tflops": flops / (ms * 1e-3) / 1e12, "gemms": per_unit_entries(units, split, peaks, peak_src)}
+    del graphs, units
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return entry
+
+
+def run_gpu(args, rank: int, world: int):
+    import torch
+
+    import __graft_entry__ as ge
+
+    ge.build()
+    import block_scaled_precision_bsq_gb300 as bsq
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    wl = WORKLOADS[args.workload]
+    peaks, peak_src = load_peaks()
+    hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    peak_bf16 = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+
+    # inputs resident in HBM
+    units = build_units(wl, bsq, dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
     # warm-up through the direct calls (first calls set kernel attributes, build tables)
@@ -476,56 +639,14 @@ def run_gpu(args, rank: int, world: int):
     torch.cuda.synchronize()
     assert bsq.device_status() == 0
 
-    # Two CUDA graphs of the same step, events recorded by graph nodes:
-    #  - the step graph (timed loop, `value`): flush, event, every unit's quantize and GEMM back
-    #    to back, event. Consecutive library kernels overlap their prologue with the previous
-    #    kernel's tail (programmatic dependent launch), as in a real layer sequence;
-    #  - the split graph (per-kernel times for `roofline` and `quantize`): flush, then per unit
-    #    event / quantize / event / GEMM / event. An event between two kernels costs the step
-    #    ~6 us (it serialises them and blocks the overlap), so this graph is replayed after the
-    #    timed loop, not in it.
-    cap = torch.cuda.Stream(device=dev)
-    cap.wait_stream(stream)
-    step_evs = tuple(torch.cuda.Event(enable_timing=True, external=True) for _ in range(2))
-    step_graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(step_graph, stream=cap):
-        flush.zero_()
-        step_evs[0].record(cap)
-        for U in units:
-            U["quant"](U["D"], cap)
-            U["gemm"](U["D"], cap)
-        step_evs[1].record(cap)
-    evs = [tuple(torch.cuda.Event(enable_timing=True, external=True) for _ in range(3)) for _ in units]
-    split_graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(split_graph, stream=cap):
-        flush.zero_()
-        for U, e in zip(units, evs):
-            e[0].record(cap)
-            U["quant"](U["D"], cap)
-            e[1].record(cap)
-            U["gemm"](U["D"], cap)
-            e[2].record(cap)
-    torch.cuda.synchronize()
-
-    def step():
-        """One replay of the step graph; returns its ms."""
-        step_graph.replay()
-        step_evs[1].synchronize()
-        return step_evs[0].elapsed_time(step_evs[1])
-
-    def split_step():
-        """One replay of the split graph; returns per unit (quantize ms, GEMM ms)."""
-        split_graph.replay()
-        evs[-1][2].synchronize()
-        return [(e[0].elapsed_time(e[1]), e[1].elapsed_time(e[2])) for e in evs]
-
+    graphs = StepGraphs(units, flush, dev)
     # our kernels per step (the batched quantize counts once; NVFP4 adds an amax pass per
     # matrix; a chained MLP's unfused variant adds its quantize pass)
     launches_per_step = sum(U["launches"] for U in units)
 
     for _ in range(args.warmup):
-        step()
-        split_step()
+        graphs.step()
+        graphs.split_step()
     torch.cuda.synchronize()
     assert bsq.device_status() == 0
 
@@ -543,7 +664,7 @@ def run_gpu(args, rank: int, world: int):
         torch.distributed.barrier()
     torch.cuda.synchronize()
     t_wall = time.perf_counter()
-    times = [step() for _ in range(args.steps)]
+    times = [graphs.step() for _ in range(args.steps)]
     torch.cuda.synchronize()
     t_wall = time.perf_counter() - t_wall
     if world > 1:
@@ -556,25 +677,42 @@ def run_gpu(args, rank: int, world: int):
     ms_per_step, value = replica_throughput(float(np.mean(times)), flops, world, dev)
 
     # per-kernel times: the split graph, after the timed loop
-    split = [split_step() for _ in range(max(20, min(args.steps, 300)))]
+    split = [graphs.split_step() for _ in range(max(20, min(args.steps, 300)))]
     q_ms = [sum(t[0] for t in ts) for ts in split]
     g_ms = [sum(t[1] for t in ts) for ts in split]
     assert bsq.device_status() == 0
+    entries = per_unit_entries(units, split, peaks, peak_src)
 
-    # dominant kernel: the GEMM
-    fmt0 = units[0]["fmt"]
+    # GEMM aggregate: sum of flops over the flops-weighted peak time of each layer's format
     gemm_ms = float(np.mean(g_ms))
     gemm_tflops = flops / (gemm_ms * 1e-3) / 1e12
-    peak_bf16 = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
-    peak_tc = peak_bf16 * NOMINAL_RATIO[fmt0]
+    t_peak = sum(U["flops"] / (peak_bf16 * NOMINAL_RATIO[U["fmt"]] * 1e12) for U in units)
+    peak_tc = flops / t_peak / 1e12
+    g_bytes = int(sum(U["gbytes"] for U in units))
+    t_ideal = sum(max(U["flops"] / (peak_bf16 * NOMINAL_RATIO[U["fmt"]] * 1e12), U["gbytes"] / (hbm * 1e9))
+                  for U in units)
+    fmts = sorted({FMT_NAME[U["fmt"]] for U in units})
     khash = kernel_source_hash()
-    traffic = recorded_traffic(khash, wl.name)
+    gemm_roof = {"bound": "tensor", "achieved": gemm_tflops, "peak": peak_tc, "unit": "TFLOP/s",
+                 "frac": gemm_tflops / peak_tc, "traffic": recorded_traffic(khash, wl.name, "gemm_kernel"),
+                 "peak_source": "%s bf16 %.1f TFLOP/s x nominal ratio (%s)" % (
+                     peak_src, peak_bf16, ", ".join("%s x%.0f" % (f, NOMINAL_RATIO[f]) for f in fmts)),
+                 "attainable_frac": t_ideal / (gemm_ms * 1e-3), "kernel": "gemm_kernel",
+                 "ms_per_step": gemm_ms, "algorithmic_bytes": g_bytes,
+                 "per_launch": "all GEMM launches of a step together: 2MNK summed over the layers / "
+                               "their summed event times"}
     q_bytes = sum(U["qbytes"] for U in units)
     q_ms_mean = float(np.mean(q_ms))
     q_gbs = q_bytes / (q_ms_mean * 1e-3) / 1e9
-    hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
-    g_bytes = int(sum(U["gbytes"] for U in units))
-    t_ideal = max(flops / (peak_tc * 1e12), g_bytes / (hbm * 1e9))
+    quant = {"bound": "hbm", "achieved": q_gbs, "unit": "GB/s", "peak": hbm, "frac": q_gbs / hbm,
+             "ms_per_step": q_ms_mean, "bytes_per_step": q_bytes, "peak_source": "%s HBM copy" % peak_src,
+             "traffic": recorded_traffic(khash, wl.name, "quantize_kernel"), "kernel": "quantize_kernel",
+             "per_launch": "all quantizer launches of a step together (NVFP4 with a computed per-tensor "
+                           "scale: its amax pass included): algorithmic bytes / summed event times"}
+    # the dominant kernel class: the larger share of the split step
+    gemm_share = gemm_ms / (gemm_ms + q_ms_mean)
+    roofline = dict(gemm_roof if gemm_share >= 0.5 else quant)
+    roofline["share"] = gemm_share if gemm_share >= 0.5 else 1.0 - gemm_share
 
     # ------------------------------------------------------------ end to end through host buffers
     e2e_steps = max(3, min(args.steps, args.e2e_steps))
@@ -629,21 +767,20 @@ def run_gpu(args, rank: int, world: int):
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
     e2e_value = world * flops / (e2e_ms * 1e-3) / 1e12
     assert bsq.device_status() == 0
+    del bufs, graphs
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
 
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": FMT_NAME[fmt0], "data": "synthetic", "config": config_of(wl),
+        "vs_baseline": None, "dtype": "+".join(fmts), "data": "synthetic", "config": config_of(wl),
         "gpu_launches": launches_per_step * args.steps,
-        "roofline": {"bound": "tensor", "achieved": gemm_tflops, "peak": peak_tc, "unit": "TFLOP/s",
-                     "frac": gemm_tflops / peak_tc, "traffic": traffic,
-                     "peak_source": "%s bf16 %.1f TFLOP/s x nominal %s ratio %.0f" % (
-                         peak_src, peak_bf16, FMT_NAME[fmt0], NOMINAL_RATIO[fmt0]),
-                     "attainable_frac": t_ideal / (gemm_ms * 1e-3), "kernel": "gemm_kernel",
-                     "gemm_ms": gemm_ms, "algorithmic_bytes": g_bytes},
+        "roofline": roofline,
+        "gemms": entries,
+        "gemm": gemm_roof,
+        "quantize": quant,
         "split_ms_per_step": float(np.mean([q + g for q, g in zip(q_ms, g_ms)])),
-        "quantize": {"achieved": q_gbs, "unit": "GB/s", "peak": hbm, "frac": q_gbs / hbm, "ms_per_step": q_ms_mean,
-                     "bytes_per_step": q_bytes, "peak_source": "%s HBM copy" % peak_src},
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms, "steps": e2e_steps,
                 "how": "Python API call by call; pinned host copies in and out every step, overlapped across "
@@ -652,10 +789,17 @@ def run_gpu(args, rank: int, world: int):
         "wall_s_timed_region": t_wall,
         "kernel_source_hash": khash,
     }
+    del units
+    torch.cuda.empty_cache()
+    if world == 1 and not args.no_other_configs and args.workload == HEADLINE:
+        line["other_configs"] = [time_other_config(n, bsq, dev, flush, peaks, peak_src, reps=30)
+                                 for n in OTHER_CONFIGS]
+        line["other_configs_note"] = ("the study's other configurations, timed per layer in the same run "
+                                      "(split graph, L2 flushed); parity cases, not the headline")
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, secs, cores, desc = oracle_sample(wl, target_s=args.cpu_seconds)
         line["cpu_baseline"] = {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc,
-                                "seconds": secs}
+                                "seconds": secs, "quantize": cpu_quantize_sample(wl)}
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0
@@ -667,10 +811,11 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="vitb_fc1_mxfp8")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=HEADLINE)
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="size of the CPU oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-other-configs", action="store_true", help="skip timing the non-headline configurations")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be >= 3")
