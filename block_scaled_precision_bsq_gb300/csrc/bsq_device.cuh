@@ -478,4 +478,56 @@ __device__ __forceinline__ uint32_t cvt_e4m3x4(float a, float b, float c, float 
   return r;
 }
 
+// ---------------------------------------------------------------------------- packed fp32 pairs
+// Two fp32 values in one 64-bit operand (`lo` in bits 0..31) of the f32x2 instructions, each lane
+// rounded to nearest even exactly like the scalar operation.
+__device__ __forceinline__ uint64_t f2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_split(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_splat(float v) { return f2(v, v); }
+
+// ---------------------------------------------------------------------------- IEEE quotients
+// NVFP4 divides every element of a block by one fp32 divisor d and rounds the IEEE quotient
+// fp32(x / d). With r = fp32(1 / d) correctly rounded (computed once per divisor), the quotient
+// follows from one multiply and two fused multiply-adds by Markstein's remainder step
+// (P. Markstein, "Computation of elementary functions on the IBM RISC System/6000 processor",
+// IBM J. Res. Develop. 34(1), 1990: from a correctly rounded reciprocal and a quotient within an
+// ulp, one exact remainder and one fused correction give the correctly rounded quotient):
+//   q0 = fp32(x r),  e = q0 d - x (exact in one fma),  q = fp32(q0 - e r).
+// The remainder is taken as q0 d - x rather than x - q0 d so that x = -0 keeps its sign.
+// Valid while nothing overflows or underflows: d in [2^-92, 2^100) and |x| r below 2^100
+// (markstein_ok); quotients far below the smallest value any code of the target format rounds
+// away from zero (2^-10 for E4M3, 2^-3 for e2m1) can carry an underflowed remainder but still
+// round to a zero code, exactly as the IEEE quotient does.
+__device__ __forceinline__ float markstein_quotient(float x, float d, float r) {
+  const float q0 = __fmul_rn(x, r);
+  const float e = __fmaf_rn(q0, d, -x);
+  return __fmaf_rn(-e, r, q0);
+}
+// True when markstein_quotient(x, d, r) is the IEEE quotient for every |x| <= xmax.
+__device__ __forceinline__ bool markstein_ok(float d, float r, float xmax) {
+  const uint32_t db = __float_as_uint(d);
+  return db >= (35u << 23) && db < (227u << 23) && __fmul_rn(xmax, r) < 0x1p100f;
+}
+
 }  // namespace bsq

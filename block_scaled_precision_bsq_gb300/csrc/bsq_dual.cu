@@ -63,7 +63,9 @@ constexpr int kDStageBytes = 16384;  // transposed codes of one tile (at most 12
 // ring, barriers; nothing static, so that two CTAs fit on an SM
 constexpr int kDRingOff = kDStageBytes;
 constexpr int kDBarOff = kDRingOff + kDStages * kDTileBytes;
-constexpr int kDSmem = kDBarOff + 128;
+constexpr int kDTabOff = kDBarOff + 128;  // NVFP4: reciprocals of the 128 block divisors
+constexpr int kDSmem = kDTabOff + 512;
+static_assert(kDCtasPerSm * (kDSmem + 1024) <= 233472, "two CTAs per SM, each with 1 KB reserved");
 
 struct DualArgs {
   int64_t rows, cols;  // R, C
@@ -173,18 +175,20 @@ __device__ __forceinline__ uint32_t sr_code(float y, float x, uint32_t h) {
   return ((yb >> 31) << kSign) | mag;
 }
 
-// The value a code encodes, x / scale: MX x * (1 / scale) (exact), NVFP4 fp32(x / fp32(s g)).
-template <int FMT>
-__device__ __forceinline__ float scaled(float x, float f) {
-  if constexpr (FMT == BSQ_NVFP4) return __fdiv_rn(x, f);
+// The value a code encodes, x / scale: MX x * (1 / scale) (exact), NVFP4 fp32(x / fp32(s g)), the
+// IEEE quotient -- by markstein_quotient with the block's reciprocal r where that is valid for the
+// whole block (kQuick), else by division.
+template <int FMT, bool kQuick>
+__device__ __forceinline__ float scaled(float x, float f, float r) {
+  if constexpr (FMT == BSQ_NVFP4) return kQuick ? markstein_quotient(x, f, r) : __fdiv_rn(x, f);
   else return x * f;
 }
 
 // Round-to-nearest-even codes of n (a multiple of 4, at most 8 for e2m1) consecutive elements
 // x[0..n) with the block factor f, packed: E4M3 one byte each (element i in byte i % 4 of
 // w[i / 4]), e2m1 one nibble each (element i in bits 4i of w[0]).
-template <int FMT, int N>
-__device__ __forceinline__ void rne_codes(const float* x, float f, uint32_t* w) {
+template <int FMT, int N, bool kQuick>
+__device__ __forceinline__ void rne_codes(const float* x, float f, float r, uint32_t* w) {
   if constexpr (FMT == BSQ_MXFP8) {
 #pragma unroll
     for (int j = 0; j < N / 4; ++j)
@@ -192,11 +196,11 @@ __device__ __forceinline__ void rne_codes(const float* x, float f, uint32_t* w) 
   } else if constexpr (N == 8) {
     float y[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) y[i] = scaled<FMT>(x[i], f);
+    for (int i = 0; i < 8; ++i) y[i] = scaled<FMT, kQuick>(x[i], f, r);
     w[0] = cvt_e2m1x8(y);
   } else {
-    w[0] = cvt_e2m1x2(scaled<FMT>(x[0], f), scaled<FMT>(x[1], f)) |
-           (cvt_e2m1x2(scaled<FMT>(x[2], f), scaled<FMT>(x[3], f)) << 8);
+    w[0] = cvt_e2m1x2(scaled<FMT, kQuick>(x[0], f, r), scaled<FMT, kQuick>(x[1], f, r)) |
+           (cvt_e2m1x2(scaled<FMT, kQuick>(x[2], f, r), scaled<FMT, kQuick>(x[3], f, r)) << 8);
   }
 }
 
@@ -208,8 +212,8 @@ __device__ __forceinline__ void rne_codes(const float* x, float f, uint32_t* w) 
 // E4M3 tests the range once per four elements: when all four scaled values lie in the normal
 // range (all but ~1 % of groups: the subnormal range sits 2^14 below a block's maximum), each
 // code is sr_code's normal-range carry form without a branch per element; otherwise sr_code.
-template <int FMT>
-__device__ __forceinline__ uint32_t sr_codes4(const float* x, float f, uint4 q) {
+template <int FMT, bool kQuick>
+__device__ __forceinline__ uint32_t sr_codes4(const float* x, float f, float r, uint4 q) {
   constexpr int kBits = (FMT == BSQ_MXFP8) ? 8 : 4;
   const uint32_t qq[4] = {q.x, q.y, q.z, q.w};
   uint32_t w = 0;
@@ -218,7 +222,7 @@ __device__ __forceinline__ uint32_t sr_codes4(const float* x, float f, uint4 q) 
     uint32_t bmin = 0xFFFFFFFFu;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      y[i] = scaled<FMT>(x[i], f);
+      y[i] = scaled<FMT, kQuick>(x[i], f, r);
       bmin = min(bmin, __float_as_uint(y[i]) & 0x7FFFFFFFu);
     }
     if (bmin >= (121u << 23)) {  // 2^-6, the smallest normal E4M3 magnitude
@@ -236,7 +240,7 @@ __device__ __forceinline__ uint32_t sr_codes4(const float* x, float f, uint4 q) 
   } else {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const float y = scaled<FMT>(x[i], f);
+      const float y = scaled<FMT, kQuick>(x[i], f, r);
       w |= sr_code<FMT>(y, FMT == BSQ_NVFP4 ? y : x[i], qq[i]) << (kBits * i);
     }
   }
@@ -252,17 +256,66 @@ __device__ __forceinline__ uint32_t sign_codes(const float* x) {
   return w;
 }
 
+// Codes of one block of BS elements xb (MX 32, NVFP4 16) with the block factor f (and NVFP4's
+// reciprocal r), packed into wb as rne_codes / sr_codes4 pack them: round to nearest even, or
+// stochastic with the random words of element group g0 (8 elements per group) in `layout`.
+template <int FMT, bool SR, bool kQuick>
+__device__ __forceinline__ void block_codes(const float* xb, float f, float r, uint64_t g0, uint32_t layout,
+                                            const DualArgs& a, uint32_t* wb) {
+  constexpr bool kFp8 = (FMT == BSQ_MXFP8);
+  constexpr int BS = (FMT == BSQ_NVFP4) ? 16 : 32;
+  if constexpr (SR) {
+#pragma unroll
+    for (int go = 0; go < BS / 8; ++go) {
+      uint4 rlo, rhi;
+      sr_words8(g0 + go, layout, a, rlo, rhi);
+      const uint32_t v0 = sr_codes4<FMT, kQuick>(xb + 8 * go, f, r, rlo);
+      const uint32_t v1 = sr_codes4<FMT, kQuick>(xb + 8 * go + 4, f, r, rhi);
+      if constexpr (kFp8) {
+        wb[2 * go] = v0;
+        wb[2 * go + 1] = v1;
+      } else {
+        wb[go] = v0 | (v1 << 16);
+      }
+    }
+  } else {
+    constexpr int kWords = BS * (kFp8 ? 8 : 4) / 32;
+#pragma unroll
+    for (int j = 0; j < kWords; ++j) rne_codes<FMT, kFp8 ? 4 : 8, kQuick>(xb + (kFp8 ? 4 : 8) * j, f, r, wb + j);
+  }
+}
+
+// NVFP4 divisors of the tensor: g, 6 g, its reciprocal (NaN where markstein_quotient is not valid
+// for 6 g) and the reciprocal of fp32(s g) for every E4M3 scale code s (NaN for s = 0 and where the
+// quotient step is not valid for that divisor), in shared memory.
+struct NvScales {
+  float g, six_g, r6;
+  const float* rtab;
+};
+
 // Block scale from the block maximum: MX the UE8M0 byte and 1 / scale; NVFP4 the E4M3 code of
-// fp32(amax / fp32(6 g)) and fp32(s g) (0 when s is 0: the block's codes are signed zeros).
+// fp32(amax / fp32(6 g)) and fp32(s g) (0 when s is 0: the block's codes are signed zeros), with r
+// the reciprocal of fp32(s g) and `quick` true when markstein_quotient gives every element's IEEE
+// quotient (scaled<FMT, true>).
 template <int FMT>
-__device__ __forceinline__ uint32_t block_scale(float amax, float g, float six_g, float& f) {
+__device__ __forceinline__ uint32_t block_scale(float amax, const NvScales& nv, float& f, float& r, bool& quick) {
   if constexpr (FMT == BSQ_NVFP4) {
-    const uint32_t sc = g != 0.0f ? (cvt_e4m3x2(__fdiv_rn(amax, six_g), 0.0f) & 0xFFu) : 0u;
-    f = __fmul_rn(e4m3_to_f32(sc), g);
+    uint32_t sc = 0;
+    if (nv.g != 0.0f) {
+      float qs;
+      if (__fmul_rn(amax, nv.r6) < 0x1p100f) qs = markstein_quotient(amax, nv.six_g, nv.r6);
+      else qs = __fdiv_rn(amax, nv.six_g);
+      sc = cvt_e4m3x2(qs, 0.0f) & 0xFFu;
+    }
+    f = __fmul_rn(e4m3_to_f32(sc), nv.g);
+    r = nv.rtab[sc];
+    quick = __fmul_rn(amax, r) < 0x1p100f;
     return sc;
   } else {
     const uint32_t sb = mx_scale_byte<FMT>(amax);
     f = mx_inv_scale(sb);
+    r = 0.0f;
+    quick = true;
     return sb;
   }
 }
@@ -359,10 +412,20 @@ __global__ void __launch_bounds__(kDThreads, kDCtasPerSm)
   if (issuer) prefetch_tmap(&col_map);
   const int64_t R = a.rows, C = a.cols;
   // NVFP4 per-tensor scale (both layouts): given, or amax / 2688 with amax in the row tail
-  float g = 0.0f, six_g = 0.0f;
+  float* nv_rtab = reinterpret_cast<float*>(d_smem + kDTabOff);
+  NvScales nv{0.0f, 0.0f, 0.0f, nv_rtab};
   if constexpr (kNv) {
-    g = a.g_in != nullptr ? *a.g_in : __fdiv_rn(__uint_as_float(a.row_tail[1]), 2688.0f);
-    six_g = __fmul_rn(6.0f, g);
+    const float g = a.g_in != nullptr ? *a.g_in : __fdiv_rn(__uint_as_float(a.row_tail[1]), 2688.0f);
+    nv.g = g;
+    nv.six_g = __fmul_rn(6.0f, g);
+    const float r6 = __frcp_rn(nv.six_g);
+    nv.r6 = markstein_ok(nv.six_g, r6, 0.0f) ? r6 : __uint_as_float(0x7FC00000u);
+    if (ct < 128) {  // the block divisors' reciprocals, one scale code per thread
+      const float d = __fmul_rn(e4m3_to_f32(static_cast<uint32_t>(ct)), g);
+      const float r = __frcp_rn(d);
+      nv_rtab[ct] = (ct != 0 && markstein_ok(d, r, 0.0f)) ? r : __uint_as_float(0x7FC00000u);
+    }
+    consumers_sync();
     if (blockIdx.x == 0 && ct == 0) {
       a.row_tail[0] = __float_as_uint(g);
       a.col_tail[0] = __float_as_uint(g);
@@ -427,29 +490,17 @@ __global__ void __launch_bounds__(kDThreads, kDCtasPerSm)
           for (int k = 0; k < BS; ++k) m[k & 3] = fmaxf(m[k & 3], fabsf(xb[k]));
           const float amax = fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
           if constexpr (kNv) run_max = max(run_max, __float_as_uint(amax));
-          float bf;
-          sbytes |= block_scale<FMT>(amax, g, six_g, bf) << (8 * h);
+          float bf, br;
+          bool quick;
+          sbytes |= block_scale<FMT>(amax, nv, bf, br, quick) << (8 * h);
           uint32_t* wb = w + h * kBlockWords;
           if (kNv && bf == 0.0f) {
             wb[0] = sign_codes<8>(xb);
             wb[1] = sign_codes<8>(xb + 8);
-          } else if constexpr (SR) {
-#pragma unroll
-            for (int go = 0; go < BS / 8; ++go) {
-              uint4 rlo, rhi;
-              sr_words8(g0 + h * (BS / 8) + go, 0u, a, rlo, rhi);
-              const uint32_t v0 = sr_codes4<FMT>(xb + 8 * go, bf, rlo);
-              const uint32_t v1 = sr_codes4<FMT>(xb + 8 * go + 4, bf, rhi);
-              if constexpr (kFp8) {
-                wb[2 * go] = v0;
-                wb[2 * go + 1] = v1;
-              } else {
-                wb[go] = v0 | (v1 << 16);
-              }
-            }
+          } else if (!kNv || quick) {
+            block_codes<FMT, SR, true>(xb, bf, br, g0 + h * (BS / 8), 0u, a, wb);
           } else {
-#pragma unroll
-            for (int j = 0; j < kBlockWords; ++j) rne_codes<FMT, kFp8 ? 4 : 8>(xb + (kFp8 ? 4 : 8) * j, bf, wb + j);
+            block_codes<FMT, SR, false>(xb, bf, br, g0 + h * (BS / 8), 0u, a, wb);
           }
         }
         if (r < R && c < C) {
@@ -517,31 +568,19 @@ __global__ void __launch_bounds__(kDThreads, kDCtasPerSm)
             for (int k = i; k < BS; k += 4) m[i] = fmaxf(m[i], fabsf(xb[k]));
           }
           const float amax = fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
-          float bf;
-          const uint32_t sbyte = block_scale<FMT>(amax, g, six_g, bf);
+          float bf, br;
+          bool quick;
+          const uint32_t sbyte = block_scale<FMT>(amax, nv, bf, br, quick);
           sbytes |= sbyte << (8 * (bb * kUnitScales + h));
           constexpr int kWords = BS * (kFp8 ? 8 : 4) / 32;  // code words of one block
           uint32_t* wb = w + h * kWords;
           if (kNv && bf == 0.0f) {
             wb[0] = sign_codes<8>(xb);
             wb[1] = sign_codes<8>(xb + 8);
-          } else if constexpr (SR) {
-#pragma unroll
-            for (int go = 0; go < BS / 8; ++go) {
-              uint4 rlo, rhi;
-              sr_words8(g0 + h * (BS / 8) + go, 1u, a, rlo, rhi);
-              const uint32_t v0 = sr_codes4<FMT>(xb + 8 * go, bf, rlo);
-              const uint32_t v1 = sr_codes4<FMT>(xb + 8 * go + 4, bf, rhi);
-              if constexpr (kFp8) {
-                wb[2 * go] = v0;
-                wb[2 * go + 1] = v1;
-              } else {
-                wb[go] = v0 | (v1 << 16);
-              }
-            }
+          } else if (!kNv || quick) {
+            block_codes<FMT, SR, true>(xb, bf, br, g0 + h * (BS / 8), 1u, a, wb);
           } else {
-#pragma unroll
-            for (int j = 0; j < kWords; ++j) rne_codes<FMT, kFp8 ? 4 : 8>(xb + (kFp8 ? 4 : 8) * j, bf, wb + j);
+            block_codes<FMT, SR, false>(xb, bf, br, g0 + h * (BS / 8), 1u, a, wb);
           }
         }
         // codes -> staging row cc, bytes [rb * kUnitCodeBytes / 32, + kUnitCodeBytes)

@@ -154,32 +154,6 @@ __device__ __forceinline__ void tma_store_3d(const void* tmap, const void* smem_
                : "memory");
 }
 
-// Packed fp32 pairs for the epilogue: two values in one 64-bit operand (`lo` in bits 0..31) of
-// the f32x2 instructions, each lane rounded to nearest even exactly like the scalar operation.
-__device__ __forceinline__ uint64_t f2(float lo, float hi) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-  return r;
-}
-__device__ __forceinline__ void f2_split(uint64_t v, float& lo, float& hi) {
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
-  uint64_t r;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-  return r;
-}
-__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
-  uint64_t r;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
-  uint64_t r;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-__device__ __forceinline__ uint64_t f2_splat(float v) { return f2(v, v); }
 
 // GELU(v) = v Phi(v) (the erf form) with Phi(v) = 1 - erfc(z) / 2 for v >= 0 and erfc(z) / 2
 // for v < 0, z = |v| / sqrt 2 (no cancellation in the negative tail), and erfc from

@@ -8,22 +8,19 @@
 // the BF16 ledger blog section 5.4; 6 for e2m1). The UE8M0 exponent of a block is
 // floor(log2(amax)) - emax with emax the exponent of the element format's top binade.
 //
-// Work mapping (four CTAs per SM for MX, two for NVFP4; persistent). The source is cut into chunks of whole rows
-// (or, for rows longer than a chunk, row pieces of whole 1024-element segments); a chunk is
-// contiguous in memory and comes in with one 1-D TMA bulk copy. A producer thread per CTA
-// keeps a ring of up to kRing chunk buffers in flight -- for a 22 MB matrix that is nearly
-// every chunk of the SM's share, requested at kernel start -- and the consumer warps (dealt
-// warp steps round-robin over the CTA's chunks) quantize a chunk straight from shared memory,
-// walking it as one flat array: each warp step covers 1024 consecutive elements, each lane 32,
-// i.e. exactly one MX block or two NVFP4 blocks, so a lane finds its block maxima without any
-// shuffle and computes one scale position per block. Codes leave as 32 (E4M3) or 16 (e2m1)
-// contiguous bytes per lane; each block's scale byte is stored at its place in the tiled
-// layout (128 rows x 4 columns per 512-byte tile, row r at byte (r % 32) * 16 +
-// ((r / 32) % 4) * 4), the lane of a row's last block also zeroing the padding columns of that
-// 4-column group. Scale bytes of the padding rows of the last row tile are written as zeros by
-// the kernel itself. (A lane-per-16-elements version with shuffles for the block maxima spent
-// ~14 instructions per element against ~10 here.) In LayerNorm mode each warp instead owns whole
-// rows of a chunk: the row's statistics, then its affine step and quantization.
+// Work mapping. bsq_quantize / bsq_quantize_batch run stream_kernel: every matrix of a batch is
+// one flat array, a warp step is 1024 consecutive elements of one matrix and a lane's piece 32 of
+// them -- one MX block, two NVFP4 blocks -- loaded straight into registers (two 32-byte loads for
+// bf16) one step ahead of the piece being quantized; no shared-memory staging and no barriers,
+// so the instructions are the element arithmetic itself: block maxima on packed bf16 pairs, the
+// scaling (MX: a power of two) or the IEEE quotient (NVFP4: Markstein's remainder step from a
+// table of correctly rounded reciprocals) on packed fp32 pairs, cvt.rn.satfinite to E4M3 / e2m1.
+// Codes leave as 32 (E4M3) or 16 (e2m1) contiguous bytes per lane; each block's scale byte is
+// stored at its place in the tiled layout (128 rows x 4 columns per 512-byte tile, row r at byte
+// (r % 32) * 16 + ((r / 32) % 4) * 4); the padding of the tiled scales is zeroed after the loop.
+// bsq_layernorm_quantize runs layernorm_kernel: chunks of whole rows brought into shared memory
+// by 1-D TMA bulk copies, each consumer warp owning whole rows (the row's statistics, then its
+// affine step and quantization).
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -36,7 +33,6 @@ namespace bsq {
 namespace {
 
 constexpr int kLaneElems = 32;         // elements per lane per step: one MX block, two NVFP4 blocks
-constexpr int kSeg = 32 * kLaneElems;   // elements per warp step
 constexpr int kChunkMax = 16384;        // bytes per chunk buffer
 constexpr int kChunkMin = 4096;         // smallest chunk worth a copy (small tensors)
 constexpr int kAmaxThreads = 256;
@@ -45,19 +41,15 @@ constexpr int kLnMaxRows = kChunkMax / (32 * 2);  // rows of a chunk: rows of at
 
 enum NvMode { kMx = 0, kNvComputed = 1, kNvGiven = 2 };
 
-// Occupancy per format (warp 0's lane 0 is the TMA producer, the other warps consume): MX, four
-// resident CTAs of 256 threads with a 3-chunk ring each (28 consumer warps per SM to hide
-// latency, 64 registers); NVFP4, whose IEEE divisions need more registers, two CTAs of 384
-// threads with a 6-chunk ring (72 registers; at 64 it spilled and ran 8-15 % slower).
-template <bool NV>
+// LayerNorm kernel: four resident CTAs of 256 threads per SM (warp 0's lane 0 is the TMA producer,
+// the other warps consume), a 3-chunk ring each.
 struct QCfg {
-  static constexpr int kThreads = NV ? 384 : 256;
-  static constexpr int kCtasPerSm = NV ? 2 : 4;
-  static constexpr int kRing = NV ? 6 : 3;
+  static constexpr int kThreads = 256;
+  static constexpr int kCtasPerSm = 4;
+  static constexpr int kRing = 3;
   static constexpr int kConsumerWarps = kThreads / 32 - 1;
   static constexpr int kSmem = kRing * kChunkMax + 128;
 };
-inline int ctas_per_sm(int fmt) { return fmt == BSQ_NVFP4 ? QCfg<true>::kCtasPerSm : QCfg<false>::kCtasPerSm; }
 
 struct QuantArgs {
   const uint8_t* src;
@@ -69,13 +61,10 @@ struct QuantArgs {
   float* g_out;         // NVFP4 computed mode (nullable)
   int64_t nsc;          // scale columns per row
   int64_t nct;          // 4-column scale tiles per row
-  // chunking: either `rows_per_chunk` whole rows (cspan == cols) or one row piece of `cspan`
-  // elements (rows_per_chunk == 1, chunks_per_row pieces per row)
-  int64_t rows_per_chunk;
-  int64_t cspan;
-  int64_t chunks_per_row;
-  int64_t nchunks;
+  int64_t rows_per_chunk;  // LayerNorm kernel: whole rows per chunk
   uint32_t cols_magic;  // floor(2^32 / cols) + 1: f / cols == umulhi(f, cols_magic) for f * cols < 2^32
+  uint64_t cols_magic64;  // floor((2^64 - 1) / cols): f / cols is umul64hi(f, .) or one more
+  int64_t elems;        // rows * cols
   // LayerNorm mode: y = (x - mean) / sqrt(var + eps) * gamma + beta per row before quantizing
   const uint16_t* gamma;  // cols bf16
   const uint16_t* beta;   // cols bf16
@@ -86,7 +75,7 @@ struct QuantArgs {
 // chunk lists are concatenated, matrix t owning global chunks [chunk_start[t], chunk_start[t+1]).
 struct QuantBatch {
   int n;
-  int64_t chunk_start[kMaxBatch + 1];
+  int64_t chunk_start[kMaxBatch + 1];  // LayerNorm kernel: chunks; streaming kernel: warp steps
   QuantArgs t[kMaxBatch];
   int* status;
 };
@@ -133,34 +122,175 @@ __device__ __forceinline__ int64_t scale_word_offset(int64_t r, int64_t c4, int6
   return ((r >> 7) * nct + (c4 >> 2)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4;
 }
 
-// Codes of 16 elements of one NVFP4 block with block maximum `amax` -> 8 bytes in w[0..1]; returns
-// the block's E4M3 scale code.
-__device__ __forceinline__ uint32_t nv_block16(const float* x, float amax, float g, float six_g, uint32_t* w) {
-  uint32_t scode = 0;
-  if (g != 0.0f) scode = cvt_e4m3x2(__fdiv_rn(amax, six_g), 0.0f) & 0xFFu;
-  const float sc = e4m3_to_f32(scode);
-  const float sg = __fmul_rn(sc, g);
-  w[0] = w[1] = 0;
-#pragma unroll
-  for (int i = 0; i < 16; i += 2) {
-    uint32_t c;
-    if (sc == 0.0f) {
-      c = ((__float_as_uint(x[i]) >> 31) << 3) | ((__float_as_uint(x[i + 1]) >> 31) << 7);
-    } else {
-      c = cvt_e2m1x2(__fdiv_rn(x[i], sg), __fdiv_rn(x[i + 1], sg));
-    }
-    w[i >> 3] |= c << (4 * (i & 7));
+// NVFP4 divisors of one matrix: g, 6 g and its reciprocal, and a table holding for every E4M3
+// scale code s the block divisor d = fp32(s g) and r = fp32(1 / d) (NaN where the remainder step
+// of markstein_quotient is not valid for that d: the block then divides).
+struct NvCtx {
+  float g = 0.0f, six_g = 0.0f, r6 = 0.0f;
+  const float2* tab = nullptr;
+};
+
+// Fill `tab` (128 entries, shared by the warp's lanes) for per-tensor scale g; returns the
+// context. Called by the whole warp.
+// With g = 0 the scale quotient is taken as amax * 0 (r6 = 0): every block scale is then 0. The
+// entry of scale code 0 is {0, 0}: the quotient step then yields a zero carrying the sign of x,
+// the code the format's rule gives a block whose scale is 0.
+__device__ __forceinline__ NvCtx nv_context(float g, float2* tab) {
+  NvCtx c;
+  c.g = g;
+  c.six_g = __fmul_rn(6.0f, g);
+  const float r6 = __frcp_rn(c.six_g);
+  if (g == 0.0f) {
+    c.r6 = 0.0f;
+  } else {
+    c.r6 = markstein_ok(c.six_g, r6, 0.0f) ? r6 : __uint_as_float(0x7FC00000u);
   }
+  __syncwarp();  // every lane is done with the previous matrix's table
+  for (uint32_t code = lane_id(); code < 128u; code += 32u) {
+    const float d = __fmul_rn(e4m3_to_f32(code), g);
+    const float r = __frcp_rn(d);
+    tab[code] = code == 0u ? make_float2(0.0f, 0.0f)
+                           : make_float2(d, markstein_ok(d, r, 0.0f) ? r : __uint_as_float(0x7FC00000u));
+  }
+  __syncwarp();
+  c.tab = tab;
+  return c;
+}
+
+// Codes of 16 elements of one NVFP4 block with block maximum `amax` -> 8 bytes in w[0..1]; returns
+// the block's E4M3 scale code s = E4M3(fp32(amax / fp32(6 g))), then e2m1(fp32(x / fp32(s g)))
+// per element, both quotients the IEEE ones (markstein_quotient where valid, else the division).
+__device__ __forceinline__ uint32_t nv_block16(const float* x, float amax, const NvCtx& c, uint32_t* w) {
+  uint32_t scode = 0;
+  if (c.g != 0.0f) {
+    float qs;
+    if (__fmul_rn(amax, c.r6) < 0x1p100f) qs = markstein_quotient(amax, c.six_g, c.r6);
+    else qs = __fdiv_rn(amax, c.six_g);
+    scode = cvt_e4m3x2(qs, 0.0f) & 0xFFu;
+  }
+  if (scode == 0u) {  // s = 0: zero codes carrying the sign of each element
+    uint32_t c0 = 0, c1 = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      c0 |= (__float_as_uint(x[i]) >> 31) << (4 * i + 3);
+      c1 |= (__float_as_uint(x[8 + i]) >> 31) << (4 * i + 3);
+    }
+    w[0] = c0;
+    w[1] = c1;
+    return 0u;
+  }
+  const float2 dr = c.tab[scode];
+  float q[16];
+  if (__fmul_rn(amax, dr.y) < 0x1p100f) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) q[i] = markstein_quotient(x[i], dr.x, dr.y);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) q[i] = __fdiv_rn(x[i], dr.x);
+  }
+  w[0] = cvt_e2m1x8(q);
+  w[1] = cvt_e2m1x8(q + 8);
   return scode;
+}
+
+// ---------------------------------------------------------------------------- bf16 fast paths
+// max(|a|, |b|) of each bf16 half (the result's sign bits are those of a and b XOR-ed; callers
+// mask them); a NaN operand gives the other one, as fmaxf does.
+__device__ __forceinline__ uint32_t bf16x2_maxabs(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+// Largest |x| of the 2 N bf16 values in w[0..N) (N a power of two), as an fp32 value (exact).
+template <int N>
+__device__ __forceinline__ float bf16_block_amax(const uint32_t* w) {
+  uint32_t m[N];
+#pragma unroll
+  for (int i = 0; i < N; ++i) m[i] = w[i];
+#pragma unroll
+  for (int n = N / 2; n >= 1; n /= 2) {
+#pragma unroll
+    for (int i = 0; i < n; ++i) m[i] = bf16x2_maxabs(m[i], m[i + n]);
+  }
+  return __uint_as_float(max(m[0] & 0x7FFFu, (m[0] >> 16) & 0x7FFFu) << 16);
+}
+
+// The bf16 pair of word v as packed fp32 (element 2i of the word in the low lane).
+__device__ __forceinline__ uint64_t bf16x2_to_f2(uint32_t v) {
+  return f2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
+}
+
+// MX block of one lane: 32 bf16 values in raw[0..16) -> codes in w (8 words E4M3, 4 e2m1);
+// returns the scale byte. The same rule as quantize32, on packed pairs.
+template <int FMT>
+__device__ __forceinline__ uint32_t mx_piece_bf16(const uint32_t* raw, uint32_t* w) {
+  constexpr uint32_t kEmax = (FMT == BSQ_MXFP8) ? 8u : 2u;
+  const uint32_t ef = __float_as_uint(bf16_block_amax<16>(raw)) >> 23;  // biased exponent of the block maximum
+  const uint32_t sbyte = ef > kEmax ? ef - kEmax : 0u;
+  const uint64_t m2 = f2_splat(__uint_as_float((254u - sbyte) << 23));  // 2^(127 - sbyte), exact
+  if constexpr (FMT == BSQ_MXFP8) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      float a, b, c, d;
+      f2_split(f2_mul(bf16x2_to_f2(raw[2 * j]), m2), a, b);
+      f2_split(f2_mul(bf16x2_to_f2(raw[2 * j + 1]), m2), c, d);
+      w[j] = cvt_e4m3x4(a, b, c, d);
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float y[8];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) f2_split(f2_mul(bf16x2_to_f2(raw[4 * j + i]), m2), y[2 * i], y[2 * i + 1]);
+      w[j] = cvt_e2m1x8(y);
+    }
+  }
+  return sbyte;
+}
+
+// NVFP4 blocks of one lane: 32 bf16 values in raw[0..16) -> codes in w[0..4), scale codes in bits
+// 0..7 and 8..15 of `sb`. Quotients by markstein_quotient's remainder step in packed form, with
+// the reciprocal negated: q0' = x (-r) = -q0, t = q0' d + x (the exact remainder x - q0 d), y =
+// t (-r) + q0' = -(q0 + t r), the negated IEEE quotient, whose code is the quotient's with the sign
+// flipped back by one XOR per eight codes. Working on -q keeps signed zeros exact without
+// negating x (x = +-0 gives -+0). Returns false when the step is not valid for some block (then
+// the caller takes the exact path).
+__device__ __forceinline__ bool nv_piece_bf16(const uint32_t* raw, const NvCtx& c, uint32_t* w, uint32_t& sb) {
+  bool quick = true;
+  sb = 0;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const uint32_t* wb = raw + 8 * h;
+    const float amax = bf16_block_amax<8>(wb);
+    quick = quick && __fmul_rn(amax, c.r6) < 0x1p100f;
+    const uint32_t scode = cvt_e4m3x2(markstein_quotient(amax, c.six_g, c.r6), 0.0f) & 0xFFu;
+    const float2 dr = c.tab[scode];
+    quick = quick && __fmul_rn(amax, dr.y) < 0x1p100f;
+    sb |= scode << (8 * h);
+    const uint64_t d2 = f2_splat(dr.x), nr2 = f2_splat(-dr.y);
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      float y[8];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint64_t x2 = bf16x2_to_f2(wb[4 * j + i]);
+        const uint64_t q0 = f2_mul(x2, nr2);
+        f2_split(f2_fma(f2_fma(q0, d2, x2), nr2, q0), y[2 * i], y[2 * i + 1]);
+      }
+      w[2 * h + j] = cvt_e2m1x8(y) ^ 0x88888888u;
+    }
+  }
+  return quick;
 }
 
 // Quantize the 32 elements of one lane: MX one block (scale byte returned in bits 0..7), NVFP4
 // two blocks (scale codes in bits 0..7 and 8..15). Codes go to w: 8 words (E4M3) or 4 (e2m1).
 template <int FMT>
-__device__ __forceinline__ uint32_t quantize32(const float (&x)[32], float g, float six_g, uint32_t* w) {
+__device__ __forceinline__ uint32_t quantize32(const float (&x)[32], const NvCtx& nv, uint32_t* w) {
   if constexpr (FMT == BSQ_NVFP4) {
-    const uint32_t s0 = nv_block16(x, abs_max<16>(x), g, six_g, w);
-    const uint32_t s1 = nv_block16(x + 16, abs_max<16>(x + 16), g, six_g, w + 2);
+    const uint32_t s0 = nv_block16(x, abs_max<16>(x), nv, w);
+    const uint32_t s1 = nv_block16(x + 16, abs_max<16>(x + 16), nv, w + 2);
     return s0 | (s1 << 8);
   } else {
     constexpr uint32_t kEmax = (FMT == BSQ_MXFP8) ? 8u : 2u;
@@ -183,12 +313,230 @@ __device__ __forceinline__ uint32_t quantize32(const float (&x)[32], float g, fl
   }
 }
 
-template <int FMT, bool F32, int NV, bool LN>
-__global__ void __launch_bounds__(QCfg<NV != kMx>::kThreads, QCfg<NV != kMx>::kCtasPerSm)
-    quantize_kernel(const __grid_constant__ QuantBatch batch) {
-  constexpr int kThreads = QCfg<NV != kMx>::kThreads;
-  constexpr int kRing = QCfg<NV != kMx>::kRing;
-  constexpr int kConsumerWarps = QCfg<NV != kMx>::kConsumerWarps;
+// ---------------------------------------------------------------------------- streaming kernel
+// Every matrix of the batch is one flat array of rows * cols elements; a warp step is 1024
+// consecutive elements of one matrix and a lane's piece 32 of them (one MX block, two NVFP4
+// blocks: a piece never crosses a row for MX, cols being a multiple of 32; an NVFP4 piece may
+// when cols % 32 == 16, and each block then finds its own row). Warps walk the concatenated step
+// list with a grid-wide stride, each lane loading its piece straight from global memory into
+// registers (two 32-byte loads for bf16, whole sectors) one step ahead of the piece it
+// quantizes: no shared-memory staging, no barriers, so nearly every instruction is the
+// element arithmetic. After the NVFP4 amax pass (which reads every source front to back) the
+// step list is walked back to front, to meet the lines still in L2.
+// Resident CTAs per SM: three for the MX formats from bf16 (up to 80 registers), two for NVFP4 and
+// fp32 sources (up to 128: NVFP4's exact fallback stays inline without spilling). Measured on
+// GB300 (51200 x 4096 bf16, L2 flushed): NVFP4 201.6 us with two against 203.7 us with three and
+// the fallback out of line; MXFP8 103.3 us with three against 115.8 with two and 110.8 with four.
+constexpr int kSThreads = 256;
+template <bool F32, bool NV>
+struct SCfg {
+  static constexpr int kCtasPerSm = (F32 || NV) ? 2 : 3;
+};
+constexpr int kSWarps = kSThreads / 32;
+
+// f / cols for f < 2^63: one 64-bit high multiply and at most one correction.
+__device__ __forceinline__ int64_t div_cols(int64_t f, int64_t cols, uint64_t magic) {
+  int64_t q = static_cast<int64_t>(__umul64hi(static_cast<uint64_t>(f), magic));
+  if (f - q * cols >= cols) ++q;
+  return q;
+}
+
+// Read-only 32-byte and 16-byte loads that do not allocate in L1 (each byte is read once).
+__device__ __forceinline__ void ld32(const uint8_t* p, uint32_t* r) {
+  asm volatile("ld.global.nc.L1::no_allocate.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "l"(p));
+}
+__device__ __forceinline__ void ld16(const uint8_t* p, uint32_t* r) {
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "l"(p));
+}
+
+// One lane's piece in flight: its matrix, element index and source words.
+template <bool F32>
+struct Piece {
+  static constexpr int kWords = F32 ? 32 : 16;
+  int t;         // matrix (-1: no step)
+  int64_t f;     // first element of the piece in the matrix
+  int live;      // elements present: 32, 16 (NVFP4: the matrix ends after the first block) or 0
+  uint32_t w[kWords];
+};
+
+// Locate global step `s` and load this lane's piece of it (zeros where the matrix has ended).
+template <bool F32>
+__device__ __forceinline__ void fetch(const QuantBatch& b, int64_t s, uint32_t lane, Piece<F32>& p) {
+  int t = 0;
+  while (t + 1 < b.n && s >= b.chunk_start[t + 1]) ++t;
+  const QuantArgs& a = b.t[t];
+  p.t = t;
+  p.f = (s - b.chunk_start[t]) * 1024 + 32 * static_cast<int64_t>(lane);
+  const int64_t left = a.elems - p.f;
+  p.live = left >= 32 ? 32 : (left >= 16 ? 16 : 0);
+  constexpr int kBytes = F32 ? 128 : 64;
+  const uint8_t* src = a.src + p.f * (F32 ? 4 : 2);
+#pragma unroll
+  for (int i = 0; i < Piece<F32>::kWords; ++i) p.w[i] = 0u;
+  if (p.live == 32) {
+    if ((reinterpret_cast<uintptr_t>(a.src) & 31u) == 0u) {
+#pragma unroll
+      for (int i = 0; i < kBytes / 32; ++i) ld32(src + 32 * i, p.w + 8 * i);
+    } else {
+#pragma unroll
+      for (int i = 0; i < kBytes / 16; ++i) ld16(src + 16 * i, p.w + 4 * i);
+    }
+  } else if (p.live == 16) {
+#pragma unroll
+    for (int i = 0; i < kBytes / 32; ++i) ld16(src + 16 * i, p.w + 4 * i);
+  }
+}
+
+template <int FMT, bool F32, int NV>
+__global__ void __launch_bounds__(kSThreads, SCfg<F32, NV != kMx>::kCtasPerSm)
+    stream_kernel(const __grid_constant__ QuantBatch batch) {
+  __shared__ float2 nv_tab[NV != kMx ? kSWarps : 1][128];  // NVFP4: each warp's divisor table
+  const uint32_t warp = threadIdx.x >> 5;
+  const uint32_t lane = threadIdx.x & 31u;
+  launch_dependents();
+  grid_dependency_wait();  // inputs and outputs may belong to the previous kernel until here
+
+  const int64_t nsteps = batch.chunk_start[batch.n];
+  const int64_t nw = static_cast<int64_t>(gridDim.x) * kSWarps;
+  auto step_of = [&](int64_t k) { return NV == kNvComputed ? nsteps - 1 - k : k; };
+  uint32_t run_max = 0;  // NVFP4 given-scale mode: running max |x| (fp32 bits) of matrix `cur`
+  int cur = -1;
+  NvCtx nv;
+  Piece<F32> pc[2];
+  int64_t k = static_cast<int64_t>(blockIdx.x) * kSWarps + warp;
+  if (k < nsteps) fetch<F32>(batch, step_of(k), lane, pc[0]);
+  // two piece buffers, alternating, so that the next step's loads are in flight while this one
+  // is quantized (the loop is unrolled by two to keep the buffers in registers)
+#pragma unroll 2
+  for (int it = 0; k < nsteps; k += nw, ++it) {
+    Piece<F32>& p = pc[it & 1];
+    if (k + nw < nsteps) fetch<F32>(batch, step_of(k + nw), lane, pc[(it + 1) & 1]);
+    const QuantArgs& a = batch.t[p.t];
+    if (p.t != cur) {  // warp-uniform: a step lies in one matrix
+      if constexpr (NV == kNvGiven) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) run_max = max(run_max, __shfl_xor_sync(0xFFFFFFFFu, run_max, o));
+        if (cur >= 0 && lane == 0 && run_max != 0) atomicMax(&batch.t[cur].tail[1], run_max);
+        run_max = 0;
+      }
+      cur = p.t;
+      if constexpr (NV != kMx) {
+        const float g = NV == kNvComputed ? __fdiv_rn(__uint_as_float(a.tail[1]), 2688.0f)  // amax / (6 * 448)
+                                         : *a.g_in;
+        nv = nv_context(g, nv_tab[NV != kMx ? warp : 0]);
+      }
+    }
+    if constexpr (NV != kMx) {
+      if (p.f == 0) {  // the matrix's first piece records g
+        a.tail[0] = __float_as_uint(nv.g);
+        if constexpr (NV == kNvComputed) {
+          if (a.g_out != nullptr) *a.g_out = nv.g;
+        }
+      }
+    }
+    if (p.live == 0) continue;
+    uint32_t w[FMT == BSQ_MXFP8 ? 8 : 4];
+    uint32_t sb;
+    // the piece's values as fp32 (exact path): fp32 sources, and NVFP4 blocks whose quotient step is
+    // not valid
+    auto exact = [&]() {
+      float x[32];
+      if constexpr (F32) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(p.w[i]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          x[2 * i] = __uint_as_float(p.w[i] << 16);
+          x[2 * i + 1] = __uint_as_float(p.w[i] & 0xFFFF0000u);
+        }
+      }
+      if constexpr (F32 && NV == kNvGiven) run_max = max(run_max, __float_as_uint(abs_max<32>(x)));
+      sb = quantize32<FMT>(x, nv, w);
+    };
+    if constexpr (F32) {
+      exact();
+    } else if constexpr (FMT == BSQ_NVFP4) {
+      if constexpr (NV == kNvGiven) run_max = max(run_max, __float_as_uint(bf16_block_amax<16>(p.w)));
+      if (!nv_piece_bf16(p.w, nv, w, sb)) exact();
+    } else {
+      sb = mx_piece_bf16<FMT>(p.w, w);
+    }
+    if constexpr (FMT == BSQ_MXFP8) {
+      uint4* dst = reinterpret_cast<uint4*>(a.codes + p.f);
+      dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+      dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    } else if constexpr (FMT == BSQ_MXFP4) {
+      *reinterpret_cast<uint4*>(a.codes + (p.f >> 1)) = make_uint4(w[0], w[1], w[2], w[3]);
+    } else {  // NVFP4 codes are 8-byte aligned only when cols % 32 == 16
+      uint2* dst = reinterpret_cast<uint2*>(a.codes + (p.f >> 1));
+      dst[0] = make_uint2(w[0], w[1]);
+      if (p.live == 32) dst[1] = make_uint2(w[2], w[3]);
+    }
+    // each block's scale byte at its place in the tiled layout (rows and columns below 2^31;
+    // the padding columns of the last 4-column group are zeroed after the loop)
+    const int64_t row64 = div_cols(p.f, a.cols, a.cols_magic64);
+    const uint32_t row = static_cast<uint32_t>(row64);
+    const uint32_t col = static_cast<uint32_t>(p.f - row64 * a.cols);
+    constexpr int kBlocks = FMT == BSQ_NVFP4 ? 2 : 1;
+#pragma unroll
+    for (int h = 0; h < kBlocks; ++h) {
+      if (h == 1 && p.live != 32) break;
+      uint32_t r = row, c = col + 16u * h;
+      if (FMT == BSQ_NVFP4 && c >= static_cast<uint32_t>(a.cols)) {  // cols % 32 == 16: the next row
+        c -= static_cast<uint32_t>(a.cols);
+        ++r;
+      }
+      const uint32_t sc = c >> (FMT == BSQ_NVFP4 ? 4 : 5);
+      const uint64_t tile = static_cast<uint64_t>(r >> 7) * static_cast<uint64_t>(a.nct) + (sc >> 2);
+      a.scales[tile * 512 + (((r & 31u) << 4) | (((r >> 5) & 3u) << 2) | (sc & 3u))] = static_cast<uint8_t>(sb >> (8 * h));
+    }
+  }
+  if constexpr (NV == kNvGiven) {
+    // the last matrix's share of |x| maxima -> its tail word 1
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) run_max = max(run_max, __shfl_xor_sync(0xFFFFFFFFu, run_max, o));
+    if (cur >= 0 && lane == 0 && run_max != 0) atomicMax(&batch.t[cur].tail[1], run_max);
+  }
+  // padding of the tiled scales reads 0: every word of the padding rows of each matrix's last row
+  // tile, and the bytes past the last scale column in each row's last 4-column group (byte
+  // stores: the row's real scale bytes in the same word are written by other lanes)
+  const int64_t tid = static_cast<int64_t>(blockIdx.x) * kSThreads + threadIdx.x;
+  const int64_t nthr = static_cast<int64_t>(gridDim.x) * kSThreads;
+  for (int m = 0; m < batch.n; ++m) {
+    const QuantArgs& a = batch.t[m];
+    const int64_t pad_rows = (128 - a.rows % 128) % 128;
+    const int64_t words = pad_rows * a.nct;
+    for (int64_t wd = tid; wd < words; wd += nthr) {
+      const int64_t r = a.rows + wd / a.nct, tc = wd % a.nct;
+      *reinterpret_cast<uint32_t*>(a.scales + scale_word_offset(r, 4 * tc, a.nct)) = 0u;
+    }
+    const int64_t pad_cols = 4 * a.nct - a.nsc;
+    for (int64_t i = tid; i < a.rows * pad_cols; i += nthr) {
+      const int64_t r = i / pad_cols, c = a.nsc + i % pad_cols;
+      a.scales[scale_word_offset(r, c, a.nct) + (c & 3)] = 0;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------- LayerNorm kernel
+// LayerNorm + MX quantization (MXFP8, MXFP4): the source is cut into chunks of whole rows (at
+// most 16 KB), each brought into shared memory by one 1-D TMA bulk copy; a producer thread keeps a
+// ring of kRing chunk buffers in flight and each consumer warp owns whole rows of a chunk, dealt
+// round-robin over the CTA's chunks: the row's mean and rstd (fp32, two passes over the row -- in
+// registers for rows of at most 1024 elements, else in shared memory -- with butterfly warp sums),
+// then y = (x - mean) * rstd * gamma + beta and the quantization of the row, 32 columns per lane,
+// with no barrier between the warps.
+template <int FMT, bool F32>
+__global__ void __launch_bounds__(QCfg::kThreads, QCfg::kCtasPerSm)
+    layernorm_kernel(const __grid_constant__ QuantBatch batch) {
+  constexpr int kThreads = QCfg::kThreads;
+  constexpr int kRing = QCfg::kRing;
+  constexpr int kConsumerWarps = QCfg::kConsumerWarps;
   constexpr int kEsize = F32 ? 4 : 2;
   extern __shared__ uint8_t q_smem_raw[];
   uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(q_smem_raw) + 127) & ~uintptr_t(127));
@@ -196,6 +544,7 @@ __global__ void __launch_bounds__(QCfg<NV != kMx>::kThreads, QCfg<NV != kMx>::kC
   __shared__ int abort_flag;
   const uint32_t warp = threadIdx.x >> 5;
   const uint32_t lane = threadIdx.x & 31u;
+  const QuantArgs& a = batch.t[0];
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kRing; ++i) {
@@ -209,29 +558,7 @@ __global__ void __launch_bounds__(QCfg<NV != kMx>::kThreads, QCfg<NV != kMx>::kC
   launch_dependents();
   grid_dependency_wait();  // inputs and outputs may belong to the previous kernel until here
 
-  const int64_t nchunks = batch.chunk_start[batch.n];
-  // global chunk c -> its matrix and local chunk index
-  auto chunk_owner = [&](int64_t c, int64_t& local) {
-    int t = 0;
-    while (t + 1 < batch.n && c >= batch.chunk_start[t + 1]) ++t;
-    local = c - batch.chunk_start[t];
-    return t;
-  };
-  // local chunk c of matrix a -> first row, rows, first column, columns
-  auto chunk_geom = [&](const QuantArgs& a, int64_t c, int64_t& r0, int64_t& nr, int64_t& c0, int64_t& nc) {
-    if (a.chunks_per_row > 1) {
-      r0 = c / a.chunks_per_row;
-      c0 = (c - r0 * a.chunks_per_row) * a.cspan;
-      nr = 1;
-      nc = min(a.cspan, a.cols - c0);
-    } else {
-      r0 = c * a.rows_per_chunk;
-      nr = min(a.rows_per_chunk, a.rows - r0);
-      c0 = 0;
-      nc = a.cols;
-    }
-  };
-
+  const int64_t nchunks = batch.chunk_start[1];
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
@@ -239,13 +566,11 @@ __global__ void __launch_bounds__(QCfg<NV != kMx>::kThreads, QCfg<NV != kMx>::kC
       uint32_t phase = 0;
       for (int64_t c = blockIdx.x; c < nchunks; c += gridDim.x) {
         if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1u, &abort_flag, batch.status)) break;
-        int64_t local;
-        const QuantArgs& a = batch.t[chunk_owner(c, local)];
-        int64_t r0, nr, c0, nc;
-        chunk_geom(a, local, r0, nr, c0, nc);
-        const uint32_t bytes = static_cast<uint32_t>(nr * nc * kEsize);
+        const int64_t r0 = c * a.rows_per_chunk;
+        const int64_t nr = min(a.rows_per_chunk, a.rows - r0);
+        const uint32_t bytes = static_cast<uint32_t>(nr * a.cols * kEsize);
         mbar_arrive_expect_tx(&full_bar[stage], bytes);
-        bulk_load(ring + stage * kChunkMax, a.src + (r0 * a.cols + c0) * kEsize, bytes, &full_bar[stage]);
+        bulk_load(ring + stage * kChunkMax, a.src + r0 * a.cols * kEsize, bytes, &full_bar[stage]);
         if (++stage == kRing) {
           stage = 0;
           phase ^= 1u;
@@ -254,259 +579,142 @@ __global__ void __launch_bounds__(QCfg<NV != kMx>::kThreads, QCfg<NV != kMx>::kC
     }
   } else {
     // ------------------------------------------------------------ consumers
-    uint32_t run_max = 0;  // NVFP4 given-scale mode: running max |x| (fp32 bits) of matrix `cur`
-    int cur = -1;          // matrix of the previous chunk
-    float g = 0.f, six_g = 0.f;
-    const int cw = static_cast<int>(warp) - 1;
-    // Warp steps are dealt round-robin over the concatenation of the CTA's chunks (not per
-    // chunk), so that a chunk whose step count is not a multiple of the warp count does not
-    // give the same warps an extra step every time. `lead`: this warp's first step in the
-    // current chunk.
-    uint32_t lead = static_cast<uint32_t>(cw);
+    const NvCtx nv;  // unused by the MX formats
+    // rows are dealt round-robin over the concatenation of the CTA's chunks, so that a chunk whose
+    // row count is not a multiple of the warp count does not give the same warps an extra row
+    // every time; `lead`: this warp's first row in the current chunk
+    uint32_t lead = warp - 1;
     int stage = 0;
     uint32_t phase = 0;
+    const int nci = static_cast<int>(a.cols);
+    const int pieces = nci * kEsize / 16;  // 16-byte pieces of a row
     for (int64_t c = blockIdx.x; c < nchunks; c += gridDim.x) {
       if (!mbar_wait_bounded_warp(&full_bar[stage], phase, &abort_flag, batch.status)) break;
-      int64_t local;
-      const int t = chunk_owner(c, local);
-      const QuantArgs& a = batch.t[t];
-      if (t != cur) {
-        if constexpr (NV == kNvGiven) {
-          // the previous matrix's share of |x| maxima -> its tail word 1
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) run_max = max(run_max, __shfl_xor_sync(0xFFFFFFFFu, run_max, o));
-          if (cur >= 0 && lane == 0 && run_max != 0) atomicMax(&batch.t[cur].tail[1], run_max);
-          run_max = 0;
-        }
-        cur = t;
-        if constexpr (NV != kMx) {
-          if constexpr (NV == kNvComputed) {
-            g = __fdiv_rn(__uint_as_float(a.tail[1]), 2688.0f);  // amax / (6 * 448)
-          } else {
-            g = *a.g_in;
-          }
-          six_g = __fmul_rn(6.0f, g);
-        }
-      }
-      if constexpr (NV != kMx) {
-        if (local == 0 && warp == 1 && lane == 0) {
-          a.tail[0] = __float_as_uint(g);
-          if constexpr (NV == kNvComputed) {
-            if (a.g_out != nullptr) *a.g_out = g;
-          }
-        }
-      }
-      int64_t r0, nr, c0, nc;
-      chunk_geom(a, local, r0, nr, c0, nc);
+      const int64_t r0 = c * a.rows_per_chunk;
+      const int64_t nr = min(a.rows_per_chunk, a.rows - r0);
       const uint8_t* buf = ring + stage * kChunkMax;
-      // the chunk as one flat array of nr * nc elements; lane piece f = 32 elements
-      const uint32_t flat = static_cast<uint32_t>(nr * nc);
-      const uint64_t elem0 = static_cast<uint64_t>(r0) * static_cast<uint64_t>(a.cols) + static_cast<uint64_t>(c0);
-      const uint32_t steps = (flat + kSeg - 1) / kSeg;
-      if constexpr (LN) {
-        // LayerNorm mode (whole rows, MX formats): each warp owns whole rows of the chunk, dealt
-        // round-robin over the CTA's chunks like the warp steps below (`lead` is this warp's first
-        // row here): the row's mean and rstd (fp32, two passes over the row -- in registers for
-        // rows of at most 1024 elements, else in shared memory -- with butterfly warp sums), then
-        // y = (x - mean) * rstd * gamma + beta and the quantization of the row, 32 columns per
-        // lane -- no barrier between the warps
-        const int nci = static_cast<int>(nc);
-        const int pieces = nci * kEsize / 16;  // 16-byte pieces of a row
-        for (uint32_t rr = lead; rr < static_cast<uint32_t>(nr); rr += kConsumerWarps) {
-          const uint8_t* rowp = buf + static_cast<size_t>(rr) * nci * kEsize;
-          auto piece_sum = [&](float mean, bool sq) {
-            float acc_s = 0.0f;
-            for (int q = static_cast<int>(lane); q < pieces; q += 32) {
-              const uint4 v = reinterpret_cast<const uint4*>(rowp)[q];
-              const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      for (uint32_t rr = lead; rr < static_cast<uint32_t>(nr); rr += kConsumerWarps) {
+        const uint8_t* rowp = buf + static_cast<size_t>(rr) * nci * kEsize;
+        auto piece_sum = [&](float mean, bool sq) {
+          float acc_s = 0.0f;
+          for (int q = static_cast<int>(lane); q < pieces; q += 32) {
+            const uint4 v = reinterpret_cast<const uint4*>(rowp)[q];
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                if constexpr (F32) {
-                  const float d = __uint_as_float(w[i]) - mean;
-                  acc_s += sq ? d * d : d;
-                } else {
-                  const float d0 = __uint_as_float(w[i] << 16) - mean, d1 = __uint_as_float(w[i] & 0xFFFF0000u) - mean;
-                  acc_s += sq ? d0 * d0 + d1 * d1 : d0 + d1;
-                }
+            for (int i = 0; i < 4; ++i) {
+              if constexpr (F32) {
+                const float d = __uint_as_float(w[i]) - mean;
+                acc_s += sq ? d * d : d;
+              } else {
+                const float d0 = __uint_as_float(w[i] << 16) - mean, d1 = __uint_as_float(w[i] & 0xFFFF0000u) - mean;
+                acc_s += sq ? d0 * d0 + d1 * d1 : d0 + d1;
               }
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) acc_s += __shfl_xor_sync(0xFFFFFFFFu, acc_s, o);
-            return acc_s;
-          };
-          const uint32_t row = static_cast<uint32_t>(r0) + rr;
-          // y = (x - mean) * rstd * gamma + beta for the 32 elements at column cc (x holds the
-          // source values), then their MX block: codes and scale byte
-          auto finish = [&](int cc, float (&x)[32], float mean, float rstd) {
-            const uint4* gp = reinterpret_cast<const uint4*>(a.gamma + cc);
-            const uint4* bp = reinterpret_cast<const uint4*>(a.beta + cc);
-#pragma unroll
-            for (int h = 0; h < 4; ++h) {
-              const uint4 gv = __ldg(gp + h), bv = __ldg(bp + h);
-              const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w}, bw[4] = {bv.x, bv.y, bv.z, bv.w};
-#pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                float& y0 = x[8 * h + 2 * i];
-                float& y1 = x[8 * h + 2 * i + 1];
-                y0 = __fadd_rn(__fmul_rn(__fmul_rn(y0 - mean, rstd), __uint_as_float(gw[i] << 16)),
-                               __uint_as_float(bw[i] << 16));
-                y1 = __fadd_rn(__fmul_rn(__fmul_rn(y1 - mean, rstd), __uint_as_float(gw[i] & 0xFFFF0000u)),
-                               __uint_as_float(bw[i] & 0xFFFF0000u));
-              }
-            }
-            const uint64_t e = static_cast<uint64_t>(row) * static_cast<uint64_t>(a.cols) + static_cast<uint64_t>(cc);
-            uint32_t w[FMT == BSQ_MXFP8 ? 8 : 4];
-            const uint32_t sb = quantize32<FMT>(x, g, six_g, w);
-            if constexpr (FMT == BSQ_MXFP8) {
-              uint4* dst = reinterpret_cast<uint4*>(a.codes + e);
-              dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-              dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-            } else {
-              *reinterpret_cast<uint4*>(a.codes + (e >> 1)) = make_uint4(w[0], w[1], w[2], w[3]);
-            }
-            const uint32_t sc = static_cast<uint32_t>(cc) >> 5;
-            uint8_t* sp = a.scales + static_cast<uint64_t>((row >> 7) * static_cast<uint32_t>(a.nct) + (sc >> 2)) * 512 +
-                          (((row & 31u) << 4) | (((row >> 5) & 3u) << 2) | (sc & 3u));
-            *sp = static_cast<uint8_t>(sb);
-            if (sc + 1 == static_cast<uint32_t>(a.nsc)) {
-              for (uint32_t j = (sc & 3u) + 1; j < 4; ++j) sp[j - (sc & 3u)] = 0;
-            }
-          };
-          if (nci <= 32 * kLaneElems) {
-            // rows of at most 1024 elements: each lane reads its 32 elements from shared memory
-            // once and keeps them in registers for both statistics passes and the quantization
-            const int cc = static_cast<int>(lane) * kLaneElems;
-            const bool act = cc < nci;
-            float x[32];
-            if (act) {
-              load32<F32>(rowp + cc * kEsize, x);
-            } else {
-#pragma unroll
-              for (int i = 0; i < 32; ++i) x[i] = 0.0f;
-            }
-            float p4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-            for (int i = 0; i < 32; ++i) p4[i & 3] += x[i];
-            float acc_s = (p4[0] + p4[1]) + (p4[2] + p4[3]);
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) acc_s += __shfl_xor_sync(0xFFFFFFFFu, acc_s, o);
-            const float mean = __fdiv_rn(acc_s, static_cast<float>(nci));
-#pragma unroll
-            for (int i = 0; i < 4; ++i) p4[i] = 0.0f;
-            if (act) {
-#pragma unroll
-              for (int i = 0; i < 32; ++i) {
-                const float d = x[i] - mean;
-                p4[i & 3] += d * d;
-              }
-            }
-            acc_s = (p4[0] + p4[1]) + (p4[2] + p4[3]);
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) acc_s += __shfl_xor_sync(0xFFFFFFFFu, acc_s, o);
-            const float var = __fdiv_rn(acc_s, static_cast<float>(nci));
-            const float rstd = __fdiv_rn(1.0f, __fsqrt_rn(var + a.eps));
-            if (act) finish(cc, x, mean, rstd);
-          } else {
-            const float mean = __fdiv_rn(piece_sum(0.0f, false), static_cast<float>(nci));
-            const float var = __fdiv_rn(piece_sum(mean, true), static_cast<float>(nci));
-            const float rstd = __fdiv_rn(1.0f, __fsqrt_rn(var + a.eps));
-            for (int cc = static_cast<int>(lane) * kLaneElems; cc < nci; cc += 32 * kLaneElems) {
-              float x[32];
-              load32<F32>(rowp + cc * kEsize, x);
-              finish(cc, x, mean, rstd);
             }
           }
-        }
-        lead = (lead + (kConsumerWarps - static_cast<uint32_t>(nr) % kConsumerWarps)) % kConsumerWarps;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty_bar[stage]);
-        if (++stage == kRing) {
-          stage = 0;
-          phase ^= 1u;
-        }
-      } else {
-        for (uint32_t base = lead * kSeg; base < flat; base += kConsumerWarps * kSeg) {
-          const uint32_t f = base + lane * kLaneElems;
-          // MX chunks hold whole 32-element blocks; an NVFP4 chunk may end half-way through a
-          // lane's piece (rows of 16k elements): then only its first block is live
-          const bool live = f < flat;
-          const bool live_hi = f + 16 < flat;
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) acc_s += __shfl_xor_sync(0xFFFFFFFFu, acc_s, o);
+          return acc_s;
+        };
+        const uint32_t row = static_cast<uint32_t>(r0) + rr;
+        // y = (x - mean) * rstd * gamma + beta for the 32 elements at column cc (x holds the
+        // source values), then their MX block: codes and scale byte
+        auto finish = [&](int cc, float (&x)[32], float mean, float rstd) {
+          const uint4* gp = reinterpret_cast<const uint4*>(a.gamma + cc);
+          const uint4* bp = reinterpret_cast<const uint4*>(a.beta + cc);
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+            const uint4 gv = __ldg(gp + h), bv = __ldg(bp + h);
+            const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w}, bw[4] = {bv.x, bv.y, bv.z, bv.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              float& y0 = x[8 * h + 2 * i];
+              float& y1 = x[8 * h + 2 * i + 1];
+              y0 = __fadd_rn(__fmul_rn(__fmul_rn(y0 - mean, rstd), __uint_as_float(gw[i] << 16)),
+                             __uint_as_float(bw[i] << 16));
+              y1 = __fadd_rn(__fmul_rn(__fmul_rn(y1 - mean, rstd), __uint_as_float(gw[i] & 0xFFFF0000u)),
+                             __uint_as_float(bw[i] & 0xFFFF0000u));
+            }
+          }
+          const uint64_t e = static_cast<uint64_t>(row) * static_cast<uint64_t>(a.cols) + static_cast<uint64_t>(cc);
+          uint32_t w[FMT == BSQ_MXFP8 ? 8 : 4];
+          const uint32_t sb = quantize32<FMT>(x, nv, w);
+          if constexpr (FMT == BSQ_MXFP8) {
+            uint4* dst = reinterpret_cast<uint4*>(a.codes + e);
+            dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+            dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+          } else {
+            *reinterpret_cast<uint4*>(a.codes + (e >> 1)) = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+          const uint32_t sc = static_cast<uint32_t>(cc) >> 5;
+          uint8_t* sp = a.scales + static_cast<uint64_t>((row >> 7) * static_cast<uint32_t>(a.nct) + (sc >> 2)) * 512 +
+                        (((row & 31u) << 4) | (((row >> 5) & 3u) << 2) | (sc & 3u));
+          *sp = static_cast<uint8_t>(sb);
+          if (sc + 1 == static_cast<uint32_t>(a.nsc)) {
+            for (uint32_t j = (sc & 3u) + 1; j < 4; ++j) sp[j - (sc & 3u)] = 0;
+          }
+        };
+        if (nci <= 32 * kLaneElems) {
+          // rows of at most 1024 elements: each lane reads its 32 elements from shared memory
+          // once and keeps them in registers for both statistics passes and the quantization
+          const int cc = static_cast<int>(lane) * kLaneElems;
+          const bool act = cc < nci;
           float x[32];
-          if (live_hi) {
-            load32<F32>(buf + f * kEsize, x);
+          if (act) {
+            load32<F32>(rowp + cc * kEsize, x);
           } else {
-  #pragma unroll
+#pragma unroll
             for (int i = 0; i < 32; ++i) x[i] = 0.0f;
-            if (live) load32<F32, 16>(buf + f * kEsize, x);  // the first block only: nothing past the chunk is read
           }
-          if constexpr (NV == kNvGiven) run_max = max(run_max, __float_as_uint(abs_max<32>(x)));
-          if (live) {
-            const uint64_t e = elem0 + f;
-            uint32_t w[FMT == BSQ_MXFP8 ? 8 : 4];
-            const uint32_t sb = quantize32<FMT>(x, g, six_g, w);
-            if constexpr (FMT == BSQ_MXFP8) {
-              uint4* dst = reinterpret_cast<uint4*>(a.codes + e);
-              dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-              dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-            } else if constexpr (FMT == BSQ_MXFP4) {
-              *reinterpret_cast<uint4*>(a.codes + (e >> 1)) = make_uint4(w[0], w[1], w[2], w[3]);
-            } else {  // NVFP4 codes are only 8-byte aligned when rows are 16k elements long
-              uint2* dst = reinterpret_cast<uint2*>(a.codes + (e >> 1));
-              dst[0] = make_uint2(w[0], w[1]);
-              if (live_hi) dst[1] = make_uint2(w[2], w[3]);
-            }
-            // each block's scale byte at its place in the tiled layout (32-bit arithmetic: rows and
-            // columns stay below 2^31, the number of 512-byte scale tiles below 2^32)
-            constexpr int kBlocks = FMT == BSQ_NVFP4 ? 2 : 1;
-  #pragma unroll
-            for (int h = 0; h < kBlocks; ++h) {
-              if (h == 1 && !live_hi) break;
-              const uint32_t fh = f + 16u * h;
-              const uint32_t rr = nr > 1 ? __umulhi(fh, a.cols_magic) : 0u;
-              const uint32_t row = static_cast<uint32_t>(r0) + rr;
-              const uint32_t col = static_cast<uint32_t>(c0) + (fh - rr * static_cast<uint32_t>(nc));
-              const uint32_t sc = col >> (FMT == BSQ_NVFP4 ? 4 : 5);
-              const uint32_t tile = (row >> 7) * static_cast<uint32_t>(a.nct) + (sc >> 2);
-              uint8_t* sp = a.scales + static_cast<uint64_t>(tile) * 512 +
-                            (((row & 31u) << 4) | (((row >> 5) & 3u) << 2) | (sc & 3u));
-              *sp = static_cast<uint8_t>(sb >> (8 * h));
-              if (sc + 1 == static_cast<uint32_t>(a.nsc)) {
-                // padding columns of the row's last 4-column group read 0
-                for (uint32_t j = (sc & 3u) + 1; j < 4; ++j) sp[j - (sc & 3u)] = 0;
-              }
+          float p4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+          for (int i = 0; i < 32; ++i) p4[i & 3] += x[i];
+          float acc_s = (p4[0] + p4[1]) + (p4[2] + p4[3]);
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) acc_s += __shfl_xor_sync(0xFFFFFFFFu, acc_s, o);
+          const float mean = __fdiv_rn(acc_s, static_cast<float>(nci));
+#pragma unroll
+          for (int i = 0; i < 4; ++i) p4[i] = 0.0f;
+          if (act) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const float d = x[i] - mean;
+              p4[i & 3] += d * d;
             }
           }
-        }
-        // first step in the next chunk: continue the round-robin where this chunk ended
-        lead = (lead + (kConsumerWarps - steps % kConsumerWarps)) % kConsumerWarps;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty_bar[stage]);
-        if (++stage == kRing) {
-          stage = 0;
-          phase ^= 1u;
+          acc_s = (p4[0] + p4[1]) + (p4[2] + p4[3]);
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) acc_s += __shfl_xor_sync(0xFFFFFFFFu, acc_s, o);
+          const float var = __fdiv_rn(acc_s, static_cast<float>(nci));
+          const float rstd = __fdiv_rn(1.0f, __fsqrt_rn(var + a.eps));
+          if (act) finish(cc, x, mean, rstd);
+        } else {
+          const float mean = __fdiv_rn(piece_sum(0.0f, false), static_cast<float>(nci));
+          const float var = __fdiv_rn(piece_sum(mean, true), static_cast<float>(nci));
+          const float rstd = __fdiv_rn(1.0f, __fsqrt_rn(var + a.eps));
+          for (int cc = static_cast<int>(lane) * kLaneElems; cc < nci; cc += 32 * kLaneElems) {
+            float x[32];
+            load32<F32>(rowp + cc * kEsize, x);
+            finish(cc, x, mean, rstd);
+          }
         }
       }
-    }
-
-    if constexpr (NV == kNvGiven) {
-      // the last matrix's share of |x| maxima -> its tail word 1
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) run_max = max(run_max, __shfl_xor_sync(0xFFFFFFFFu, run_max, o));
-      if (cur >= 0 && lane == 0 && run_max != 0) atomicMax(&batch.t[cur].tail[1], run_max);
+      lead = (lead + (kConsumerWarps - static_cast<uint32_t>(nr) % kConsumerWarps)) % kConsumerWarps;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty_bar[stage]);
+      if (++stage == kRing) {
+        stage = 0;
+        phase ^= 1u;
+      }
     }
   }
 
-  // scale bytes of the padding rows of each matrix's last row tile read 0
-  for (int m = 0; m < batch.n; ++m) {
-    const QuantArgs& a = batch.t[m];
-    const int64_t pad_rows = (128 - a.rows % 128) % 128;
-    if (pad_rows == 0) continue;
-    const int64_t words = pad_rows * a.nct;
-    for (int64_t w = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; w < words;
-         w += static_cast<int64_t>(gridDim.x) * kThreads) {
-      const int64_t r = a.rows + w / a.nct, tc = w % a.nct;
-      *reinterpret_cast<uint32_t*>(a.scales + scale_word_offset(r, 4 * tc, a.nct)) = 0u;
-    }
+  // scale bytes of the padding rows of the last row tile read 0
+  const int64_t pad_rows = (128 - a.rows % 128) % 128;
+  const int64_t words = pad_rows * a.nct;
+  for (int64_t w = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; w < words;
+       w += static_cast<int64_t>(gridDim.x) * kThreads) {
+    const int64_t r = a.rows + w / a.nct, tc = w % a.nct;
+    *reinterpret_cast<uint32_t*>(a.scales + scale_word_offset(r, 4 * tc, a.nct)) = 0u;
   }
 }
 
@@ -552,28 +760,41 @@ __global__ void __launch_bounds__(kAmaxThreads) amax_kernel(const uint4* src, in
   }
 }
 
-template <int FMT, bool F32, int NV, bool LN = false>
-cudaError_t launch_q(const QuantBatch& b, int grid, cudaStream_t stream, int device) {
-  using Q = QCfg<NV != kMx>;
-  static PerDevice<cudaError_t> setup;  // the shared-memory opt-in holds per device
-  const cudaError_t attr = setup.run(device, [] {
-    return cudaFuncSetAttribute(quantize_kernel<FMT, F32, NV, LN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                Q::kSmem);
-  });
-  if (attr != cudaSuccess) return attr;
-  // programmatic dependent launch: the kernel may be launched while the previous kernel in
-  // the stream finishes; it waits for it (grid_dependency_wait) before touching memory
+// Programmatic dependent launch for every kernel here: the kernel may be launched while the
+// previous kernel in the stream finishes; it waits for it (grid_dependency_wait) before touching
+// memory.
+template <typename... Args>
+cudaError_t launch_pdl(void (*kernel)(Args...), int grid, int threads, int smem, cudaStream_t stream,
+                       const Args&... args) {
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   at[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(Q::kThreads);
-  cfg.dynamicSmemBytes = Q::kSmem;
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, quantize_kernel<FMT, F32, NV, LN>, b);
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+template <int FMT, bool F32, int NV>
+cudaError_t launch_stream(const QuantBatch& b, int num_sms, cudaStream_t stream) {
+  const int64_t ctas = ceil_div(b.chunk_start[b.n], kSWarps);
+  const int grid =
+      static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(ctas, SCfg<F32, NV != kMx>::kCtasPerSm * num_sms)));
+  return launch_pdl(stream_kernel<FMT, F32, NV>, grid, kSThreads, 0, stream, b);
+}
+
+template <int FMT, bool F32>
+cudaError_t launch_ln(const QuantBatch& b, int grid, cudaStream_t stream, int device) {
+  static PerDevice<cudaError_t> setup;  // the shared-memory opt-in holds per device
+  const cudaError_t attr = setup.run(device, [] {
+    return cudaFuncSetAttribute(layernorm_kernel<FMT, F32>, cudaFuncAttributeMaxDynamicSharedMemorySize, QCfg::kSmem);
+  });
+  if (attr != cudaSuccess) return attr;
+  return launch_pdl(layernorm_kernel<FMT, F32>, grid, QCfg::kThreads, QCfg::kSmem, stream, b);
 }
 
 }  // namespace
@@ -614,47 +835,22 @@ int launch_amax(const void* src, bool src_f32, int64_t elems, uint32_t* out, cud
   return cudaGetLastError() == cudaSuccess ? BSQ_OK : BSQ_ERR_LAUNCH;
 }
 
-// The batch's chunking (chunk size, per-matrix chunk counts) and per-matrix arguments.
-void build_batch(QuantBatch& b, int fmt, bool src_f32, int count, const QuantItem* items, const DeviceInfo& dev) {
-  const int64_t esize = src_f32 ? 4 : 2;
-  b.n = count;
-  b.status = dev.status;
-  // Chunk size: at most one ring buffer, and small enough that every SM gets a few chunks
-  // (a 5 MB matrix is then still spread over all SMs and copied in parallel).
-  int64_t total_bytes = 0;
-  for (int i = 0; i < count; ++i) total_bytes += items[i].rows * items[i].cols * esize;
-  const int64_t target = std::max<int64_t>(
-      kChunkMin, std::min<int64_t>(kChunkMax, total_bytes / (4 * ctas_per_sm(fmt) * static_cast<int64_t>(dev.num_sms))));
-  b.chunk_start[0] = 0;
-  for (int i = 0; i < count; ++i) {
-    const QuantItem& it = items[i];
-    QuantArgs& a = b.t[i];
-    a.src = static_cast<const uint8_t*>(it.src);
-    a.rows = it.rows;
-    a.cols = it.cols;
-    a.codes = static_cast<uint8_t*>(it.codes);
-    a.scales = static_cast<uint8_t*>(it.scales);
-    a.nsc = it.cols / block_size(fmt);
-    a.nct = ceil_div(a.nsc, 4);
-    a.cols_magic = static_cast<uint32_t>((uint64_t{1} << 32) / static_cast<uint64_t>(it.cols) + 1);
-    const int64_t row_bytes = it.cols * esize;
-    if (row_bytes <= target) {
-      a.rows_per_chunk = target / row_bytes;
-      a.cspan = it.cols;
-      a.chunks_per_row = 1;
-      a.nchunks = ceil_div(it.rows, a.rows_per_chunk);
-    } else {
-      a.rows_per_chunk = 1;
-      a.cspan = std::max<int64_t>(1, kChunkMax / (esize * kSeg)) * kSeg;  // whole segments per piece
-      a.chunks_per_row = ceil_div(it.cols, a.cspan);
-      a.nchunks = it.rows * a.chunks_per_row;
-    }
-    b.chunk_start[i + 1] = b.chunk_start[i] + a.nchunks;
-    if (fmt == BSQ_NVFP4) {
-      a.tail = reinterpret_cast<uint32_t*>(a.scales + scales_body_bytes(fmt, it.rows, it.cols));
-      a.g_in = it.global_scale;
-      a.g_out = it.global_scale;
-    }
+// Per-matrix arguments of a batch.
+void fill_args(QuantArgs& a, int fmt, const QuantItem& it) {
+  a.src = static_cast<const uint8_t*>(it.src);
+  a.rows = it.rows;
+  a.cols = it.cols;
+  a.elems = it.rows * it.cols;
+  a.codes = static_cast<uint8_t*>(it.codes);
+  a.scales = static_cast<uint8_t*>(it.scales);
+  a.nsc = it.cols / block_size(fmt);
+  a.nct = ceil_div(a.nsc, 4);
+  a.cols_magic = static_cast<uint32_t>((uint64_t{1} << 32) / static_cast<uint64_t>(it.cols) + 1);
+  a.cols_magic64 = ~uint64_t{0} / static_cast<uint64_t>(it.cols);
+  if (fmt == BSQ_NVFP4) {
+    a.tail = reinterpret_cast<uint32_t*>(a.scales + scales_body_bytes(fmt, it.rows, it.cols));
+    a.g_in = it.global_scale;
+    a.g_out = it.global_scale;
   }
 }
 
@@ -662,48 +858,64 @@ int launch_quantize_batch(int fmt, bool src_f32, bool global_given, int count, c
                           cudaStream_t stream, const DeviceInfo& dev) {
   if (count < 1 || count > kMaxBatch) return BSQ_ERR_ARG;
   QuantBatch b{};
-  build_batch(b, fmt, src_f32, count, items, dev);
-  const int grid =
-      static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(b.chunk_start[count], ctas_per_sm(fmt) * dev.num_sms)));
+  b.n = count;
+  b.status = dev.status;
+  b.chunk_start[0] = 0;
+  for (int i = 0; i < count; ++i) {  // warp steps of 1024 elements, concatenated
+    fill_args(b.t[i], fmt, items[i]);
+    b.chunk_start[i + 1] = b.chunk_start[i] + ceil_div(b.t[i].elems, 32 * kLaneElems);
+  }
 
   cudaError_t err = cudaSuccess;
   if (fmt == BSQ_NVFP4) {
     for (int i = 0; i < count; ++i) {
       const QuantArgs& a = b.t[i];
       if (cudaMemsetAsync(a.tail, 0, 16, stream) != cudaSuccess) return BSQ_ERR_LAUNCH;
-      if (!global_given && launch_amax(a.src, src_f32, a.rows * a.cols, a.tail + 1, stream, dev) != BSQ_OK)
+      if (!global_given && launch_amax(a.src, src_f32, a.elems, a.tail + 1, stream, dev) != BSQ_OK)
         return BSQ_ERR_LAUNCH;
     }
     if (!global_given) {
-      err = src_f32 ? launch_q<BSQ_NVFP4, true, kNvComputed>(b, grid, stream, dev.device)
-                    : launch_q<BSQ_NVFP4, false, kNvComputed>(b, grid, stream, dev.device);
+      err = src_f32 ? launch_stream<BSQ_NVFP4, true, kNvComputed>(b, dev.num_sms, stream)
+                    : launch_stream<BSQ_NVFP4, false, kNvComputed>(b, dev.num_sms, stream);
     } else {
-      err = src_f32 ? launch_q<BSQ_NVFP4, true, kNvGiven>(b, grid, stream, dev.device)
-                    : launch_q<BSQ_NVFP4, false, kNvGiven>(b, grid, stream, dev.device);
+      err = src_f32 ? launch_stream<BSQ_NVFP4, true, kNvGiven>(b, dev.num_sms, stream)
+                    : launch_stream<BSQ_NVFP4, false, kNvGiven>(b, dev.num_sms, stream);
     }
   } else if (fmt == BSQ_MXFP8) {
-    err = src_f32 ? launch_q<BSQ_MXFP8, true, kMx>(b, grid, stream, dev.device) : launch_q<BSQ_MXFP8, false, kMx>(b, grid, stream, dev.device);
+    err = src_f32 ? launch_stream<BSQ_MXFP8, true, kMx>(b, dev.num_sms, stream)
+                  : launch_stream<BSQ_MXFP8, false, kMx>(b, dev.num_sms, stream);
   } else {
-    err = src_f32 ? launch_q<BSQ_MXFP4, true, kMx>(b, grid, stream, dev.device) : launch_q<BSQ_MXFP4, false, kMx>(b, grid, stream, dev.device);
+    err = src_f32 ? launch_stream<BSQ_MXFP4, true, kMx>(b, dev.num_sms, stream)
+                  : launch_stream<BSQ_MXFP4, false, kMx>(b, dev.num_sms, stream);
   }
   return err == cudaSuccess ? BSQ_OK : BSQ_ERR_LAUNCH;
 }
 
 int launch_layernorm_quantize(int fmt, bool src_f32, const QuantItem& item, const uint16_t* gamma,
                               const uint16_t* beta, float eps, cudaStream_t stream, const DeviceInfo& dev) {
+  const int64_t esize = src_f32 ? 4 : 2;
+  const int64_t row_bytes = item.cols * esize;
+  if (row_bytes > kChunkMax) return BSQ_ERR_SHAPE;  // whole rows only
   QuantBatch b{};
-  build_batch(b, fmt, src_f32, 1, &item, dev);
-  if (b.t[0].chunks_per_row != 1 || b.t[0].rows_per_chunk > kLnMaxRows) return BSQ_ERR_SHAPE;  // whole rows only
-  b.t[0].gamma = gamma;
-  b.t[0].beta = beta;
-  b.t[0].eps = eps;
-  const int grid =
-      static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(b.chunk_start[1], ctas_per_sm(fmt) * dev.num_sms)));
+  b.n = 1;
+  b.status = dev.status;
+  QuantArgs& a = b.t[0];
+  fill_args(a, fmt, item);
+  // chunks of whole rows: at most one ring buffer, and small enough that every SM gets a few
+  const int64_t target = std::max<int64_t>(
+      kChunkMin, std::min<int64_t>(kChunkMax, a.elems * esize / (4 * QCfg::kCtasPerSm * static_cast<int64_t>(dev.num_sms))));
+  a.rows_per_chunk = std::max<int64_t>(1, std::min<int64_t>(target / row_bytes, kLnMaxRows));
+  b.chunk_start[0] = 0;
+  b.chunk_start[1] = ceil_div(a.rows, a.rows_per_chunk);
+  a.gamma = gamma;
+  a.beta = beta;
+  a.eps = eps;
+  const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(b.chunk_start[1], QCfg::kCtasPerSm * dev.num_sms)));
   cudaError_t err;
   if (fmt == BSQ_MXFP8) {
-    err = src_f32 ? launch_q<BSQ_MXFP8, true, kMx, true>(b, grid, stream, dev.device) : launch_q<BSQ_MXFP8, false, kMx, true>(b, grid, stream, dev.device);
+    err = src_f32 ? launch_ln<BSQ_MXFP8, true>(b, grid, stream, dev.device) : launch_ln<BSQ_MXFP8, false>(b, grid, stream, dev.device);
   } else {
-    err = src_f32 ? launch_q<BSQ_MXFP4, true, kMx, true>(b, grid, stream, dev.device) : launch_q<BSQ_MXFP4, false, kMx, true>(b, grid, stream, dev.device);
+    err = src_f32 ? launch_ln<BSQ_MXFP4, true>(b, grid, stream, dev.device) : launch_ln<BSQ_MXFP4, false>(b, grid, stream, dev.device);
   }
   return err == cudaSuccess ? BSQ_OK : BSQ_ERR_LAUNCH;
 }

@@ -85,3 +85,91 @@ def test_dual_codes_near_decision_points(s, g, stochastic):
         assert np.array_equal(codes, w.codes), "%s: %d of %d code bytes differ (first at %d)" % (
             name, int((codes != w.codes).sum()), codes.size, int(np.argmax(codes != w.codes)))
         assert np.array_equal(q.scales.cpu().numpy(), w.tiled_scales()), name
+
+
+def _all_scales_matrix(g, seed):
+    """fp32 blocks for every nonzero E4M3 scale code s: element 0 of each 16-element block is
+    fp32(6 fp32(s g)) (the block's scale is then s), the other 15 carry the quotient targets of
+    _targets() times fp32(s g), all targets dealt over the blocks of each s. Rows of 64."""
+    t = _targets()
+    per = -(-len(t) // 15)  # blocks per scale code
+    blocks = []
+    rng = np.random.default_rng(seed)
+    for code in range(1, 127):
+        s = oracle.decode_e4m3(code)
+        d = np.float32(np.float32(s) * np.float32(g))
+        tt = np.resize(t, per * 15).reshape(per, 15)
+        b = np.empty((per, 16), np.float32)
+        b[:, 0] = np.float32(np.float32(6.0) * d)
+        b[:, 1:] = (tt * d).astype(np.float32)
+        for row in b:
+            rng.shuffle(row[1:])
+        blocks.append(b)
+    x = np.concatenate(blocks)
+    pad = (-len(x)) % 4
+    if pad:
+        x = np.concatenate([x, np.zeros((pad, 16), np.float32)])
+    return x.reshape(-1, 64)
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_quantize_every_scale_code_near_decision_points(seed):
+    """For ten per-tensor scales g spread log-uniformly over 2^-40 .. 2^40 (so that d = fp32(s g)
+    takes 1260 different significands), every one of the 126 nonzero block scales s with element
+    quotients on and within three ulps of each e2m1 decision point: codes and scales bit-exact
+    against the oracle's IEEE division."""
+    bsq = _bsq()
+    rng = np.random.default_rng(100 + seed)
+    for g in np.exp2(rng.uniform(-40, 40, size=10)).astype(np.float32):
+        g = float(g)
+        x = _all_scales_matrix(g, seed)
+        want = oracle.quantize("nvfp4", x, global_scale=g)
+        got = bsq.quantize("nvfp4", to_dev(x), global_scale=torch.tensor([g], dtype=torch.float32, device="cuda"))
+        assert bsq.device_status() == 0
+        codes = got.codes.cpu().numpy()
+        assert np.array_equal(codes, want.codes), "g=%r: %d of %d code bytes differ (first at %d)" % (
+            g, int((codes != want.codes).sum()), codes.size, int(np.argmax(codes != want.codes)))
+        assert np.array_equal(got.scales.cpu().numpy(), want.tiled_scales()), "g=%r scales" % g
+
+
+@pytest.mark.parametrize("seed", range(2))
+def test_quantize_bf16_every_value_every_scale_code(seed):
+    """bf16 sources: for three per-tensor scales and every nonzero block scale s, blocks holding
+    every bf16 value whose quotient x / fp32(s g) lies in [1/8, 8) (both signs), with an element
+    6 s g fixing the scale: the whole range where e2m1 codes are decided, bit-exact."""
+    from workloads import f32_to_bf16_bits
+
+    bsq = _bsq()
+    rng = np.random.default_rng(200 + seed)
+    allbf = (np.arange(0x8000, dtype=np.uint32) << 16).view(np.float32)  # every non-negative bf16
+    allbf = allbf[np.isfinite(allbf)]
+    for g in np.exp2(rng.uniform(-20, 20, size=3)).astype(np.float32):
+        g = float(g)
+        blocks = []
+        for code in range(1, 127):
+            s = oracle.decode_e4m3(code)
+            d = np.float32(np.float32(s) * np.float32(g))
+            amax_bf = f32_to_bf16_bits(np.array([np.float32(6.0) * d], np.float32))
+            amax = (amax_bf.astype(np.uint32) << 16).view(np.float32)[0]
+            q = allbf / d
+            v = allbf[(q >= 0.125) & (q < 8.0) & (allbf <= amax)]
+            v = np.concatenate([v, -v])
+            rng.shuffle(v)
+            n = -(-len(v) // 15) * 15
+            v = np.resize(v, n).reshape(-1, 15)
+            b = np.empty((len(v), 16), np.float32)
+            b[:, 0] = amax
+            b[:, 1:] = v
+            blocks.append(b)
+        x = np.concatenate(blocks)
+        pad = (-len(x)) % 4
+        if pad:
+            x = np.concatenate([x, np.zeros((pad, 16), np.float32)])
+        xb = f32_to_bf16_bits(x.reshape(-1, 64))  # exact: every value is a bf16 value
+        want = oracle.quantize("nvfp4", xb, global_scale=g)
+        got = bsq.quantize("nvfp4", to_dev(xb), global_scale=torch.tensor([g], dtype=torch.float32, device="cuda"))
+        assert bsq.device_status() == 0
+        codes = got.codes.cpu().numpy()
+        assert np.array_equal(codes, want.codes), "g=%r: %d of %d code bytes differ" % (
+            g, int((codes != want.codes).sum()), codes.size)
+        assert np.array_equal(got.scales.cpu().numpy(), want.tiled_scales()), "g=%r scales" % g
