@@ -357,38 +357,43 @@ __device__ __forceinline__ void ld16(const uint8_t* p, uint32_t* r) {
 template <bool F32>
 struct Piece {
   static constexpr int kWords = F32 ? 32 : 16;
-  int t;         // matrix (-1: no step)
-  int64_t f;     // first element of the piece in the matrix
-  int live;      // elements present: 32, 16 (NVFP4: the matrix ends after the first block) or 0
+  int t;      // matrix
+  int64_t f;  // first element of the piece in the matrix
+  int live;   // elements present: 32, 16 (NVFP4: the matrix ends after the first block) or 0
   uint32_t w[kWords];
 };
 
-// Locate global step `s` and load this lane's piece of it (zeros where the matrix has ended).
-template <bool F32>
-__device__ __forceinline__ void fetch(const QuantBatch& b, int64_t s, uint32_t lane, Piece<F32>& p) {
+// The fields of one batch matrix a warp works with, held in registers while its steps last
+// (the batch itself lives in the constant bank, where a dynamically indexed read costs an
+// address computation and a load every time).
+struct Mat {
+  int t = -1;
+  int64_t s0 = 0, s1 = 0;  // its warp steps [s0, s1) in the concatenated list
+  const uint8_t* src;
+  uint8_t* codes;
+  uint8_t* scales;
+  int64_t elems, cols, nct;
+  uint64_t magic;
+  bool aligned32;
+};
+
+__device__ __forceinline__ Mat find_mat(const QuantBatch& b, int64_t s) {
   int t = 0;
   while (t + 1 < b.n && s >= b.chunk_start[t + 1]) ++t;
   const QuantArgs& a = b.t[t];
-  p.t = t;
-  p.f = (s - b.chunk_start[t]) * 1024 + 32 * static_cast<int64_t>(lane);
-  const int64_t left = a.elems - p.f;
-  p.live = left >= 32 ? 32 : (left >= 16 ? 16 : 0);
-  constexpr int kBytes = F32 ? 128 : 64;
-  const uint8_t* src = a.src + p.f * (F32 ? 4 : 2);
-#pragma unroll
-  for (int i = 0; i < Piece<F32>::kWords; ++i) p.w[i] = 0u;
-  if (p.live == 32) {
-    if ((reinterpret_cast<uintptr_t>(a.src) & 31u) == 0u) {
-#pragma unroll
-      for (int i = 0; i < kBytes / 32; ++i) ld32(src + 32 * i, p.w + 8 * i);
-    } else {
-#pragma unroll
-      for (int i = 0; i < kBytes / 16; ++i) ld16(src + 16 * i, p.w + 4 * i);
-    }
-  } else if (p.live == 16) {
-#pragma unroll
-    for (int i = 0; i < kBytes / 32; ++i) ld16(src + 16 * i, p.w + 4 * i);
-  }
+  Mat m;
+  m.t = t;
+  m.s0 = b.chunk_start[t];
+  m.s1 = b.chunk_start[t + 1];
+  m.src = a.src;
+  m.codes = a.codes;
+  m.scales = a.scales;
+  m.elems = a.elems;
+  m.cols = a.cols;
+  m.nct = a.nct;
+  m.magic = a.cols_magic64;
+  m.aligned32 = (reinterpret_cast<uintptr_t>(a.src) & 31u) == 0u;
+  return m;
 }
 
 template <int FMT, bool F32, int NV>
@@ -403,28 +408,50 @@ __global__ void __launch_bounds__(kSThreads, SCfg<F32, NV != kMx>::kCtasPerSm)
   const int64_t nsteps = batch.chunk_start[batch.n];
   const int64_t nw = static_cast<int64_t>(gridDim.x) * kSWarps;
   auto step_of = [&](int64_t k) { return NV == kNvComputed ? nsteps - 1 - k : k; };
-  uint32_t run_max = 0;  // NVFP4 given-scale mode: running max |x| (fp32 bits) of matrix `cur`
-  int cur = -1;
+  uint32_t run_max = 0;  // NVFP4 given-scale mode: running max |x| (fp32 bits) of matrix mp
   NvCtx nv;
-  Piece<F32> pc[2];
-  int64_t k = static_cast<int64_t>(blockIdx.x) * kSWarps + warp;
-  if (k < nsteps) fetch<F32>(batch, step_of(k), lane, pc[0]);
-  // two piece buffers, alternating, so that the next step's loads are in flight while this one
-  // is quantized (the loop is unrolled by two to keep the buffers in registers)
-#pragma unroll 2
-  for (int it = 0; k < nsteps; k += nw, ++it) {
-    Piece<F32>& p = pc[it & 1];
-    if (k + nw < nsteps) fetch<F32>(batch, step_of(k + nw), lane, pc[(it + 1) & 1]);
-    const QuantArgs& a = batch.t[p.t];
-    if (p.t != cur) {  // warp-uniform: a step lies in one matrix
+  Mat mf, mp;  // the matrix of the step being fetched, and of the step being quantized
+  constexpr int kBytes = F32 ? 128 : 64;
+
+  // load this lane's piece of global step s (zeros where the matrix has ended)
+  auto fetch = [&](Piece<F32>& p, int64_t s) {
+    if (s < mf.s0 || s >= mf.s1) mf = find_mat(batch, s);  // warp-uniform
+    p.t = mf.t;
+    p.f = (s - mf.s0) * 1024 + 32 * static_cast<int64_t>(lane);
+    const int64_t left = mf.elems - p.f;
+    const uint8_t* src = mf.src + p.f * (F32 ? 4 : 2);
+    if (left >= 32) {
+      p.live = 32;
+      if (mf.aligned32) {
+#pragma unroll
+        for (int i = 0; i < kBytes / 32; ++i) ld32(src + 32 * i, p.w + 8 * i);
+      } else {
+#pragma unroll
+        for (int i = 0; i < kBytes / 16; ++i) ld16(src + 16 * i, p.w + 4 * i);
+      }
+    } else {
+      p.live = left >= 16 ? 16 : 0;
+#pragma unroll
+      for (int i = 0; i < Piece<F32>::kWords; ++i) p.w[i] = 0u;
+      if (p.live == 16) {
+#pragma unroll
+        for (int i = 0; i < kBytes / 32; ++i) ld16(src + 16 * i, p.w + 4 * i);
+      }
+    }
+  };
+
+  // quantize one fetched piece
+  auto process = [&](Piece<F32>& p) {
+    if (p.t != mp.t) {  // warp-uniform: a step lies in one matrix
       if constexpr (NV == kNvGiven) {
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) run_max = max(run_max, __shfl_xor_sync(0xFFFFFFFFu, run_max, o));
-        if (cur >= 0 && lane == 0 && run_max != 0) atomicMax(&batch.t[cur].tail[1], run_max);
+        if (mp.t >= 0 && lane == 0 && run_max != 0) atomicMax(&batch.t[mp.t].tail[1], run_max);
         run_max = 0;
       }
-      cur = p.t;
+      mp = find_mat(batch, p.t == mf.t ? mf.s0 : batch.chunk_start[p.t]);
       if constexpr (NV != kMx) {
+        const QuantArgs& a = batch.t[p.t];
         const float g = NV == kNvComputed ? __fdiv_rn(__uint_as_float(a.tail[1]), 2688.0f)  // amax / (6 * 448)
                                          : *a.g_in;
         nv = nv_context(g, nv_tab[NV != kMx ? warp : 0]);
@@ -432,13 +459,14 @@ __global__ void __launch_bounds__(kSThreads, SCfg<F32, NV != kMx>::kCtasPerSm)
     }
     if constexpr (NV != kMx) {
       if (p.f == 0) {  // the matrix's first piece records g
+        const QuantArgs& a = batch.t[p.t];
         a.tail[0] = __float_as_uint(nv.g);
         if constexpr (NV == kNvComputed) {
           if (a.g_out != nullptr) *a.g_out = nv.g;
         }
       }
     }
-    if (p.live == 0) continue;
+    if (p.live == 0) return;
     uint32_t w[FMT == BSQ_MXFP8 ? 8 : 4];
     uint32_t sb;
     // the piece's values as fp32 (exact path): fp32 sources, and NVFP4 blocks whose quotient step is
@@ -467,40 +495,55 @@ __global__ void __launch_bounds__(kSThreads, SCfg<F32, NV != kMx>::kCtasPerSm)
       sb = mx_piece_bf16<FMT>(p.w, w);
     }
     if constexpr (FMT == BSQ_MXFP8) {
-      uint4* dst = reinterpret_cast<uint4*>(a.codes + p.f);
+      uint4* dst = reinterpret_cast<uint4*>(mp.codes + p.f);
       dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
       dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
     } else if constexpr (FMT == BSQ_MXFP4) {
-      *reinterpret_cast<uint4*>(a.codes + (p.f >> 1)) = make_uint4(w[0], w[1], w[2], w[3]);
+      *reinterpret_cast<uint4*>(mp.codes + (p.f >> 1)) = make_uint4(w[0], w[1], w[2], w[3]);
     } else {  // NVFP4 codes are 8-byte aligned only when cols % 32 == 16
-      uint2* dst = reinterpret_cast<uint2*>(a.codes + (p.f >> 1));
+      uint2* dst = reinterpret_cast<uint2*>(mp.codes + (p.f >> 1));
       dst[0] = make_uint2(w[0], w[1]);
       if (p.live == 32) dst[1] = make_uint2(w[2], w[3]);
     }
     // each block's scale byte at its place in the tiled layout (rows and columns below 2^31;
     // the padding columns of the last 4-column group are zeroed after the loop)
-    const int64_t row64 = div_cols(p.f, a.cols, a.cols_magic64);
+    const int64_t row64 = div_cols(p.f, mp.cols, mp.magic);
     const uint32_t row = static_cast<uint32_t>(row64);
-    const uint32_t col = static_cast<uint32_t>(p.f - row64 * a.cols);
+    const uint32_t col = static_cast<uint32_t>(p.f - row64 * mp.cols);
     constexpr int kBlocks = FMT == BSQ_NVFP4 ? 2 : 1;
 #pragma unroll
     for (int h = 0; h < kBlocks; ++h) {
       if (h == 1 && p.live != 32) break;
       uint32_t r = row, c = col + 16u * h;
-      if (FMT == BSQ_NVFP4 && c >= static_cast<uint32_t>(a.cols)) {  // cols % 32 == 16: the next row
-        c -= static_cast<uint32_t>(a.cols);
+      if (FMT == BSQ_NVFP4 && c >= static_cast<uint32_t>(mp.cols)) {  // cols % 32 == 16: the next row
+        c -= static_cast<uint32_t>(mp.cols);
         ++r;
       }
       const uint32_t sc = c >> (FMT == BSQ_NVFP4 ? 4 : 5);
-      const uint64_t tile = static_cast<uint64_t>(r >> 7) * static_cast<uint64_t>(a.nct) + (sc >> 2);
-      a.scales[tile * 512 + (((r & 31u) << 4) | (((r >> 5) & 3u) << 2) | (sc & 3u))] = static_cast<uint8_t>(sb >> (8 * h));
+      const uint64_t tile = static_cast<uint64_t>(r >> 7) * static_cast<uint64_t>(mp.nct) + (sc >> 2);
+      mp.scales[tile * 512 + (((r & 31u) << 4) | (((r >> 5) & 3u) << 2) | (sc & 3u))] = static_cast<uint8_t>(sb >> (8 * h));
     }
+  };
+
+  // two piece buffers, alternating: the next step's loads are in flight while this one is
+  // quantized
+  Piece<F32> pa, pb;
+  int64_t k = static_cast<int64_t>(blockIdx.x) * kSWarps + warp;
+  if (k < nsteps) fetch(pa, step_of(k));
+  while (k < nsteps) {
+    if (k + nw < nsteps) fetch(pb, step_of(k + nw));
+    process(pa);
+    k += nw;
+    if (k >= nsteps) break;
+    if (k + nw < nsteps) fetch(pa, step_of(k + nw));
+    process(pb);
+    k += nw;
   }
   if constexpr (NV == kNvGiven) {
     // the last matrix's share of |x| maxima -> its tail word 1
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) run_max = max(run_max, __shfl_xor_sync(0xFFFFFFFFu, run_max, o));
-    if (cur >= 0 && lane == 0 && run_max != 0) atomicMax(&batch.t[cur].tail[1], run_max);
+    if (mp.t >= 0 && lane == 0 && run_max != 0) atomicMax(&batch.t[mp.t].tail[1], run_max);
   }
   // padding of the tiled scales reads 0: every word of the padding rows of each matrix's last row
   // tile, and the bytes past the last scale column in each row's last 4-column group (byte
