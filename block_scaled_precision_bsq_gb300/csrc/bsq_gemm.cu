@@ -52,7 +52,9 @@ constexpr int BN = 256;           // columns of the output tile (both CTAs)
 constexpr int BNH = BN / 2;       // rows of B held per CTA
 constexpr int kChunkBytes = 128;  // K bytes per stage: one 128-byte swizzle span per row
 constexpr int kMmasPerStage = 4;  // 32 K bytes per MMA
-constexpr int kNumEpiWarps = 8;
+constexpr int kNumEpiWarps = 8;  // two per TMEM lane quadrant, each draining 128 columns
+constexpr int kWarpCols = 4 * BN / kNumEpiWarps;
+constexpr int kAccRegs = kWarpCols / 32;  // 32-column TMEM loads per warp
 constexpr int kFirstEpiWarp = 2;
 constexpr int kThreads = (kFirstEpiWarp + kNumEpiWarps) * 32;
 constexpr int kAccCols = BN;  // fp32 accumulator columns in TMEM
@@ -97,11 +99,11 @@ struct Smem {
   static constexpr int sfb_off = sfa_off + S * kSfaBytes;
   static constexpr int epi_off = ((sfb_off + S * kSfbBytes) + 1023) / 1024 * 1024;
   static constexpr int bias_off = epi_off + kNumEpiWarps * Cfg<FMT>::kEpiBufs * kEpiChunkBytes;
-  static constexpr int bar_off = bias_off + kNumEpiWarps * 128 * 4;
+  static constexpr int bar_off = bias_off + kNumEpiWarps * kWarpCols * 4;
   static constexpr int kNumBars = 2 * S + 3;
   static constexpr int misc_off = bar_off + kNumBars * 8;
   static constexpr int total = misc_off + 16;
-  static constexpr int alloc = total + 1024;  // slack for aligning the base to 1024
+  static constexpr int alloc = total;  // the dynamic region is 1024-byte aligned (checked at kernel start)
 };
 static_assert(Smem<BSQ_MXFP8>::alloc <= 232448, "MXFP8 shared memory budget");
 static_assert(Smem<BSQ_NVFP4>::alloc <= 232448, "NVFP4 shared memory budget");
@@ -211,8 +213,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   using C = Cfg<FMT>;
   using L = Smem<FMT>;
   constexpr int S = C::kStages;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem[];
+  // the 128-byte swizzled operand tiles need a 1024-byte aligned base (uniform: every thread of
+  // both CTAs leaves before touching a barrier)
+  if (smem_u32(smem) & 1023u) {
+    if (threadIdx.x == 0) atomicCAS(args.status, 0, BSQ_ERR_LAUNCH);
+    return;
+  }
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::bar_off);
   uint64_t* full_bar = bars;                // leader: both CTAs' operands of a stage landed
   uint64_t* empty_bar = bars + S;           // the pair's MMAs are done with a stage
@@ -372,46 +379,59 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_wait_bounded(drain_bar, 0, nullptr, args.status);
   } else if (warp >= static_cast<uint32_t>(kFirstEpiWarp)) {
     // ------------------------------------------------------------------ epilogue (both CTAs)
-    const uint32_t e = warp - kFirstEpiWarp;  // 0..7
-    const uint32_t quad = warp & 3u;                  // TMEM lane quadrant this warp may access
-    const uint32_t half = e >> 2;
+    const uint32_t e = warp - kFirstEpiWarp;
+    const uint32_t quad = warp & 3u;  // TMEM lane quadrant this warp may access
+    const uint32_t cgrp = e >> 2;     // which kWarpCols of the tile's 256 columns
     constexpr int NB = C::kEpiBufs;
     uint8_t* stage_base = smem + L::epi_off + e * NB * L::kEpiChunkBytes;
     uint32_t nstores = 0;  // stores issued by this warp: staging buffer nstores % NB is next
-    float* bias_s = reinterpret_cast<float*>(smem + L::bias_off) + e * 128;
+    float* bias_s = reinterpret_cast<float*>(smem + L::bias_off) + e * kWarpCols;
     const uint32_t tmem_empty_leader = mapa_shared(smem_u32(tmem_empty), 0);
     float alpha = 1.0f;
     if constexpr (FMT == BSQ_NVFP4) alpha = __fmul_rn(*args.ga, *args.gb);
+    // this lane's kAccRegs bias values (consecutive columns from kAccRegs lane of the warp's
+    // kWarpCols, bf16 pairs) of unit u, zero past N or without bias; loaded one unit ahead so that
+    // their latency hides behind the stores of the unit before
+    using BiasRegs = uint32_t[kAccRegs / 2];
+    auto load_bias = [&](int u, BiasRegs& b) {
+      const int pt = u % args.num_pairs;
+      const int n = (pt % args.tiles_n) * BN + static_cast<int>(cgrp) * kWarpCols + kAccRegs * static_cast<int>(lane);
+      const int bn = (EPI == kEpiConvT || EPI == kEpiConvTGelu) ? n % args.cv_c : n;  // ConvT: per channel
+#pragma unroll
+      for (int i = 0; i < kAccRegs / 2; ++i) b[i] = 0u;
+      if (args.bias != nullptr && n < args.N) {
+#pragma unroll
+        for (int i = 0; i < kAccRegs / 2; ++i) b[i] = reinterpret_cast<const uint32_t*>(args.bias + bn)[i];
+      }
+    };
+    BiasRegs bias_next;
+    if (first_pair < args.num_units) load_bias(first_pair, bias_next);
     uint32_t acc_phase = 0;
     for (int u = first_pair; u < args.num_units; u += pair_stride) {
       const int split = u / args.num_pairs, pt = u - split * args.num_pairs;
       const int m_blk = 2 * (pt / args.tiles_n) + static_cast<int>(rank);
       const int n_blk = pt % args.tiles_n;
-      const int n0 = n_blk * BN + half * 128;
+      const int n0 = n_blk * BN + static_cast<int>(cgrp) * kWarpCols;
       const int m0 = m_blk * BM + quad * 32;
-      // bias of this warp's 128 columns (zero past N or without bias)
-      __syncwarp();
+      __syncwarp();  // every lane is done reading the previous unit's bias
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int n = n0 + 4 * lane + i;
-        const int bn = (EPI == kEpiConvT || EPI == kEpiConvTGelu) ? n % args.cv_c : n;  // ConvT: per channel
-        bias_s[4 * lane + i] =
-            (args.bias != nullptr && n < args.N) ? __uint_as_float(static_cast<uint32_t>(args.bias[bn]) << 16) : 0.0f;
-      }
+      for (int i = 0; i < kAccRegs / 2; ++i)
+        *reinterpret_cast<uint64_t*>(&bias_s[kAccRegs * lane + 2 * i]) =
+            f2(__uint_as_float(bias_next[i] << 16), __uint_as_float(bias_next[i] & 0xFFFF0000u));
       __syncwarp();
       if (!mbar_wait_bounded(tmem_full, acc_phase, abort_flag, args.status)) break;
       acc_phase ^= 1u;
       tc_fence_after();
-      uint32_t acc[4][32];
-      const uint32_t taddr = tmem_base + ((quad * 32u) << 16) + half * 128u;
+      uint32_t acc[kAccRegs][32];
+      const uint32_t taddr = tmem_base + ((quad * 32u) << 16) + cgrp * kWarpCols;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) tmem_ld_32x32b_x32(taddr + 32u * j, acc[j]);
+      for (int j = 0; j < kAccRegs; ++j) tmem_ld_32x32b_x32(taddr + 32u * j, acc[j]);
       tmem_ld_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_remote(tmem_empty_leader);  // accumulator may be overwritten now
+      if (u + pair_stride < args.num_units) load_bias(u + pair_stride, bias_next);
 
-      // the epilogue value of column c of this warp's 128: alpha * acc + bias (and GELU)
       // the epilogue values of columns c, c + 1 (c even), packed: alpha * acc + bias (and GELU)
       auto value2 = [&](int c, float& lo, float& hi) {
         const uint64_t a2 = f2(__uint_as_float(acc[c >> 5][c & 31]), __uint_as_float(acc[c >> 5][(c + 1) & 31]));
@@ -423,47 +443,52 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if constexpr (EPI != kEpiBf16 && EPI != kEpiConvT) gelu_erf2(lo, hi);
       };
-      // quantized epilogues: all 128 values first (in place), one MX block per 32 columns (the
-      // MX rule: exponent of the block's largest magnitude minus that of the element format's
-      // top binade), scale word of the row's four blocks stored in the tiled layout (zero for
-      // the padding rows of the tile)
+      // quantized epilogues: all kWarpCols values first (in place), one MX block per 32 columns
+      // (the MX rule: exponent of the block's largest magnitude minus that of the element format's
+      // top binade), the row's kAccRegs scale bytes stored in the tiled layout's 32-bit word of
+      // four blocks, or half of it (zero for the padding rows of the tile)
       constexpr bool kQuant = (EPI == kEpiGeluMxfp8 || EPI == kEpiGeluMxfp4);
-      float mul[4] = {1.0f, 1.0f, 1.0f, 1.0f};
+      float mul[kAccRegs];
       if constexpr (kQuant) {
 #pragma unroll
-        for (int c = 0; c < 128; c += 2) {
+        for (int c = 0; c < kWarpCols; c += 2) {
           float lo, hi;
           value2(c, lo, hi);
           acc[c >> 5][c & 31] = __float_as_uint(lo);
           acc[c >> 5][(c + 1) & 31] = __float_as_uint(hi);
         }
         constexpr uint32_t kEmax = (EPI == kEpiGeluMxfp8) ? 8u : 2u;
-        uint32_t word = 0;
+        uint32_t sword = 0;  // the row's scale bytes, block bk in byte bk
 #pragma unroll
-        for (int bk = 0; bk < 4; ++bk) {
+        for (int bk = 0; bk < kAccRegs; ++bk) {
           float amax = 0.0f;
 #pragma unroll
           for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(__uint_as_float(acc[bk][i])));
           const uint32_t ef = __float_as_uint(amax) >> 23;
           const uint32_t sbyte = ef > kEmax ? ef - kEmax : 0u;
           mul[bk] = __uint_as_float((254u - sbyte) << 23);  // 2^(127 - sbyte), exact
-          word |= sbyte << (8 * bk);
+          sword |= sbyte << (8 * bk);
         }
-        // rows of the padded output tiles only: with an odd number of 128-row tiles the last
-        // pair's second CTA computes a tile that lies wholly past them
+        // the words of the padded output tiles only: with an odd number of 128-row tiles the last
+        // pair's second CTA computes a tile that lies wholly past them, and a word's second half
+        // may lie wholly past N (padding blocks: zero)
         const uint32_t r = static_cast<uint32_t>(m0) + lane;
-        if (n0 < args.N && (r >> 7) < (static_cast<uint32_t>(args.M) + 127u) >> 7) {
+        if ((n0 >> 7) < args.q_nct && (r >> 7) < (static_cast<uint32_t>(args.M) + 127u) >> 7) {
           const uint64_t off = (static_cast<uint64_t>(r >> 7) * static_cast<uint64_t>(args.q_nct) +
-                                static_cast<uint64_t>(n0 >> 7)) * 512 + (r & 31u) * 16 + ((r >> 5) & 3u) * 4;
-          *reinterpret_cast<uint32_t*>(args.qscales + off) = r < static_cast<uint32_t>(args.M) ? word : 0u;
+                                static_cast<uint64_t>(n0 >> 7)) * 512 + (r & 31u) * 16 + ((r >> 5) & 3u) * 4 +
+                               ((n0 >> 5) & 3);
+          const uint32_t v = r < static_cast<uint32_t>(args.M) && n0 < args.N ? sword : 0u;
+          if constexpr (kAccRegs == 4) *reinterpret_cast<uint32_t*>(args.qscales + off) = v;
+          else *reinterpret_cast<uint16_t*>(args.qscales + off) = static_cast<uint16_t>(v);
         }
       }
 
       // store: chunks of 32 rows x RB bytes through the staging buffer and TMA
-      constexpr int EC = C::kEpiCols;
-      constexpr int RB = EC * 2;  // bytes of a staged row: 64 or 32
-      constexpr int kRowBytes =
-          (EPI == kEpiF32Partial) ? 512 : (EPI == kEpiGeluMxfp8) ? 128 : (EPI == kEpiGeluMxfp4 ? 64 : 256);
+      constexpr int kRowBytes = (EPI == kEpiF32Partial) ? 4 * kWarpCols
+                                : (EPI == kEpiGeluMxfp8) ? kWarpCols
+                                : (EPI == kEpiGeluMxfp4) ? kWarpCols / 2 : 2 * kWarpCols;
+      constexpr int RB = kRowBytes < 64 ? kRowBytes : 64;  // bytes of a staged row: 64 or 32
+      static_assert(32 * RB <= L::kEpiChunkBytes, "staging chunk");
       const int row_units = (EPI == kEpiGeluMxfp4) ? (args.N >> 1) : args.N;  // TMA x extent of a row
 #pragma unroll
       for (int j = 0; j < kRowBytes / RB; ++j) {
@@ -683,9 +708,12 @@ int run_gemm(const void* A, const void* A_scales, const void* B, const void* B_s
   } else if constexpr (EPI == kEpiBf16 || EPI == kEpiGeluBf16) {
     ok_out = make_map_2d(&mOut, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, out, N, M, static_cast<uint64_t>(N) * 2, EC, 32, osw);
   } else {
-    // code bytes of an output row: N (E4M3) or N / 2 (e2m1); staged rows of 2 * EC bytes
+    // code bytes of an output row: N (E4M3) or N / 2 (e2m1); staged rows of 64 bytes, or 32 (e2m1 codes of a
+    // warp's 64 columns)
     const uint64_t rb = (EPI == kEpiGeluMxfp8) ? static_cast<uint64_t>(N) : static_cast<uint64_t>(N) / 2;
-    ok_out = make_map_2d(&mOut, CU_TENSOR_MAP_DATA_TYPE_UINT8, out, rb, M, rb, 2 * EC, 32, osw);
+    ok_out = (EPI == kEpiGeluMxfp8 || kWarpCols / 2 >= 64)
+                 ? make_map_2d(&mOut, CU_TENSOR_MAP_DATA_TYPE_UINT8, out, rb, M, rb, 2 * EC, 32, osw)
+                 : make_map_2d(&mOut, CU_TENSOR_MAP_DATA_TYPE_UINT8, out, rb, M, rb, 32, 32, CU_TENSOR_MAP_SWIZZLE_32B);
   }
   if (!ok_out ||
       !make_map_2d(&mA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, kbytes, M, kbytes, kChunkBytes, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
