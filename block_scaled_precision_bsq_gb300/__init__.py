@@ -75,6 +75,9 @@ _lib.bsq_get_device_status.restype = _int
 _lib.bsq_get_device_status.argtypes = [_vp]
 _lib.bsq_selftest_timeout.restype = _int
 _lib.bsq_selftest_timeout.argtypes = [_i64, _vp]
+_lib.bsq_test_inject_stall.restype = _int
+_lib.bsq_test_inject_stall.argtypes = [_int, _i64, _i64]
+KERNEL_GEMM, KERNEL_DUAL, KERNEL_LAYERNORM = 1, 2, 3
 _lib.bsq_last_error.restype = _int
 _lib.bsq_strerror.restype = ctypes.c_char_p
 _lib.bsq_strerror.argtypes = [_int]
@@ -83,6 +86,7 @@ EXPORTS = ("bsq_codes_bytes", "bsq_scales_bytes", "bsq_quantize", "bsq_quantize_
            "bsq_quantize_dual", "bsq_delayed_global_scale", "bsq_gemm", "bsq_gemm_splitk", "bsq_gemm_splitk_splits",
            "bsq_gemm_splitk_scratch",
            "bsq_gemm_gelu", "bsq_gemm_gelu_quantize", "bsq_convt2x2", "bsq_get_device_status", "bsq_selftest_timeout",
+           "bsq_test_inject_stall",
            "bsq_last_error", "bsq_strerror")
 
 Ptr = Union[int, None, torch.Tensor]
@@ -205,6 +209,10 @@ def bsq_get_device_status(stream=None) -> int:
 
 def bsq_selftest_timeout(limit_ns: int, stream=None) -> int:
     return int(_lib.bsq_selftest_timeout(int(limit_ns), _stream(stream)))
+
+
+def bsq_test_inject_stall(kernel: int, after_stages: int, wait_limit_ns: int) -> int:
+    return int(_lib.bsq_test_inject_stall(int(kernel), int(after_stages), int(wait_limit_ns)))
 
 
 def bsq_last_error() -> int:

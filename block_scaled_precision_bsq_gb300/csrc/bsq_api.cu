@@ -20,6 +20,8 @@ __device__ int g_status_word;
 namespace {
 
 DeviceInfo g_dev[kMaxDevices];
+thread_local int t_stall_kernel = 0;  // BSQ_KERNEL_* of the armed stall, 0 = none
+thread_local StallInjection t_stall;
 std::once_flag g_dev_once[kMaxDevices];
 thread_local int t_last_error = 0;
 
@@ -48,6 +50,12 @@ __global__ void selftest_timeout_kernel(int64_t limit_ns, int* status) {
 }  // namespace
 
 int record_error(int code) { return fail(code); }
+
+StallInjection take_stall(int kernel) {
+  if (t_stall_kernel != kernel) return StallInjection{};
+  t_stall_kernel = 0;
+  return t_stall;
+}
 
 const DeviceInfo* current_device() {
   int dev = -1;
@@ -316,6 +324,19 @@ int bsq_selftest_timeout(int64_t limit_ns, bsq_stream_t stream) {
   if (dev == nullptr) return fail(BSQ_ERR_ARCH);
   const int st = bsq::launch_selftest_timeout(limit_ns, reinterpret_cast<cudaStream_t>(stream), *dev);
   return st == BSQ_OK ? BSQ_OK : fail(st);
+}
+
+int bsq_test_inject_stall(int kernel, int64_t after_stages, int64_t wait_limit_ns) {
+  if (kernel != BSQ_KERNEL_GEMM && kernel != BSQ_KERNEL_DUAL && kernel != BSQ_KERNEL_LAYERNORM) return fail(BSQ_ERR_ARG);
+  if (after_stages < -1 || wait_limit_ns < 1000 || wait_limit_ns > 10000000000ll) return fail(BSQ_ERR_ARG);
+  if (after_stages == -1) {  // disarm
+    bsq::t_stall_kernel = 0;
+    return BSQ_OK;
+  }
+  bsq::t_stall_kernel = kernel;
+  bsq::t_stall.after = after_stages;
+  bsq::t_stall.limit_ns = static_cast<uint64_t>(wait_limit_ns);
+  return BSQ_OK;
 }
 
 int bsq_last_error(void) { return bsq::t_last_error; }

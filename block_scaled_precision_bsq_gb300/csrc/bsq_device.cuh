@@ -114,8 +114,22 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
 
 // Whole-warp form of mbar_wait_bounded: every lane waits (bounded) and the warp agrees on the
 // outcome, so a timeout seen by any lane sends the whole warp down the same path.
-__device__ __forceinline__ bool mbar_wait_bounded_warp(uint64_t* bar, uint32_t parity, volatile int* abort, int* status) {
-  return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity, abort, status)) != 0;
+__device__ __forceinline__ bool mbar_wait_bounded_warp(uint64_t* bar, uint32_t parity, volatile int* abort, int* status,
+                                                       uint64_t limit_ns = kWaitLimitNs) {
+  return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity, abort, status, limit_ns)) != 0;
+}
+
+// Before a CTA that loads by TMA into a ring of `stages` buffers exits, every load it issued must
+// have landed (a copy still in flight would write into shared memory a later CTA may own). The
+// producer armed `armed` stages in ring order from stage 0, phase 0; for each stage this waits
+// (bounded, ignoring the abort flag) for the phase of its last arming. Phases already completed
+// return at once, so on the normal path this costs nothing.
+__device__ __forceinline__ void wait_armed_stages(uint64_t* full_bar, int stages, int64_t armed, int* status,
+                                                  uint64_t limit_ns = kWaitLimitNs) {
+  for (int s = 0; s < stages && s < armed; ++s) {
+    const int64_t arms = (armed - s + stages - 1) / stages;  // times stage s was armed
+    mbar_wait_bounded(&full_bar[s], static_cast<uint32_t>((arms - 1) & 1), nullptr, status, limit_ns);
+  }
 }
 
 // ---------------------------------------------------------------------------- TMA

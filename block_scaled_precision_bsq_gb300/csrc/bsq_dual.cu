@@ -87,6 +87,8 @@ struct DualArgs {
   const float* g_in;  // given mode (else g = amax / 2688 from row_tail[1], put there beforehand)
   float* g_out;       // computed mode: receives g (nullable)
   int* status;
+  int64_t stall_after;  // injected stall (tests): the producer stops after this many tiles; -1 = none
+  uint64_t wait_ns;     // limit of every bounded wait
 };
 
 // Philox4x32-10 of the SC'11 paper: ten rounds of two 32 x 32 -> 64-bit products mixed into
@@ -390,17 +392,22 @@ __global__ void __launch_bounds__(kDThreads, kDCtasPerSm)
       prefetch_tmap(&src_map);
       int stage = 0;
       uint32_t phase = 0;
+      int64_t armed = 0;  // tiles loaded so far (ring order from stage 0)
       for (int64_t t = blockIdx.x; t < a.ntiles; t += gridDim.x) {
-        if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1u, abort_flag, a.status)) break;
+        if (armed == a.stall_after) break;  // injected stall: no more loads, none announced
+        if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1u, abort_flag, a.status, a.wait_ns)) break;
         const int64_t ti = t / a.tiles_c, tj = t - ti * a.tiles_c;
         mbar_arrive_expect_tx(&full_bar[stage], kDTileBytes);
         tma_load_2d(ring + stage * kDTileBytes, &src_map, &full_bar[stage], static_cast<int32_t>(tj * kDCols),
                     static_cast<int32_t>(ti * kRows));
+        ++armed;
         if (++stage == kDStages) {
           stage = 0;
           phase ^= 1u;
         }
       }
+      // nothing this CTA loads may still be in flight when it exits
+      wait_armed_stages(full_bar, kDStages, armed, a.status, a.wait_ns);
     }
     return;
   }
@@ -440,7 +447,7 @@ __global__ void __launch_bounds__(kDThreads, kDCtasPerSm)
   int stage = 0;
   uint32_t phase = 0;
   for (int64_t t = blockIdx.x; t < a.ntiles; t += gridDim.x) {
-    const bool ok = mbar_wait_bounded_warp(&full_bar[stage], phase, abort_flag, a.status);
+    const bool ok = mbar_wait_bounded_warp(&full_bar[stage], phase, abort_flag, a.status, a.wait_ns);
     const int64_t ti = t / a.tiles_c, tj = t - ti * a.tiles_c;
     const int64_t r0 = ti * kRows, c0 = tj * kDCols;
     const uint8_t* tile = ring + stage * kDTileBytes;
@@ -691,6 +698,9 @@ int launch_quantize_dual(int fmt, bool src_f32, bool stochastic, bool global_giv
     a.keys[2 * i + 1] = a.seed_hi + static_cast<uint32_t>(i) * 0xBB67AE85u;
   }
   a.status = dev.status;
+  const StallInjection inj = take_stall(BSQ_KERNEL_DUAL);
+  a.stall_after = inj.after;
+  a.wait_ns = inj.limit_ns;
   if (fmt == BSQ_NVFP4) {
     a.row_tail = reinterpret_cast<uint32_t*>(a.row_scales + scales_body_bytes(fmt, rows, cols));
     a.col_tail = reinterpret_cast<uint32_t*>(a.col_scales + scales_body_bytes(fmt, cols, rows));

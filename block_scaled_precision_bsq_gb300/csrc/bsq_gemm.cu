@@ -203,6 +203,8 @@ struct GemmArgs {
   int nk;  // stages per tile: K bytes / 128
   int cv_c, cv_w;  // ConvT epilogues: output channels C_out, input width W
   int* status;
+  int64_t stall_after;  // injected stall (tests): producers stop after this many stages; -1 = none
+  uint64_t wait_ns;     // limit of every bounded wait
 };
 
 template <int FMT, int EPI>
@@ -276,13 +278,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
+    int64_t armed = 0;  // stages armed so far (ring order from stage 0)
     for (int u = first_pair; u < args.num_units && ok; u += pair_stride) {
       const int split = u / args.num_pairs, pt = u - split * args.num_pairs;
       const int m_blk = 2 * (pt / args.tiles_n) + static_cast<int>(rank);
       const int n_blk = pt % args.tiles_n;
       const int kb1 = (split + 1) * args.nk / args.splits;
       for (int kb = split * args.nk / args.splits; kb < kb1; ++kb) {
-        if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1u, abort_flag, args.status)) {
+        if (armed == args.stall_after) {  // injected stall: no more loads, none announced
+          ok = false;
+          break;
+        }
+        if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1u, abort_flag, args.status, args.wait_ns)) {
           ok = false;
           break;
         }
@@ -294,12 +301,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d_to_leader(smem + L::sfa_off + stage * L::kSfaBytes, &mapSfa, bar, 0, kb * C::kAtoms, m_blk, keep);
         tma_load_3d_to_leader(smem + L::sfb_off + stage * L::kSfbBytes, &mapSfb, bar, 0, kb * C::kAtoms, 2 * n_blk,
                               keep);
+        ++armed;
         if (++stage == S) {
           stage = 0;
           phase ^= 1u;
         }
       }
     }
+    // both CTAs' loads complete on the leader's full barriers: the leader waits for every stage
+    // it armed, and neither CTA passes the final cluster barrier before that
+    if (leader) wait_armed_stages(full_bar, S, armed, args.status, args.wait_ns);
   } else if (warp == 1 && leader) {
     // ------------------------------------------------------------------ MMA issuer (leader)
     const bool issuer = elect_one_sync();
@@ -316,12 +327,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int split = u / args.num_pairs;
       const int kb0 = split * args.nk / args.splits, kb1 = (split + 1) * args.nk / args.splits;
       // wait until both CTAs' epilogues have drained the accumulator of the previous tile
-      if (!mbar_wait_bounded_warp(tmem_empty, acc_phase ^ 1u, abort_flag, args.status)) break;
+      if (!mbar_wait_bounded_warp(tmem_empty, acc_phase ^ 1u, abort_flag, args.status, args.wait_ns)) break;
       acc_phase ^= 1u;
       tc_fence_after();
       for (int kb = kb0; kb < kb1; ++kb) {
         // both CTAs' operands of the stage landed
-        if (!mbar_wait_bounded_warp(&full_bar[stage], phase, abort_flag, args.status)) {
+        if (!mbar_wait_bounded_warp(&full_bar[stage], phase, abort_flag, args.status, args.wait_ns)) {
           ok = false;
           break;
         }
@@ -376,7 +387,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // every tensor-core operation of the issuing lane must finish before TMEM is released
     if (issuer) tc_commit_pair(drain_bar);
     __syncwarp();
-    mbar_wait_bounded(drain_bar, 0, nullptr, args.status);
+    mbar_wait_bounded(drain_bar, 0, nullptr, args.status, args.wait_ns);
   } else if (warp >= static_cast<uint32_t>(kFirstEpiWarp)) {
     // ------------------------------------------------------------------ epilogue (both CTAs)
     const uint32_t e = warp - kFirstEpiWarp;
@@ -419,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         *reinterpret_cast<uint64_t*>(&bias_s[kAccRegs * lane + 2 * i]) =
             f2(__uint_as_float(bias_next[i] << 16), __uint_as_float(bias_next[i] & 0xFFFF0000u));
       __syncwarp();
-      if (!mbar_wait_bounded(tmem_full, acc_phase, abort_flag, args.status)) break;
+      if (!mbar_wait_bounded(tmem_full, acc_phase, abort_flag, args.status, args.wait_ns)) break;
       acc_phase ^= 1u;
       tc_fence_after();
       uint32_t acc[kAccRegs][32];
@@ -740,6 +751,9 @@ int run_gemm(const void* A, const void* A_scales, const void* B, const void* B_s
   a.splits = (EPI == kEpiF32Partial) ? splits : 1;
   a.num_units = a.num_pairs * a.splits;
   a.status = dev.status;
+  const StallInjection inj = take_stall(BSQ_KERNEL_GEMM);
+  a.stall_after = inj.after;
+  a.wait_ns = inj.limit_ns;
   const int clusters = std::min(a.num_units, std::min(max_clusters, dev.num_sms / 2));
 
   cudaLaunchAttribute at[2];

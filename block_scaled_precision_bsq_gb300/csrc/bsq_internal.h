@@ -46,6 +46,16 @@ struct PerDevice {
   }
 };
 
+// A stall injected into the next launch of one kernel class on the calling thread
+// (bsq_test_inject_stall): the producers stop issuing loads after `after` pipeline stages (-1:
+// none) and the launch's bounded waits give up after `limit_ns`.
+struct StallInjection {
+  int64_t after = -1;
+  uint64_t limit_ns = 2000000000ull;
+};
+// Takes (and clears) the calling thread's injection if it names `kernel` (BSQ_KERNEL_*); else none.
+StallInjection take_stall(int kernel);
+
 // Record `code` as the calling thread's last error (bsq_last_error) and return it.
 int record_error(int code);
 

@@ -78,6 +78,8 @@ struct QuantBatch {
   int64_t chunk_start[kMaxBatch + 1];  // LayerNorm kernel: chunks; streaming kernel: warp steps
   QuantArgs t[kMaxBatch];
   int* status;
+  int64_t stall_after;  // LayerNorm kernel, injected stall (tests): loads stop after this many chunks; -1 = none
+  uint64_t wait_ns;     // LayerNorm kernel: limit of every bounded wait
 };
 
 // The first N (16 or 32) source elements of one lane's piece (bf16 or fp32) -> fp32 values.
@@ -607,18 +609,23 @@ __global__ void __launch_bounds__(QCfg::kThreads, QCfg::kCtasPerSm)
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
+      int64_t armed = 0;  // chunks loaded so far (ring order from stage 0)
       for (int64_t c = blockIdx.x; c < nchunks; c += gridDim.x) {
-        if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1u, &abort_flag, batch.status)) break;
+        if (armed == batch.stall_after) break;  // injected stall: no more loads, none announced
+        if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1u, &abort_flag, batch.status, batch.wait_ns)) break;
         const int64_t r0 = c * a.rows_per_chunk;
         const int64_t nr = min(a.rows_per_chunk, a.rows - r0);
         const uint32_t bytes = static_cast<uint32_t>(nr * a.cols * kEsize);
         mbar_arrive_expect_tx(&full_bar[stage], bytes);
         bulk_load(ring + stage * kChunkMax, a.src + r0 * a.cols * kEsize, bytes, &full_bar[stage]);
+        ++armed;
         if (++stage == kRing) {
           stage = 0;
           phase ^= 1u;
         }
       }
+      // nothing this CTA loads may still be in flight when it exits
+      wait_armed_stages(full_bar, kRing, armed, batch.status, batch.wait_ns);
     }
   } else {
     // ------------------------------------------------------------ consumers
@@ -632,7 +639,7 @@ __global__ void __launch_bounds__(QCfg::kThreads, QCfg::kCtasPerSm)
     const int nci = static_cast<int>(a.cols);
     const int pieces = nci * kEsize / 16;  // 16-byte pieces of a row
     for (int64_t c = blockIdx.x; c < nchunks; c += gridDim.x) {
-      if (!mbar_wait_bounded_warp(&full_bar[stage], phase, &abort_flag, batch.status)) break;
+      if (!mbar_wait_bounded_warp(&full_bar[stage], phase, &abort_flag, batch.status, batch.wait_ns)) break;
       const int64_t r0 = c * a.rows_per_chunk;
       const int64_t nr = min(a.rows_per_chunk, a.rows - r0);
       const uint8_t* buf = ring + stage * kChunkMax;
@@ -942,6 +949,9 @@ int launch_layernorm_quantize(int fmt, bool src_f32, const QuantItem& item, cons
   QuantBatch b{};
   b.n = 1;
   b.status = dev.status;
+  const StallInjection inj = take_stall(BSQ_KERNEL_LAYERNORM);
+  b.stall_after = inj.after;
+  b.wait_ns = inj.limit_ns;
   QuantArgs& a = b.t[0];
   fill_args(a, fmt, item);
   // chunks of whole rows: at most one ring buffer, and small enough that every SM gets a few

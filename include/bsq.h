@@ -347,6 +347,28 @@ int bsq_get_device_status(bsq_stream_t stream);
  */
 int bsq_selftest_timeout(int64_t limit_ns, bsq_stream_t stream);
 
+/*
+ * bsq_test_inject_stall: a test of the failure path of the kernels that wait on barriers, with no
+ * GPU fault: arms a one-shot stall for the calling thread's next launch of one kernel class.
+ *   kernel         BSQ_KERNEL_GEMM (every bsq_gemm* and bsq_convt2x2 launch), BSQ_KERNEL_DUAL
+ *                  (bsq_quantize_dual) or BSQ_KERNEL_LAYERNORM (bsq_layernorm_quantize)
+ *   after_stages   >= 0: the producers of that launch stop issuing loads -- and never announce the
+ *                  missing bytes -- after this many pipeline stages per CTA, so a consumer waits for
+ *                  a stage that never arrives; -1: disarm any stall armed on the calling thread
+ *   wait_limit_ns  the limit of every bounded wait in that launch, in [1e3, 1e10] (the default
+ *                  limit is 2 s)
+ * The starved wait gives up after wait_limit_ns; the kernel then records BSQ_ERR_TIMEOUT in the
+ * device status word, every role leaves its loop, the loads already issued are waited for (so
+ * nothing is left in flight), tensor-core work drains, TMEM is released and the kernel returns.
+ * The launch's outputs are incomplete; the next launch of the kernel runs normally. The method has
+ * no counterpart: this exists for the tests. Errors: BSQ_ERR_ARG for an unknown kernel, after_stages
+ * below -1 or a limit out of range.
+ */
+#define BSQ_KERNEL_GEMM 1
+#define BSQ_KERNEL_DUAL 2
+#define BSQ_KERNEL_LAYERNORM 3
+int bsq_test_inject_stall(int kernel, int64_t after_stages, int64_t wait_limit_ns);
+
 /* bsq_last_error: the calling thread's last non-zero return code (0 if none). */
 int bsq_last_error(void);
 

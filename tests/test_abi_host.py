@@ -153,3 +153,14 @@ def test_no_multicast_bulk_or_tensor_copy_in_the_sources():
             if "cp.async.bulk" in m.group(0) or "tcgen05.commit" not in m.group(0):
                 offenders.append("%s: %s" % (name, m.group(0)))
     assert not offenders, offenders
+
+
+def test_stall_injection_argument_errors(bsq):
+    inj = bsq.bsq_test_inject_stall
+    assert inj(0, 1, 10**6) == bsq.ERR_ARG          # unknown kernel
+    assert inj(4, 1, 10**6) == bsq.ERR_ARG
+    assert inj(bsq.KERNEL_GEMM, -2, 10**6) == bsq.ERR_ARG
+    assert inj(bsq.KERNEL_DUAL, 1, 999) == bsq.ERR_ARG
+    assert inj(bsq.KERNEL_LAYERNORM, 1, 10**10 + 1) == bsq.ERR_ARG
+    assert inj(bsq.KERNEL_GEMM, 0, 10**6) == bsq.OK   # armed for this thread's next GEMM launch
+    assert inj(bsq.KERNEL_GEMM, -1, 10**6) == bsq.OK  # disarmed again
