@@ -18,7 +18,9 @@ from typing import Optional, Union
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libbsq.so")
+# BSQ_LIBRARY=checked selects the checked build (device-side index checks, status
+# BSQ_ERR_DEVICE_CHECK on a failed check); the default is the normal build
+LIB_PATH = os.path.join(_HERE, "libbsq_checked.so" if os.environ.get("BSQ_LIBRARY") == "checked" else "libbsq.so")
 
 MXFP8, NVFP4, MXFP4 = 1, 2, 3
 FLAG_SRC_F32 = 0x100
@@ -26,11 +28,11 @@ FLAG_GLOBAL_GIVEN = 0x200
 FLAG_STOCHASTIC = 0x400
 FORMATS = {"mxfp8": MXFP8, "nvfp4": NVFP4, "mxfp4": MXFP4}
 
-OK, ERR_ARG, ERR_SHAPE, ERR_ALIGN, ERR_ARCH, ERR_LAUNCH, ERR_TIMEOUT = 0, -1, -2, -3, -4, -5, -6
+OK, ERR_ARG, ERR_SHAPE, ERR_ALIGN, ERR_ARCH, ERR_LAUNCH, ERR_TIMEOUT, ERR_DEVICE_CHECK = 0, -1, -2, -3, -4, -5, -6, -7
 
 if not os.path.exists(LIB_PATH):
-    raise ImportError("libbsq.so is not built (run block_scaled_precision_bsq_gb300.build.build() "
-                      "or __graft_entry__.build()); there is no fallback implementation")
+    raise ImportError("%s is not built (run block_scaled_precision_bsq_gb300.build.build() "
+                      "or __graft_entry__.build()); there is no fallback implementation" % os.path.basename(LIB_PATH))
 
 _lib = ctypes.CDLL(LIB_PATH)
 _i64, _vp, _int = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
@@ -75,6 +77,8 @@ _lib.bsq_get_device_status.restype = _int
 _lib.bsq_get_device_status.argtypes = [_vp]
 _lib.bsq_selftest_timeout.restype = _int
 _lib.bsq_selftest_timeout.argtypes = [_i64, _vp]
+_lib.bsq_selftest_device_check.restype = _int
+_lib.bsq_selftest_device_check.argtypes = [_vp]
 _lib.bsq_test_inject_stall.restype = _int
 _lib.bsq_test_inject_stall.argtypes = [_int, _i64, _i64]
 KERNEL_GEMM, KERNEL_DUAL, KERNEL_LAYERNORM = 1, 2, 3
@@ -86,7 +90,7 @@ EXPORTS = ("bsq_codes_bytes", "bsq_scales_bytes", "bsq_quantize", "bsq_quantize_
            "bsq_quantize_dual", "bsq_delayed_global_scale", "bsq_gemm", "bsq_gemm_splitk", "bsq_gemm_splitk_splits",
            "bsq_gemm_splitk_scratch",
            "bsq_gemm_gelu", "bsq_gemm_gelu_quantize", "bsq_convt2x2", "bsq_get_device_status", "bsq_selftest_timeout",
-           "bsq_test_inject_stall",
+           "bsq_selftest_device_check", "bsq_test_inject_stall",
            "bsq_last_error", "bsq_strerror")
 
 Ptr = Union[int, None, torch.Tensor]
@@ -209,6 +213,10 @@ def bsq_get_device_status(stream=None) -> int:
 
 def bsq_selftest_timeout(limit_ns: int, stream=None) -> int:
     return int(_lib.bsq_selftest_timeout(int(limit_ns), _stream(stream)))
+
+
+def bsq_selftest_device_check(stream=None) -> int:
+    return int(_lib.bsq_selftest_device_check(_stream(stream)))
 
 
 def bsq_test_inject_stall(kernel: int, after_stages: int, wait_limit_ns: int) -> int:

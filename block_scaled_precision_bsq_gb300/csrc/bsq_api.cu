@@ -79,6 +79,17 @@ const DeviceInfo* current_device() {
   return d.status != nullptr ? &d : nullptr;
 }
 
+namespace {
+// One thread evaluating an index check that fails: records BSQ_ERR_DEVICE_CHECK in the checked
+// build, nothing in the normal one.
+__global__ void selftest_device_check_kernel(int* status) {
+  const volatile int index = 1, size = 1;
+  volatile int sink = 0;
+  if (in_bounds(index < size, status)) sink = index;  // the guarded access touches nothing shared
+  (void)sink;
+}
+}  // namespace
+
 int launch_selftest_timeout(int64_t limit_ns, cudaStream_t stream, const DeviceInfo& dev) {
   selftest_timeout_kernel<<<1, 32, 0, stream>>>(limit_ns, dev.status);
   return cudaGetLastError() == cudaSuccess ? BSQ_OK : BSQ_ERR_LAUNCH;
@@ -339,6 +350,13 @@ int bsq_test_inject_stall(int kernel, int64_t after_stages, int64_t wait_limit_n
   return BSQ_OK;
 }
 
+int bsq_selftest_device_check(bsq_stream_t stream) {
+  const bsq::DeviceInfo* dev = bsq::current_device();
+  if (dev == nullptr) return fail(BSQ_ERR_ARCH);
+  bsq::selftest_device_check_kernel<<<1, 1, 0, reinterpret_cast<cudaStream_t>(stream)>>>(dev->status);
+  return cudaGetLastError() == cudaSuccess ? BSQ_OK : fail(BSQ_ERR_LAUNCH);
+}
+
 int bsq_last_error(void) { return bsq::t_last_error; }
 
 const char* bsq_strerror(int status) {
@@ -350,6 +368,7 @@ const char* bsq_strerror(int status) {
     case BSQ_ERR_ARCH: return "no compute capability 10.3 (GB300) device";
     case BSQ_ERR_LAUNCH: return "CUDA launch or runtime error";
     case BSQ_ERR_TIMEOUT: return "a kernel's bounded wait timed out";
+    case BSQ_ERR_DEVICE_CHECK: return "a kernel's index check failed (checked build)";
     default: return "unknown status";
   }
 }

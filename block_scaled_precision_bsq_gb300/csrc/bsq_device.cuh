@@ -27,6 +27,23 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 
 __device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31u; }
 
+// Index checks of the checked build (compiled with BSQ_DEVICE_CHECKS=1): an access whose computed
+// index falls outside its buffer records BSQ_ERR_DEVICE_CHECK in the status word and is skipped
+// (`if (in_bounds(...)) access`). In the normal build the test compiles to nothing.
+#ifndef BSQ_DEVICE_CHECKS
+#define BSQ_DEVICE_CHECKS 0
+#endif
+__device__ __forceinline__ bool in_bounds(bool ok, int* status) {
+#if BSQ_DEVICE_CHECKS
+  if (!ok) atomicCAS(status, 0, BSQ_ERR_DEVICE_CHECK);
+  return ok;
+#else
+  (void)ok;
+  (void)status;
+  return true;
+#endif
+}
+
 __device__ __forceinline__ bool elect_lane0() { return (threadIdx.x & 31u) == 0u; }
 
 // Programmatic dependent launch. A kernel launched with programmatic stream serialization

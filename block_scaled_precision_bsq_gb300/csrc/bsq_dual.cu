@@ -89,6 +89,8 @@ struct DualArgs {
   int* status;
   int64_t stall_after;  // injected stall (tests): the producer stops after this many tiles; -1 = none
   uint64_t wait_ns;     // limit of every bounded wait
+  int64_t codes_bytes;  // size of each layout's code buffer (index checks)
+  int64_t row_scales_bytes, col_scales_bytes;  // tiled scale bodies of the two layouts
 };
 
 // Philox4x32-10 of the SC'11 paper: ten rounds of two 32 x 32 -> 64-bit products mixed into
@@ -510,7 +512,8 @@ __global__ void __launch_bounds__(kDThreads, kDCtasPerSm)
             block_codes<FMT, SR, false>(xb, bf, br, g0 + h * (BS / 8), 0u, a, wb);
           }
         }
-        if (r < R && c < C) {
+        if (r < R && c < C &&
+            in_bounds((kFp8 ? r * C + c + 32 : (r * C + c) / 2 + 16) <= a.codes_bytes, a.status)) {
           const int64_t idx = r * C + c;
           if constexpr (kFp8) {
             uint4* dst = reinterpret_cast<uint4*>(a.row_codes + idx);
@@ -534,7 +537,7 @@ __global__ void __launch_bounds__(kDThreads, kDCtasPerSm)
         const int64_t grp = c / (4 * BS);  // 4-scale-column group of the row layout
         if ((lane & (kNv ? 1u : 3u)) == 0 && grp < a.nct_row) {
           const int64_t off = ((r >> 7) * a.nct_row + grp) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4;
-          *reinterpret_cast<uint32_t*>(a.row_scales + off) = sw;
+          if (in_bounds(off + 4 <= a.row_scales_bytes, a.status)) *reinterpret_cast<uint32_t*>(a.row_scales + off) = sw;
         }
       }
     }
@@ -603,9 +606,11 @@ __global__ void __launch_bounds__(kDThreads, kDCtasPerSm)
       if (grp < a.nct_col) {
         const int64_t off =
             (tj * a.nct_col + grp) * 512 + (cc & 31) * 16 + ((cc >> 5) & 3) * 4 + (rt / BS) % 4;
-        if constexpr (kBytes == 4) *reinterpret_cast<uint32_t*>(a.col_scales + off) = sbytes;
-        else if constexpr (kBytes == 2) *reinterpret_cast<uint16_t*>(a.col_scales + off) = static_cast<uint16_t>(sbytes);
-        else a.col_scales[off] = static_cast<uint8_t>(sbytes);
+        if (in_bounds(off + kBytes <= a.col_scales_bytes, a.status)) {
+          if constexpr (kBytes == 4) *reinterpret_cast<uint32_t*>(a.col_scales + off) = sbytes;
+          else if constexpr (kBytes == 2) *reinterpret_cast<uint16_t*>(a.col_scales + off) = static_cast<uint16_t>(sbytes);
+          else a.col_scales[off] = static_cast<uint8_t>(sbytes);
+        }
       }
     }
 
@@ -691,6 +696,9 @@ int launch_quantize_dual(int fmt, bool src_f32, bool stochastic, bool global_giv
   a.ntiles = (ceil_div(rows, 128) * 128 / tile_rows) * a.tiles_c;
   a.nct_row = ceil_div(cols, 4 * bs);
   a.nct_col = ceil_div(rows, 4 * bs);
+  a.codes_bytes = fmt == BSQ_MXFP8 ? rows * cols : rows * cols / 2;
+  a.row_scales_bytes = scales_body_bytes(fmt, rows, cols);
+  a.col_scales_bytes = scales_body_bytes(fmt, cols, rows);
   a.seed_lo = static_cast<uint32_t>(seed);
   a.seed_hi = static_cast<uint32_t>(seed >> 32);
   for (int i = 0; i < 10; ++i) {

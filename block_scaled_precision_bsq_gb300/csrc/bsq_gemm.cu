@@ -205,6 +205,8 @@ struct GemmArgs {
   int* status;
   int64_t stall_after;  // injected stall (tests): producers stop after this many stages; -1 = none
   uint64_t wait_ns;     // limit of every bounded wait
+  int64_t qscales_bytes;  // size of the quantized epilogues' tiled scale body (index checks)
+  int bias_len;           // bias values: N, or C_out for the transposed convolutions
 };
 
 template <int FMT, int EPI>
@@ -410,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int bn = (EPI == kEpiConvT || EPI == kEpiConvTGelu) ? n % args.cv_c : n;  // ConvT: per channel
 #pragma unroll
       for (int i = 0; i < kAccRegs / 2; ++i) b[i] = 0u;
-      if (args.bias != nullptr && n < args.N) {
+      if (args.bias != nullptr && n < args.N && in_bounds(bn >= 0 && bn + kAccRegs <= args.bias_len, args.status)) {
 #pragma unroll
         for (int i = 0; i < kAccRegs / 2; ++i) b[i] = reinterpret_cast<const uint32_t*>(args.bias + bn)[i];
       }
@@ -489,8 +491,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 static_cast<uint64_t>(n0 >> 7)) * 512 + (r & 31u) * 16 + ((r >> 5) & 3u) * 4 +
                                ((n0 >> 5) & 3);
           const uint32_t v = r < static_cast<uint32_t>(args.M) && n0 < args.N ? sword : 0u;
-          if constexpr (kAccRegs == 4) *reinterpret_cast<uint32_t*>(args.qscales + off) = v;
-          else *reinterpret_cast<uint16_t*>(args.qscales + off) = static_cast<uint16_t>(v);
+          if (in_bounds(off + kAccRegs <= static_cast<uint64_t>(args.qscales_bytes), args.status)) {
+            if constexpr (kAccRegs == 4) *reinterpret_cast<uint32_t*>(args.qscales + off) = v;
+            else *reinterpret_cast<uint16_t*>(args.qscales + off) = static_cast<uint16_t>(v);
+          }
         }
       }
 
@@ -739,6 +743,8 @@ int run_gemm(const void* A, const void* A_scales, const void* B, const void* B_s
   a.bias = static_cast<const uint16_t*>(bias);
   a.qscales = static_cast<uint8_t*>(out_scales);
   a.q_nct = static_cast<int>(ceil_div(N / 32, 4));
+  a.qscales_bytes = ceil_div(M, 128) * a.q_nct * 512;
+  a.bias_len = static_cast<int>((EPI == kEpiConvT || EPI == kEpiConvTGelu) ? N / 4 : N);
   a.ga = reinterpret_cast<const float*>(static_cast<const uint8_t*>(A_scales) + scales_body_bytes(FMT, M, K));
   a.gb = reinterpret_cast<const float*>(static_cast<const uint8_t*>(B_scales) + scales_body_bytes(FMT, N, K));
   a.M = static_cast<int>(M);

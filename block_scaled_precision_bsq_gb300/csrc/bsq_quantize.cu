@@ -65,6 +65,8 @@ struct QuantArgs {
   uint32_t cols_magic;  // floor(2^32 / cols) + 1: f / cols == umulhi(f, cols_magic) for f * cols < 2^32
   uint64_t cols_magic64;  // floor((2^64 - 1) / cols): f / cols is umul64hi(f, .) or one more
   int64_t elems;        // rows * cols
+  int64_t codes_bytes;  // sizes of the code buffer and of the tiled scale body (index checks)
+  int64_t scales_bytes;
   // LayerNorm mode: y = (x - mean) / sqrt(var + eps) * gamma + beta per row before quantizing
   const uint16_t* gamma;  // cols bf16
   const uint16_t* beta;   // cols bf16
@@ -377,6 +379,7 @@ struct Mat {
   int64_t elems, cols, nct;
   uint64_t magic;
   bool aligned32;
+  int64_t codes_bytes, scales_bytes;
 };
 
 __device__ __forceinline__ Mat find_mat(const QuantBatch& b, int64_t s) {
@@ -395,6 +398,8 @@ __device__ __forceinline__ Mat find_mat(const QuantBatch& b, int64_t s) {
   m.nct = a.nct;
   m.magic = a.cols_magic64;
   m.aligned32 = (reinterpret_cast<uintptr_t>(a.src) & 31u) == 0u;
+  m.codes_bytes = a.codes_bytes;
+  m.scales_bytes = a.scales_bytes;
   return m;
 }
 
@@ -420,7 +425,8 @@ __global__ void __launch_bounds__(kSThreads, SCfg<F32, NV != kMx>::kCtasPerSm)
     if (s < mf.s0 || s >= mf.s1) mf = find_mat(batch, s);  // warp-uniform
     p.t = mf.t;
     p.f = (s - mf.s0) * 1024 + 32 * static_cast<int64_t>(lane);
-    const int64_t left = mf.elems - p.f;
+    int64_t left = mf.elems - p.f;
+    if (!in_bounds(p.f >= 0, batch.status)) left = 0;
     const uint8_t* src = mf.src + p.f * (F32 ? 4 : 2);
     if (left >= 32) {
       p.live = 32;
@@ -496,16 +502,20 @@ __global__ void __launch_bounds__(kSThreads, SCfg<F32, NV != kMx>::kCtasPerSm)
     } else {
       sb = mx_piece_bf16<FMT>(p.w, w);
     }
-    if constexpr (FMT == BSQ_MXFP8) {
-      uint4* dst = reinterpret_cast<uint4*>(mp.codes + p.f);
-      dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-      dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-    } else if constexpr (FMT == BSQ_MXFP4) {
-      *reinterpret_cast<uint4*>(mp.codes + (p.f >> 1)) = make_uint4(w[0], w[1], w[2], w[3]);
-    } else {  // NVFP4 codes are 8-byte aligned only when cols % 32 == 16
-      uint2* dst = reinterpret_cast<uint2*>(mp.codes + (p.f >> 1));
-      dst[0] = make_uint2(w[0], w[1]);
-      if (p.live == 32) dst[1] = make_uint2(w[2], w[3]);
+    const int64_t cb = (FMT == BSQ_MXFP8) ? p.f : (p.f >> 1);  // first code byte of the piece
+    const int64_t cn = (FMT == BSQ_MXFP8) ? 32 : p.live / 2;  // code bytes of the piece
+    if (in_bounds(cb >= 0 && cb + cn <= mp.codes_bytes, batch.status)) {
+      if constexpr (FMT == BSQ_MXFP8) {
+        uint4* dst = reinterpret_cast<uint4*>(mp.codes + p.f);
+        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+      } else if constexpr (FMT == BSQ_MXFP4) {
+        *reinterpret_cast<uint4*>(mp.codes + (p.f >> 1)) = make_uint4(w[0], w[1], w[2], w[3]);
+      } else {  // NVFP4 codes are 8-byte aligned only when cols % 32 == 16
+        uint2* dst = reinterpret_cast<uint2*>(mp.codes + (p.f >> 1));
+        dst[0] = make_uint2(w[0], w[1]);
+        if (p.live == 32) dst[1] = make_uint2(w[2], w[3]);
+      }
     }
     // each block's scale byte at its place in the tiled layout (rows and columns below 2^31;
     // the padding columns of the last 4-column group are zeroed after the loop)
@@ -523,7 +533,8 @@ __global__ void __launch_bounds__(kSThreads, SCfg<F32, NV != kMx>::kCtasPerSm)
       }
       const uint32_t sc = c >> (FMT == BSQ_NVFP4 ? 4 : 5);
       const uint64_t tile = static_cast<uint64_t>(r >> 7) * static_cast<uint64_t>(mp.nct) + (sc >> 2);
-      mp.scales[tile * 512 + (((r & 31u) << 4) | (((r >> 5) & 3u) << 2) | (sc & 3u))] = static_cast<uint8_t>(sb >> (8 * h));
+      const uint64_t so = tile * 512 + (((r & 31u) << 4) | (((r >> 5) & 3u) << 2) | (sc & 3u));
+      if (in_bounds(so < static_cast<uint64_t>(mp.scales_bytes), batch.status)) mp.scales[so] = static_cast<uint8_t>(sb >> (8 * h));
     }
   };
 
@@ -558,12 +569,14 @@ __global__ void __launch_bounds__(kSThreads, SCfg<F32, NV != kMx>::kCtasPerSm)
     const int64_t words = pad_rows * a.nct;
     for (int64_t wd = tid; wd < words; wd += nthr) {
       const int64_t r = a.rows + wd / a.nct, tc = wd % a.nct;
-      *reinterpret_cast<uint32_t*>(a.scales + scale_word_offset(r, 4 * tc, a.nct)) = 0u;
+      const int64_t so = scale_word_offset(r, 4 * tc, a.nct);
+      if (in_bounds(so + 4 <= a.scales_bytes, batch.status)) *reinterpret_cast<uint32_t*>(a.scales + so) = 0u;
     }
     const int64_t pad_cols = 4 * a.nct - a.nsc;
     for (int64_t i = tid; i < a.rows * pad_cols; i += nthr) {
       const int64_t r = i / pad_cols, c = a.nsc + i % pad_cols;
-      a.scales[scale_word_offset(r, c, a.nct) + (c & 3)] = 0;
+      const int64_t so = scale_word_offset(r, c, a.nct) + (c & 3);
+      if (in_bounds(so < a.scales_bytes, batch.status)) a.scales[so] = 0;
     }
   }
 }
@@ -615,9 +628,12 @@ __global__ void __launch_bounds__(QCfg::kThreads, QCfg::kCtasPerSm)
         if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1u, &abort_flag, batch.status, batch.wait_ns)) break;
         const int64_t r0 = c * a.rows_per_chunk;
         const int64_t nr = min(a.rows_per_chunk, a.rows - r0);
-        const uint32_t bytes = static_cast<uint32_t>(nr * a.cols * kEsize);
+        // a skipped (out-of-range) chunk still completes its stage, with no bytes
+        const bool ok = in_bounds(r0 >= 0 && nr > 0 && nr * a.cols * kEsize <= kChunkMax && (r0 + nr) <= a.rows,
+                                  batch.status);
+        const uint32_t bytes = ok ? static_cast<uint32_t>(nr * a.cols * kEsize) : 0u;
         mbar_arrive_expect_tx(&full_bar[stage], bytes);
-        bulk_load(ring + stage * kChunkMax, a.src + r0 * a.cols * kEsize, bytes, &full_bar[stage]);
+        if (ok) bulk_load(ring + stage * kChunkMax, a.src + r0 * a.cols * kEsize, bytes, &full_bar[stage]);
         ++armed;
         if (++stage == kRing) {
           stage = 0;
@@ -688,19 +704,25 @@ __global__ void __launch_bounds__(QCfg::kThreads, QCfg::kCtasPerSm)
           const uint64_t e = static_cast<uint64_t>(row) * static_cast<uint64_t>(a.cols) + static_cast<uint64_t>(cc);
           uint32_t w[FMT == BSQ_MXFP8 ? 8 : 4];
           const uint32_t sb = quantize32<FMT>(x, nv, w);
-          if constexpr (FMT == BSQ_MXFP8) {
-            uint4* dst = reinterpret_cast<uint4*>(a.codes + e);
-            dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-            dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-          } else {
-            *reinterpret_cast<uint4*>(a.codes + (e >> 1)) = make_uint4(w[0], w[1], w[2], w[3]);
+          const uint64_t cb = (FMT == BSQ_MXFP8) ? e : (e >> 1);
+          if (in_bounds(cb + (FMT == BSQ_MXFP8 ? 32 : 16) <= static_cast<uint64_t>(a.codes_bytes), batch.status)) {
+            if constexpr (FMT == BSQ_MXFP8) {
+              uint4* dst = reinterpret_cast<uint4*>(a.codes + e);
+              dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+              dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+            } else {
+              *reinterpret_cast<uint4*>(a.codes + (e >> 1)) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
           }
           const uint32_t sc = static_cast<uint32_t>(cc) >> 5;
-          uint8_t* sp = a.scales + static_cast<uint64_t>((row >> 7) * static_cast<uint32_t>(a.nct) + (sc >> 2)) * 512 +
-                        (((row & 31u) << 4) | (((row >> 5) & 3u) << 2) | (sc & 3u));
-          *sp = static_cast<uint8_t>(sb);
-          if (sc + 1 == static_cast<uint32_t>(a.nsc)) {
-            for (uint32_t j = (sc & 3u) + 1; j < 4; ++j) sp[j - (sc & 3u)] = 0;
+          const uint64_t so = static_cast<uint64_t>((row >> 7) * static_cast<uint32_t>(a.nct) + (sc >> 2)) * 512 +
+                              (((row & 31u) << 4) | (((row >> 5) & 3u) << 2) | (sc & 3u));
+          if (in_bounds(so + (4 - (sc & 3u)) <= static_cast<uint64_t>(a.scales_bytes), batch.status)) {
+            uint8_t* sp = a.scales + so;
+            *sp = static_cast<uint8_t>(sb);
+            if (sc + 1 == static_cast<uint32_t>(a.nsc)) {
+              for (uint32_t j = (sc & 3u) + 1; j < 4; ++j) sp[j - (sc & 3u)] = 0;
+            }
           }
         };
         if (nci <= 32 * kLaneElems) {
@@ -764,7 +786,8 @@ __global__ void __launch_bounds__(QCfg::kThreads, QCfg::kCtasPerSm)
   for (int64_t w = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; w < words;
        w += static_cast<int64_t>(gridDim.x) * kThreads) {
     const int64_t r = a.rows + w / a.nct, tc = w % a.nct;
-    *reinterpret_cast<uint32_t*>(a.scales + scale_word_offset(r, 4 * tc, a.nct)) = 0u;
+    const int64_t so = scale_word_offset(r, 4 * tc, a.nct);
+    if (in_bounds(so + 4 <= a.scales_bytes, batch.status)) *reinterpret_cast<uint32_t*>(a.scales + so) = 0u;
   }
 }
 
@@ -897,6 +920,8 @@ void fill_args(QuantArgs& a, int fmt, const QuantItem& it) {
   a.nct = ceil_div(a.nsc, 4);
   a.cols_magic = static_cast<uint32_t>((uint64_t{1} << 32) / static_cast<uint64_t>(it.cols) + 1);
   a.cols_magic64 = ~uint64_t{0} / static_cast<uint64_t>(it.cols);
+  a.codes_bytes = fmt == BSQ_MXFP8 ? a.elems : a.elems / 2;
+  a.scales_bytes = scales_body_bytes(fmt, it.rows, it.cols);
   if (fmt == BSQ_NVFP4) {
     a.tail = reinterpret_cast<uint32_t*>(a.scales + scales_body_bytes(fmt, it.rows, it.cols));
     a.g_in = it.global_scale;

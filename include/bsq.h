@@ -56,6 +56,8 @@ typedef enum { BSQ_MXFP8 = 1, BSQ_NVFP4 = 2, BSQ_MXFP4 = 3 } bsq_format;
 #define BSQ_ERR_ARCH -4    /* no CUDA device, or not compute capability 10.3 */
 #define BSQ_ERR_LAUNCH -5  /* the CUDA runtime reported an error at launch */
 #define BSQ_ERR_TIMEOUT -6 /* a kernel's bounded wait gave up (device status only) */
+#define BSQ_ERR_DEVICE_CHECK -7 /* checked build (libbsq_checked.so) only: a kernel's index check
+                                   failed and the access was skipped (device status only) */
 
 /*
  * bsq_codes_bytes: size of the element-code buffer of a rows x cols matrix.
@@ -334,8 +336,13 @@ int bsq_convt2x2(int fmt, const void* A, const void* A_scales, const void* B, co
 /*
  * bsq_get_device_status: synchronise `stream`, then read and clear the current device's
  * status word. Returns BSQ_OK, BSQ_ERR_TIMEOUT (a kernel's bounded wait on an mbarrier
- * gave up; that kernel returned early and its outputs are incomplete) or BSQ_ERR_LAUNCH
- * (a CUDA error while synchronising).
+ * gave up; that kernel returned early and its outputs are incomplete), BSQ_ERR_DEVICE_CHECK (the
+ * checked build only: a kernel computed an index outside one of its buffers and skipped that
+ * access) or BSQ_ERR_LAUNCH (a CUDA error while synchronising).
+ * The checked build, libbsq_checked.so, is the same library compiled with BSQ_DEVICE_CHECKS=1:
+ * every global load or store whose address a kernel computes itself (not the tensor copies, which
+ * the tensor maps bound) is tested against its buffer's size first. It is the stand-in for a
+ * memory checker.
  */
 int bsq_get_device_status(bsq_stream_t stream);
 
@@ -346,6 +353,14 @@ int bsq_get_device_status(bsq_stream_t stream);
  * every bounded wait without faulting or hanging the GPU. limit_ns in [1e3, 1e10].
  */
 int bsq_selftest_timeout(int64_t limit_ns, bsq_stream_t stream);
+
+/*
+ * bsq_selftest_device_check: enqueue a one-thread kernel whose single index check fails. The
+ * checked build (libbsq_checked.so) records BSQ_ERR_DEVICE_CHECK in the device status word; the
+ * normal build, whose checks compile to nothing, records nothing. Shows which build is loaded and
+ * that its checks report through the status word without a trap.
+ */
+int bsq_selftest_device_check(bsq_stream_t stream);
 
 /*
  * bsq_test_inject_stall: a test of the failure path of the kernels that wait on barriers, with no

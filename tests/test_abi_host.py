@@ -164,3 +164,13 @@ def test_stall_injection_argument_errors(bsq):
     assert inj(bsq.KERNEL_LAYERNORM, 1, 10**10 + 1) == bsq.ERR_ARG
     assert inj(bsq.KERNEL_GEMM, 0, 10**6) == bsq.OK   # armed for this thread's next GEMM launch
     assert inj(bsq.KERNEL_GEMM, -1, 10**6) == bsq.OK  # disarmed again
+
+
+def test_checked_build_exports_the_same_symbols(bsq):
+    spec = importlib.util.spec_from_file_location("_bsq_build2", os.path.join(ROOT, "block_scaled_precision_bsq_gb300",
+                                                                             "build.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    lib = ctypes.CDLL(mod.build(checked=True))
+    for n in declared_functions():
+        assert hasattr(lib, n), n
