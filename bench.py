@@ -352,18 +352,124 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(kernel_hash: str, workload: str, kernel: str):
-    """DRAM bytes per step of `kernel`'s launches (read + write, from the committed ncu summary
-    `profiles/traffic.json`), if the capture was taken on the current kernel sources; else None."""
-    p = os.path.join(ROOT, "profiles", "traffic.json")
-    if not os.path.exists(p):
+TRAFFIC_PATH = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+def kernel_class(name: str):
+    """The bench's kernel class of a launch in an ncu launch list: "gemm" for the GEMM kernels,
+    "quantize" for the library's other kernels, None for anything else (the L2 flush, copies)."""
+    if "bsq::" not in name:
         return None
-    with open(p) as f:
+    return "gemm" if ("gemm" in name or "splitk" in name) else "quantize"
+
+
+def recorded_traffic(kernel_hash: str, workload: str, cls: str, path: str = TRAFFIC_PATH):
+    """DRAM bytes (read + write) per step of kernel class `cls`, from the ncu record
+    `profiles/traffic.json` (written by --record-traffic), if that capture was taken on the
+    current kernel sources; else None."""
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
         d = json.load(f)
-    e = d.get(workload, {}).get(kernel)
+    e = d.get(workload)
     if not e or e.get("kernel_source_hash") != kernel_hash:
         return None
-    return e.get("dram_bytes_per_step")
+    return e.get("classes", {}).get(cls, {}).get("dram_bytes_per_step")
+
+
+def traffic_capture(args):
+    """--traffic-capture SIDECAR: the workload's step `--warmup` times through the direct library
+    calls, each after an L2 flush, nothing else on the device; for an ncu launch list with DRAM
+    counters (`ncu --metrics gpu__time_duration.sum,dram__bytes_read.sum,dram__bytes_write.sum
+    --csv`). Writes SIDECAR: the workload, the number of steps run and the kernel source hash,
+    which --record-traffic needs to turn the launch list into bytes per step."""
+    import torch
+
+    import __graft_entry__ as ge
+
+    ge.build()
+    import block_scaled_precision_bsq_gb300 as bsq
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    wl = WORKLOADS[args.workload]
+    layers = args.layers.split(",") if args.layers else None
+    units = build_units(wl, bsq, dev, layers)
+    assert units, "no layer of %s is named %s" % (wl.name, args.layers)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    s = torch.cuda.current_stream()
+    torch.cuda.synchronize()
+    for _ in range(args.warmup):
+        flush.zero_()
+        for U in units:
+            U["quant"](U["D"], s)
+            U["gemm"](U["D"], s)
+        torch.cuda.synchronize()
+    assert bsq.device_status() == 0
+    with open(args.traffic_capture, "w") as f:
+        json.dump({"workload": wl.name + ("[%s]" % args.layers if args.layers else ""), "steps": args.warmup,
+                   "kernel_source_hash": kernel_source_hash(),
+                   "launches_per_step": sum(U["launches"] for U in units)}, f)
+    return 0
+
+
+def record_traffic(csv_path: str, sidecar_path: str, command: str, out_path: str = TRAFFIC_PATH):
+    """--record-traffic CSV SIDECAR: per kernel class, the DRAM bytes per step of a
+    --traffic-capture run's ncu launch list, into profiles/traffic.json under the workload."""
+    import csv
+    import re
+
+    with open(sidecar_path) as f:
+        side = json.load(f)
+    with open(csv_path, newline="") as f:
+        rows = [r for r in csv.reader(f)]
+    head = next(i for i, r in enumerate(rows) if "Kernel Name" in r and "Metric Name" in r)
+    h = rows[head]
+    col = {k: h.index(k) for k in ("ID", "Kernel Name", "Metric Name", "Metric Unit", "Metric Value")}
+    scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "ns": 1e-3, "nsecond": 1e-3, "us": 1.0,
+             "usecond": 1.0, "ms": 1e3, "msecond": 1e3}
+    launches = {}
+    for r in rows[head + 1:]:
+        if len(r) < len(h):
+            continue
+        e = launches.setdefault(r[col["ID"]], {"name": r[col["Kernel Name"]]})
+        e[r[col["Metric Name"]]] = float(r[col["Metric Value"]].replace(",", "")) * scale[r[col["Metric Unit"]]]
+    steps = side["steps"]
+    ours = [e for e in launches.values() if kernel_class(e["name"]) is not None]
+    if len(ours) != steps * side["launches_per_step"]:
+        raise SystemExit("launch list holds %d library launches, expected %d steps x %d" % (
+            len(ours), steps, side["launches_per_step"]))
+    classes, kernels = {}, {}
+    for e in ours:
+        b = e["dram__bytes_read.sum"] + e["dram__bytes_write.sum"]
+        for d, key in ((classes, kernel_class(e["name"])), (kernels, re.sub(r"\(.*", "", e["name"]).replace(
+                "void ", "").replace("bsq::<unnamed>::", ""))):
+            a = d.setdefault(key, {"launches": 0, "dram_read": 0.0, "dram_write": 0.0, "us": 0.0})
+            a["launches"] += 1
+            a["dram_read"] += e["dram__bytes_read.sum"]
+            a["dram_write"] += e["dram__bytes_write.sum"]
+            a["us"] += e["gpu__time_duration.sum"]
+    def per_step(a):
+        return {"launches_per_step": a["launches"] / steps,
+                "dram_bytes_per_step": int(round((a["dram_read"] + a["dram_write"]) / steps)),
+                "dram_read_per_step": int(round(a["dram_read"] / steps)),
+                "dram_write_per_step": int(round(a["dram_write"] / steps)),
+                "ncu_us_per_step": a["us"] / steps}
+    d = {}
+    if os.path.exists(out_path):
+        with open(out_path) as f:
+            d = json.load(f)
+    d[side["workload"]] = {
+        "kernel_source_hash": side["kernel_source_hash"], "steps_captured": steps, "command": command,
+        "note": "ncu launch list (one pass, --clock-control none): cold-cache, serialised launches; the "
+                "first launch of each step follows a 256 MB L2 flush whose dirty lines it writes back",
+        "classes": {k: per_step(v) for k, v in sorted(classes.items())},
+        "kernels": {k: per_step(v) for k, v in sorted(kernels.items())}}
+    with open(out_path, "w") as f:
+        json.dump(d, f, indent=1, sort_keys=True)
+        f.write("\n")
+    print(json.dumps(d[side["workload"]]["classes"]))
+    return 0
 
 
 def _host(x):
@@ -374,15 +480,18 @@ def _host(x):
     return (t.view(torch.bfloat16) if x.dtype == np.uint16 else t).pin_memory()
 
 
-def build_units(wl, bsq, dev):
+def build_units(wl, bsq, dev, layers=None):
     """The step of workload `wl` as units: one per linear layer (or one per chained MLP /
     training step). A unit holds its pinned host inputs, an `alloc` making one device buffer set
-    (e2e double-buffers them), its quantize and GEMM phases, and its flops / algorithmic bytes."""
+    (e2e double-buffers them), its quantize and GEMM phases, and its flops / algorithmic bytes.
+    `layers`: the names of the layers to keep (unchained workloads; for profiling one layer)."""
     import torch
 
     units = []
     if wl.chain is None:
         for g in wl.gemms:
+            if layers and g.name not in layers:
+                continue
             bias = make_bias(g)
             hosts = {"a": _host(make_activations(g)), "b": _host(make_weights(g)),
                      "bias": _host(bias) if bias is not None else None}
@@ -408,6 +517,7 @@ def build_units(wl, bsq, dev):
 
             units.append({"name": g.name, "gemms": [g], "hosts": hosts, "alloc": alloc, "quant": quant, "gemm": gemm,
                           "fmt": g.fmt, "flops": g.flops, "launches": 2 + (2 if g.fmt == NVFP4 else 0),
+                          "qkernels": ["stream_kernel"] + (["amax_kernel"] if g.fmt == NVFP4 else []),
                           "qbytes": quant_bytes(g.fmt, g.M, g.K, 4 if g.src_f32 else 2, True) +
                                     quant_bytes(g.fmt, g.N, g.K, 4 if g.src_f32 else 2, True),
                           "gbytes": gemm_bytes(g.fmt, g.M, g.N, g.K, bias is not None)})
@@ -456,6 +566,8 @@ def build_units(wl, bsq, dev):
         nv = fmt == NVFP4
         units.append({"name": "train_step", "gemms": [g, g, g], "hosts": hosts, "alloc": alloc, "quant": quant,
                       "gemm": gemm, "fmt": fmt, "flops": 3 * g.flops, "outs": ("out", "dx", "dw"),
+                      "qkernels": ["dual_kernel"] + (["amax_kernel"] if nv else []) +
+                                  (["delayed_scale_kernel"] if delayed else []),
                       # duals + GEMMs (+ the split-K sum); NVFP4: amax passes of X and W, the delayed-scale kernel
                       "launches": 6 + (1 if dw_splits > 1 else 0) + (2 if nv else 0) + (1 if delayed else 0) +
                                   (1 if nv and not delayed else 0),
@@ -501,6 +613,8 @@ def build_units(wl, bsq, dev):
 
         units.append({"name": "mlp", "gemms": [g1, g2], "hosts": hosts, "alloc": alloc, "quant": quant, "gemm": gemm,
                       "fmt": fmt, "flops": g1.flops + g2.flops, "launches": (4 if ln else 3) if fused else 4,
+                      "qkernels": (["layernorm_kernel"] if ln else []) + ["stream_kernel"] +
+                                  (["amax_kernel"] if fmt == NVFP4 else []),
                       "qbytes": sum(quant_bytes(fmt, r, c, 2, True) for r, c in ((g1.M, g1.K), (g1.N, g1.K), (g2.N, g2.K))),
                       "gbytes": gemm_bytes(fmt, g1.M, g1.N, g1.K, True) + gemm_bytes(fmt, g2.M, g2.N, g2.K, True) -
                                 (2 * g1.M * g1.N if fused else 0) +
@@ -694,7 +808,7 @@ def run_gpu(args, rank: int, world: int):
     fmts = sorted({FMT_NAME[U["fmt"]] for U in units})
     khash = kernel_source_hash()
     gemm_roof = {"bound": "tensor", "achieved": gemm_tflops, "peak": peak_tc, "unit": "TFLOP/s",
-                 "frac": gemm_tflops / peak_tc, "traffic": recorded_traffic(khash, wl.name, "gemm_kernel"),
+                 "frac": gemm_tflops / peak_tc, "traffic": recorded_traffic(khash, wl.name, "gemm"),
                  "peak_source": "%s bf16 %.1f TFLOP/s x nominal ratio (%s)" % (
                      peak_src, peak_bf16, ", ".join("%s x%.0f" % (f, NOMINAL_RATIO[f]) for f in fmts)),
                  "attainable_frac": t_ideal / (gemm_ms * 1e-3), "kernel": "gemm_kernel",
@@ -706,7 +820,8 @@ def run_gpu(args, rank: int, world: int):
     q_gbs = q_bytes / (q_ms_mean * 1e-3) / 1e9
     quant = {"bound": "hbm", "achieved": q_gbs, "unit": "GB/s", "peak": hbm, "frac": q_gbs / hbm,
              "ms_per_step": q_ms_mean, "bytes_per_step": q_bytes, "peak_source": "%s HBM copy" % peak_src,
-             "traffic": recorded_traffic(khash, wl.name, "quantize_kernel"), "kernel": "quantize_kernel",
+             "traffic": recorded_traffic(khash, wl.name, "quantize"), "kernel": "quantize (%s)" % ", ".join(
+                 sorted({k for U in units for k in U["qkernels"]})),
              "per_launch": "all quantizer launches of a step together (NVFP4 with a computed per-tensor "
                            "scale: its amax pass included): algorithmic bytes / summed event times"}
     # the dominant kernel class: the larger share of the split step
@@ -816,7 +931,17 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="size of the CPU oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-other-configs", action="store_true", help="skip timing the non-headline configurations")
+    ap.add_argument("--traffic-capture", metavar="SIDECAR",
+                    help="run --warmup steps for an ncu launch list with DRAM counters, write SIDECAR, print nothing")
+    ap.add_argument("--record-traffic", nargs=2, metavar=("CSV", "SIDECAR"),
+                    help="turn a --traffic-capture run's ncu CSV into profiles/traffic.json (no GPU)")
+    ap.add_argument("--traffic-command", default="", help="the capture's command line, stored with the record")
+    ap.add_argument("--layers", help="with --traffic-capture: only these layers (comma-separated names)")
     args = ap.parse_args()
+    if args.record_traffic:
+        return record_traffic(args.record_traffic[0], args.record_traffic[1], args.traffic_command)
+    if args.traffic_capture:
+        return traffic_capture(args)
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be >= 3")
 

@@ -323,18 +323,23 @@ __device__ __forceinline__ uint32_t quantize32(const float (&x)[32], const NvCtx
 // blocks: a piece never crosses a row for MX, cols being a multiple of 32; an NVFP4 piece may
 // when cols % 32 == 16, and each block then finds its own row). Warps walk the concatenated step
 // list with a grid-wide stride, each lane loading its piece straight from global memory into
-// registers (two 32-byte loads for bf16, whole sectors) one step ahead of the piece it
-// quantizes: no shared-memory staging, no barriers, so nearly every instruction is the
-// element arithmetic. After the NVFP4 amax pass (which reads every source front to back) the
-// step list is walked back to front, to meet the lines still in L2.
-// Resident CTAs per SM: three for the MX formats from bf16 (up to 80 registers), two for NVFP4 and
-// fp32 sources (up to 128: NVFP4's exact fallback stays inline without spilling). Measured on
-// GB300 (51200 x 4096 bf16, L2 flushed): NVFP4 201.6 us with two against 203.7 us with three and
-// the fallback out of line; MXFP8 103.3 us with three against 115.8 with two and 110.8 with four.
+// registers (two 32-byte loads for bf16, whole sectors): no shared-memory staging, no barriers, so
+// nearly every instruction is the element arithmetic. After the NVFP4 amax pass (which reads
+// every source front to back) the step list is walked back to front, to meet the lines still in
+// L2.
+// Latency hiding, per SM: the MX formats from bf16 load each piece one step ahead of the piece
+// they quantize, with three CTAs (up to 80 registers); NVFP4 from bf16 keeps no second piece in
+// registers and relies on three CTAs (up to 80 registers) alone; fp32 sources prefetch with two
+// CTAs (up to 128). Measured on GB300 (51200 x 4096 bf16, L2 flushed): NVFP4 (amax pass
+// included) 192 us this way against 200 us with the prefetch at two CTAs, 191-230 us at 128
+// threads per CTA with 4 to 6 CTAs; MXFP8 103.3 us with three CTAs against 115.8 with two and
+// 110.8 with four. A deeper prefetch ring in shared memory (cp.async, 2 to 8 pieces per thread)
+// gained nothing for NVFP4 and lost 8-10% for the MX formats.
 constexpr int kSThreads = 256;
 template <bool F32, bool NV>
 struct SCfg {
-  static constexpr int kCtasPerSm = (F32 || NV) ? 2 : 3;
+  static constexpr bool kPrefetch = F32 || !NV;
+  static constexpr int kCtasPerSm = F32 ? 2 : 3;
 };
 constexpr int kSWarps = kSThreads / 32;
 
@@ -538,19 +543,27 @@ __global__ void __launch_bounds__(kSThreads, SCfg<F32, NV != kMx>::kCtasPerSm)
     }
   };
 
-  // two piece buffers, alternating: the next step's loads are in flight while this one is
-  // quantized
   Piece<F32> pa, pb;
   int64_t k = static_cast<int64_t>(blockIdx.x) * kSWarps + warp;
-  if (k < nsteps) fetch(pa, step_of(k));
-  while (k < nsteps) {
-    if (k + nw < nsteps) fetch(pb, step_of(k + nw));
-    process(pa);
-    k += nw;
-    if (k >= nsteps) break;
-    if (k + nw < nsteps) fetch(pa, step_of(k + nw));
-    process(pb);
-    k += nw;
+  if constexpr (SCfg<F32, NV != kMx>::kPrefetch) {
+    // two piece buffers, alternating: the next step's loads are in flight while this one is
+    // quantized
+    if (k < nsteps) fetch(pa, step_of(k));
+    while (k < nsteps) {
+      if (k + nw < nsteps) fetch(pb, step_of(k + nw));
+      process(pa);
+      k += nw;
+      if (k >= nsteps) break;
+      if (k + nw < nsteps) fetch(pa, step_of(k + nw));
+      process(pb);
+      k += nw;
+    }
+  } else {
+    // one buffer: the loads of other warps cover this warp's quantization
+    for (; k < nsteps; k += nw) {
+      fetch(pa, step_of(k));
+      process(pa);
+    }
   }
   if constexpr (NV == kNvGiven) {
     // the last matrix's share of |x| maxima -> its tail word 1
