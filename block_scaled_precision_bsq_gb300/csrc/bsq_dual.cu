@@ -716,7 +716,9 @@ int launch_quantize_dual(int fmt, bool src_f32, bool stochastic, bool global_giv
     a.g_out = global_given ? nullptr : global_scale;
     if (cudaMemsetAsync(a.row_tail, 0, 16, stream) != cudaSuccess) return BSQ_ERR_LAUNCH;
     if (cudaMemsetAsync(a.col_tail, 0, 16, stream) != cudaSuccess) return BSQ_ERR_LAUNCH;
-    if (!global_given && launch_amax(src, src_f32, rows * cols, a.row_tail + 1, stream, dev) != BSQ_OK)
+    const int64_t elems = rows * cols;
+    uint32_t* amax_out = a.row_tail + 1;
+    if (!global_given && launch_amax(&src, &elems, &amax_out, 1, src_f32, stream, dev) != BSQ_OK)
       return BSQ_ERR_LAUNCH;
   }
   CUtensorMap map, col_map;

@@ -76,10 +76,11 @@ using QuantItem = bsq_quant_item;
 int launch_quantize_batch(int fmt, bool src_f32, bool global_given, int count, const QuantItem* items,
                           cudaStream_t stream, const DeviceInfo& dev);
 
-// Largest |x| of `elems` bf16 / fp32 values (elems * size a multiple of 16 bytes), atomically
-// max-ed into *out as fp32 bits (out must hold 0 or an earlier maximum).
-int launch_amax(const void* src, bool src_f32, int64_t elems, uint32_t* out, cudaStream_t stream,
-                const DeviceInfo& dev);
+// For each of n (1..BSQ_MAX_BATCH) sources: the largest |x| of its elems[i] bf16 / fp32 values
+// (elems * size a multiple of 16 bytes), atomically max-ed into *outs[i] as fp32 bits (which
+// must hold 0 or an earlier maximum). One launch.
+int launch_amax(const void* const* srcs, const int64_t* elems, uint32_t* const* outs, int n, bool src_f32,
+                cudaStream_t stream, const DeviceInfo& dev);
 
 // g_out = fp32(fp32(amax * headroom) / 2688), amax from the tail of an NVFP4 scale buffer of a
 // rows x cols matrix.

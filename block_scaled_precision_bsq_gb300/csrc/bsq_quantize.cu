@@ -67,6 +67,7 @@ struct QuantArgs {
   int64_t elems;        // rows * cols
   int64_t codes_bytes;  // sizes of the code buffer and of the tiled scale body (index checks)
   int64_t scales_bytes;
+  bool scale_words;     // NVFP4 with cols a multiple of 64: scale bytes stored as words
   // LayerNorm mode: y = (x - mean) / sqrt(var + eps) * gamma + beta per row before quantizing
   const uint16_t* gamma;  // cols bf16
   const uint16_t* beta;   // cols bf16
@@ -385,6 +386,7 @@ struct Mat {
   uint64_t magic;
   bool aligned32;
   int64_t codes_bytes, scales_bytes;
+  bool words;  // NVFP4: every 4-column group of scale bytes lies in one row and one lane pair
 };
 
 __device__ __forceinline__ Mat find_mat(const QuantBatch& b, int64_t s) {
@@ -405,6 +407,7 @@ __device__ __forceinline__ Mat find_mat(const QuantBatch& b, int64_t s) {
   m.aligned32 = (reinterpret_cast<uintptr_t>(a.src) & 31u) == 0u;
   m.codes_bytes = a.codes_bytes;
   m.scales_bytes = a.scales_bytes;
+  m.words = a.scale_words;
   return m;
 }
 
@@ -479,9 +482,9 @@ __global__ void __launch_bounds__(kSThreads, SCfg<F32, NV != kMx>::kCtasPerSm)
         }
       }
     }
-    if (p.live == 0) return;
+    const bool live = p.live != 0;  // lanes past the matrix's end still take part in the shuffles
     uint32_t w[FMT == BSQ_MXFP8 ? 8 : 4];
-    uint32_t sb;
+    uint32_t sb = 0;
     // the piece's values as fp32 (exact path): fp32 sources, and NVFP4 blocks whose quotient step is
     // not valid
     auto exact = [&]() {
@@ -499,47 +502,68 @@ __global__ void __launch_bounds__(kSThreads, SCfg<F32, NV != kMx>::kCtasPerSm)
       if constexpr (F32 && NV == kNvGiven) run_max = max(run_max, __float_as_uint(abs_max<32>(x)));
       sb = quantize32<FMT>(x, nv, w);
     };
-    if constexpr (F32) {
-      exact();
-    } else if constexpr (FMT == BSQ_NVFP4) {
-      if constexpr (NV == kNvGiven) run_max = max(run_max, __float_as_uint(bf16_block_amax<16>(p.w)));
-      if (!nv_piece_bf16(p.w, nv, w, sb)) exact();
-    } else {
-      sb = mx_piece_bf16<FMT>(p.w, w);
-    }
-    const int64_t cb = (FMT == BSQ_MXFP8) ? p.f : (p.f >> 1);  // first code byte of the piece
-    const int64_t cn = (FMT == BSQ_MXFP8) ? 32 : p.live / 2;  // code bytes of the piece
-    if (in_bounds(cb >= 0 && cb + cn <= mp.codes_bytes, batch.status)) {
-      if constexpr (FMT == BSQ_MXFP8) {
-        uint4* dst = reinterpret_cast<uint4*>(mp.codes + p.f);
-        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-      } else if constexpr (FMT == BSQ_MXFP4) {
-        *reinterpret_cast<uint4*>(mp.codes + (p.f >> 1)) = make_uint4(w[0], w[1], w[2], w[3]);
-      } else {  // NVFP4 codes are 8-byte aligned only when cols % 32 == 16
-        uint2* dst = reinterpret_cast<uint2*>(mp.codes + (p.f >> 1));
-        dst[0] = make_uint2(w[0], w[1]);
-        if (p.live == 32) dst[1] = make_uint2(w[2], w[3]);
+    if (live) {
+      if constexpr (F32) {
+        exact();
+      } else if constexpr (FMT == BSQ_NVFP4) {
+        if constexpr (NV == kNvGiven) run_max = max(run_max, __float_as_uint(bf16_block_amax<16>(p.w)));
+        if (!nv_piece_bf16(p.w, nv, w, sb)) exact();
+      } else {
+        sb = mx_piece_bf16<FMT>(p.w, w);
+      }
+      // codes: the piece's 32 (E4M3) or 16 (e2m1; 8 if only the first NVFP4 block is present)
+      // bytes at code byte f (E4M3) or f / 2, 16-byte aligned since f is a multiple of 32
+      const int64_t cb = (FMT == BSQ_MXFP8) ? p.f : (p.f >> 1);
+      const int64_t cn = (FMT == BSQ_MXFP8) ? 32 : p.live / 2;
+      if (in_bounds(cb >= 0 && cb + cn <= mp.codes_bytes, batch.status)) {
+        if constexpr (FMT == BSQ_MXFP8) {
+          uint4* dst = reinterpret_cast<uint4*>(mp.codes + cb);
+          dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+          dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        } else if (p.live == 32) {
+          *reinterpret_cast<uint4*>(mp.codes + cb) = make_uint4(w[0], w[1], w[2], w[3]);
+        } else {
+          *reinterpret_cast<uint2*>(mp.codes + cb) = make_uint2(w[0], w[1]);
+        }
       }
     }
-    // each block's scale byte at its place in the tiled layout (rows and columns below 2^31;
-    // the padding columns of the last 4-column group are zeroed after the loop)
-    const int64_t row64 = div_cols(p.f, mp.cols, mp.magic);
-    const uint32_t row = static_cast<uint32_t>(row64);
-    const uint32_t col = static_cast<uint32_t>(p.f - row64 * mp.cols);
-    constexpr int kBlocks = FMT == BSQ_NVFP4 ? 2 : 1;
+    // scale bytes at their places in the tiled layout (rows and columns below 2^31)
+    if (FMT == BSQ_NVFP4 && mp.words) {
+      // cols a multiple of 64: the 4 scale bytes of each aligned 4-column group of a row are the
+      // two blocks of an even lane and of the next lane, whose 32-bit word the even lane stores
+      // (one store where there were four byte stores into the same word; measured on GB300 the
+      // same for MXFP4 / MXFP8 with 4-lane groups, so those keep their byte stores)
+      const uint32_t v = sb & 0xFFFFu;
+      const uint32_t word = v | (__shfl_down_sync(0xFFFFFFFFu, v, 1) << 16);
+      if (live && (lane & 1u) == 0u) {
+        const int64_t row64 = div_cols(p.f, mp.cols, mp.magic);
+        const uint32_t r = static_cast<uint32_t>(row64);
+        const uint32_t sc = static_cast<uint32_t>(p.f - row64 * mp.cols) >> 4;
+        const uint64_t tile = static_cast<uint64_t>(r >> 7) * static_cast<uint64_t>(mp.nct) + (sc >> 2);
+        const uint64_t so = tile * 512 + (((r & 31u) << 4) | (((r >> 5) & 3u) << 2));
+        if (in_bounds(so + 4 <= static_cast<uint64_t>(mp.scales_bytes), batch.status))
+          *reinterpret_cast<uint32_t*>(mp.scales + so) = word;
+      }
+    } else if (live) {
+      // byte stores (the padding columns of the last 4-column group are zeroed after the loop)
+      const int64_t row64 = div_cols(p.f, mp.cols, mp.magic);
+      const uint32_t row = static_cast<uint32_t>(row64);
+      const uint32_t col = static_cast<uint32_t>(p.f - row64 * mp.cols);
+      constexpr int kBlocks = FMT == BSQ_NVFP4 ? 2 : 1;
 #pragma unroll
-    for (int h = 0; h < kBlocks; ++h) {
-      if (h == 1 && p.live != 32) break;
-      uint32_t r = row, c = col + 16u * h;
-      if (FMT == BSQ_NVFP4 && c >= static_cast<uint32_t>(mp.cols)) {  // cols % 32 == 16: the next row
-        c -= static_cast<uint32_t>(mp.cols);
-        ++r;
+      for (int h = 0; h < kBlocks; ++h) {
+        if (h == 1 && p.live != 32) break;
+        uint32_t r = row, c = col + 16u * h;
+        if (FMT == BSQ_NVFP4 && c >= static_cast<uint32_t>(mp.cols)) {  // cols % 32 == 16: the next row
+          c -= static_cast<uint32_t>(mp.cols);
+          ++r;
+        }
+        const uint32_t sc = c >> (FMT == BSQ_NVFP4 ? 4 : 5);
+        const uint64_t tile = static_cast<uint64_t>(r >> 7) * static_cast<uint64_t>(mp.nct) + (sc >> 2);
+        const uint64_t so = tile * 512 + (((r & 31u) << 4) | (((r >> 5) & 3u) << 2) | (sc & 3u));
+        if (in_bounds(so < static_cast<uint64_t>(mp.scales_bytes), batch.status))
+          mp.scales[so] = static_cast<uint8_t>(sb >> (8 * h));
       }
-      const uint32_t sc = c >> (FMT == BSQ_NVFP4 ? 4 : 5);
-      const uint64_t tile = static_cast<uint64_t>(r >> 7) * static_cast<uint64_t>(mp.nct) + (sc >> 2);
-      const uint64_t so = tile * 512 + (((r & 31u) << 4) | (((r >> 5) & 3u) << 2) | (sc & 3u));
-      if (in_bounds(so < static_cast<uint64_t>(mp.scales_bytes), batch.status)) mp.scales[so] = static_cast<uint8_t>(sb >> (8 * h));
     }
   };
 
@@ -804,45 +828,60 @@ __global__ void __launch_bounds__(QCfg::kThreads, QCfg::kCtasPerSm)
   }
 }
 
-// Tensor amax (NVFP4 computed-scale mode): max |x| over the tensor, NaN skipped like the block
-// maxima -> atomicMax on the fp32 bits at `out` (non-negative floats order like their bit
-// patterns). Reads use the default cache policy so that the quantize pass that follows finds
-// the tensor in L2 when it fits.
+// Tensor amax (NVFP4 computed-scale mode) of every matrix of a list: max |x| over each tensor,
+// NaN skipped like the block maxima -> atomicMax on the fp32 bits at its `out` (non-negative
+// floats order like their bit patterns). The CTAs stride over each matrix in turn, so one launch
+// serves a whole batch. Reads use the default cache policy so that the quantize pass that
+// follows finds the most recently read lines in L2.
+struct AmaxList {
+  const uint4* src[kMaxBatch];
+  int64_t nvec[kMaxBatch];  // 16-byte vectors of each source
+  uint32_t* out[kMaxBatch];
+  int n;
+};
+
 template <bool F32>
-__global__ void __launch_bounds__(kAmaxThreads) amax_kernel(const uint4* src, int64_t nvec, uint32_t* out) {
+__global__ void __launch_bounds__(kAmaxThreads) amax_kernel(const __grid_constant__ AmaxList list) {
   constexpr int kU = 4;
-  float m = 0.0f;
+  __shared__ float red[kAmaxThreads / 32];
+  launch_dependents();
+  grid_dependency_wait();  // the sources and the zeroed tails may belong to earlier work until here
   const int64_t tid = static_cast<int64_t>(blockIdx.x) * kAmaxThreads + threadIdx.x;
   const int64_t nthr = static_cast<int64_t>(gridDim.x) * kAmaxThreads;
-  for (int64_t i = tid; i < nvec; i += nthr * kU) {
-    uint4 v[kU];
+  for (int t = 0; t < list.n; ++t) {
+    const uint4* src = list.src[t];
+    const int64_t nvec = list.nvec[t];
+    float m = 0.0f;
+    for (int64_t i = tid; i < nvec; i += nthr * kU) {
+      uint4 v[kU];
 #pragma unroll
-    for (int u = 0; u < kU; ++u) {
-      const int64_t j = i + u * nthr;
-      v[u] = j < nvec ? __ldg(src + j) : make_uint4(0, 0, 0, 0);
-    }
+      for (int u = 0; u < kU; ++u) {
+        const int64_t j = i + u * nthr;
+        v[u] = j < nvec ? __ldg(src + j) : make_uint4(0, 0, 0, 0);
+      }
 #pragma unroll
-    for (int u = 0; u < kU; ++u) {
-      const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+      for (int u = 0; u < kU; ++u) {
+        const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        if constexpr (F32) {
-          m = fmaxf(m, fabsf(__uint_as_float(w[q])));
-        } else {
-          m = fmaxf(m, fmaxf(fabsf(__uint_as_float(w[q] << 16)), fabsf(__uint_as_float(w[q] & 0xFFFF0000u))));
+        for (int q = 0; q < 4; ++q) {
+          if constexpr (F32) {
+            m = fmaxf(m, fabsf(__uint_as_float(w[q])));
+          } else {
+            m = fmaxf(m, fmaxf(fabsf(__uint_as_float(w[q] << 16)), fabsf(__uint_as_float(w[q] & 0xFFFF0000u))));
+          }
         }
       }
     }
-  }
-  __shared__ float red[kAmaxThreads / 32];
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    float b = 0.0f;
-    for (int i = 0; i < kAmaxThreads / 32; ++i) b = fmaxf(b, red[i]);
-    atomicMax(out, __float_as_uint(b));
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float b = 0.0f;
+      for (int i = 0; i < kAmaxThreads / 32; ++i) b = fmaxf(b, red[i]);
+      if (b != 0.0f) atomicMax(list.out[t], __float_as_uint(b));
+    }
+    __syncthreads();  // red[] is reused by the next matrix
   }
 }
 
@@ -912,13 +951,22 @@ int launch_delayed_scale(const void* prev_scales, int64_t rows, int64_t cols, fl
                                                                                             : BSQ_ERR_LAUNCH;
 }
 
-int launch_amax(const void* src, bool src_f32, int64_t elems, uint32_t* out, cudaStream_t stream,
-                const DeviceInfo& dev) {
-  const int64_t nvec = elems * (src_f32 ? 4 : 2) / 16;
-  const int agrid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(ceil_div(nvec, kAmaxThreads * 4), dev.num_sms * 8)));
-  if (src_f32) amax_kernel<true><<<agrid, kAmaxThreads, 0, stream>>>(static_cast<const uint4*>(src), nvec, out);
-  else amax_kernel<false><<<agrid, kAmaxThreads, 0, stream>>>(static_cast<const uint4*>(src), nvec, out);
-  return cudaGetLastError() == cudaSuccess ? BSQ_OK : BSQ_ERR_LAUNCH;
+int launch_amax(const void* const* srcs, const int64_t* elems, uint32_t* const* outs, int n, bool src_f32,
+                cudaStream_t stream, const DeviceInfo& dev) {
+  if (n < 1 || n > kMaxBatch) return BSQ_ERR_ARG;
+  AmaxList l{};
+  l.n = n;
+  int64_t most = 0;
+  for (int i = 0; i < n; ++i) {
+    l.src[i] = static_cast<const uint4*>(srcs[i]);
+    l.nvec[i] = elems[i] * (src_f32 ? 4 : 2) / 16;
+    l.out[i] = outs[i];
+    most = std::max(most, l.nvec[i]);
+  }
+  const int agrid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(ceil_div(most, kAmaxThreads * 4), dev.num_sms * 8)));
+  const cudaError_t e = src_f32 ? launch_pdl(amax_kernel<true>, agrid, kAmaxThreads, 0, stream, l)
+                                : launch_pdl(amax_kernel<false>, agrid, kAmaxThreads, 0, stream, l);
+  return e == cudaSuccess ? BSQ_OK : BSQ_ERR_LAUNCH;
 }
 
 // Per-matrix arguments of a batch.
@@ -935,6 +983,7 @@ void fill_args(QuantArgs& a, int fmt, const QuantItem& it) {
   a.cols_magic64 = ~uint64_t{0} / static_cast<uint64_t>(it.cols);
   a.codes_bytes = fmt == BSQ_MXFP8 ? a.elems : a.elems / 2;
   a.scales_bytes = scales_body_bytes(fmt, it.rows, it.cols);
+  a.scale_words = fmt == BSQ_NVFP4 && it.cols % 64 == 0;
   if (fmt == BSQ_NVFP4) {
     a.tail = reinterpret_cast<uint32_t*>(a.scales + scales_body_bytes(fmt, it.rows, it.cols));
     a.g_in = it.global_scale;
@@ -956,12 +1005,18 @@ int launch_quantize_batch(int fmt, bool src_f32, bool global_given, int count, c
 
   cudaError_t err = cudaSuccess;
   if (fmt == BSQ_NVFP4) {
+    const void* srcs[kMaxBatch];
+    int64_t elems[kMaxBatch];
+    uint32_t* outs[kMaxBatch];
     for (int i = 0; i < count; ++i) {
       const QuantArgs& a = b.t[i];
       if (cudaMemsetAsync(a.tail, 0, 16, stream) != cudaSuccess) return BSQ_ERR_LAUNCH;
-      if (!global_given && launch_amax(a.src, src_f32, a.elems, a.tail + 1, stream, dev) != BSQ_OK)
-        return BSQ_ERR_LAUNCH;
+      srcs[i] = a.src;
+      elems[i] = a.elems;
+      outs[i] = a.tail + 1;
     }
+    // one amax launch for the whole batch
+    if (!global_given && launch_amax(srcs, elems, outs, count, src_f32, stream, dev) != BSQ_OK) return BSQ_ERR_LAUNCH;
     if (!global_given) {
       err = src_f32 ? launch_stream<BSQ_NVFP4, true, kNvComputed>(b, dev.num_sms, stream)
                     : launch_stream<BSQ_NVFP4, false, kNvComputed>(b, dev.num_sms, stream);
