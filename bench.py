@@ -516,7 +516,8 @@ def build_units(wl, bsq, dev, layers=None):
                     bsq.gemm(D["qa"], D["qb"], D["bias"], out=D["out"], stream=s)
 
             units.append({"name": g.name, "gemms": [g], "hosts": hosts, "alloc": alloc, "quant": quant, "gemm": gemm,
-                          "fmt": g.fmt, "flops": g.flops, "launches": 2 + (2 if g.fmt == NVFP4 else 0),
+                          # the batched quantize, the GEMM; NVFP4: one amax pass for both matrices
+                          "fmt": g.fmt, "flops": g.flops, "launches": 2 + (1 if g.fmt == NVFP4 else 0),
                           "qkernels": ["stream_kernel"] + (["amax_kernel"] if g.fmt == NVFP4 else []),
                           "qbytes": quant_bytes(g.fmt, g.M, g.K, 4 if g.src_f32 else 2, True) +
                                     quant_bytes(g.fmt, g.N, g.K, 4 if g.src_f32 else 2, True),
@@ -754,8 +755,8 @@ def run_gpu(args, rank: int, world: int):
     assert bsq.device_status() == 0
 
     graphs = StepGraphs(units, flush, dev)
-    # our kernels per step (the batched quantize counts once; NVFP4 adds an amax pass per
-    # matrix; a chained MLP's unfused variant adds its quantize pass)
+    # our kernels per step (the batched quantize counts once; NVFP4 adds one amax pass per
+    # batch; a chained MLP's unfused variant adds its quantize pass)
     launches_per_step = sum(U["launches"] for U in units)
 
     for _ in range(args.warmup):
