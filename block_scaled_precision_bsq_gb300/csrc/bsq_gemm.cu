@@ -403,8 +403,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     float alpha = 1.0f;
     if constexpr (FMT == BSQ_NVFP4) alpha = __fmul_rn(*args.ga, *args.gb);
     // this lane's kAccRegs bias values (consecutive columns from kAccRegs lane of the warp's
-    // kWarpCols, bf16 pairs) of unit u, zero past N or without bias; loaded one unit ahead so that
-    // their latency hides behind the stores of the unit before
+    // kWarpCols, bf16 pairs) of unit u, zero past N or without bias. They are loaded at the top of
+    // the unit, where their latency hides behind the wait for the unit's accumulator. Loading them
+    // a unit ahead, during the store phase of the unit before, measured slower on GB300: NVFP4 fc1
+    // at M = 51200 96.4 -> 100.3 us, the MXFP4 GELU-quantize fc1 188 -> 204 us.
     using BiasRegs = uint32_t[kAccRegs / 2];
     auto load_bias = [&](int u, BiasRegs& b) {
       const int pt = u % args.num_pairs;
@@ -417,8 +419,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < kAccRegs / 2; ++i) b[i] = reinterpret_cast<const uint32_t*>(args.bias + bn)[i];
       }
     };
-    BiasRegs bias_next;
-    if (first_pair < args.num_units) load_bias(first_pair, bias_next);
     uint32_t acc_phase = 0;
     for (int u = first_pair; u < args.num_units; u += pair_stride) {
       const int split = u / args.num_pairs, pt = u - split * args.num_pairs;
@@ -426,11 +426,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int n_blk = pt % args.tiles_n;
       const int n0 = n_blk * BN + static_cast<int>(cgrp) * kWarpCols;
       const int m0 = m_blk * BM + quad * 32;
+      BiasRegs bias;
+      load_bias(u, bias);
       __syncwarp();  // every lane is done reading the previous unit's bias
 #pragma unroll
       for (int i = 0; i < kAccRegs / 2; ++i)
         *reinterpret_cast<uint64_t*>(&bias_s[kAccRegs * lane + 2 * i]) =
-            f2(__uint_as_float(bias_next[i] << 16), __uint_as_float(bias_next[i] & 0xFFFF0000u));
+            f2(__uint_as_float(bias[i] << 16), __uint_as_float(bias[i] & 0xFFFF0000u));
       __syncwarp();
       if (!mbar_wait_bounded(tmem_full, acc_phase, abort_flag, args.status, args.wait_ns)) break;
       acc_phase ^= 1u;
@@ -443,7 +445,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_remote(tmem_empty_leader);  // accumulator may be overwritten now
-      if (u + pair_stride < args.num_units) load_bias(u + pair_stride, bias_next);
 
       // the epilogue values of columns c, c + 1 (c even), packed: alpha * acc + bias (and GELU)
       auto value2 = [&](int c, float& lo, float& hi) {

@@ -126,6 +126,30 @@ def test_batch_equals_single_calls_and_oracle(fmt, f32):
             assert qm.global_scale.item() == o.g
 
 
+def test_batch_nvfp4_mixed_magnitudes_and_narrow_rows():
+    """One batch of NVFP4 matrices whose magnitudes differ by 10^8 (and one all-zero matrix):
+    the single amax launch must give every matrix its own per-tensor scale. The shapes put many
+    rows into one 1024-element warp step (cols 64, 128, 192: the word-wide scale stores of lane
+    pairs) and a width that is not a multiple of 64 (1088: byte stores)."""
+    bsq = _bsq()
+    shapes = [(33, 64), (9, 192), (130, 128), (5, 1088)]
+    mags = [1e-4, 1.0, 1e4, 0.0]
+    from workloads import bf16_bits_to_f32, f32_to_bf16_bits
+
+    xs_np = [f32_to_bf16_bits((bf16_bits_to_f32(random_matrix(r, c, seed=60 + i, dist="student_t4")) *
+                               np.float32(m)).astype(np.float32))
+             for i, ((r, c), m) in enumerate(zip(shapes, mags))]
+    xs = [to_dev(x) for x in xs_np]
+    many = bsq.quantize_many("nvfp4", xs)
+    assert bsq.device_status() == 0
+    for x_np, qm, m in zip(xs_np, many, mags):
+        o = oracle.quantize("nvfp4", x_np)
+        assert np.array_equal(qm.codes.cpu().numpy(), o.codes), "magnitude %g" % m
+        assert np.array_equal(qm.scales.cpu().numpy(), o.tiled_scales()), "magnitude %g" % m
+        assert qm.global_scale.item() == o.g
+        assert (o.g == 0.0) == (m == 0.0)
+
+
 def test_batch_nvfp4_given_scales():
     bsq = _bsq()
     xs_np = [random_matrix(64, 256, seed=50, dist="normal"), random_matrix(200, 512, seed=51, dist="student_t4")]
