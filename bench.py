@@ -340,15 +340,44 @@ def replica_throughput(ms_local: float, flops_per_rank: int, world: int, device=
 
 
 # ----------------------------------------------------------------------------------- GPU arm
+def _code_only(text: str) -> str:
+    """C / C++ / CUDA source without its comments and with runs of whitespace collapsed (string
+    literals kept as they are): what the compiler sees, so that editing a comment does not count
+    as a kernel change."""
+    import re
+
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c == '"':  # string literal
+            j = i + 1
+            while j < n and text[j] != '"':
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return re.sub(r"\s+", " ", "".join(out)).strip()
+
+
 def kernel_source_hash() -> str:
-    """Hash of every kernel source of the library (csrc/*.cu, *.cuh, *.h) and the public header:
-    the key of the recorded DRAM traffic, so that any kernel change invalidates the record."""
+    """Hash of the code (comments and whitespace aside) of every kernel source of the library
+    (csrc/*.cu, *.cuh, *.h) and of the public header: the key of the recorded DRAM traffic, so
+    that any kernel change invalidates the record."""
     h = hashlib.sha256()
     pkg = os.path.join(ROOT, "block_scaled_precision_bsq_gb300", "csrc")
     paths = sorted(os.path.join(pkg, n) for n in os.listdir(pkg) if n.endswith((".cu", ".cuh", ".h")))
     for path in paths + [os.path.join(ROOT, "include", "bsq.h")]:
-        with open(path, "rb") as f:
-            h.update(os.path.basename(path).encode() + f.read())
+        with open(path, encoding="utf-8") as f:
+            h.update(os.path.basename(path).encode() + _code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

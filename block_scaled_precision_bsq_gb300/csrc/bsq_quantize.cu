@@ -11,13 +11,15 @@
 // Work mapping. bsq_quantize / bsq_quantize_batch run stream_kernel: every matrix of a batch is
 // one flat array, a warp step is 1024 consecutive elements of one matrix and a lane's piece 32 of
 // them -- one MX block, two NVFP4 blocks -- loaded straight into registers (two 32-byte loads for
-// bf16) one step ahead of the piece being quantized; no shared-memory staging and no barriers,
-// so the instructions are the element arithmetic itself: block maxima on packed bf16 pairs, the
-// scaling (MX: a power of two) or the IEEE quotient (NVFP4: Markstein's remainder step from a
-// table of correctly rounded reciprocals) on packed fp32 pairs, cvt.rn.satfinite to E4M3 / e2m1.
-// Codes leave as 32 (E4M3) or 16 (e2m1) contiguous bytes per lane; each block's scale byte is
-// stored at its place in the tiled layout (128 rows x 4 columns per 512-byte tile, row r at byte
-// (r % 32) * 16 + ((r / 32) % 4) * 4); the padding of the tiled scales is zeroed after the loop.
+// bf16; the MX formats one step ahead of the piece being quantized); no shared-memory staging
+// and no barriers, so the instructions are the element arithmetic itself: block maxima on packed
+// bf16 pairs, the scaling (MX: a power of two) or the IEEE quotient (NVFP4: Markstein's remainder
+// step from a table of correctly rounded reciprocals) on packed fp32 pairs, cvt.rn.satfinite to
+// E4M3 / e2m1. Codes leave as 32 (E4M3) or 16 (e2m1) contiguous bytes per lane; each block's scale
+// byte is stored at its place in the tiled layout (128 rows x 4 columns per 512-byte tile, row r at
+// byte (r % 32) * 16 + ((r / 32) % 4) * 4), as 32-bit words of two lanes for NVFP4 when the row
+// length allows; the padding of the tiled scales is zeroed after the loop. NVFP4 with a computed
+// per-tensor scale first runs amax_kernel, one launch over every matrix of the batch.
 // bsq_layernorm_quantize runs layernorm_kernel: chunks of whole rows brought into shared memory
 // by 1-D TMA bulk copies, each consumer warp owning whole rows (the row's statistics, then its
 // affine step and quantization).

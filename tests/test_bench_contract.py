@@ -75,3 +75,16 @@ def test_record_traffic_per_step_bytes(tmp_path):
     side.write_text(json.dumps({"workload": "w", "steps": 2, "kernel_source_hash": "abc", "launches_per_step": 3}))
     with pytest.raises(SystemExit):  # a launch list of 3 steps is not 2 steps
         bench.record_traffic(str(csv_path), str(side), "cmd", out_path=str(out))
+
+
+def test_kernel_hash_ignores_comments_only():
+    """The traffic record's key changes with the code, not with its comments or layout."""
+    sys.path.insert(0, ROOT)
+    import bench
+
+    a = 'int f(int x) {  // doubles x\n  return 2 * x; /* two */ }\nconst char* s = "a // b";\n'
+    b = '/* file header */\nint f(int x) {\n  return 2 * x;\n}\nconst char* s = "a // b";  // kept\n'
+    c = 'int f(int x) { return 3 * x; }\nconst char* s = "a // b";\n'
+    assert bench._code_only(a) == bench._code_only(b)
+    assert bench._code_only(a) != bench._code_only(c)
+    assert '"a // b"' in bench._code_only(a)
