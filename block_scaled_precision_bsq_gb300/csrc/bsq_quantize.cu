@@ -20,9 +20,10 @@
 // byte (r % 32) * 16 + ((r / 32) % 4) * 4), as 32-bit words of two lanes for NVFP4 when the row
 // length allows; the padding of the tiled scales is zeroed after the loop. NVFP4 with a computed
 // per-tensor scale first runs amax_kernel, one launch over every matrix of the batch.
-// bsq_layernorm_quantize runs layernorm_kernel: chunks of whole rows brought into shared memory
-// by 1-D TMA bulk copies, each consumer warp owning whole rows (the row's statistics, then its
-// affine step and quantization).
+// bsq_layernorm_quantize runs ln_stream_kernel for bf16 rows of at most 1024 elements (one row per
+// warp step, in registers) and layernorm_kernel otherwise: chunks of whole rows brought into
+// shared memory by 1-D TMA bulk copies, each consumer warp owning whole rows (the row's
+// statistics, then its affine step and quantization).
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -620,6 +621,150 @@ __global__ void __launch_bounds__(kSThreads, SCfg<F32, NV != kMx>::kCtasPerSm)
   }
 }
 
+// ---------------------------------------------------------------------------- LayerNorm rows
+// Statistics of a row of at most 1024 elements held in registers, 32 per lane (zeros in lanes
+// past the row's end, act = false there): mean = sum / n and var = sum (x - mean)^2 / n in fp32
+// (two passes, each lane's four running sums of every fourth element, then a butterfly warp
+// sum), rstd = 1 / sqrt(var + eps). Every warp of the row gets the same values.
+__device__ __forceinline__ void ln_row_stats(const float (&x)[32], bool act, int n, float eps, float& mean,
+                                             float& rstd) {
+  float p4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+  for (int i = 0; i < 32; ++i) p4[i & 3] += x[i];
+  float acc_s = (p4[0] + p4[1]) + (p4[2] + p4[3]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc_s += __shfl_xor_sync(0xFFFFFFFFu, acc_s, o);
+  mean = __fdiv_rn(acc_s, static_cast<float>(n));
+#pragma unroll
+  for (int i = 0; i < 4; ++i) p4[i] = 0.0f;
+  if (act) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const float d = x[i] - mean;
+      p4[i & 3] += d * d;
+    }
+  }
+  acc_s = (p4[0] + p4[1]) + (p4[2] + p4[3]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc_s += __shfl_xor_sync(0xFFFFFFFFu, acc_s, o);
+  const float var = __fdiv_rn(acc_s, static_cast<float>(n));
+  rstd = __fdiv_rn(1.0f, __fsqrt_rn(var + eps));
+}
+
+// y = (x - mean) * rstd * gamma + beta for the 32 elements of row `row` at column cc (x holds the
+// source values; each step rounded in fp32), then their MX block: codes and scale byte (the
+// padding columns of the row's last 4-column scale group are zeroed by the lane of the row's last
+// block).
+template <int FMT>
+__device__ __forceinline__ void ln_finish(const QuantArgs& a, int* status, uint32_t row, int cc, float (&x)[32],
+                                          float mean, float rstd) {
+  const uint4* gp = reinterpret_cast<const uint4*>(a.gamma + cc);
+  const uint4* bp = reinterpret_cast<const uint4*>(a.beta + cc);
+#pragma unroll
+  for (int h = 0; h < 4; ++h) {
+    const uint4 gv = __ldg(gp + h), bv = __ldg(bp + h);
+    const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w}, bw[4] = {bv.x, bv.y, bv.z, bv.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float& y0 = x[8 * h + 2 * i];
+      float& y1 = x[8 * h + 2 * i + 1];
+      y0 = __fadd_rn(__fmul_rn(__fmul_rn(y0 - mean, rstd), __uint_as_float(gw[i] << 16)),
+                     __uint_as_float(bw[i] << 16));
+      y1 = __fadd_rn(__fmul_rn(__fmul_rn(y1 - mean, rstd), __uint_as_float(gw[i] & 0xFFFF0000u)),
+                     __uint_as_float(bw[i] & 0xFFFF0000u));
+    }
+  }
+  const uint64_t e = static_cast<uint64_t>(row) * static_cast<uint64_t>(a.cols) + static_cast<uint64_t>(cc);
+  uint32_t w[FMT == BSQ_MXFP8 ? 8 : 4];
+  const uint32_t sb = quantize32<FMT>(x, NvCtx(), w);
+  const uint64_t cb = (FMT == BSQ_MXFP8) ? e : (e >> 1);
+  if (in_bounds(cb + (FMT == BSQ_MXFP8 ? 32 : 16) <= static_cast<uint64_t>(a.codes_bytes), status)) {
+    if constexpr (FMT == BSQ_MXFP8) {
+      uint4* dst = reinterpret_cast<uint4*>(a.codes + e);
+      dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+      dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    } else {
+      *reinterpret_cast<uint4*>(a.codes + (e >> 1)) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
+  const uint32_t sc = static_cast<uint32_t>(cc) >> 5;
+  const uint64_t so = static_cast<uint64_t>((row >> 7) * static_cast<uint32_t>(a.nct) + (sc >> 2)) * 512 +
+                      (((row & 31u) << 4) | (((row >> 5) & 3u) << 2) | (sc & 3u));
+  if (in_bounds(so + (4 - (sc & 3u)) <= static_cast<uint64_t>(a.scales_bytes), status)) {
+    uint8_t* sp = a.scales + so;
+    *sp = static_cast<uint8_t>(sb);
+    if (sc + 1 == static_cast<uint32_t>(a.nsc)) {
+      for (uint32_t j = (sc & 3u) + 1; j < 4; ++j) sp[j - (sc & 3u)] = 0;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------- LayerNorm, streaming
+// LayerNorm + MX quantization of bf16 rows of at most 1024 elements (ViT-B's 768 and ViT-L's 1024
+// channels): one row per warp step, lane l holding columns [32 l, 32 l + 32) in registers -- loaded
+// straight from global memory -- for both statistics passes, the affine step and the quantization
+// (ln_row_stats, ln_finish: the arithmetic of the shared-memory kernel below, so both give the
+// same bytes). No shared memory, no barriers: 32 warps per SM, each with its own row, hide the
+// latency of a row's loads and two warp reductions. Measured on GB300 (bf16 51200 x 1024 -> MXFP4,
+// L2 flushed): 43 us, against 55 us for the shared-memory kernel; 44.6 us with 3 CTAs per SM and
+// 50.2 us with the next row prefetched into registers at 3 CTAs (its 80 registers spill).
+template <int FMT>
+__global__ void __launch_bounds__(kSThreads, 4) ln_stream_kernel(const __grid_constant__ QuantBatch batch) {
+  const uint32_t warp = threadIdx.x >> 5;
+  const uint32_t lane = threadIdx.x & 31u;
+  launch_dependents();
+  grid_dependency_wait();  // inputs and outputs may belong to the previous kernel until here
+  const QuantArgs& a = batch.t[0];
+  const int nci = static_cast<int>(a.cols);
+  const int cc = static_cast<int>(lane) * kLaneElems;
+  const bool act = cc < nci;
+  const bool aligned32 = (reinterpret_cast<uintptr_t>(a.src) & 31u) == 0u;
+  const int64_t nw = static_cast<int64_t>(gridDim.x) * kSWarps;
+  // this lane's 16 words (32 bf16) of row r (zeros past the row's end or past the last row)
+  auto fetch = [&](uint32_t (&w)[16], int64_t r) {
+    const int64_t off = r * a.cols + cc;
+    if (act && r < a.rows && in_bounds(off >= 0 && off + 32 <= a.elems, batch.status)) {
+      const uint8_t* src = a.src + off * 2;
+      if (aligned32) {
+        ld32(src, w);
+        ld32(src + 32, w + 8);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) ld16(src + 16 * i, w + 4 * i);
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) w[i] = 0u;
+    }
+  };
+  auto process = [&](const uint32_t (&w)[16], int64_t r) {
+    float x[32];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      x[2 * i] = __uint_as_float(w[i] << 16);
+      x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+    float mean, rstd;
+    ln_row_stats(x, act, nci, a.eps, mean, rstd);
+    if (act) ln_finish<FMT>(a, batch.status, static_cast<uint32_t>(r), cc, x, mean, rstd);
+  };
+  uint32_t w[16];
+  for (int64_t r = static_cast<int64_t>(blockIdx.x) * kSWarps + warp; r < a.rows; r += nw) {
+    fetch(w, r);
+    process(w, r);
+  }
+  // padding of the tiled scales reads 0: every word of the padding rows of the last row tile (the
+  // padding columns of each row's last group are zeroed by ln_finish)
+  const int64_t tid = static_cast<int64_t>(blockIdx.x) * kSThreads + threadIdx.x;
+  const int64_t nthr = static_cast<int64_t>(gridDim.x) * kSThreads;
+  const int64_t pad_rows = (128 - a.rows % 128) % 128;
+  for (int64_t wd = tid; wd < pad_rows * a.nct; wd += nthr) {
+    const int64_t pr = a.rows + wd / a.nct, tc = wd % a.nct;
+    const int64_t so = scale_word_offset(pr, 4 * tc, a.nct);
+    if (in_bounds(so + 4 <= a.scales_bytes, batch.status)) *reinterpret_cast<uint32_t*>(a.scales + so) = 0u;
+  }
+}
+
 // ---------------------------------------------------------------------------- LayerNorm kernel
 // LayerNorm + MX quantization (MXFP8, MXFP4): the source is cut into chunks of whole rows (at
 // most 16 KB), each brought into shared memory by one 1-D TMA bulk copy; a producer thread keeps a
@@ -721,48 +866,8 @@ __global__ void __launch_bounds__(QCfg::kThreads, QCfg::kCtasPerSm)
           return acc_s;
         };
         const uint32_t row = static_cast<uint32_t>(r0) + rr;
-        // y = (x - mean) * rstd * gamma + beta for the 32 elements at column cc (x holds the
-        // source values), then their MX block: codes and scale byte
         auto finish = [&](int cc, float (&x)[32], float mean, float rstd) {
-          const uint4* gp = reinterpret_cast<const uint4*>(a.gamma + cc);
-          const uint4* bp = reinterpret_cast<const uint4*>(a.beta + cc);
-#pragma unroll
-          for (int h = 0; h < 4; ++h) {
-            const uint4 gv = __ldg(gp + h), bv = __ldg(bp + h);
-            const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w}, bw[4] = {bv.x, bv.y, bv.z, bv.w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              float& y0 = x[8 * h + 2 * i];
-              float& y1 = x[8 * h + 2 * i + 1];
-              y0 = __fadd_rn(__fmul_rn(__fmul_rn(y0 - mean, rstd), __uint_as_float(gw[i] << 16)),
-                             __uint_as_float(bw[i] << 16));
-              y1 = __fadd_rn(__fmul_rn(__fmul_rn(y1 - mean, rstd), __uint_as_float(gw[i] & 0xFFFF0000u)),
-                             __uint_as_float(bw[i] & 0xFFFF0000u));
-            }
-          }
-          const uint64_t e = static_cast<uint64_t>(row) * static_cast<uint64_t>(a.cols) + static_cast<uint64_t>(cc);
-          uint32_t w[FMT == BSQ_MXFP8 ? 8 : 4];
-          const uint32_t sb = quantize32<FMT>(x, nv, w);
-          const uint64_t cb = (FMT == BSQ_MXFP8) ? e : (e >> 1);
-          if (in_bounds(cb + (FMT == BSQ_MXFP8 ? 32 : 16) <= static_cast<uint64_t>(a.codes_bytes), batch.status)) {
-            if constexpr (FMT == BSQ_MXFP8) {
-              uint4* dst = reinterpret_cast<uint4*>(a.codes + e);
-              dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-              dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-            } else {
-              *reinterpret_cast<uint4*>(a.codes + (e >> 1)) = make_uint4(w[0], w[1], w[2], w[3]);
-            }
-          }
-          const uint32_t sc = static_cast<uint32_t>(cc) >> 5;
-          const uint64_t so = static_cast<uint64_t>((row >> 7) * static_cast<uint32_t>(a.nct) + (sc >> 2)) * 512 +
-                              (((row & 31u) << 4) | (((row >> 5) & 3u) << 2) | (sc & 3u));
-          if (in_bounds(so + (4 - (sc & 3u)) <= static_cast<uint64_t>(a.scales_bytes), batch.status)) {
-            uint8_t* sp = a.scales + so;
-            *sp = static_cast<uint8_t>(sb);
-            if (sc + 1 == static_cast<uint32_t>(a.nsc)) {
-              for (uint32_t j = (sc & 3u) + 1; j < 4; ++j) sp[j - (sc & 3u)] = 0;
-            }
-          }
+          ln_finish<FMT>(a, batch.status, row, cc, x, mean, rstd);
         };
         if (nci <= 32 * kLaneElems) {
           // rows of at most 1024 elements: each lane reads its 32 elements from shared memory
@@ -776,27 +881,8 @@ __global__ void __launch_bounds__(QCfg::kThreads, QCfg::kCtasPerSm)
 #pragma unroll
             for (int i = 0; i < 32; ++i) x[i] = 0.0f;
           }
-          float p4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-          for (int i = 0; i < 32; ++i) p4[i & 3] += x[i];
-          float acc_s = (p4[0] + p4[1]) + (p4[2] + p4[3]);
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) acc_s += __shfl_xor_sync(0xFFFFFFFFu, acc_s, o);
-          const float mean = __fdiv_rn(acc_s, static_cast<float>(nci));
-#pragma unroll
-          for (int i = 0; i < 4; ++i) p4[i] = 0.0f;
-          if (act) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const float d = x[i] - mean;
-              p4[i & 3] += d * d;
-            }
-          }
-          acc_s = (p4[0] + p4[1]) + (p4[2] + p4[3]);
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) acc_s += __shfl_xor_sync(0xFFFFFFFFu, acc_s, o);
-          const float var = __fdiv_rn(acc_s, static_cast<float>(nci));
-          const float rstd = __fdiv_rn(1.0f, __fsqrt_rn(var + a.eps));
+          float mean, rstd;
+          ln_row_stats(x, act, nci, a.eps, mean, rstd);
           if (act) finish(cc, x, mean, rstd);
         } else {
           const float mean = __fdiv_rn(piece_sum(0.0f, false), static_cast<float>(nci));
@@ -924,6 +1010,13 @@ cudaError_t launch_ln(const QuantBatch& b, int grid, cudaStream_t stream, int de
   return launch_pdl(layernorm_kernel<FMT, F32>, grid, QCfg::kThreads, QCfg::kSmem, stream, b);
 }
 
+template <int FMT>
+cudaError_t launch_ln_stream(const QuantBatch& b, int num_sms, cudaStream_t stream) {
+  const int64_t ctas = ceil_div(b.t[0].rows, kSWarps);
+  const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(ctas, 4 * static_cast<int64_t>(num_sms))));
+  return launch_pdl(ln_stream_kernel<FMT>, grid, kSThreads, 0, stream, b);
+}
+
 }  // namespace
 
 namespace {
@@ -1044,20 +1137,27 @@ int launch_layernorm_quantize(int fmt, bool src_f32, const QuantItem& item, cons
   QuantBatch b{};
   b.n = 1;
   b.status = dev.status;
+  QuantArgs& a = b.t[0];
+  fill_args(a, fmt, item);
+  a.gamma = gamma;
+  a.beta = beta;
+  a.eps = eps;
+  if (!src_f32 && item.cols <= 32 * kLaneElems) {
+    // bf16 rows of at most 1024 elements: the streaming kernel (it waits on no barrier, so an
+    // injected stall has nothing to act on and stays armed for the shared-memory kernel)
+    const cudaError_t err = fmt == BSQ_MXFP8 ? launch_ln_stream<BSQ_MXFP8>(b, dev.num_sms, stream)
+                                             : launch_ln_stream<BSQ_MXFP4>(b, dev.num_sms, stream);
+    return err == cudaSuccess ? BSQ_OK : BSQ_ERR_LAUNCH;
+  }
   const StallInjection inj = take_stall(BSQ_KERNEL_LAYERNORM);
   b.stall_after = inj.after;
   b.wait_ns = inj.limit_ns;
-  QuantArgs& a = b.t[0];
-  fill_args(a, fmt, item);
   // chunks of whole rows: at most one ring buffer, and small enough that every SM gets a few
   const int64_t target = std::max<int64_t>(
       kChunkMin, std::min<int64_t>(kChunkMax, a.elems * esize / (4 * QCfg::kCtasPerSm * static_cast<int64_t>(dev.num_sms))));
   a.rows_per_chunk = std::max<int64_t>(1, std::min<int64_t>(target / row_bytes, kLnMaxRows));
   b.chunk_start[0] = 0;
   b.chunk_start[1] = ceil_div(a.rows, a.rows_per_chunk);
-  a.gamma = gamma;
-  a.beta = beta;
-  a.eps = eps;
   const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(b.chunk_start[1], QCfg::kCtasPerSm * dev.num_sms)));
   cudaError_t err;
   if (fmt == BSQ_MXFP8) {

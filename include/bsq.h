@@ -121,6 +121,9 @@ int bsq_quantize(int fmt_flags, const void* src, int64_t rows, int64_t cols, voi
  * Codes and scales are the MX quantization of the kernel's fp32 y; a code differs from that of
  * the exact value only where the exact value lies within the fp32 rounding of the statistics
  * and the affine step of a rounding boundary.
+ * Work mapping: bf16 rows of at most 1024 elements run one row per warp with the row in
+ * registers; other rows are staged through shared memory. Both give the same bytes for the same
+ * values.
  * Shapes: as bsq_quantize for MX, and a row of at most 16384 bytes (cols <= 8192 bf16 or 4096
  * fp32), else BSQ_ERR_SHAPE. Errors: BSQ_ERR_ARG for another format or flag, NULL gamma /
  * beta or a negative or non-finite eps; otherwise as bsq_quantize.
@@ -366,7 +369,10 @@ int bsq_selftest_device_check(bsq_stream_t stream);
  * bsq_test_inject_stall: a test of the failure path of the kernels that wait on barriers, with no
  * GPU fault: arms a one-shot stall for the calling thread's next launch of one kernel class.
  *   kernel         BSQ_KERNEL_GEMM (every bsq_gemm* and bsq_convt2x2 launch), BSQ_KERNEL_DUAL
- *                  (bsq_quantize_dual) or BSQ_KERNEL_LAYERNORM (bsq_layernorm_quantize)
+ *                  (bsq_quantize_dual) or BSQ_KERNEL_LAYERNORM (bsq_layernorm_quantize on fp32
+ *                  sources or rows longer than 1024 elements: its shared-memory kernel; bf16 rows
+ *                  of at most 1024 elements run a kernel that waits on no barrier, and the stall
+ *                  stays armed past such a launch)
  *   after_stages   >= 0: the producers of that launch stop issuing loads -- and never announce the
  *                  missing bytes -- after this many pipeline stages per CTA, so a consumer waits for
  *                  a stage that never arrives; -1: disarm any stall armed on the calling thread

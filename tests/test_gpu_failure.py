@@ -104,8 +104,10 @@ def test_dual_stall_times_out_and_next_dual_is_bit_exact(fmt, stochastic, after)
 @pytest.mark.parametrize("fmt", ["mxfp8", "mxfp4"])
 @pytest.mark.parametrize("after", [0, 2])
 def test_layernorm_stall_times_out_and_next_call_is_unchanged(fmt, after):
+    """Rows of 2048 bf16 take the shared-memory LayerNorm kernel (4096 one-row chunks over at most
+    608 CTAs), whose producer the stall stops."""
     bsq = _bsq()
-    rows, cols = 4096, 1024
+    rows, cols = 4096, 2048
     x = (torch.randn(rows, cols, device="cuda") * 3 + 1).to(torch.bfloat16)
     g = (1 + 0.1 * torch.randn(cols, device="cuda")).to(torch.bfloat16)
     b = (0.1 * torch.randn(cols, device="cuda")).to(torch.bfloat16)
@@ -130,4 +132,24 @@ def test_injection_is_one_shot_and_only_for_the_named_kernel():
     bsq.gemm(qa, qb)                # consumes the stall
     assert bsq.device_status() == bsq.ERR_TIMEOUT
     bsq.gemm(qa, qb)                # one shot: runs normally
+    assert bsq.device_status() == bsq.OK
+
+
+def test_layernorm_stall_waits_for_the_shared_memory_kernel():
+    """bf16 rows of at most 1024 elements take the streaming LayerNorm kernel, which waits on no
+    barrier: an armed LayerNorm stall does not act there and stays armed for the next launch of
+    the shared-memory kernel."""
+    bsq = _bsq()
+    g1 = (1 + 0.1 * torch.randn(1024, device="cuda")).to(torch.bfloat16)
+    b1 = (0.1 * torch.randn(1024, device="cuda")).to(torch.bfloat16)
+    g2 = (1 + 0.1 * torch.randn(2048, device="cuda")).to(torch.bfloat16)
+    b2 = (0.1 * torch.randn(2048, device="cuda")).to(torch.bfloat16)
+    x1 = torch.randn(512, 1024, device="cuda").to(torch.bfloat16)
+    x2 = torch.randn(2048, 2048, device="cuda").to(torch.bfloat16)
+    assert bsq.bsq_test_inject_stall(bsq.KERNEL_LAYERNORM, 0, LIMIT_NS) == bsq.OK
+    bsq.layernorm_quantize("mxfp8", x1, g1, b1, 1e-6)
+    assert bsq.device_status() == bsq.OK
+    bsq.layernorm_quantize("mxfp8", x2, g2, b2, 1e-6)
+    assert bsq.device_status() == bsq.ERR_TIMEOUT
+    bsq.layernorm_quantize("mxfp8", x2, g2, b2, 1e-6)
     assert bsq.device_status() == bsq.OK

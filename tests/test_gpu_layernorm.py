@@ -85,3 +85,19 @@ def test_layernorm_quantize_full_size_sampled_rows():
     codes = q.codes.cpu().numpy().reshape(rows, cols)[idx]
     plain = plain_scales(q.scales.cpu().numpy(), rows, cols, row_idx=idx)
     check_mx_band("mxfp8", codes, plain, exact, _band(x[idx], g, b, 1e-6, exact))
+
+
+@pytest.mark.parametrize("fmt", ["mxfp8", "mxfp4"])
+@pytest.mark.parametrize("rows,cols", [(300, 768), (129, 1024), (33, 96)])
+def test_streaming_and_shared_memory_kernels_agree(fmt, rows, cols):
+    """bf16 rows of at most 1024 elements take the streaming kernel, fp32 rows the shared-memory
+    kernel; both run the same row statistics and affine arithmetic, so the same values (a bf16
+    matrix and its exact fp32 copy) give the same bytes."""
+    bsq = _bsq()
+    x, g, b = _inputs(rows, cols, seed=120 + cols)
+    xd = to_dev(x)
+    q16 = bsq.layernorm_quantize(fmt, xd, to_dev(g), to_dev(b), 1e-6)
+    q32 = bsq.layernorm_quantize(fmt, xd.float(), to_dev(g), to_dev(b), 1e-6)
+    assert bsq.device_status() == 0
+    assert torch.equal(q16.codes, q32.codes)
+    assert torch.equal(q16.scales, q32.scales)
