@@ -52,13 +52,48 @@ constexpr int BN = 256;           // columns of the output tile (both CTAs)
 constexpr int BNH = BN / 2;       // rows of B held per CTA
 constexpr int kChunkBytes = 128;  // K bytes per stage: one 128-byte swizzle span per row
 constexpr int kMmasPerStage = 4;  // 32 K bytes per MMA
-constexpr int kNumEpiWarps = 8;  // two per TMEM lane quadrant, each draining 128 columns
-constexpr int kWarpCols = 4 * BN / kNumEpiWarps;
-constexpr int kAccRegs = kWarpCols / 32;  // 32-column TMEM loads per warp
 constexpr int kFirstEpiWarp = 2;
-constexpr int kThreads = (kFirstEpiWarp + kNumEpiWarps) * 32;
 constexpr int kAccCols = BN;  // fp32 accumulator columns in TMEM
 constexpr uint32_t kTmemCols = 512;
+
+// Epilogue modes. kEpiBf16: out = bf16(v), v = alpha * acc + bias. kEpiGeluBf16: out =
+// bf16(GELU(v)) (the "fc1 + GELU" epilogue every stack of the "lightly-train - DINOv3 + EoMT on
+// RTX 5090" README fuses, section 4.3). kEpiGeluMxfp8 / kEpiGeluMxfp4: GELU(v) quantized along
+// the output row straight into MX codes and tiled scales, the fc2 operand (the MXFP8 stack's
+// fc1 epilogue, same section); bytes laid out as bsq_quantize writes them. kEpiConvT /
+// kEpiConvTGelu: the head's kernel-2 stride-2 transposed convolution (same README section: the
+// ScaleBlocks' ConvT, then GELU): column n = (2 dy + dx) C_out + co of output row (b, h, w) is
+// stored at pixel (b, 2h + dy, 2w + dx), channel co, of the NHWC output, with bias[co].
+// kEpiF32Partial: split-K -- K is cut into `splits` equal ranges of stages, the work units are
+// (tile, range) pairs, and each unit stores its raw fp32 accumulator (no alpha, no bias) into
+// slice `range` of an fp32 workspace of splits x M x N; splitk_finalize_kernel sums the slices.
+// For shapes with fewer tiles than SM pairs and a long K (the weight gradient dW = dY^T X:
+// M, N the weight's shape, K the token count), where one unit per tile leaves SMs idle.
+enum EpiMode {
+  kEpiBf16 = 0,
+  kEpiGeluBf16 = 1,
+  kEpiGeluMxfp8 = 2,
+  kEpiGeluMxfp4 = 3,
+  kEpiConvT = 4,
+  kEpiConvTGelu = 5,
+  kEpiF32Partial = 6
+};
+
+// Epilogue warps per CTA, by epilogue mode. The GELU epilogues are bound by their arithmetic
+// (about 10 instructions per value) and run 16 warps, four per TMEM lane quadrant, of 64 columns
+// each; the others are bound by their store phase, where more warps (and so more TMA stores in
+// flight beside the operand loads) made the kernel slower, and run 8 warps of 128 columns.
+// Measured on GB300, L2 flushed, M = 51200, K = 1024, N = 4096: fc1 with GELU into MXFP4 codes
+// 188 -> 164 us with 16 warps; the plain NVFP4 fc1 96 -> 117 us with 16.
+template <int EPI>
+struct Epi {
+  static constexpr bool kGelu =
+      EPI == kEpiGeluBf16 || EPI == kEpiGeluMxfp8 || EPI == kEpiGeluMxfp4 || EPI == kEpiConvTGelu;
+  static constexpr int kWarps = kGelu ? 16 : 8;
+  static constexpr int kWarpCols = 4 * BN / kWarps;
+  static constexpr int kAccRegs = kWarpCols / 32;  // 32-column TMEM loads per warp
+  static constexpr int kThreads = (kFirstEpiWarp + kWarps) * 32;
+};
 
 // Per format: kStages stages in the ring, kAtoms 512-byte scale atoms per 128 rows per stage
 // (4 scale columns of 128 rows each), kEpiCols output columns per epilogue store chunk and
@@ -84,10 +119,16 @@ template <int FMT>
 __host__ __device__ constexpr int sf_cols() {
   return 12 * Cfg<FMT>::kAtoms;
 }
+// Pipeline stages of a (format, epilogue) kernel: MXFP8 with 16 epilogue warps takes 5, the
+// staging buffers of the 8 extra warps not fitting beside a sixth.
+template <int FMT, int EPI>
+__host__ __device__ constexpr int stages() {
+  return (FMT == BSQ_MXFP8 && Epi<EPI>::kWarps == 16) ? 5 : Cfg<FMT>::kStages;
+}
 
-template <int FMT>
+template <int FMT, int EPI>
 struct Smem {
-  static constexpr int S = Cfg<FMT>::kStages;
+  static constexpr int S = stages<FMT, EPI>();
   static constexpr int kABytes = BM * kChunkBytes;   // own 128 rows of A
   static constexpr int kBBytes = BNH * kChunkBytes;  // own 128-row half of B
   static constexpr int kSfaBytes = Cfg<FMT>::kAtoms * 512;      // this CTA's 128 A rows
@@ -98,19 +139,13 @@ struct Smem {
   static constexpr int sfa_off = b_off + S * kBBytes;
   static constexpr int sfb_off = sfa_off + S * kSfaBytes;
   static constexpr int epi_off = ((sfb_off + S * kSfbBytes) + 1023) / 1024 * 1024;
-  static constexpr int bias_off = epi_off + kNumEpiWarps * Cfg<FMT>::kEpiBufs * kEpiChunkBytes;
-  static constexpr int bar_off = bias_off + kNumEpiWarps * kWarpCols * 4;
+  static constexpr int bias_off = epi_off + Epi<EPI>::kWarps * Cfg<FMT>::kEpiBufs * kEpiChunkBytes;
+  static constexpr int bar_off = bias_off + Epi<EPI>::kWarps * Epi<EPI>::kWarpCols * 4;
   static constexpr int kNumBars = 2 * S + 3;
   static constexpr int misc_off = bar_off + kNumBars * 8;
   static constexpr int total = misc_off + 16;
   static constexpr int alloc = total;  // the dynamic region is 1024-byte aligned (checked at kernel start)
 };
-static_assert(Smem<BSQ_MXFP8>::alloc <= 232448, "MXFP8 shared memory budget");
-static_assert(Smem<BSQ_NVFP4>::alloc <= 232448, "NVFP4 shared memory budget");
-static_assert(Smem<BSQ_MXFP4>::alloc <= 232448, "MXFP4 shared memory budget");
-static_assert(kAccCols + Cfg<BSQ_MXFP8>::kStages * sf_cols<BSQ_MXFP8>() <= 512, "TMEM budget");
-static_assert(kAccCols + Cfg<BSQ_NVFP4>::kStages * sf_cols<BSQ_NVFP4>() <= 512, "TMEM budget");
-static_assert(kAccCols + Cfg<BSQ_MXFP4>::kStages * sf_cols<BSQ_MXFP4>() <= 512, "TMEM budget");
 
 // Instruction descriptor of a block-scaled MMA (kinds mxf8f6f4 / mxf4 / mxf4nvf4):
 // bits 4-5 scale-factor B id, 7-9 A type, 10-12 B type, 15/16 A/B major (0 = K-major),
@@ -124,28 +159,6 @@ __host__ __device__ constexpr uint32_t make_idesc(uint32_t sf_id) {
          (static_cast<uint32_t>((2 * BM) >> 7) << 27) | (sf_id << 29);
 }
 
-// Epilogue modes. kEpiBf16: out = bf16(v), v = alpha * acc + bias. kEpiGeluBf16: out =
-// bf16(GELU(v)) (the "fc1 + GELU" epilogue every stack of the "lightly-train - DINOv3 + EoMT on
-// RTX 5090" README fuses, section 4.3). kEpiGeluMxfp8 / kEpiGeluMxfp4: GELU(v) quantized along
-// the output row straight into MX codes and tiled scales, the fc2 operand (the MXFP8 stack's
-// fc1 epilogue, same section); bytes laid out as bsq_quantize writes them. kEpiConvT /
-// kEpiConvTGelu: the head's kernel-2 stride-2 transposed convolution (same README section: the
-// ScaleBlocks' ConvT, then GELU): column n = (2 dy + dx) C_out + co of output row (b, h, w) is
-// stored at pixel (b, 2h + dy, 2w + dx), channel co, of the NHWC output, with bias[co].
-// kEpiF32Partial: split-K -- K is cut into `splits` equal ranges of stages, the work units are
-// (tile, range) pairs, and each unit stores its raw fp32 accumulator (no alpha, no bias) into
-// slice `range` of an fp32 workspace of splits x M x N; splitk_finalize_kernel sums the slices.
-// For shapes with fewer tiles than SM pairs and a long K (the weight gradient dW = dY^T X:
-// M, N the weight's shape, K the token count), where one unit per tile leaves SMs idle.
-enum EpiMode {
-  kEpiBf16 = 0,
-  kEpiGeluBf16 = 1,
-  kEpiGeluMxfp8 = 2,
-  kEpiGeluMxfp4 = 3,
-  kEpiConvT = 4,
-  kEpiConvTGelu = 5,
-  kEpiF32Partial = 6
-};
 
 // 3-D tile store (coordinates innermost first).
 __device__ __forceinline__ void tma_store_3d(const void* tmap, const void* smem_src, int32_t c0, int32_t c1,
@@ -210,13 +223,18 @@ struct GemmArgs {
 };
 
 template <int FMT, int EPI>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Epi<EPI>::kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
                 const __grid_constant__ CUtensorMap mapSfa, const __grid_constant__ CUtensorMap mapSfb,
                 const __grid_constant__ CUtensorMap mapOut, const GemmArgs args) {
   using C = Cfg<FMT>;
-  using L = Smem<FMT>;
-  constexpr int S = C::kStages;
+  using L = Smem<FMT, EPI>;
+  constexpr int S = stages<FMT, EPI>();
+  constexpr int kNumEpiWarps = Epi<EPI>::kWarps;
+  constexpr int kWarpCols = Epi<EPI>::kWarpCols;
+  constexpr int kAccRegs = Epi<EPI>::kAccRegs;
+  static_assert(L::alloc <= 232448, "shared memory budget");
+  static_assert(kAccCols + S * sf_cols<FMT>() <= 512, "TMEM budget");
   extern __shared__ __align__(1024) uint8_t smem[];
   // the 128-byte swizzled operand tiles need a 1024-byte aligned base (uniform: every thread of
   // both CTAs leaves before touching a barrier)
@@ -695,13 +713,13 @@ int run_gemm(const void* A, const void* A_scales, const void* B, const void* B_s
   // per device: the shared-memory opt-in and the number of co-resident clusters (0 = unusable)
   static PerDevice<int> setup;
   const int max_clusters = setup.run(dev.device, [] {
-    if (cudaFuncSetAttribute(gemm_kernel<FMT, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<FMT>::alloc) !=
+    if (cudaFuncSetAttribute(gemm_kernel<FMT, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<FMT, EPI>::alloc) !=
         cudaSuccess) {
       cudaGetLastError();
       return 0;
     }
     cudaLaunchAttribute at[2];
-    cudaLaunchConfig_t cfg = pair_launch_config(at, 1, kThreads, Smem<FMT>::alloc, nullptr);
+    cudaLaunchConfig_t cfg = pair_launch_config(at, 1, Epi<EPI>::kThreads, Smem<FMT, EPI>::alloc, nullptr);
     int n = 0;
     if (cudaOccupancyMaxActiveClusters(&n, gemm_kernel<FMT, EPI>, &cfg) != cudaSuccess) {
       cudaGetLastError();
@@ -727,7 +745,7 @@ int run_gemm(const void* A, const void* A_scales, const void* B, const void* B_s
     // code bytes of an output row: N (E4M3) or N / 2 (e2m1); staged rows of 64 bytes, or 32 (e2m1 codes of a
     // warp's 64 columns)
     const uint64_t rb = (EPI == kEpiGeluMxfp8) ? static_cast<uint64_t>(N) : static_cast<uint64_t>(N) / 2;
-    ok_out = (EPI == kEpiGeluMxfp8 || kWarpCols / 2 >= 64)
+    ok_out = (EPI == kEpiGeluMxfp8 || Epi<EPI>::kWarpCols / 2 >= 64)
                  ? make_map_2d(&mOut, CU_TENSOR_MAP_DATA_TYPE_UINT8, out, rb, M, rb, 2 * EC, 32, osw)
                  : make_map_2d(&mOut, CU_TENSOR_MAP_DATA_TYPE_UINT8, out, rb, M, rb, 32, 32, CU_TENSOR_MAP_SWIZZLE_32B);
   }
@@ -764,7 +782,7 @@ int run_gemm(const void* A, const void* A_scales, const void* B, const void* B_s
   const int clusters = std::min(a.num_units, std::min(max_clusters, dev.num_sms / 2));
 
   cudaLaunchAttribute at[2];
-  cudaLaunchConfig_t cfg = pair_launch_config(at, clusters, kThreads, Smem<FMT>::alloc, stream);
+  cudaLaunchConfig_t cfg = pair_launch_config(at, clusters, Epi<EPI>::kThreads, Smem<FMT, EPI>::alloc, stream);
   if (cudaLaunchKernelEx(&cfg, gemm_kernel<FMT, EPI>, mA, mB, mSfa, mSfb, mOut, a) != cudaSuccess)
     return BSQ_ERR_LAUNCH;
   return cudaGetLastError() == cudaSuccess ? BSQ_OK : BSQ_ERR_LAUNCH;
