@@ -197,6 +197,19 @@ __device__ __forceinline__ void rne_codes(const float* x, float f, float r, uint
 #pragma unroll
     for (int j = 0; j < N / 4; ++j)
       w[j] = cvt_e4m3x4(x[4 * j] * f, x[4 * j + 1] * f, x[4 * j + 2] * f, x[4 * j + 3] * f);
+  } else if constexpr (N == 8 && FMT == BSQ_NVFP4 && kQuick) {
+    // markstein_quotient on packed pairs with the reciprocal negated: q0' = x (-r) = -q0,
+    // t = q0' f + x (the exact remainder x - q0 f), y = t (-r) + q0' = -(q0 + t r), the negated
+    // IEEE quotient; one XOR per eight codes flips the signs back, signed zeros included
+    const uint64_t f2v = f2_splat(f), nr2 = f2_splat(-r);
+    float y[8];
+#pragma unroll
+    for (int i = 0; i < 8; i += 2) {
+      const uint64_t x2 = f2(x[i], x[i + 1]);
+      const uint64_t q0 = f2_mul(x2, nr2);
+      f2_split(f2_fma(f2_fma(q0, f2v, x2), nr2, q0), y[i], y[i + 1]);
+    }
+    w[0] = cvt_e2m1x8(y) ^ 0x88888888u;
   } else if constexpr (N == 8) {
     float y[8];
 #pragma unroll
