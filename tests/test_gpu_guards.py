@@ -142,3 +142,48 @@ def test_convt_stays_inside_output():
     ref = bsq.convt2x2(qx, qw, B, H, W, bias, gelu=True)
     assert bsq.device_status() == 0
     assert out.intact() and _same(out.t, ref)
+
+
+def _offset_copy(x: torch.Tensor, offset_bytes: int) -> torch.Tensor:
+    """x's values in a tensor whose data starts `offset_bytes` past a 256-byte boundary (16-byte
+    aligned, not 32): the kernels' 16-byte load path."""
+    n = x.numel() * x.element_size()
+    buf = torch.empty(n + 256, dtype=torch.uint8, device=x.device)
+    y = buf[offset_bytes:offset_bytes + n].view(x.dtype).view(x.shape)
+    y.copy_(x)
+    assert y.data_ptr() % 32 == offset_bytes % 32
+    return y
+
+
+@pytest.mark.parametrize("fmt", ["mxfp8", "nvfp4", "mxfp4"])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_quantize_source_aligned_to_16_bytes_only(fmt, dtype):
+    """A source 16-byte aligned but not 32 takes the 16-byte loads: the same bytes as from an
+    aligned copy (ragged rows, NVFP4 both per-tensor scale modes)."""
+    bsq = _bsq()
+    x = (torch.randn(257, 160, device="cuda", generator=torch.Generator(device="cuda").manual_seed(3)) * 3).to(dtype)
+    y = _offset_copy(x, 16)
+    a, b = bsq.quantize(fmt, x), bsq.quantize(fmt, y)
+    assert bsq.device_status() == 0
+    assert _same(a.codes, b.codes) and _same(a.scales, b.scales)
+    if fmt == "nvfp4":
+        g = torch.tensor([0.01], dtype=torch.float32, device="cuda")
+        a, b = bsq.quantize(fmt, x, global_scale=g), bsq.quantize(fmt, y, global_scale=g)
+        assert bsq.device_status() == 0
+        assert _same(a.codes, b.codes) and _same(a.scales, b.scales)
+
+
+@pytest.mark.parametrize("fmt", ["mxfp8", "mxfp4"])
+@pytest.mark.parametrize("cols", [768, 1024, 2048])
+def test_layernorm_source_aligned_to_16_bytes_only(fmt, cols):
+    """The same for LayerNorm + quantize, on both of its kernels (rows of at most 1024 bf16 run the
+    streaming one)."""
+    bsq = _bsq()
+    gen = torch.Generator(device="cuda").manual_seed(cols)
+    x = (torch.randn(131, cols, device="cuda", generator=gen) * 3 + 1).to(torch.bfloat16)
+    g = (1 + 0.1 * torch.randn(cols, device="cuda", generator=gen)).to(torch.bfloat16)
+    b = (0.1 * torch.randn(cols, device="cuda", generator=gen)).to(torch.bfloat16)
+    y = _offset_copy(x, 16)
+    p, q = bsq.layernorm_quantize(fmt, x, g, b, 1e-6), bsq.layernorm_quantize(fmt, y, g, b, 1e-6)
+    assert bsq.device_status() == 0
+    assert _same(p.codes, q.codes) and _same(p.scales, q.scales)
