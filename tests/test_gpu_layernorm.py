@@ -72,19 +72,21 @@ def test_layernorm_quantize_fp32_source():
                   _band(x, g, b, 1e-5, exact))
 
 
-def test_layernorm_quantize_full_size_sampled_rows():
-    """ViT-L LN before fc1 at its full size (M=7168, 1024 channels), MXFP8, sampled rows."""
+@pytest.mark.parametrize("fmt,rows", [("mxfp8", 7168), ("mxfp4", 51200)])
+def test_layernorm_quantize_full_size_sampled_rows(fmt, rows):
+    """ViT-L LN before fc1 at its full sizes (M = 7168 MXFP8 and M = 51200 MXFP4, 1024 channels:
+    the streaming kernel, ten rows per warp at 51200), sampled rows."""
     bsq = _bsq()
-    rows, cols = 7168, 1024
+    cols = 1024
     x, g, b = _inputs(rows, cols, seed=97)
-    q = bsq.layernorm_quantize("mxfp8", to_dev(x), to_dev(g), to_dev(b), 1e-6)
+    q = bsq.layernorm_quantize(fmt, to_dev(x), to_dev(g), to_dev(b), 1e-6)
     assert bsq.device_status() == 0
     idx = np.unique(np.concatenate([np.arange(0, rows, 128), np.arange(127, rows, 128),
                                     np.random.default_rng(1).integers(0, rows, 64)]))
     exact = oracle.layernorm(x[idx], g, b, 1e-6)
-    codes = q.codes.cpu().numpy().reshape(rows, cols)[idx]
+    codes = element_codes(fmt, q.codes.cpu().numpy(), rows, cols)[idx]
     plain = plain_scales(q.scales.cpu().numpy(), rows, cols, row_idx=idx)
-    check_mx_band("mxfp8", codes, plain, exact, _band(x[idx], g, b, 1e-6, exact))
+    check_mx_band(fmt, codes, plain, exact, _band(x[idx], g, b, 1e-6, exact))
 
 
 @pytest.mark.parametrize("fmt", ["mxfp8", "mxfp4"])

@@ -68,6 +68,16 @@ def test_nvfp4_cols_multiple_of_16_only():
         _compare("nvfp4", random_matrix(5, cols, seed=cols), label="nvfp4 cols=%d" % cols)
 
 
+@pytest.mark.parametrize("rows,cols", [(1025, 48), (300, 272), (77, 1040), (3, 16)])
+@pytest.mark.parametrize("f32", [False, True])
+def test_nvfp4_blocks_across_rows_many_steps(rows, cols, f32):
+    """cols % 32 == 16: a lane's two NVFP4 blocks may lie in two rows, and the last piece of the
+    matrix may hold a single block; with many warp steps, both per-tensor scale modes."""
+    x = random_matrix(rows, cols, seed=rows + cols, dist="student_t4", src_f32=f32)
+    _compare("nvfp4", x, label="nvfp4 %dx%d" % (rows, cols))
+    _compare("nvfp4", x, global_scale=0.02, label="nvfp4 given %dx%d" % (rows, cols))
+
+
 @pytest.mark.parametrize("fmt", ["mxfp8", "nvfp4", "mxfp4"])
 def test_special_values(fmt):
     # zeros, negative zeros, exact ties, saturating blocks, subnormal bf16, a zero block
