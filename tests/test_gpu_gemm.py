@@ -64,6 +64,20 @@ def test_linear_end_to_end(fmt, M, N, K):
 
 
 @pytest.mark.parametrize("fmt", ["mxfp8", "nvfp4", "mxfp4"])
+def test_linear_massive_activations(fmt):
+    """Quantizer + GEMM on ViT-L block 0's massive activations (maximum 1992 on the class and
+    register tokens, rms 9; the README's section 5.5) against the oracle, every output of a
+    ragged 1029-token, two-image batch."""
+    M, N, K = 1029, 1024, 1024
+    a = random_matrix(M, K, seed=77, dist="massive")
+    b = random_matrix(N, K, seed=78, std=0.02)
+    bias = f32_to_bf16_bits(np.random.default_rng(79).standard_normal(N).astype(np.float32) * 0.01)
+    out = _run_linear(fmt, a, b, bias)
+    qa, qb = oracle.quantize(fmt, a), oracle.quantize(fmt, b)
+    check_gemm_rows(bf16_to_f64(out), qa, qb, bias, np.arange(M), "%s massive" % fmt)
+
+
+@pytest.mark.parametrize("fmt", ["mxfp8", "nvfp4", "mxfp4"])
 def test_gemm_no_bias_and_structured_scales(fmt):
     """Rows, columns and K blocks with very different scales: a wrong scale-factor mapping
     (row of A, row of B, or K block) shows up as large errors."""

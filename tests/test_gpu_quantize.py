@@ -48,6 +48,17 @@ def test_quantize_bf16_matches_oracle(fmt, rows, cols, dist):
 
 
 @pytest.mark.parametrize("fmt", ["mxfp8", "nvfp4", "mxfp4"])
+@pytest.mark.parametrize("rows,cols", [(2053, 1024), (1029, 4096)])
+def test_quantize_massive_activations(fmt, rows, cols):
+    """ViT-L block 0's massive activations (the README's section 5.5: maximum 1992, rms 9) on the
+    class and register tokens of each 1024-token image. The block holding 1992 saturates MXFP8
+    (shared exponent 2^2, 498 -> 448) and MXFP4 (2^8, 7.8 -> 6), and under NVFP4 it takes the
+    largest E4M3 block scale, 448, since g = 1992 / 2688. Ragged rows; bit-exact."""
+    x = random_matrix(rows, cols, seed=rows + cols, dist="massive")
+    _compare(fmt, x, label="%s massive %dx%d" % (fmt, rows, cols))
+
+
+@pytest.mark.parametrize("fmt", ["mxfp8", "nvfp4", "mxfp4"])
 @pytest.mark.parametrize("rows,cols", [(3, 32), (128, 256), (131, 1024)])
 def test_quantize_fp32_matches_oracle(fmt, rows, cols):
     x = random_matrix(rows, cols, seed=5, dist="uniform_exp", src_f32=True)

@@ -2,7 +2,7 @@
 import numpy as np
 import torch
 
-from workloads import WORKLOADS, bf16_bits_to_f32, f32_to_bf16_bits, make_activations, make_weights
+from workloads import WORKLOADS, bf16_bits_to_f32, f32_to_bf16_bits, make_activations, make_weights, random_matrix
 
 
 def test_bf16_rounding_matches_torch():
@@ -27,3 +27,14 @@ def test_row_slices_match_full_draw_and_are_deterministic():
     # 4 outlier channels (0.5 % of 768) scaled x20
     col_rms = np.sqrt((x.astype(np.float64) ** 2).mean(axis=0))
     assert (col_rms > 5).sum() == 4
+
+
+def test_massive_activation_recipe():
+    """The massive-activation stress input: maximum exactly 1992 on a special token, rms about 9,
+    the large values confined to the first 5 tokens of each 1024-token image."""
+    x = bf16_bits_to_f32(random_matrix(2053, 512, seed=11, dist="massive")).astype(np.float64)
+    assert np.abs(x).max() == 1992.0
+    assert 8.5 < np.sqrt(np.mean(x * x)) < 12.0
+    special = (np.arange(2053) % 1024) < 5
+    assert np.abs(x[~special]).max() < 100.0
+    assert (np.abs(x[special]) >= 500.0).sum() == 2 * special.sum()

@@ -249,6 +249,17 @@ def random_matrix(rows: int, cols: int, seed: int, std: float = 1.0, dist: str =
     elif dist == "uniform_exp":
         # magnitudes spread over many binades, random signs
         x = np.exp2(rng.uniform(-30, 30, size=(rows, cols))) * rng.choice([-1.0, 1.0], size=(rows, cols))
+    elif dist == "massive":
+        # ViT-L block 0's input as the "lightly-train - DINOv3 + EoMT on RTX 5090" README describes it
+        # (section 5.5): rms about 9, with massive activations on the class and register tokens
+        # reaching 1992. Rows are tokens, 1024 per image; the first 5 of each image carry values of
+        # magnitude 500..1992 in 2 channels, one of them exactly 1992.
+        x = rng.standard_normal((rows, cols)) * 9.0
+        tok = np.flatnonzero(np.arange(rows) % 1024 < 5)
+        ch = rng.choice(cols, size=min(2, cols), replace=False)
+        x[np.ix_(tok, ch)] = rng.uniform(500.0, 1992.0, size=(tok.size, ch.size)) * \
+            rng.choice([-1.0, 1.0], size=(tok.size, ch.size))
+        x[0, ch[0]] = 1992.0
     else:
         x = rng.standard_normal((rows, cols)) * std
     return _store(x, src_f32)
