@@ -99,6 +99,9 @@ struct Epi {
 // (4 scale columns of 128 rows each), kEpiCols output columns per epilogue store chunk and
 // kEpiBufs staging buffers per epilogue warp (stores in flight per warp). A
 // stage's scale slot in TMEM takes 4 columns per A atom and 8 per B atom (two 128-row halves).
+// One staging buffer: the output's stores and the operand loads share the SMs' path to L2, and
+// with two buffers the faster store stream starves the operand feed (measured on GB300, FP4 at
+// M = 51200, K = 1024, N = 4096: 96 -> 112 us).
 template <int FMT>
 struct Cfg;
 template <>
