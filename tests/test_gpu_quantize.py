@@ -6,7 +6,7 @@ import torch
 
 import oracle
 from tests.gpu_util import to_dev
-from workloads import WORKLOADS, f32_to_bf16_bits, make_activations, make_weights, random_matrix
+from workloads import WORKLOADS, bf16_bits_to_f32, f32_to_bf16_bits, make_activations, make_weights, random_matrix
 
 pytestmark = pytest.mark.gpu
 
@@ -56,6 +56,38 @@ def test_quantize_massive_activations(fmt, rows, cols):
     largest E4M3 block scale, 448, since g = 1992 / 2688. Ragged rows; bit-exact."""
     x = random_matrix(rows, cols, seed=rows + cols, dist="massive")
     _compare(fmt, x, label="%s massive %dx%d" % (fmt, rows, cols))
+
+
+@pytest.mark.parametrize("fmt", ["mxfp8", "nvfp4", "mxfp4"])
+def test_quantize_past_2_31_elements(fmt):
+    """524544 x 4096 bf16, 2^31 + 2^20 elements (4.3 GB): element, code and scale offsets past 2^31.
+    The rows repeat a seeded 4095-row base, so a row written at a wrapped offset would land on a
+    row of other content. Sampled rows on both sides of element 2^31 against the oracle; NVFP4's
+    per-tensor scale against the base's exact maximum."""
+    bsq = _bsq()
+    rows, cols, nb = 524544, 4096, 4095
+    base = random_matrix(nb, cols, seed=31, dist="student_t4")
+    x = to_dev(base).repeat((rows + nb - 1) // nb, 1)[:rows]
+    q = bsq.quantize(fmt, x)
+    assert bsq.device_status() == 0
+    del x
+    torch.cuda.empty_cache()
+    edge = (1 << 31) // cols  # the row holding element 2^31
+    idx = np.array(sorted({0, 1, 127, 128, edge - 1, edge, edge + 1, rows - 1} |
+                          set(np.random.default_rng(3).integers(0, rows, 24).tolist())), dtype=np.int64)
+    g = None
+    if fmt == "nvfp4":
+        g = float(np.float32(np.abs(bf16_bits_to_f32(base)).max()) / np.float32(2688.0))
+        assert q.global_scale.item() == g
+    ref = oracle.quantize(fmt, base[idx % nb], global_scale=g)
+    rb = cols if fmt == "mxfp8" else cols // 2
+    flat = q.codes.view(-1)
+    got = torch.stack([flat[int(r) * rb:(int(r) + 1) * rb] for r in idx]).cpu().numpy()
+    assert np.array_equal(got, ref.codes.reshape(len(idx), rb))
+    nsc = cols // (16 if fmt == "nvfp4" else 32)
+    off = np.array([[oracle.scale_tiled_offset(int(r), c, nsc) for c in range(nsc)] for r in idx], dtype=np.int64)
+    sc = q.scales.view(-1)[torch.from_numpy(off.ravel()).cuda()].cpu().numpy().reshape(len(idx), nsc)
+    assert np.array_equal(sc, ref.scales.reshape(len(idx), nsc))
 
 
 @pytest.mark.parametrize("fmt", ["mxfp8", "nvfp4", "mxfp4"])
