@@ -64,6 +64,32 @@ def test_linear_end_to_end(fmt, M, N, K):
 
 
 @pytest.mark.parametrize("fmt", ["mxfp8", "nvfp4", "mxfp4"])
+def test_gemm_output_past_2_31_elements(fmt):
+    """M = 524544, N = 4096, K = 256: a bf16 output of 2^31 + 2^20 elements (4.3 GB), stored by the
+    epilogue's tensor map past element 2^31. A's rows repeat a seeded 4095-row base, so an output
+    row stored at a wrapped offset would hold another row's values; sampled rows on both sides of
+    element 2^31 against the oracle."""
+    bsq = _bsq()
+    M, N, K, nb = 524544, 4096, 256, 4095
+    base = random_matrix(nb, K, seed=41, dist="student_t4")
+    b = random_matrix(N, K, seed=42, std=0.02)
+    bias = f32_to_bf16_bits(np.random.default_rng(43).standard_normal(N).astype(np.float32) * 0.01)
+    qa = bsq.quantize(fmt, to_dev(base).repeat((M + nb - 1) // nb, 1)[:M])
+    qb = bsq.quantize(fmt, to_dev(b))
+    out = bsq.gemm(qa, qb, to_dev(bias))
+    assert bsq.device_status() == 0
+    edge = (1 << 31) // N  # the output row holding element 2^31
+    idx = np.array(sorted({0, 1, 127, 128, edge - 1, edge, edge + 1, M - 1} |
+                          set(np.random.default_rng(4).integers(0, M, 24).tolist())), dtype=np.int64)
+    got = bf16_to_f64(out[torch.from_numpy(idx).cuda()])
+    del out
+    torch.cuda.empty_cache()
+    ra = oracle.quantize(fmt, base[idx % nb], global_scale=qa.global_scale.item() if fmt == "nvfp4" else None)
+    rb = oracle.quantize(fmt, b, global_scale=qb.global_scale.item() if fmt == "nvfp4" else None)
+    check_gemm_rows(got, ra, rb, bias, np.arange(len(idx)), "%s M = %d" % (fmt, M))
+
+
+@pytest.mark.parametrize("fmt", ["mxfp8", "nvfp4", "mxfp4"])
 def test_linear_massive_activations(fmt):
     """Quantizer + GEMM on ViT-L block 0's massive activations (maximum 1992 on the class and
     register tokens, rms 9; the README's section 5.5) against the oracle, every output of a
