@@ -973,15 +973,15 @@ __global__ void __launch_bounds__(kAmaxThreads) amax_kernel(const __grid_constan
   }
 }
 
-// Programmatic dependent launch for every kernel here: the kernel may be launched while the
-// previous kernel in the stream finishes; it waits for it (grid_dependency_wait) before touching
-// memory.
+// Launch with programmatic dependent launch where `pdl` is set: the kernel may then be launched
+// while the previous kernel in the stream finishes; every kernel here waits for it
+// (grid_dependency_wait) before touching memory, so the flag changes timing, not results.
 template <typename... Args>
-cudaError_t launch_pdl(void (*kernel)(Args...), int grid, int threads, int smem, cudaStream_t stream,
+cudaError_t launch_pdl(void (*kernel)(Args...), int grid, int threads, int smem, cudaStream_t stream, bool pdl,
                        const Args&... args) {
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  at[0].val.programmaticStreamSerializationAllowed = 1;
+  at[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(threads);
@@ -992,12 +992,18 @@ cudaError_t launch_pdl(void (*kernel)(Args...), int grid, int threads, int smem,
   return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
+// The streaming kernel takes programmatic dependent launch only right after the batch's own amax
+// pass. After other kernels (a GEMM in a layer sequence) its early-launched CTAs measured slower on
+// GB300: graph-replayed with the L2 flushed, the ViT-L MLP step at M = 51200 (MXFP4 + NVFP4) took
+// 695.9 us with it on for every quantizer launch and 685.7 us with it off, the ViT-L MXFP8 layers
+// at M = 7168 131.1 against 127.0 us; the NVFP4 ones at M = 7168 kept it after their amax pass
+// (157.2 us with it off there too, against 154.5 us).
 template <int FMT, bool F32, int NV>
 cudaError_t launch_stream(const QuantBatch& b, int num_sms, cudaStream_t stream) {
   const int64_t ctas = ceil_div(b.chunk_start[b.n], kSWarps);
   const int grid =
       static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(ctas, SCfg<F32, NV != kMx>::kCtasPerSm * num_sms)));
-  return launch_pdl(stream_kernel<FMT, F32, NV>, grid, kSThreads, 0, stream, b);
+  return launch_pdl(stream_kernel<FMT, F32, NV>, grid, kSThreads, 0, stream, NV == kNvComputed, b);
 }
 
 template <int FMT, bool F32>
@@ -1007,14 +1013,14 @@ cudaError_t launch_ln(const QuantBatch& b, int grid, cudaStream_t stream, int de
     return cudaFuncSetAttribute(layernorm_kernel<FMT, F32>, cudaFuncAttributeMaxDynamicSharedMemorySize, QCfg::kSmem);
   });
   if (attr != cudaSuccess) return attr;
-  return launch_pdl(layernorm_kernel<FMT, F32>, grid, QCfg::kThreads, QCfg::kSmem, stream, b);
+  return launch_pdl(layernorm_kernel<FMT, F32>, grid, QCfg::kThreads, QCfg::kSmem, stream, true, b);
 }
 
 template <int FMT>
 cudaError_t launch_ln_stream(const QuantBatch& b, int num_sms, cudaStream_t stream) {
   const int64_t ctas = ceil_div(b.t[0].rows, kSWarps);
   const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(ctas, 4 * static_cast<int64_t>(num_sms))));
-  return launch_pdl(ln_stream_kernel<FMT>, grid, kSThreads, 0, stream, b);
+  return launch_pdl(ln_stream_kernel<FMT>, grid, kSThreads, 0, stream, true, b);
 }
 
 }  // namespace
@@ -1059,8 +1065,8 @@ int launch_amax(const void* const* srcs, const int64_t* elems, uint32_t* const* 
     most = std::max(most, l.nvec[i]);
   }
   const int agrid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(ceil_div(most, kAmaxThreads * 4), dev.num_sms * 8)));
-  const cudaError_t e = src_f32 ? launch_pdl(amax_kernel<true>, agrid, kAmaxThreads, 0, stream, l)
-                                : launch_pdl(amax_kernel<false>, agrid, kAmaxThreads, 0, stream, l);
+  const cudaError_t e = src_f32 ? launch_pdl(amax_kernel<true>, agrid, kAmaxThreads, 0, stream, true, l)
+                                : launch_pdl(amax_kernel<false>, agrid, kAmaxThreads, 0, stream, true, l);
   return e == cudaSuccess ? BSQ_OK : BSQ_ERR_LAUNCH;
 }
 
